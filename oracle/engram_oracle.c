@@ -1,0 +1,344 @@
+/*
+ * Engram conditional memory -- CPU ORACLE for the hash-gather and context-aware-gate hot path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the package's smoke check and the
+ * benchmark's CPU-baseline leg load this library.  The product path (the CUDA
+ * library under engram_conditional_memory_gb300/) never calls it, links it or
+ * shares any code, header, table or constant with it.
+ *
+ * Everything here is a plain scalar loop written straight from the definitions,
+ * one token at a time, with fp64 accumulation.  Nothing is blocked, fused,
+ * vectorised or reordered beyond what the definition states.  Sources:
+ *
+ *   [T34]  TileLang tutorial, ch. 34 "TileKernels: Engram and mHC"
+ *            sec. 1.2  the four parts of Engram (compression P: V->V', multi-head
+ *                      multiply-XOR hashing into prime-sized tables, the
+ *                      context-aware gate alpha = sigmoid(RMSNorm(h)^T RMSNorm(k)/sqrt(d)),
+ *                      output alpha * v)
+ *            sec. 2.1  tensors and the data flow fused_weight -> gate_fwd -> gate_bwd
+ *                      -> grad_w_reduce; the saved dot / alpha / rstd_x / rstd_k
+ *            sec. 2.3  addressing: (max_n - 1) * heads rows per token, exclusive
+ *                      prefix-sum offsets into one concatenated table
+ *            sec. 3.1  the weighted-RMSNorm identity that allows w_h (*) w_k folding
+ *            sec. 4.2  backward chain rule of the gate
+ *            sec. 4.3  the weight-gradient reduction: sum the partials, then
+ *                      grad_w_h += S * w_k and grad_w_k += S * w_h
+ *   [T13]  TileLang tutorial, ch. 13 "elementwise / norm / RoPE", sec. 5.4:
+ *          the RMS mean divides by the true length d.
+ *
+ * Readings where the pages leave a step open (each one is also listed in the
+ * design notes):
+ *   - the exact hash: h = XOR_{j<n} (uint64) id'[t-j] * M[n,k,j] (mod 2^64),
+ *     idx = h mod p[n,k] with unsigned 64-bit modulo; j = 0 is the current token,
+ *     positions before the sequence start contribute the pad id 0;
+ *   - the gate uses the plain sigmoid of the paper's Eq. 4 (no signed square root)
+ *     and outputs alpha * v (no residual);
+ *   - eps sits inside the root: rstd = 1 / sqrt(mean(x^2) + eps).
+ *
+ * Pins (every function is checked against something other than itself, in the
+ * CPU test suite): closed-form hash cases with special multipliers and tiny
+ * primes, sequence resets, brute-force invariants; gathered rows against a table
+ * whose rows encode their own index; the gate against torch's rms_norm +
+ * sigmoid in fp64, the k = 0 and h = +-k closed forms and the fused/unfused
+ * identity; the backward against torch autograd and central finite differences;
+ * the reduction against constant partials with closed-form sums.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#define EO_F32 0
+#define EO_BF16 1
+
+#define EO_OK 0
+#define EO_ERR_ARG 1
+#define EO_ERR_INDEX 2
+
+/* Element i of a row-major tensor stored as fp32 or as raw bfloat16 bits, exactly widened to double. */
+static double eo_load(const void *base, int dtype, int64_t i)
+{
+    if (dtype == EO_F32)
+        return (double)((const float *)base)[i];
+    uint32_t u = (uint32_t)((const uint16_t *)base)[i] << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+static double eo_sigmoid(double z)
+{
+    if (z >= 0.0)
+        return 1.0 / (1.0 + exp(-z));
+    double e = exp(z);
+    return e / (1.0 + e);
+}
+
+/* ------------------------------------------------------------------------- */
+/* A0-A1: compression and the multi-head N-gram hash  [T34 sec. 1.2, 2.3]      */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * For each token t in [t_begin, t_end) and each table (n, k), n = min_order ..
+ * min_order + num_orders - 1, k = 0 .. heads - 1, in that order (table index
+ * (n - min_order) * heads + k):
+ *     id'(q) = compress_map[token_ids[q]]  (identity if compress_map is NULL),
+ *              or the pad id 0 when q lies before the start of t's sequence;
+ *     h = 0;  for j = 0 .. n-1:  h ^= id'(t - j) * M[table][j]   (mod 2^64)
+ *     idx = h mod primes[table]
+ * out_idx is [(t_end - t_begin), tables].  multipliers is [tables][mult_stride].
+ * seq_offsets holds num_seqs + 1 boundaries (0 = first, T = last).
+ */
+int eo_hash_indices(const int32_t *token_ids, int64_t T,
+                    const int64_t *seq_offsets, int32_t num_seqs,
+                    const int32_t *compress_map, int32_t vocab,
+                    int32_t min_order, int32_t num_orders, int32_t heads,
+                    const uint64_t *multipliers, int32_t mult_stride,
+                    const uint64_t *primes,
+                    int64_t t_begin, int64_t t_end, int64_t *out_idx)
+{
+    const int32_t tables = num_orders * heads;
+    if (!token_ids || !seq_offsets || !multipliers || !primes || !out_idx)
+        return EO_ERR_ARG;
+    if (num_seqs < 1 || min_order < 1 || num_orders < 1 || heads < 1)
+        return EO_ERR_ARG;
+    if (mult_stride < min_order + num_orders - 1 || t_begin < 0 || t_end > T || t_begin > t_end)
+        return EO_ERR_ARG;
+    if (seq_offsets[0] != 0 || seq_offsets[num_seqs] != T)
+        return EO_ERR_ARG;
+    for (int32_t tb = 0; tb < tables; ++tb)
+        if (primes[tb] == 0)
+            return EO_ERR_ARG;
+
+    for (int64_t t = t_begin; t < t_end; ++t) {
+        /* The sequence holding t: the one with seq_offsets[s] <= t < seq_offsets[s+1]. */
+        int64_t start = -1;
+        for (int32_t s = 0; s < num_seqs; ++s)
+            if (seq_offsets[s] <= t && t < seq_offsets[s + 1])
+                start = seq_offsets[s];
+        if (start < 0)
+            return EO_ERR_ARG;
+
+        for (int32_t ni = 0; ni < num_orders; ++ni) {
+            const int32_t n = min_order + ni;
+            for (int32_t k = 0; k < heads; ++k) {
+                const int32_t tb = ni * heads + k;
+                uint64_t h = 0;
+                for (int32_t j = 0; j < n; ++j) {
+                    const int64_t q = t - j;
+                    uint64_t id = 0; /* pad id before the sequence start */
+                    if (q >= start) {
+                        const int32_t raw = token_ids[q];
+                        if (raw < 0 || raw >= vocab)
+                            return EO_ERR_INDEX;
+                        id = (uint64_t)(compress_map ? compress_map[raw] : raw);
+                    }
+                    h ^= id * multipliers[(int64_t)tb * mult_stride + j];
+                }
+                out_idx[(t - t_begin) * tables + tb] = (int64_t)(h % primes[tb]);
+            }
+        }
+    }
+    return EO_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* A2: the gather from the concatenated table  [T34 sec. 2.3]                 */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * All tables E_{n,k} live in one [sum(primes), row] table; table tb starts at
+ * the exclusive prefix sum of primes[0..tb-1].  For each token t < ntok and
+ * table tb the output row (t, tb) is a byte copy of table row
+ * offset[tb] + idx[t][tb].  out is [ntok, tables, row_bytes] bytes, i.e. the
+ * concatenation e_t in table order.
+ */
+int eo_gather_rows(const void *table, int64_t table_rows, int32_t row_bytes,
+                   const uint64_t *primes, int32_t tables,
+                   const int64_t *idx, int64_t ntok, void *out)
+{
+    if (!table || !primes || !idx || !out || row_bytes <= 0 || tables <= 0)
+        return EO_ERR_ARG;
+    for (int64_t t = 0; t < ntok; ++t) {
+        uint64_t offset = 0;
+        for (int32_t tb = 0; tb < tables; ++tb) {
+            const int64_t i = idx[t * tables + tb];
+            if (i < 0 || (uint64_t)i >= primes[tb])
+                return EO_ERR_INDEX;
+            const uint64_t row = offset + (uint64_t)i;
+            if (row >= (uint64_t)table_rows)
+                return EO_ERR_INDEX;
+            memcpy((char *)out + (t * tables + tb) * (int64_t)row_bytes,
+                   (const char *)table + (int64_t)row * row_bytes, (size_t)row_bytes);
+            offset += primes[tb];
+        }
+    }
+    return EO_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* B0: the weight fold  [T34 sec. 3.1]                                         */
+/* ------------------------------------------------------------------------- */
+
+/* w[i] = w_h[i] * w_k[i] in fp64 (the GPU path rounds it to fp32). */
+int eo_fuse_weight(const float *w_h, const float *w_k, int32_t d, double *w)
+{
+    if (!w_h || !w_k || !w || d <= 0)
+        return EO_ERR_ARG;
+    for (int32_t i = 0; i < d; ++i)
+        w[i] = (double)w_h[i] * (double)w_k[i];
+    return EO_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* B1: the context-aware gate, forward  [T34 sec. 1.2 item 3, 2.1, 3.1]        */
+/* ------------------------------------------------------------------------- */
+
+/* Statistics of one token: rstd of h and of k, the fused-weight dot product, and z. */
+struct eo_token_stats {
+    double rh, rk, dot, z_unfused, z_fused, alpha;
+};
+
+static void eo_token_forward(const void *h, const void *k, int dtype, const float *w_h, const float *w_k,
+                             int64_t t, int32_t d, double eps, struct eo_token_stats *st)
+{
+    const int64_t base = t * (int64_t)d;
+    double sh = 0.0, sk = 0.0;
+    for (int32_t i = 0; i < d; ++i) {
+        const double x = eo_load(h, dtype, base + i);
+        const double y = eo_load(k, dtype, base + i);
+        sh += x * x;
+        sk += y * y;
+    }
+    /* RMSNorm scale: 1 / sqrt(mean(x^2) + eps), mean over the true length d. */
+    st->rh = 1.0 / sqrt(sh / (double)d + eps);
+    st->rk = 1.0 / sqrt(sk / (double)d + eps);
+
+    /* Paper form: normalise both vectors with their own RMSNorm weights, then take
+     * the inner product scaled by 1/sqrt(d). */
+    double acc = 0.0;
+    for (int32_t i = 0; i < d; ++i) {
+        const double nh = eo_load(h, dtype, base + i) * st->rh * (double)w_h[i];
+        const double nk = eo_load(k, dtype, base + i) * st->rk * (double)w_k[i];
+        acc += nh * nk;
+    }
+    st->z_unfused = acc / sqrt((double)d);
+
+    /* The saved statistic: dot = sum_i h_i * (w_h,i * w_k,i) * k_i, and the z it gives. */
+    double dot = 0.0;
+    for (int32_t i = 0; i < d; ++i)
+        dot += eo_load(h, dtype, base + i) * ((double)w_h[i] * (double)w_k[i]) * eo_load(k, dtype, base + i);
+    st->dot = dot;
+    st->z_fused = st->rh * st->rk * dot / sqrt((double)d);
+
+    st->alpha = eo_sigmoid(st->z_unfused);
+}
+
+/*
+ * For t in [t_begin, t_end):  alpha_t = sigmoid(RMSNorm(h_t; w_h) . RMSNorm(k_t; w_k) / sqrt(d)),
+ * out_t = alpha_t * v_t, plus the saved statistics rstd_h, rstd_k and dot.
+ * Row-major inputs [T, d]; outputs are indexed from t_begin.  z_fused (nullable)
+ * receives rstd_h * rstd_k * dot / sqrt(d), which must equal the paper-form z.
+ */
+int eo_gate_fwd(const void *h, const void *k, const void *v, int dtype,
+                const float *w_h, const float *w_k, int64_t T, int32_t d, double eps,
+                int64_t t_begin, int64_t t_end,
+                double *out, double *alpha, double *rstd_h, double *rstd_k, double *dot, double *z_fused)
+{
+    if (!h || !k || !v || !w_h || !w_k || !out || !alpha || !rstd_h || !rstd_k || !dot)
+        return EO_ERR_ARG;
+    if ((dtype != EO_F32 && dtype != EO_BF16) || d <= 0 || t_begin < 0 || t_end > T || t_begin > t_end)
+        return EO_ERR_ARG;
+    for (int64_t t = t_begin; t < t_end; ++t) {
+        struct eo_token_stats st;
+        eo_token_forward(h, k, dtype, w_h, w_k, t, d, eps, &st);
+        const int64_t o = t - t_begin;
+        alpha[o] = st.alpha;
+        rstd_h[o] = st.rh;
+        rstd_k[o] = st.rk;
+        dot[o] = st.dot;
+        if (z_fused)
+            z_fused[o] = st.z_fused;
+        for (int32_t i = 0; i < d; ++i)
+            out[o * d + i] = st.alpha * eo_load(v, dtype, t * (int64_t)d + i);
+    }
+    return EO_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* B2: the gate backward  [T34 sec. 4.1, 4.2]                                  */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * Given the upstream gradient g = dL/dout for t in [t_begin, t_end), with
+ * w_i = w_h,i * w_k,i and s = 1/sqrt(d):
+ *     dv_t    = alpha_t * g_t
+ *     dalpha  = sum_i g_i v_i
+ *     c_t     = dalpha * alpha (1 - alpha) * s * rh * rk            (= dL/d dot)
+ *     dh_t,i  = c_t * (w_i k_i - dot * rh^2 * h_i / d)
+ *     dk_t,i  = c_t * (w_i h_i - dot * rk^2 * k_i / d)
+ *     dweight_i = sum_t c_t h_t,i k_t,i                             (= dL/dw_i)
+ * The forward statistics are recomputed here in fp64 from h and k.
+ * dweight [d] is overwritten with the sum over [t_begin, t_end) in token order.
+ */
+int eo_gate_bwd(const void *g, const void *h, const void *k, const void *v, int dtype,
+                const float *w_h, const float *w_k, int64_t T, int32_t d, double eps,
+                int64_t t_begin, int64_t t_end,
+                double *dh, double *dk, double *dv, double *dweight)
+{
+    if (!g || !h || !k || !v || !w_h || !w_k || !dh || !dk || !dv || !dweight)
+        return EO_ERR_ARG;
+    if ((dtype != EO_F32 && dtype != EO_BF16) || d <= 0 || t_begin < 0 || t_end > T || t_begin > t_end)
+        return EO_ERR_ARG;
+    const double s = 1.0 / sqrt((double)d);
+    for (int32_t i = 0; i < d; ++i)
+        dweight[i] = 0.0;
+    for (int64_t t = t_begin; t < t_end; ++t) {
+        struct eo_token_stats st;
+        eo_token_forward(h, k, dtype, w_h, w_k, t, d, eps, &st);
+        const int64_t base = t * (int64_t)d;
+        const int64_t o = (t - t_begin) * (int64_t)d;
+
+        double dalpha = 0.0;
+        for (int32_t i = 0; i < d; ++i)
+            dalpha += eo_load(g, dtype, base + i) * eo_load(v, dtype, base + i);
+        const double c = dalpha * st.alpha * (1.0 - st.alpha) * s * st.rh * st.rk;
+
+        for (int32_t i = 0; i < d; ++i) {
+            const double hi = eo_load(h, dtype, base + i);
+            const double ki = eo_load(k, dtype, base + i);
+            const double wi = (double)w_h[i] * (double)w_k[i];
+            dv[o + i] = st.alpha * eo_load(g, dtype, base + i);
+            dh[o + i] = c * (wi * ki - st.dot * st.rh * st.rh * hi / (double)d);
+            dk[o + i] = c * (wi * hi - st.dot * st.rk * st.rk * ki / (double)d);
+            dweight[i] += c * hi * ki;
+        }
+    }
+    return EO_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* B3: the weight-gradient reduction  [T34 sec. 4.3, 4.4]                      */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * S_i = sum_{p<P} partial[p][i] (fp64, p ascending).  When w_h and w_k are given,
+ * inc_h = S (*) w_k and inc_k = S (*) w_h are the increments that the reduction
+ * adds to the accumulated fp32 parameter gradients of w_h and w_k.
+ */
+int eo_grad_w_reduce(const float *partial, int32_t P, int32_t d,
+                     const float *w_h, const float *w_k, double *S, double *inc_h, double *inc_k)
+{
+    if (!partial || !S || P < 0 || d <= 0)
+        return EO_ERR_ARG;
+    for (int32_t i = 0; i < d; ++i) {
+        double acc = 0.0;
+        for (int32_t p = 0; p < P; ++p)
+            acc += (double)partial[(int64_t)p * d + i];
+        S[i] = acc;
+        if (w_h && w_k && inc_h && inc_k) {
+            inc_h[i] = acc * (double)w_k[i];
+            inc_k[i] = acc * (double)w_h[i];
+        }
+    }
+    return EO_OK;
+}
