@@ -1,0 +1,289 @@
+"""Thin Python binding of the Engram C ABI (include/engram.h).
+
+Argument marshalling only: torch tensors provide device memory and the current
+stream; every step of the hot path runs in the CUDA library.  There is no CPU or
+PyTorch fallback: if the library is missing, loading fails with an error.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import numpy as np
+import torch
+
+from . import build as _build
+
+_c = ctypes
+_p, _i32, _i64 = _c.c_void_p, _c.c_int32, _c.c_int64
+
+F32, BF16 = 0, 1
+_DTYPES = {torch.float32: F32, torch.bfloat16: BF16}
+
+DEVERR_TOKEN_ID = 0x1
+DEVERR_COMPRESSED = 0x2
+DEVERR_SEQ_OFFSETS = 0x4
+DEVERR_TIMEOUT = 0x8
+
+
+class EngramError(RuntimeError):
+    def __init__(self, status: int, where: str, text: str):
+        super().__init__(f"{where}: status {status} ({text})")
+        self.status = status
+
+
+class _HashSpec(_c.Structure):
+    _fields_ = [("min_order", _i32), ("num_orders", _i32), ("heads", _i32), ("mult_stride", _i32),
+                ("multipliers", _p), ("primes", _p)]
+
+
+class _HashGatherArgs(_c.Structure):
+    _fields_ = [("token_ids", _p), ("T", _i64), ("seq_offsets", _p), ("num_seqs", _i32),
+                ("compress_map", _p), ("vocab", _i32), ("vocab_c", _i32),
+                ("table", _p), ("table_rows", _i64), ("row_dim", _i32), ("dtype", _c.c_int),
+                ("out_indices", _p), ("out_rows", _p), ("err_word", _p)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library():
+    """Load libengram_gb300.so (built in-tree by `build.build()`); raise if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB
+        if not os.path.exists(path):
+            raise RuntimeError(f"Engram CUDA library not built ({path}); run __graft_entry__.build() first")
+        lib = _c.CDLL(path)
+        st = _c.c_int
+        sig = {
+            "engram_abi_version": (_i32, []),
+            "engram_status_string": (_c.c_char_p, [st]),
+            "engram_last_error_string": (_c.c_char_p, []),
+            "engram_set_validation": (_i32, [_i32]),
+            "engram_set_max_ctas": (_i32, [_i32]),
+            "engram_read_error_word": (st, [_p, _p, _p]),
+            "engram_device_status": (st, [_p, _i32]),
+            "engram_hash_gather": (st, [_p, _p, _p]),
+            "engram_fuse_weight": (st, [_p, _p, _c.c_int, _p, _i32, _p]),
+            "engram_gate_fwd": (st, [_p, _p, _p, _c.c_int, _p, _i64, _i32, _c.c_float, _p, _p, _p, _p, _p, _p]),
+            "engram_gate_bwd_num_partials": (st, [_i64, _i32, _p]),
+            "engram_gate_bwd": (st, [_p, _p, _p, _p, _c.c_int, _p, _p, _p, _p, _p, _i64, _i32, _p, _p, _p, _p,
+                                     _i32, _p]),
+            "engram_grad_w_reduce": (st, [_p, _i32, _i32, _p, _p, _p, _p, _p, _p]),
+        }
+        for name, (res, args) in sig.items():
+            f = getattr(lib, name)
+            f.restype, f.argtypes = res, args
+        _lib = lib
+        return lib
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        lib = load_library()
+        raise EngramError(status, where, lib.engram_last_error_string().decode())
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _need(t, name, dtype=None, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t
+
+
+def set_validation(level: int) -> int:
+    return load_library().engram_set_validation(level)
+
+
+def set_max_ctas(max_ctas: int) -> int:
+    """Cap the CTAs per launch (0 = none); returns the previous cap."""
+    return load_library().engram_set_max_ctas(max_ctas)
+
+
+def abi_version() -> int:
+    return load_library().engram_abi_version()
+
+
+# ----------------------------------------------------------------------------- B0 / B1
+
+
+def fuse_weight(w_h, w_k, out=None, stream=None):
+    """w_fused = w_h * w_k in fp32 (w_h, w_k fp32 or bf16)."""
+    lib = load_library()
+    _need(w_h, "w_h")
+    _need(w_k, "w_k", w_h.dtype)
+    d = w_h.numel()
+    out = torch.empty(d, dtype=torch.float32, device=w_h.device) if out is None else _need(out, "out", torch.float32)
+    _check(lib.engram_fuse_weight(_ptr(w_h), _ptr(w_k), _DTYPES[w_h.dtype], _ptr(out), d, _stream(stream)),
+           "engram_fuse_weight")
+    return out
+
+
+def gate_fwd(h, k, v, w_fused, eps: float = 1e-6, out=None, save_for_backward: bool = True, stats=None,
+             stream=None):
+    """out = alpha * v with alpha = sigmoid(RMSNorm(h)·RMSNorm(k)/sqrt(d)); returns (out, alpha, rstd_h, rstd_k, dot).
+
+    The statistics are None unless save_for_backward.  `stats` may supply the four [T] fp32 buffers.
+    """
+    lib = load_library()
+    _need(h, "h")
+    _need(k, "k", h.dtype)
+    _need(v, "v", h.dtype)
+    _need(w_fused, "w_fused", torch.float32)
+    T, d = h.shape
+    out = torch.empty_like(v) if out is None else _need(out, "out", h.dtype)
+    if save_for_backward:
+        if stats is None:
+            stats = tuple(torch.empty(T, dtype=torch.float32, device=h.device) for _ in range(4))
+        alpha, rh, rk, dot = (_need(x, "stat", torch.float32) for x in stats)
+    else:
+        alpha = rh = rk = dot = None
+    _check(lib.engram_gate_fwd(_ptr(h), _ptr(k), _ptr(v), _DTYPES[h.dtype], _ptr(w_fused), T, d, float(eps),
+                               _ptr(out), _ptr(alpha), _ptr(rh), _ptr(rk), _ptr(dot), _stream(stream)),
+           "engram_gate_fwd")
+    return out, alpha, rh, rk, dot
+
+
+# ----------------------------------------------------------------------------- B2 / B3
+
+
+def gate_bwd_num_partials(T: int, d: int) -> int:
+    lib = load_library()
+    P = _c.c_int32(0)
+    _check(lib.engram_gate_bwd_num_partials(T, d, _c.byref(P)), "engram_gate_bwd_num_partials")
+    return P.value
+
+
+def gate_bwd(dout, h, k, v, w_fused, alpha, rstd_h, rstd_k, dot, P: int | None = None, dh=None, dk=None, dv=None,
+             dw_partial=None, stream=None):
+    """Returns (dh, dk, dv, dw_partial [P, d] fp32)."""
+    lib = load_library()
+    for name, t in (("dout", dout), ("h", h), ("k", k), ("v", v)):
+        _need(t, name, h.dtype)
+    for name, t in (("w_fused", w_fused), ("alpha", alpha), ("rstd_h", rstd_h), ("rstd_k", rstd_k), ("dot", dot)):
+        _need(t, name, torch.float32)
+    T, d = h.shape
+    if P is None:
+        P = gate_bwd_num_partials(T, d) if dw_partial is None else dw_partial.shape[0]
+    dh = torch.empty_like(h) if dh is None else _need(dh, "dh", h.dtype)
+    dk = torch.empty_like(k) if dk is None else _need(dk, "dk", h.dtype)
+    dv = torch.empty_like(v) if dv is None else _need(dv, "dv", h.dtype)
+    if dw_partial is None:
+        dw_partial = torch.empty((P, d), dtype=torch.float32, device=h.device)
+    else:
+        _need(dw_partial, "dw_partial", torch.float32)
+    _check(lib.engram_gate_bwd(_ptr(dout), _ptr(h), _ptr(k), _ptr(v), _DTYPES[h.dtype], _ptr(w_fused), _ptr(alpha),
+                               _ptr(rstd_h), _ptr(rstd_k), _ptr(dot), T, d, _ptr(dh), _ptr(dk), _ptr(dv),
+                               _ptr(dw_partial), P, _stream(stream)),
+           "engram_gate_bwd")
+    return dh, dk, dv, dw_partial
+
+
+def grad_w_reduce(dw_partial, dweight_fused=None, w_h=None, w_k=None, grad_w_h=None, grad_w_k=None,
+                  want_dweight: bool = True, stream=None):
+    """dweight_fused = sum_p dw_partial[p]; with weights, grad_w_h += S*w_k and grad_w_k += S*w_h."""
+    lib = load_library()
+    _need(dw_partial, "dw_partial", torch.float32)
+    P, d = dw_partial.shape
+    if dweight_fused is None and want_dweight:
+        dweight_fused = torch.empty(d, dtype=torch.float32, device=dw_partial.device)
+    for name, t in (("w_h", w_h), ("w_k", w_k), ("grad_w_h", grad_w_h), ("grad_w_k", grad_w_k)):
+        if t is not None:
+            _need(t, name, torch.float32)
+    _check(lib.engram_grad_w_reduce(_ptr(dw_partial), P, d, _ptr(dweight_fused), _ptr(w_h), _ptr(w_k),
+                                    _ptr(grad_w_h), _ptr(grad_w_k), _stream(stream)),
+           "engram_grad_w_reduce")
+    return dweight_fused
+
+
+# ----------------------------------------------------------------------------- A0-A2
+
+
+class HashSpec:
+    """The hash hyper-parameters, kept as host arrays for the C ABI."""
+
+    def __init__(self, min_order: int, num_orders: int, heads: int, multipliers, primes):
+        self.min_order, self.num_orders, self.heads = int(min_order), int(num_orders), int(heads)
+        self.multipliers = np.ascontiguousarray(multipliers, dtype=np.uint64)
+        self.primes = np.ascontiguousarray(primes, dtype=np.uint64)
+        self.tables = self.num_orders * self.heads
+        if self.multipliers.ndim != 2 or self.multipliers.shape[0] != self.tables or len(self.primes) != self.tables:
+            raise ValueError("multipliers must be [tables, stride] and primes [tables]")
+
+    def _c(self):
+        return _HashSpec(self.min_order, self.num_orders, self.heads, self.multipliers.shape[1],
+                         self.multipliers.ctypes.data, self.primes.ctypes.data)
+
+
+def hash_gather(spec: HashSpec, token_ids, seq_offsets, table, compress_map=None, vocab: int | None = None,
+                vocab_c: int | None = None, want_rows: bool = True, want_indices: bool = False, out_rows=None,
+                out_indices=None, err_word=None, stream=None):
+    """Returns (rows [T, tables*row_dim] or None, indices [T, tables] int32 or None)."""
+    lib = load_library()
+    _need(token_ids, "token_ids", torch.int32)
+    _need(seq_offsets, "seq_offsets", torch.int64)
+    _need(table, "table")
+    if compress_map is not None:
+        _need(compress_map, "compress_map", torch.int32)
+    T = token_ids.numel()
+    rows_total, row_dim = table.shape
+    if vocab is None:
+        vocab = compress_map.numel() if compress_map is not None else (1 << 31) - 1
+    if vocab_c is None:
+        vocab_c = vocab
+    if want_rows and out_rows is None:
+        out_rows = torch.empty((T, spec.tables * row_dim), dtype=table.dtype, device=table.device)
+    if want_indices and out_indices is None:
+        out_indices = torch.empty((T, spec.tables), dtype=torch.int32, device=table.device)
+    args = _HashGatherArgs(_ptr(token_ids), T, _ptr(seq_offsets), seq_offsets.numel() - 1, _ptr(compress_map),
+                           vocab, vocab_c, _ptr(table), rows_total, row_dim, _DTYPES[table.dtype],
+                           _ptr(out_indices), _ptr(out_rows), _ptr(err_word))
+    cspec = spec._c()
+    _check(lib.engram_hash_gather(_c.byref(cspec), _c.byref(args), _stream(stream)), "engram_hash_gather")
+    return out_rows, out_indices
+
+
+# ----------------------------------------------------------------------------- errors
+
+
+def read_error_word(err_word, stream=None) -> int:
+    """Synchronises the stream and returns the device error word's bits."""
+    lib = load_library()
+    out = _c.c_uint32(0)
+    st = lib.engram_read_error_word(_ptr(err_word), _stream(stream), _c.byref(out))
+    if st not in (0, 6):
+        _check(st, "engram_read_error_word")
+    return out.value
+
+
+def device_status(clear: bool = False) -> int:
+    """Synchronises the device and returns the library's device status bits on the current device."""
+    lib = load_library()
+    out = _c.c_uint32(0)
+    st = lib.engram_device_status(_c.byref(out), 1 if clear else 0)
+    if st not in (0, 6):
+        _check(st, "engram_device_status")
+    return out.value

@@ -1,0 +1,191 @@
+// Internal helpers of the Engram GB300 library: host-side validation and error
+// state, and the device-side building blocks (mbarrier, bulk async copies,
+// bounded waits, bf16 packing) shared by the kernels.  sm_103a only.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "engram.h"
+
+namespace engram {
+
+// ---------------------------------------------------------------------------- host side
+
+// Per-device facts the launchers need (cached on first use of each device).
+struct DeviceInfo {
+    int device;
+    int num_sms;
+    int smem_optin;          // max dynamic shared memory per block (opt-in)
+    uint32_t *status_word;   // device address of the library's status word on this device
+};
+
+// Fills `info` for the current device.  ENGRAM_ERR_CUDA on failure.
+engram_status current_device(DeviceInfo *info);
+
+// Records `msg` as the calling thread's last error text and returns `st`.
+engram_status fail(engram_status st, const char *fmt, ...);
+
+// ENGRAM_ERR_DEVICE unless `p` is device (or managed) memory reachable from `device`
+// (skipped at validation level 0).  NULL pointers are the caller's business.
+engram_status check_device_ptr(const void *p, int device, const char *name);
+
+// ENGRAM_ERR_CUDA with the runtime's text if the last launch failed.
+engram_status check_launch(const char *what);
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline int dtype_size(engram_dtype dt) { return dt == ENGRAM_F32 ? 4 : (dt == ENGRAM_BF16 ? 2 : 0); }
+
+// Applies the process-wide CTA cap (engram_set_max_ctas) to a grid size (>= 1 in, >= 1 out).
+int64_t cap_grid(int64_t grid);
+
+// Opts a kernel into `bytes` of dynamic shared memory (idempotent, cheap after the first call).
+engram_status set_smem(const void *kernel, int bytes);
+
+// ---------------------------------------------------------------------------- device side
+
+// Longest time a pipeline wait may take before the kernel gives up (ns).
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+// Makes initialised barriers visible to the async (TMA) proxy and the other threads.
+__device__ __forceinline__ void mbar_init_fence() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Waits for phase `parity` of `bar` to complete; false after kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    }
+    return true;
+}
+
+// An L2 policy that evicts first: for data streamed through exactly once.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// Bulk (TMA) copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from
+// global to this CTA's shared memory; completion is signalled on `bar` as tx bytes.
+__device__ __forceinline__ void bulk_load(void *dst_smem, const void *src_gmem, uint32_t bytes, uint64_t *bar,
+                                          uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+        ::"r"(smem_addr(dst_smem)), "l"(src_gmem), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+// Named barrier over `count` threads (a multiple of 32) of this CTA.
+__device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+// Sets bits in an optional device error word and in the library's status word.
+__device__ __forceinline__ void report(uint32_t *status_word, uint32_t *err_word, uint32_t bits) {
+    if (status_word) atomicOr(status_word, bits);
+    if (err_word) atomicOr(err_word, bits);
+}
+
+// ---- element packing: one 16-byte vector = 8 bf16 or 4 fp32 values
+
+template <typename T>
+struct Vec;
+
+template <>
+struct Vec<float> {
+    static constexpr int N = 4;
+    __device__ __forceinline__ static void unpack(const uint4 &u, float (&x)[N]) {
+        x[0] = __uint_as_float(u.x);
+        x[1] = __uint_as_float(u.y);
+        x[2] = __uint_as_float(u.z);
+        x[3] = __uint_as_float(u.w);
+    }
+    __device__ __forceinline__ static uint4 pack(const float (&x)[N]) {
+        return make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]), __float_as_uint(x[2]),
+                          __float_as_uint(x[3]));
+    }
+};
+
+template <>
+struct Vec<__nv_bfloat16> {
+    static constexpr int N = 8;
+    __device__ __forceinline__ static void unpack(const uint4 &u, float (&x)[N]) {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            x[2 * i] = __uint_as_float(w[i] << 16);
+            x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    }
+    __device__ __forceinline__ static uint32_t pack2(float lo, float hi) {
+        __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t *>(&b);
+    }
+    __device__ __forceinline__ static uint4 pack(const float (&x)[N]) {
+        return make_uint4(pack2(x[0], x[1]), pack2(x[2], x[3]), pack2(x[4], x[5]), pack2(x[6], x[7]));
+    }
+};
+
+__device__ __forceinline__ uint4 ld_shared_v4(const void *p) {
+    uint4 r;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "r"(smem_addr(p))
+                 : "memory");
+    return r;
+}
+
+__device__ __forceinline__ void st_global_v4(void *p, const uint4 &v) {
+    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+}  // namespace engram

@@ -1,0 +1,77 @@
+// The row-streaming pipeline shared by the gate forward and backward kernels.
+//
+// A CTA has NCW consumer warps and one producer warp.  The producer's elected
+// lane streams whole token rows (h, k, v, and dout for the backward) from HBM
+// into a ring of S shared-memory stages with 1-D bulk async copies (TMA),
+// signalling each stage's `full` mbarrier with the transferred byte count.  The
+// consumers cooperate on one token per stage: every consumer thread owns the
+// 16-byte vectors j = c, c + 32*NCW, c + 64*NCW, ... of the row, reduces its
+// partial sums with warp shuffles and then across warps through shared memory,
+// and releases the stage on its `empty` mbarrier (one arrival per warp).
+//
+// No row is kept on chip beyond its stage: the paper-form output alpha * v
+// needs h and k only for three sums, so each tensor is read from HBM once.
+#pragma once
+
+#include "engram_internal.cuh"
+
+namespace engram {
+
+// Template instances: NCW in {1, 2, 4, 8} consumer warps, up to VPT vectors per thread.
+constexpr int kVPT = 4;
+
+// Host-side choice of consumer warps for a row of `row_bytes` bytes.
+inline int pick_consumer_warps(int row_bytes) {
+    const int nvec = row_bytes / 16;
+    int ncw = 1;
+    while (ncw < 8 && ncw * 32 * kVPT < nvec) ncw *= 2;
+    return ncw;
+}
+
+struct PipelineShape {
+    int stages;         // S
+    int blocks_per_sm;  // resident CTAs per SM the grid is sized for
+    int smem_bytes;     // dynamic shared memory per CTA
+};
+
+// Stage ring + 2*S mbarriers + the [2][NCW][4] fp32 cross-warp reduction buffer.
+inline int pipeline_smem_bytes(int stages, int stage_bytes, int ncw) {
+    return stages * stage_bytes + 2 * stages * 8 + 2 * ncw * 4 * 4;
+}
+
+// Picks S and the CTAs per SM so that about `budget` bytes per SM are in flight:
+// at least 2 stages, preferring >= 2 CTAs per SM (one CTA's reduction bubble is
+// hidden by the other's copies) and >= 3 stages when they fit.
+inline PipelineShape pick_pipeline(int stage_bytes, int ncw, int smem_optin) {
+    const int budget = 200 * 1024;
+    PipelineShape best{0, 0, 0};
+    const int pref[][2] = {{4, 3}, {3, 3}, {2, 3}, {2, 2}, {1, 3}, {1, 2}};  // (blocks per SM, min stages)
+    for (const auto &bp : pref) {
+        const int b = bp[0];
+        int s = budget / (b * stage_bytes);
+        if (s > 8) s = 8;
+        if (s < bp[1]) continue;
+        const int smem = pipeline_smem_bytes(s, stage_bytes, ncw);
+        if (smem > smem_optin) continue;
+        best = {s, b, smem};
+        break;
+    }
+    return best;
+}
+
+// Sum over a named barrier's threads of a "failed" flag: every consumer thread
+// learns whether any of them gave up waiting, so they leave the loop together.
+__device__ __forceinline__ bool named_sync_or(uint32_t id, uint32_t count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.or.pred p, %2, %3, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
+}  // namespace engram

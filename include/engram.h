@@ -1,0 +1,267 @@
+/*
+ * engram.h -- C ABI of the GB300 (sm_103a) Engram conditional-memory hot path.
+ *
+ * The library implements the data-parallel hot path of Engram's conditional
+ * memory as hand-written CUDA kernels:
+ *
+ *   A  the deterministic multi-head N-gram hash over compressed token ids and the
+ *      gather of rows from prime-sized embedding tables  (engram_hash_gather);
+ *   B  the context-aware gate: weight fold (engram_fuse_weight), forward
+ *      (engram_gate_fwd), backward (engram_gate_bwd) and the deterministic
+ *      cross-block weight-gradient reduction (engram_grad_w_reduce).
+ *
+ * Sources (the TileLang tutorial, ch. 34 "TileKernels: Engram and mHC"):
+ *   sec. 1.2  the method: compression P: V -> V', K hash heads per N-gram order into
+ *             prime-sized tables E_{n,k}, the gate
+ *             alpha_t = sigmoid(RMSNorm(h_t)^T RMSNorm(k_t) / sqrt(d)), output alpha_t v_t;
+ *   sec. 2.1  the operator chain fused_weight -> gate_fwd -> gate_bwd -> grad_w_reduce
+ *             and the saved per-token statistics;
+ *   sec. 2.3  addressing: (max_n - 1) * heads rows per token, one concatenated table
+ *             indexed through exclusive prefix-sum offsets;
+ *   sec. 3.1  the fold w_fused = w_h (*) w_k that turns two RMSNorms and a dot
+ *             product into one pass over h and k;
+ *   sec. 4.1-4.4  backward, per-block partial weight gradients, the separate
+ *             reduction kernel with accumulate (main_grad) semantics.
+ *
+ * Conventions for every entry point:
+ *   - Tensor pointers are DEVICE pointers of the current CUDA device, owned by
+ *     the caller.  The library never allocates, frees or keeps them.
+ *   - Per-token tensors may be NULL when the token count is 0 (an empty tensor
+ *     has no storage); dw_partial may be NULL when P is 0.
+ *   - Tensors are dense, row-major, and start on a 16-byte boundary; rows of
+ *     [T, d] tensors are d elements long (so d * element size must be a
+ *     multiple of 16 bytes).
+ *   - Every call is asynchronous on `stream` (NULL = the legacy default
+ *     stream) and never synchronises, except engram_read_error_word and
+ *     engram_device_status, which say so.
+ *   - Host-side argument checks run before anything is launched; a call that
+ *     returns an error other than ENGRAM_ERR_CUDA has launched nothing.
+ *   - Thread safety: calls from several host threads are safe; the text behind
+ *     engram_last_error_string() is per thread.
+ *   - The kernels contain no unbounded wait: a pipeline wait that exceeds about
+ *     two seconds gives up, sets ENGRAM_DEVERR_TIMEOUT in the library's device
+ *     status word and returns.
+ */
+#ifndef ENGRAM_GB300_H
+#define ENGRAM_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The CUDA stream type (cudaStream_t) without including the CUDA headers. */
+typedef struct CUstream_st *engram_stream_t;
+
+#define ENGRAM_ABI_VERSION 1
+
+/* Largest number of hash tables (orders x heads) and largest N-gram order. */
+#define ENGRAM_MAX_TABLES 32
+#define ENGRAM_MAX_ORDER 8
+/* Largest gate row, in bytes (d * element size): 8192 bf16 or 4096 fp32 elements. */
+#define ENGRAM_MAX_ROW_BYTES 16384
+
+typedef enum {
+    ENGRAM_F32 = 0,  /* IEEE binary32 */
+    ENGRAM_BF16 = 1  /* bfloat16; results are rounded to nearest even */
+} engram_dtype;
+
+typedef enum {
+    ENGRAM_OK = 0,
+    ENGRAM_ERR_NULL = 1,   /* a required pointer is NULL */
+    ENGRAM_ERR_SHAPE = 2,  /* a size is negative, zero where it may not be, or too large */
+    ENGRAM_ERR_DTYPE = 3,  /* unknown dtype, or a dtype the entry point does not take */
+    ENGRAM_ERR_ALIGN = 4,  /* a tensor or a row does not start on a 16-byte boundary */
+    ENGRAM_ERR_CUDA = 5,   /* a CUDA runtime call failed; see engram_last_error_string() */
+    ENGRAM_ERR_INDEX = 6,  /* engram_read_error_word found a device-side error bit */
+    ENGRAM_ERR_DEVICE = 7  /* a pointer is not device memory of the current device */
+} engram_status;
+
+/* Bits of a device error word (engram_hash_gather's err_word, engram_device_status). */
+#define ENGRAM_DEVERR_TOKEN_ID 0x1u    /* a raw token id outside [0, vocab): hashed as the pad id 0 */
+#define ENGRAM_DEVERR_COMPRESSED 0x2u  /* a compressed id outside [0, vocab_c): hashed as 0 */
+#define ENGRAM_DEVERR_SEQ_OFFSETS 0x4u /* seq_offsets not 0 = o_0 <= o_1 <= ... <= o_S = T */
+#define ENGRAM_DEVERR_TIMEOUT 0x8u     /* a bounded in-kernel wait gave up (should never happen) */
+
+/* ------------------------------------------------------------------------- */
+/* Library information and errors                                            */
+/* ------------------------------------------------------------------------- */
+
+/* ENGRAM_ABI_VERSION of the loaded library. */
+int32_t engram_abi_version(void);
+
+/* Static text for a status code. */
+const char *engram_status_string(engram_status status);
+
+/* Text of the last ENGRAM_ERR_CUDA (or other error) raised on the calling thread; "" if none. */
+const char *engram_last_error_string(void);
+
+/*
+ * Device-pointer checks.  level 1 (default) asks the CUDA runtime whether every
+ * tensor pointer is device memory of the current device (ENGRAM_ERR_DEVICE
+ * otherwise); level 0 skips that query and keeps only the host-side checks.
+ * Returns the previous level.  Process-wide.
+ */
+int32_t engram_set_validation(int32_t level);
+
+/*
+ * Caps the number of CTAs each kernel launch uses (0 = no cap, the default:
+ * grids are sized from the SM count).  For sharing the GPU with concurrent work
+ * on other streams.  Results do not depend on it: every partition of the work
+ * is fixed by the problem sizes alone.  Returns the previous cap.  Process-wide.
+ */
+int32_t engram_set_max_ctas(int32_t max_ctas);
+
+/*
+ * Copies a device error word to *host_out.  SYNCHRONISES `stream` first.
+ * Returns ENGRAM_ERR_INDEX when any bit is set, ENGRAM_OK otherwise.
+ */
+engram_status engram_read_error_word(const uint32_t *err_word, engram_stream_t stream, uint32_t *host_out);
+
+/*
+ * The library's own device status word of the current device (ENGRAM_DEVERR_* bits
+ * OR-ed by every kernel, e.g. ENGRAM_DEVERR_TIMEOUT).  SYNCHRONISES the device.
+ * clear != 0 resets it to 0 after reading.
+ */
+engram_status engram_device_status(uint32_t *host_out, int32_t clear);
+
+/* ------------------------------------------------------------------------- */
+/* A0-A2: compression, multi-head N-gram hash and gather  (ch. 34 sec. 1.2 item 2, sec. 2.3) */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * Fixed hash hyper-parameters (host memory; read during the call only).
+ *
+ * Tables are numbered in (order ascending, head ascending) order:
+ * table = (n - min_order) * heads + k for n in [min_order, min_order + num_orders),
+ * k in [0, heads).  tables = num_orders * heads <= ENGRAM_MAX_TABLES.
+ * multipliers is [tables][mult_stride] (mult_stride >= max order), primes is
+ * [tables]; primes are the row counts p_{n,k} of the tables, each in [1, 2^31).
+ * They need not be prime, but the method's collision behaviour assumes it.
+ */
+typedef struct {
+    int32_t min_order;           /* smallest N-gram order n (>= 1; the method uses 2) */
+    int32_t num_orders;          /* number of orders (>= 1); max order <= ENGRAM_MAX_ORDER */
+    int32_t heads;               /* K hash heads per order (>= 1) */
+    int32_t mult_stride;         /* row length of `multipliers` */
+    const uint64_t *multipliers; /* HOST [tables][mult_stride]; entry j < n multiplies id'[t - j] */
+    const uint64_t *primes;      /* HOST [tables] */
+} engram_hash_spec;
+
+typedef struct {
+    const int32_t *token_ids;    /* [T] raw ids in [0, vocab) */
+    int64_t T;                   /* number of tokens (>= 0) */
+    const int64_t *seq_offsets;  /* [num_seqs + 1] boundaries 0 = o_0 <= ... <= o_S = T (cu_seqlens) */
+    int32_t num_seqs;            /* >= 1 */
+    const int32_t *compress_map; /* [vocab] -> [0, vocab_c), the compression P; NULL = identity */
+    int32_t vocab;               /* raw vocabulary size (>= 1) */
+    int32_t vocab_c;             /* compressed vocabulary size (>= 1; = vocab when compress_map is NULL) */
+    const void *table;           /* [table_rows, row_dim] concatenated E_{n,k}, table order */
+    int64_t table_rows;          /* >= sum(primes) */
+    int32_t row_dim;             /* elements per row; row_dim * element size a multiple of 16 bytes */
+    engram_dtype dtype;          /* element type of table and out_rows (bit copies either way) */
+    int32_t *out_indices;        /* [T, tables] local index idx_{n,k}(t) in [0, p); NULL = not written */
+    void *out_rows;              /* [T, tables * row_dim] e_t = concatenated rows; NULL = not written */
+    uint32_t *err_word;          /* device word, OR-ed with ENGRAM_DEVERR_* bits; NULL = not reported */
+} engram_hash_gather_args;
+
+/*
+ * For every token t (in the sequence s with o_s <= t < o_{s+1}) and table (n, k):
+ *     id'(q) = compress_map[token_ids[q]] for o_s <= q, else the pad id 0;
+ *     h      = XOR over j < n of  (uint64) id'(t - j) * multipliers[table][j]   (mod 2^64);
+ *     idx    = h mod primes[table]   (unsigned 64-bit);
+ *     row    = (exclusive prefix sum of primes before `table`) + idx;
+ *     out_rows[t, table * row_dim : (table + 1) * row_dim] = table[row, :]   (bit copy).
+ * The pages name only a "lightweight multiplicative-XOR hash"; this exact form
+ * is the library's reading (ch. 34 sec. 1.2 item 2).  Indices depend only on the
+ * ids, so results are bit-identical across runs and devices (sec. 2.3).
+ * Bad ids are reported through err_word and hashed as 0; no read leaves the table.
+ */
+engram_status engram_hash_gather(const engram_hash_spec *spec, const engram_hash_gather_args *args,
+                                 engram_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
+/* B0: weight fold  (ch. 34 sec. 3.1, sec. 4.1)                               */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * w_fused[i] = w_h[i] * w_k[i], computed and stored in fp32, for i < d.
+ * w_h and w_k are the RMSNorm weights of the hidden state and of the key, in
+ * `dtype` (fp32 or bf16, both widened exactly to fp32).  Run once per weight update.
+ */
+engram_status engram_fuse_weight(const void *w_h, const void *w_k, engram_dtype dtype, float *w_fused,
+                                 int32_t d, engram_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
+/* B1: gate forward  (ch. 34 sec. 1.2 item 3, sec. 2.1, sec. 3.1-3.2)          */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * For each token t < T, with rows h_t, k_t, v_t of length d in `dtype` and
+ * s = 1/sqrt(d):
+ *     rstd_h = 1/sqrt(sum_i h_i^2 / d + eps),  rstd_k likewise,
+ *     dot    = sum_i h_i * w_fused_i * k_i,
+ *     alpha  = sigmoid(s * rstd_h * rstd_k * dot),
+ *     out_t  = alpha * v_t     (in `dtype`, rounded to nearest even for bf16).
+ * All arithmetic is fp32.  alpha, rstd_h, rstd_k and dot are [T] fp32 and are
+ * saved for the backward; each may be NULL (inference needs none of them).
+ * out may not alias h, k or v.
+ */
+engram_status engram_gate_fwd(const void *h, const void *k, const void *v, engram_dtype dtype,
+                              const float *w_fused, int64_t T, int32_t d, float eps,
+                              void *out, float *alpha, float *rstd_h, float *rstd_k, float *dot,
+                              engram_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
+/* B2: gate backward  (ch. 34 sec. 4.1-4.2)                                   */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * The recommended number of weight-gradient partials P for (T, d).  A function
+ * of T and d only (never of the GPU), so the partials and the reduced gradient
+ * are bitwise reproducible on any device.  Host only.
+ */
+engram_status engram_gate_bwd_num_partials(int64_t T, int32_t d, int32_t *P);
+
+/*
+ * Given dout = dL/dout [T, d] and the forward's saved alpha, rstd_h, rstd_k,
+ * dot [T] (fp32), with w = w_fused and s = 1/sqrt(d), for each token:
+ *     dv     = alpha * dout
+ *     dalpha = sum_i dout_i v_i
+ *     c      = dalpha * alpha * (1 - alpha) * s * rstd_h * rstd_k
+ *     dh_i   = c * (w_i k_i - dot * rstd_h^2 * h_i / d)
+ *     dk_i   = c * (w_i h_i - dot * rstd_k^2 * k_i / d)
+ * and the weight-gradient partials
+ *     dw_partial[p, i] = sum over t in [p*C, min(T, (p+1)*C)) of c_t h_t,i k_t,i,
+ * C = ceil(T / P), tokens summed in ascending order (a partial with no token is 0).
+ * dh, dk, dv are [T, d] in `dtype`; dw_partial is [P, d] fp32, P >= 1.
+ * Outputs may not alias inputs.
+ */
+engram_status engram_gate_bwd(const void *dout, const void *h, const void *k, const void *v, engram_dtype dtype,
+                              const float *w_fused, const float *alpha, const float *rstd_h,
+                              const float *rstd_k, const float *dot, int64_t T, int32_t d,
+                              void *dh, void *dk, void *dv, float *dw_partial, int32_t P,
+                              engram_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
+/* B3: weight-gradient reduction  (ch. 34 sec. 4.3-4.4; determinism: the DSL article's
+ *     "partitioned writes plus one ordered reduction instead of atomics")      */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * S = sum over p < P of dw_partial[p, :] in a fixed order that depends on P only
+ * (bitwise reproducible).  dweight_fused (nullable) receives S.  When the four
+ * weight pointers are given (all or none):
+ *     grad_w_h += S * w_k,   grad_w_k += S * w_h     (accumulate, like a main_grad buffer)
+ * w_h, w_k, grad_w_h, grad_w_k are [d] fp32.  At least one output must be given.
+ */
+engram_status engram_grad_w_reduce(const float *dw_partial, int32_t P, int32_t d, float *dweight_fused,
+                                   const float *w_h, const float *w_k, float *grad_w_h, float *grad_w_k,
+                                   engram_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ENGRAM_GB300_H */

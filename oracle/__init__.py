@@ -52,7 +52,7 @@ def _load():
             lib.eo_gate_fwd.argtypes = [_p, _p, _p, ctypes.c_int, _p, _p, _i64, _i32, _f64, _i64, _i64,
                                         _p, _p, _p, _p, _p, _p]
             lib.eo_gate_bwd.argtypes = [_p, _p, _p, _p, ctypes.c_int, _p, _p, _i64, _i32, _f64, _i64, _i64,
-                                        _p, _p, _p, _p]
+                                        _p, _p, _p, _p, _p]
             lib.eo_grad_w_reduce.argtypes = [_p, _i32, _i32, _p, _p, _p, _p, _p]
             for f in ("eo_hash_indices", "eo_gather_rows", "eo_fuse_weight", "eo_gate_fwd", "eo_gate_bwd",
                       "eo_grad_w_reduce"):
@@ -142,7 +142,7 @@ def gate_fwd(h, k, v, w_h, w_k, eps: float, t_begin: int = 0, t_end: int | None 
 
 
 def gate_bwd(dout, h, k, v, w_h, w_k, eps: float, t_begin: int = 0, t_end: int | None = None) -> dict:
-    """fp64 dh, dk, dv [n, d] and dweight [d] (sum over the token range)."""
+    """fp64 dh, dk, dv [n, d], dweight [d] (sum over the token range) and dweight_abs [d] (sum of |terms|)."""
     lib = _load()
     g, h, k, v = (np.ascontiguousarray(x) for x in (dout, h, k, v))
     dt = _dtype_code(h)
@@ -154,8 +154,10 @@ def gate_bwd(dout, h, k, v, w_h, w_k, eps: float, t_begin: int = 0, t_end: int |
     n = t_end - t_begin
     res = {name: np.zeros((n, d), dtype=np.float64) for name in ("dh", "dk", "dv")}
     res["dweight"] = np.zeros(d, dtype=np.float64)
+    res["dweight_abs"] = np.zeros(d, dtype=np.float64)
     rc = lib.eo_gate_bwd(_ptr(g), _ptr(h), _ptr(k), _ptr(v), dt, _ptr(wh), _ptr(wk), T, d, float(eps), t_begin,
-                         t_end, _ptr(res["dh"]), _ptr(res["dk"]), _ptr(res["dv"]), _ptr(res["dweight"]))
+                         t_end, _ptr(res["dh"]), _ptr(res["dk"]), _ptr(res["dv"]), _ptr(res["dweight"]),
+                         _ptr(res["dweight_abs"]))
     _check(rc, "gate_bwd")
     return res
 

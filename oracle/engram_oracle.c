@@ -279,19 +279,24 @@ int eo_gate_fwd(const void *h, const void *k, const void *v, int dtype,
  *     dweight_i = sum_t c_t h_t,i k_t,i                             (= dL/dw_i)
  * The forward statistics are recomputed here in fp64 from h and k.
  * dweight [d] is overwritten with the sum over [t_begin, t_end) in token order.
+ * dweight_abs (nullable) receives sum_t |c_t h_t,i k_t,i|, the magnitude scale
+ * that an fp32 accumulation of dweight is compared against.
  */
 int eo_gate_bwd(const void *g, const void *h, const void *k, const void *v, int dtype,
                 const float *w_h, const float *w_k, int64_t T, int32_t d, double eps,
                 int64_t t_begin, int64_t t_end,
-                double *dh, double *dk, double *dv, double *dweight)
+                double *dh, double *dk, double *dv, double *dweight, double *dweight_abs)
 {
     if (!g || !h || !k || !v || !w_h || !w_k || !dh || !dk || !dv || !dweight)
         return EO_ERR_ARG;
     if ((dtype != EO_F32 && dtype != EO_BF16) || d <= 0 || t_begin < 0 || t_end > T || t_begin > t_end)
         return EO_ERR_ARG;
     const double s = 1.0 / sqrt((double)d);
-    for (int32_t i = 0; i < d; ++i)
+    for (int32_t i = 0; i < d; ++i) {
         dweight[i] = 0.0;
+        if (dweight_abs)
+            dweight_abs[i] = 0.0;
+    }
     for (int64_t t = t_begin; t < t_end; ++t) {
         struct eo_token_stats st;
         eo_token_forward(h, k, dtype, w_h, w_k, t, d, eps, &st);
@@ -311,6 +316,8 @@ int eo_gate_bwd(const void *g, const void *h, const void *k, const void *v, int 
             dh[o + i] = c * (wi * ki - st.dot * st.rh * st.rh * hi / (double)d);
             dk[o + i] = c * (wi * hi - st.dot * st.rk * st.rk * ki / (double)d);
             dweight[i] += c * hi * ki;
+            if (dweight_abs)
+                dweight_abs[i] += fabs(c * hi * ki);
         }
     }
     return EO_OK;

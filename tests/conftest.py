@@ -16,6 +16,8 @@ def pytest_configure(config):
 def cuda_lib():
     """The CUDA library binding; a GPU test fails loudly when the library is missing."""
     import engram_conditional_memory_gb300 as ecm
+    from engram_conditional_memory_gb300 import build
 
+    build.build()  # no-op when the in-tree library is up to date
     ecm.load_library()
     return ecm

@@ -1,0 +1,117 @@
+"""The C-ABI library on a machine without a GPU: it builds, loads, exports every
+symbol include/engram.h declares, and rejects bad arguments on the host before
+touching the device (no compute call is made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "engram.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from engram_conditional_memory_gb300 import build
+
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def _declared():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w\s\*]+?\b(engram_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for required in ("engram_hash_gather", "engram_fuse_weight", "engram_gate_fwd", "engram_gate_bwd",
+                     "engram_gate_bwd_num_partials", "engram_grad_w_reduce"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in _declared() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_host_side_rejections(lib):
+    st = ctypes.c_int
+    lib.engram_gate_fwd.restype = st
+    lib.engram_gate_fwd.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32,
+                                                            ctypes.c_float] + [ctypes.c_void_p] * 6
+    lib.engram_gate_fwd.argtypes[3] = ctypes.c_int
+    fake = ctypes.c_void_p(0x10000)  # never dereferenced: each call below fails before any CUDA call
+    odd = ctypes.c_void_p(0x10008)
+    # NULL input
+    assert lib.engram_gate_fwd(None, fake, fake, 1, fake, 8, 64, 1e-6, fake, None, None, None, None, None) == 1
+    # unknown dtype
+    assert lib.engram_gate_fwd(fake, fake, fake, 7, fake, 8, 64, 1e-6, fake, None, None, None, None, None) == 3
+    # negative T, and a row that is not a multiple of 16 bytes (d = 4 bf16)
+    assert lib.engram_gate_fwd(fake, fake, fake, 1, fake, -1, 64, 1e-6, fake, None, None, None, None, None) == 2
+    assert lib.engram_gate_fwd(fake, fake, fake, 1, fake, 8, 4, 1e-6, fake, None, None, None, None, None) == 4
+    # row too long (8200 bf16 > 16 KB) and a misaligned tensor
+    assert lib.engram_gate_fwd(fake, fake, fake, 1, fake, 8, 8200, 1e-6, fake, None, None, None, None, None) == 2
+    assert lib.engram_gate_fwd(odd, fake, fake, 1, fake, 8, 64, 1e-6, fake, None, None, None, None, None) == 4
+    lib.engram_last_error_string.restype = ctypes.c_char_p
+    assert b"aligned" in lib.engram_last_error_string()
+
+    lib.engram_grad_w_reduce.restype = st
+    lib.engram_grad_w_reduce.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32] + [ctypes.c_void_p] * 6
+    assert lib.engram_grad_w_reduce(None, 4, 64, fake, None, None, None, None, None) == 1
+    assert lib.engram_grad_w_reduce(fake, 4, 64, None, None, None, None, None, None) == 1  # no output
+    assert lib.engram_grad_w_reduce(fake, 4, 64, fake, fake, None, None, None, None) == 1  # weights not all given
+    assert lib.engram_grad_w_reduce(fake, 4, 66, fake, None, None, None, None, None) == 4
+    assert lib.engram_grad_w_reduce(fake, -1, 64, fake, None, None, None, None, None) == 2
+
+
+def test_partition_rule(lib):
+    lib.engram_gate_bwd_num_partials.restype = ctypes.c_int
+    lib.engram_gate_bwd_num_partials.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)]
+    P = ctypes.c_int32()
+
+    def parts(T, d=4096):
+        assert lib.engram_gate_bwd_num_partials(T, d, ctypes.byref(P)) == 0
+        return P.value
+
+    assert parts(0) == 1 and parts(1) == 1 and parts(16) == 1 and parts(17) == 2
+    assert parts(4096) == 256 and parts(16384) == 1024 and parts(131072) == 1024
+    for T in (1, 100, 4096, 16384, 32768, 131072, 139_000):
+        p = parts(T)
+        chunk = -(-T // p)
+        assert 1 <= p <= 1024 and chunk >= min(T, 15) and (p - 1) * chunk < T <= p * chunk
+    assert lib.engram_gate_bwd_num_partials(-1, 64, ctypes.byref(P)) == 2
+
+
+def test_hash_gather_host_rejections(lib):
+    import numpy as np
+
+    from engram_conditional_memory_gb300.binding import _HashGatherArgs, _HashSpec
+
+    lib.engram_hash_gather.restype = ctypes.c_int
+    lib.engram_hash_gather.argtypes = [ctypes.c_void_p] * 3
+    mult = np.ones((4, 3), dtype=np.uint64)
+    primes = np.array([5, 7, 11, 13], dtype=np.uint64)
+    spec = _HashSpec(2, 2, 2, 3, mult.ctypes.data, primes.ctypes.data)
+    fake = 0x10000
+    args = _HashGatherArgs(fake, 10, fake, 1, None, 100, 100, fake, 36, 8, 1, None, fake, None)
+    # too few table rows for sum(primes) = 36 - 1
+    args.table_rows = 35
+    assert lib.engram_hash_gather(ctypes.byref(spec), ctypes.byref(args), None) == 2
+    args.table_rows = 36
+    args.row_dim = 4  # 8-byte rows
+    assert lib.engram_hash_gather(ctypes.byref(spec), ctypes.byref(args), None) == 4
+    args.row_dim = 8
+    bad = _HashSpec(2, 2, 2, 2, mult.ctypes.data, primes.ctypes.data)  # stride 2 < max order 3
+    assert lib.engram_hash_gather(ctypes.byref(bad), ctypes.byref(args), None) == 2
+    many = _HashSpec(2, 2, 17, 3, mult.ctypes.data, primes.ctypes.data)  # 34 tables > 32
+    assert lib.engram_hash_gather(ctypes.byref(many), ctypes.byref(args), None) == 2
+    zero = np.array([5, 0, 11, 13], dtype=np.uint64)
+    zspec = _HashSpec(2, 2, 2, 3, mult.ctypes.data, zero.ctypes.data)
+    assert lib.engram_hash_gather(ctypes.byref(zspec), ctypes.byref(args), None) == 2
+    args.out_rows = None
+    assert lib.engram_hash_gather(ctypes.byref(spec), ctypes.byref(args), None) == 1  # no output at all
+    args.token_ids = None
+    args.out_rows = fake
+    assert lib.engram_hash_gather(ctypes.byref(spec), ctypes.byref(args), None) == 1  # NULL ids with T > 0
