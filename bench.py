@@ -1,0 +1,578 @@
+#!/usr/bin/env python3
+"""Benchmark of the Engram conditional-memory hot path on GB300.
+
+One step = one pass of the whole hot path over one batch of 16 sequences x 4096
+tokens (65,536 tokens):
+  1. hash + gather of every token's 16 table rows (orders {2, 3} x 8 heads,
+     ~2.0M-row prime tables, 64 bf16 per row, 4.1 GB resident) -> e [65536, 1024];
+  2. the weight fold w = w_h * w_k;
+  3. the context-aware gate, forward + backward + weight-gradient reduction,
+     on four micro-batches of T = 16384 tokens at d = 4096 (bf16), the
+     reduction accumulating into fp32 grad_w_h / grad_w_k.
+The reported value is tokens/s through the whole step (whole job, all ranks).
+Inputs are resident in HBM (the device-timed value) or copied from pinned host
+memory every step (the `e2e` value).  The per-step working set (4.1 GB table,
+2 GB of gate inputs) is far larger than L2, so no flush is needed.
+
+`--impl reference` times the CPU oracle (the correctness reference, plain C,
+fp64) on the host cores instead, each step a bounded sample of the same
+workload scaled to the whole step.
+"""
+from __future__ import annotations
+
+import argparse
+import datetime as _dt
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "gate fwd+bwd tokens/s and HBM GB/s (% of roofline); hash-gather rows/s"
+SEQS, SEQ_LEN = 16, 4096
+MICRO_T, D = 16384, 4096
+EPS = 1e-6
+WORKLOAD = (f"engram step: hash+gather {SEQS}x{SEQ_LEN} tokens (Zipf(1.1) ids over V=128000 -> V'=98560, "
+            f"16 tables of ~2.0M x 64 bf16 = 4.1 GB) + weight fold + gate fwd/bwd/grad_w_reduce on "
+            f"4 micro-batches T={MICRO_T} d={D} bf16")
+
+
+# ----------------------------------------------------------------------------- host-side plumbing
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    return rank, local, world
+
+
+def aggregate_max(value: float, group_backend_device=None) -> float:
+    """Max of a per-rank scalar over all ranks (identity without torch.distributed)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=group_backend_device or "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(device=None):
+    import torch.distributed as dist
+
+    if dist.is_available() and dist.is_initialized():
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def load_traffic(kernel: str):
+    """ncu DRAM bytes per launch recorded for `kernel`, or None when its source changed since the capture."""
+    import hashlib
+
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)[kernel]
+    except (OSError, KeyError, ValueError):
+        return None
+    h = hashlib.sha256()
+    for src in rec["sources"]:
+        with open(os.path.join(ROOT, src), "rb") as f:
+            h.update(f.read())
+    return rec["dram_bytes_per_launch"] if h.hexdigest() == rec["sources_sha256"] else None
+
+
+class ClockSampler:
+    """nvidia-smi samples (SM clock, throttle reasons) taken while the timed region runs."""
+
+    FIELDS = ["timestamp", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = os.path.join("/tmp", f"engram_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={','.join(self.FIELDS)}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self, t0: _dt.datetime, t1: _dt.datetime):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) != len(self.FIELDS):
+                    continue
+                try:
+                    ts = _dt.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
+                    rows.append((ts, float(parts[1]), float(parts[2]), parts[4:]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        inside = [r for r in rows if t0 <= r[0] <= t1]
+        window = "timed region"
+        if len(inside) < 3:  # short timed region: widen to the samples around it
+            pad = _dt.timedelta(seconds=0.5)
+            inside = [r for r in rows if t0 - pad <= r[0] <= t1 + pad]
+            window = "timed region +- 0.5 s"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "window": window}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in inside for n, v in zip(names, r[3]) if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": reasons, "samples": len(inside), "window": window}
+
+
+# ----------------------------------------------------------------------------- the workload
+
+def algorithmic_bytes(P: int):
+    """Algorithmic HBM bytes per launch of each kernel in one step (see the design notes)."""
+    T_all = SEQS * SEQ_LEN
+    tables, row_bytes = 16, 128
+    return {
+        "hash_gather": T_all * (4 + 4 + 2 * tables * row_bytes),  # id, compressed id, 16 rows read + e_t written
+        "fuse_weight": 3 * 4 * D,
+        "gate_fwd": MICRO_T * (8 * D + 16),                       # h, k, v read, out written, 4 fp32 stats
+        "gate_bwd": MICRO_T * (14 * D + 16) + P * D * 4,         # dout, v, h, k, stats read; dh, dk, dv, partials
+        "grad_w_reduce": P * D * 4 + 7 * D * 4,                   # partials, w_h, w_k, grads (r+w), dweight
+    }
+
+
+def make_workload(device):
+    import torch
+
+    from synth import device as SD
+    from synth import workloads as W
+
+    hw = W.hash_gather_64k(num_seqs=SEQS, seq_len=SEQ_LEN)
+    gates = [W.GateWorkload(name=f"mb{i}", T=MICRO_T, d=D, dtype="bf16", seed=3 * 101 + 7 + 1000003 * i)
+             for i in range(4)]
+    import engram_conditional_memory_gb300 as ecm
+
+    s = hw.spec
+    wk = {
+        "hw": hw,
+        "spec": ecm.HashSpec(s.min_order, s.num_orders, s.heads, s.multipliers, s.primes),
+        "ids": torch.from_numpy(hw.token_ids).to(device),
+        "offs": torch.from_numpy(hw.seq_offsets).to(device),
+        "cmap": torch.from_numpy(hw.compress_map).to(device),
+        "table": SD.hash_table(hw, device),
+        "mb": [SD.gate_device_inputs(g, device) for g in gates],
+    }
+    w0 = wk["mb"][0]
+    wk["w_h"], wk["w_k"] = w0["w_h"], w0["w_k"]
+    T_all = hw.T
+    wk["rows"] = torch.empty((T_all, s.tables * hw.row_dim), dtype=torch.bfloat16, device=device)
+    wk["w_fused"] = torch.empty(D, dtype=torch.float32, device=device)
+    P = ecm.gate_bwd_num_partials(MICRO_T, D)
+    wk["P"] = P
+    wk["out"] = [torch.empty((MICRO_T, D), dtype=torch.bfloat16, device=device) for _ in range(4)]
+    wk["dh"] = [torch.empty_like(o) for o in wk["out"]]
+    wk["dk"] = [torch.empty_like(o) for o in wk["out"]]
+    wk["dv"] = [torch.empty_like(o) for o in wk["out"]]
+    wk["stats"] = [tuple(torch.empty(MICRO_T, dtype=torch.float32, device=device) for _ in range(4))
+                   for _ in range(4)]
+    wk["part"] = [torch.empty((P, D), dtype=torch.float32, device=device) for _ in range(4)]
+    wk["dweight"] = torch.empty(D, dtype=torch.float32, device=device)
+    wk["grad_w_h"] = torch.zeros(D, dtype=torch.float32, device=device)
+    wk["grad_w_k"] = torch.zeros(D, dtype=torch.float32, device=device)
+    return wk
+
+
+def run_step(wk, mark=None):
+    """Launch one step (14 kernels) on the current stream; `mark(name)` is called after each launch."""
+    import engram_conditional_memory_gb300 as ecm
+
+    hw = wk["hw"]
+    ecm.hash_gather(wk["spec"], wk["ids"], wk["offs"], wk["table"], wk["cmap"], hw.vocab, hw.vocab_c,
+                    out_rows=wk["rows"])
+    mark and mark("hash_gather")
+    ecm.fuse_weight(wk["w_h"], wk["w_k"], out=wk["w_fused"])
+    mark and mark("fuse_weight")
+    for i, m in enumerate(wk["mb"]):
+        st = wk["stats"][i]
+        ecm.gate_fwd(m["h"], m["k"], m["v"], wk["w_fused"], EPS, out=wk["out"][i], stats=st)
+        mark and mark("gate_fwd")
+        ecm.gate_bwd(m["dout"], m["h"], m["k"], m["v"], wk["w_fused"], *st, P=wk["P"], dh=wk["dh"][i],
+                     dk=wk["dk"][i], dv=wk["dv"][i], dw_partial=wk["part"][i])
+        mark and mark("gate_bwd")
+        ecm.grad_w_reduce(wk["part"][i], dweight_fused=wk["dweight"], w_h=wk["w_h"], w_k=wk["w_k"],
+                          grad_w_h=wk["grad_w_h"], grad_w_k=wk["grad_w_k"])
+        mark and mark("grad_w_reduce")
+    return 14
+
+
+# ----------------------------------------------------------------------------- device timing
+
+def time_device(wk, steps, warmup, device):
+    import torch
+
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        run_step(wk)
+    torch.cuda.synchronize()
+    # events between consecutive launches: per-kernel durations inside the timed region
+    bounds = []
+
+    def mark(name):
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(stream)
+        bounds.append((name, e))
+
+    barrier(device)
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    wall0 = _dt.datetime.now()
+    start.record(stream)
+    prev = start
+    launches = 0
+    for _ in range(steps):
+        launches += run_step(wk, mark)
+    end.record(stream)
+    torch.cuda.synchronize()
+    wall1 = _dt.datetime.now()
+    barrier(device)
+    elapsed = start.elapsed_time(end)
+    per = {}
+    for name, e in bounds:
+        per.setdefault(name, []).append(prev.elapsed_time(e))
+        prev = e
+    return elapsed, per, launches, wall0, wall1
+
+
+def time_e2e(wk, steps, warmup, device):
+    """Same step through the public API, with each step's inputs copied from pinned host memory first
+    and the step's result (the accumulated fp32 weight gradients) read back to the host."""
+    import torch
+
+    stream = torch.cuda.current_stream()
+    host_ids = wk["ids"].cpu().pin_memory()
+    host_mb = [{n: m[n].cpu().pin_memory() for n in ("h", "k", "v", "dout")} for m in wk["mb"]]
+    res_h = torch.empty(2 * D, dtype=torch.float32, pin_memory=True)
+    h2d = host_ids.numel() * 4 + sum(t.numel() * t.element_size() for m in host_mb for t in m.values())
+    d2h = res_h.numel() * 4
+
+    def step():
+        wk["ids"].copy_(host_ids, non_blocking=True)
+        for m, hm in zip(wk["mb"], host_mb):
+            for n, t in hm.items():
+                m[n].copy_(t, non_blocking=True)
+        run_step(wk)
+        res_h[:D].copy_(wk["grad_w_h"], non_blocking=True)
+        res_h[D:].copy_(wk["grad_w_k"], non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(device)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        step()
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(device)
+    return start.elapsed_time(end), h2d, d2h
+
+
+# ----------------------------------------------------------------------------- the CPU oracle
+
+def _oracle_threads():
+    return max(1, os.cpu_count() or 1)
+
+
+def oracle_step_seconds(hw, table_host, gate_host, gate_tokens: int, hash_tokens: int):
+    """Wall time of the oracle on a sample: hash + gather of `hash_tokens` tokens and gate fwd + bwd of
+    `gate_tokens` tokens, split over all host threads; returns (t_hash, t_gate, threads)."""
+    import oracle
+
+    n = _oracle_threads()
+    s = hw.spec
+
+    def hash_part(b):
+        idx = oracle.hash_indices(hw.token_ids, hw.seq_offsets, hw.compress_map, hw.vocab, s.min_order,
+                                  s.num_orders, s.heads, s.multipliers, s.primes, b[0], b[1])
+        oracle.gather_rows(table_host, s.primes, idx)
+
+    def gate_part(b):
+        sl = slice(b[0], b[1])
+        g = gate_host
+        oracle.gate_fwd(g["h"][sl], g["k"][sl], g["v"][sl], g["w_h"], g["w_k"], EPS)
+        oracle.gate_bwd(g["dout"][sl], g["h"][sl], g["k"][sl], g["v"][sl], g["w_h"], g["w_k"], EPS)
+
+    with ThreadPoolExecutor(n) as ex:
+        hb = [(hash_tokens * i // n, hash_tokens * (i + 1) // n) for i in range(n)]
+        t0 = time.perf_counter()
+        list(ex.map(hash_part, hb))
+        t1 = time.perf_counter()
+        gb = [(gate_tokens * i // n, gate_tokens * (i + 1) // n) for i in range(n)]
+        list(ex.map(gate_part, gb))
+        t2 = time.perf_counter()
+    return t1 - t0, t2 - t1, n
+
+
+def gate_host_sample(wk, n_tokens):
+    """Host copies (bf16 bits) of the first n_tokens rows of micro-batch 0."""
+    out = {}
+    m = wk["mb"][0]
+    for name in ("h", "k", "v", "dout"):
+        t = m[name][:n_tokens].contiguous().cpu()
+        out[name] = t.view(__import__("torch").int16).numpy().view(np.uint16)
+    out["w_h"] = m["w_h"].cpu().numpy()
+    out["w_k"] = m["w_k"].cpu().numpy()
+    return out
+
+
+def gate_host_sample_synth(n_tokens):
+    """The same micro-batch drawn on the host (the reference arm runs without a GPU)."""
+    from synth import workloads as W
+
+    g = W.GateWorkload(name="mb0", T=n_tokens, d=D, dtype="bf16", seed=3 * 101 + 7)
+    return W.gate_host_inputs(g)
+
+
+def cpu_baseline(hw, gate_host, gate_tokens, reps=1):
+    table_host = np.zeros((hw.spec.total_rows, hw.row_dim), dtype=np.uint16)
+    T_all = hw.T
+    oracle_step_seconds(hw, table_host, gate_host, min(gate_tokens, 256), T_all)  # first touch of table pages
+    best = None
+    for _ in range(reps):
+        t_hash, t_gate, n = oracle_step_seconds(hw, table_host, gate_host, gate_tokens, T_all)
+        step_s = t_hash + t_gate * (4 * MICRO_T / gate_tokens)
+        best = step_s if best is None else min(best, step_s)
+    return T_all / best, n, best
+
+
+# ----------------------------------------------------------------------------- single-op runs (profiling)
+
+def main_only(args, device):
+    """Time one kernel alone on its workload: the small cases the ncu captures are taken on."""
+    import torch
+
+    import engram_conditional_memory_gb300 as ecm
+    from synth import device as SD
+    from synth import workloads as W
+
+    op = args.only
+    stream = torch.cuda.current_stream()
+    if op.startswith("hash_gather"):
+        if op == "hash_gather_small":  # 4 x 4096 tokens, 16 tables of ~200k rows (0.41 GB, > L2)
+            hw = W.hash_gather_64k(num_seqs=4, seq_len=SEQ_LEN)
+            hw = W.HashGatherWorkload(**{**hw.__dict__, "spec": W.hash_spec(4 * 7919 + 11, 2, 2, 8, 200_003)})
+        else:
+            hw = W.hash_gather_64k(num_seqs=SEQS, seq_len=SEQ_LEN)
+        s = hw.spec
+        spec = ecm.HashSpec(s.min_order, s.num_orders, s.heads, s.multipliers, s.primes)
+        ids, offs = torch.from_numpy(hw.token_ids).to(device), torch.from_numpy(hw.seq_offsets).to(device)
+        cmap, table = torch.from_numpy(hw.compress_map).to(device), SD.hash_table(hw, device)
+        rows = torch.empty((hw.T, s.tables * hw.row_dim), dtype=table.dtype, device=device)
+        nbytes = hw.T * (8 + 2 * s.tables * hw.row_dim * 2)
+
+        def launch():
+            ecm.hash_gather(spec, ids, offs, table, cmap, hw.vocab, hw.vocab_c, out_rows=rows)
+    else:
+        wl = {"gate_fwd_2k": W.gate_fwd_2k()}.get(op, W.gate_train_4k())
+        t = SD.gate_device_inputs(wl, device)
+        wf = ecm.fuse_weight(t["w_h"], t["w_k"])
+        out, *st = ecm.gate_fwd(t["h"], t["k"], t["v"], wf, EPS)
+        P = ecm.gate_bwd_num_partials(wl.T, wl.d)
+        dh, dk, dv, part = ecm.gate_bwd(t["dout"], t["h"], t["k"], t["v"], wf, *st, P=P)
+        if op == "gate_bwd":
+            nbytes = wl.T * (14 * wl.d + 16) + P * wl.d * 4
+
+            def launch():
+                ecm.gate_bwd(t["dout"], t["h"], t["k"], t["v"], wf, *st, P=P, dh=dh, dk=dk, dv=dv, dw_partial=part)
+        elif op == "grad_w_reduce":
+            nbytes = P * wl.d * 4 + wl.d * 4
+
+            def launch():
+                ecm.grad_w_reduce(part, dweight_fused=wf)
+        else:  # gate_fwd on T=16384 d=4096, or gate_fwd_2k on T=8192 d=2048
+            nbytes = wl.T * (8 * wl.d + 16)
+
+            def launch():
+                ecm.gate_fwd(t["h"], t["k"], t["v"], wf, EPS, out=out, stats=st)
+    for _ in range(args.warmup):
+        launch()
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    ev[0].record(stream)
+    for i in range(args.steps):
+        launch()
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    times = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    peak, kind = load_peaks()
+    med = statistics.median(times)
+    gbs = nbytes / (med / 1e3) / 1e9
+    print(json.dumps({"only": op, "median_ms": med, "min_ms": min(times), "bytes": nbytes, "GBps": gbs,
+                      "frac": gbs / peak, "peak": peak, "peak_kind": kind, "launches": args.steps}), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end timing (profiling runs)")
+    ap.add_argument("--only", choices=["hash_gather", "hash_gather_small", "gate_fwd", "gate_fwd_2k", "gate_bwd",
+                                       "grad_w_reduce"],
+                    help="time one kernel alone on its workload (consecutive launches, L2 not flushed)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, local, world = dist_env()
+    if args.impl == "reference":
+        return main_reference(args, rank, world)
+    return main_native(args, rank, local, world)
+
+
+def main_reference(args, rank, world):
+    """The CPU oracle on the host cores; rank 0 alone works and prints under torchrun."""
+    if rank != 0:
+        return 0
+    from synth import workloads as W
+
+    hw = W.hash_gather_64k(num_seqs=SEQS, seq_len=SEQ_LEN)
+    gate_tokens = 1024
+    gate_host = gate_host_sample_synth(gate_tokens)
+    table_host = np.zeros((hw.spec.total_rows, hw.row_dim), dtype=np.uint16)
+    T_all = hw.T
+    step_s = []
+    n = 1
+    for i in range(args.warmup + args.steps):
+        t_hash, t_gate, n = oracle_step_seconds(hw, table_host, gate_host, gate_tokens, T_all)
+        if i >= args.warmup:
+            step_s.append(t_hash + t_gate * (4 * MICRO_T / gate_tokens))
+    mean_s = sum(step_s) / len(step_s)
+    value = T_all / mean_s
+    sample = (f"per step: hash+gather of all {T_all} tokens, gate fwd+bwd of {gate_tokens} of the "
+              f"{4 * MICRO_T} gate tokens (scaled x{4 * MICRO_T // gate_tokens})")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_s * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "tokens_per_step": T_all, "parallelism": "replicas"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": n, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main_native(args, rank, local, world):
+    import torch
+    import torch.distributed as dist
+
+    import engram_conditional_memory_gb300 as ecm
+
+    if not torch.cuda.is_available():
+        print("bench.py: no CUDA device", file=sys.stderr)
+        return 2
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl", device_id=device)
+    ecm.load_library()
+    if args.only:
+        return main_only(args, device)
+    wk = make_workload(device)
+    props = torch.cuda.get_device_properties(device)
+    gpu_id = f"GPU-{props.uuid}" if getattr(props, "uuid", None) else str(local)
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    elapsed, per, launches, w0, w1 = time_device(wk, args.steps, args.warmup, device)
+    clocks = sampler.stop(w0, w1)
+    max_ms = aggregate_max(elapsed, device)
+    T_all = wk["hw"].T
+    value = world * T_all * args.steps / (max_ms / 1e3)
+    peak, peak_kind = load_peaks()
+    ab = algorithmic_bytes(wk["P"])
+    ops = {}
+    for name, times in per.items():
+        avg = sum(times) / len(times)
+        gbs = ab[name] / (avg / 1e3) / 1e9
+        ops[name] = {"avg_ms": avg, "launches": len(times), "bytes": ab[name], "GBps": gbs, "frac": gbs / peak}
+    step_bytes = ab["hash_gather"] + ab["fuse_weight"] + 4 * (ab["gate_fwd"] + ab["gate_bwd"] + ab["grad_w_reduce"])
+    dom = "gate_bwd"
+    roof = {"bound": "hbm", "kernel": dom, "achieved": ops[dom]["GBps"], "peak": peak, "unit": "GB/s",
+            "frac": ops[dom]["GBps"] / peak, "peak_kind": f"{peak_kind} (copy bandwidth)",
+            "traffic": load_traffic(dom), "algorithmic_bytes_per_launch": ab[dom]}
+    e2e = None
+    if not args.no_e2e:
+        e_ms, h2d, d2h = time_e2e(wk, args.steps, args.warmup, device)
+        e_max = aggregate_max(e_ms, device)
+        e2e = {"value": world * T_all * args.steps / (e_max / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        gate_tokens = 16384
+        v, n, step_s = cpu_baseline(wk["hw"], gate_host_sample(wk, gate_tokens), gate_tokens)
+        cpu = {"value": v, "unit": "tokens/s", "cores": n, "kind": "oracle",
+               "sample": f"hash+gather of all {T_all} tokens and gate fwd+bwd of {gate_tokens} of the "
+                         f"{4 * MICRO_T} gate tokens (micro-batch 0, scaled x4); est. {step_s:.2f} s/step"}
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": max_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "math": "fp32 accumulate; uint64 hash",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "tokens_per_step": T_all, "global_batch": world * T_all,
+                       "seq_len": SEQ_LEN, "parallelism": f"replicas x{world}",
+                       "l2": "no flush: per-step working set 6.1 GB >> 129 MB L2"},
+            "hbm_gbs": step_bytes / (max_ms / args.steps / 1e3) / 1e9,
+            "hash_gather_rows_per_s": 16 * T_all / (ops["hash_gather"]["avg_ms"] / 1e3),
+            "roofline": roof, "ops": ops, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
