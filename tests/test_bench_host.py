@@ -1,0 +1,66 @@
+"""Host-side logic of bench.py on CPU: the multi-rank path (2 gloo ranks, replicas only), the
+reference arm's rank handling, and the algorithmic byte counts the roofline divides by."""
+import io
+import os
+import socket
+import sys
+from contextlib import redirect_stdout
+
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    import torch.distributed as dist
+
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        elapsed = 100.0 + 25.0 * rank  # rank 1 is the slow one
+        slowest = bench.aggregate_max(elapsed)
+        bench.barrier()
+        q.put((rank, slowest, bench.dist_env()))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_ranks_take_the_max_time():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert [g[1] for g in got] == [125.0, 125.0]
+    assert got[0][2] == (0, 0, 2) and got[1][2] == (1, 1, 2)
+
+
+def test_reference_arm_other_ranks_exit_quietly(monkeypatch):
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--impl", "reference", "--gpus", "2", "--steps", "1",
+                                      "--warmup", "3"])
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        assert bench.main() == 0
+    assert buf.getvalue() == ""
+
+
+def test_algorithmic_bytes_per_unit():
+    ab = bench.algorithmic_bytes(P=1024)
+    T_all, d = bench.SEQS * bench.SEQ_LEN, bench.D
+    assert ab["hash_gather"] == T_all * 4104          # 4 + 4 + 16 rows x 128 B read + written
+    assert ab["gate_fwd"] == bench.MICRO_T * 32784    # 8d + 16 at d = 4096
+    assert ab["gate_bwd"] == bench.MICRO_T * 57360 + 1024 * d * 4  # 14d + 16, plus the partial rows
