@@ -17,6 +17,7 @@ from .binding import (  # noqa: F401
     device_status,
     fuse_weight,
     gate_bwd,
+    gate_bwd_reduce_noalloc,
     gate_bwd_num_partials,
     gate_fwd,
     grad_w_reduce,

@@ -79,6 +79,8 @@ def load_library():
             "engram_gate_bwd": (st, [_p, _p, _p, _p, _c.c_int, _p, _p, _p, _p, _p, _i64, _i32, _p, _p, _p, _p,
                                      _i32, _p]),
             "engram_grad_w_reduce": (st, [_p, _i32, _i32, _p, _p, _p, _p, _p, _p]),
+            "engram_gate_bwd_reduce_noalloc": (st, [_p, _p, _p, _p, _c.c_int, _p, _p, _p, _p, _p, _i64, _i32, _p, _p,
+                                                    _p, _p, _p, _p, _p, _p, _p]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)
@@ -217,6 +219,31 @@ def grad_w_reduce(dw_partial, dweight_fused=None, w_h=None, w_k=None, grad_w_h=N
                                     _ptr(grad_w_h), _ptr(grad_w_k), _stream(stream)),
            "engram_grad_w_reduce")
     return dweight_fused
+
+
+def gate_bwd_reduce_noalloc(dout, h, k, v, w_fused, alpha, rstd_h, rstd_k, dot, dh=None, dk=None, dv=None,
+                            dweight_fused=None, w_h=None, w_k=None, grad_w_h=None, grad_w_k=None,
+                            want_dweight: bool = True, stream=None):
+    """Backward + weight-gradient reduction without a caller-provided partials buffer.
+
+    For callers that cannot allocate device memory: the partials live in the library's
+    own fixed 16 MiB device array (see include/engram.h).  Returns (dh, dk, dv, dweight_fused).
+    """
+    lib = load_library()
+    for name, t in (("dout", dout), ("h", h), ("k", k), ("v", v)):
+        _need(t, name, h.dtype)
+    T, d = h.shape
+    dh = torch.empty_like(h) if dh is None else _need(dh, "dh", h.dtype)
+    dk = torch.empty_like(k) if dk is None else _need(dk, "dk", h.dtype)
+    dv = torch.empty_like(v) if dv is None else _need(dv, "dv", h.dtype)
+    if dweight_fused is None and want_dweight:
+        dweight_fused = torch.empty(d, dtype=torch.float32, device=h.device)
+    _check(lib.engram_gate_bwd_reduce_noalloc(_ptr(dout), _ptr(h), _ptr(k), _ptr(v), _DTYPES[h.dtype], _ptr(w_fused),
+                                              _ptr(alpha), _ptr(rstd_h), _ptr(rstd_k), _ptr(dot), T, d, _ptr(dh),
+                                              _ptr(dk), _ptr(dv), _ptr(dweight_fused), _ptr(w_h), _ptr(w_k),
+                                              _ptr(grad_w_h), _ptr(grad_w_k), _stream(stream)),
+           "engram_gate_bwd_reduce_noalloc")
+    return dh, dk, dv, dweight_fused
 
 
 # ----------------------------------------------------------------------------- A0-A2

@@ -16,6 +16,7 @@
 // tokens in ascending order, so every partial -- and the reduced gradient -- is
 // bitwise identical on any GPU and for any grid size.
 #include <algorithm>
+#include <mutex>
 
 #include "gate_pipeline.cuh"
 
@@ -388,4 +389,120 @@ extern "C" engram_status engram_grad_w_reduce(const float *dw_partial, int32_t P
         reinterpret_cast<const float4 *>(w_h), reinterpret_cast<const float4 *>(w_k),
         reinterpret_cast<float4 *>(grad_w_h), reinterpret_cast<float4 *>(grad_w_k));
     return check_launch("engram_grad_w_reduce");
+}
+
+// ---------------------------------------------------------------------------------------------
+// Allocation-free backward + reduction for callers that cannot allocate device memory.
+//
+// Some callers cannot call cudaMalloc: an embedding that has handed the whole device to a
+// framework's caching allocator or to a fixed arena reserved at start-up (a raw allocation
+// would fail or fragment it), or a serving loop that forbids allocation after start-up
+// (cudaMalloc / cudaFree may synchronise the device and stall every stream).  For them,
+// engram_gate_bwd_reduce_noalloc keeps the [P, d] weight-gradient partials in the library's
+// own file-scope device array instead of a caller buffer.
+// ---------------------------------------------------------------------------------------------
+
+// 16 MiB of partials, held on every device that loads the library until the process exits.
+static __device__ __align__(256) float g_noalloc_partials[ENGRAM_NOALLOC_SCRATCH_BYTES / sizeof(float)];
+
+namespace {
+
+constexpr int kNoallocMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+float *g_noalloc_addr[kNoallocMaxDevices];
+
+// The array's device address on `device` (which must be current).  The symbol's host-side
+// name is only a stand-in; the address is looked up once per device and cached.
+engram_status noalloc_scratch(int device, float **out) {
+    if (device < 0 || device >= kNoallocMaxDevices)
+        return fail(ENGRAM_ERR_CUDA, "engram_gate_bwd_reduce_noalloc: device %d out of range", device);
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_addr[device]) {
+        float *p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void **>(&p), g_noalloc_partials);
+        if (e != cudaSuccess || !p)
+            return fail(ENGRAM_ERR_CUDA, "engram_gate_bwd_reduce_noalloc: scratch address on device %d: %s", device,
+                        cudaGetErrorString(e));
+        g_noalloc_addr[device] = p;
+    }
+    *out = g_noalloc_addr[device];
+    return ENGRAM_OK;
+}
+
+}  // namespace
+
+extern "C" engram_status engram_gate_bwd_reduce_noalloc(
+    const void *dout, const void *h, const void *k, const void *v, engram_dtype dtype, const float *w_fused,
+    const float *alpha, const float *rstd_h, const float *rstd_k, const float *dot, int64_t T, int32_t d,
+    void *dh, void *dk, void *dv, float *dweight_fused, const float *w_h, const float *w_k, float *grad_w_h,
+    float *grad_w_k, engram_stream_t stream) {
+    const char *fn = "engram_gate_bwd_reduce_noalloc";
+    const int nw = (w_h != nullptr) + (w_k != nullptr) + (grad_w_h != nullptr) + (grad_w_k != nullptr);
+    if (nw != 0 && nw != 4) return fail(ENGRAM_ERR_NULL, "%s: w_h, w_k, grad_w_h, grad_w_k must be given together", fn);
+    if (!dweight_fused && nw == 0) return fail(ENGRAM_ERR_NULL, "%s: no weight-gradient output", fn);
+    if (!w_fused || (T > 0 && (!dout || !h || !k || !v || !alpha || !rstd_h || !rstd_k || !dot || !dh || !dk || !dv)))
+        return fail(ENGRAM_ERR_NULL, "%s: NULL pointer", fn);
+    const int es = dtype_size(dtype);
+    if (es == 0) return fail(ENGRAM_ERR_DTYPE, "%s: dtype %d", fn, (int)dtype);
+    if (T < 0 || d <= 0) return fail(ENGRAM_ERR_SHAPE, "%s: T = %lld, d = %d", fn, (long long)T, d);
+    const int64_t row_bytes = static_cast<int64_t>(d) * es;
+    if (row_bytes % 16 != 0) return fail(ENGRAM_ERR_ALIGN, "%s: row of %lld bytes", fn, (long long)row_bytes);
+    if (row_bytes > ENGRAM_MAX_ROW_BYTES)
+        return fail(ENGRAM_ERR_SHAPE, "%s: row of %lld bytes exceeds %d", fn, (long long)row_bytes,
+                    ENGRAM_MAX_ROW_BYTES);
+    int32_t P = 0;
+    engram_status st = engram_gate_bwd_num_partials(T, d, &P);
+    if (st != ENGRAM_OK) return st;
+    const int64_t need = static_cast<int64_t>(P) * d * static_cast<int64_t>(sizeof(float));
+    if (need > static_cast<int64_t>(ENGRAM_NOALLOC_SCRATCH_BYTES))
+        return fail(ENGRAM_ERR_SHAPE,
+                    "%s: T = %lld, d = %d needs %lld bytes of weight-gradient partials (P = %d), more than the %u "
+                    "bytes this entry point holds; call engram_gate_bwd with a caller-allocated buffer instead",
+                    fn, (long long)T, d, (long long)need, P, (unsigned)ENGRAM_NOALLOC_SCRATCH_BYTES);
+    const void *ptrs[] = {dout, h, k, v, w_fused, dh, dk, dv, dweight_fused, w_h, w_k, grad_w_h, grad_w_k};
+    for (const void *q : ptrs)
+        if (q && !aligned16(q)) return fail(ENGRAM_ERR_ALIGN, "%s: tensor not 16-byte aligned", fn);
+    DeviceInfo dev;
+    if ((st = current_device(&dev)) != ENGRAM_OK) return st;
+    const void *dptrs[] = {dout, h, k, v, w_fused, alpha, rstd_h, rstd_k, dot, dh, dk, dv, dweight_fused, w_h, w_k,
+                           grad_w_h, grad_w_k};
+    for (const void *q : dptrs)
+        if ((st = check_device_ptr(q, dev.device, fn)) != ENGRAM_OK) return st;
+    float *scratch = nullptr;
+    if ((st = noalloc_scratch(dev.device, &scratch)) != ENGRAM_OK) return st;
+
+    // Backward into the scratch partials.  Every one of the P rows is written (rows of
+    // partials without tokens are written as zeros), so nothing needs clearing first.
+    GateBwdParams p{};
+    p.g = static_cast<const uint8_t *>(dout);
+    p.h = static_cast<const uint8_t *>(h);
+    p.k = static_cast<const uint8_t *>(k);
+    p.v = static_cast<const uint8_t *>(v);
+    p.w = w_fused;
+    p.alpha = alpha;
+    p.rstd_h = rstd_h;
+    p.rstd_k = rstd_k;
+    p.dot = dot;
+    p.dh = static_cast<uint8_t *>(dh);
+    p.dk = static_cast<uint8_t *>(dk);
+    p.dv = static_cast<uint8_t *>(dv);
+    p.dw_partial = scratch;
+    p.status = dev.status_word;
+    p.T = T;
+    p.P = P;
+    p.chunk = ceil_div(T, P);
+    p.d = d;
+    p.row_bytes = static_cast<uint32_t>(row_bytes);
+    p.scale = 1.0f / sqrtf(static_cast<float>(d));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    st = dtype == ENGRAM_F32 ? dispatch_bwd<float>(p, dev, s) : dispatch_bwd<__nv_bfloat16>(p, dev, s);
+    if (st != ENGRAM_OK) return st;
+
+    // Ordered reduction of the partials, on the same stream.
+    const int d4 = d / 4;
+    grad_w_reduce_kernel<<<(d4 + kCV - 1) / kCV, kRG * kCV, 0, s>>>(
+        reinterpret_cast<const float4 *>(scratch), P, d4, reinterpret_cast<float4 *>(dweight_fused),
+        reinterpret_cast<const float4 *>(w_h), reinterpret_cast<const float4 *>(w_k),
+        reinterpret_cast<float4 *>(grad_w_h), reinterpret_cast<float4 *>(grad_w_k));
+    return check_launch(fn);
 }

@@ -260,6 +260,50 @@ engram_status engram_grad_w_reduce(const float *dw_partial, int32_t P, int32_t d
                                    const float *w_h, const float *w_k, float *grad_w_h, float *grad_w_k,
                                    engram_stream_t stream);
 
+/* ------------------------------------------------------------------------- */
+/* Allocation-free backward + reduction                                       */
+/* ------------------------------------------------------------------------- */
+
+/* Bytes of weight-gradient partials that engram_gate_bwd_reduce_noalloc holds (16 MiB). */
+#define ENGRAM_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/*
+ * The paper has no counterpart to this entry point; it exists for callers that
+ * cannot allocate device memory.  Examples: a program that has handed all device
+ * memory to a framework's caching allocator or to an arena reserved at start-up,
+ * where a raw cudaMalloc would fail or fragment that pool; and a serving loop that
+ * forbids allocation once it runs, because cudaMalloc and cudaFree can synchronise
+ * the device and stall every stream.
+ *
+ * It computes what engram_gate_bwd followed by engram_grad_w_reduce compute, with
+ * P = engram_gate_bwd_num_partials(T, d): the same dh, dk, dv, dweight_fused
+ * (nullable) and, when the four weight pointers are given, the same
+ * accumulation into grad_w_h and grad_w_k.  Arguments have the meaning, layout
+ * and ownership they have there; the caller still provides every input and
+ * output.  Only the [P, d] fp32 partials move: they live in one array of
+ * ENGRAM_NOALLOC_SCRATCH_BYTES that the library keeps on each device that
+ * loads it, until the process exits.  The call allocates and frees nothing.
+ *
+ * Limits and rules:
+ *   - Sizes whose partials need more than ENGRAM_NOALLOC_SCRATCH_BYTES
+ *     (P * d * 4 bytes; e.g. T >= 9361 at d = 7168) are rejected with
+ *     ENGRAM_ERR_SHAPE and a message; use engram_gate_bwd with a buffer then.
+ *   - The first call on a device looks up the array's device address on that
+ *     device (cudaGetSymbolAddress) and caches it: make that first call, with the
+ *     device current, before any stream capture on it.
+ *   - All calls share the one array, which keeps whatever the last call left
+ *     there.  Each call overwrites every partial row it reads, so nothing has to
+ *     be cleared between calls, but calls that overlap on the GPU (other
+ *     streams, other host threads) race on it: order them on one stream or
+ *     synchronise between them.
+ */
+engram_status engram_gate_bwd_reduce_noalloc(const void *dout, const void *h, const void *k, const void *v,
+                                             engram_dtype dtype, const float *w_fused, const float *alpha,
+                                             const float *rstd_h, const float *rstd_k, const float *dot,
+                                             int64_t T, int32_t d, void *dh, void *dk, void *dv,
+                                             float *dweight_fused, const float *w_h, const float *w_k,
+                                             float *grad_w_h, float *grad_w_k, engram_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
