@@ -212,11 +212,16 @@ __global__ void __launch_bounds__((NCW + 1) * 32) gate_bwd_kernel(const __grid_c
     }
 }
 
-// S = sum_p partial[p]: column slices of 4*kCV columns per CTA; row group r of the
-// CTA sums partials [r*R, min(P, (r+1)*R)) in ascending order, R = ceil(P/kRG), then
-// row group 0 adds the kRG group sums in ascending order.  The order depends on P only.
-constexpr int kRG = 16;
-constexpr int kCV = 16;
+// S = sum_p partial[p]: column slices of 4*kCV columns per CTA.  Row group r of the CTA
+// sums the contiguous partials [r*R, min(P, (r+1)*R)), R = ceil(P / kRG), in ascending
+// order, with all its loads issued before the adds (16-byte loads, 64 contiguous bytes per
+// row segment); then one thread per column adds the kRG group sums in ascending order.
+// The order depends on P only.  With kRG = 64 every partial row of a d = 4096, P = 1024
+// reduction is in flight at once: the kernel is bound by one round trip to L2, where the
+// backward has just written the partials.
+constexpr int kRG = 64;
+constexpr int kCV = 4;
+constexpr int kReduceBatch = 8;
 
 __global__ void __launch_bounds__(kRG *kCV)
     grad_w_reduce_kernel(const float4 *__restrict__ part, int32_t P, int32_t d4, float4 *__restrict__ dweight,
@@ -231,13 +236,19 @@ __global__ void __launch_bounds__(kRG *kCV)
     const int p1 = p0 + rows < P ? p0 + rows : P;
     float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
     if (col < d4) {
-#pragma unroll 4
-        for (int q = p0; q < p1; ++q) {
-            const float4 x = __ldg(part + static_cast<size_t>(q) * d4 + col);
-            s.x += x.x;
-            s.y += x.y;
-            s.z += x.z;
-            s.w += x.w;
+        for (int q0 = p0; q0 < p1; q0 += kReduceBatch) {
+            float4 x[kReduceBatch];
+#pragma unroll
+            for (int b = 0; b < kReduceBatch; ++b)
+                if (q0 + b < p1) x[b] = __ldg(part + static_cast<size_t>(q0 + b) * d4 + col);
+#pragma unroll
+            for (int b = 0; b < kReduceBatch; ++b)
+                if (q0 + b < p1) {
+                    s.x += x[b].x;
+                    s.y += x[b].y;
+                    s.z += x[b].z;
+                    s.w += x[b].w;
+                }
         }
     }
     sums[r][cv] = s;

@@ -11,23 +11,27 @@
 //   h = XOR_{j<n} (uint64) id'(t - j) * M[table][j]  (mod 2^64),  idx = h mod p[table],
 //   id'(q) = pad id 0 for q before the start of t's sequence.
 //
-// Kernel layout: a CTA owns a tile of kTile consecutive tokens at a time.
-//   1. the compressed ids of the tile plus its (max_order - 1)-token look-back
-//      window and every token's sequence start go to shared memory (coalesced);
-//   2. the tile's kTile x tables hashes are computed, one per thread, into a
-//      shared table of row numbers (and the optional index output);
-//   3. the tile's rows are gathered with 16-byte loads -- 8 consecutive threads
-//      per 128-byte row, so each row is read as whole 32-byte sectors -- and
-//      written as one contiguous block (the tile's e_t rows are adjacent).
+// Kernel layout: a persistent CTA walks tiles of kTile consecutive tokens, software-pipelined
+// so that the next tile's hashing overlaps the current tile's row loads:
+//   1. the compressed ids of the tile plus its (max_order - 1)-token look-back window and
+//      every token's sequence start (a binary search in the sequence offsets, which are
+//      staged in shared memory once per CTA when they fit) go to shared memory;
+//   2. the tile's kTile x tables hashes are computed, one per thread, into a shared table
+//      of row numbers (and the optional index output);
+//   3. the tile's rows are gathered with 16-byte loads -- 8 consecutive threads per 128-byte
+//      row, so each row is read as whole 32-byte sectors -- and written as one contiguous
+//      block (the tile's e_t rows are adjacent).
+// Steps 1-2 of tile i+1 run while the loads of step 3 of tile i are in flight.
 #include <algorithm>
 
 #include "engram_internal.cuh"
 
 namespace engram {
 
-constexpr int kTile = 32;           // tokens per tile
-constexpr int kHashThreads = 256;   // threads per CTA
-constexpr int kBatch = 16;          // 16-byte vectors in flight per thread
+constexpr int kTile = 32;            // tokens per tile
+constexpr int kHashThreads = 256;    // threads per CTA
+constexpr int kBatch = 16;           // 16-byte vectors in flight per thread
+constexpr int kSmemSeqs = 4096;      // sequence offsets staged in shared memory up to this count
 
 struct HashGatherParams {
     const int32_t *ids;
@@ -51,113 +55,167 @@ struct HashGatherParams {
     uint64_t mult[ENGRAM_MAX_TABLES][ENGRAM_MAX_ORDER];
 };
 
-// Start of the sequence holding token t: the last o_s <= t (upper bound search),
-// clamped into [0, t] so that malformed offsets can never send a read out of range.
+// Start of the sequence holding token t: the last o_s <= t (upper bound search over
+// offs[0..num_seqs]), clamped into [0, t] so that malformed offsets can never send a read
+// out of range.
 __device__ __forceinline__ int64_t sequence_start(const int64_t *offs, int32_t num_seqs, int64_t t) {
     int lo = 0, hi = num_seqs;  // invariant: answer in [lo, hi)
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if (__ldg(offs + mid) <= t) lo = mid;
+        if (offs[mid] <= t) lo = mid;
         else hi = mid;
     }
-    int64_t s = __ldg(offs + lo);
+    int64_t s = offs[lo];
     if (s > t) s = t;
     if (s < 0) s = 0;
     return s;
 }
 
-__global__ void __launch_bounds__(kHashThreads) hash_gather_kernel(const __grid_constant__ HashGatherParams p) {
-    __shared__ int32_t cid[kTile + ENGRAM_MAX_ORDER];
-    __shared__ int64_t start[kTile];
-    __shared__ int64_t rows[kTile][ENGRAM_MAX_TABLES];
+struct TileState {
+    int32_t cid[2][kTile + ENGRAM_MAX_ORDER];
+    int64_t start[2][kTile];
+    int64_t rows[2][kTile][ENGRAM_MAX_TABLES];
+};
+
+// Step 1 for tile `tile` into buffer `b`: compressed ids of positions t0 - back .. t0 + ntok - 1
+// and the sequence start of each token.
+__device__ __forceinline__ void tile_ids(const HashGatherParams &p, const int64_t *offs, TileState &st, int b,
+                                         int64_t tile, int tid) {
+    const int back = p.max_order - 1;
+    const int64_t t0 = tile * kTile;
+    const int ntok = static_cast<int>(p.T - t0 < kTile ? p.T - t0 : kTile);
+    if (tid < ntok + back) {
+        const int64_t q = t0 - back + tid;
+        int32_t id = 0;
+        if (q >= 0) {
+            const int32_t raw = __ldg(p.ids + q);
+            if (raw < 0 || raw >= p.vocab) {
+                report(p.status, p.err_word, ENGRAM_DEVERR_TOKEN_ID);
+            } else {
+                id = p.cmap ? __ldg(p.cmap + raw) : raw;
+                if (id < 0 || id >= p.vocab_c) {
+                    report(p.status, p.err_word, ENGRAM_DEVERR_COMPRESSED);
+                    id = 0;
+                }
+            }
+        }
+        st.cid[b][tid] = id;
+    }
+    if (tid >= kHashThreads - kTile) {
+        const int i = tid - (kHashThreads - kTile);
+        if (i < ntok) st.start[b][i] = sequence_start(offs, p.num_seqs, t0 + i);
+    }
+}
+
+// Step 2 for tile `tile` from buffer `b`: one hash per (token, table).
+__device__ __forceinline__ void tile_hash(const HashGatherParams &p, TileState &st, int b, int64_t tile, int tid) {
+    const int back = p.max_order - 1;
+    const int64_t t0 = tile * kTile;
+    const int ntok = static_cast<int>(p.T - t0 < kTile ? p.T - t0 : kTile);
+    for (int e = tid; e < ntok * p.tables; e += kHashThreads) {
+        const int i = e / p.tables;
+        const int tb = e - i * p.tables;
+        const int64_t t = t0 + i;
+        const int n = p.order[tb];
+        uint64_t h = 0;
+        for (int j = 0; j < n; ++j) {
+            const uint64_t id = (t - j >= st.start[b][i]) ? static_cast<uint64_t>(st.cid[b][i + back - j]) : 0ull;
+            h ^= id * p.mult[tb][j];
+        }
+        const uint64_t idx = h % p.prime[tb];
+        st.rows[b][i][tb] = p.row_off[tb] + static_cast<int64_t>(idx);
+        if (p.out_idx) p.out_idx[t * p.tables + tb] = static_cast<int32_t>(idx);
+    }
+}
+
+__global__ void __launch_bounds__(kHashThreads, 2) hash_gather_kernel(const __grid_constant__ HashGatherParams p) {
+    extern __shared__ __align__(16) int64_t smem_offs[];  // [num_seqs + 1] when staged
+    __shared__ TileState st;
 
     const int tid = threadIdx.x;
-    const int back = p.max_order - 1;
     const int64_t ntiles = (p.T + kTile - 1) / kTile;
-    const uint32_t vpr = p.row_bytes / 16;                  // 16-byte vectors per table row
+    const uint32_t vpr = p.row_bytes / 16;                       // 16-byte vectors per table row
     const uint32_t vpt = vpr * static_cast<uint32_t>(p.tables);  // per token (one e_t row)
 
-    // One CTA checks the sequence boundaries: 0 = o_0 <= o_1 <= ... <= o_S = T.
+    // Sequence offsets: staged in shared memory when they fit; one CTA also checks that
+    // 0 = o_0 <= o_1 <= ... <= o_S = T.
+    const bool staged = p.num_seqs + 1 <= kSmemSeqs;
+    const int64_t *offs = p.seq_offsets;
+    if (staged) {
+        for (int s = tid; s <= p.num_seqs; s += kHashThreads) smem_offs[s] = p.seq_offsets[s];
+        offs = smem_offs;
+    }
+    __syncthreads();
     if (blockIdx.x == 0) {
         for (int s = tid; s <= p.num_seqs; s += kHashThreads) {
-            const int64_t o = p.seq_offsets[s];
+            const int64_t o = offs[s];
             bool bad = (s == 0 && o != 0) || (s == p.num_seqs && o != p.T) || o < 0 || o > p.T;
-            if (s > 0 && p.seq_offsets[s - 1] > o) bad = true;
+            if (s > 0 && offs[s - 1] > o) bad = true;
             if (bad) report(p.status, p.err_word, ENGRAM_DEVERR_SEQ_OFFSETS);
         }
     }
 
-    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    int64_t tile = blockIdx.x;
+    int b = 0;
+    if (tile < ntiles) {
+        tile_ids(p, offs, st, 0, tile, tid);
+        __syncthreads();
+        tile_hash(p, st, 0, tile, tid);
+    }
+    __syncthreads();
+
+    for (; tile < ntiles; tile += gridDim.x, b ^= 1) {
         const int64_t t0 = tile * kTile;
         const int ntok = static_cast<int>(p.T - t0 < kTile ? p.T - t0 : kTile);
+        const int64_t next = tile + gridDim.x;
+        const uint32_t total = p.out_rows ? static_cast<uint32_t>(ntok) * vpt : 0u;
+        uint8_t *dst = p.out_rows + static_cast<size_t>(t0) * vpt * 16;
 
-        // 1. compressed ids of positions t0 - back .. t0 + ntok - 1, and sequence starts
-        if (tid < ntok + back) {
-            const int64_t q = t0 - back + tid;
-            int32_t id = 0;
-            if (q >= 0) {
-                const int32_t raw = __ldg(p.ids + q);
-                if (raw < 0 || raw >= p.vocab) {
-                    report(p.status, p.err_word, ENGRAM_DEVERR_TOKEN_ID);
-                } else {
-                    id = p.cmap ? __ldg(p.cmap + raw) : raw;
-                    if (id < 0 || id >= p.vocab_c) {
-                        report(p.status, p.err_word, ENGRAM_DEVERR_COMPRESSED);
-                        id = 0;
-                    }
-                }
-            }
-            cid[tid] = id;
-        }
-        if (tid >= kHashThreads - kTile) {
-            const int i = tid - (kHashThreads - kTile);
-            if (i < ntok) start[i] = sequence_start(p.seq_offsets, p.num_seqs, t0 + i);
-        }
-        __syncthreads();
-
-        // 2. one hash per (token, table)
-        for (int e = tid; e < ntok * p.tables; e += kHashThreads) {
-            const int i = e / p.tables;
-            const int tb = e - i * p.tables;
-            const int64_t t = t0 + i;
-            const int n = p.order[tb];
-            uint64_t h = 0;
-            for (int j = 0; j < n; ++j) {
-                const uint64_t id = (t - j >= start[i]) ? static_cast<uint64_t>(cid[i + back - j]) : 0ull;
-                h ^= id * p.mult[tb][j];
-            }
-            const uint64_t idx = h % p.prime[tb];
-            rows[i][tb] = p.row_off[tb] + static_cast<int64_t>(idx);
-            if (p.out_idx) p.out_idx[t * p.tables + tb] = static_cast<int32_t>(idx);
-        }
-        __syncthreads();
-
-        // 3. gather: vector e of the tile is (token e / vpt, table (e % vpt) / vpr, piece e % vpr)
-        if (p.out_rows) {
-            const uint32_t total = static_cast<uint32_t>(ntok) * vpt;
-            uint8_t *dst = p.out_rows + static_cast<size_t>(t0) * vpt * 16;
-            for (uint32_t base = 0; base < total; base += kHashThreads * kBatch) {
-                uint4 buf[kBatch];
+        // 3a. first batch of this tile's row loads (vector e = token e / vpt, table (e % vpt) / vpr)
+        uint4 buf[kBatch];
 #pragma unroll
-                for (int b = 0; b < kBatch; ++b) {
-                    const uint32_t e = base + b * kHashThreads + tid;
-                    if (e < total) {
-                        const uint32_t i = e / vpt;
-                        const uint32_t r = e - i * vpt;
-                        const uint32_t tb = r / vpr;
-                        const uint32_t piece = r - tb * vpr;
-                        const uint8_t *src = p.table + static_cast<size_t>(rows[i][tb]) * p.row_bytes + piece * 16;
-                        buf[b] = __ldg(reinterpret_cast<const uint4 *>(src));
-                    }
-                }
-#pragma unroll
-                for (int b = 0; b < kBatch; ++b) {
-                    const uint32_t e = base + b * kHashThreads + tid;
-                    if (e < total) st_global_v4(dst + static_cast<size_t>(e) * 16, buf[b]);
-                }
+        for (int k = 0; k < kBatch; ++k) {
+            const uint32_t e = k * kHashThreads + tid;
+            if (e < total) {
+                const uint32_t i = e / vpt;
+                const uint32_t r = e - i * vpt;
+                const uint32_t tb = r / vpr;
+                const uint32_t piece = r - tb * vpr;
+                const uint8_t *src = p.table + static_cast<size_t>(st.rows[b][i][tb]) * p.row_bytes + piece * 16;
+                buf[k] = __ldg(reinterpret_cast<const uint4 *>(src));
             }
         }
-        __syncthreads();  // the tile's shared state is rewritten next iteration
+        // 1-2 of the next tile while those loads are in flight
+        if (next < ntiles) tile_ids(p, offs, st, b ^ 1, next, tid);
+        __syncthreads();
+        if (next < ntiles) tile_hash(p, st, b ^ 1, next, tid);
+        // 3b. store the first batch, then any further batches of this tile
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+            const uint32_t e = k * kHashThreads + tid;
+            if (e < total) st_global_v4(dst + static_cast<size_t>(e) * 16, buf[k]);
+        }
+        for (uint32_t base = kHashThreads * kBatch; base < total; base += kHashThreads * kBatch) {
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                const uint32_t e = base + k * kHashThreads + tid;
+                if (e < total) {
+                    const uint32_t i = e / vpt;
+                    const uint32_t r = e - i * vpt;
+                    const uint32_t tb = r / vpr;
+                    const uint32_t piece = r - tb * vpr;
+                    const uint8_t *src =
+                        p.table + static_cast<size_t>(st.rows[b][i][tb]) * p.row_bytes + piece * 16;
+                    buf[k] = __ldg(reinterpret_cast<const uint4 *>(src));
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                const uint32_t e = base + k * kHashThreads + tid;
+                if (e < total) st_global_v4(dst + static_cast<size_t>(e) * 16, buf[k]);
+            }
+        }
+        __syncthreads();  // buffer b is rewritten two tiles from now; b ^ 1 is complete
     }
 }
 
@@ -236,10 +294,16 @@ extern "C" engram_status engram_hash_gather(const engram_hash_spec *spec, const 
     p.max_order = max_order;
     p.row_bytes = static_cast<uint32_t>(row_bytes);
 
+    // Persistent grid: as many CTAs as fit on the device at once (>= 1: T = 0 still checks the offsets).
+    const int dyn = a->num_seqs + 1 <= kSmemSeqs ? (a->num_seqs + 1) * static_cast<int>(sizeof(int64_t)) : 0;
+    if ((st = set_smem(reinterpret_cast<const void *>(hash_gather_kernel), dyn)) != ENGRAM_OK) return st;
+    int per_sm = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, hash_gather_kernel, kHashThreads, dyn);
+    if (e != cudaSuccess) return fail(ENGRAM_ERR_CUDA, "engram_hash_gather occupancy: %s", cudaGetErrorString(e));
     const int64_t ntiles = (a->T + kTile - 1) / kTile;
-    int64_t grid = static_cast<int64_t>(dev.num_sms) * 4;
+    int64_t grid = static_cast<int64_t>(dev.num_sms) * std::max(per_sm, 1);
     if (grid > ntiles) grid = ntiles;
-    grid = cap_grid(grid);  // >= 1: T = 0 still validates the sequence offsets
-    hash_gather_kernel<<<static_cast<unsigned>(grid), kHashThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
+    grid = cap_grid(grid);
+    hash_gather_kernel<<<static_cast<unsigned>(grid), kHashThreads, dyn, reinterpret_cast<cudaStream_t>(stream)>>>(p);
     return check_launch("engram_hash_gather");
 }
