@@ -240,7 +240,55 @@ def run_step(wk, mark=None):
 
 # ----------------------------------------------------------------------------- device timing
 
+def capture_step(wk, device):
+    """The step as one CUDA graph (14 kernel nodes).  The library's per-device set-up and each
+    kernel's shared-memory attribute are done by an eager step first; device-pointer checks are
+    off during capture (they were made by that eager step on the same buffers)."""
+    import torch
+
+    import engram_conditional_memory_gb300 as ecm
+
+    side = torch.cuda.Stream(device)
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        run_step(wk)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    prev = ecm.set_validation(0)
+    try:
+        with torch.cuda.graph(graph):
+            run_step(wk)
+    finally:
+        ecm.set_validation(prev)
+    return graph
+
+
+def time_graph(graph, steps, warmup, device):
+    """Device time of `steps` replays of the step graph (CUDA events on the replaying stream)."""
+    import torch
+
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    barrier(device)
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    wall0 = _dt.datetime.now()
+    start.record(stream)
+    for _ in range(steps):
+        graph.replay()
+    end.record(stream)
+    torch.cuda.synchronize()
+    wall1 = _dt.datetime.now()
+    barrier(device)
+    return start.elapsed_time(end), 14 * steps, wall0, wall1
+
+
 def time_device(wk, steps, warmup, device):
+    """Eager steps with a CUDA event between consecutive launches: the per-kernel durations."""
     import torch
 
     stream = torch.cuda.current_stream()
@@ -278,23 +326,53 @@ def time_device(wk, steps, warmup, device):
 
 
 def time_e2e(wk, steps, warmup, device):
-    """Same step through the public API, with each step's inputs copied from pinned host memory first
-    and the step's result (the accumulated fp32 weight gradients) read back to the host."""
+    """Same step through the public API, with each step's inputs copied from pinned host memory and
+    the step's result (the accumulated fp32 weight gradients) read back to the host.
+
+    Copies run on a copy stream into the four micro-batch buffers, so micro-batch i+1 crosses the
+    host link while micro-batch i computes; events order every reuse of a buffer or of the ids.
+    """
     import torch
 
-    stream = torch.cuda.current_stream()
+    import engram_conditional_memory_gb300 as ecm
+
+    comp = torch.cuda.current_stream()
+    copy = torch.cuda.Stream(device)
+    names = ("h", "k", "v", "dout")
     host_ids = wk["ids"].cpu().pin_memory()
-    host_mb = [{n: m[n].cpu().pin_memory() for n in ("h", "k", "v", "dout")} for m in wk["mb"]]
+    host_mb = [{n: m[n].cpu().pin_memory() for n in names} for m in wk["mb"]]
     res_h = torch.empty(2 * D, dtype=torch.float32, pin_memory=True)
     h2d = host_ids.numel() * 4 + sum(t.numel() * t.element_size() for m in host_mb for t in m.values())
     d2h = res_h.numel() * 4
+    ready = [torch.cuda.Event() for _ in range(4)]   # micro-batch i's inputs are on the device
+    done = [torch.cuda.Event() for _ in range(4)]    # compute has finished reading micro-batch i
+    ids_ready, hash_done = torch.cuda.Event(), torch.cuda.Event()
+    hw = wk["hw"]
 
     def step():
-        wk["ids"].copy_(host_ids, non_blocking=True)
-        for m, hm in zip(wk["mb"], host_mb):
-            for n, t in hm.items():
-                m[n].copy_(t, non_blocking=True)
-        run_step(wk)
+        with torch.cuda.stream(copy):
+            copy.wait_event(hash_done)  # the previous step's hash has read the id buffer
+            wk["ids"].copy_(host_ids, non_blocking=True)
+            ids_ready.record(copy)
+            for i, m in enumerate(wk["mb"]):
+                copy.wait_event(done[i])  # the previous step has finished with this buffer
+                for n in names:
+                    m[n].copy_(host_mb[i][n], non_blocking=True)
+                ready[i].record(copy)
+        comp.wait_event(ids_ready)
+        ecm.hash_gather(wk["spec"], wk["ids"], wk["offs"], wk["table"], wk["cmap"], hw.vocab, hw.vocab_c,
+                        out_rows=wk["rows"])
+        hash_done.record(comp)
+        ecm.fuse_weight(wk["w_h"], wk["w_k"], out=wk["w_fused"])
+        for i, m in enumerate(wk["mb"]):
+            comp.wait_event(ready[i])
+            st = wk["stats"][i]
+            ecm.gate_fwd(m["h"], m["k"], m["v"], wk["w_fused"], EPS, out=wk["out"][i], stats=st)
+            ecm.gate_bwd(m["dout"], m["h"], m["k"], m["v"], wk["w_fused"], *st, P=wk["P"], dh=wk["dh"][i],
+                         dk=wk["dk"][i], dv=wk["dv"][i], dw_partial=wk["part"][i])
+            done[i].record(comp)
+            ecm.grad_w_reduce(wk["part"][i], dweight_fused=wk["dweight"], w_h=wk["w_h"], w_k=wk["w_k"],
+                              grad_w_h=wk["grad_w_h"], grad_w_k=wk["grad_w_k"])
         res_h[:D].copy_(wk["grad_w_h"], non_blocking=True)
         res_h[D:].copy_(wk["grad_w_k"], non_blocking=True)
 
@@ -304,10 +382,11 @@ def time_e2e(wk, steps, warmup, device):
     barrier(device)
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
-    start.record(stream)
+    start.record(comp)
+    copy.wait_event(start)  # no copy of the timed region starts before the start event
     for _ in range(steps):
         step()
-    end.record(stream)
+    end.record(comp)
     torch.cuda.synchronize()
     barrier(device)
     return start.elapsed_time(end), h2d, d2h
@@ -522,11 +601,13 @@ def main_native(args, rank, local, world):
     wk = make_workload(device)
     props = torch.cuda.get_device_properties(device)
     gpu_id = f"GPU-{props.uuid}" if getattr(props, "uuid", None) else str(local)
+    graph = capture_step(wk, device)
     sampler = ClockSampler(gpu_id)
     sampler.start()
-    elapsed, per, launches, w0, w1 = time_device(wk, args.steps, args.warmup, device)
+    elapsed, launches, w0, w1 = time_graph(graph, args.steps, args.warmup, device)
     clocks = sampler.stop(w0, w1)
     max_ms = aggregate_max(elapsed, device)
+    _, per, _, _, _ = time_device(wk, args.steps, args.warmup, device)
     T_all = wk["hw"].T
     value = world * T_all * args.steps / (max_ms / 1e3)
     peak, peak_kind = load_peaks()
@@ -562,7 +643,9 @@ def main_native(args, rank, local, world):
             "data": "synthetic",
             "config": {"workload": WORKLOAD, "tokens_per_step": T_all, "global_batch": world * T_all,
                        "seq_len": SEQ_LEN, "parallelism": f"replicas x{world}",
-                       "l2": "no flush: per-step working set 6.1 GB >> 129 MB L2"},
+                       "l2": "no flush: per-step working set 6.1 GB >> 129 MB L2",
+                       "timing": "value: CUDA-graph replays of the 14-launch step; ops/roofline: eager steps "
+                                 "with an event between launches; e2e: eager calls with host copies"},
             "hbm_gbs": step_bytes / (max_ms / args.steps / 1e3) / 1e9,
             "hash_gather_rows_per_s": 16 * T_all / (ops["hash_gather"]["avg_ms"] / 1e3),
             "roofline": roof, "ops": ops, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,

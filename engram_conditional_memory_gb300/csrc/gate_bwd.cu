@@ -281,15 +281,14 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 template <typename T, int NCW>
 engram_status launch_bwd(const GateBwdParams &p, const DeviceInfo &dev, cudaStream_t stream) {
     const auto kern = gate_bwd_kernel<T, NCW>;
-    const PipelineShape shape = pick_pipeline(4 * static_cast<int>(p.row_bytes), NCW, dev.smem_optin);
+    const PipelineShape shape = pick_bwd_pipeline(4 * static_cast<int>(p.row_bytes), NCW, dev.smem_optin);
     if (shape.stages == 0) return fail(ENGRAM_ERR_SHAPE, "engram_gate_bwd: row of %u bytes does not fit", p.row_bytes);
     engram_status st = set_smem(reinterpret_cast<const void *>(kern), shape.smem_bytes);
     if (st != ENGRAM_OK) return st;
     GateBwdParams q = p;
     q.stages = shape.stages;
-    int64_t grid = static_cast<int64_t>(dev.num_sms) * shape.blocks_per_sm;
-    if (grid > p.P) grid = p.P;
-    grid = cap_grid(grid);
+    // One CTA per partial (the kernel's partial loop then runs once per CTA).
+    const int64_t grid = cap_grid(p.P);
     kern<<<static_cast<unsigned>(grid), (NCW + 1) * 32, shape.smem_bytes, stream>>>(q);
     return check_launch("engram_gate_bwd");
 }

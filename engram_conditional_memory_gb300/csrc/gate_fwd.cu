@@ -189,7 +189,7 @@ namespace {
 template <typename T, int NCW>
 engram_status launch_fwd(const GateFwdParams &p, const DeviceInfo &dev, cudaStream_t stream) {
     const auto kern = gate_fwd_kernel<T, NCW>;
-    const PipelineShape shape = pick_pipeline(3 * static_cast<int>(p.row_bytes), NCW, dev.smem_optin);
+    const PipelineShape shape = pick_fwd_pipeline(3 * static_cast<int>(p.row_bytes), NCW, dev.smem_optin);
     if (shape.stages == 0) return fail(ENGRAM_ERR_SHAPE, "engram_gate_fwd: row of %u bytes does not fit", p.row_bytes);
     engram_status st = set_smem(reinterpret_cast<const void *>(kern), shape.smem_bytes);
     if (st != ENGRAM_OK) return st;

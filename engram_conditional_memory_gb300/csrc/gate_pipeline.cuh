@@ -30,7 +30,7 @@ inline int pick_consumer_warps(int row_bytes) {
 
 struct PipelineShape {
     int stages;         // S
-    int blocks_per_sm;  // resident CTAs per SM the grid is sized for
+    int blocks_per_sm;  // resident CTAs per SM a persistent grid is sized for (0: one CTA per work unit)
     int smem_bytes;     // dynamic shared memory per CTA
 };
 
@@ -39,24 +39,29 @@ inline int pipeline_smem_bytes(int stages, int stage_bytes, int ncw) {
     return stages * stage_bytes + 2 * stages * 8 + 2 * ncw * 4 * 4;
 }
 
-// Picks S and the CTAs per SM so that about `budget` bytes per SM are in flight:
-// at least 2 stages, preferring >= 2 CTAs per SM (one CTA's reduction bubble is
-// hidden by the other's copies) and >= 3 stages when they fit.
-inline PipelineShape pick_pipeline(int stage_bytes, int ncw, int smem_optin) {
-    const int budget = 200 * 1024;
-    PipelineShape best{0, 0, 0};
-    const int pref[][2] = {{4, 3}, {3, 3}, {2, 3}, {2, 2}, {1, 3}, {1, 2}};  // (blocks per SM, min stages)
-    for (const auto &bp : pref) {
-        const int b = bp[0];
-        int s = budget / (b * stage_bytes);
-        if (s > 8) s = 8;
-        if (s < bp[1]) continue;
+// Forward: two stages per CTA and as many resident CTAs per SM (1..4) as keep about
+// 160 KB of rows in flight per SM.  Measured on GB300 (T = 8192..131072, d = 2048..7168):
+// more CTAs with fewer stages beat fewer, deeper CTAs, because each CTA works on one token
+// at a time and its reduction bubble is hidden by the other CTAs' copies.
+inline PipelineShape pick_fwd_pipeline(int stage_bytes, int ncw, int smem_optin) {
+    const int smem = pipeline_smem_bytes(2, stage_bytes, ncw);
+    if (smem > smem_optin) return {0, 0, 0};
+    int b = (160 * 1024 + stage_bytes) / (2 * stage_bytes);  // round(160 KB / (2 stages))
+    b = b < 1 ? 1 : (b > 4 ? 4 : b);
+    while (b > 1 && b * smem > 227 * 1024) --b;
+    return {2, b, smem};
+}
+
+// Backward: three stages per CTA (two when three do not fit) and one CTA per weight-gradient
+// partial, left to the hardware scheduler: CTAs start as others finish, which balances the
+// P equal chunks over the SMs far better than a persistent grid (P is fixed by T alone, so
+// it is rarely a multiple of the resident CTA count).
+inline PipelineShape pick_bwd_pipeline(int stage_bytes, int ncw, int smem_optin) {
+    for (int s = 3; s >= 2; --s) {
         const int smem = pipeline_smem_bytes(s, stage_bytes, ncw);
-        if (smem > smem_optin) continue;
-        best = {s, b, smem};
-        break;
+        if (smem <= smem_optin) return {s, 0, smem};
     }
-    return best;
+    return {0, 0, 0};
 }
 
 // Sum over a named barrier's threads of a "failed" flag: every consumer thread
