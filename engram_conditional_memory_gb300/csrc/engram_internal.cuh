@@ -117,6 +117,13 @@ __device__ __forceinline__ void bulk_load(void *dst_smem, const void *src_gmem, 
         : "memory");
 }
 
+// The same bulk copy with the default L2 policy.
+__device__ __forceinline__ void bulk_load_plain(void *dst_smem, const void *src_gmem, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(smem_addr(dst_smem)), "l"(src_gmem), "r"(bytes), "r"(smem_addr(bar))
+                 : "memory");
+}
+
 // Named barrier over `count` threads (a multiple of 32) of this CTA.
 __device__ __forceinline__ void named_sync(uint32_t id, uint32_t count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");

@@ -159,7 +159,8 @@ typedef struct {
     int32_t vocab_c;             /* compressed vocabulary size (>= 1; = vocab when compress_map is NULL) */
     const void *table;           /* [table_rows, row_dim] concatenated E_{n,k}, table order */
     int64_t table_rows;          /* >= sum(primes) */
-    int32_t row_dim;             /* elements per row; row_dim * element size a multiple of 16 bytes */
+    int32_t row_dim;             /* elements per row; row_dim * element size a multiple of 16 bytes,
+                                    and tables * row bytes (one token's e_t row) at most 64 KB */
     engram_dtype dtype;          /* element type of table and out_rows (bit copies either way) */
     int32_t *out_indices;        /* [T, tables] local index idx_{n,k}(t) in [0, p); NULL = not written */
     void *out_rows;              /* [T, tables * row_dim] e_t = concatenated rows; NULL = not written */

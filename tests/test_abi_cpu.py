@@ -102,7 +102,11 @@ def test_hash_gather_host_rejections(lib):
     args.table_rows = 36
     args.row_dim = 4  # 8-byte rows
     assert lib.engram_hash_gather(ctypes.byref(spec), ctypes.byref(args), None) == 4
+    args.row_dim = 16384  # 4 tables x 32 KB rows = a 128 KB e_t row, over the 64 KB the kernel takes
+    args.table_rows = 1 << 20
+    assert lib.engram_hash_gather(ctypes.byref(spec), ctypes.byref(args), None) == 2
     args.row_dim = 8
+    args.table_rows = 36
     bad = _HashSpec(2, 2, 2, 2, mult.ctypes.data, primes.ctypes.data)  # stride 2 < max order 3
     assert lib.engram_hash_gather(ctypes.byref(bad), ctypes.byref(args), None) == 2
     many = _HashSpec(2, 2, 17, 3, mult.ctypes.data, primes.ctypes.data)  # 34 tables > 32

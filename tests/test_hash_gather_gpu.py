@@ -122,6 +122,7 @@ def test_ragged_sequences_and_tails(lengths):
     (2, 2, 2, 16, "f32"),
     (3, 1, 1, 100, "f32"),     # one table, 400-byte rows
     (2, 3, 5, 24, "bf16"),     # 15 tables, 48-byte rows
+    (2, 1, 32, 1024, "bf16"),  # the largest e_t row, 32 x 2 KB = 64 KB: one token per tile
 ])
 def test_table_shapes(min_order, num_orders, heads, row_dim, dtype):
     T = 777
