@@ -54,8 +54,12 @@ def _load():
             lib.eo_gate_bwd.argtypes = [_p, _p, _p, _p, ctypes.c_int, _p, _p, _i64, _i32, _f64, _i64, _i64,
                                         _p, _p, _p, _p, _p]
             lib.eo_grad_w_reduce.argtypes = [_p, _i32, _i32, _p, _p, _p, _p, _p]
+            lib.eo_gate_hc_fwd.argtypes = [_p, _p, ctypes.c_int, _p, _p, _i64, _i32, _i32, _f64, _f64, _i64, _i64,
+                                           _p, _p, _p, _p, _p]
+            lib.eo_gate_hc_bwd.argtypes = [_p, _p, _p, ctypes.c_int, _p, _p, _i64, _i32, _i32, _f64, _f64, _i64,
+                                           _i64, _p, _p, _p, _p]
             for f in ("eo_hash_indices", "eo_gather_rows", "eo_fuse_weight", "eo_gate_fwd", "eo_gate_bwd",
-                      "eo_grad_w_reduce"):
+                      "eo_grad_w_reduce", "eo_gate_hc_fwd", "eo_gate_hc_bwd"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -178,3 +182,45 @@ def grad_w_reduce(partial, w_h=None, w_k=None) -> dict:
     if wh is not None:
         out["inc_h"], out["inc_k"] = inc_h, inc_k
     return out
+
+
+def gate_hc_fwd(x, kv, w_h, w_k, eps: float, clamp: float, t_begin: int = 0, t_end: int | None = None) -> dict:
+    """Multi-branch gate: x [T, hc, d], kv [T, hc+1, d], w_h/w_k [hc, d] -> fp64 out [n, hc, d] and
+    gate, rstd_x, rstd_k, dot [n, hc]."""
+    lib = _load()
+    x, kv = np.ascontiguousarray(x), np.ascontiguousarray(kv)
+    dt = _dtype_code(x)
+    assert _dtype_code(kv) == dt
+    T, hc, d = x.shape
+    assert kv.shape == (T, hc + 1, d)
+    wh = np.ascontiguousarray(w_h, dtype=np.float32).reshape(hc, d)
+    wk = np.ascontiguousarray(w_k, dtype=np.float32).reshape(hc, d)
+    t_end = T if t_end is None else t_end
+    n = t_end - t_begin
+    res = {name: np.zeros((n, hc), dtype=np.float64) for name in ("gate", "rstd_x", "rstd_k", "dot")}
+    res["out"] = np.zeros((n, hc, d), dtype=np.float64)
+    rc = lib.eo_gate_hc_fwd(_ptr(x), _ptr(kv), dt, _ptr(wh), _ptr(wk), T, hc, d, float(eps), float(clamp), t_begin,
+                            t_end, _ptr(res["out"]), _ptr(res["gate"]), _ptr(res["rstd_x"]), _ptr(res["rstd_k"]),
+                            _ptr(res["dot"]))
+    _check(rc, "gate_hc_fwd")
+    return res
+
+
+def gate_hc_bwd(dout, x, kv, w_h, w_k, eps: float, clamp: float, t_begin: int = 0, t_end: int | None = None) -> dict:
+    """fp64 dx [n, hc, d], dkv [n, hc+1, d], dweight and dweight_abs [hc, d]."""
+    lib = _load()
+    g, x, kv = (np.ascontiguousarray(a) for a in (dout, x, kv))
+    dt = _dtype_code(x)
+    assert _dtype_code(g) == dt and _dtype_code(kv) == dt
+    T, hc, d = x.shape
+    wh = np.ascontiguousarray(w_h, dtype=np.float32).reshape(hc, d)
+    wk = np.ascontiguousarray(w_k, dtype=np.float32).reshape(hc, d)
+    t_end = T if t_end is None else t_end
+    n = t_end - t_begin
+    res = {"dx": np.zeros((n, hc, d), dtype=np.float64), "dkv": np.zeros((n, hc + 1, d), dtype=np.float64),
+           "dweight": np.zeros((hc, d), dtype=np.float64), "dweight_abs": np.zeros((hc, d), dtype=np.float64)}
+    rc = lib.eo_gate_hc_bwd(_ptr(g), _ptr(x), _ptr(kv), dt, _ptr(wh), _ptr(wk), T, hc, d, float(eps), float(clamp),
+                            t_begin, t_end, _ptr(res["dx"]), _ptr(res["dkv"]), _ptr(res["dweight"]),
+                            _ptr(res["dweight_abs"]))
+    _check(rc, "gate_hc_bwd")
+    return res

@@ -26,6 +26,10 @@
  *   [T13]  TileLang tutorial, ch. 13 "elementwise / norm / RoPE", sec. 5.4:
  *          the RMS mean divides by the true length d.
  *
+ *   NEXT-1 (the multi-branch production gate of the TileKernels release): T34 sec. 2.1
+ *   (x [T, hc, d], kv [T, hc+1, d], the signed-sqrt + clamp activation, out = x + alpha v),
+ *   sec. 3.2 (forward) and sec. 4.2 (backward, including the zero-gradient clamp branch).
+ *
  * Readings where the pages leave a step open (each one is also listed in the
  * design notes):
  *   - the exact hash: h = XOR_{j<n} (uint64) id'[t-j] * M[n,k,j] (mod 2^64),
@@ -40,7 +44,8 @@
  * primes, sequence resets, brute-force invariants; gathered rows against a table
  * whose rows encode their own index; the gate against torch's rms_norm +
  * sigmoid in fp64, the k = 0 and h = +-k closed forms and the fused/unfused
- * identity; the backward against torch autograd and central finite differences;
+ * identity; the backward against torch autograd and central finite differences
+ * (both forms of the gate, the multi-branch one also through its clamp branch);
  * the reduction against constant partials with closed-form sums.
  */
 #include <math.h>
@@ -345,6 +350,137 @@ int eo_grad_w_reduce(const float *partial, int32_t P, int32_t d,
         if (w_h && w_k && inc_h && inc_k) {
             inc_h[i] = acc * (double)w_k[i];
             inc_k[i] = acc * (double)w_h[i];
+        }
+    }
+    return EO_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* NEXT-1: the multi-branch gate of the TileKernels release  [T34 sec. 2.1, 3.2, 4.2] */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * hc branches share one value.  x is [T, hc, d]; kv is [T, hc+1, d] with rows 0..hc-1 the
+ * branch keys and row hc the shared value; w_h and w_k are [hc, d].  For branch h of token t,
+ * with s = 1/sqrt(d) and the clamp value c:
+ *     rstd_x = 1/sqrt(sum_i x^2/d + eps),   rstd_k likewise over the key row,
+ *     dot    = sum_i x_i (w_h,i w_k,i) k_i,
+ *     z      = s * rstd_x * rstd_k * dot            (the paper form's pre-activation)
+ *     gate   = sigmoid(sign(z) * sqrt(max(|z|, c)))  (sign(0) taken as +, as copysign(., +0) gives)
+ *     out    = x + gate * v.
+ * Here too the paper form is evaluated: both RMSNorms with their own weights, then the scaled
+ * inner product; the saved dot is the fused-weight sum.  Outputs are indexed from t_begin.
+ */
+static void eo_branch_forward(const void *x, const void *kv, int dtype, const float *w_h, const float *w_k,
+                              int64_t t, int32_t hc, int32_t h, int32_t d, double eps, double clamp,
+                              double *rx, double *rk, double *dot, double *z_out, double *gate)
+{
+    const int64_t xb = (t * hc + h) * (int64_t)d;
+    const int64_t kb = (t * (hc + 1) + h) * (int64_t)d;
+    const float *wh = w_h + (int64_t)h * d, *wk = w_k + (int64_t)h * d;
+    double sx = 0.0, sk = 0.0;
+    for (int32_t i = 0; i < d; ++i) {
+        const double a = eo_load(x, dtype, xb + i), b = eo_load(kv, dtype, kb + i);
+        sx += a * a;
+        sk += b * b;
+    }
+    *rx = 1.0 / sqrt(sx / (double)d + eps);
+    *rk = 1.0 / sqrt(sk / (double)d + eps);
+    double acc = 0.0, dt = 0.0;
+    for (int32_t i = 0; i < d; ++i) {
+        const double a = eo_load(x, dtype, xb + i), b = eo_load(kv, dtype, kb + i);
+        acc += (a * (*rx) * (double)wh[i]) * (b * (*rk) * (double)wk[i]);
+        dt += a * ((double)wh[i] * (double)wk[i]) * b;
+    }
+    const double z = acc / sqrt((double)d);
+    const double m = fabs(z) > clamp ? fabs(z) : clamp;
+    const double sgn = signbit(z) ? -1.0 : 1.0;
+    *dot = dt;
+    *z_out = z;
+    *gate = eo_sigmoid(sgn * sqrt(m));
+}
+
+int eo_gate_hc_fwd(const void *x, const void *kv, int dtype, const float *w_h, const float *w_k,
+                   int64_t T, int32_t hc, int32_t d, double eps, double clamp, int64_t t_begin, int64_t t_end,
+                   double *out, double *gate, double *rstd_x, double *rstd_k, double *dot)
+{
+    if (!x || !kv || !w_h || !w_k || !out || !gate || !rstd_x || !rstd_k || !dot)
+        return EO_ERR_ARG;
+    if ((dtype != EO_F32 && dtype != EO_BF16) || hc < 1 || d <= 0 || t_begin < 0 || t_end > T || t_begin > t_end)
+        return EO_ERR_ARG;
+    for (int64_t t = t_begin; t < t_end; ++t) {
+        const int64_t vb = (t * (hc + 1) + hc) * (int64_t)d;
+        for (int32_t h = 0; h < hc; ++h) {
+            double rx, rk, dt, z, g;
+            eo_branch_forward(x, kv, dtype, w_h, w_k, t, hc, h, d, eps, clamp, &rx, &rk, &dt, &z, &g);
+            const int64_t o = (t - t_begin) * hc + h;
+            gate[o] = g;
+            rstd_x[o] = rx;
+            rstd_k[o] = rk;
+            dot[o] = dt;
+            const int64_t xb = (t * hc + h) * (int64_t)d;
+            for (int32_t i = 0; i < d; ++i)
+                out[o * d + i] = eo_load(x, dtype, xb + i) + g * eo_load(kv, dtype, vb + i);
+        }
+    }
+    return EO_OK;
+}
+
+/*
+ * Backward of eo_gate_hc_fwd for tokens [t_begin, t_end), g = dL/dout [T, hc, d]:
+ *     dgate_h = sum_i g_h,i v_i
+ *     c_h     = 0 when |z_h| < c (the clamp holds the activation constant there), else
+ *               dgate_h * gate_h (1 - gate_h) / (2 sqrt|z_h|) * s * rstd_x * rstd_k   (= dL/d dot_h)
+ *     dx_h    = g_h + c_h (w_h (*) w_k * k_h - dot_h rstd_x^2 x_h / d)
+ *     dk_h    = c_h (w_h (*) w_k * x_h - dot_h rstd_k^2 k_h / d)
+ *     dv      = sum_h gate_h g_h
+ *     dweight[h, i] = sum_t c_h x_h,i k_h,i   ([hc, d], token order), dweight_abs the sum of |terms|.
+ * dx is [n, hc, d], dkv is [n, hc+1, d] (row hc = dv).
+ */
+int eo_gate_hc_bwd(const void *g, const void *x, const void *kv, int dtype, const float *w_h, const float *w_k,
+                   int64_t T, int32_t hc, int32_t d, double eps, double clamp, int64_t t_begin, int64_t t_end,
+                   double *dx, double *dkv, double *dweight, double *dweight_abs)
+{
+    if (!g || !x || !kv || !w_h || !w_k || !dx || !dkv || !dweight)
+        return EO_ERR_ARG;
+    if ((dtype != EO_F32 && dtype != EO_BF16) || hc < 1 || d <= 0 || t_begin < 0 || t_end > T || t_begin > t_end)
+        return EO_ERR_ARG;
+    const double s = 1.0 / sqrt((double)d);
+    for (int64_t i = 0; i < (int64_t)hc * d; ++i) {
+        dweight[i] = 0.0;
+        if (dweight_abs)
+            dweight_abs[i] = 0.0;
+    }
+    for (int64_t t = t_begin; t < t_end; ++t) {
+        const int64_t vb = (t * (hc + 1) + hc) * (int64_t)d;
+        const int64_t o = t - t_begin;
+        double *dv = dkv + (o * (hc + 1) + hc) * (int64_t)d;
+        for (int32_t i = 0; i < d; ++i)
+            dv[i] = 0.0;
+        for (int32_t h = 0; h < hc; ++h) {
+            double rx, rk, dt, z, gt;
+            eo_branch_forward(x, kv, dtype, w_h, w_k, t, hc, h, d, eps, clamp, &rx, &rk, &dt, &z, &gt);
+            const int64_t xb = (t * hc + h) * (int64_t)d;
+            const int64_t kb = (t * (hc + 1) + h) * (int64_t)d;
+            double dgate = 0.0;
+            for (int32_t i = 0; i < d; ++i)
+                dgate += eo_load(g, dtype, xb + i) * eo_load(kv, dtype, vb + i);
+            double c = 0.0;
+            if (!(fabs(z) < clamp))
+                c = dgate * gt * (1.0 - gt) / (2.0 * sqrt(fabs(z))) * s * rx * rk;
+            double *dxr = dx + (o * hc + h) * (int64_t)d;
+            double *dkr = dkv + (o * (hc + 1) + h) * (int64_t)d;
+            for (int32_t i = 0; i < d; ++i) {
+                const double xi = eo_load(x, dtype, xb + i), ki = eo_load(kv, dtype, kb + i);
+                const double gi = eo_load(g, dtype, xb + i);
+                const double wi = (double)w_h[(int64_t)h * d + i] * (double)w_k[(int64_t)h * d + i];
+                dxr[i] = gi + c * (wi * ki - dt * rx * rx * xi / (double)d);
+                dkr[i] = c * (wi * xi - dt * rk * rk * ki / (double)d);
+                dv[i] += gt * gi;
+                dweight[(int64_t)h * d + i] += c * xi * ki;
+                if (dweight_abs)
+                    dweight_abs[(int64_t)h * d + i] += fabs(c * xi * ki);
+            }
         }
     }
     return EO_OK;

@@ -175,3 +175,35 @@ def gate_host_inputs(w: GateWorkload):
     out["w_h"] = G.normal(w.seed + 7001, w.d, 1.0, 0.1).astype(np.float32)
     out["w_k"] = G.normal(w.seed + 7002, w.d, 1.0, 0.1).astype(np.float32)
     return out
+
+
+@dataclass
+class GateHcWorkload:
+    """The multi-branch gate: hc branches per token sharing one value row."""
+
+    name: str
+    T: int
+    hc: int
+    d: int
+    dtype: str
+    seed: int
+    eps: float = 1e-6
+    clamp: float = 1e-6
+
+
+def gate_hc_host_inputs(w: GateHcWorkload):
+    """x [T, hc, d], kv [T, hc+1, d], dout [T, hc, d] ~ N(0, 1); w_h, w_k [hc, d] ~ N(1, 0.1) fp32."""
+    out = {}
+    shapes = {"x": (w.T, w.hc, w.d), "kv": (w.T, w.hc + 1, w.d), "dout": (w.T, w.hc, w.d)}
+    for i, (name, shp) in enumerate(shapes.items()):
+        n = shp[0] * shp[1] * shp[2]
+        x = G.normal(w.seed + 3000 * (i + 1), n).reshape(shp)
+        out[name] = x.astype(np.float32) if w.dtype == "f32" else G.to_bf16_bits(x)
+    out["w_h"] = G.normal(w.seed + 9001, w.hc * w.d, 1.0, 0.1).astype(np.float32).reshape(w.hc, w.d)
+    out["w_k"] = G.normal(w.seed + 9002, w.hc * w.d, 1.0, 0.1).astype(np.float32).reshape(w.hc, w.d)
+    return out
+
+
+def gate_hc_4x4k(seed: int = 6) -> GateHcWorkload:
+    """The production shape: 4 branches, T = 8192 tokens, d = 4096, bf16."""
+    return GateHcWorkload(name="gate_hc4_T8192_d4096", T=8192, hc=4, d=4096, dtype="bf16", seed=seed * 101 + 13)

@@ -297,3 +297,79 @@ def test_grad_w_reduce_closed_forms():
     np.testing.assert_array_equal(r["inc_h"], P * np.arange(d) * wk.astype(np.float64))
     np.testing.assert_array_equal(r["inc_k"], P * np.arange(d) * wh.astype(np.float64))
     assert (oracle.grad_w_reduce(np.zeros((0, d), dtype=np.float32))["S"] == 0).all()
+
+
+# ----------------------------------------------------------------------------- the multi-branch gate
+
+def _torch_gate_hc(x, kv, wh, wk, eps, clamp):
+    T, hc, d = x.shape
+    k, v = kv[:, :hc], kv[:, hc]
+    nx = F.rms_norm(x, (d,), None, eps) * wh
+    nk = F.rms_norm(k, (d,), None, eps) * wk
+    z = (nx * nk).sum(-1) / math.sqrt(d)
+    s = torch.copysign(torch.sqrt(torch.clamp(z.abs(), min=clamp)), z)
+    gate = torch.sigmoid(s)
+    return x + gate[..., None] * v[:, None, :], gate
+
+
+@pytest.mark.parametrize("dtype,hc,d", [("f32", 4, 64), ("bf16", 4, 128), ("f32", 1, 96), ("bf16", 2, 256)])
+def test_gate_hc_matches_torch_forward_and_autograd(dtype, hc, d):
+    wl = W.GateHcWorkload(name="pin", T=12, hc=hc, d=d, dtype=dtype, seed=500 + hc * d)
+    x = W.gate_hc_host_inputs(wl)
+    t = {n: torch.from_numpy(_f64(x[n])).requires_grad_() for n in ("x", "kv")}
+    wh = torch.from_numpy(x["w_h"].astype(np.float64)).requires_grad_()
+    wk = torch.from_numpy(x["w_k"].astype(np.float64)).requires_grad_()
+    out, gate = _torch_gate_hc(t["x"], t["kv"], wh, wk, wl.eps, wl.clamp)
+    f = oracle.gate_hc_fwd(x["x"], x["kv"], x["w_h"], x["w_k"], wl.eps, wl.clamp)
+    np.testing.assert_allclose(f["gate"], gate.detach().numpy(), rtol=0, atol=1e-13)
+    np.testing.assert_allclose(f["out"], out.detach().numpy(), rtol=1e-12, atol=1e-13)
+    g = torch.from_numpy(_f64(x["dout"]))
+    (out * g).sum().backward()
+    b = oracle.gate_hc_bwd(x["dout"], x["x"], x["kv"], x["w_h"], x["w_k"], wl.eps, wl.clamp)
+    np.testing.assert_allclose(b["dx"], t["x"].grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(b["dkv"], t["kv"].grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(b["dweight"] * x["w_k"], wh.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(b["dweight"] * x["w_h"], wk.grad.numpy(), rtol=1e-10, atol=1e-12)
+
+
+def test_gate_hc_zero_key_hits_the_clamp():
+    # k = 0 gives z = 0, held at the clamp: gate = sigmoid(+sqrt(1e-6)) = sigmoid(0.001), and no gradient
+    # reaches x or k through the gate (dx = dout exactly, dk = 0); dv = sum_h gate * dout_h.
+    wl = W.GateHcWorkload(name="pin", T=6, hc=4, d=32, dtype="f32", seed=77)
+    x = W.gate_hc_host_inputs(wl)
+    kv = x["kv"].copy()
+    kv[:, :4] = 0.0
+    f = oracle.gate_hc_fwd(x["x"], kv, x["w_h"], x["w_k"], wl.eps, wl.clamp)
+    g0 = 1.0 / (1.0 + math.exp(-0.001))
+    assert np.allclose(f["gate"], g0, rtol=0, atol=1e-16)
+    np.testing.assert_allclose(f["out"], x["x"] + g0 * kv[:, 4][:, None, :].astype(np.float64), rtol=1e-15)
+    b = oracle.gate_hc_bwd(x["dout"], x["x"], kv, x["w_h"], x["w_k"], wl.eps, wl.clamp)
+    np.testing.assert_array_equal(b["dx"], x["dout"].astype(np.float64))
+    assert (b["dkv"][:, :4] == 0).all() and (b["dweight"] == 0).all()
+    np.testing.assert_allclose(b["dkv"][:, 4], g0 * x["dout"].astype(np.float64).sum(1), rtol=1e-14)
+
+
+def test_gate_hc_finite_differences():
+    wl = W.GateHcWorkload(name="pin", T=5, hc=4, d=48, dtype="f32", seed=91)
+    x = W.gate_hc_host_inputs(wl)
+    b = oracle.gate_hc_bwd(x["dout"], x["x"], x["kv"], x["w_h"], x["w_k"], wl.eps, wl.clamp)
+
+    def loss(xx):
+        f = oracle.gate_hc_fwd(xx["x"], xx["kv"], xx["w_h"], xx["w_k"], wl.eps, wl.clamp)
+        return float((f["out"] * x["dout"].astype(np.float64)).sum())
+
+    delta = 2.0 ** -12
+    checked = 0
+    for name, grad, idx in (("x", b["dx"], [(0, 0, 0), (3, 2, 17), (4, 3, 47)]),
+                            ("kv", b["dkv"], [(1, 0, 5), (2, 3, 30), (0, 4, 7), (4, 4, 40)])):
+        for ix in idx:
+            base = x[name][ix]
+            plus, minus = np.float32(base + delta), np.float32(base - delta)
+            if float(plus) - float(base) != delta or float(base) - float(minus) != delta:
+                continue
+            xp = dict(x); xp[name] = x[name].copy(); xp[name][ix] = plus
+            xm = dict(x); xm[name] = x[name].copy(); xm[name][ix] = minus
+            fd = (loss(xp) - loss(xm)) / (2 * delta)
+            assert abs(fd - grad[ix]) <= 1e-6 * max(1.0, abs(fd)), (name, ix)
+            checked += 1
+    assert checked >= 5
