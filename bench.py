@@ -487,6 +487,29 @@ def main_only(args, device):
 
         def launch():
             ecm.hash_gather(spec, ids, offs, table, cmap, hw.vocab, hw.vocab_c, out_rows=rows)
+    elif op.startswith("gate_hc"):
+        # the multi-branch gate at its production shape: T = 8192, hc = 4, d = 4096, bf16
+        wl = W.gate_hc_4x4k()
+        T, hc, d = wl.T, wl.hc, wl.d
+        x = SD.normal_tensor((T * hc, d), wl.seed + 1, 0.0, 1.0, "bf16", device).reshape(T, hc, d)
+        kv = SD.normal_tensor((T * (hc + 1), d), wl.seed + 2, 0.0, 1.0, "bf16", device).reshape(T, hc + 1, d)
+        g = SD.normal_tensor((T * hc, d), wl.seed + 3, 0.0, 1.0, "bf16", device).reshape(T, hc, d)
+        w_h = SD.normal_tensor((1, hc * d), wl.seed + 4, 1.0, 0.1, "f32", device).reshape(-1)
+        w_k = SD.normal_tensor((1, hc * d), wl.seed + 5, 1.0, 0.1, "f32", device).reshape(-1)
+        wf = ecm.fuse_weight(w_h, w_k).reshape(hc, d)
+        out, *st = ecm.gate_hc_fwd(x, kv, wf, wl.eps, wl.clamp)
+        P = ecm.gate_bwd_num_partials(T, hc * d)
+        dx, dkv, part = ecm.gate_hc_bwd(g, x, kv, wf, *st, clamp=wl.clamp, P=P)
+        if op == "gate_hc_bwd":
+            nbytes = T * ((5 * hc + 2) * 2 * d + 16 * hc) + P * hc * d * 4
+
+            def launch():
+                ecm.gate_hc_bwd(g, x, kv, wf, *st, clamp=wl.clamp, P=P, dx=dx, dkv=dkv, dw_partial=part)
+        else:
+            nbytes = T * ((3 * hc + 1) * 2 * d + 16 * hc)
+
+            def launch():
+                ecm.gate_hc_fwd(x, kv, wf, wl.eps, wl.clamp, out=out, stats=st)
     else:
         wl = {"gate_fwd_2k": W.gate_fwd_2k()}.get(op, W.gate_train_4k())
         t = SD.gate_device_inputs(wl, device)
@@ -538,7 +561,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end timing (profiling runs)")
     ap.add_argument("--only", choices=["hash_gather", "hash_gather_small", "gate_fwd", "gate_fwd_2k", "gate_bwd",
-                                       "grad_w_reduce"],
+                                       "grad_w_reduce", "gate_hc_fwd", "gate_hc_bwd"],
                     help="time one kernel alone on its workload (consecutive launches, L2 not flushed)")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -20,6 +20,8 @@ from .binding import (  # noqa: F401
     gate_bwd_reduce_noalloc,
     gate_bwd_num_partials,
     gate_fwd,
+    gate_hc_bwd,
+    gate_hc_fwd,
     grad_w_reduce,
     hash_gather,
     library_path,

@@ -79,6 +79,10 @@ def load_library():
             "engram_gate_bwd": (st, [_p, _p, _p, _p, _c.c_int, _p, _p, _p, _p, _p, _i64, _i32, _p, _p, _p, _p,
                                      _i32, _p]),
             "engram_grad_w_reduce": (st, [_p, _i32, _i32, _p, _p, _p, _p, _p, _p]),
+            "engram_gate_hc_fwd": (st, [_p, _p, _c.c_int, _p, _i64, _i32, _i32, _c.c_float, _c.c_float, _p, _p, _p,
+                                        _p, _p, _p]),
+            "engram_gate_hc_bwd": (st, [_p, _p, _p, _c.c_int, _p, _p, _p, _p, _p, _i64, _i32, _i32, _c.c_float, _p,
+                                        _p, _p, _i32, _p]),
             "engram_gate_bwd_reduce_noalloc": (st, [_p, _p, _p, _p, _c.c_int, _p, _p, _p, _p, _p, _i64, _i32, _p, _p,
                                                     _p, _p, _p, _p, _p, _p, _p]),
         }
@@ -244,6 +248,55 @@ def gate_bwd_reduce_noalloc(dout, h, k, v, w_fused, alpha, rstd_h, rstd_k, dot, 
                                               _ptr(grad_w_h), _ptr(grad_w_k), _stream(stream)),
            "engram_gate_bwd_reduce_noalloc")
     return dh, dk, dv, dweight_fused
+
+
+def gate_hc_fwd(x, kv, w_fused, eps: float = 1e-6, clamp: float = 1e-6, out=None, save_for_backward: bool = True,
+                inplace: bool = False, stats=None, stream=None):
+    """Multi-branch gate: x [T, hc, d], kv [T, hc+1, d], w_fused [hc, d] fp32.
+
+    Returns (out, gate, rstd_x, rstd_k, dot); with inplace, out is x itself (and nothing is saved).
+    """
+    lib = load_library()
+    _need(x, "x")
+    _need(kv, "kv", x.dtype)
+    _need(w_fused, "w_fused", torch.float32)
+    T, hc, d = x.shape
+    if inplace:
+        if save_for_backward:
+            raise ValueError("inplace overwrites x, which the backward reads; pass save_for_backward=False")
+        out = x
+    elif out is None:
+        out = torch.empty_like(x)
+    if save_for_backward:
+        if stats is None:
+            stats = tuple(torch.empty((T, hc), dtype=torch.float32, device=x.device) for _ in range(4))
+        gate, rx, rk, dot = stats
+    else:
+        gate = rx = rk = dot = None
+    _check(lib.engram_gate_hc_fwd(_ptr(x), _ptr(kv), _DTYPES[x.dtype], _ptr(w_fused), T, hc, d, float(eps),
+                                  float(clamp), _ptr(out), _ptr(gate), _ptr(rx), _ptr(rk), _ptr(dot), _stream(stream)),
+           "engram_gate_hc_fwd")
+    return out, gate, rx, rk, dot
+
+
+def gate_hc_bwd(dout, x, kv, w_fused, gate, rstd_x, rstd_k, dot, clamp: float = 1e-6, P: int | None = None, dx=None,
+                dkv=None, dw_partial=None, stream=None):
+    """Returns (dx [T, hc, d], dkv [T, hc+1, d], dw_partial [P, hc, d] fp32)."""
+    lib = load_library()
+    for name, t in (("dout", dout), ("x", x), ("kv", kv)):
+        _need(t, name, x.dtype)
+    T, hc, d = x.shape
+    if P is None:
+        P = gate_bwd_num_partials(T, hc * d) if dw_partial is None else dw_partial.shape[0]
+    dx = torch.empty_like(x) if dx is None else _need(dx, "dx", x.dtype)
+    dkv = torch.empty_like(kv) if dkv is None else _need(dkv, "dkv", x.dtype)
+    if dw_partial is None:
+        dw_partial = torch.empty((P, hc, d), dtype=torch.float32, device=x.device)
+    _check(lib.engram_gate_hc_bwd(_ptr(dout), _ptr(x), _ptr(kv), _DTYPES[x.dtype], _ptr(w_fused), _ptr(gate),
+                                  _ptr(rstd_x), _ptr(rstd_k), _ptr(dot), T, hc, d, float(clamp), _ptr(dx), _ptr(dkv),
+                                  _ptr(dw_partial), P, _stream(stream)),
+           "engram_gate_hc_bwd")
+    return dx, dkv, dw_partial
 
 
 # ----------------------------------------------------------------------------- A0-A2

@@ -1,0 +1,652 @@
+// The multi-branch gate of the TileKernels release (NEXT-1 of the hot path).
+//
+// TileLang tutorial, ch. 34 "TileKernels: Engram and mHC":
+//   sec. 2.1  hidden_states x [T, hc, d] and kv [T, hc+1, d] (rows 0..hc-1 the branch keys,
+//             row hc the value shared by the branches); per branch h
+//             alpha = sigmoid(sign(z) * sqrt(max(|z|, clamp))), z = dot * rstd_x * rstd_k / sqrt(d),
+//             dot = sum_i x_i (w_h (*) w_e)_i k_i, out = x + alpha * v;
+//   sec. 3.2  the forward kernel (the saved dot, alpha, rstd_x, rstd_k; in-place writing excludes
+//             saving for the backward);
+//   sec. 4.2  the backward: dL/dalpha = sum_i dout_i v_i; zero gradient where |z| < clamp;
+//             grad_x = dout + c (k w - x dot rstd_x^2 / d), grad_k = c (x w - k dot rstd_k^2 / d),
+//             and the per-block partials of dL/dw_fused = c x k.
+// The shared value's gradient is dv = sum_h alpha_h dout_h.
+//
+// Design: one stage holds a whole token -- x [hc, d] and kv [hc+1, d] (plus dout [hc, d] in the
+// backward), two or three 1-D bulk async copies -- so the shared value crosses HBM once per token
+// and its gradient sums the branches inside one thread: consumer thread c owns the 16-byte
+// vectors jj = c, c + 32*NCW, ... of every branch row.  The weight-gradient partials are laid out
+// [P, hc * d], so the plain weight fold and the ordered reduction serve this variant unchanged.
+#include <algorithm>
+
+#include "gate_pipeline.cuh"
+
+namespace engram {
+
+// Vectors per branch row a thread may own: HC * kVpb <= 4 keeps the fp32 weights and gradient
+// accumulators in registers.
+template <int HC>
+struct HcShape {
+    static constexpr int kVpb = 4 / HC;
+};
+
+struct GateHcFwdParams {
+    const uint8_t *x, *kv;
+    const float *w;  // [hc, d]
+    uint8_t *out;
+    float *gate, *rstd_x, *rstd_k, *dot;  // [T, hc]
+    uint32_t *status;
+    int64_t T;
+    int32_t d;
+    uint32_t row_bytes;
+    int32_t stages;
+    float eps, clamp, scale;
+};
+
+struct GateHcBwdParams {
+    const uint8_t *g, *x, *kv;
+    const float *w, *gate, *rstd_x, *rstd_k, *dot;
+    uint8_t *dx, *dkv;
+    float *dw_partial;  // [P, hc * d]
+    uint32_t *status;
+    int64_t T;
+    int64_t chunk;
+    int32_t P;
+    int32_t d;
+    uint32_t row_bytes;
+    int32_t stages;
+    float clamp, scale;
+};
+
+inline int hc_smem_bytes(int stages, int stage_bytes, int ncw, int hc) {
+    return stages * stage_bytes + 2 * stages * 8 + 2 * ncw * 4 * hc * 4;
+}
+
+__device__ __forceinline__ float hc_activation(float z, float clamp) {
+    const float r = sqrtf(fmaxf(fabsf(z), clamp));
+    return 1.0f / (1.0f + expf(-copysignf(r, z)));
+}
+
+// Both kernels below have no separate producer warp: a 17-warp CTA would put five warps on one
+// SM sub-partition and cap a thread at ~100 registers, too few for the per-branch weights and
+// gradient accumulators.  Thread 0 issues a token's bulk copies instead, refilling a stage as soon
+// as a CTA barrier shows every thread is done with it.
+
+// Issue the copies of one token into a stage and arm its barrier (thread 0 only).
+__device__ __forceinline__ void hc_issue(uint8_t *dst, uint64_t *bar, uint32_t bytes, uint64_t pol,
+                                         const uint8_t *a, uint32_t na, const uint8_t *b, uint32_t nb,
+                                         const uint8_t *c, uint32_t nc) {
+    mbar_arrive_expect_tx(bar, bytes);
+    bulk_load(dst, a, na, bar, pol);
+    bulk_load(dst + na, b, nb, bar, pol);
+    if (c) bulk_load(dst + na + nb, c, nc, bar, pol);
+}
+
+// Forward: G groups of NCW warps share one CTA and a ring of S token stages; group g works on
+// the CTA's tokens g, g + G, ...  While one group reduces and writes a token, the other's data is
+// landing and being read, so the CTA's one-token-at-a-time latency is hidden inside the SM.
+// Thread index gc within a group owns vectors jj = gc, gc + 32*NCW, ... (VPB of them) of every
+// branch row.  Groups synchronise on their own named barriers (ids 1..G).
+template <typename T, int HC, int NCW, int G, int VPB>
+__global__ void __launch_bounds__(G * NCW * 32, 1) gate_hc_fwd_kernel(const __grid_constant__ GateHcFwdParams p) {
+    using V = Vec<T>;
+    constexpr int EV = V::N;
+    constexpr int NC = NCW * 32;
+    extern __shared__ __align__(128) uint8_t smem[];
+
+    const uint32_t rb = p.row_bytes;
+    const uint32_t stage = (2 * HC + 1) * rb;  // x [HC rows] then kv [HC + 1 rows]
+    const int S = p.stages;
+    const int nvec = static_cast<int>(rb / 16);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + static_cast<size_t>(S) * stage);
+    uint32_t *issued_cnt = reinterpret_cast<uint32_t *>(full + S);  // per stage, for the final drain
+    float *red = reinterpret_cast<float *>(full + 2 * S);           // [G][2][NCW][4 * HC]
+
+    const int group = threadIdx.x / NC;
+    const int gc = threadIdx.x - group * NC;
+    const int gwarp = gc >> 5;
+    const int lane = gc & 31;
+    const int64_t first = blockIdx.x, stride = gridDim.x;
+    const int64_t n_my = first < p.T ? (p.T - 1 - first) / stride + 1 : 0;
+    const uint64_t pol = l2_evict_first_policy();
+    auto issue = [&](int64_t it) {
+        const int64_t tok = first + it * stride;
+        const int st = static_cast<int>(it % S);
+        issued_cnt[st] += 1;
+        hc_issue(smem + static_cast<size_t>(st) * stage, &full[st], stage, pol,
+                 p.x + static_cast<size_t>(tok) * HC * rb, HC * rb, p.kv + static_cast<size_t>(tok) * (HC + 1) * rb,
+                 (HC + 1) * rb, nullptr, 0);
+    };
+    if (threadIdx.x == 0) {
+        for (int q = 0; q < S; ++q) {
+            mbar_init(&full[q], 1);
+            issued_cnt[q] = 0;
+        }
+        mbar_init_fence();
+        for (int64_t q = 0; q < S && q < n_my; ++q) issue(q);
+    }
+
+    float w[HC][VPB][EV];
+#pragma unroll
+    for (int h = 0; h < HC; ++h)
+#pragma unroll
+        for (int m = 0; m < VPB; ++m) {
+            const int jj = gc + m * NC;
+#pragma unroll
+            for (int e = 0; e < EV; ++e) w[h][m][e] = 0.f;
+            if (jj < nvec) {
+#pragma unroll
+                for (int e = 0; e < EV; e += 4) {
+                    const float4 q = __ldg(reinterpret_cast<const float4 *>(p.w + static_cast<size_t>(h) * p.d + jj * EV + e));
+                    w[h][m][e] = q.x;
+                    w[h][m][e + 1] = q.y;
+                    w[h][m][e + 2] = q.z;
+                    w[h][m][e + 3] = q.w;
+                }
+            }
+        }
+    const float inv_d = 1.0f / static_cast<float>(p.d);
+    __syncthreads();  // barriers initialised
+
+    float *gred = red + static_cast<size_t>(group) * 2 * NCW * 4 * HC;
+    int64_t li = 0;  // this group's iteration count
+    for (int64_t it = group; it < n_my; it += G, ++li) {
+        const int s = static_cast<int>(it % S);
+        const bool ok = mbar_wait(&full[s], static_cast<uint32_t>((it / S) & 1));
+        const uint8_t *st = smem + static_cast<size_t>(s) * stage;
+        const uint8_t *kst = st + HC * rb;
+
+        float acc[HC][3];
+#pragma unroll
+        for (int h = 0; h < HC; ++h) acc[h][0] = acc[h][1] = acc[h][2] = 0.f;
+        if (ok) {
+#pragma unroll
+            for (int h = 0; h < HC; ++h)
+#pragma unroll
+                for (int m = 0; m < VPB; ++m) {
+                    const int jj = gc + m * NC;
+                    if (jj < nvec) {
+                        float xv[EV], kx[EV];
+                        V::unpack(*reinterpret_cast<const uint4 *>(st + h * rb + jj * 16), xv);
+                        V::unpack(*reinterpret_cast<const uint4 *>(kst + h * rb + jj * 16), kx);
+#pragma unroll
+                        for (int e = 0; e < EV; ++e) {
+                            acc[h][0] = fmaf(xv[e], xv[e], acc[h][0]);
+                            acc[h][1] = fmaf(kx[e], kx[e], acc[h][1]);
+                            acc[h][2] = fmaf(xv[e] * w[h][m][e], kx[e], acc[h][2]);
+                        }
+                    }
+                }
+        }
+        float *rbuf = gred + (li & 1) * NCW * 4 * HC;
+#pragma unroll
+        for (int h = 0; h < HC; ++h)
+#pragma unroll
+            for (int q = 0; q < 3; ++q) {
+                const float v = warp_sum(acc[h][q]);
+                if (lane == 0) rbuf[(gwarp * HC + h) * 4 + q] = v;
+            }
+        if (named_sync_or(1 + group, NC, !ok)) {
+            if (gc == 0) report(p.status, nullptr, ENGRAM_DEVERR_TIMEOUT);
+            break;
+        }
+        // Cross-warp totals: lane l of every warp sums quantity l (l < 4 HC, slot 3 of each branch
+        // unused) over the group's warps in a fixed order, then the totals are broadcast by shuffles.
+        float tot = 0.f;
+        if (lane < 4 * HC) {
+#pragma unroll
+            for (int q = 0; q < NCW; ++q) tot += rbuf[q * HC * 4 + lane];
+        }
+        float gate[HC], rx[HC], rk[HC], dt[HC];
+#pragma unroll
+        for (int h = 0; h < HC; ++h) {
+            const float a = __shfl_sync(0xffffffffu, tot, h * 4 + 0);
+            const float b = __shfl_sync(0xffffffffu, tot, h * 4 + 1);
+            const float dd = __shfl_sync(0xffffffffu, tot, h * 4 + 2);
+            rx[h] = 1.0f / sqrtf(a * inv_d + p.eps);
+            rk[h] = 1.0f / sqrtf(b * inv_d + p.eps);
+            dt[h] = dd;
+            gate[h] = hc_activation(dd * rx[h] * rk[h] * p.scale, p.clamp);
+        }
+
+        // out = x + gate * v (the value row is kv row HC)
+        const int64_t tok = first + it * stride;
+        uint8_t *orow = p.out + static_cast<size_t>(tok) * HC * rb;
+#pragma unroll
+        for (int m = 0; m < VPB; ++m) {
+            const int jj = gc + m * NC;
+            if (jj < nvec) {
+                float vv[EV];
+                V::unpack(*reinterpret_cast<const uint4 *>(kst + HC * rb + jj * 16), vv);
+#pragma unroll
+                for (int h = 0; h < HC; ++h) {
+                    float xv[EV];
+                    V::unpack(*reinterpret_cast<const uint4 *>(st + h * rb + jj * 16), xv);
+#pragma unroll
+                    for (int e = 0; e < EV; ++e) xv[e] = fmaf(gate[h], vv[e], xv[e]);
+                    st_global_v4(orow + h * rb + jj * 16, V::pack(xv));
+                }
+            }
+        }
+        if (gc < HC) {
+            const size_t o = static_cast<size_t>(tok) * HC + gc;
+            if (p.gate) p.gate[o] = gate[gc];
+            if (p.rstd_x) p.rstd_x[o] = rx[gc];
+            if (p.rstd_k) p.rstd_k[o] = rk[gc];
+            if (p.dot) p.dot[o] = dt[gc];
+        }
+        named_sync(1 + group, NC);  // the whole group is done with stage s: refill it
+        if (gc == 0 && it + S < n_my) issue(it + S);
+    }
+    // Never leave while a copy into this CTA's shared memory may be in flight: wait for the last
+    // copy issued into every stage (a completed phase returns at once).
+    __syncthreads();
+    if (threadIdx.x == 0)
+        for (int q = 0; q < S; ++q)
+            if (issued_cnt[q] > 0 && !mbar_wait(&full[q], (issued_cnt[q] - 1) & 1u))
+                report(p.status, nullptr, ENGRAM_DEVERR_TIMEOUT);
+}
+
+template <typename T, int HC, int NCW>
+__global__ void __launch_bounds__(NCW * 32, 1) gate_hc_bwd_kernel(const __grid_constant__ GateHcBwdParams p) {
+    using V = Vec<T>;
+    constexpr int EV = V::N;
+    constexpr int NC = NCW * 32;
+    constexpr int VPB = HcShape<HC>::kVpb;
+    extern __shared__ __align__(128) uint8_t smem[];
+
+    const uint32_t rb = p.row_bytes;
+    const uint32_t stage = (3 * HC + 1) * rb;  // dout [HC], x [HC], kv [HC + 1]
+    const int S = p.stages;
+    const int nvec = static_cast<int>(rb / 16);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + static_cast<size_t>(S) * stage);
+    float *red = reinterpret_cast<float *>(full + 2 * S);  // [2][NCW][4 * HC]
+
+    const int c = threadIdx.x;
+    const int warp = c >> 5;
+    const int lane = c & 31;
+    // The CTA's tokens, in order: its partials b, b + G, ... each a chunk of C tokens (only the
+    // last partial of the whole pass can be shorter, and it is the last of its CTA).
+    const int64_t G = gridDim.x, C = p.chunk;
+    int64_t n_my = 0;
+    for (int64_t pp = blockIdx.x; pp < p.P; pp += G) {
+        const int64_t t0 = pp * C;
+        n_my += t0 >= p.T ? 0 : (t0 + C < p.T ? C : p.T - t0);
+    }
+    const uint64_t pol = l2_evict_first_policy();
+    auto token_of = [&](int64_t j) { return (blockIdx.x + (j / C) * G) * C + j % C; };
+    auto issue = [&](int64_t j) {
+        const int64_t t = token_of(j);
+        hc_issue(smem + static_cast<size_t>(j % S) * stage, &full[j % S], stage, pol,
+                 p.g + static_cast<size_t>(t) * HC * rb, HC * rb, p.x + static_cast<size_t>(t) * HC * rb, HC * rb,
+                 p.kv + static_cast<size_t>(t) * (HC + 1) * rb, (HC + 1) * rb);
+    };
+    int64_t issued = 0;
+    if (c == 0) {
+        for (int q = 0; q < S; ++q) mbar_init(&full[q], 1);
+        mbar_init_fence();
+        for (; issued < S && issued < n_my; ++issued) issue(issued);
+    }
+
+    float w[HC][VPB][EV];
+#pragma unroll
+    for (int h = 0; h < HC; ++h)
+#pragma unroll
+        for (int m = 0; m < VPB; ++m) {
+            const int jj = c + m * NC;
+#pragma unroll
+            for (int e = 0; e < EV; ++e) w[h][m][e] = 0.f;
+            if (jj < nvec) {
+#pragma unroll
+                for (int e = 0; e < EV; e += 4) {
+                    const float4 q = __ldg(reinterpret_cast<const float4 *>(p.w + static_cast<size_t>(h) * p.d + jj * EV + e));
+                    w[h][m][e] = q.x;
+                    w[h][m][e + 1] = q.y;
+                    w[h][m][e + 2] = q.z;
+                    w[h][m][e + 3] = q.w;
+                }
+            }
+        }
+    const float inv_d = 1.0f / static_cast<float>(p.d);
+    __syncthreads();  // barriers initialised
+
+    int64_t it = 0;
+    bool failed = false;
+    for (int64_t pp = blockIdx.x; pp < p.P && !failed; pp += G) {
+        const int64_t t0 = pp * C;
+        const int64_t t1 = t0 + C < p.T ? t0 + C : p.T;
+        float acc[HC][VPB][EV];
+#pragma unroll
+        for (int h = 0; h < HC; ++h)
+#pragma unroll
+            for (int m = 0; m < VPB; ++m)
+#pragma unroll
+                for (int e = 0; e < EV; ++e) acc[h][m][e] = 0.f;
+
+        for (int64_t t = t0; t < t1; ++t, ++it) {
+            const int s = static_cast<int>(it % S);
+            float gt[HC], rx[HC], rk[HC], dt[HC];
+#pragma unroll
+            for (int h = 0; h < HC; ++h) {
+                const size_t o = static_cast<size_t>(t) * HC + h;
+                gt[h] = __ldg(p.gate + o);
+                rx[h] = __ldg(p.rstd_x + o);
+                rk[h] = __ldg(p.rstd_k + o);
+                dt[h] = __ldg(p.dot + o);
+            }
+            const bool ok = mbar_wait(&full[s], static_cast<uint32_t>((it / S) & 1));
+            const uint8_t *gst = smem + static_cast<size_t>(s) * stage;
+            const uint8_t *xst = gst + HC * rb;
+            const uint8_t *kst = gst + 2 * HC * rb;
+
+            // pass 1: dgate_h partials, and dv = sum_h gate_h dout_h
+            float dg[HC];
+#pragma unroll
+            for (int h = 0; h < HC; ++h) dg[h] = 0.f;
+            if (ok) {
+#pragma unroll
+                for (int m = 0; m < VPB; ++m) {
+                    const int jj = c + m * NC;
+                    if (jj < nvec) {
+                        float vv[EV], dv[EV];
+                        V::unpack(*reinterpret_cast<const uint4 *>(kst + HC * rb + jj * 16), vv);
+#pragma unroll
+                        for (int e = 0; e < EV; ++e) dv[e] = 0.f;
+#pragma unroll
+                        for (int h = 0; h < HC; ++h) {
+                            float gv[EV];
+                            V::unpack(*reinterpret_cast<const uint4 *>(gst + h * rb + jj * 16), gv);
+#pragma unroll
+                            for (int e = 0; e < EV; ++e) {
+                                dg[h] = fmaf(gv[e], vv[e], dg[h]);
+                                dv[e] = fmaf(gt[h], gv[e], dv[e]);
+                            }
+                        }
+                        st_global_v4(p.dkv + (static_cast<size_t>(t) * (HC + 1) + HC) * rb + jj * 16, V::pack(dv));
+                    }
+                }
+            }
+            float *rbuf = red + (it & 1) * NCW * 4 * HC;
+#pragma unroll
+            for (int h = 0; h < HC; ++h) {
+                const float v = warp_sum(dg[h]);
+                if (lane == 0) rbuf[(warp * HC + h) * 4] = v;
+            }
+            if (__syncthreads_or(!ok)) {
+                if (c == 0) report(p.status, nullptr, ENGRAM_DEVERR_TIMEOUT);
+                failed = true;
+                break;
+            }
+            // cross-warp totals of dgate: lane h sums branch h over the warps, then a broadcast
+            float tot = 0.f;
+            if (lane < HC) {
+#pragma unroll
+                for (int q = 0; q < NCW; ++q) tot += rbuf[(q * HC + lane) * 4];
+            }
+            float cc[HC], cx[HC], ck[HC];
+#pragma unroll
+            for (int h = 0; h < HC; ++h) {
+                const float D = __shfl_sync(0xffffffffu, tot, h);
+                // dL/d dot through the sigmoid, the signed square root and the scaling; the clamp
+                // holds the activation constant where |z| < clamp, so no gradient flows there.
+                const float sc = p.scale * rx[h] * rk[h];
+                const float z = dt[h] * sc;
+                const float a = gt[h];
+                cc[h] = fabsf(z) < p.clamp ? 0.f : D * a * (1.0f - a) / (2.0f * sqrtf(fabsf(z))) * sc;
+                cx[h] = cc[h] * dt[h] * rx[h] * rx[h] * inv_d;
+                ck[h] = cc[h] * dt[h] * rk[h] * rk[h] * inv_d;
+            }
+
+            // pass 2: dx = dout + c (w k - dot rstd_x^2 x / d), dk = c (w x - dot rstd_k^2 k / d), dw partials
+#pragma unroll
+            for (int h = 0; h < HC; ++h)
+#pragma unroll
+                for (int m = 0; m < VPB; ++m) {
+                    const int jj = c + m * NC;
+                    if (jj < nvec) {
+                        float xv[EV], kx[EV], gv[EV], ox[EV], okk[EV];
+                        V::unpack(*reinterpret_cast<const uint4 *>(xst + h * rb + jj * 16), xv);
+                        V::unpack(*reinterpret_cast<const uint4 *>(kst + h * rb + jj * 16), kx);
+                        V::unpack(*reinterpret_cast<const uint4 *>(gst + h * rb + jj * 16), gv);
+#pragma unroll
+                        for (int e = 0; e < EV; ++e) {
+                            const float cw = cc[h] * w[h][m][e];
+                            ox[e] = gv[e] + fmaf(cw, kx[e], -cx[h] * xv[e]);
+                            okk[e] = fmaf(cw, xv[e], -ck[h] * kx[e]);
+                            acc[h][m][e] = fmaf(cc[h] * xv[e], kx[e], acc[h][m][e]);
+                        }
+                        st_global_v4(p.dx + (static_cast<size_t>(t) * HC + h) * rb + jj * 16, V::pack(ox));
+                        st_global_v4(p.dkv + (static_cast<size_t>(t) * (HC + 1) + h) * rb + jj * 16, V::pack(okk));
+                    }
+                }
+            __syncthreads();  // every thread is done with stage s: refill it
+            if (c == 0 && issued < n_my) issue(issued++);
+        }
+        if (failed) break;
+
+        float *prow = p.dw_partial + static_cast<size_t>(pp) * HC * p.d;
+#pragma unroll
+        for (int h = 0; h < HC; ++h)
+#pragma unroll
+            for (int m = 0; m < VPB; ++m) {
+                const int jj = c + m * NC;
+                if (jj < nvec) {
+#pragma unroll
+                    for (int e = 0; e < EV; e += 4)
+                        *reinterpret_cast<float4 *>(prow + static_cast<size_t>(h) * p.d + jj * EV + e) =
+                            make_float4(acc[h][m][e], acc[h][m][e + 1], acc[h][m][e + 2], acc[h][m][e + 3]);
+                }
+            }
+    }
+    if (c == 0)
+        for (int64_t q = it; q < issued; ++q)
+            if (!mbar_wait(&full[q % S], static_cast<uint32_t>((q / S) & 1)))
+                report(p.status, nullptr, ENGRAM_DEVERR_TIMEOUT);
+}
+
+namespace {
+
+// Smallest NCW in {2, 4, 8, 16} whose threads cover a branch row with at most HcShape<HC>::kVpb
+// vectors each; 0 when none does.
+template <int HC>
+int hc_consumer_warps(int nvec) {
+    for (int ncw = 2; ncw <= 16; ncw *= 2)
+        if (ncw * 32 * HcShape<HC>::kVpb >= nvec) return ncw;
+    return 0;
+}
+
+// Forward launch: two groups of NCW warps, VPB = 2 * HcShape<HC>::kVpb vectors per branch row
+// (the forward keeps no gradient accumulators, so it can afford twice the weights per thread).
+template <typename T, int HC, int NCW>
+engram_status launch_hc_fwd(const GateHcFwdParams &p, const DeviceInfo &dev, cudaStream_t stream) {
+    constexpr int G = 2;
+    constexpr int NCWG = NCW / 2 > 0 ? NCW / 2 : 1;
+    const auto kern = gate_hc_fwd_kernel<T, HC, NCWG, G, 2 * HcShape<HC>::kVpb>;
+    // As many stages as fit (2..4): one stage is a whole token, and with a single CTA per SM the
+    // refill of a stage is issued only once the CTA is done with it, so depth must come from stages.
+    const int stage = (2 * HC + 1) * static_cast<int>(p.row_bytes);
+    int S = 4;
+    while (S > 2 && hc_smem_bytes(S, stage, NCW, HC) > 220 * 1024) --S;
+    const int smem = hc_smem_bytes(S, stage, NCW, HC);
+    if (smem > dev.smem_optin)
+        return fail(ENGRAM_ERR_SHAPE, "engram_gate_hc_fwd: a token of %d bytes does not fit twice in shared memory",
+                    stage);
+    engram_status st = set_smem(reinterpret_cast<const void *>(kern), smem);
+    if (st != ENGRAM_OK) return st;
+    int b = 227 * 1024 / smem;
+    b = b < 1 ? 1 : (b > 4 ? 4 : b);
+    GateHcFwdParams q = p;
+    q.stages = S;
+    int64_t grid = static_cast<int64_t>(dev.num_sms) * b;
+    if (grid > p.T) grid = p.T;
+    grid = cap_grid(grid);
+    kern<<<static_cast<unsigned>(grid), G * NCWG * 32, smem, stream>>>(q);
+    return check_launch("engram_gate_hc_fwd");
+}
+
+template <typename T, int HC, int NCW>
+engram_status launch_hc_bwd(const GateHcBwdParams &p, const DeviceInfo &dev, cudaStream_t stream) {
+    const auto kern = gate_hc_bwd_kernel<T, HC, NCW>;
+    const int stage = (3 * HC + 1) * static_cast<int>(p.row_bytes);
+    int S = 3;
+    while (S >= 2 && hc_smem_bytes(S, stage, NCW, HC) > dev.smem_optin) --S;
+    if (S < 2)
+        return fail(ENGRAM_ERR_SHAPE, "engram_gate_hc_bwd: a token of %d bytes does not fit twice in shared memory",
+                    stage);
+    const int smem = hc_smem_bytes(S, stage, NCW, HC);
+    engram_status st = set_smem(reinterpret_cast<const void *>(kern), smem);
+    if (st != ENGRAM_OK) return st;
+    GateHcBwdParams q = p;
+    q.stages = S;
+    const int64_t grid = cap_grid(p.P);  // one CTA per partial, as in the single-branch backward
+    kern<<<static_cast<unsigned>(grid), NCW * 32, smem, stream>>>(q);
+    return check_launch("engram_gate_hc_bwd");
+}
+
+template <typename T, int HC>
+engram_status dispatch_hc_fwd(const GateHcFwdParams &p, const DeviceInfo &dev, cudaStream_t s) {
+    switch (hc_consumer_warps<HC>(static_cast<int>(p.row_bytes / 16))) {
+        case 2: return launch_hc_fwd<T, HC, 2>(p, dev, s);
+        case 4: return launch_hc_fwd<T, HC, 4>(p, dev, s);
+        case 8: return launch_hc_fwd<T, HC, 8>(p, dev, s);
+        case 16: return launch_hc_fwd<T, HC, 16>(p, dev, s);
+        default: return fail(ENGRAM_ERR_SHAPE, "engram_gate_hc_fwd: d = %d too large for %d branches", p.d, HC);
+    }
+}
+
+template <typename T, int HC>
+engram_status dispatch_hc_bwd(const GateHcBwdParams &p, const DeviceInfo &dev, cudaStream_t s) {
+    switch (hc_consumer_warps<HC>(static_cast<int>(p.row_bytes / 16))) {
+        case 2: return launch_hc_bwd<T, HC, 2>(p, dev, s);
+        case 4: return launch_hc_bwd<T, HC, 4>(p, dev, s);
+        case 8: return launch_hc_bwd<T, HC, 8>(p, dev, s);
+        case 16: return launch_hc_bwd<T, HC, 16>(p, dev, s);
+        default: return fail(ENGRAM_ERR_SHAPE, "engram_gate_hc_bwd: d = %d too large for %d branches", p.d, HC);
+    }
+}
+
+template <typename T>
+engram_status dispatch_hc_fwd_t(int hc, const GateHcFwdParams &p, const DeviceInfo &dev, cudaStream_t s) {
+    switch (hc) {
+        case 1: return dispatch_hc_fwd<T, 1>(p, dev, s);
+        case 2: return dispatch_hc_fwd<T, 2>(p, dev, s);
+        default: return dispatch_hc_fwd<T, 4>(p, dev, s);
+    }
+}
+
+template <typename T>
+engram_status dispatch_hc_bwd_t(int hc, const GateHcBwdParams &p, const DeviceInfo &dev, cudaStream_t s) {
+    switch (hc) {
+        case 1: return dispatch_hc_bwd<T, 1>(p, dev, s);
+        case 2: return dispatch_hc_bwd<T, 2>(p, dev, s);
+        default: return dispatch_hc_bwd<T, 4>(p, dev, s);
+    }
+}
+
+engram_status hc_common_checks(const char *fn, engram_dtype dtype, int64_t T, int32_t hc, int32_t d, int *es,
+                               int64_t *row_bytes) {
+    *es = dtype_size(dtype);
+    if (*es == 0) return fail(ENGRAM_ERR_DTYPE, "%s: dtype %d", fn, (int)dtype);
+    if (hc != 1 && hc != 2 && hc != 4) return fail(ENGRAM_ERR_SHAPE, "%s: hc = %d (1, 2 or 4)", fn, hc);
+    if (T < 0 || d <= 0) return fail(ENGRAM_ERR_SHAPE, "%s: T = %lld, d = %d", fn, (long long)T, d);
+    *row_bytes = static_cast<int64_t>(d) * *es;
+    if (*row_bytes % 16 != 0) return fail(ENGRAM_ERR_ALIGN, "%s: row of %lld bytes", fn, (long long)*row_bytes);
+    if (*row_bytes > ENGRAM_MAX_ROW_BYTES)
+        return fail(ENGRAM_ERR_SHAPE, "%s: row of %lld bytes exceeds %d", fn, (long long)*row_bytes,
+                    ENGRAM_MAX_ROW_BYTES);
+    return ENGRAM_OK;
+}
+
+}  // namespace
+}  // namespace engram
+
+using namespace engram;
+
+extern "C" engram_status engram_gate_hc_fwd(const void *x, const void *kv, engram_dtype dtype, const float *w_fused,
+                                            int64_t T, int32_t hc, int32_t d, float eps, float clamp_value,
+                                            void *out, float *gate, float *rstd_x, float *rstd_k, float *dot,
+                                            engram_stream_t stream) {
+    const char *fn = "engram_gate_hc_fwd";
+    if (!w_fused || (T > 0 && (!x || !kv || !out))) return fail(ENGRAM_ERR_NULL, "%s: NULL pointer", fn);
+    int es;
+    int64_t row_bytes;
+    engram_status st = hc_common_checks(fn, dtype, T, hc, d, &es, &row_bytes);
+    if (st != ENGRAM_OK) return st;
+    if (out == x && (gate || rstd_x || rstd_k || dot))
+        return fail(ENGRAM_ERR_SHAPE, "%s: in-place output overwrites x, which a backward reads; save no statistic", fn);
+    if (!(clamp_value >= 0.0f)) return fail(ENGRAM_ERR_SHAPE, "%s: clamp_value %g", fn, clamp_value);
+    const void *al[] = {x, kv, w_fused, out};
+    for (const void *q : al)
+        if (!aligned16(q)) return fail(ENGRAM_ERR_ALIGN, "%s: tensor not 16-byte aligned", fn);
+    DeviceInfo dev;
+    if ((st = current_device(&dev)) != ENGRAM_OK) return st;
+    const void *dp[] = {x, kv, w_fused, out, gate, rstd_x, rstd_k, dot};
+    for (const void *q : dp)
+        if ((st = check_device_ptr(q, dev.device, fn)) != ENGRAM_OK) return st;
+    if (T == 0) return ENGRAM_OK;
+    GateHcFwdParams p{};
+    p.x = static_cast<const uint8_t *>(x);
+    p.kv = static_cast<const uint8_t *>(kv);
+    p.w = w_fused;
+    p.out = static_cast<uint8_t *>(out);
+    p.gate = gate;
+    p.rstd_x = rstd_x;
+    p.rstd_k = rstd_k;
+    p.dot = dot;
+    p.status = dev.status_word;
+    p.T = T;
+    p.d = d;
+    p.row_bytes = static_cast<uint32_t>(row_bytes);
+    p.eps = eps;
+    p.clamp = clamp_value;
+    p.scale = 1.0f / sqrtf(static_cast<float>(d));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    return dtype == ENGRAM_F32 ? dispatch_hc_fwd_t<float>(hc, p, dev, s) : dispatch_hc_fwd_t<__nv_bfloat16>(hc, p, dev, s);
+}
+
+extern "C" engram_status engram_gate_hc_bwd(const void *dout, const void *x, const void *kv, engram_dtype dtype,
+                                            const float *w_fused, const float *gate, const float *rstd_x,
+                                            const float *rstd_k, const float *dot, int64_t T, int32_t hc, int32_t d,
+                                            float clamp_value, void *dx, void *dkv, float *dw_partial, int32_t P,
+                                            engram_stream_t stream) {
+    const char *fn = "engram_gate_hc_bwd";
+    if (!w_fused || !dw_partial ||
+        (T > 0 && (!dout || !x || !kv || !gate || !rstd_x || !rstd_k || !dot || !dx || !dkv)))
+        return fail(ENGRAM_ERR_NULL, "%s: NULL pointer", fn);
+    int es;
+    int64_t row_bytes;
+    engram_status st = hc_common_checks(fn, dtype, T, hc, d, &es, &row_bytes);
+    if (st != ENGRAM_OK) return st;
+    if (P < 1) return fail(ENGRAM_ERR_SHAPE, "%s: P = %d", fn, P);
+    if (!(clamp_value >= 0.0f)) return fail(ENGRAM_ERR_SHAPE, "%s: clamp_value %g", fn, clamp_value);
+    const void *al[] = {dout, x, kv, w_fused, dx, dkv, dw_partial};
+    for (const void *q : al)
+        if (!aligned16(q)) return fail(ENGRAM_ERR_ALIGN, "%s: tensor not 16-byte aligned", fn);
+    DeviceInfo dev;
+    if ((st = current_device(&dev)) != ENGRAM_OK) return st;
+    const void *dp[] = {dout, x, kv, w_fused, gate, rstd_x, rstd_k, dot, dx, dkv, dw_partial};
+    for (const void *q : dp)
+        if ((st = check_device_ptr(q, dev.device, fn)) != ENGRAM_OK) return st;
+    GateHcBwdParams p{};
+    p.g = static_cast<const uint8_t *>(dout);
+    p.x = static_cast<const uint8_t *>(x);
+    p.kv = static_cast<const uint8_t *>(kv);
+    p.w = w_fused;
+    p.gate = gate;
+    p.rstd_x = rstd_x;
+    p.rstd_k = rstd_k;
+    p.dot = dot;
+    p.dx = static_cast<uint8_t *>(dx);
+    p.dkv = static_cast<uint8_t *>(dkv);
+    p.dw_partial = dw_partial;
+    p.status = dev.status_word;
+    p.T = T;
+    p.P = P;
+    p.chunk = (T + P - 1) / P;
+    p.d = d;
+    p.row_bytes = static_cast<uint32_t>(row_bytes);
+    p.clamp = clamp_value;
+    p.scale = 1.0f / sqrtf(static_cast<float>(d));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    return dtype == ENGRAM_F32 ? dispatch_hc_bwd_t<float>(hc, p, dev, s) : dispatch_hc_bwd_t<__nv_bfloat16>(hc, p, dev, s);
+}

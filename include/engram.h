@@ -262,6 +262,46 @@ engram_status engram_grad_w_reduce(const float *dw_partial, int32_t P, int32_t d
                                    engram_stream_t stream);
 
 /* ------------------------------------------------------------------------- */
+/* The multi-branch gate of the TileKernels release  (ch. 34 sec. 2.1, 3.2, 4.2) */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * hc branches (hc = 1, 2 or 4; the release fixes 4) share one value row.  x is [T, hc, d],
+ * kv is [T, hc+1, d] (rows 0..hc-1 the branch keys, row hc the shared value), w_fused is
+ * [hc, d] fp32 (engram_fuse_weight over hc*d elements).  For branch h of token t, s = 1/sqrt(d):
+ *     rstd_x = 1/sqrt(sum_i x_i^2 / d + eps),  rstd_k likewise over the key row,
+ *     dot    = sum_i x_i w_fused[h, i] k_i,     z = s * rstd_x * rstd_k * dot,
+ *     gate   = sigmoid(sign(z) * sqrt(max(|z|, clamp_value)))   (sign(+0) = +),
+ *     out    = x + gate * v.
+ * gate, rstd_x, rstd_k, dot are [T, hc] fp32, each nullable.  out may equal x (in-place
+ * writing) only when no statistic is saved: a backward needs the original x, so that
+ * combination is refused (ENGRAM_ERR_SHAPE).  One token's rows must fit twice in shared
+ * memory ((2 hc + 1) * d * element size per copy) and d must be at most 4096 bf16 / 2048
+ * fp32 elements for hc = 4 (twice / four times that for hc = 2 / 1).
+ */
+engram_status engram_gate_hc_fwd(const void *x, const void *kv, engram_dtype dtype, const float *w_fused,
+                                 int64_t T, int32_t hc, int32_t d, float eps, float clamp_value, void *out,
+                                 float *gate, float *rstd_x, float *rstd_k, float *dot, engram_stream_t stream);
+
+/*
+ * Backward of engram_gate_hc_fwd given dout = dL/dout [T, hc, d] and the saved statistics:
+ *     dgate_h = sum_i dout_h,i v_i
+ *     c_h     = 0 where |z_h| < clamp_value (the clamp holds the gate constant), else
+ *               dgate_h gate_h (1 - gate_h) / (2 sqrt|z_h|) * s rstd_x rstd_k      (= dL/d dot_h)
+ *     dx_h    = dout_h + c_h (w_h k_h - dot_h rstd_x^2 x_h / d)
+ *     dk_h    = c_h (w_h x_h - dot_h rstd_k^2 k_h / d)
+ *     dv      = sum_h gate_h dout_h
+ * dx is [T, hc, d]; dkv is [T, hc+1, d] (row hc = dv).  dw_partial is [P, hc, d] fp32 with
+ * partial p the sum of c_h x_h k_h over tokens [p*C, min(T, (p+1)*C)), C = ceil(T / P) --
+ * reduce it with engram_grad_w_reduce over hc*d columns.
+ */
+engram_status engram_gate_hc_bwd(const void *dout, const void *x, const void *kv, engram_dtype dtype,
+                                 const float *w_fused, const float *gate, const float *rstd_x,
+                                 const float *rstd_k, const float *dot, int64_t T, int32_t hc, int32_t d,
+                                 float clamp_value, void *dx, void *dkv, float *dw_partial, int32_t P,
+                                 engram_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
 /* Allocation-free backward + reduction                                       */
 /* ------------------------------------------------------------------------- */
 

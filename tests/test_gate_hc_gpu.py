@@ -1,0 +1,172 @@
+"""GPU parity of the multi-branch gate (x [T, hc, d], kv [T, hc+1, d]) against the CPU oracle.
+
+Sizes: small fp32/bf16 cases for hc = 1, 2, 4; the production shape T = 8192, hc = 4, d = 4096
+(bf16) element by element; edge cases: the clamp branch (k = 0), in-place writing, an empty
+batch, and bitwise reruns.  The fused weight is [hc, d] (engram_fuse_weight over hc*d) and the
+partials reduce with engram_grad_w_reduce over hc*d columns.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import engram_conditional_memory_gb300 as ecm
+import oracle
+from synth import workloads as W
+from tests import gpu_helpers as H
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(autouse=True)
+def _status_clean(cuda_lib):
+    ecm.device_status(clear=True)
+    yield
+    assert ecm.device_status() == 0, "a kernel reported a device-side error"
+
+
+def _dev(x):
+    out = {}
+    for n, a in x.items():
+        t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if a.dtype == np.uint16 else torch.from_numpy(a)
+        out[n] = t.to(DEV)
+    return out
+
+
+def _run(t, wl, P=None):
+    T, hc, d = t["x"].shape
+    wf = ecm.fuse_weight(t["w_h"].reshape(-1), t["w_k"].reshape(-1)).reshape(hc, d)
+    out, gate, rx, rk, dot = ecm.gate_hc_fwd(t["x"], t["kv"], wf, wl.eps, wl.clamp)
+    dx, dkv, part = ecm.gate_hc_bwd(t["dout"], t["x"], t["kv"], wf, gate, rx, rk, dot, wl.clamp, P=P)
+    dw = ecm.grad_w_reduce(part.reshape(part.shape[0], hc * d)).reshape(hc, d)
+    return dict(wf=wf, out=out, gate=gate, rstd_x=rx, rstd_k=rk, dot=dot, dx=dx, dkv=dkv, part=part, dw=dw)
+
+
+def _check(r, x, wl, f=None, b=None):
+    """Element-wise parity with the oracle.
+
+    Tolerances: those of the single-branch gate, plus, for everything downstream of the
+    activation's slope, the error that the fp32 dot product carries into it.  The signed square
+    root has slope 1/(2 sqrt|z|) (up to 1/(2 sqrt(clamp)) = 500), so a dot-product error dz
+    becomes a relative error dz / (2 |z|) of c = dL/d dot; dx, dk and the weight gradient inherit
+    it in proportion to the c-weighted terms.  dz is the dot tolerance mapped to z.
+    """
+    f = f or oracle.gate_hc_fwd(x["x"], x["kv"], x["w_h"], x["w_k"], wl.eps, wl.clamp)
+    b = b or oracle.gate_hc_bwd(x["dout"], x["x"], x["kv"], x["w_h"], x["w_k"], wl.eps, wl.clamp)
+    check_plain = H.assert_close_bf16 if wl.dtype == "bf16" else H.assert_close_rows
+    assert np.abs(H.as_f64(r["gate"]) - f["gate"]).max() <= H.ALPHA_ATOL
+    np.testing.assert_allclose(H.as_f64(r["rstd_x"]), f["rstd_x"], rtol=H.RSTD_RTOL)
+    np.testing.assert_allclose(H.as_f64(r["rstd_k"]), f["rstd_k"], rtol=H.RSTD_RTOL)
+    xf, kvf, gf = H._f64(x["x"]), H._f64(x["kv"]), H._f64(x["dout"])
+    kf, vf = kvf[:, :wl.hc], kvf[:, wl.hc]
+    w = (x["w_h"] * x["w_k"]).astype(np.float64)[None]
+    dot_scale = np.abs(xf * w * kf).sum(-1)
+    dot_tol = 2e-5 * dot_scale + 1e-6
+    assert (np.abs(H.as_f64(r["dot"]) - f["dot"]) <= dot_tol).all()
+    check_plain(r["out"], f["out"], "out")
+    # c = dL/d dot (fp64, from the oracle's statistics) and its relative sensitivity to dz
+    sc = f["rstd_x"] * f["rstd_k"] / math.sqrt(wl.d)
+    z = f["dot"] * sc
+    dgate = (gf * vf[:, None, :]).sum(-1)
+    live = ~(np.abs(z) < wl.clamp)
+    c = np.where(live, dgate * f["gate"] * (1 - f["gate"]) / (2 * np.sqrt(np.maximum(np.abs(z), wl.clamp))) * sc, 0.0)
+    rel_c = np.where(live, dot_tol * sc / (2 * np.maximum(np.abs(z), wl.clamp)), 0.0)
+    extra = (rel_c * np.abs(c))[..., None]
+    base = (lambda ref: H.BF16_ATOL + H.BF16_RTOL * np.abs(ref)) if wl.dtype == "bf16" else \
+        (lambda ref: 1e-5 * np.abs(ref).max(axis=-1, keepdims=True) + 1e-4 * np.abs(ref))
+    dotx = (f["dot"] * f["rstd_x"] ** 2 / wl.d)[..., None]
+    dotk = (f["dot"] * f["rstd_k"] ** 2 / wl.d)[..., None]
+    dx, dk = H.as_f64(r["dx"]), H.as_f64(r["dkv"])[:, :wl.hc]
+    tol_dx = base(b["dx"]) + extra * (np.abs(w * kf) + np.abs(xf * dotx))
+    tol_dk = base(b["dkv"][:, :wl.hc]) + extra * (np.abs(w * xf) + np.abs(kf * dotk))
+    bad = np.abs(dx - b["dx"]) > tol_dx
+    assert not bad.any(), f"dx: {bad.sum()} outside tolerance at {np.argwhere(bad)[:3].tolist()}"
+    bad = np.abs(dk - b["dkv"][:, :wl.hc]) > tol_dk
+    assert not bad.any(), f"dk: {bad.sum()} outside tolerance at {np.argwhere(bad)[:3].tolist()}"
+    bad = np.abs(H.as_f64(r["dkv"])[:, wl.hc] - b["dkv"][:, wl.hc]) > base(b["dkv"][:, wl.hc])
+    assert not bad.any(), f"dv: {bad.sum()} outside tolerance"
+    dw_extra = np.einsum("th,thi->hi", rel_c * np.abs(c), np.abs(xf * kf))
+    assert (np.abs(H.as_f64(r["dw"]) - b["dweight"]) <= 1e-4 * b["dweight_abs"] + dw_extra + 1e-7).all()
+    return f, b
+
+
+@pytest.mark.parametrize("dtype,hc,d,T", [("f32", 4, 64, 37), ("bf16", 4, 128, 50), ("bf16", 4, 4096, 40),
+                                          ("f32", 4, 2048, 9), ("bf16", 2, 1000, 33), ("f32", 1, 96, 70),
+                                          ("bf16", 1, 7168, 21), ("bf16", 2, 8192, 5)])
+def test_small_cases(dtype, hc, d, T):
+    wl = W.GateHcWorkload(name="t", T=T, hc=hc, d=d, dtype=dtype, seed=700 + hc * d + T)
+    x = W.gate_hc_host_inputs(wl)
+    r = _run(_dev(x), wl)
+    torch.cuda.synchronize()
+    _check(r, x, wl)
+
+
+def test_production_shape_every_element():
+    wl = W.gate_hc_4x4k()
+    x = W.gate_hc_host_inputs(wl)
+    r = _run(_dev(x), wl)
+    torch.cuda.synchronize()
+    n = 16
+    bounds = [(wl.T * i // n, wl.T * (i + 1) // n) for i in range(n)]
+    from concurrent.futures import ThreadPoolExecutor
+
+    def part(bnd):
+        a, b = bnd
+        return (oracle.gate_hc_fwd(x["x"], x["kv"], x["w_h"], x["w_k"], wl.eps, wl.clamp, a, b),
+                oracle.gate_hc_bwd(x["dout"], x["x"], x["kv"], x["w_h"], x["w_k"], wl.eps, wl.clamp, a, b))
+
+    with ThreadPoolExecutor(n) as ex:
+        parts = list(ex.map(part, bounds))
+    f = {k: np.concatenate([p[0][k] for p in parts]) for k in parts[0][0]}
+    b = {k: np.concatenate([p[1][k] for p in parts]) for k in ("dx", "dkv")}
+    b["dweight"] = np.sum([p[1]["dweight"] for p in parts], axis=0)
+    b["dweight_abs"] = np.sum([p[1]["dweight_abs"] for p in parts], axis=0)
+    _check(r, x, wl, f, b)
+
+
+def test_zero_keys_hit_the_clamp():
+    wl = W.GateHcWorkload(name="k0", T=64, hc=4, d=512, dtype="bf16", seed=41)
+    x = W.gate_hc_host_inputs(wl)
+    x["kv"][:, :4] = 0  # bf16 +0
+    t = _dev(x)
+    r = _run(t, wl)
+    g0 = 1.0 / (1.0 + math.exp(-0.001))
+    assert np.abs(H.as_f64(r["gate"]) - g0).max() <= 1e-6
+    assert torch.equal(r["dx"], t["dout"])  # no gradient through the clamped gate
+    assert (r["dkv"][:, :4] == 0).all() and (r["part"] == 0).all()
+    _check(r, x, wl)
+
+
+def test_in_place_forward_matches_and_refuses_saving():
+    wl = W.GateHcWorkload(name="ip", T=300, hc=4, d=1024, dtype="bf16", seed=42)
+    x = W.gate_hc_host_inputs(wl)
+    t = _dev(x)
+    wf = ecm.fuse_weight(t["w_h"].reshape(-1), t["w_k"].reshape(-1)).reshape(4, 1024)
+    ref, *_ = ecm.gate_hc_fwd(t["x"], t["kv"], wf, save_for_backward=False)
+    xin = t["x"].clone()
+    out, *_ = ecm.gate_hc_fwd(xin, t["kv"], wf, save_for_backward=False, inplace=True)
+    assert out.data_ptr() == xin.data_ptr() and torch.equal(xin, ref)
+    stats = tuple(torch.empty((300, 4), dtype=torch.float32, device=DEV) for _ in range(4))
+    # out == x with a statistic requested: refused on the host (a backward would read the overwritten x)
+    lib = ecm.load_library()
+    st = lib.engram_gate_hc_fwd(xin.data_ptr(), t["kv"].data_ptr(), 1, wf.data_ptr(), 300, 4, 1024, 1e-6, 1e-6,
+                                xin.data_ptr(), stats[0].data_ptr(), None, None, None,
+                                torch.cuda.current_stream().cuda_stream)
+    assert st == 2 and torch.equal(xin, ref)
+    with pytest.raises(ValueError):
+        ecm.gate_hc_fwd(xin, t["kv"], wf, inplace=True)
+
+
+def test_empty_batch_and_bitwise_reruns():
+    wl = W.GateHcWorkload(name="e", T=0, hc=4, d=256, dtype="bf16", seed=1)
+    x = W.gate_hc_host_inputs(wl)
+    t = _dev(x)
+    r = _run(t, wl, P=3)
+    assert r["out"].shape == (0, 4, 256) and (r["part"] == 0).all()
+    wl = W.GateHcWorkload(name="d", T=3000, hc=4, d=4096, dtype="bf16", seed=2)
+    t = _dev(W.gate_hc_host_inputs(wl))
+    a, b = _run(t, wl), _run(t, wl)
+    for k in ("out", "gate", "dx", "dkv", "part", "dw"):
+        assert torch.equal(a[k], b[k]), k
