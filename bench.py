@@ -482,6 +482,8 @@ def main_only(args, device):
         spec = ecm.HashSpec(s.min_order, s.num_orders, s.heads, s.multipliers, s.primes)
         ids, offs = torch.from_numpy(hw.token_ids).to(device), torch.from_numpy(hw.seq_offsets).to(device)
         cmap, table = torch.from_numpy(hw.compress_map).to(device), SD.hash_table(hw, device)
+        if op == "hash_gather_host":  # the same 4.1 GB table, page-locked in host memory
+            table = table.cpu().pin_memory()
         rows = torch.empty((hw.T, s.tables * hw.row_dim), dtype=table.dtype, device=device)
         nbytes = hw.T * (8 + 2 * s.tables * hw.row_dim * 2)
 
@@ -550,6 +552,74 @@ def main_only(args, device):
     return 0
 
 
+# ----------------------------------------------------------------------------- table offload
+
+def main_offload(args, device):
+    """The step with its tables in host memory: the hash + gather of the next batch (its rows follow
+    from the ids alone, so it can run ahead) reads the page-locked host table on a side stream, with
+    a few CTAs, while this step's gate work runs; versus the step with the table in HBM."""
+    import torch
+
+    import engram_conditional_memory_gb300 as ecm
+
+    wk = make_workload(device)
+    host_table = wk["table"].cpu().pin_memory()
+    hw = wk["hw"]
+    comp = torch.cuda.current_stream()
+    side = torch.cuda.Stream(device)
+    rows_next = torch.empty_like(wk["rows"])
+    fetched = torch.cuda.Event()
+
+    def gate_part():
+        ecm.fuse_weight(wk["w_h"], wk["w_k"], out=wk["w_fused"])
+        for i, m in enumerate(wk["mb"]):
+            st = wk["stats"][i]
+            ecm.gate_fwd(m["h"], m["k"], m["v"], wk["w_fused"], EPS, out=wk["out"][i], stats=st)
+            ecm.gate_bwd(m["dout"], m["h"], m["k"], m["v"], wk["w_fused"], *st, P=wk["P"], dh=wk["dh"][i],
+                         dk=wk["dk"][i], dv=wk["dv"][i], dw_partial=wk["part"][i])
+            ecm.grad_w_reduce(wk["part"][i], dweight_fused=wk["dweight"], w_h=wk["w_h"], w_k=wk["w_k"],
+                              grad_w_h=wk["grad_w_h"], grad_w_k=wk["grad_w_k"])
+
+    def offload_step():
+        side.wait_event(fetched)  # rows_next is free once the previous step's prefetch was consumed
+        with torch.cuda.stream(side):
+            prev = ecm.set_max_ctas(args.offload_ctas)
+            ecm.hash_gather(wk["spec"], wk["ids"], wk["offs"], host_table, wk["cmap"], hw.vocab, hw.vocab_c,
+                            out_rows=rows_next)
+            ecm.set_max_ctas(prev)
+        gate_part()
+        comp.wait_stream(side)  # the next step's rows are in HBM by the end of this step
+        fetched.record(comp)
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(comp)
+        side.wait_event(a)
+        for _ in range(args.steps):
+            fn()
+        b.record(comp)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / args.steps
+
+    dev_ms = timed(lambda: run_step(wk))
+    off_ms = timed(offload_step)
+    host_alone = timed(lambda: ecm.hash_gather(wk["spec"], wk["ids"], wk["offs"], host_table, wk["cmap"], hw.vocab,
+                                               hw.vocab_c, out_rows=rows_next))
+    # the prefetched rows equal the ones gathered from HBM
+    ecm.hash_gather(wk["spec"], wk["ids"], wk["offs"], host_table, wk["cmap"], hw.vocab, hw.vocab_c, out_rows=rows_next)
+    run_step(wk)
+    torch.cuda.synchronize()
+    same = bool(torch.equal(rows_next, wk["rows"]))
+    print(json.dumps({"offload": {"step_ms_table_in_hbm": dev_ms, "step_ms_table_in_host_memory": off_ms,
+                                  "overhead": off_ms / dev_ms - 1.0, "host_gather_alone_ms": host_alone,
+                                  "offload_ctas": args.offload_ctas, "rows_identical": same,
+                                  "workload": WORKLOAD}}), flush=True)
+    return 0
+
+
 # ----------------------------------------------------------------------------- main
 
 def main():
@@ -560,8 +630,11 @@ def main():
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end timing (profiling runs)")
-    ap.add_argument("--only", choices=["hash_gather", "hash_gather_small", "gate_fwd", "gate_fwd_2k", "gate_bwd",
-                                       "grad_w_reduce", "gate_hc_fwd", "gate_hc_bwd"],
+    ap.add_argument("--offload", action="store_true",
+                    help="the step with the tables in host memory, prefetched on a side stream (vs in HBM)")
+    ap.add_argument("--offload-ctas", type=int, default=32, help="CTAs of the host-table gather in --offload")
+    ap.add_argument("--only", choices=["hash_gather", "hash_gather_small", "hash_gather_host", "gate_fwd",
+                                       "gate_fwd_2k", "gate_bwd", "grad_w_reduce", "gate_hc_fwd", "gate_hc_bwd"],
                     help="time one kernel alone on its workload (consecutive launches, L2 not flushed)")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -621,6 +694,8 @@ def main_native(args, rank, local, world):
     ecm.load_library()
     if args.only:
         return main_only(args, device)
+    if args.offload:
+        return main_offload(args, device)
     wk = make_workload(device)
     props = torch.cuda.get_device_properties(device)
     gpu_id = f"GPU-{props.uuid}" if getattr(props, "uuid", None) else str(local)

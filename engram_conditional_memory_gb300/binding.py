@@ -73,6 +73,7 @@ def load_library():
             "engram_read_error_word": (st, [_p, _p, _p]),
             "engram_device_status": (st, [_p, _i32]),
             "engram_hash_gather": (st, [_p, _p, _p]),
+            "engram_hash_gather_host": (st, [_p, _p, _p]),
             "engram_fuse_weight": (st, [_p, _p, _c.c_int, _p, _i32, _p]),
             "engram_gate_fwd": (st, [_p, _p, _p, _c.c_int, _p, _i64, _i32, _c.c_float, _p, _p, _p, _p, _p, _p]),
             "engram_gate_bwd_num_partials": (st, [_i64, _i32, _p]),
@@ -321,11 +322,21 @@ class HashSpec:
 def hash_gather(spec: HashSpec, token_ids, seq_offsets, table, compress_map=None, vocab: int | None = None,
                 vocab_c: int | None = None, want_rows: bool = True, want_indices: bool = False, out_rows=None,
                 out_indices=None, err_word=None, stream=None):
-    """Returns (rows [T, tables*row_dim] or None, indices [T, tables] int32 or None)."""
+    """Returns (rows [T, tables*row_dim] or None, indices [T, tables] int32 or None).
+
+    A table in pinned host memory (a CPU tensor with is_pinned()) is read over the host link
+    (engram_hash_gather_host); a CUDA table is read from HBM.
+    """
     lib = load_library()
     _need(token_ids, "token_ids", torch.int32)
     _need(seq_offsets, "seq_offsets", torch.int64)
-    _need(table, "table")
+    host_table = not table.is_cuda
+    if host_table:
+        if not (table.is_pinned() and table.is_contiguous()):
+            raise ValueError("a host table must be a contiguous, pinned CPU tensor")
+    else:
+        _need(table, "table")
+    device = token_ids.device
     if compress_map is not None:
         _need(compress_map, "compress_map", torch.int32)
     T = token_ids.numel()
@@ -335,14 +346,15 @@ def hash_gather(spec: HashSpec, token_ids, seq_offsets, table, compress_map=None
     if vocab_c is None:
         vocab_c = vocab
     if want_rows and out_rows is None:
-        out_rows = torch.empty((T, spec.tables * row_dim), dtype=table.dtype, device=table.device)
+        out_rows = torch.empty((T, spec.tables * row_dim), dtype=table.dtype, device=device)
     if want_indices and out_indices is None:
-        out_indices = torch.empty((T, spec.tables), dtype=torch.int32, device=table.device)
+        out_indices = torch.empty((T, spec.tables), dtype=torch.int32, device=device)
     args = _HashGatherArgs(_ptr(token_ids), T, _ptr(seq_offsets), seq_offsets.numel() - 1, _ptr(compress_map),
                            vocab, vocab_c, _ptr(table), rows_total, row_dim, _DTYPES[table.dtype],
                            _ptr(out_indices), _ptr(out_rows), _ptr(err_word))
     cspec = spec._c()
-    _check(lib.engram_hash_gather(_c.byref(cspec), _c.byref(args), _stream(stream)), "engram_hash_gather")
+    fn = lib.engram_hash_gather_host if host_table else lib.engram_hash_gather
+    _check(fn(_c.byref(cspec), _c.byref(args), _stream(stream)), "engram_hash_gather")
     return out_rows, out_indices
 
 

@@ -258,12 +258,100 @@ __global__ void __launch_bounds__(kHashThreads) hash_gather_kernel(const __grid_
     if (tid == 0) bulk_wait_all();  // every store has completed before the CTA's shared memory goes away
 }
 
+// The same hash + gather with the table in page-locked host memory (NEXT-3: the paper's offload
+// of the tables to host memory, possible because the rows a token needs follow from its ids
+// alone).  Rows cross the host link with plain 16-byte loads through the table's device-mapped
+// address -- 8 threads per 128-byte row, kBatch vectors in flight per thread -- issued before the
+// next tile is hashed so that the link's latency overlaps the hashing; each tile's e_t rows are
+// then written to device memory in one contiguous block.
+constexpr int kBatch = 16;
+
+__global__ void __launch_bounds__(kHashThreads, 2) hash_gather_host_kernel(const __grid_constant__ HashGatherParams p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ TileIds st;
+
+    const int tid = threadIdx.x;
+    const int staged_entries = p.staged_seqs ? p.num_seqs + 1 : 0;
+    const HashSmemLayout L = hash_smem_layout(p.tile_tokens, p.tables, 0u, staged_entries);  // no tiles
+    int64_t *rows = reinterpret_cast<int64_t *>(smem + L.rows);
+    const int64_t ntiles = (p.T + p.tile_tokens - 1) / p.tile_tokens;
+    const uint32_t vpr = p.row_bytes / 16;                       // 16-byte vectors per table row
+    const uint32_t vpt = vpr * static_cast<uint32_t>(p.tables);  // per token (one e_t row)
+
+    const int64_t *offs = p.seq_offsets;
+    if (p.staged_seqs) {
+        int64_t *so = reinterpret_cast<int64_t *>(smem + L.offs);
+        for (int s = tid; s <= p.num_seqs; s += kHashThreads) so[s] = p.seq_offsets[s];
+        offs = so;
+    }
+    __syncthreads();
+    if (blockIdx.x == 0) {
+        for (int s = tid; s <= p.num_seqs; s += kHashThreads) {
+            const int64_t o = offs[s];
+            bool bad = (s == 0 && o != 0) || (s == p.num_seqs && o != p.T) || o < 0 || o > p.T;
+            if (s > 0 && offs[s - 1] > o) bad = true;
+            if (bad) report(p.status, p.err_word, ENGRAM_DEVERR_SEQ_OFFSETS);
+        }
+    }
+
+    int64_t tile = blockIdx.x;
+    if (tile < ntiles) {
+        tile_ids(p, offs, st, 0, tile, tid);
+        __syncthreads();
+        tile_hash(p, st, rows, 0, tile, tid);
+    }
+    __syncthreads();
+
+    for (int b = 0; tile < ntiles; tile += gridDim.x, b ^= 1) {
+        const int64_t t0 = tile * p.tile_tokens;
+        const int ntok = static_cast<int>(p.T - t0 < p.tile_tokens ? p.T - t0 : p.tile_tokens);
+        const int64_t next = tile + gridDim.x;
+        const uint32_t total = p.out_rows ? static_cast<uint32_t>(ntok) * vpt : 0u;
+        uint8_t *dst = p.out_rows + static_cast<size_t>(t0) * vpt * 16;
+        const int64_t *r = rows + static_cast<size_t>(b) * p.tile_tokens * p.tables;
+
+        for (uint32_t base = 0; base < total || base == 0; base += kHashThreads * kBatch) {
+            uint4 buf[kBatch];
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                const uint32_t e = base + k * kHashThreads + tid;
+                if (e < total) {
+                    const uint32_t i = e / vpt;
+                    const uint32_t rr = e - i * vpt;
+                    const uint32_t tb = rr / vpr;
+                    const uint32_t piece = rr - tb * vpr;
+                    buf[k] = *reinterpret_cast<const uint4 *>(
+                        p.table + static_cast<size_t>(r[i * p.tables + tb]) * p.row_bytes + piece * 16);
+                }
+            }
+            if (base == 0) {  // hash the next tile while the first batch crosses the link
+                if (next < ntiles) tile_ids(p, offs, st, b ^ 1, next, tid);
+                __syncthreads();
+                if (next < ntiles) tile_hash(p, st, rows, b ^ 1, next, tid);
+            }
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                const uint32_t e = base + k * kHashThreads + tid;
+                if (e < total) st_global_v4(dst + static_cast<size_t>(e) * 16, buf[k]);
+            }
+            if (total == 0) break;
+        }
+        __syncthreads();  // rows[b] is rewritten two tiles from now; rows[b ^ 1] is complete
+    }
+}
+
 }  // namespace engram
 
 using namespace engram;
 
-extern "C" engram_status engram_hash_gather(const engram_hash_spec *spec, const engram_hash_gather_args *a,
-                                            engram_stream_t stream) {
+namespace {
+
+// Host-side checks and kernel parameters shared by both entry points.  `host_table` selects a
+// page-locked host table (whose device-mapped address replaces a->table in the parameters).
+engram_status prepare_hash_gather(const engram_hash_spec *spec, const engram_hash_gather_args *a, bool host_table,
+                                  HashGatherParams *pp, DeviceInfo *devp) {
+    HashGatherParams &p = *pp;
+    DeviceInfo &dev = *devp;
     if (!spec || !a) return fail(ENGRAM_ERR_NULL, "engram_hash_gather: NULL argument");
     if (!spec->multipliers || !spec->primes) return fail(ENGRAM_ERR_NULL, "engram_hash_gather: NULL spec array");
     // token_ids and the outputs may be NULL only when there is no token.
@@ -292,7 +380,7 @@ extern "C" engram_status engram_hash_gather(const engram_hash_spec *spec, const 
     if (!aligned16(a->table) || (a->out_rows && !aligned16(a->out_rows)) || !aligned16(a->seq_offsets))
         return fail(ENGRAM_ERR_ALIGN, "engram_hash_gather: table, out_rows or seq_offsets not 16-byte aligned");
 
-    HashGatherParams p{};
+    p = HashGatherParams{};
     int64_t sum = 0;
     for (int tb = 0; tb < tables; ++tb) {
         const uint64_t pr = spec->primes[tb];
@@ -309,20 +397,38 @@ extern "C" engram_status engram_hash_gather(const engram_hash_spec *spec, const 
         return fail(ENGRAM_ERR_SHAPE, "engram_hash_gather: sum(primes) = %lld > table_rows = %lld", (long long)sum,
                     (long long)a->table_rows);
 
-    DeviceInfo dev;
     engram_status st = current_device(&dev);
     if (st != ENGRAM_OK) return st;
-    const void *ptrs[] = {a->token_ids, a->seq_offsets, a->compress_map, a->table, a->out_indices, a->out_rows,
-                          a->err_word};
+    const void *ptrs[] = {a->token_ids, a->seq_offsets, a->compress_map, host_table ? nullptr : a->table,
+                          a->out_indices, a->out_rows, a->err_word};
     const char *names[] = {"token_ids", "seq_offsets", "compress_map", "table", "out_indices", "out_rows",
                            "err_word"};
     for (int i = 0; i < 7; ++i)
         if ((st = check_device_ptr(ptrs[i], dev.device, names[i])) != ENGRAM_OK) return st;
+    const void *table = a->table;
+    if (host_table) {
+        // Only page-locked host memory registered with CUDA is read (checked at every validation
+        // level: pageable memory must never reach the kernel); then its device-side address.
+        cudaPointerAttributes attr;
+        cudaError_t e = cudaPointerGetAttributes(&attr, a->table);
+        if (e != cudaSuccess || attr.type != cudaMemoryTypeHost) {
+            cudaGetLastError();
+            return fail(ENGRAM_ERR_DEVICE, "engram_hash_gather_host: table is not page-locked host memory");
+        }
+        void *dptr = nullptr;
+        e = cudaHostGetDevicePointer(&dptr, const_cast<void *>(a->table), 0);
+        if (e != cudaSuccess || !dptr) {
+            cudaGetLastError();
+            return fail(ENGRAM_ERR_DEVICE, "engram_hash_gather_host: table is not page-locked, mapped host memory (%s)",
+                        cudaGetErrorString(e));
+        }
+        table = dptr;
+    }
 
     p.ids = a->token_ids;
     p.seq_offsets = a->seq_offsets;
     p.cmap = a->compress_map;
-    p.table = static_cast<const uint8_t *>(a->table);
+    p.table = static_cast<const uint8_t *>(table);
     p.out_rows = static_cast<uint8_t *>(a->out_rows);
     p.out_idx = a->out_indices;
     p.err_word = a->err_word;
@@ -335,6 +441,19 @@ extern "C" engram_status engram_hash_gather(const engram_hash_spec *spec, const 
     p.max_order = max_order;
     p.row_bytes = static_cast<uint32_t>(row_bytes);
 
+    return ENGRAM_OK;
+}
+
+}  // namespace
+
+extern "C" engram_status engram_hash_gather(const engram_hash_spec *spec, const engram_hash_gather_args *a,
+                                            engram_stream_t stream) {
+    HashGatherParams p;
+    DeviceInfo dev;
+    engram_status st = prepare_hash_gather(spec, a, false, &p, &dev);
+    if (st != ENGRAM_OK) return st;
+    const int tables = p.tables;
+    const int64_t row_bytes = p.row_bytes;
     // Tile of ~kTileBytes of e_t rows; persistent grid of as many CTAs as fit at once
     // (>= 1: T = 0 still checks the offsets).
     const int et_bytes = static_cast<int>(row_bytes) * tables;
@@ -354,4 +473,28 @@ extern "C" engram_status engram_hash_gather(const engram_hash_spec *spec, const 
     grid = cap_grid(grid);
     hash_gather_kernel<<<static_cast<unsigned>(grid), kHashThreads, dyn, reinterpret_cast<cudaStream_t>(stream)>>>(p);
     return check_launch("engram_hash_gather");
+}
+
+extern "C" engram_status engram_hash_gather_host(const engram_hash_spec *spec, const engram_hash_gather_args *a,
+                                                 engram_stream_t stream) {
+    HashGatherParams p;
+    DeviceInfo dev;
+    engram_status st = prepare_hash_gather(spec, a, true, &p, &dev);
+    if (st != ENGRAM_OK) return st;
+    // Tiles of kTileMax tokens (the e_t rows go through registers, not shared memory); persistent grid.
+    p.tile_tokens = kTileMax;
+    p.staged_seqs = a->num_seqs + 1 <= kSmemSeqs ? 1 : 0;
+    const HashSmemLayout L = hash_smem_layout(p.tile_tokens, p.tables, 0u, p.staged_seqs ? a->num_seqs + 1 : 0);
+    const int dyn = static_cast<int>(L.total);
+    if ((st = set_smem(reinterpret_cast<const void *>(hash_gather_host_kernel), dyn)) != ENGRAM_OK) return st;
+    int per_sm = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, hash_gather_host_kernel, kHashThreads, dyn);
+    if (e != cudaSuccess) return fail(ENGRAM_ERR_CUDA, "engram_hash_gather_host occupancy: %s", cudaGetErrorString(e));
+    const int64_t ntiles = (a->T + p.tile_tokens - 1) / p.tile_tokens;
+    int64_t grid = static_cast<int64_t>(dev.num_sms) * std::max(per_sm, 1);
+    if (grid > ntiles) grid = ntiles;
+    grid = cap_grid(grid);
+    hash_gather_host_kernel<<<static_cast<unsigned>(grid), kHashThreads, dyn,
+                              reinterpret_cast<cudaStream_t>(stream)>>>(p);
+    return check_launch("engram_hash_gather_host");
 }

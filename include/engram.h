@@ -182,6 +182,17 @@ typedef struct {
 engram_status engram_hash_gather(const engram_hash_spec *spec, const engram_hash_gather_args *args,
                                  engram_stream_t stream);
 
+/*
+ * The same computation with the table in HOST memory (the Engram paper's offload of the tables,
+ * possible because a token's rows follow from its ids alone; ch. 34 sec. 2.3).  args->table must
+ * be page-locked and mapped into the device's address space (cudaHostAlloc, or cudaHostRegister
+ * with cudaHostRegisterMapped; torch's pin_memory() qualifies): anything else returns
+ * ENGRAM_ERR_DEVICE.  Every other pointer is device memory as above.  Rows cross the host link
+ * with ordinary loads, so the call's speed is set by that link, not by HBM.
+ */
+engram_status engram_hash_gather_host(const engram_hash_spec *spec, const engram_hash_gather_args *args,
+                                      engram_stream_t stream);
+
 /* ------------------------------------------------------------------------- */
 /* B0: weight fold  (ch. 34 sec. 3.1, sec. 4.1)                               */
 /* ------------------------------------------------------------------------- */

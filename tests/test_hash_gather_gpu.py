@@ -183,3 +183,39 @@ def test_indices_are_reproducible_across_grids():
             assert torch.equal(idx, base)
     finally:
         ecm.set_max_ctas(0)
+
+
+# ----------------------------------------------------------------------------- tables in host memory
+
+@pytest.mark.parametrize("lengths,row_dim,dtype", [([64], 16, "f32"), ([31, 1, 0, 100], 64, "bf16"),
+                                                   ([4096] * 4, 64, "bf16")])
+def test_host_resident_table_bit_exact(lengths, row_dim, dtype):
+    T = int(sum(lengths))
+    ids = G.uniform_int(T + 11, T, 0, 2000)
+    cmap = G.surjection(8, 2000, 1500)
+    w = _custom(ids, lengths, 2, 2, 8, row_dim, dtype, cmap=cmap, vocab=2000, seed=T + 1, anchor=20011)
+    dev_table = SD.hash_table(w, DEV)
+    host_table = dev_table.cpu().pin_memory()
+    rows_h, idx_h = _run(w, host_table)
+    rows_d, idx_d = _run(w, dev_table)
+    assert torch.equal(idx_h, idx_d) and torch.equal(rows_h, rows_d)
+    _check(w, dev_table, rows_h, idx_h)
+
+
+def test_host_table_must_be_pinned():
+    w = W.tiny_hash()
+    table = torch.from_numpy(w.table_host.copy())  # pageable
+    with pytest.raises(ValueError):
+        _run(w, table)
+    lib = ecm.load_library()
+    from engram_conditional_memory_gb300.binding import _HashGatherArgs
+    s = w.spec
+    spec = ecm.HashSpec(s.min_order, s.num_orders, s.heads, s.multipliers, s.primes)
+    ids = torch.from_numpy(w.token_ids).to(DEV)
+    offs = torch.from_numpy(w.seq_offsets).to(DEV)
+    out = torch.empty((w.T, 4 * 16), dtype=torch.float32, device=DEV)
+    import ctypes
+    args = _HashGatherArgs(ids.data_ptr(), w.T, offs.data_ptr(), 1, None, w.vocab, w.vocab, table.data_ptr(),
+                           table.shape[0], 16, 0, None, out.data_ptr(), None)
+    cspec = spec._c()
+    assert lib.engram_hash_gather_host(ctypes.byref(cspec), ctypes.byref(args), None) == 7  # ENGRAM_ERR_DEVICE
