@@ -58,7 +58,12 @@ def _load():
                                            _p, _p, _p, _p, _p]
             lib.eo_gate_hc_bwd.argtypes = [_p, _p, _p, ctypes.c_int, _p, _p, _i64, _i32, _i32, _f64, _f64, _i64,
                                            _i64, _p, _p, _p, _p]
-            for f in ("eo_hash_indices", "eo_gather_rows", "eo_fuse_weight", "eo_gate_fwd", "eo_gate_bwd",
+            lib.eo_sinkhorn_momentum.argtypes = [_p, ctypes.c_int, _p, _i64, _f64, ctypes.c_int, _p, _p]
+            lib.eo_sinkhorn_step.argtypes = [_p, _p, _p, _i64, _i32, _f64, _i64, _i64, _p, _p, _p]
+            lib.eo_sinkhorn_col_update.argtypes = [_p, _p, _i32, _f64, _p]
+            lib.eo_sinkhorn_finalize.argtypes = [_p, _p, _p, _i64, _i32, _f64, _f64, _p]
+            for f in ("eo_sinkhorn_momentum", "eo_sinkhorn_step", "eo_sinkhorn_col_update", "eo_sinkhorn_finalize",
+                      "eo_hash_indices", "eo_gather_rows", "eo_fuse_weight", "eo_gate_fwd", "eo_gate_bwd",
                       "eo_grad_w_reduce", "eo_gate_hc_fwd", "eo_gate_hc_bwd"):
                 getattr(lib, f).restype = ctypes.c_int
             _lib = lib
@@ -224,3 +229,52 @@ def gate_hc_bwd(dout, x, kv, w_h, w_k, eps: float, clamp: float, t_begin: int = 
                             _ptr(res["dweight_abs"]))
     _check(rc, "gate_hc_bwd")
     return res
+
+
+def sinkhorn_momentum(grad, momentum, beta1: float, nesterov: bool) -> dict:
+    """m' = beta1 m + g; input = g + beta1 m' (nesterov) or m' -> fp64 {"momentum", "input"}."""
+    lib = _load()
+    g = np.ascontiguousarray(grad)
+    m = np.ascontiguousarray(momentum, dtype=np.float32)
+    n = g.size
+    out = {"momentum": np.zeros(n, dtype=np.float64), "input": np.zeros(n, dtype=np.float64)}
+    rc = lib.eo_sinkhorn_momentum(_ptr(g), _dtype_code(g), _ptr(m), n, float(beta1), int(bool(nesterov)),
+                                  _ptr(out["momentum"]), _ptr(out["input"]))
+    _check(rc, "sinkhorn_momentum")
+    return {k: v.reshape(g.shape) for k, v in out.items()}
+
+
+def sinkhorn_step(matrix, row_scale, col_scale, eps: float, r_begin: int = 0, r_end: int | None = None) -> dict:
+    """Row step over rows [r_begin, r_end): fp64 row_norm, row_scale [n] and col_sumsq [head_dim]."""
+    lib = _load()
+    mat = np.ascontiguousarray(matrix, dtype=np.float32)
+    rs = np.ascontiguousarray(row_scale, dtype=np.float32)
+    cs = np.ascontiguousarray(col_scale, dtype=np.float32)
+    R, D = mat.shape
+    r_end = R if r_end is None else r_end
+    out = {"row_norm": np.zeros(r_end - r_begin), "row_scale": np.zeros(r_end - r_begin), "col_sumsq": np.zeros(D)}
+    rc = lib.eo_sinkhorn_step(_ptr(mat), _ptr(rs), _ptr(cs), R, D, float(eps), r_begin, r_end, _ptr(out["row_norm"]),
+                              _ptr(out["row_scale"]), _ptr(out["col_sumsq"]))
+    _check(rc, "sinkhorn_step")
+    return out
+
+
+def sinkhorn_col_update(col_sumsq, col_scale, eps: float) -> np.ndarray:
+    lib = _load()
+    s = np.ascontiguousarray(col_sumsq, dtype=np.float64)
+    cs = np.ascontiguousarray(col_scale, dtype=np.float32)
+    out = np.zeros(cs.size)
+    _check(lib.eo_sinkhorn_col_update(_ptr(s), _ptr(cs), cs.size, float(eps), _ptr(out)), "sinkhorn_col_update")
+    return out
+
+
+def sinkhorn_finalize(matrix, row_scale, col_scale, eps: float, alpha: float) -> np.ndarray:
+    lib = _load()
+    mat = np.ascontiguousarray(matrix, dtype=np.float32)
+    rs = np.ascontiguousarray(row_scale, dtype=np.float32)
+    cs = np.ascontiguousarray(col_scale, dtype=np.float32)
+    R, D = mat.shape
+    out = np.zeros((R, D))
+    rc = lib.eo_sinkhorn_finalize(_ptr(mat), _ptr(rs), _ptr(cs), R, D, float(eps), float(alpha), _ptr(out))
+    _check(rc, "sinkhorn_finalize")
+    return out

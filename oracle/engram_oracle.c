@@ -29,6 +29,8 @@
  *   NEXT-1 (the multi-branch production gate of the TileKernels release): T34 sec. 2.1
  *   (x [T, hc, d], kv [T, hc+1, d], the signed-sqrt + clamp activation, out = x + alpha v),
  *   sec. 3.2 (forward) and sec. 4.2 (backward, including the zero-gradient clamp branch).
+ *   NEXT-4 (the Engram Sinkhorn of the TileKernels release): T34 sec. 5.3 -- momentum update,
+ *   the row step with its column partial sums, the ordered reduction, finalize.
  *
  * Readings where the pages leave a step open (each one is also listed in the
  * design notes):
@@ -482,6 +484,102 @@ int eo_gate_hc_bwd(const void *g, const void *x, const void *kv, int dtype, cons
                     dweight_abs[(int64_t)h * d + i] += fabs(c * xi * ki);
             }
         }
+    }
+    return EO_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* NEXT-4: the Engram Sinkhorn (row / column L2 scaling)  [T34 sec. 5.3]      */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * Momentum update (the momentum form of T34 sec. 5.3 step 1; the exact update is this
+ * library's reading): m <- beta1 * m + g;  input = nesterov ? g + beta1 * m : m.
+ * grad is fp32 or bf16 [n], momentum_in fp32 [n]; outputs are fp64 [n].
+ */
+int eo_sinkhorn_momentum(const void *grad, int dtype, const float *momentum_in, int64_t n, double beta1,
+                         int nesterov, double *momentum_out, double *input_out)
+{
+    if (!grad || !momentum_in || !momentum_out || !input_out || n < 0 || (dtype != EO_F32 && dtype != EO_BF16))
+        return EO_ERR_ARG;
+    for (int64_t i = 0; i < n; ++i) {
+        const double g = eo_load(grad, dtype, i);
+        const double m = beta1 * (double)momentum_in[i] + g;
+        momentum_out[i] = m;
+        input_out[i] = nesterov ? g + beta1 * m : m;
+    }
+    return EO_OK;
+}
+
+/*
+ * The row step (T34 sec. 5.3 step 2), for rows [r_begin, r_end) of a [rows, head_dim] matrix:
+ *     x          = row_scale[r] * matrix[r, :] (*) col_scale
+ *     row_norm   = ||x||_2
+ *     row_scale' = row_scale[r] / (row_norm + eps)
+ *     col_sumsq += (x / (row_norm + eps))^2         (column-wise, rows in ascending order)
+ * Outputs indexed from r_begin (row_norm, row_scale_out [n]); col_sumsq [head_dim] is overwritten.
+ */
+int eo_sinkhorn_step(const float *matrix, const float *row_scale, const float *col_scale, int64_t rows,
+                     int32_t head_dim, double eps, int64_t r_begin, int64_t r_end,
+                     double *row_norm, double *row_scale_out, double *col_sumsq)
+{
+    if (!matrix || !row_scale || !col_scale || !row_norm || !row_scale_out || !col_sumsq)
+        return EO_ERR_ARG;
+    if (head_dim <= 0 || r_begin < 0 || r_end > rows || r_begin > r_end)
+        return EO_ERR_ARG;
+    for (int32_t c = 0; c < head_dim; ++c)
+        col_sumsq[c] = 0.0;
+    for (int64_t r = r_begin; r < r_end; ++r) {
+        double ss = 0.0;
+        for (int32_t c = 0; c < head_dim; ++c) {
+            const double x = (double)row_scale[r] * (double)matrix[r * head_dim + c] * (double)col_scale[c];
+            ss += x * x;
+        }
+        const double nrm = sqrt(ss);
+        const double inv = 1.0 / (nrm + eps);
+        row_norm[r - r_begin] = nrm;
+        row_scale_out[r - r_begin] = (double)row_scale[r] * inv;
+        for (int32_t c = 0; c < head_dim; ++c) {
+            const double x = (double)row_scale[r] * (double)matrix[r * head_dim + c] * (double)col_scale[c] * inv;
+            col_sumsq[c] += x * x;
+        }
+    }
+    return EO_OK;
+}
+
+/*
+ * The column step that the caller of T34's step_reduce performs: the reduced column sums of squares
+ * give the column L2 norms, and col_scale' = col_scale / (sqrt(col_sumsq) + eps).
+ */
+int eo_sinkhorn_col_update(const double *col_sumsq, const float *col_scale, int32_t head_dim, double eps,
+                           double *col_scale_out)
+{
+    if (!col_sumsq || !col_scale || !col_scale_out || head_dim <= 0)
+        return EO_ERR_ARG;
+    for (int32_t c = 0; c < head_dim; ++c)
+        col_scale_out[c] = (double)col_scale[c] / (sqrt(col_sumsq[c]) + eps);
+    return EO_OK;
+}
+
+/*
+ * Finalize (T34 sec. 5.3 step 4): out[r, :] = alpha * x / (||x||_2 + eps), x = row_scale[r] * matrix[r, :]
+ * (*) col_scale.  out is [rows, head_dim] fp64.
+ */
+int eo_sinkhorn_finalize(const float *matrix, const float *row_scale, const float *col_scale, int64_t rows,
+                         int32_t head_dim, double eps, double alpha, double *out)
+{
+    if (!matrix || !row_scale || !col_scale || !out || head_dim <= 0 || rows < 0)
+        return EO_ERR_ARG;
+    for (int64_t r = 0; r < rows; ++r) {
+        double ss = 0.0;
+        for (int32_t c = 0; c < head_dim; ++c) {
+            const double x = (double)row_scale[r] * (double)matrix[r * head_dim + c] * (double)col_scale[c];
+            ss += x * x;
+        }
+        const double f = alpha / (sqrt(ss) + eps);
+        for (int32_t c = 0; c < head_dim; ++c)
+            out[r * head_dim + c] =
+                (double)row_scale[r] * (double)matrix[r * head_dim + c] * (double)col_scale[c] * f;
     }
     return EO_OK;
 }

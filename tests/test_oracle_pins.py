@@ -373,3 +373,84 @@ def test_gate_hc_finite_differences():
             assert abs(fd - grad[ix]) <= 1e-6 * max(1.0, abs(fd)), (name, ix)
             checked += 1
     assert checked >= 5
+
+
+# ----------------------------------------------------------------------------- the Engram Sinkhorn
+
+def test_sinkhorn_row_step_against_numpy_norms():
+    R, D, eps = 37, 50, 1e-6
+    m = G.normal(601, R * D).astype(np.float32).reshape(R, D)
+    ones_r, ones_c = np.ones(R, dtype=np.float32), np.ones(D, dtype=np.float32)
+    r = oracle.sinkhorn_step(m, ones_r, ones_c, eps)
+    norms = np.linalg.norm(m.astype(np.float64), axis=1)
+    np.testing.assert_allclose(r["row_norm"], norms, rtol=1e-13)
+    np.testing.assert_allclose(r["row_scale"], 1.0 / (norms + eps), rtol=1e-13)
+    unit = m.astype(np.float64) / (norms + eps)[:, None]
+    np.testing.assert_allclose(r["col_sumsq"], np.linalg.norm(unit, axis=0) ** 2, rtol=1e-12)
+    # scales enter as row_scale * m * col_scale: scaling m by 3 and row_scale by 1/3 changes nothing
+    rs = np.full(R, 1.0 / 3.0, dtype=np.float32)
+    r3 = oracle.sinkhorn_step((3 * m).astype(np.float32), rs, ones_c, eps)
+    np.testing.assert_allclose(r3["row_norm"], norms, rtol=1e-6)
+    # row ranges partition the column sums
+    a = oracle.sinkhorn_step(m, ones_r, ones_c, eps, 0, 20)
+    b = oracle.sinkhorn_step(m, ones_r, ones_c, eps, 20, R)
+    np.testing.assert_allclose(a["col_sumsq"] + b["col_sumsq"], r["col_sumsq"], rtol=1e-13)
+
+
+def _sinkhorn_iterate(m, steps, eps=1e-6):
+    R, D = m.shape
+    rs, cs = np.ones(R, dtype=np.float32), np.ones(D, dtype=np.float32)
+    col_l2 = None
+    for _ in range(steps):
+        st = oracle.sinkhorn_step(m, rs, cs, eps)
+        rs = st["row_scale"].astype(np.float32)
+        col_l2 = np.sqrt(st["col_sumsq"])                 # column norms seen before the column step
+        cs = oracle.sinkhorn_col_update(st["col_sumsq"], cs, eps).astype(np.float32)
+    it = rs[:, None].astype(np.float64) * m * cs[None, :]
+    return rs, cs, col_l2, np.linalg.norm(it, axis=1)     # row norms seen before finalize
+
+
+def test_sinkhorn_fixed_point_matches_the_printed_walkthrough():
+    with open(os.path.join(os.path.dirname(__file__), "golden", "sinkhorn_demo.json")) as f:
+        demo = json.load(f)
+    R, D, alpha = demo["rows"], demo["head_dim"], demo["alpha"]
+    m = np.abs(G.normal(602, R * D)).astype(np.float32).reshape(R, D) + 0.1
+    rs, cs, col_l2, row_l2 = _sinkhorn_iterate(m, 60)
+    fp = demo["fixed_point"]
+    np.testing.assert_allclose(col_l2, fp["col_l2_before_col_step"], rtol=1e-5)
+    np.testing.assert_allclose(row_l2, fp["row_l2_before_finalize"], rtol=1e-5)
+    # the pages' printed values lie next to the same fixed point (their run stopped at step 7)
+    assert np.allclose(demo["printed"]["col_l2_before_col_step_step7"], fp["col_l2_before_col_step"], atol=1e-3)
+    assert np.allclose(demo["printed"]["row_l2_before_finalize"], fp["row_l2_before_finalize"], atol=1e-3)
+    out = oracle.sinkhorn_finalize(m, rs, cs, 1e-6, alpha)
+    np.testing.assert_allclose(np.linalg.norm(out, axis=1), demo["printed"]["row_l2_after_finalize"], rtol=1e-5)
+    # after a row step every row of the iterate is a unit vector (up to eps)
+    st = oracle.sinkhorn_step(m, rs, cs, 1e-6)
+    it = st["row_scale"][:, None] * m * cs[None, :]
+    assert np.abs(np.linalg.norm(it, axis=1) - 1).max() < 1e-5
+
+
+def test_sinkhorn_momentum_closed_forms():
+    g = G.normal(603, 64).astype(np.float32)
+    m0 = np.zeros(64, dtype=np.float32)
+    plain = oracle.sinkhorn_momentum(g, m0, 0.9, False)
+    nest = oracle.sinkhorn_momentum(g, m0, 0.9, True)
+    np.testing.assert_array_equal(plain["momentum"], g.astype(np.float64))
+    np.testing.assert_array_equal(plain["input"], g.astype(np.float64))
+    np.testing.assert_allclose(nest["input"], 1.9 * g.astype(np.float64), rtol=1e-15)
+    m1 = plain["momentum"].astype(np.float32)
+    second = oracle.sinkhorn_momentum(g, m1, 0.5, False)
+    np.testing.assert_allclose(second["momentum"], 1.5 * g.astype(np.float64), rtol=1e-7)
+    zero_beta = oracle.sinkhorn_momentum(g, m1, 0.0, True)
+    np.testing.assert_array_equal(zero_beta["input"], g.astype(np.float64))
+
+
+def test_sinkhorn_nesterov_with_prior_momentum():
+    # m' = beta m0 + g and input = g + beta m' = (1 + beta) g + beta^2 m0: with m0 != 0 this tells the
+    # Nesterov look-ahead apart from m' + beta g, which agrees with it only when m0 = 0.
+    g = G.normal(604, 32).astype(np.float32)
+    m0 = G.normal(605, 32).astype(np.float32)
+    beta = 0.75
+    r = oracle.sinkhorn_momentum(g, m0, beta, True)
+    expect = (1 + beta) * g.astype(np.float64) + beta ** 2 * m0.astype(np.float64)
+    np.testing.assert_allclose(r["input"], expect, rtol=1e-14, atol=1e-15)
