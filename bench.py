@@ -23,6 +23,7 @@ from __future__ import annotations
 import argparse
 import datetime as _dt
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -512,6 +513,40 @@ def main_only(args, device):
 
             def launch():
                 ecm.gate_hc_fwd(x, kv, wf, wl.eps, wl.clamp, out=out, stats=st)
+    elif op.startswith("sinkhorn"):
+        # the Engram Sinkhorn on 16384 x 5120 fp32 (bf16 gradient): 335 MB per matrix, > L2
+        sw = W.sinkhorn_16k_x_5120()
+        R, D = sw.rows, sw.head_dim
+        grad = SD.normal_tensor((R, D), sw.seed + 1, 0.0, 1.0, "bf16", device)
+        mom = SD.normal_tensor((R, D), sw.seed + 2, 0.0, 0.5, "f32", device)
+        rs = torch.ones(R, dtype=torch.float32, device=device)
+        cs = torch.ones(D, dtype=torch.float32, device=device)
+        inp = ecm.sinkhorn_momentum_update(grad, mom, sw.beta1, sw.nesterov)
+        P = ecm.sinkhorn_num_partials(R, D)
+        nrm, part = ecm.sinkhorn_step(inp, rs, cs, sw.eps, P=P)
+        csum = ecm.sinkhorn_step_reduce(part, col_scale=cs, eps=sw.eps)
+        out = ecm.sinkhorn_finalize(inp, rs, cs, sw.eps, math.sqrt(D))
+        b_mom = R * D * (2 + 4 + 4 + 4)
+        b_step = R * D * 4 + R * 12 + D * 4 + P * D * 4
+        b_red = P * D * 4 + 3 * D * 4
+        b_fin = 2 * R * D * 4 + R * 4 + D * 4
+        fns = {
+            "sinkhorn_momentum": (b_mom, lambda: ecm.sinkhorn_momentum_update(grad, mom, sw.beta1, sw.nesterov,
+                                                                               sinkhorn_input=inp)),
+            "sinkhorn_step": (b_step, lambda: ecm.sinkhorn_step(inp, rs, cs, sw.eps, P=P, row_norm=nrm,
+                                                                col_sumsq_partial=part)),
+            "sinkhorn_reduce": (b_red, lambda: ecm.sinkhorn_step_reduce(part, col_sumsq=csum, col_scale=cs,
+                                                                        eps=sw.eps)),
+            "sinkhorn_finalize": (b_fin, lambda: ecm.sinkhorn_finalize(inp, rs, cs, sw.eps, math.sqrt(D), out=out)),
+        }
+        if op == "sinkhorn":  # one optimizer pass: momentum, one row + column step, finalize
+            nbytes = b_mom + b_step + b_red + b_fin
+
+            def launch():
+                for k in ("sinkhorn_momentum", "sinkhorn_step", "sinkhorn_reduce", "sinkhorn_finalize"):
+                    fns[k][1]()
+        else:
+            nbytes, launch = fns[op]
     else:
         wl = {"gate_fwd_2k": W.gate_fwd_2k()}.get(op, W.gate_train_4k())
         t = SD.gate_device_inputs(wl, device)
@@ -634,7 +669,9 @@ def main():
                     help="the step with the tables in host memory, prefetched on a side stream (vs in HBM)")
     ap.add_argument("--offload-ctas", type=int, default=32, help="CTAs of the host-table gather in --offload")
     ap.add_argument("--only", choices=["hash_gather", "hash_gather_small", "hash_gather_host", "gate_fwd",
-                                       "gate_fwd_2k", "gate_bwd", "grad_w_reduce", "gate_hc_fwd", "gate_hc_bwd"],
+                                       "gate_fwd_2k", "gate_bwd", "grad_w_reduce", "gate_hc_fwd", "gate_hc_bwd",
+                                       "sinkhorn", "sinkhorn_momentum", "sinkhorn_step", "sinkhorn_reduce",
+                                       "sinkhorn_finalize"],
                     help="time one kernel alone on its workload (consecutive launches, L2 not flushed)")
     args = ap.parse_args()
     if args.warmup < 3:

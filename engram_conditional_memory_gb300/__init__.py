@@ -29,4 +29,9 @@ from .binding import (  # noqa: F401
     read_error_word,
     set_max_ctas,
     set_validation,
+    sinkhorn_finalize,
+    sinkhorn_momentum_update,
+    sinkhorn_num_partials,
+    sinkhorn_step,
+    sinkhorn_step_reduce,
 )

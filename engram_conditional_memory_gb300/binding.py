@@ -86,6 +86,11 @@ def load_library():
                                         _p, _p, _i32, _p]),
             "engram_gate_bwd_reduce_noalloc": (st, [_p, _p, _p, _p, _c.c_int, _p, _p, _p, _p, _p, _i64, _i32, _p, _p,
                                                     _p, _p, _p, _p, _p, _p, _p]),
+            "engram_sinkhorn_momentum_update": (st, [_p, _c.c_int, _p, _p, _i64, _c.c_float, _i32, _p]),
+            "engram_sinkhorn_num_partials": (st, [_i64, _i32, _p]),
+            "engram_sinkhorn_step": (st, [_p, _p, _p, _i64, _i32, _c.c_float, _p, _p, _i32, _p]),
+            "engram_sinkhorn_step_reduce": (st, [_p, _i32, _i32, _p, _p, _c.c_float, _p]),
+            "engram_sinkhorn_finalize": (st, [_p, _p, _p, _i64, _i32, _c.c_float, _c.c_float, _p, _p]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)
@@ -298,6 +303,81 @@ def gate_hc_bwd(dout, x, kv, w_fused, gate, rstd_x, rstd_k, dot, clamp: float = 
                                   _ptr(dw_partial), P, _stream(stream)),
            "engram_gate_hc_bwd")
     return dx, dkv, dw_partial
+
+
+# ----------------------------------------------------------------------------- the Engram Sinkhorn
+
+
+def sinkhorn_momentum_update(grad, momentum, beta1: float, nesterov: bool, sinkhorn_input=None, stream=None):
+    """momentum = beta1 * momentum + grad (in place); returns the fp32 Sinkhorn input."""
+    lib = load_library()
+    _need(grad, "grad")
+    _need(momentum, "momentum", torch.float32)
+    if grad.shape != momentum.shape:
+        raise ValueError(f"grad {tuple(grad.shape)} and momentum {tuple(momentum.shape)} differ")
+    out = torch.empty_like(momentum) if sinkhorn_input is None else _need(sinkhorn_input, "sinkhorn_input",
+                                                                         torch.float32)
+    _check(lib.engram_sinkhorn_momentum_update(_ptr(grad), _DTYPES[grad.dtype], _ptr(momentum), _ptr(out),
+                                               momentum.numel(), float(beta1), int(bool(nesterov)), _stream(stream)),
+           "engram_sinkhorn_momentum_update")
+    return out
+
+
+def sinkhorn_num_partials(rows: int, head_dim: int) -> int:
+    lib = load_library()
+    P = _c.c_int32(0)
+    _check(lib.engram_sinkhorn_num_partials(rows, head_dim, _c.byref(P)), "engram_sinkhorn_num_partials")
+    return P.value
+
+
+def sinkhorn_step(matrix, row_scale, col_scale, eps: float = 1e-6, P: int | None = None, row_norm=None,
+                  col_sumsq_partial=None, want_row_norm: bool = True, stream=None):
+    """Row step (row_scale updated in place).  Returns (row_norm [rows] or None, col_sumsq_partial [P, head_dim])."""
+    lib = load_library()
+    _need(matrix, "matrix", torch.float32)
+    _need(row_scale, "row_scale", torch.float32)
+    _need(col_scale, "col_scale", torch.float32)
+    rows, D = matrix.shape
+    if P is None:
+        P = sinkhorn_num_partials(rows, D) if col_sumsq_partial is None else col_sumsq_partial.shape[0]
+    if row_norm is None and want_row_norm:
+        row_norm = torch.empty(rows, dtype=torch.float32, device=matrix.device)
+    if col_sumsq_partial is None:
+        col_sumsq_partial = torch.empty((P, D), dtype=torch.float32, device=matrix.device)
+    else:
+        _need(col_sumsq_partial, "col_sumsq_partial", torch.float32)
+    _check(lib.engram_sinkhorn_step(_ptr(matrix), _ptr(row_scale), _ptr(col_scale), rows, D, float(eps),
+                                    _ptr(row_norm), _ptr(col_sumsq_partial), P, _stream(stream)),
+           "engram_sinkhorn_step")
+    return row_norm, col_sumsq_partial
+
+
+def sinkhorn_step_reduce(col_sumsq_partial, col_sumsq=None, col_scale=None, eps: float = 1e-6,
+                         want_col_sumsq: bool = True, stream=None):
+    """Ordered reduction of the partials; with col_scale, also col_scale /= sqrt(col_sumsq) + eps in place."""
+    lib = load_library()
+    _need(col_sumsq_partial, "col_sumsq_partial", torch.float32)
+    P, D = col_sumsq_partial.shape
+    if col_sumsq is None and want_col_sumsq:
+        col_sumsq = torch.empty(D, dtype=torch.float32, device=col_sumsq_partial.device)
+    if col_scale is not None:
+        _need(col_scale, "col_scale", torch.float32)
+    _check(lib.engram_sinkhorn_step_reduce(_ptr(col_sumsq_partial), P, D, _ptr(col_sumsq), _ptr(col_scale), float(eps),
+                                           _stream(stream)),
+           "engram_sinkhorn_step_reduce")
+    return col_sumsq
+
+
+def sinkhorn_finalize(matrix, row_scale, col_scale, eps: float = 1e-6, alpha: float = 1.0, out=None, stream=None):
+    """out = alpha * x / (||x|| + eps) per row, x = row_scale * matrix * col_scale."""
+    lib = load_library()
+    _need(matrix, "matrix", torch.float32)
+    rows, D = matrix.shape
+    out = torch.empty_like(matrix) if out is None else _need(out, "out", torch.float32)
+    _check(lib.engram_sinkhorn_finalize(_ptr(matrix), _ptr(row_scale), _ptr(col_scale), rows, D, float(eps),
+                                        float(alpha), _ptr(out), _stream(stream)),
+           "engram_sinkhorn_finalize")
+    return out
 
 
 # ----------------------------------------------------------------------------- A0-A2

@@ -313,6 +313,65 @@ engram_status engram_gate_hc_bwd(const void *dout, const void *x, const void *kv
                                  engram_stream_t stream);
 
 /* ------------------------------------------------------------------------- */
+/* The Engram Sinkhorn of the TileKernels release: row / column L2 scaling of a  */
+/* [rows, head_dim] fp32 matrix  (ch. 34 sec. 5.3, the Engram version's four     */
+/* kernels)                                                                      */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * Momentum update, in place on momentum [n] fp32, with grad [n] fp32 or bf16:
+ *     m = beta1 * m + g;   sinkhorn_input = nesterov ? g + beta1 * m : m     (fp32 [n]).
+ * The pages name the arguments (grad, momentum, beta1, nesterov) and the fp32 result, not the
+ * update itself; this is the plain heavy-ball / Nesterov form.  sinkhorn_input may not alias
+ * momentum.  All three pointers 16-byte aligned device memory; n == 0 is a no-op.
+ */
+engram_status engram_sinkhorn_momentum_update(const void *grad, engram_dtype dtype, float *momentum,
+                                              float *sinkhorn_input, int64_t n, float beta1, int32_t nesterov,
+                                              engram_stream_t stream);
+
+/*
+ * The number of column partials the library recommends for `rows` rows: about 16 or more rows
+ * per partial and at most 1024 partials.  It depends on rows only, so the partials and their
+ * reduction are bitwise reproducible on any device.  Host only.
+ */
+engram_status engram_sinkhorn_num_partials(int64_t rows, int32_t head_dim, int32_t *P);
+
+/*
+ * The row step over matrix [rows, head_dim] fp32 (row-major), row_scale [rows] and
+ * col_scale [head_dim] fp32.  For each row r, with x = row_scale[r] * matrix[r, :] (*) col_scale:
+ *     row_norm[r]  = ||x||_2                                  (row_norm nullable)
+ *     row_scale[r] = row_scale[r] / (row_norm[r] + eps)       (in place)
+ * and the column partials
+ *     col_sumsq_partial[p, c] = sum over r in [p*C, min(rows, (p+1)*C)) of (x_c / (row_norm[r] + eps))^2,
+ * C = ceil(rows / P), rows in ascending order, a partial with no row 0.  col_sumsq_partial is
+ * [P, head_dim] fp32, P >= 1.  head_dim a multiple of 4 and at most 8192; matrix, col_scale and
+ * col_sumsq_partial 16-byte aligned.  Outputs may not alias the matrix or col_scale.
+ */
+engram_status engram_sinkhorn_step(const float *matrix, float *row_scale, const float *col_scale, int64_t rows,
+                                   int32_t head_dim, float eps, float *row_norm, float *col_sumsq_partial,
+                                   int32_t P, engram_stream_t stream);
+
+/*
+ * col_sumsq[c] = sum over p < P of col_sumsq_partial[p, c] in a fixed order that depends on P
+ * only (groups of ceil(P / 64) consecutive partials, each summed in ascending order, then the
+ * groups in ascending order).  col_sumsq [head_dim] is nullable; when col_scale [head_dim] is
+ * given, the column step of the alternating iteration is applied in place:
+ *     col_scale[c] = col_scale[c] / (sqrt(col_sumsq[c]) + eps).
+ * At least one of the two outputs must be given.  16-byte aligned device pointers.
+ */
+engram_status engram_sinkhorn_step_reduce(const float *col_sumsq_partial, int32_t P, int32_t head_dim,
+                                          float *col_sumsq, float *col_scale, float eps, engram_stream_t stream);
+
+/*
+ * out[r, :] = alpha * x / (||x||_2 + eps), x = row_scale[r] * matrix[r, :] (*) col_scale:
+ * out [rows, head_dim] fp32, not aliasing matrix.  Shape rules as for engram_sinkhorn_step;
+ * rows == 0 is a no-op.
+ */
+engram_status engram_sinkhorn_finalize(const float *matrix, const float *row_scale, const float *col_scale,
+                                       int64_t rows, int32_t head_dim, float eps, float alpha, float *out,
+                                       engram_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
 /* Allocation-free backward + reduction                                       */
 /* ------------------------------------------------------------------------- */
 

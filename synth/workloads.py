@@ -207,3 +207,36 @@ def gate_hc_host_inputs(w: GateHcWorkload):
 def gate_hc_4x4k(seed: int = 6) -> GateHcWorkload:
     """The production shape: 4 branches, T = 8192 tokens, d = 4096, bf16."""
     return GateHcWorkload(name="gate_hc4_T8192_d4096", T=8192, hc=4, d=4096, dtype="bf16", seed=seed * 101 + 13)
+
+
+@dataclass
+class SinkhornWorkload:
+    """The Engram Sinkhorn's inputs: a gradient and momentum of one [rows, head_dim] matrix."""
+
+    name: str
+    rows: int
+    head_dim: int
+    grad_dtype: str  # "f32" | "bf16"
+    seed: int
+    eps: float = 1e-6
+    beta1: float = 0.9
+    nesterov: bool = True
+
+
+def sinkhorn_host_inputs(w: SinkhornWorkload):
+    """grad [rows, head_dim] ~ N(0, 1) (fp32 or bf16 bits), momentum ~ N(0, 0.5) fp32, and
+    positive row / column scales ~ U(0.5, 2) fp32 (an iteration in progress)."""
+    n = w.rows * w.head_dim
+    g = G.normal(w.seed + 11, n).reshape(w.rows, w.head_dim)
+    return {
+        "grad": g.astype(np.float32) if w.grad_dtype == "f32" else G.to_bf16_bits(g),
+        "momentum": G.normal(w.seed + 12, n, 0.0, 0.5).astype(np.float32).reshape(w.rows, w.head_dim),
+        "row_scale": (0.5 + 1.5 * G.uniform01(w.seed + 13, w.rows)).astype(np.float32),
+        "col_scale": (0.5 + 1.5 * G.uniform01(w.seed + 14, w.head_dim)).astype(np.float32),
+    }
+
+
+def sinkhorn_16k_x_5120(seed: int = 7) -> SinkhornWorkload:
+    """16384 rows of head_dim 5120 (the largest head_dim the release's tests use): 335 MB fp32."""
+    return SinkhornWorkload(name="sinkhorn_R16384_D5120", rows=16384, head_dim=5120, grad_dtype="bf16",
+                            seed=seed * 101 + 17)

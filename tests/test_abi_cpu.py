@@ -119,3 +119,56 @@ def test_hash_gather_host_rejections(lib):
     args.token_ids = None
     args.out_rows = fake
     assert lib.engram_hash_gather(ctypes.byref(spec), ctypes.byref(args), None) == 1  # NULL ids with T > 0
+
+
+def test_sinkhorn_host_side_rejections(lib):
+    """Argument errors of the Sinkhorn calls are caught on the host, before any CUDA call."""
+    vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+    lib.engram_sinkhorn_step.restype = ctypes.c_int
+    lib.engram_sinkhorn_step.argtypes = [vp, vp, vp, i64, i32, f32, vp, vp, i32, vp]
+    lib.engram_sinkhorn_step_reduce.restype = ctypes.c_int
+    lib.engram_sinkhorn_step_reduce.argtypes = [vp, i32, i32, vp, vp, f32, vp]
+    lib.engram_sinkhorn_finalize.restype = ctypes.c_int
+    lib.engram_sinkhorn_finalize.argtypes = [vp, vp, vp, i64, i32, f32, f32, vp, vp]
+    lib.engram_sinkhorn_momentum_update.restype = ctypes.c_int
+    lib.engram_sinkhorn_momentum_update.argtypes = [vp, ctypes.c_int, vp, vp, i64, f32, i32, vp]
+    fake, odd = vp(0x10000), vp(0x10008)
+    step = lib.engram_sinkhorn_step
+    assert step(fake, fake, fake, 64, 130, 1e-6, None, fake, 4, None) == 4       # head_dim not a multiple of 4
+    assert step(fake, fake, fake, 64, 8196, 1e-6, None, fake, 4, None) == 2      # head_dim above 8192
+    assert step(fake, fake, fake, -1, 64, 1e-6, None, fake, 4, None) == 2
+    assert step(fake, fake, fake, 64, 64, 1e-6, None, fake, 0, None) == 2        # P = 0
+    assert step(None, fake, fake, 64, 64, 1e-6, None, fake, 4, None) == 1
+    assert step(fake, fake, fake, 64, 64, 1e-6, None, None, 4, None) == 1        # no partials
+    assert step(odd, fake, fake, 64, 64, 1e-6, None, fake, 4, None) == 4
+    red = lib.engram_sinkhorn_step_reduce
+    assert red(fake, 4, 64, None, None, 1e-6, None) == 1                         # neither output
+    assert red(fake, 0, 64, fake, None, 1e-6, None) == 2
+    assert red(fake, 4, 66, fake, None, 1e-6, None) == 4
+    assert red(fake, 4, 64, odd, None, 1e-6, None) == 4
+    fin = lib.engram_sinkhorn_finalize
+    assert fin(fake, fake, fake, 0, 64, 1e-6, 1.0, fake, None) == 0              # no row: nothing to do
+    assert fin(fake, fake, fake, 8, 64, 1e-6, 1.0, None, None) == 1
+    assert fin(fake, fake, fake, 8, 64, 1e-6, 1.0, fake, None) == 2              # out aliases matrix
+    mom = lib.engram_sinkhorn_momentum_update
+    assert mom(fake, 1, fake, vp(0x20000), 0, 0.9, 1, None) == 0                 # n = 0
+    assert mom(fake, 9, fake, vp(0x20000), 16, 0.9, 1, None) == 3                # dtype
+    assert mom(fake, 1, fake, fake, 16, 0.9, 1, None) == 2                       # input aliases momentum
+    assert mom(fake, 1, odd, vp(0x20000), 16, 0.9, 1, None) == 4
+    assert mom(None, 1, fake, vp(0x20000), 16, 0.9, 1, None) == 1
+
+
+def test_sinkhorn_partition_rule(lib):
+    lib.engram_sinkhorn_num_partials.restype = ctypes.c_int
+    lib.engram_sinkhorn_num_partials.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)]
+    P = ctypes.c_int32()
+
+    def parts(rows):
+        assert lib.engram_sinkhorn_num_partials(rows, 5120, ctypes.byref(P)) == 0
+        return P.value
+
+    assert parts(0) == 1 and parts(16) == 1 and parts(17) == 2 and parts(16384) == 1024 and parts(10**7) == 1024
+    for rows in (1, 15, 100, 8192, 16385, 10**6):
+        p = parts(rows)
+        chunk = -(-rows // p)
+        assert 1 <= p <= 1024 and (p - 1) * chunk < rows <= p * chunk
