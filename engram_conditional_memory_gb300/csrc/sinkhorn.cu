@@ -12,26 +12,33 @@
 //              with the row step, applied in the same pass.
 //   finalize:  out[r, :] = alpha * x / (||x|| + eps).
 //
-// GB300 design.  The row kernels stream whole rows through a ring of shared-memory stages filled
-// by 1-D bulk (TMA) copies that thread 0 issues; a CTA works on one row at a time with all of its
-// threads (as the pages' kernel does) while the next rows land.  A thread owns the float4 column
-// vectors tid, tid + 256, ... of every row, so the column accumulators and col_scale stay in
-// registers for the CTA's whole life.  One barrier per row carries the row norm's cross-warp
-// partials, the timeout consensus and the release of the stage.  Partial p holds rows
-// [p * C, min(rows, (p + 1) * C)), C = ceil(rows / P), summed in ascending order by whichever CTA
-// owns it, so the partials and the reduced columns are bitwise reproducible for any grid.
+// GB300 design.  The row kernels stream whole rows through a ring of shared-memory stages that a
+// producer warp fills with 1-D bulk (TMA) copies.  Two consumer groups of four warps take
+// alternate rows: a group works on one row at a time with all of its threads (as the pages' kernel
+// does with the whole CTA), and the two groups' per-row reduction chains overlap, which a single
+// row-at-a-time CTA cannot do.  A consumer thread owns the float4 column vectors gt, gt + 128, ...
+// (gt its index in the group) of every row, so col_scale and the column accumulators stay in
+// registers.  Each row costs one barrier of its group, which carries the row norm's cross-warp
+// partials and the timeout consensus; the stage is then released to the producer.  The producer
+// also delivers each row's row_scale next to its stage, so no consumer waits on a global load.
+//
+// Partial p holds rows [p * C, min(rows, (p + 1) * C)), C = ceil(rows / P).  Within a partial,
+// group 0 sums the rows of even offset and group 1 those of odd offset, each in ascending order,
+// and the partial is group 0's sum plus group 1's.  That order depends on rows and P only, so the
+// partials and the reduced columns are bitwise reproducible for any grid.
 #include <algorithm>
 
-#include "engram_internal.cuh"
+#include "gate_pipeline.cuh"
 
 namespace engram {
 
-constexpr int kSkThreads = 256;               // threads per CTA of the row kernels
-constexpr int kSkWarps = kSkThreads / 32;
-constexpr int kSkMaxVpt = 8;                  // float4 vectors per thread: head_dim <= 4 * 8 * 256
-constexpr int kSkMaxHeadDim = 4 * kSkMaxVpt * kSkThreads;
+constexpr int kSkGroupThreads = 128;                    // one consumer group: 4 warps
+constexpr int kSkGroupWarps = kSkGroupThreads / 32;
+constexpr int kSkConsumers = 2 * kSkGroupThreads;
+constexpr int kSkThreads = kSkConsumers + 32;           // + the producer warp
+constexpr int kSkMaxVpt = 16;                           // float4 vectors per thread: head_dim <= 4 * 16 * 128
+constexpr int kSkMaxHeadDim = 4 * kSkMaxVpt * kSkGroupThreads;
 constexpr int kSkMaxStages = 32;
-constexpr int kSkRingBytes = 192 * 1024;      // shared memory for the ring of row stages
 
 struct SinkhornParams {
     const float *matrix;
@@ -51,44 +58,122 @@ struct SinkhornParams {
     float alpha;
 };
 
-inline int sk_stages(int64_t row_bytes) {
-    const int64_t s = kSkRingBytes / row_bytes;
-    return static_cast<int>(s < 2 ? 2 : (s > kSkMaxStages ? kSkMaxStages : s));
+// Shared memory: ring [S][row] | exchange row (step only) | full [S] | empty [S] |
+// row_scale per stage [S] | row-norm partials [2 groups][2][4 warps].  S as large as fits.
+inline int sk_smem_bytes(int stages, int64_t row_bytes, bool exchange) {
+    return static_cast<int>(stages * row_bytes + (exchange ? row_bytes : 0)) + stages * 20 + 2 * 2 * kSkGroupWarps * 4;
 }
 
-// ring | full barriers [S] | row-norm partials [2][warps] | row_scale windows [2][threads]
-inline int sk_smem_bytes(int stages, int64_t row_bytes) {
-    return static_cast<int>(stages * row_bytes) + stages * 8 + 2 * kSkWarps * 4 + 2 * kSkThreads * 4;
+inline int sk_stages(int64_t row_bytes, bool exchange, int smem_limit) {
+    int s = kSkMaxStages;
+    while (s > 2 && sk_smem_bytes(s, row_bytes, exchange) > smem_limit) --s;
+    return s;
 }
 
-// The ring of row stages shared by the step and the finalize kernels.
-struct SkRing {
-    uint8_t *stages;
+struct SkShared {
+    uint8_t *ring;
+    float4 *xrow;      // the step's exchange row for combining the two groups' partial sums
     uint64_t *full;
+    uint64_t *empty;
+    float *rs;         // row_scale of the row in each stage, written by the producer
     float *red;
-    float *rsw;
     uint32_t row_bytes;
     int S;
-    uint64_t pol;
+};
 
-    // Thread 0 only: copy one row into the stage of the CTA's j-th row and arm its barrier.
-    __device__ __forceinline__ void issue(int64_t j, const float *src) const {
-        uint64_t *bar = &full[j % S];
-        mbar_arrive_expect_tx(bar, row_bytes);
-        bulk_load(stages + static_cast<size_t>(j % S) * row_bytes, src, row_bytes, bar, pol);
+__device__ __forceinline__ SkShared sk_carve(uint8_t *smem, const SinkhornParams &p, bool exchange) {
+    SkShared sh;
+    sh.row_bytes = static_cast<uint32_t>(p.d) * 4u;
+    sh.S = p.stages;
+    sh.ring = smem;
+    uint8_t *q = smem + static_cast<size_t>(sh.S) * sh.row_bytes;
+    sh.xrow = reinterpret_cast<float4 *>(q);
+    if (exchange) q += sh.row_bytes;
+    sh.full = reinterpret_cast<uint64_t *>(q);
+    sh.empty = sh.full + sh.S;
+    sh.rs = reinterpret_cast<float *>(sh.empty + sh.S);
+    sh.red = sh.rs + sh.S;
+    return sh;
+}
+
+// The producer warp: copies the CTA's n rows in order into the ring.  They start at row `first`
+// and come in runs of run_rows consecutive rows, a run's end `gap` rows before the next run's
+// start, so each row's address advances without a division.  The lanes also load row_scale for
+// the rows, 32 at a time and one batch ahead (row_of maps the CTA's q-th row to its matrix row),
+// and lane 0 parks each row's value next to its stage before arming the stage's barrier, whose
+// completion publishes it.  A stage is refilled once the consumer group that read it has
+// released it.  Before returning, lane 0 waits (bounded) for its copies still in flight, so none
+// lands after the CTA has exited.
+template <typename RowOf>
+__device__ __forceinline__ void sk_produce(const SkShared &sh, const SinkhornParams &p, int64_t n, int64_t first,
+                                           int64_t run_rows, int64_t gap, RowOf row_of) {
+    const int lane = threadIdx.x & 31;
+    const uint64_t pol = l2_evict_first_policy();
+    const float *src = p.matrix + static_cast<size_t>(first) * p.d;
+    int64_t left = run_rows, q = 0;
+    int stage = 0;
+    uint32_t round = 0;
+    float rs_batch = 0.f, rs_next = lane < n ? p.row_scale_in[row_of(lane)] : 0.f;
+    for (; q < n; ++q) {
+        const int slot = static_cast<int>(q & 31);
+        if (slot == 0) {
+            rs_batch = rs_next;
+            const int64_t qn = q + 32 + lane;
+            rs_next = qn < n ? p.row_scale_in[row_of(qn)] : 0.f;
+        }
+        const bool ok = __all_sync(0xffffffffu, round == 0 || mbar_wait(&sh.empty[stage], (round - 1) & 1u));
+        if (!ok) {
+            if (lane == 0) report(p.status, nullptr, ENGRAM_DEVERR_TIMEOUT);
+            break;
+        }
+        const float rs = __shfl_sync(0xffffffffu, rs_batch, slot);
+        if (lane == 0) {
+            sh.rs[stage] = rs;
+            mbar_arrive_expect_tx(&sh.full[stage], sh.row_bytes);
+            bulk_load(sh.ring + static_cast<size_t>(stage) * sh.row_bytes, src, sh.row_bytes, &sh.full[stage], pol);
+        }
+        src += p.d;
+        if (--left == 0) {
+            src += gap * p.d;
+            left = run_rows;
+        }
+        if (++stage == sh.S) {
+            stage = 0;
+            ++round;
+        }
+    }
+    if (lane == 0)
+        for (int64_t k = q > sh.S ? q - sh.S : 0; k < q; ++k)
+            if (!mbar_wait(&sh.full[k % sh.S], static_cast<uint32_t>((k / sh.S) & 1)))
+                report(p.status, nullptr, ENGRAM_DEVERR_TIMEOUT);
+}
+
+// A consumer group's position in the ring: the stage and phase of the CTA's j-th row, moved
+// forward by small steps.
+struct SkSlot {
+    int64_t j;
+    int s;
+    uint32_t phase;
+    __device__ __forceinline__ void move_to(int64_t target, int S) {
+        s += static_cast<int>(target - j);
+        j = target;
+        while (s >= S) {
+            s -= S;
+            phase ^= 1u;
+        }
     }
 };
 
 // Loads stage s into x[] (scaled by rs and the column scales) and returns this thread's sum of
 // squares; x is zero where the thread has no column or the wait failed.
 template <int VPT>
-__device__ __forceinline__ float sk_load_row(const SkRing &ring, int s, float rs, const float4 (&cs)[VPT], int d4,
-                                             bool ok, float4 (&x)[VPT]) {
-    const uint8_t *src = ring.stages + static_cast<size_t>(s) * ring.row_bytes;
+__device__ __forceinline__ float sk_load_row(const SkShared &sh, int s, int gt, float rs, const float4 (&cs)[VPT],
+                                             int d4, bool ok, float4 (&x)[VPT]) {
+    const uint8_t *src = sh.ring + static_cast<size_t>(s) * sh.row_bytes;
     float ss = 0.f;
 #pragma unroll
     for (int m = 0; m < VPT; ++m) {
-        const int jj = threadIdx.x + m * kSkThreads;
+        const int jj = gt + m * kSkGroupThreads;
         if (ok && jj < d4) {
             const uint4 u = ld_shared_v4(src + static_cast<size_t>(jj) * 16);
             x[m] = make_float4(__uint_as_float(u.x) * rs * cs[m].x, __uint_as_float(u.y) * rs * cs[m].y,
@@ -96,47 +181,33 @@ __device__ __forceinline__ float sk_load_row(const SkRing &ring, int s, float rs
         } else {
             x[m] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        ss = fmaf(x[m].x, x[m].x, fmaf(x[m].y, x[m].y, fmaf(x[m].z, x[m].z, fmaf(x[m].w, x[m].w, ss))));
+        ss += fmaf(x[m].x, x[m].x, x[m].y * x[m].y) + fmaf(x[m].z, x[m].z, x[m].w * x[m].w);
     }
     return ss;
 }
 
-// Common prologue of the row kernels: carve shared memory, initialise the barriers, issue the
-// first stages (thread 0) and load the column scales.
-template <int VPT, typename RowOf>
-__device__ __forceinline__ SkRing sk_prologue(const SinkhornParams &p, uint8_t *smem, int64_t n_my, RowOf row_of,
-                                              float4 (&cs)[VPT], int64_t *issued) {
-    SkRing ring;
-    ring.row_bytes = static_cast<uint32_t>(p.d) * 4u;
-    ring.S = p.stages;
-    ring.stages = smem;
-    ring.full = reinterpret_cast<uint64_t *>(smem + static_cast<size_t>(ring.S) * ring.row_bytes);
-    ring.red = reinterpret_cast<float *>(ring.full + ring.S);
-    ring.rsw = ring.red + 2 * kSkWarps;
-    ring.pol = l2_evict_first_policy();
-    *issued = 0;
-    if (threadIdx.x == 0) {
-        for (int q = 0; q < ring.S; ++q) mbar_init(&ring.full[q], 1);
-        mbar_init_fence();
-        for (; *issued < ring.S && *issued < n_my; ++*issued)
-            ring.issue(*issued, p.matrix + static_cast<size_t>(row_of(*issued)) * p.d);
-    }
-    const int d4 = p.d >> 2;
+// The group-wide sum of the per-thread values, after the group barrier `id` (which also ORs the
+// threads' failure flags).  Returns false when a thread of the group failed.
+__device__ __forceinline__ bool sk_group_total(const SkShared &sh, int g, int gw, int lane, int parity, float ss,
+                                               bool ok, float *total) {
+    ss = warp_sum(ss);
+    float *red = sh.red + (g * 2 + parity) * kSkGroupWarps;
+    if (lane == 0) red[gw] = ss;
+    if (named_sync_or(1 + g, kSkGroupThreads, !ok)) return false;
+    float t = 0.f;
 #pragma unroll
-    for (int m = 0; m < VPT; ++m) {
-        const int jj = threadIdx.x + m * kSkThreads;
-        cs[m] = jj < d4 ? __ldg(reinterpret_cast<const float4 *>(p.col_scale) + jj) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    return ring;
+    for (int q = 0; q < kSkGroupWarps; ++q) t += red[q];
+    *total = t;
+    return true;
 }
 
-// Thread 0 waits (bounded) for the copies it issued that nobody consumed, so that no bulk copy
-// lands in shared memory after the CTA has exited.
-__device__ __forceinline__ void sk_drain(const SkRing &ring, int64_t consumed, int64_t issued, uint32_t *status) {
-    if (threadIdx.x != 0) return;
-    for (int64_t q = consumed; q < issued; ++q)
-        if (!mbar_wait(&ring.full[q % ring.S], static_cast<uint32_t>((q / ring.S) & 1)))
-            report(status, nullptr, ENGRAM_DEVERR_TIMEOUT);
+template <int VPT>
+__device__ __forceinline__ void sk_load_col_scale(const float *col_scale, int gt, int d4, float4 (&cs)[VPT]) {
+#pragma unroll
+    for (int m = 0; m < VPT; ++m) {
+        const int jj = gt + m * kSkGroupThreads;
+        cs[m] = jj < d4 ? __ldg(reinterpret_cast<const float4 *>(col_scale) + jj) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
 }
 
 // ------------------------------------------------------------------------------- the row step
@@ -144,75 +215,64 @@ __device__ __forceinline__ void sk_drain(const SkRing &ring, int64_t consumed, i
 template <int VPT>
 __global__ void __launch_bounds__(kSkThreads, 1) sinkhorn_step_kernel(const __grid_constant__ SinkhornParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int d4 = p.d >> 2;
+    const SkShared sh = sk_carve(smem, p, true);
+    const int tid = threadIdx.x, lane = tid & 31;
     const int64_t G = gridDim.x, C = p.chunk;
 
-    // This CTA owns the partials blockIdx.x, blockIdx.x + G, ...; every one but the last non-empty
-    // partial of the matrix is full, so the CTA's j-th row is found without a table.
+    // This CTA owns the partials blockIdx.x, blockIdx.x + G, ...; all but the matrix's last
+    // non-empty partial are full, so they are runs of C rows, (G - 1) C rows apart.
     int64_t n_my = 0;
     for (int64_t pp = blockIdx.x; pp < p.P; pp += G) {
         const int64_t t0 = pp * C;
         n_my += t0 >= p.rows ? 0 : (t0 + C < p.rows ? C : p.rows - t0);
     }
-    auto row_of = [&](int64_t j) { return (blockIdx.x + (j / C) * G) * C + j % C; };
-
-    float4 cs[VPT];
-    int64_t issued;
-    const SkRing ring = sk_prologue<VPT>(p, smem, n_my, row_of, cs, &issued);
-    // row_scale of this CTA's rows, one window of kSkThreads rows at a time, the next window's
-    // load in flight while the current one is used.  row_scale is rewritten in place, but a row
-    // is written only after it has been read.
-    float rs_next = tid < n_my ? p.row_scale_in[row_of(tid)] : 0.f;
+    if (tid == 0) {
+        for (int q = 0; q < sh.S; ++q) {
+            mbar_init(&sh.full[q], 1);
+            mbar_init(&sh.empty[q], 1);
+        }
+        mbar_init_fence();
+    }
     __syncthreads();  // barriers initialised
+    if (tid >= kSkConsumers) {
+        sk_produce(sh, p, n_my, blockIdx.x * C, C, (G - 1) * C,
+                   [&](int64_t q) { return (blockIdx.x + (q / C) * G) * C + q % C; });
+        return;
+    }
 
-    int64_t j = 0;
-    int s = 0;
-    uint32_t phase = 0;
+    const int g = tid / kSkGroupThreads, gt = tid % kSkGroupThreads, gw = gt >> 5;
+    const int d4 = p.d >> 2;
+    float4 cs[VPT];
+    sk_load_col_scale<VPT>(p.col_scale, gt, d4, cs);
+
+    SkSlot slot{0, 0, 0};
+    int parity = 0;
     bool failed = false;
-    for (int64_t pp = blockIdx.x; pp < p.P && !failed; pp += G) {
+    int64_t jbase = 0;
+    for (int64_t pp = blockIdx.x; pp < p.P; pp += G, jbase += C) {
         const int64_t t0 = pp * C;
-        const int64_t t1 = t0 + C < p.rows ? t0 + C : p.rows;
+        const int64_t len = t0 >= p.rows ? 0 : (t0 + C < p.rows ? C : p.rows - t0);
         float4 acc[VPT];
 #pragma unroll
         for (int m = 0; m < VPT; ++m) acc[m] = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int64_t r = t0; r < t1; ++r, ++j) {
-            const int wpos = static_cast<int>(j % kSkThreads);
-            float *win = ring.rsw + ((j / kSkThreads) & 1) * kSkThreads;
-            if (wpos == 0) {
-                win[tid] = rs_next;
-                const int64_t jn = j + kSkThreads + tid;
-                rs_next = jn < n_my ? p.row_scale_in[row_of(jn)] : 0.f;
-                __syncthreads();
-            }
-            const bool ok = mbar_wait(&ring.full[s], phase);
-            const float rs = win[wpos];
+        for (int64_t i = g; i < len && !failed; i += 2) {
+            slot.move_to(jbase + i, sh.S);
+            const bool ok = mbar_wait(&sh.full[slot.s], slot.phase);
+            const float rs = sh.rs[slot.s];
             float4 x[VPT];
-            const float ss = warp_sum(sk_load_row<VPT>(ring, s, rs, cs, d4, ok, x));
-            float *red = ring.red + (j & 1) * kSkWarps;
-            if (lane == 0) red[warp] = ss;
-            if (__syncthreads_or(!ok)) {
-                if (tid == 0) report(p.status, nullptr, ENGRAM_DEVERR_TIMEOUT);
+            const float ss = sk_load_row<VPT>(sh, slot.s, gt, rs, cs, d4, ok, x);
+            float tot;
+            if (!sk_group_total(sh, g, gw, lane, parity, ss, ok, &tot)) {
                 failed = true;
                 break;
             }
-            // every thread holds its part of row j in registers: stage s can be refilled
-            if (tid == 0 && issued < n_my) {
-                ring.issue(issued, p.matrix + static_cast<size_t>(row_of(issued)) * p.d);
-                ++issued;
-            }
-            if (++s == ring.S) {
-                s = 0;
-                phase ^= 1u;
-            }
-            float tot = 0.f;
-#pragma unroll
-            for (int q = 0; q < kSkWarps; ++q) tot += red[q];
+            parity ^= 1;
+            if (gt == 0) mbar_arrive(&sh.empty[slot.s]);  // the group holds the row in registers
             const float nrm = sqrtf(tot);
             const float inv = 1.0f / (nrm + p.eps);
-            if (tid == 0) {
-                if (p.row_norm) p.row_norm[r] = nrm;
-                p.row_scale_out[r] = rs * inv;
+            if (gt == 0) {
+                if (p.row_norm) p.row_norm[t0 + i] = nrm;
+                p.row_scale_out[t0 + i] = rs * inv;
             }
 #pragma unroll
             for (int m = 0; m < VPT; ++m) {
@@ -223,15 +283,32 @@ __global__ void __launch_bounds__(kSkThreads, 1) sinkhorn_step_kernel(const __gr
                 acc[m].w = fmaf(y.w, y.w, acc[m].w);
             }
         }
-        if (failed) break;
-        float4 *prow = reinterpret_cast<float4 *>(p.partial + static_cast<size_t>(pp) * p.d);
+        // partial = (group 0's rows) + (group 1's rows): group 1 parks its sum in the exchange row,
+        // group 0 adds its own and writes the partial; the second barrier frees the exchange row
+        if (g == 1 && !failed) {
 #pragma unroll
-        for (int m = 0; m < VPT; ++m) {
-            const int jj = tid + m * kSkThreads;
-            if (jj < d4) prow[jj] = acc[m];
+            for (int m = 0; m < VPT; ++m) {
+                const int jj = gt + m * kSkGroupThreads;
+                if (jj < d4) sh.xrow[jj] = acc[m];
+            }
         }
+        if (named_sync_or(3, kSkConsumers, failed)) {
+            if (tid == 0) report(p.status, nullptr, ENGRAM_DEVERR_TIMEOUT);
+            break;
+        }
+        if (g == 0) {
+            float4 *prow = reinterpret_cast<float4 *>(p.partial + static_cast<size_t>(pp) * p.d);
+#pragma unroll
+            for (int m = 0; m < VPT; ++m) {
+                const int jj = gt + m * kSkGroupThreads;
+                if (jj < d4) {
+                    const float4 o = sh.xrow[jj];
+                    prow[jj] = make_float4(acc[m].x + o.x, acc[m].y + o.y, acc[m].z + o.z, acc[m].w + o.w);
+                }
+            }
+        }
+        named_sync(4, kSkConsumers);
     }
-    sk_drain(ring, j, issued, p.status);
 }
 
 // ------------------------------------------------------------------------------- finalize
@@ -239,60 +316,51 @@ __global__ void __launch_bounds__(kSkThreads, 1) sinkhorn_step_kernel(const __gr
 template <int VPT>
 __global__ void __launch_bounds__(kSkThreads, 1) sinkhorn_finalize_kernel(const __grid_constant__ SinkhornParams p) {
     extern __shared__ __align__(128) uint8_t smem[];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int d4 = p.d >> 2;
-    // a contiguous, balanced range of rows per CTA
+    const SkShared sh = sk_carve(smem, p, false);
+    const int tid = threadIdx.x, lane = tid & 31;
+    // a contiguous, balanced range of rows per CTA; the groups take alternate rows of it
     const int64_t r0 = p.rows * blockIdx.x / gridDim.x;
     const int64_t n_my = p.rows * (blockIdx.x + 1) / gridDim.x - r0;
-    auto row_of = [&](int64_t j) { return r0 + j; };
-
-    float4 cs[VPT];
-    int64_t issued;
-    const SkRing ring = sk_prologue<VPT>(p, smem, n_my, row_of, cs, &issued);
-    float rs_next = tid < n_my ? __ldg(p.row_scale_in + r0 + tid) : 0.f;
-    __syncthreads();  // barriers initialised
-
-    int64_t j = 0;
-    int s = 0;
-    uint32_t phase = 0;
-    for (; j < n_my; ++j) {
-        const int wpos = static_cast<int>(j % kSkThreads);
-        float *win = ring.rsw + ((j / kSkThreads) & 1) * kSkThreads;
-        if (wpos == 0) {
-            win[tid] = rs_next;
-            const int64_t jn = j + kSkThreads + tid;
-            rs_next = jn < n_my ? __ldg(p.row_scale_in + r0 + jn) : 0.f;
-            __syncthreads();
+    if (tid == 0) {
+        for (int q = 0; q < sh.S; ++q) {
+            mbar_init(&sh.full[q], 1);
+            mbar_init(&sh.empty[q], 1);
         }
-        const bool ok = mbar_wait(&ring.full[s], phase);
+        mbar_init_fence();
+    }
+    __syncthreads();  // barriers initialised
+    if (tid >= kSkConsumers) {
+        sk_produce(sh, p, n_my, r0, n_my, 0, [&](int64_t q) { return r0 + q; });
+        return;
+    }
+
+    const int g = tid / kSkGroupThreads, gt = tid % kSkGroupThreads, gw = gt >> 5;
+    const int d4 = p.d >> 2;
+    float4 cs[VPT];
+    sk_load_col_scale<VPT>(p.col_scale, gt, d4, cs);
+
+    SkSlot slot{0, 0, 0};
+    int parity = 0;
+    for (int64_t j = g; j < n_my; j += 2) {
+        slot.move_to(j, sh.S);
+        const bool ok = mbar_wait(&sh.full[slot.s], slot.phase);
         float4 x[VPT];
-        const float ss = warp_sum(sk_load_row<VPT>(ring, s, win[wpos], cs, d4, ok, x));
-        float *red = ring.red + (j & 1) * kSkWarps;
-        if (lane == 0) red[warp] = ss;
-        if (__syncthreads_or(!ok)) {
-            if (tid == 0) report(p.status, nullptr, ENGRAM_DEVERR_TIMEOUT);
+        const float ss = sk_load_row<VPT>(sh, slot.s, gt, sh.rs[slot.s], cs, d4, ok, x);
+        float tot;
+        if (!sk_group_total(sh, g, gw, lane, parity, ss, ok, &tot)) {
+            if (gt == 0) report(p.status, nullptr, ENGRAM_DEVERR_TIMEOUT);
             break;
         }
-        if (tid == 0 && issued < n_my) {
-            ring.issue(issued, p.matrix + static_cast<size_t>(row_of(issued)) * p.d);
-            ++issued;
-        }
-        if (++s == ring.S) {
-            s = 0;
-            phase ^= 1u;
-        }
-        float tot = 0.f;
-#pragma unroll
-        for (int q = 0; q < kSkWarps; ++q) tot += red[q];
+        parity ^= 1;
+        if (gt == 0) mbar_arrive(&sh.empty[slot.s]);
         const float f = p.alpha / (sqrtf(tot) + p.eps);
         float4 *orow = reinterpret_cast<float4 *>(p.out + static_cast<size_t>(r0 + j) * p.d);
 #pragma unroll
         for (int m = 0; m < VPT; ++m) {
-            const int jj = tid + m * kSkThreads;
+            const int jj = gt + m * kSkGroupThreads;
             if (jj < d4) __stcs(orow + jj, make_float4(x[m].x * f, x[m].y * f, x[m].z * f, x[m].w * f));
         }
     }
-    sk_drain(ring, j, issued, p.status);
 }
 
 // ------------------------------------------------------------------------------- ordered reduction
@@ -427,25 +495,51 @@ engram_status sk_check_ptrs(const char *fn, const void *const *ptrs, int n, int 
 
 using SkKernel = void (*)(SinkhornParams);
 
-SkKernel sk_step_kernel(int vpt) {
-    static const SkKernel k[kSkMaxVpt] = {sinkhorn_step_kernel<1>, sinkhorn_step_kernel<2>, sinkhorn_step_kernel<3>,
-                                          sinkhorn_step_kernel<4>, sinkhorn_step_kernel<5>, sinkhorn_step_kernel<6>,
-                                          sinkhorn_step_kernel<7>, sinkhorn_step_kernel<8>};
-    return k[vpt - 1];
+// VPT is instantiated for 1..6, 8, 10, 12 and 16 vectors per thread; a head_dim takes the
+// smallest that covers it.
+constexpr int kSkVpts[] = {1, 2, 3, 4, 5, 6, 8, 10, 12, 16};
+
+int sk_vpt(int32_t head_dim) {
+    const int need = (head_dim / 4 + kSkGroupThreads - 1) / kSkGroupThreads;
+    for (int v : kSkVpts)
+        if (v >= need) return v;
+    return 0;
 }
 
-SkKernel sk_finalize_kernel(int vpt) {
-    static const SkKernel k[kSkMaxVpt] = {
-        sinkhorn_finalize_kernel<1>, sinkhorn_finalize_kernel<2>, sinkhorn_finalize_kernel<3>,
-        sinkhorn_finalize_kernel<4>, sinkhorn_finalize_kernel<5>, sinkhorn_finalize_kernel<6>,
-        sinkhorn_finalize_kernel<7>, sinkhorn_finalize_kernel<8>};
-    return k[vpt - 1];
+template <template <int> class Tag>
+SkKernel sk_pick(int vpt);
+
+template <int V>
+struct StepTag {
+    static constexpr SkKernel k = sinkhorn_step_kernel<V>;
+};
+template <int V>
+struct FinTag {
+    static constexpr SkKernel k = sinkhorn_finalize_kernel<V>;
+};
+
+template <template <int> class Tag>
+SkKernel sk_pick(int vpt) {
+    switch (vpt) {
+        case 1: return Tag<1>::k;
+        case 2: return Tag<2>::k;
+        case 3: return Tag<3>::k;
+        case 4: return Tag<4>::k;
+        case 5: return Tag<5>::k;
+        case 6: return Tag<6>::k;
+        case 8: return Tag<8>::k;
+        case 10: return Tag<10>::k;
+        case 12: return Tag<12>::k;
+        default: return Tag<16>::k;
+    }
 }
 
 // Launches a row kernel on min(units, SMs) CTAs: one per SM, the ring takes most of its memory.
-engram_status sk_launch(const char *fn, SkKernel kernel, const SinkhornParams &prm, int64_t units,
+engram_status sk_launch(const char *fn, SkKernel kernel, SinkhornParams prm, bool exchange, int64_t units,
                         const DeviceInfo &dev, engram_stream_t stream) {
-    const int smem = sk_smem_bytes(prm.stages, static_cast<int64_t>(prm.d) * 4);
+    const int64_t row_bytes = static_cast<int64_t>(prm.d) * 4;
+    prm.stages = sk_stages(row_bytes, exchange, dev.smem_optin);
+    const int smem = sk_smem_bytes(prm.stages, row_bytes, exchange);
     if (smem > dev.smem_optin)
         return fail(ENGRAM_ERR_SHAPE, "%s: %d bytes of shared memory exceed %d", fn, smem, dev.smem_optin);
     engram_status st = set_smem(reinterpret_cast<const void *>(kernel), smem);
@@ -455,7 +549,7 @@ engram_status sk_launch(const char *fn, SkKernel kernel, const SinkhornParams &p
     return check_launch(fn);
 }
 
-int sk_vpt(int32_t head_dim) { return (head_dim / 4 + kSkThreads - 1) / kSkThreads; }
+
 
 }  // namespace
 }  // namespace engram
@@ -525,9 +619,8 @@ extern "C" engram_status engram_sinkhorn_step(const float *matrix, float *row_sc
     prm.chunk = rows == 0 ? 1 : (rows + P - 1) / P;
     prm.P = P;
     prm.d = head_dim;
-    prm.stages = sk_stages(static_cast<int64_t>(head_dim) * 4);
     prm.eps = eps;
-    return sk_launch(fn, sk_step_kernel(sk_vpt(head_dim)), prm, P, dev, stream);
+    return sk_launch(fn, sk_pick<StepTag>(sk_vpt(head_dim)), prm, true, P, dev, stream);
 }
 
 extern "C" engram_status engram_sinkhorn_step_reduce(const float *col_sumsq_partial, int32_t P, int32_t head_dim,
@@ -568,8 +661,7 @@ extern "C" engram_status engram_sinkhorn_finalize(const float *matrix, const flo
     prm.status = dev.status_word;
     prm.rows = rows;
     prm.d = head_dim;
-    prm.stages = sk_stages(static_cast<int64_t>(head_dim) * 4);
     prm.eps = eps;
     prm.alpha = alpha;
-    return sk_launch(fn, sk_finalize_kernel(sk_vpt(head_dim)), prm, rows, dev, stream);
+    return sk_launch(fn, sk_pick<FinTag>(sk_vpt(head_dim)), prm, false, rows, dev, stream);
 }

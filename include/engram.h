@@ -343,9 +343,11 @@ engram_status engram_sinkhorn_num_partials(int64_t rows, int32_t head_dim, int32
  *     row_scale[r] = row_scale[r] / (row_norm[r] + eps)       (in place)
  * and the column partials
  *     col_sumsq_partial[p, c] = sum over r in [p*C, min(rows, (p+1)*C)) of (x_c / (row_norm[r] + eps))^2,
- * C = ceil(rows / P), rows in ascending order, a partial with no row 0.  col_sumsq_partial is
- * [P, head_dim] fp32, P >= 1.  head_dim a multiple of 4 and at most 8192; matrix, col_scale and
- * col_sumsq_partial 16-byte aligned.  Outputs may not alias the matrix or col_scale.
+ * C = ceil(rows / P), a partial with no row 0.  Summation order (fixed by rows and P only, so the
+ * result is bitwise reproducible on any device): the rows at even offsets from p*C in ascending
+ * order, the rows at odd offsets in ascending order, then the first sum plus the second.
+ * col_sumsq_partial is [P, head_dim] fp32, P >= 1.  head_dim a multiple of 4 and at most 8192;
+ * matrix, col_scale and col_sumsq_partial 16-byte aligned.  Outputs may not alias the matrix or col_scale.
  */
 engram_status engram_sinkhorn_step(const float *matrix, float *row_scale, const float *col_scale, int64_t rows,
                                    int32_t head_dim, float eps, float *row_norm, float *col_sumsq_partial,

@@ -8,11 +8,13 @@ point; bitwise reruns on different grids.
 
 Tolerances are derived from the fp32 arithmetic of the kernels (u = 2^-24, all sums are of positive
 terms, so a chain of n roundings costs at most about n u relative):
-  * the row's sum of squares: per thread 4 VPT fused multiply-adds (VPT = ceil(head_dim / 1024)),
-    5 shuffle levels, 8 warp partials in order, each term x^2 with x = row_scale * m * col_scale
-    two roundings off -> ss_rel = (4 VPT + 20) u; row_norm = sqrt: ss_rel / 2 + u;
-  * row_scale / (row_norm + eps): + 3 u;  y = x / (row_norm + eps) and y^2, C rows in order:
-    2 (nrm_rel + 5 u) + (C + 1) u;  the reduction adds (ceil(P / 64) + 64) u;
+  * the row's sum of squares: per thread VPT float4 vectors (VPT = ceil(head_dim / 512)), each a
+    3-rounding tree, added in order; 5 shuffle levels; 4 warp partials in order; each term x^2 with
+    x = row_scale * m * col_scale two roundings off -> at most (4 VPT + 20) u; row_norm = sqrt:
+    ss_rel / 2 + u;
+  * row_scale / (row_norm + eps): + 3 u;  y = x / (row_norm + eps) and y^2, the partial's rows in
+    two interleaved ascending chains added at the end: 2 (nrm_rel + 5 u) + (C + 1) u;  the
+    reduction adds (ceil(P / 64) + 64) u;
   * finalize: alpha x / (||x|| + eps): nrm_rel + 5 u;
   * momentum: one fused multiply-add, correctly rounded: |gpu - ref| <= u |ref| (plus u beta |m'|
     for the Nesterov look-ahead, which reads the rounded m').
@@ -45,7 +47,7 @@ def _status_clean(cuda_lib):
 
 
 def _vpt(D):
-    return -(-D // 1024)
+    return -(-D // 512)
 
 
 def _nrm_rel(D):
