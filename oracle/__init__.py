@@ -62,7 +62,11 @@ def _load():
             lib.eo_sinkhorn_step.argtypes = [_p, _p, _p, _i64, _i32, _f64, _i64, _i64, _p, _p, _p]
             lib.eo_sinkhorn_col_update.argtypes = [_p, _p, _i32, _f64, _p]
             lib.eo_sinkhorn_finalize.argtypes = [_p, _p, _p, _i64, _i32, _f64, _f64, _p]
-            for f in ("eo_sinkhorn_momentum", "eo_sinkhorn_step", "eo_sinkhorn_col_update", "eo_sinkhorn_finalize",
+            lib.eo_short_conv_fwd.argtypes = [_p, _p, ctypes.c_int, _p, _p, _p, _p, _i32, _i64, _i32, _i32, _i32,
+                                              _f64, _i64, _i64, _p, _p, _p]
+            lib.eo_short_conv_bwd.argtypes = [_p, _p, ctypes.c_int, _p, _p, _p, _p, _i32, _i64, _i32, _i32, _i32,
+                                              _f64, _i64, _i64, _p, _p, _p, _p, _p, _p, _p, _p]
+            for f in ("eo_short_conv_fwd", "eo_short_conv_bwd", "eo_sinkhorn_momentum", "eo_sinkhorn_step", "eo_sinkhorn_col_update", "eo_sinkhorn_finalize",
                       "eo_hash_indices", "eo_gather_rows", "eo_fuse_weight", "eo_gate_fwd", "eo_gate_bwd",
                       "eo_grad_w_reduce", "eo_gate_hc_fwd", "eo_gate_hc_bwd"):
                 getattr(lib, f).restype = ctypes.c_int
@@ -278,3 +282,55 @@ def sinkhorn_finalize(matrix, row_scale, col_scale, eps: float, alpha: float) ->
     rc = lib.eo_sinkhorn_finalize(_ptr(mat), _ptr(rs), _ptr(cs), R, D, float(eps), float(alpha), _ptr(out))
     _check(rc, "sinkhorn_finalize")
     return out
+
+
+def _conv_common(v, norm_w, conv_w, bias, seq_offsets):
+    v = np.ascontiguousarray(v)
+    T, d = v.shape
+    nw = np.ascontiguousarray(norm_w, dtype=np.float32).reshape(d)
+    cw = np.ascontiguousarray(conv_w, dtype=np.float32)
+    assert cw.ndim == 2 and cw.shape[0] == d
+    b = None if bias is None else np.ascontiguousarray(bias, dtype=np.float32).reshape(d)
+    offs = np.ascontiguousarray(seq_offsets, dtype=np.int64)
+    return v, T, d, nw, cw, b, offs
+
+
+def short_conv_fwd(v, h, norm_w, conv_w, bias, seq_offsets, dilation: int, eps: float, t_begin: int = 0,
+                   t_end: int | None = None) -> dict:
+    """out = H + SiLU(c) + V~ with c the causal depthwise conv of RMSNorm(V~): fp64 out, c [n, d], rstd [n]."""
+    lib = _load()
+    v, T, d, nw, cw, b, offs = _conv_common(v, norm_w, conv_w, bias, seq_offsets)
+    dt = _dtype_code(v)
+    if h is not None:
+        h = np.ascontiguousarray(h)
+        assert _dtype_code(h) == dt and h.shape == v.shape
+    t_end = T if t_end is None else t_end
+    n = t_end - t_begin
+    res = {"out": np.zeros((n, d)), "c": np.zeros((n, d)), "rstd": np.zeros(n)}
+    rc = lib.eo_short_conv_fwd(_ptr(v), _ptr(h), dt, _ptr(nw), _ptr(cw), _ptr(b), _ptr(offs), offs.size - 1, T, d,
+                               cw.shape[1], int(dilation), float(eps), t_begin, t_end, _ptr(res["out"]),
+                               _ptr(res["c"]), _ptr(res["rstd"]))
+    _check(rc, "short_conv_fwd")
+    return res
+
+
+def short_conv_bwd(g, v, norm_w, conv_w, bias, seq_offsets, dilation: int, eps: float, t_begin: int = 0,
+                   t_end: int | None = None) -> dict:
+    """fp64 dv [n, d], dconv_w [d, w], dbias [d], dnorm_w [d] over tokens [t_begin, t_end), and the
+    matching *_abs magnitude sums."""
+    lib = _load()
+    v, T, d, nw, cw, b, offs = _conv_common(v, norm_w, conv_w, bias, seq_offsets)
+    g = np.ascontiguousarray(g)
+    dt = _dtype_code(v)
+    assert _dtype_code(g) == dt and g.shape == v.shape
+    t_end = T if t_end is None else t_end
+    n, w = t_end - t_begin, cw.shape[1]
+    res = {"dv": np.zeros((n, d)), "dconv_w": np.zeros((d, w)), "dbias": np.zeros(d), "dnorm_w": np.zeros(d),
+           "dv_abs": np.zeros((n, d)), "dconv_w_abs": np.zeros((d, w)), "dbias_abs": np.zeros(d),
+           "dnorm_w_abs": np.zeros(d)}
+    rc = lib.eo_short_conv_bwd(_ptr(g), _ptr(v), dt, _ptr(nw), _ptr(cw), _ptr(b), _ptr(offs), offs.size - 1, T, d,
+                               w, int(dilation), float(eps), t_begin, t_end, _ptr(res["dv"]), _ptr(res["dconv_w"]),
+                               _ptr(res["dbias"]), _ptr(res["dnorm_w"]), _ptr(res["dv_abs"]),
+                               _ptr(res["dconv_w_abs"]), _ptr(res["dbias_abs"]), _ptr(res["dnorm_w_abs"]))
+    _check(rc, "short_conv_bwd")
+    return res

@@ -31,6 +31,8 @@
  *   sec. 3.2 (forward) and sec. 4.2 (backward, including the zero-gradient clamp branch).
  *   NEXT-4 (the Engram Sinkhorn of the TileKernels release): T34 sec. 5.3 -- momentum update,
  *   the row step with its column partial sums, the ordered reduction, finalize.
+ *   NEXT-2 (the short convolution after the gate): T34 sec. 1.2 item 4 -- Y = SiLU(Conv1D(
+ *   RMSNorm(V~))) + V~, H <- H + Y, kernel size 4, dilation the largest N-gram order.
  *
  * Readings where the pages leave a step open (each one is also listed in the
  * design notes):
@@ -52,6 +54,7 @@
  */
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #define EO_F32 0
@@ -581,5 +584,215 @@ int eo_sinkhorn_finalize(const float *matrix, const float *row_scale, const floa
             out[r * head_dim + c] =
                 (double)row_scale[r] * (double)matrix[r * head_dim + c] * (double)col_scale[c] * f;
     }
+    return EO_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* NEXT-2: the short convolution + SiLU + residual after the gate  [T34 sec. 1.2 item 4] */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * The pages give only Y = SiLU(Conv1D(RMSNorm(V~))) + V~ and H <- H + Y, with kernel size w = 4
+ * and the dilation equal to the largest N-gram order (the step is not in the TileKernels release).
+ * Readings (listed in the design notes):
+ *   - V~ [T, d] is the gate's output sequence alpha_t v_t; RMSNorm has a learnable weight
+ *     norm_w [d] and eps inside the root, like the gate's norms;
+ *   - Conv1D is depthwise (one w-tap filter per channel, conv_w [d][w], optional bias [d]) and
+ *     causal within each sequence: tap i multiplies the token (w - 1 - i) * dilation steps back, so
+ *     tap w - 1 is the current token (torch's conv1d layout with (w - 1) * dilation left padding);
+ *     positions before the sequence start are zero;
+ *   - out = H + SiLU(c) + V~ (H nullable: then out = Y).
+ */
+
+static int eo_seq_of(const int64_t *offs, int32_t num_seqs, int64_t t)
+{
+    int lo = 0, hi = num_seqs - 1;
+    while (lo < hi) { /* largest s with offs[s] <= t */
+        const int mid = (lo + hi + 1) / 2;
+        if (offs[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+static double eo_conv_rstd(const void *v, int dtype, int64_t t, int32_t d, double eps)
+{
+    double ss = 0.0;
+    for (int32_t j = 0; j < d; ++j) {
+        const double x = eo_load(v, dtype, t * (int64_t)d + j);
+        ss += x * x;
+    }
+    return 1.0 / sqrt(ss / (double)d + eps);
+}
+
+/*
+ * rstd of the tokens [lo, hi) around the range a call works on, computed once per token (the
+ * same value the definition gives at every use; nothing is reordered).
+ */
+typedef struct {
+    int64_t lo, hi;
+    double *r;
+} eo_rstd_cache;
+
+static int eo_rstd_cache_fill(eo_rstd_cache *rc, const void *v, int dtype, int64_t T, int32_t d, double eps,
+                              int64_t lo, int64_t hi)
+{
+    rc->lo = lo < 0 ? 0 : lo;
+    rc->hi = hi > T ? T : hi;
+    rc->r = (double *)malloc(sizeof(double) * (size_t)(rc->hi > rc->lo ? rc->hi - rc->lo : 1));
+    if (!rc->r) return EO_ERR_ARG;
+    for (int64_t t = rc->lo; t < rc->hi; ++t)
+        rc->r[t - rc->lo] = eo_conv_rstd(v, dtype, t, d, eps);
+    return EO_OK;
+}
+
+/* u[t', j] = V~[t', j] * rstd(t') * norm_w[j] when t' lies in [seq_start, T), else 0. */
+static double eo_conv_u(const void *v, int dtype, const float *norm_w, const eo_rstd_cache *rc, int64_t tp,
+                        int64_t seq_start, int32_t d, int32_t j)
+{
+    if (tp < seq_start) return 0.0;
+    return eo_load(v, dtype, tp * (int64_t)d + j) * rc->r[tp - rc->lo] * (double)norm_w[j];
+}
+
+/* c[t, j] = bias[j] + sum_i conv_w[j][i] * u[t - (w - 1 - i) * dilation, j] */
+static double eo_conv_c(const void *v, int dtype, const float *norm_w, const float *conv_w, const float *bias,
+                        const eo_rstd_cache *rc, int64_t t, int64_t seq_start, int32_t d, int32_t w, int32_t dil,
+                        int32_t j)
+{
+    double c = bias ? (double)bias[j] : 0.0;
+    for (int32_t i = 0; i < w; ++i)
+        c += (double)conv_w[(int64_t)j * w + i] *
+             eo_conv_u(v, dtype, norm_w, rc, t - (int64_t)(w - 1 - i) * dil, seq_start, d, j);
+    return c;
+}
+
+static int eo_conv_args(const void *v, int dtype, const float *norm_w, const float *conv_w,
+                        const int64_t *offs, int32_t num_seqs, int64_t T, int32_t d, int32_t w, int32_t dil,
+                        int64_t t_begin, int64_t t_end)
+{
+    if (!v || !norm_w || !conv_w || !offs || num_seqs < 1 || d <= 0 || w < 1 || dil < 1)
+        return EO_ERR_ARG;
+    if ((dtype != EO_F32 && dtype != EO_BF16) || t_begin < 0 || t_end > T || t_begin > t_end)
+        return EO_ERR_ARG;
+    if (offs[0] != 0 || offs[num_seqs] != T)
+        return EO_ERR_ARG;
+    for (int32_t s = 0; s < num_seqs; ++s)
+        if (offs[s + 1] < offs[s]) return EO_ERR_ARG;
+    return EO_OK;
+}
+
+/*
+ * Forward for tokens [t_begin, t_end): out = H + SiLU(c) + V~ (rows indexed from t_begin, fp64),
+ * c (nullable) the convolution output, rstd (nullable) [n] the RMSNorm statistic of V~.
+ */
+int eo_short_conv_fwd(const void *v, const void *h, int dtype, const float *norm_w, const float *conv_w,
+                      const float *bias, const int64_t *offs, int32_t num_seqs, int64_t T, int32_t d, int32_t w,
+                      int32_t dil, double eps, int64_t t_begin, int64_t t_end, double *out, double *c_out,
+                      double *rstd)
+{
+    if (eo_conv_args(v, dtype, norm_w, conv_w, offs, num_seqs, T, d, w, dil, t_begin, t_end) != EO_OK || !out)
+        return EO_ERR_ARG;
+    eo_rstd_cache rc;
+    if (eo_rstd_cache_fill(&rc, v, dtype, T, d, eps, t_begin - (int64_t)(w - 1) * dil, t_end) != EO_OK)
+        return EO_ERR_ARG;
+    for (int64_t t = t_begin; t < t_end; ++t) {
+        const int64_t s0 = offs[eo_seq_of(offs, num_seqs, t)];
+        if (rstd) rstd[t - t_begin] = rc.r[t - rc.lo];
+        for (int32_t j = 0; j < d; ++j) {
+            const double c = eo_conv_c(v, dtype, norm_w, conv_w, bias, &rc, t, s0, d, w, dil, j);
+            const double y = c * eo_sigmoid(c) + eo_load(v, dtype, t * (int64_t)d + j);
+            out[(t - t_begin) * d + j] = (h ? eo_load(h, dtype, t * (int64_t)d + j) : 0.0) + y;
+            if (c_out) c_out[(t - t_begin) * d + j] = c;
+        }
+    }
+    free(rc.r);
+    return EO_OK;
+}
+
+/* dL/dc at (t, j) given dout = g: g * SiLU'(c), SiLU'(c) = s (1 + c (1 - s)), s = sigmoid(c). */
+static double eo_conv_dc(const void *g, const void *v, int dtype, const float *norm_w, const float *conv_w,
+                         const float *bias, const eo_rstd_cache *rc, int64_t t, int64_t seq_start, int32_t d,
+                         int32_t w, int32_t dil, int32_t j)
+{
+    const double c = eo_conv_c(v, dtype, norm_w, conv_w, bias, rc, t, seq_start, d, w, dil, j);
+    const double s = eo_sigmoid(c);
+    return eo_load(g, dtype, t * (int64_t)d + j) * s * (1.0 + c * (1.0 - s));
+}
+
+/*
+ * Backward for tokens [t_begin, t_end), given g = dL/dout [T, d] (dL/dH = g, not returned):
+ *     du[t, j]  = sum_i conv_w[j][i] * dc[t + (w - 1 - i) * dil, j]   (same sequence only)
+ *     s[t]      = sum_j norm_w[j] du[t, j] V~[t, j]
+ *     dV~[t, j] = g[t, j] + rstd(t) norm_w[j] du[t, j] - rstd(t)^3 V~[t, j] s[t] / d
+ * and, accumulated over the range (zeroed first):
+ *     dconv_w[j][i] += dc[t, j] * u[t - (w - 1 - i) * dil, j]
+ *     dbias[j]      += dc[t, j]
+ *     dnorm_w[j]    += du[t, j] * V~[t, j] * rstd(t)
+ * dv is [n, d] from t_begin.  The *_abs outputs (nullable) are the same sums over |terms|, for
+ * tolerances: dv_abs[t, j] = |g| + |rstd norm_w du| + |rstd^3 V~ s / d|.
+ */
+int eo_short_conv_bwd(const void *g, const void *v, int dtype, const float *norm_w, const float *conv_w,
+                      const float *bias, const int64_t *offs, int32_t num_seqs, int64_t T, int32_t d, int32_t w,
+                      int32_t dil, double eps, int64_t t_begin, int64_t t_end, double *dv, double *dconv_w,
+                      double *dbias, double *dnorm_w, double *dv_abs, double *dconv_w_abs, double *dbias_abs,
+                      double *dnorm_w_abs)
+{
+    if (eo_conv_args(v, dtype, norm_w, conv_w, offs, num_seqs, T, d, w, dil, t_begin, t_end) != EO_OK || !g ||
+        !dv || !dconv_w || !dbias || !dnorm_w)
+        return EO_ERR_ARG;
+    for (int64_t k = 0; k < (int64_t)d * w; ++k) {
+        dconv_w[k] = 0.0;
+        if (dconv_w_abs) dconv_w_abs[k] = 0.0;
+    }
+    for (int32_t j = 0; j < d; ++j) {
+        dbias[j] = dnorm_w[j] = 0.0;
+        if (dbias_abs) dbias_abs[j] = 0.0;
+        if (dnorm_w_abs) dnorm_w_abs[j] = 0.0;
+    }
+    eo_rstd_cache rc;
+    if (eo_rstd_cache_fill(&rc, v, dtype, T, d, eps, t_begin - (int64_t)(w - 1) * dil,
+                           t_end + (int64_t)(w - 1) * dil) != EO_OK)
+        return EO_ERR_ARG;
+    for (int64_t t = t_begin; t < t_end; ++t) {
+        const int sq = eo_seq_of(offs, num_seqs, t);
+        const int64_t s0 = offs[sq], s1 = offs[sq + 1];
+        const double r = rc.r[t - rc.lo];
+        double *row = dv + (t - t_begin) * d;
+        double s = 0.0, s_abs = 0.0;
+        for (int32_t j = 0; j < d; ++j) {
+            /* du from the taps that read token t: tokens t + (w - 1 - i) * dil of the same sequence */
+            double du = 0.0;
+            for (int32_t i = 0; i < w; ++i) {
+                const int64_t tf = t + (int64_t)(w - 1 - i) * dil;
+                if (tf < s1)
+                    du += (double)conv_w[(int64_t)j * w + i] *
+                          eo_conv_dc(g, v, dtype, norm_w, conv_w, bias, &rc, tf, s0, d, w, dil, j);
+            }
+            const double x = eo_load(v, dtype, t * (int64_t)d + j);
+            row[j] = du; /* kept here until s is known */
+            s += (double)norm_w[j] * du * x;
+            s_abs += fabs((double)norm_w[j] * du * x);
+            dnorm_w[j] += du * x * r;
+            if (dnorm_w_abs) dnorm_w_abs[j] += fabs(du * x * r);
+            /* weight gradients of the taps at token t */
+            const double dc = eo_conv_dc(g, v, dtype, norm_w, conv_w, bias, &rc, t, s0, d, w, dil, j);
+            dbias[j] += dc;
+            if (dbias_abs) dbias_abs[j] += fabs(dc);
+            for (int32_t i = 0; i < w; ++i) {
+                const double u = eo_conv_u(v, dtype, norm_w, &rc, t - (int64_t)(w - 1 - i) * dil, s0, d, j);
+                dconv_w[(int64_t)j * w + i] += dc * u;
+                if (dconv_w_abs) dconv_w_abs[(int64_t)j * w + i] += fabs(dc * u);
+            }
+        }
+        for (int32_t j = 0; j < d; ++j) {
+            const double du = row[j];
+            const double x = eo_load(v, dtype, t * (int64_t)d + j);
+            const double gj = eo_load(g, dtype, t * (int64_t)d + j);
+            row[j] = gj + r * (double)norm_w[j] * du - r * r * r * x * s / (double)d;
+            if (dv_abs)
+                dv_abs[(t - t_begin) * d + j] =
+                    fabs(gj) + fabs(r * (double)norm_w[j] * du) + fabs(r * r * r * x) * s_abs / (double)d;
+        }
+    }
+    free(rc.r);
     return EO_OK;
 }

@@ -454,3 +454,106 @@ def test_sinkhorn_nesterov_with_prior_momentum():
     r = oracle.sinkhorn_momentum(g, m0, beta, True)
     expect = (1 + beta) * g.astype(np.float64) + beta ** 2 * m0.astype(np.float64)
     np.testing.assert_allclose(r["input"], expect, rtol=1e-14, atol=1e-15)
+
+
+# ----------------------------------------------------------------------------- the short conv after the gate
+
+def _conv_case(lengths, d, w, dil, seed, dtype="f32", bias=True):
+    T = int(sum(lengths))
+    v = G.normal(seed, T * d).reshape(T, d)
+    h = G.normal(seed + 1, T * d).reshape(T, d)
+    g = G.normal(seed + 2, T * d).reshape(T, d)
+    conv = lambda a: a.astype(np.float32) if dtype == "f32" else G.to_bf16_bits(a)
+    return dict(v=conv(v), h=conv(h), g=conv(g), norm_w=G.normal(seed + 3, d, 1.0, 0.1).astype(np.float32),
+                conv_w=G.normal(seed + 4, d * w, 0.0, 0.5).astype(np.float32).reshape(d, w),
+                bias=G.normal(seed + 5, d, 0.0, 0.1).astype(np.float32) if bias else None,
+                offs=G.offsets_from_lengths(lengths), dil=dil, T=T, d=d, w=w)
+
+
+def _as64(a):
+    return torch.from_numpy((a.astype(np.uint32) << 16).view(np.float32).astype(np.float64) if a.dtype == np.uint16
+                            else a.astype(np.float64))
+
+
+def _torch_short_conv(c, eps, v=None, norm_w=None, conv_w=None, bias=None):
+    """torch's rms_norm + depthwise conv1d (dilation, left padding, per sequence) + silu, fp64."""
+    v = _as64(c["v"]) if v is None else v
+    nw = torch.from_numpy(c["norm_w"].astype(np.float64)) if norm_w is None else norm_w
+    cw = torch.from_numpy(c["conv_w"].astype(np.float64)) if conv_w is None else conv_w
+    b = (None if c["bias"] is None else torch.from_numpy(c["bias"].astype(np.float64))) if bias is None else bias
+    u = torch.nn.functional.rms_norm(v, (c["d"],), nw, eps)
+    pad = (c["w"] - 1) * c["dil"]
+    outs = []
+    for s in range(len(c["offs"]) - 1):
+        a, e = int(c["offs"][s]), int(c["offs"][s + 1])
+        if a == e:
+            continue
+        x = u[a:e].T.unsqueeze(0)
+        y = torch.nn.functional.conv1d(x, cw.unsqueeze(1), b, padding=pad, dilation=c["dil"], groups=c["d"])
+        outs.append(y[0, :, : e - a].T)
+    conv = torch.cat(outs)
+    return conv, _as64(c["h"]) + torch.nn.functional.silu(conv) + v
+
+
+@pytest.mark.parametrize("lengths,d,w,dil,dtype", [([13, 9], 6, 4, 3, "f32"), ([20], 5, 4, 1, "bf16"),
+                                                    ([4, 0, 11, 2], 3, 3, 2, "f32"), ([7], 4, 1, 3, "f32")])
+def test_short_conv_against_torch_conv1d(lengths, d, w, dil, dtype):
+    c = _conv_case(lengths, d, w, dil, 610 + d, dtype)
+    eps = 1e-6
+    r = oracle.short_conv_fwd(c["v"], c["h"], c["norm_w"], c["conv_w"], c["bias"], c["offs"], dil, eps)
+    conv, out = _torch_short_conv(c, eps)
+    np.testing.assert_allclose(r["c"], conv.numpy(), rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(r["out"], out.numpy(), rtol=1e-12, atol=1e-13)
+    vv = _as64(c["v"]).numpy()
+    np.testing.assert_allclose(r["rstd"], 1 / np.sqrt((vv ** 2).mean(axis=1) + eps), rtol=1e-14)
+
+
+def test_short_conv_backward_against_autograd():
+    c = _conv_case([13, 1, 9], 6, 4, 3, 620, "f32")
+    eps = 1e-6
+    v = _as64(c["v"]).requires_grad_()
+    nw = torch.from_numpy(c["norm_w"].astype(np.float64)).requires_grad_()
+    cw = torch.from_numpy(c["conv_w"].astype(np.float64)).requires_grad_()
+    b = torch.from_numpy(c["bias"].astype(np.float64)).requires_grad_()
+    _, out = _torch_short_conv(c, eps, v, nw, cw, b)
+    (out * _as64(c["g"])).sum().backward()
+    r = oracle.short_conv_bwd(c["g"], c["v"], c["norm_w"], c["conv_w"], c["bias"], c["offs"], 3, eps)
+    np.testing.assert_allclose(r["dv"], v.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(r["dconv_w"], cw.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(r["dbias"], b.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(r["dnorm_w"], nw.grad.numpy(), rtol=1e-10, atol=1e-12)
+    # token ranges partition the weight gradients and give the same per-token rows
+    a = oracle.short_conv_bwd(c["g"], c["v"], c["norm_w"], c["conv_w"], c["bias"], c["offs"], 3, eps, 0, 10)
+    z = oracle.short_conv_bwd(c["g"], c["v"], c["norm_w"], c["conv_w"], c["bias"], c["offs"], 3, eps, 10, c["T"])
+    for k in ("dconv_w", "dbias", "dnorm_w"):
+        np.testing.assert_allclose(a[k] + z[k], r[k], rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(np.concatenate([a["dv"], z["dv"]]), r["dv"], rtol=1e-13, atol=1e-15)
+
+
+def test_short_conv_closed_forms():
+    c = _conv_case([10, 7], 4, 4, 3, 630, "f32", bias=False)
+    eps = 1e-6
+    vv, hh = _as64(c["v"]).numpy(), _as64(c["h"]).numpy()
+    u = vv / np.sqrt((vv ** 2).mean(axis=1, keepdims=True) + eps) * c["norm_w"].astype(np.float64)
+    silu = lambda x: x / (1 + np.exp(-x))
+    # the current-token tap alone: c = u
+    delta = np.zeros((4, 4), dtype=np.float32)
+    delta[:, 3] = 1
+    r = oracle.short_conv_fwd(c["v"], c["h"], c["norm_w"], delta, None, c["offs"], 3, eps)
+    np.testing.assert_allclose(r["c"], u, rtol=1e-14, atol=1e-15)
+    np.testing.assert_allclose(r["out"], hh + silu(u) + vv, rtol=1e-13)
+    # the oldest tap alone: c[t] = u[t - 9] inside a sequence, 0 for its first 9 tokens (SiLU(0) = 0)
+    old = np.zeros((4, 4), dtype=np.float32)
+    old[:, 0] = 1
+    r = oracle.short_conv_fwd(c["v"], None, c["norm_w"], old, None, c["offs"], 3, eps)
+    for s0, s1 in ((0, 10), (10, 17)):
+        np.testing.assert_array_equal(r["c"][s0:min(s1, s0 + 9)], 0)
+        np.testing.assert_array_equal(r["out"][s0:min(s1, s0 + 9)], vv[s0:min(s1, s0 + 9)])
+        for t in range(s0 + 9, s1):
+            np.testing.assert_allclose(r["c"][t], u[t - 9], rtol=1e-14)
+    # SiLU'(0) = 1/2: with every tap 0 and bias 0, dv = g and the weight gradients follow from dc = g / 2
+    zero = np.zeros((4, 4), dtype=np.float32)
+    b = oracle.short_conv_bwd(c["g"], c["v"], c["norm_w"], zero, None, c["offs"], 3, eps)
+    np.testing.assert_allclose(b["dv"], _as64(c["g"]).numpy(), rtol=1e-15)
+    np.testing.assert_allclose(b["dbias"], _as64(c["g"]).numpy().sum(0) / 2, rtol=1e-13)
+    np.testing.assert_array_equal(b["dnorm_w"], 0)
