@@ -513,6 +513,38 @@ def main_only(args, device):
 
             def launch():
                 ecm.gate_hc_fwd(x, kv, wf, wl.eps, wl.clamp, out=out, stats=st)
+    elif op.startswith("short_conv"):
+        # the short conv after the gate's micro-batch: 4 x 4096 tokens, d = 4096 bf16, width 4, dilation 3
+        cw = W.short_conv_4x4k()
+        T, d = cw.T, cw.d
+        v = SD.normal_tensor((T, d), cw.seed + 1, 0.0, 0.5, "bf16", device)
+        h = SD.normal_tensor((T, d), cw.seed + 2, 0.0, 1.0, "bf16", device)
+        g = SD.normal_tensor((T, d), cw.seed + 3, 0.0, 1.0, "bf16", device)
+        nw = SD.normal_tensor((1, d), cw.seed + 4, 1.0, 0.1, "f32", device).reshape(-1)
+        cwt = SD.normal_tensor((d, cw.width), cw.seed + 5, 0.0, 0.5, "f32", device)
+        bias = SD.normal_tensor((1, d), cw.seed + 6, 0.0, 0.1, "f32", device).reshape(-1)
+        offs = torch.arange(0, T + 1, 4096, dtype=torch.int64, device=device)
+        out, rstd = ecm.short_conv_fwd(v, nw, cwt, offs, cw.dilation, h=h, bias=bias)
+        dv, part = ecm.short_conv_bwd(g, v, nw, cwt, rstd, offs, cw.dilation, bias=bias)
+        tdot = torch.empty((T, ecm.short_conv_dot_blocks(d)), dtype=torch.float32, device=device)
+        red = ecm.short_conv_grad_reduce(part, cw.width, d)
+        P = part.shape[0]
+        if op == "short_conv_fwd":  # the op's own bytes: V~ and H read, out written, rstd written
+            nbytes = 3 * T * d * 2 + 4 * T
+
+            def launch():
+                ecm.short_conv_fwd(v, nw, cwt, offs, cw.dilation, h=h, bias=bias, out=out, rstd=rstd)
+        elif op == "short_conv_bwd":  # dout, V~, rstd read; dv and the partials written
+            nbytes = 3 * T * d * 2 + 4 * T + P * (cw.width + 2) * d * 4
+
+            def launch():
+                ecm.short_conv_bwd(g, v, nw, cwt, rstd, offs, cw.dilation, bias=bias, dv=dv, token_dot=tdot,
+                                   dw_partial=part)
+        else:
+            nbytes = P * (cw.width + 2) * d * 4 + (cw.width + 2) * d * 4
+
+            def launch():
+                ecm.short_conv_grad_reduce(part, cw.width, d, out=red)
     elif op.startswith("sinkhorn"):
         # the Engram Sinkhorn on 16384 x 5120 fp32 (bf16 gradient): 335 MB per matrix, > L2
         sw = W.sinkhorn_16k_x_5120()
@@ -671,7 +703,7 @@ def main():
     ap.add_argument("--only", choices=["hash_gather", "hash_gather_small", "hash_gather_host", "gate_fwd",
                                        "gate_fwd_2k", "gate_bwd", "grad_w_reduce", "gate_hc_fwd", "gate_hc_bwd",
                                        "sinkhorn", "sinkhorn_momentum", "sinkhorn_step", "sinkhorn_reduce",
-                                       "sinkhorn_finalize"],
+                                       "sinkhorn_finalize", "short_conv_fwd", "short_conv_bwd", "short_conv_reduce"],
                     help="time one kernel alone on its workload (consecutive launches, L2 not flushed)")
     args = ap.parse_args()
     if args.warmup < 3:

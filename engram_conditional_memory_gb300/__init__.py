@@ -29,6 +29,11 @@ from .binding import (  # noqa: F401
     read_error_word,
     set_max_ctas,
     set_validation,
+    short_conv_bwd,
+    short_conv_dot_blocks,
+    short_conv_fwd,
+    short_conv_grad_reduce,
+    short_conv_num_partials,
     sinkhorn_finalize,
     sinkhorn_momentum_update,
     sinkhorn_num_partials,

@@ -86,6 +86,13 @@ def load_library():
                                         _p, _p, _i32, _p]),
             "engram_gate_bwd_reduce_noalloc": (st, [_p, _p, _p, _p, _c.c_int, _p, _p, _p, _p, _p, _i64, _i32, _p, _p,
                                                     _p, _p, _p, _p, _p, _p, _p]),
+            "engram_short_conv_fwd": (st, [_p, _p, _c.c_int, _p, _p, _p, _p, _i32, _i64, _i32, _i32, _i32,
+                                           _c.c_float, _p, _p, _p]),
+            "engram_short_conv_num_partials": (st, [_i64, _i32, _p]),
+            "engram_short_conv_dot_blocks": (st, [_i32, _p]),
+            "engram_short_conv_bwd": (st, [_p, _p, _c.c_int, _p, _p, _p, _p, _p, _i32, _i64, _i32, _i32, _i32, _p,
+                                           _p, _p, _i32, _p]),
+            "engram_short_conv_grad_reduce": (st, [_p, _i32, _i32, _i32, _p, _p, _p, _p]),
             "engram_sinkhorn_momentum_update": (st, [_p, _c.c_int, _p, _p, _i64, _c.c_float, _i32, _p]),
             "engram_sinkhorn_num_partials": (st, [_i64, _i32, _p]),
             "engram_sinkhorn_step": (st, [_p, _p, _p, _i64, _i32, _c.c_float, _p, _p, _i32, _p]),
@@ -303,6 +310,82 @@ def gate_hc_bwd(dout, x, kv, w_fused, gate, rstd_x, rstd_k, dot, clamp: float = 
                                   _ptr(dw_partial), P, _stream(stream)),
            "engram_gate_hc_bwd")
     return dx, dkv, dw_partial
+
+
+# ----------------------------------------------------------------------------- the short conv after the gate
+
+
+def short_conv_fwd(v, norm_w, conv_w, seq_offsets, dilation: int, h=None, bias=None, eps: float = 1e-6, out=None,
+                   rstd=None, stream=None):
+    """out = h + SiLU(causal depthwise conv of RMSNorm(v)) + v, per sequence.  Returns (out, rstd)."""
+    lib = load_library()
+    _need(v, "v")
+    _need(norm_w, "norm_w", torch.float32)
+    _need(conv_w, "conv_w", torch.float32)
+    _need(seq_offsets, "seq_offsets", torch.int64)
+    if h is not None:
+        _need(h, "h", v.dtype)
+    if bias is not None:
+        _need(bias, "bias", torch.float32)
+    T, d = v.shape
+    width = conv_w.shape[1]
+    out = torch.empty_like(v) if out is None else _need(out, "out", v.dtype)
+    rstd = torch.empty(T, dtype=torch.float32, device=v.device) if rstd is None else _need(rstd, "rstd", torch.float32)
+    _check(lib.engram_short_conv_fwd(_ptr(v), _ptr(h), _DTYPES[v.dtype], _ptr(norm_w), _ptr(conv_w), _ptr(bias),
+                                     _ptr(seq_offsets), seq_offsets.numel() - 1, T, d, width, int(dilation), float(eps),
+                                     _ptr(out), _ptr(rstd), _stream(stream)),
+           "engram_short_conv_fwd")
+    return out, rstd
+
+
+def short_conv_num_partials(T: int, dilation: int) -> int:
+    lib = load_library()
+    P = _c.c_int32(0)
+    _check(lib.engram_short_conv_num_partials(T, dilation, _c.byref(P)), "engram_short_conv_num_partials")
+    return P.value
+
+
+def short_conv_dot_blocks(d: int) -> int:
+    lib = load_library()
+    nb = _c.c_int32(0)
+    _check(lib.engram_short_conv_dot_blocks(d, _c.byref(nb)), "engram_short_conv_dot_blocks")
+    return nb.value
+
+
+def short_conv_bwd(dout, v, norm_w, conv_w, rstd, seq_offsets, dilation: int, bias=None, dv=None, token_dot=None,
+                   dw_partial=None, stream=None):
+    """Returns (dv, dw_partial [P, width + 2, d]); dL/dh is dout itself."""
+    lib = load_library()
+    _need(dout, "dout", v.dtype)
+    _need(v, "v")
+    T, d = v.shape
+    width = conv_w.shape[1]
+    P = short_conv_num_partials(T, dilation)
+    dv = torch.empty_like(v) if dv is None else _need(dv, "dv", v.dtype)
+    if token_dot is None:
+        token_dot = torch.empty((T, short_conv_dot_blocks(d)), dtype=torch.float32, device=v.device)
+    if dw_partial is None:
+        dw_partial = torch.empty((P, width + 2, d), dtype=torch.float32, device=v.device)
+    _check(lib.engram_short_conv_bwd(_ptr(dout), _ptr(v), _DTYPES[v.dtype], _ptr(norm_w), _ptr(conv_w), _ptr(bias),
+                                     _ptr(rstd), _ptr(seq_offsets), seq_offsets.numel() - 1, T, d, width,
+                                     int(dilation), _ptr(dv), _ptr(token_dot), _ptr(dw_partial), P, _stream(stream)),
+           "engram_short_conv_bwd")
+    return dv, dw_partial
+
+
+def short_conv_grad_reduce(dw_partial, width: int, d: int, want_bias: bool = True, out=None, stream=None):
+    """Returns (dconv_w [d, width], dbias [d] or None, dnorm_w [d])."""
+    lib = load_library()
+    P = dw_partial.shape[0] if dw_partial is not None else 0
+    dev = dw_partial.device
+    dconv_w, dbias, dnorm_w = out if out is not None else (
+        torch.empty((d, width), dtype=torch.float32, device=dev),
+        torch.empty(d, dtype=torch.float32, device=dev) if want_bias else None,
+        torch.empty(d, dtype=torch.float32, device=dev))
+    _check(lib.engram_short_conv_grad_reduce(_ptr(dw_partial), P, width, d, _ptr(dconv_w), _ptr(dbias), _ptr(dnorm_w),
+                                             _stream(stream)),
+           "engram_short_conv_grad_reduce")
+    return dconv_w, dbias, dnorm_w
 
 
 # ----------------------------------------------------------------------------- the Engram Sinkhorn

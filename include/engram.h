@@ -313,6 +313,64 @@ engram_status engram_gate_hc_bwd(const void *dout, const void *x, const void *kv
                                  engram_stream_t stream);
 
 /* ------------------------------------------------------------------------- */
+/* The short convolution after the gate  (ch. 34 sec. 1.2 item 4)             */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * Y = SiLU(Conv1D(RMSNorm(V~))) + V~ and H <- H + Y, for V~ = the gate's output sequence [T, d].
+ * With u = V~ * rstd * norm_w, rstd = 1/sqrt(sum_j V~_j^2 / d + eps), per token t and channel c:
+ *     conv[t, c] = bias[c] + sum_{i < width} conv_w[c, i] * u[t - (width - 1 - i) * dilation, c]
+ * where u is 0 before the start of t's sequence (sequences from seq_offsets, cu_seqlens style:
+ * [num_seqs + 1] int64, 0 first, T last, non-decreasing), and
+ *     out[t, c] = h[t, c] + SiLU(conv[t, c]) + V~[t, c]        (h nullable: then without it).
+ * conv_w is [d, width] fp32 (torch's depthwise [d, 1, width] layout; tap width - 1 is the current
+ * token), norm_w [d] and bias [d] (nullable) fp32.  width 1..4, dilation >= 1 (the pages: 4 and
+ * the largest N-gram order).  rstd [T] fp32 is required: it is written and is the backward's
+ * saved statistic.  v, h, out are [T, d] in `dtype`, rows a multiple of 16 bytes, d <= 8192,
+ * 16-byte aligned; out may equal h (in place) but not v.
+ */
+engram_status engram_short_conv_fwd(const void *v, const void *h, engram_dtype dtype, const float *norm_w,
+                                    const float *conv_w, const float *bias, const int64_t *seq_offsets,
+                                    int32_t num_seqs, int64_t T, int32_t d, int32_t width, int32_t dilation,
+                                    float eps, void *out, float *rstd, engram_stream_t stream);
+
+/*
+ * Weight-gradient partials of engram_short_conv_bwd: P = ceil(T / L) * dilation with
+ * L = max(256, ceil(T / 256)) tokens per time chunk; one partial per (chunk, residue class of
+ * t mod dilation).  Depends on T and dilation only.  Host only.
+ */
+engram_status engram_short_conv_num_partials(int64_t T, int32_t dilation, int32_t *P);
+
+/* Channel blocks nb = ceil(d / 128): engram_short_conv_bwd's token_dot workspace is [T, nb] fp32. */
+engram_status engram_short_conv_dot_blocks(int32_t d, int32_t *nb);
+
+/*
+ * Backward of engram_short_conv_fwd given dout = dL/dout [T, d] and its saved rstd; dL/dh = dout
+ * (not written).  With dc = dout * SiLU'(conv) and, within each sequence,
+ *     du[t, c] = sum_i conv_w[c, i] * dc[t + (width - 1 - i) * dilation, c],
+ *     s[t]     = sum_c norm_w[c] du[t, c] V~[t, c]   (128-channel blocks in ascending order),
+ *     dv[t, c] = dout[t, c] + rstd norm_w[c] du[t, c] - rstd^3 V~[t, c] s[t] / d,
+ * dv [T, d] in `dtype` (not aliasing v or dout), token_dot [T, nb] fp32 workspace, and
+ * dw_partial [P, width + 2, d] fp32 with P = engram_short_conv_num_partials(T, dilation): row
+ * (chunk, class) holds, over that work item's tokens, sum dc * u_tap for each tap i (rows
+ * 0..width-1), sum dc (row width) and sum du * V~ * rstd (row width + 1), each token's terms in
+ * ascending time order.  Reduce it with engram_short_conv_grad_reduce.
+ */
+engram_status engram_short_conv_bwd(const void *dout, const void *v, engram_dtype dtype, const float *norm_w,
+                                    const float *conv_w, const float *bias, const float *rstd,
+                                    const int64_t *seq_offsets, int32_t num_seqs, int64_t T, int32_t d,
+                                    int32_t width, int32_t dilation, void *dv, float *token_dot, float *dw_partial,
+                                    int32_t P, engram_stream_t stream);
+
+/*
+ * dconv_w [d, width], dbias [d] (nullable) and dnorm_w [d] = the sums of the P partial rows of
+ * engram_short_conv_bwd, in a fixed order that depends on P only (64 groups of consecutive
+ * partials, each in ascending order, then the groups in ascending order).  P = 0 writes zeros.
+ */
+engram_status engram_short_conv_grad_reduce(const float *dw_partial, int32_t P, int32_t width, int32_t d,
+                                            float *dconv_w, float *dbias, float *dnorm_w, engram_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
 /* The Engram Sinkhorn of the TileKernels release: row / column L2 scaling of a  */
 /* [rows, head_dim] fp32 matrix  (ch. 34 sec. 5.3, the Engram version's four     */
 /* kernels)                                                                      */

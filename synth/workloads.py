@@ -240,3 +240,46 @@ def sinkhorn_16k_x_5120(seed: int = 7) -> SinkhornWorkload:
     """16384 rows of head_dim 5120 (the largest head_dim the release's tests use): 335 MB fp32."""
     return SinkhornWorkload(name="sinkhorn_R16384_D5120", rows=16384, head_dim=5120, grad_dtype="bf16",
                             seed=seed * 101 + 17)
+
+
+@dataclass
+class ShortConvWorkload:
+    """The short convolution after the gate over packed sequences."""
+
+    name: str
+    lengths: list
+    d: int
+    width: int
+    dilation: int
+    dtype: str
+    seed: int
+    eps: float = 1e-6
+    bias: bool = True
+    with_h: bool = True
+
+    @property
+    def T(self) -> int:
+        return int(sum(self.lengths))
+
+
+def short_conv_host_inputs(w: ShortConvWorkload):
+    """V~ = alpha * N(0, 1) with a per-token gate alpha ~ U(0, 1) (the gate's output), H and dout ~ N(0, 1);
+    norm_w ~ N(1, 0.1), conv_w [d, width] ~ N(0, 0.5), bias ~ N(0, 0.1) fp32; seq_offsets int64."""
+    T, d = w.T, w.d
+    alpha = G.uniform01(w.seed + 20, T)[:, None]
+    conv = (lambda a: a.astype(np.float32)) if w.dtype == "f32" else G.to_bf16_bits
+    out = {"v": conv(alpha * G.normal(w.seed + 21, T * d).reshape(T, d)),
+           "h": conv(G.normal(w.seed + 22, T * d).reshape(T, d)) if w.with_h else None,
+           "dout": conv(G.normal(w.seed + 23, T * d).reshape(T, d)),
+           "norm_w": G.normal(w.seed + 24, d, 1.0, 0.1).astype(np.float32),
+           "conv_w": G.normal(w.seed + 25, d * w.width, 0.0, 0.5).astype(np.float32).reshape(d, w.width),
+           "bias": G.normal(w.seed + 26, d, 0.0, 0.1).astype(np.float32) if w.bias else None,
+           "seq_offsets": G.offsets_from_lengths(w.lengths)}
+    return out
+
+
+def short_conv_4x4k(seed: int = 8) -> ShortConvWorkload:
+    """After the gate's micro-batch: 4 sequences x 4096 tokens, d = 4096 bf16, width 4, dilation 3
+    (the largest N-gram order of the hash workload)."""
+    return ShortConvWorkload(name="short_conv_4x4096_d4096", lengths=[4096] * 4, d=4096, width=4, dilation=3,
+                             dtype="bf16", seed=seed * 101 + 19)
