@@ -7,18 +7,23 @@
 // GB300 design.  The convolution couples tokens only along time, one channel at a time, and the
 // RMSNorm couples channels only within a token, through one scalar.  So:
 //   * conv_rstd_kernel: a warp per token computes rstd = 1/sqrt(mean(V~^2) + eps);
-//   * conv_stencil_kernel: a warp owns 128 channels of one residue class t = r (mod dilation):
-//     every tap of a class token lies in the same class, so the warp sweeps its tokens in time
-//     order keeping the last three taps' inputs in registers, with no other warp involved.  Each
-//     warp streams its rows (V~ and H, or V~ and dout) through its own ring of shared-memory
-//     stages filled by 1-D bulk (TMA) copies that its lane 0 issues, so the bytes in flight do not
-//     depend on occupancy.  Per-token scalars (rstd, and the backward's row dots) come 64 tokens at
-//     a time, two per lane, one window ahead, and reach a token by a shuffle.
+//   * conv_fwd_kernel: persistent CTAs, each on one 512-byte channel block, stream tiles of 64
+//     tokens plus the taps' halo into shared memory with 1-D bulk (TMA) copies, two or three tiles
+//     in flight, and compute every output from the tile: the taps are read back from shared memory
+//     instead of being carried along time, so there is no per-token bookkeeping;
+//   * conv_stencil_kernel (the backward): a warp owns 128 channels of one residue class
+//     t = r (mod dilation).  Every tap of a class token lies in the same class, so the warp sweeps
+//     its tokens in time order carrying the last three taps' inputs and the du still collecting
+//     contributions in registers.  Each warp streams its rows (V~ and dout) through its own ring of
+//     shared-memory stages filled by bulk copies that its lane 0 issues, and keeps a stage resident
+//     for the three tokens that read it back.  Per-token scalars (rstd, the row dots) come 64
+//     tokens at a time, two per lane, one window ahead, and reach a token by a shuffle.
 // The backward is two sweeps: the first gives each token's partial dot s = sum_j norm_w du V~ over
-// the warp's channels, the second the full dV~ = dout + rstd norm_w du - rstd^3 V~ s / d with s
-// summed over the warps in a fixed order, and the weight-gradient partials of its (time chunk,
-// residue) work item.  conv_grad_reduce_kernel sums those partials in a fixed order.  The time
-// chunks depend on T only, so the weight gradients are bitwise reproducible on any GPU.
+// the warp's channels and the taps' and bias's gradient partials of its (time chunk, residue) work
+// item, the second the full dV~ = dout + rstd norm_w du - rstd^3 V~ s / d with s summed over the
+// channel blocks in a fixed order, and the norm weight's partials.  conv_grad_reduce_kernel sums
+// the partials in a fixed order.  The time chunks depend on T only, so the weight gradients are
+// bitwise reproducible on any GPU.
 #include <algorithm>
 
 #include "engram_internal.cuh"
@@ -32,7 +37,7 @@ constexpr int kScAges = 4;              // taps: width <= 4
 constexpr int kScRingBytes = 8192;      // per warp: stages x (V~ segment + second segment)
 constexpr int kScMaxBlocks = 64;        // channel blocks per row: d <= 64 * 128
 
-enum ScMode { kScFwd = 0, kScBwdDot = 1, kScBwdFinal = 2 };
+enum ScMode { kScBwdDot = 1, kScBwdFinal = 2 };  // the backward sweeps
 
 struct ScParams {
     const uint8_t *v;          // V~ [T, d]
@@ -67,7 +72,9 @@ template <>
 struct Ev4<float> {
     static constexpr int kBytes = 16;
     __device__ __forceinline__ static void load_smem(const uint8_t *p, float (&x)[4]) {
-        const uint4 u = ld_shared_v4(p);
+        uint4 u;
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(u.x), "=r"(u.y), "=r"(u.z), "=r"(u.w)
+                     : "r"(smem_addr(p)));
         x[0] = __uint_as_float(u.x), x[1] = __uint_as_float(u.y), x[2] = __uint_as_float(u.z),
         x[3] = __uint_as_float(u.w);
     }
@@ -81,7 +88,7 @@ struct Ev4<__nv_bfloat16> {
     static constexpr int kBytes = 8;
     __device__ __forceinline__ static void load_smem(const uint8_t *p, float (&x)[4]) {
         uint32_t a, b;
-        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(a), "=r"(b) : "r"(smem_addr(p)) : "memory");
+        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(a), "=r"(b) : "r"(smem_addr(p)));
         x[0] = __uint_as_float(a << 16), x[1] = __uint_as_float(a & 0xffff0000u);
         x[2] = __uint_as_float(b << 16), x[3] = __uint_as_float(b & 0xffff0000u);
     }
@@ -91,7 +98,9 @@ struct Ev4<__nv_bfloat16> {
     }
 };
 
-__device__ __forceinline__ float sc_sigmoid(float c) { return 1.0f / (1.0f + expf(-c)); }
+// SiLU's sigmoid with the fast exponential and division (a few ulp; the outputs are rounded far
+// coarser, and the tolerances carry the bound).
+__device__ __forceinline__ float sc_sigmoid_fast(float c) { return __fdividef(1.0f, 1.0f + __expf(-c)); }
 
 // Index of the sequence holding token t: the largest s with offs[s] <= t (offsets assumed sorted).
 __device__ __forceinline__ int sc_seq_of(const int64_t *offs, int num_seqs, int64_t t) {
@@ -116,7 +125,7 @@ __global__ void __launch_bounds__(256) conv_rstd_kernel(const uint8_t *__restric
     for (int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += warps) {
         const uint4 *row = reinterpret_cast<const uint4 *>(v + static_cast<size_t>(t) * d * sizeof(E));
         float ss = 0.f;
-#pragma unroll 4
+#pragma unroll 8
         for (int j = lane; j < nvec; j += 32) {
             float x[V::N];
             V::unpack(__ldcs(row + j), x);
@@ -128,22 +137,213 @@ __global__ void __launch_bounds__(256) conv_rstd_kernel(const uint8_t *__restric
     }
 }
 
+// ------------------------------------------------------------------------------- forward
+
+constexpr int kScTileTokens = 64;       // tokens per forward tile
+constexpr int kScMaxDil = 32;           // forward: the halo of (width - 1) * dilation rows stays small
+
+// Shared memory of one tile buffer: rows [rows_max][32] uint4, rstd [rows_max], sequence starts
+// [kScTileTokens] int64; two buffers, then two mbarriers.
+__host__ __device__ inline int sc_fwd_buf_bytes(int width, int dil) {
+    const int rows = kScTileTokens + (width - 1) * dil;
+    // rounded to 128 bytes: the second buffer's rows are bulk-copy destinations (16-byte aligned)
+    return (rows * 512 + ((rows + 1) & ~1) * 4 + kScTileTokens * 8 + 127) & ~127;
+}
+// three tile buffers where they fit two CTAs per SM, else two
+inline int sc_fwd_nbuf(int width, int dil) { return 3 * sc_fwd_buf_bytes(width, dil) + 24 <= 113 * 1024 ? 3 : 2; }
+inline int sc_fwd_smem(int width, int dil) { return sc_fwd_nbuf(width, dil) * (sc_fwd_buf_bytes(width, dil) + 8); }
+
+struct ScFwdParams {
+    const uint8_t *v, *h;
+    const float *norm_w, *conv_w, *bias, *rstd;
+    const int64_t *offs;
+    uint8_t *out;
+    uint32_t *status;
+    int64_t T;
+    int32_t num_seqs, d, width, dil, nblk, ntiles, nbuf;
+};
+
+// Persistent CTAs, each on one channel block of 512 bytes (its taps, folded with norm_w, loaded
+// once) and the tiles j, j + J, ... of kScTileTokens tokens (J CTAs per block).  A tile's V~ rows and
+// the halo of (width - 1) * dilation rows before it reach shared memory by 1-D bulk (TMA) copies,
+// one row segment per lane of warp 0, completing on the buffer's mbarrier; the next one or two
+// tiles' copies are in flight while this one is computed.  Lane l of warp w computes channel vector l of the
+// tile's tokens w, w + 8, ...:
+//   conv = bias + sum_a (conv_w[width-1-a] norm_w) rstd[t - a dil] V~[t - a dil],
+//   out  = H + SiLU(conv) + V~,
+// with taps before the token's sequence start left out.
+template <typename E>
+__global__ void __launch_bounds__(256, 2) conv_fwd_kernel(const __grid_constant__ ScFwdParams p) {
+    using V = Vec<E>;
+    constexpr int N = V::N;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int width = p.width, dil = p.dil;
+    const int halo = (width - 1) * dil;
+    const int rows_max = kScTileTokens + halo;
+    const int buf_bytes = sc_fwd_buf_bytes(width, dil);
+    const int nbuf = p.nbuf;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + static_cast<size_t>(nbuf) * buf_bytes);
+    const int nvec = p.d / N;
+    const int cb = static_cast<int>(blockIdx.x % p.nblk);
+    const int J = static_cast<int>(gridDim.x / p.nblk);
+    const int j0 = static_cast<int>(blockIdx.x / p.nblk);
+    if (j0 >= J) return;  // whole CTA: a grid that is not a multiple of the block count
+    const int jv = cb * 32 + lane;
+    const bool active = jv < nvec;
+    const int jv_c = active ? jv : 0;
+    const int nv_blk = nvec - cb * 32 < 32 ? nvec - cb * 32 : 32;
+    const uint32_t seg = static_cast<uint32_t>(nv_blk) * 16u;
+    const size_t row_bytes = static_cast<size_t>(nvec) * 16;
+
+    auto tile_rows = [&](int b) { return reinterpret_cast<uint4(*)[32]>(smem + static_cast<size_t>(b) * buf_bytes); };
+    auto tile_rs = [&](int b) {
+        return reinterpret_cast<float *>(smem + static_cast<size_t>(b) * buf_bytes + static_cast<size_t>(rows_max) * 512);
+    };
+    auto tile_ss = [&](int b) {
+        return reinterpret_cast<int64_t *>(smem + static_cast<size_t>(b) * buf_bytes +
+                                           static_cast<size_t>(rows_max) * 512 + ((rows_max + 1) & ~1) * 4);
+    };
+    // tile j covers tokens [j K, min(T, (j + 1) K)) and buffers rows from max(0, j K - halo)
+    auto first_row = [&](int j) {
+        const int64_t t0 = static_cast<int64_t>(j) * kScTileTokens;
+        return t0 - halo > 0 ? t0 - halo : static_cast<int64_t>(0);
+    };
+    auto tile_end = [&](int j) {
+        const int64_t t1 = (static_cast<int64_t>(j) + 1) * kScTileTokens;
+        return t1 < p.T ? t1 : p.T;
+    };
+    // start tile j's copies into buffer b (warp 0), and its rstd and sequence starts (all threads)
+    auto stage_tile = [&](int j, int b) {
+        const int64_t r0 = first_row(j), t0 = static_cast<int64_t>(j) * kScTileTokens, t1 = tile_end(j);
+        const int nrows = static_cast<int>(t1 - r0);
+        if (warp == 0) {
+            if (lane == 0) mbar_arrive_expect_tx(&bars[b], seg * static_cast<uint32_t>(nrows));
+            __syncwarp();
+            uint4(*rows)[32] = tile_rows(b);
+            for (int i = lane; i < nrows; i += 32)
+                bulk_load_plain(&rows[i][0], p.v + static_cast<size_t>(r0 + i) * row_bytes + static_cast<size_t>(cb) * 512,
+                                seg, &bars[b]);
+        }
+        float *rs = tile_rs(b);
+        for (int i = threadIdx.x; i < nrows; i += blockDim.x) rs[i] = __ldg(p.rstd + r0 + i);
+        if (threadIdx.x < t1 - t0) tile_ss(b)[threadIdx.x] = __ldg(p.offs + sc_seq_of(p.offs, p.num_seqs, t0 + threadIdx.x));
+    };
+
+    // this lane's channels: the taps by age folded with norm_w, and the bias (16-byte loads)
+    float KW[kScAges][N], bv[N];
+    {
+        float nw[N], cw[N][kScAges];
+        const float4 *nw4 = reinterpret_cast<const float4 *>(p.norm_w + static_cast<size_t>(jv_c) * N);
+        const float4 *b4 = p.bias ? reinterpret_cast<const float4 *>(p.bias + static_cast<size_t>(jv_c) * N) : nullptr;
+#pragma unroll
+        for (int q = 0; q < N / 4; ++q) {
+            const float4 a = __ldg(nw4 + q);
+            nw[4 * q] = a.x, nw[4 * q + 1] = a.y, nw[4 * q + 2] = a.z, nw[4 * q + 3] = a.w;
+            const float4 bb = b4 ? __ldg(b4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+            bv[4 * q] = bb.x, bv[4 * q + 1] = bb.y, bv[4 * q + 2] = bb.z, bv[4 * q + 3] = bb.w;
+        }
+#pragma unroll
+        for (int e = 0; e < N; ++e) {
+            const size_t c = static_cast<size_t>(jv_c) * N + e;
+            if (width == kScAges) {
+                const float4 w4 = __ldg(reinterpret_cast<const float4 *>(p.conv_w + c * kScAges));
+                cw[e][0] = w4.x, cw[e][1] = w4.y, cw[e][2] = w4.z, cw[e][3] = w4.w;
+            } else {
+#pragma unroll
+                for (int i = 0; i < kScAges; ++i) cw[e][i] = i < width ? __ldg(p.conv_w + c * width + i) : 0.f;
+            }
+#pragma unroll
+            for (int a = 0; a < kScAges; ++a) KW[a][e] = a < width ? cw[e][width - 1 - a] * nw[e] : 0.f;
+        }
+    }
+    const uint4 *h4 = p.h ? reinterpret_cast<const uint4 *>(p.h) + jv_c : nullptr;
+    uint4 *o4 = reinterpret_cast<uint4 *>(p.out) + jv_c;
+
+    if (threadIdx.x == 0) {
+        for (int q = 0; q < nbuf; ++q) mbar_init(&bars[q], 1);
+        mbar_init_fence();
+    }
+    __syncthreads();
+    for (int q = 0; q < nbuf - 1 && j0 + q * J < p.ntiles; ++q) stage_tile(j0 + q * J, q);
+    __syncthreads();  // the first tiles' rstd and sequence starts
+
+    constexpr int kPer = kScTileTokens / 8;  // tokens per warp and tile, their H rows in two halves
+    constexpr int kHalf = kPer / 2;
+    int it = 0;
+    for (int j = j0; j < p.ntiles; j += J, ++it) {
+        const int b = it % nbuf;
+        const uint32_t phase = static_cast<uint32_t>((it / nbuf) & 1);
+        const int jn = j + (nbuf - 1) * J;
+        const int bn = (it + nbuf - 1) % nbuf;
+        if (jn < p.ntiles) stage_tile(jn, bn);  // freed by the previous tile's closing barrier
+        const int64_t t0 = static_cast<int64_t>(j) * kScTileTokens, t1 = tile_end(j), r0 = first_row(j);
+        uint4 hv[kHalf];
+        auto load_h = [&](int k0) {
+#pragma unroll
+            for (int k = 0; k < kHalf; ++k) {
+                const int64_t t = t0 + warp + 8 * (k0 + k);
+                hv[k] = (h4 && t < t1) ? __ldcs(h4 + static_cast<size_t>(t) * nvec) : make_uint4(0u, 0u, 0u, 0u);
+            }
+        };
+        load_h(0);
+        const bool ok = mbar_wait(&bars[b], phase);
+        if (__syncthreads_or(!ok)) {
+            // a copy that never landed: report, and let thread 0 wait (bounded) for what is in flight
+            if (threadIdx.x == 0) {
+                report(p.status, nullptr, ENGRAM_DEVERR_TIMEOUT);
+                for (int q = 0; q < nbuf - 1 && j + q * J < p.ntiles; ++q)
+                    mbar_wait(&bars[(it + q) % nbuf], static_cast<uint32_t>(((it + q) / nbuf) & 1));
+            }
+            return;
+        }
+        uint4(*rows)[32] = tile_rows(b);
+        const float *rs = tile_rs(b);
+        const int64_t *ss = tile_ss(b);
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            if (k == kHalf) load_h(kHalf);
+            const int lt = warp + 8 * k;
+            const int64_t t = t0 + lt;
+            if (t >= t1) break;
+            const int64_t s0 = ss[lt];
+            float c[N], x0[N];
+#pragma unroll
+            for (int e = 0; e < N; ++e) c[e] = bv[e];
+#pragma unroll
+            for (int a = 0; a < kScAges; ++a) {
+                const int64_t ta = t - static_cast<int64_t>(a) * dil;
+                if (a < width && ta >= s0) {
+                    const int ri = static_cast<int>(ta - r0);
+                    float x[N];
+                    V::unpack(rows[ri][lane], x);
+                    const float ra = rs[ri];
+#pragma unroll
+                    for (int e = 0; e < N; ++e) c[e] = fmaf(KW[a][e], x[e] * ra, c[e]);
+                    if (a == 0) {
+#pragma unroll
+                        for (int e = 0; e < N; ++e) x0[e] = x[e];
+                    }
+                }
+            }
+            float y[N];
+            V::unpack(hv[k % kHalf], y);
+            float o[N];
+#pragma unroll
+            for (int e = 0; e < N; ++e) o[e] = fmaf(c[e], sc_sigmoid_fast(c[e]), x0[e] + y[e]);
+            if (active) __stcs(o4 + static_cast<size_t>(t) * nvec, V::pack(o));
+        }
+        __syncthreads();  // buffer b is free; the next tile's rstd and sequence starts are visible
+    }
+}
+
 // ------------------------------------------------------------------------------- the stencil sweep
 
 // Per-token scalars of the warp's sweep (indexed by the sweep position q), 64 at a time: lane l
 // holds positions w0 + l and w0 + 32 + l of the current window and the next window's two.
 struct ScWindow {
     float lo, hi, nlo, nhi;
-    int64_t w0;
 };
-
-// The row-dot total of token t: the nb partials in ascending order.
-__device__ __forceinline__ float sc_dot_total(const ScParams &p, int64_t t) {
-    const float *row = p.token_dot + static_cast<size_t>(t) * p.nb;
-    float s = 0.f;
-    for (int b = 0; b < p.nb; ++b) s += __ldg(row + b);
-    return s;
-}
 
 template <typename E, int MODE>
 __global__ void __launch_bounds__(kScWarps * 32) conv_stencil_kernel(const __grid_constant__ ScParams p) {
@@ -188,13 +388,6 @@ __global__ void __launch_bounds__(kScWarps * 32) conv_stencil_kernel(const __gri
     // the sweep: class tokens from up to three taps before the chunk (their inputs only) to the
     // chunk's end, or three taps past it for the backward (their dc completes the chunk's du)
     const int64_t t_first = first_class(t_lo);
-    float dK[kScAges][kScEV], db[kScEV], dnw[kScEV];
-#pragma unroll
-    for (int e = 0; e < kScEV; ++e) {
-        db[e] = dnw[e] = 0.f;
-#pragma unroll
-        for (int a = 0; a < kScAges; ++a) dK[a][e] = 0.f;
-    }
     int64_t n_sw = 0, t_a = t_first;
     int s = 0;
     if (t_first < t_hi) {
@@ -202,79 +395,123 @@ __global__ void __launch_bounds__(kScWarps * 32) conv_stencil_kernel(const __gri
         const int64_t hist = t_first - static_cast<int64_t>(kScAges - 1) * dil;
         const int64_t s0 = __ldg(p.offs + s);
         t_a = first_class(hist > s0 ? hist : s0);
-        int64_t t_b = MODE == kScFwd ? t_hi : t_hi + static_cast<int64_t>(kScAges - 1) * dil;
+        int64_t t_b = t_hi + static_cast<int64_t>(kScAges - 1) * dil;
         if (t_b > p.T) t_b = p.T;
         n_sw = (t_b - t_a + dil - 1) / dil;
     }
 
+    // lane 0 streams the sweep's rows: a lead-in token (before the chunk) needs V~ only.  A stage
+    // stays resident for three tokens after its own, which read it back as their taps' inputs.
     const uint64_t pol = l2_evict_first_policy();
-    const bool two = MODE != kScFwd || p.x2 != nullptr;
-    // lane 0: sweep position q into stage q % S; a lead-in token (before the chunk) needs V~ only
-    auto issue = [&](int64_t q) {
-        const int st = static_cast<int>(q % S);
-        const int64_t t = t_a + q * dil;
-        const bool second = two && t >= t_lo;
-        uint8_t *dst = ring + static_cast<size_t>(st) * 2 * seg_max;
-        mbar_arrive_expect_tx(&full[st], second ? 2 * seg : seg);
-        bulk_load(dst, p.v + static_cast<size_t>(t) * row_bytes + static_cast<size_t>(c0) * sizeof(E), seg, &full[st],
-                  pol);
-        if (second)
-            bulk_load(dst + seg_max, p.x2 + static_cast<size_t>(t) * row_bytes + static_cast<size_t>(c0) * sizeof(E),
-                      seg, &full[st], pol);
+    constexpr bool two = true;
+    const size_t col_off = static_cast<size_t>(c0) * sizeof(E);
+    const size_t step_bytes = static_cast<size_t>(dil) * row_bytes;
+    const uint8_t *src_v = p.v + static_cast<size_t>(t_a) * row_bytes + col_off;
+    const uint8_t *src_2 = two ? p.x2 + static_cast<size_t>(t_a) * row_bytes + col_off : nullptr;
+    int64_t issued = 0, t_issue = t_a;
+    int ist = 0;
+    auto issue = [&]() {
+        const bool second = two && t_issue >= t_lo;
+        uint8_t *dst = ring + static_cast<size_t>(ist) * 2 * seg_max;
+        mbar_arrive_expect_tx(&full[ist], second ? 2 * seg : seg);
+        bulk_load(dst, src_v, seg, &full[ist], pol);
+        if (second) bulk_load(dst + seg_max, src_2, seg, &full[ist], pol);
+        src_v += step_bytes;
+        if (two) src_2 += step_bytes;
+        t_issue += dil;
+        ++issued;
+        if (++ist == S) ist = 0;
     };
-    int64_t issued = 0;
     if (lane == 0) {
         for (int q = 0; q < S; ++q) mbar_init(&full[q], 1);
         mbar_init_fence();
-        for (; issued < S && issued < n_sw; ++issued) issue(issued);
+        while (issued < S && issued < n_sw) issue();
     }
     __syncwarp();
 
-    // scalar windows: rstd, and the backward's row-dot totals in the final sweep
-    auto scalar_at = [&](int64_t q, bool dot) -> float {
-        const int64_t t = t_a + q * dil;
-        if (q >= n_sw) return 0.f;
-        return dot ? sc_dot_total(p, t) : __ldg(p.rstd + t);
+    // positions q of the sweep (token t_a + q dil): the chunk's tokens are [q_lo, q_hi)
+    const int64_t n_sw_l = n_sw;
+    const int nq = static_cast<int>(n_sw_l);
+    const int q_lo = static_cast<int>((t_first - t_a) / dil);
+    const int q_hi = static_cast<int>((t_hi - t_a + dil - 1) / dil);
+    const int nb = p.nb;
+    const float inv_d = 1.0f / static_cast<float>(p.d);
+    const int num_seqs = p.num_seqs;
+    const int64_t *offs = p.offs;
+    const float *rstd_p = p.rstd;
+    const float *tdot = p.token_dot;
+    float *tdot_out = p.token_dot_out;
+    auto pos_of = [&](int64_t tt) {  // first position whose token is >= tt
+        return tt <= t_a ? 0 : static_cast<int>((tt - t_a + dil - 1) / dil);
     };
-    ScWindow wr{0.f, 0.f, scalar_at(lane, false), scalar_at(32 + lane, false), -64};
-    ScWindow ws{0.f, 0.f, 0.f, 0.f, -64};
-    if (MODE == kScBwdFinal) ws.nlo = scalar_at(lane, true), ws.nhi = scalar_at(32 + lane, true);
 
-    // histories by age (1..3): the RMSNorm output u, the raw inputs and scalars of those tokens,
-    // and (backward) the du still collecting contributions and the token it belongs to
+    // scalar windows: rstd, and the backward's row-dot totals (column 0 of token_dot) in the final sweep
+    auto scalar_at = [&](int q, bool dot) -> float {
+        if (q >= nq) return 0.f;
+        const int64_t t = t_a + static_cast<int64_t>(q) * dil;
+        return dot ? __ldg(tdot + static_cast<size_t>(t) * nb) : __ldg(rstd_p + t);
+    };
+    ScWindow wr{0.f, 0.f, scalar_at(lane, false), scalar_at(32 + lane, false)};
+    ScWindow ws{0.f, 0.f, 0.f, 0.f};
+    if (MODE == kScBwdFinal) ws.nlo = scalar_at(lane, true), ws.nhi = scalar_at(32 + lane, true);
+    int w0 = -64;
+
+    // histories by age (1..3): the RMSNorm output u and the scalars of those tokens, and (backward)
+    // the du still collecting contributions and whether its token is the chunk's.  The raw rows of
+    // those tokens stay in their stages.
     float u1[kScEV] = {}, u2[kScEV] = {}, u3[kScEV] = {};
-    float x1[kScEV] = {}, x2[kScEV] = {}, x3[kScEV] = {};
-    float g1[kScEV] = {}, g2[kScEV] = {}, g3[kScEV] = {};
     float P1[kScEV] = {}, P2[kScEV] = {}, P3[kScEV] = {};
     float r1 = 0.f, r2 = 0.f, r3 = 0.f, sd1 = 0.f, sd2 = 0.f, sd3 = 0.f;
-    int64_t pend1 = -1, pend2 = -1, pend3 = -1;
-    int64_t seq_end = n_sw > 0 ? __ldg(p.offs + s + 1) : 0;
+    bool pend1 = false, pend2 = false, pend3 = false;
+    int q_seq_end = nq > 0 ? pos_of(__ldg(offs + s + 1)) : 0;
+    float dK[kScAges][kScEV], db[kScEV], dnw[kScEV];
+#pragma unroll
+    for (int e = 0; e < kScEV; ++e) {
+        db[e] = dnw[e] = 0.f;
+#pragma unroll
+        for (int a = 0; a < kScAges; ++a) dK[a][e] = 0.f;
+    }
+    int st = 0;          // stage of position q
+    uint32_t ph = 0;     // its phase
+    auto stage_back = [&](int a) { return st - a < 0 ? st - a + S : st - a; };
+    // this lane's output row segment of position q, and the row-dot entry
+    uint8_t *out_q = p.out ? p.out + static_cast<size_t>(t_a) * row_bytes + col_off + lane * EV::kBytes : nullptr;
+    float *dot_q = tdot_out ? tdot_out + static_cast<size_t>(t_a) * nb + cb : nullptr;
+    const size_t dot_step = static_cast<size_t>(dil) * nb;
 
-    // backward: a token's du is complete -> its row-dot partial, or its dv and dnorm_w share
-    auto emit = [&](int64_t te, const float (&du)[kScEV], const float (&x)[kScEV], const float (&g)[kScEV], float rt,
-                    float sd) {
+    // backward: a token's du is complete -> its row-dot partial, or its dv and dnorm_w share.  Its
+    // V~ and dout are read back from its stage, `age` positions behind the current one.
+    auto emit = [&](int age, const float (&du)[kScEV], float rt, float sd) {
+        float x[kScEV] = {}, g[kScEV] = {};
+        const uint8_t *stg = ring + static_cast<size_t>(stage_back(age)) * 2 * seg_max;
+        if (active) {
+            EV::load_smem(stg + lane * EV::kBytes, x);
+            if (MODE == kScBwdFinal) EV::load_smem(stg + seg_max + lane * EV::kBytes, g);
+        }
         if (MODE == kScBwdDot) {
             float acc = 0.f;
 #pragma unroll
             for (int e = 0; e < kScEV; ++e) acc = fmaf(nw[e] * du[e], x[e], acc);
             acc = warp_sum(acc);
-            if (lane == 0) p.token_dot_out[static_cast<size_t>(te) * p.nb + cb] = acc;
+            if (lane == 0) dot_q[-static_cast<ptrdiff_t>(age * dot_step)] = acc;
         } else if (MODE == kScBwdFinal) {
-            const float k3 = rt * rt * rt * sd / static_cast<float>(p.d);
+            const float k3 = rt * rt * rt * sd * inv_d;
             float o[kScEV];
 #pragma unroll
             for (int e = 0; e < kScEV; ++e) {
                 o[e] = g[e] + rt * nw[e] * du[e] - k3 * x[e];
                 dnw[e] = fmaf(du[e] * x[e], rt, dnw[e]);
             }
-            if (active) EV::store(p.out + static_cast<size_t>(te) * row_bytes + (c0 + lane * kScEV) * sizeof(E), o);
+            if (active) EV::store(out_q - static_cast<ptrdiff_t>(age * step_bytes), o);
         }
     };
+    // the pending du have no more contributions (a sequence ended, or the sweep did); called
+    // before position q is processed, so the pending tokens sit 1..3 positions back
     auto flush = [&]() {
-        if (pend3 >= 0) emit(pend3, P3, x3, g3, r3, sd3);
-        if (pend2 >= 0) emit(pend2, P2, x2, g2, r2, sd2);
-        if (pend1 >= 0) emit(pend1, P1, x1, g1, r1, sd1);
-        pend1 = pend2 = pend3 = -1;
+        if (pend3) emit(3, P3, r3, sd3);
+        if (pend2) emit(2, P2, r2, sd2);
+        if (pend1) emit(1, P1, r1, sd1);
+        pend1 = pend2 = pend3 = false;
 #pragma unroll
         for (int e = 0; e < kScEV; ++e) {
             u1[e] = u2[e] = u3[e] = 0.f;
@@ -283,75 +520,62 @@ __global__ void __launch_bounds__(kScWarps * 32) conv_stencil_kernel(const __gri
     };
 
     bool failed = false;
-    int64_t q = 0;
-    for (; q < n_sw; ++q) {
-        const int64_t t = t_a + q * dil;
+    int q = 0;
+    for (; q < nq; ++q) {
         // a new sequence: the taps reach back no further, and the pending du are complete
-        if (t >= seq_end) {
-            if (MODE != kScFwd) flush();
-            else {
-#pragma unroll
-                for (int e = 0; e < kScEV; ++e) u1[e] = u2[e] = u3[e] = 0.f;
-            }
-            if (t >= t_hi) break;  // the backward's look-ahead stays in the chunk's last sequence
-            while (s + 1 < p.num_seqs && t >= __ldg(p.offs + s + 1)) ++s;
-            seq_end = __ldg(p.offs + s + 1);
+        if (q >= q_seq_end) {
+            flush();
+            if (q >= q_hi) break;  // the backward's look-ahead stays in the chunk's last sequence
+            const int64_t t = t_a + static_cast<int64_t>(q) * dil;
+            while (s + 1 < num_seqs && t >= __ldg(offs + s + 1)) ++s;
+            q_seq_end = pos_of(__ldg(offs + s + 1));
+            if (q_seq_end <= q) q_seq_end = q + 1;  // malformed offsets: treat the token as its own sequence
         }
         // scalars of position q
-        if (q - wr.w0 >= 64) {
-            wr.w0 += 64;
+        if (q - w0 >= 64) {
+            w0 += 64;
             wr.lo = wr.nlo, wr.hi = wr.nhi;
-            wr.nlo = scalar_at(wr.w0 + 64 + lane, false), wr.nhi = scalar_at(wr.w0 + 96 + lane, false);
+            wr.nlo = scalar_at(w0 + 64 + lane, false), wr.nhi = scalar_at(w0 + 96 + lane, false);
             if (MODE == kScBwdFinal) {
-                ws.w0 = wr.w0;
                 ws.lo = ws.nlo, ws.hi = ws.nhi;
-                ws.nlo = scalar_at(wr.w0 + 64 + lane, true), ws.nhi = scalar_at(wr.w0 + 96 + lane, true);
+                ws.nlo = scalar_at(w0 + 64 + lane, true), ws.nhi = scalar_at(w0 + 96 + lane, true);
             }
         }
-        const int wq = static_cast<int>(q - wr.w0);
+        const int wq = q - w0;
         const float rt = __shfl_sync(0xffffffffu, wq < 32 ? wr.lo : wr.hi, wq & 31);
         const float sdt = MODE == kScBwdFinal ? __shfl_sync(0xffffffffu, wq < 32 ? ws.lo : ws.hi, wq & 31) : 0.f;
 
-        // the row segments of token t
-        const int st = static_cast<int>(q % S);
-        const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[st], static_cast<uint32_t>((q / S) & 1)));
+        // the row segments of position q
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[st], ph));
         if (!ok) {
             if (lane == 0) report(p.status, nullptr, ENGRAM_DEVERR_TIMEOUT);
             failed = true;
             break;
         }
         const uint8_t *stage = ring + static_cast<size_t>(st) * 2 * seg_max;
+        const bool in_chunk = q >= q_lo && q < q_hi;
+        const bool led = q < q_lo;  // lead-in: the taps' inputs only
         float x0[kScEV] = {}, y0[kScEV] = {};
         if (active) {
             EV::load_smem(stage + lane * EV::kBytes, x0);
-            if (two && t >= t_lo) EV::load_smem(stage + seg_max + lane * EV::kBytes, y0);
+            if (two && !led) EV::load_smem(stage + seg_max + lane * EV::kBytes, y0);
         }
-        __syncwarp();
-        if (lane == 0 && issued < n_sw) issue(issued++);  // every lane holds its part of the stage
 
         float u0[kScEV], c[kScEV];
 #pragma unroll
         for (int e = 0; e < kScEV; ++e) {
             u0[e] = x0[e] * rt * nw[e];
-            c[e] = bias[e] + K[0][e] * u0[e] + K[1][e] * u1[e] + K[2][e] * u2[e] + K[3][e] * u3[e];
+            c[e] = fmaf(K[3][e], u3[e], fmaf(K[2][e], u2[e], fmaf(K[1][e], u1[e], fmaf(K[0][e], u0[e], bias[e]))));
         }
-        const bool in_chunk = t >= t_lo && t < t_hi;
-        if (MODE == kScFwd) {
-            if (in_chunk && active) {
-                float o[kScEV];
-#pragma unroll
-                for (int e = 0; e < kScEV; ++e) o[e] = c[e] * sc_sigmoid(c[e]) + x0[e] + y0[e];
-                EV::store(p.out + static_cast<size_t>(t) * row_bytes + (c0 + lane * kScEV) * sizeof(E), o);
-            }
-        } else {
+        {
             // dc = dout SiLU'(c) for the chunk's tokens and the look-ahead; 0 for the lead-in
             float dc[kScEV];
 #pragma unroll
             for (int e = 0; e < kScEV; ++e) {
-                const float sg = sc_sigmoid(c[e]);
-                dc[e] = t >= t_lo ? y0[e] * sg * (1.0f + c[e] * (1.0f - sg)) : 0.f;
+                const float sg = sc_sigmoid_fast(c[e]);
+                dc[e] = led ? 0.f : y0[e] * sg * fmaf(c[e], 1.0f - sg, 1.0f);
             }
-            if (MODE == kScBwdFinal && in_chunk) {
+            if (MODE == kScBwdDot && in_chunk) {  // the taps' and the bias's gradients, in the first sweep
 #pragma unroll
                 for (int e = 0; e < kScEV; ++e) {
                     db[e] += dc[e];
@@ -362,11 +586,11 @@ __global__ void __launch_bounds__(kScWarps * 32) conv_stencil_kernel(const __gri
                 }
             }
             // the token three taps back has all its contributions
-            if (pend3 >= 0) {
+            if (pend3) {
                 float du[kScEV];
 #pragma unroll
                 for (int e = 0; e < kScEV; ++e) du[e] = fmaf(K[3][e], dc[e], P3[e]);
-                emit(pend3, du, x3, g3, r3, sd3);
+                emit(3, du, r3, sd3);
             }
 #pragma unroll
             for (int e = 0; e < kScEV; ++e) {
@@ -374,30 +598,38 @@ __global__ void __launch_bounds__(kScWarps * 32) conv_stencil_kernel(const __gri
                 P2[e] = fmaf(K[1][e], dc[e], P1[e]);
                 P1[e] = K[0][e] * dc[e];
             }
-            pend3 = pend2, pend2 = pend1, pend1 = in_chunk ? t : -1;
+            pend3 = pend2, pend2 = pend1, pend1 = in_chunk;
         }
-        // age the histories
+        // age the histories and move to the next position
 #pragma unroll
-        for (int e = 0; e < kScEV; ++e) {
-            u3[e] = u2[e], u2[e] = u1[e], u1[e] = u0[e];
-            x3[e] = x2[e], x2[e] = x1[e], x1[e] = x0[e];
-            g3[e] = g2[e], g2[e] = g1[e], g1[e] = y0[e];
-        }
+        for (int e = 0; e < kScEV; ++e) u3[e] = u2[e], u2[e] = u1[e], u1[e] = u0[e];
         r3 = r2, r2 = r1, r1 = rt;
         sd3 = sd2, sd2 = sd1, sd1 = sdt;
+        if (++st == S) {
+            st = 0;
+            ph ^= 1u;
+        }
+        if (out_q) out_q += step_bytes;
+        if (dot_q) dot_q += dot_step;
+        // positions q - 2 .. q stay resident; the stage of q - 3 takes the next row
+        __syncwarp();
+        if (lane == 0 && issued < n_sw_l && issued < q + S - 2) issue();
     }
-    if (MODE != kScFwd && !failed) flush();
+    if (!failed) flush();
 
-    if (MODE == kScBwdFinal && !failed) {
-        // this work item's weight-gradient partial row: taps (by tap index), bias, norm weight
-        float *prow = p.partial + static_cast<size_t>(k * dil + r) * (p.width + 2) * p.d;
-        if (active) {
+    if (!failed && active) {
+        // this work item's weight-gradient partial row: the taps (by tap index) and the bias from the
+        // first sweep, the norm weight from the second
+        const int d = p.d, width = p.width;
+        float *prow = p.partial + static_cast<size_t>(k * dil + r) * (width + 2) * d;
 #pragma unroll
-            for (int e = 0; e < kScEV; ++e) {
-                const int c = c0 + lane * kScEV + e;
-                for (int i = 0; i < p.width; ++i) prow[static_cast<size_t>(i) * p.d + c] = dK[p.width - 1 - i][e];
-                prow[static_cast<size_t>(p.width) * p.d + c] = db[e];
-                prow[static_cast<size_t>(p.width + 1) * p.d + c] = dnw[e];
+        for (int e = 0; e < kScEV; ++e) {
+            const int c = c0 + lane * kScEV + e;
+            if (MODE == kScBwdDot) {
+                for (int i = 0; i < width; ++i) prow[static_cast<size_t>(i) * d + c] = dK[width - 1 - i][e];
+                prow[static_cast<size_t>(width) * d + c] = db[e];
+            } else {
+                prow[static_cast<size_t>(width + 1) * d + c] = dnw[e];
             }
         }
     }
@@ -406,6 +638,18 @@ __global__ void __launch_bounds__(kScWarps * 32) conv_stencil_kernel(const __gri
         for (int64_t qq = q; qq < issued; ++qq)
             if (!mbar_wait(&full[qq % S], static_cast<uint32_t>((qq / S) & 1)))
                 report(p.status, nullptr, ENGRAM_DEVERR_TIMEOUT);
+}
+
+// The row-dot total of each token, its nb channel-block partials in ascending order, written to
+// the row's first entry (which the final sweep reads).
+__global__ void __launch_bounds__(256) conv_dot_total_kernel(float *__restrict__ token_dot, int64_t T, int32_t nb) {
+    for (int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; t < T;
+         t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        float *row = token_dot + static_cast<size_t>(t) * nb;
+        float s = 0.f;
+        for (int b = 0; b < nb; ++b) s += row[b];
+        row[0] = s;
+    }
 }
 
 // ------------------------------------------------------------------------------- weight-gradient reduction
@@ -547,23 +791,55 @@ extern "C" engram_status engram_short_conv_fwd(const void *v, const void *h, eng
     if (!norm_w || !conv_w || !seq_offsets) return fail(ENGRAM_ERR_NULL, "%s: NULL pointer", fn);
     if (T == 0) return ENGRAM_OK;
     if (!v || !out || !rstd) return fail(ENGRAM_ERR_NULL, "%s: NULL pointer", fn);
+    if (dilation > kScMaxDil) return fail(ENGRAM_ERR_SHAPE, "%s: dilation = %d exceeds %d", fn, dilation, kScMaxDil);
     if (out == v) return fail(ENGRAM_ERR_SHAPE, "%s: out may not alias V~ (later tokens read it as taps)", fn);
     const void *ptrs[] = {v, h, out, norm_w, conv_w, bias, seq_offsets, rstd};
     DeviceInfo dev;
-    if ((st = sc_ptrs(fn, ptrs, 8, 3, &dev)) != ENGRAM_OK) return st;
+    if ((st = sc_ptrs(fn, ptrs, 8, 6, &dev)) != ENGRAM_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const int64_t grid = cap_grid(std::min<int64_t>((T + 7) / 8, static_cast<int64_t>(dev.num_sms) * 8));
+    const int64_t rgrid = cap_grid(std::min<int64_t>((T + 7) / 8, static_cast<int64_t>(dev.num_sms) * 8));
     if (dtype == ENGRAM_F32)
-        conv_rstd_kernel<float><<<static_cast<unsigned>(grid), 256, 0, s>>>(static_cast<const uint8_t *>(v), T, d,
+        conv_rstd_kernel<float><<<static_cast<unsigned>(rgrid), 256, 0, s>>>(static_cast<const uint8_t *>(v), T, d,
                                                                             eps, rstd);
     else
-        conv_rstd_kernel<__nv_bfloat16><<<static_cast<unsigned>(grid), 256, 0, s>>>(static_cast<const uint8_t *>(v),
+        conv_rstd_kernel<__nv_bfloat16><<<static_cast<unsigned>(rgrid), 256, 0, s>>>(static_cast<const uint8_t *>(v),
                                                                                     T, d, eps, rstd);
     if ((st = check_launch(fn)) != ENGRAM_OK) return st;
-    ScParams prm = sc_params(v, norm_w, conv_w, bias, rstd, seq_offsets, num_seqs, T, d, width, dilation, dev);
-    prm.x2 = static_cast<const uint8_t *>(h);
-    prm.out = static_cast<uint8_t *>(out);
-    return sc_dispatch<kScFwd>(fn, dtype, prm, s);
+    const int nvec = static_cast<int>(static_cast<int64_t>(d) * dtype_size(dtype) / 16);
+    ScFwdParams fp{};
+    fp.v = static_cast<const uint8_t *>(v);
+    fp.h = static_cast<const uint8_t *>(h);
+    fp.norm_w = norm_w;
+    fp.conv_w = conv_w;
+    fp.bias = bias;
+    fp.rstd = rstd;
+    fp.offs = seq_offsets;
+    fp.out = static_cast<uint8_t *>(out);
+    fp.status = dev.status_word;
+    fp.T = T;
+    fp.num_seqs = num_seqs;
+    fp.d = d;
+    fp.width = width;
+    fp.dil = dilation;
+    fp.nblk = (nvec + 31) / 32;
+    const int64_t ntiles = (T + kScTileTokens - 1) / kScTileTokens;
+    if (ntiles > 0x7fffffff) return fail(ENGRAM_ERR_SHAPE, "%s: too many tokens", fn);
+    fp.ntiles = static_cast<int32_t>(ntiles);
+    fp.nbuf = sc_fwd_nbuf(width, dilation);
+    // two CTAs per SM, each on one channel block; J CTAs share a block's tiles
+    const int64_t per_block = std::max<int64_t>(1, std::min<int64_t>(ntiles, (2 * dev.num_sms + fp.nblk - 1) / fp.nblk));
+    const int64_t grid = cap_grid(per_block * fp.nblk) / fp.nblk * fp.nblk;
+    if (grid < fp.nblk) return fail(ENGRAM_ERR_SHAPE, "%s: the CTA cap is below %d channel blocks", fn, fp.nblk);
+    const int smem = sc_fwd_smem(width, dilation);
+    if (dtype == ENGRAM_F32) {
+        if ((st = set_smem(reinterpret_cast<const void *>(conv_fwd_kernel<float>), smem)) != ENGRAM_OK) return st;
+        conv_fwd_kernel<float><<<static_cast<unsigned>(grid), 256, smem, s>>>(fp);
+    } else {
+        if ((st = set_smem(reinterpret_cast<const void *>(conv_fwd_kernel<__nv_bfloat16>), smem)) != ENGRAM_OK)
+            return st;
+        conv_fwd_kernel<__nv_bfloat16><<<static_cast<unsigned>(grid), 256, smem, s>>>(fp);
+    }
+    return check_launch(fn);
 }
 
 extern "C" engram_status engram_short_conv_bwd(const void *dout, const void *v, engram_dtype dtype,
@@ -589,7 +865,11 @@ extern "C" engram_status engram_short_conv_bwd(const void *dout, const void *v, 
     ScParams prm = sc_params(v, norm_w, conv_w, bias, rstd, seq_offsets, num_seqs, T, d, width, dilation, dev);
     prm.x2 = static_cast<const uint8_t *>(dout);
     prm.token_dot_out = token_dot;
+    prm.partial = dw_partial;
     if ((st = sc_dispatch<kScBwdDot>(fn, dtype, prm, s)) != ENGRAM_OK) return st;
+    conv_dot_total_kernel<<<static_cast<unsigned>(std::min<int64_t>((T + 255) / 256, 4096)), 256, 0, s>>>(
+        token_dot, T, prm.nb);
+    if ((st = check_launch(fn)) != ENGRAM_OK) return st;
     prm.token_dot = token_dot;
     prm.token_dot_out = nullptr;
     prm.out = static_cast<uint8_t *>(dv);
