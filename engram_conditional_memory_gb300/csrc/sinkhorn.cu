@@ -416,50 +416,98 @@ __global__ void __launch_bounds__(kSkRG *kSkCV)
 
 // ------------------------------------------------------------------------------- momentum
 
-// Eight elements per thread and iteration: 16- or 32-byte gradient loads, 2 x 16-byte momentum
-// loads and 4 x 16-byte stores.  The n % 8 tail is done element by element.
+// Chunks of kMomChunk elements (grad and momentum) reach shared memory by two 1-D bulk (TMA) copies
+// each, kMomStages chunks in flight per CTA, thread 0 issuing; a thread updates eight elements of a
+// chunk and writes momentum and the Sinkhorn input straight to global memory.  Chunk c of the n8
+// groups of eight goes to CTA c mod grid.  The n % 8 tail is done element by element.
+constexpr int kMomChunk = 2048;   // elements per chunk: 256 threads x 8
+constexpr int kMomStages = 4;
+
+__host__ __device__ inline int sk_mom_smem(int gsize) { return kMomStages * kMomChunk * (gsize + 4) + kMomStages * 8; }
+
 template <typename G>
-__device__ __forceinline__ void sk_load8(const G *grad, int64_t v, float (&g)[8]);
+__device__ __forceinline__ void sk_unpack8(const uint8_t *src, float (&g)[8]);
 
 template <>
-__device__ __forceinline__ void sk_load8<float>(const float *grad, int64_t v, float (&g)[8]) {
-    const float4 a = __ldcs(reinterpret_cast<const float4 *>(grad) + 2 * v);
-    const float4 b = __ldcs(reinterpret_cast<const float4 *>(grad) + 2 * v + 1);
-    g[0] = a.x, g[1] = a.y, g[2] = a.z, g[3] = a.w, g[4] = b.x, g[5] = b.y, g[6] = b.z, g[7] = b.w;
+__device__ __forceinline__ void sk_unpack8<float>(const uint8_t *src, float (&g)[8]) {
+    const uint4 a = ld_shared_v4(src), b = ld_shared_v4(src + 16);
+    g[0] = __uint_as_float(a.x), g[1] = __uint_as_float(a.y), g[2] = __uint_as_float(a.z), g[3] = __uint_as_float(a.w);
+    g[4] = __uint_as_float(b.x), g[5] = __uint_as_float(b.y), g[6] = __uint_as_float(b.z), g[7] = __uint_as_float(b.w);
 }
 
 template <>
-__device__ __forceinline__ void sk_load8<__nv_bfloat16>(const __nv_bfloat16 *grad, int64_t v, float (&g)[8]) {
-    const uint4 u = __ldcs(reinterpret_cast<const uint4 *>(grad) + v);
-    Vec<__nv_bfloat16>::unpack(u, g);
+__device__ __forceinline__ void sk_unpack8<__nv_bfloat16>(const uint8_t *src, float (&g)[8]) {
+    Vec<__nv_bfloat16>::unpack(ld_shared_v4(src), g);
 }
 
 template <typename G>
 __global__ void __launch_bounds__(256) sinkhorn_momentum_kernel(const G *__restrict__ grad, float *__restrict__ m,
                                                                 float *__restrict__ out, int64_t n, float beta,
-                                                                int nesterov) {
+                                                                int nesterov, uint32_t *status) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    constexpr int gsize = static_cast<int>(sizeof(G));
+    const int tid = threadIdx.x;
+    const size_t stage_bytes = static_cast<size_t>(kMomChunk) * (gsize + 4);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kMomStages * stage_bytes);
     const int64_t n8 = n >> 3;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t v = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; v < n8; v += stride) {
-        float g[8];
-        sk_load8<G>(grad, v, g);
-        float4 *mv = reinterpret_cast<float4 *>(m) + 2 * v;
-        float4 *ov = reinterpret_cast<float4 *>(out) + 2 * v;
-        const float4 m0 = mv[0], m1 = mv[1];
-        const float mo[8] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w};
-        float mn[8], o[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            mn[e] = fmaf(beta, mo[e], g[e]);
-            o[e] = nesterov ? fmaf(beta, mn[e], g[e]) : mn[e];
-        }
-        mv[0] = make_float4(mn[0], mn[1], mn[2], mn[3]);
-        mv[1] = make_float4(mn[4], mn[5], mn[6], mn[7]);
-        __stcs(ov, make_float4(o[0], o[1], o[2], o[3]));
-        __stcs(ov + 1, make_float4(o[4], o[5], o[6], o[7]));
+    const int64_t nchunks = (n8 * 8 + kMomChunk - 1) / kMomChunk;
+    const int64_t G_ = gridDim.x;
+    const int64_t n_my = blockIdx.x < nchunks ? (nchunks - 1 - blockIdx.x) / G_ + 1 : 0;
+    const uint64_t pol = l2_evict_first_policy();
+    auto issue = [&](int64_t k) {  // thread 0: this CTA's k-th chunk into stage k % kMomStages
+        const int64_t c = blockIdx.x + k * G_;
+        const int64_t e0 = c * kMomChunk;
+        const int64_t cnt = n8 * 8 - e0 < kMomChunk ? n8 * 8 - e0 : kMomChunk;  // a multiple of 8
+        uint8_t *dst = smem + static_cast<size_t>(k % kMomStages) * stage_bytes;
+        uint64_t *bar = &full[k % kMomStages];
+        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(cnt * (gsize + 4)));
+        bulk_load(dst, grad + e0, static_cast<uint32_t>(cnt * gsize), bar, pol);
+        bulk_load(dst + static_cast<size_t>(kMomChunk) * gsize, m + e0, static_cast<uint32_t>(cnt * 4), bar, pol);
+    };
+    int64_t issued = 0;
+    if (tid == 0) {
+        for (int q = 0; q < kMomStages; ++q) mbar_init(&full[q], 1);
+        mbar_init_fence();
+        for (; issued < kMomStages && issued < n_my; ++issued) issue(issued);
     }
-    if (blockIdx.x == 0 && threadIdx.x < (n & 7)) {
-        const int64_t i = (n8 << 3) + threadIdx.x;
+    __syncthreads();
+    int64_t k = 0;
+    for (; k < n_my; ++k) {
+        const int st = static_cast<int>(k % kMomStages);
+        const bool ok = mbar_wait(&full[st], static_cast<uint32_t>((k / kMomStages) & 1));
+        const int64_t e0 = (blockIdx.x + k * G_) * kMomChunk;
+        const int64_t e = e0 + tid * 8;
+        const uint8_t *stg = smem + static_cast<size_t>(st) * stage_bytes;
+        if (ok && e < n8 * 8) {
+            float g[8], mo[8];
+            sk_unpack8<G>(stg + static_cast<size_t>(tid) * 8 * gsize, g);
+            sk_unpack8<float>(stg + static_cast<size_t>(kMomChunk) * gsize + static_cast<size_t>(tid) * 32, mo);
+            float mn[8], o[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                mn[q] = fmaf(beta, mo[q], g[q]);
+                o[q] = nesterov ? fmaf(beta, mn[q], g[q]) : mn[q];
+            }
+            float4 *mv = reinterpret_cast<float4 *>(m + e);
+            float4 *ov = reinterpret_cast<float4 *>(out + e);
+            mv[0] = make_float4(mn[0], mn[1], mn[2], mn[3]);
+            mv[1] = make_float4(mn[4], mn[5], mn[6], mn[7]);
+            __stcs(ov, make_float4(o[0], o[1], o[2], o[3]));
+            __stcs(ov + 1, make_float4(o[4], o[5], o[6], o[7]));
+        }
+        if (__syncthreads_or(!ok)) {
+            if (tid == 0) report(status, nullptr, ENGRAM_DEVERR_TIMEOUT);
+            break;
+        }
+        // every thread has read its part of the stage: refill it
+        if (tid == 0 && issued < n_my) issue(issued++);
+    }
+    if (tid == 0)  // copies issued but not consumed (after a timeout) land before the CTA leaves
+        for (int64_t q = k; q < issued; ++q)
+            if (!mbar_wait(&full[q % kMomStages], static_cast<uint32_t>((q / kMomStages) & 1)))
+                report(status, nullptr, ENGRAM_DEVERR_TIMEOUT);
+    if (blockIdx.x == 0 && tid < (n & 7)) {
+        const int64_t i = (n8 << 3) + tid;
         const float g = static_cast<float>(grad[i]);
         const float mn = fmaf(beta, m[i], g);
         m[i] = mn;
@@ -569,17 +617,24 @@ extern "C" engram_status engram_sinkhorn_momentum_update(const void *grad, engra
     DeviceInfo dev;
     engram_status st = sk_check_ptrs(fn, ptrs, 3, 3, &dev);
     if (st != ENGRAM_OK) return st;
-    const int threads = 256;
-    const int64_t vecs = std::max<int64_t>(1, n >> 3);
-    const int64_t blocks =
-        cap_grid(std::min<int64_t>((vecs + threads - 1) / threads, static_cast<int64_t>(dev.num_sms) * 8));
+    const int64_t nchunks = std::max<int64_t>(1, ((n >> 3) * 8 + kMomChunk - 1) / kMomChunk);
+    const int64_t blocks = cap_grid(std::min<int64_t>(nchunks, static_cast<int64_t>(dev.num_sms) * 2));
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (dtype == ENGRAM_F32)
-        sinkhorn_momentum_kernel<float><<<static_cast<unsigned>(blocks), threads, 0, s>>>(
-            static_cast<const float *>(grad), momentum, sinkhorn_input, n, beta1, nesterov != 0);
-    else
-        sinkhorn_momentum_kernel<__nv_bfloat16><<<static_cast<unsigned>(blocks), threads, 0, s>>>(
-            static_cast<const __nv_bfloat16 *>(grad), momentum, sinkhorn_input, n, beta1, nesterov != 0);
+    if (dtype == ENGRAM_F32) {
+        const int smem = sk_mom_smem(4);
+        if ((st = set_smem(reinterpret_cast<const void *>(sinkhorn_momentum_kernel<float>), smem)) != ENGRAM_OK)
+            return st;
+        sinkhorn_momentum_kernel<float><<<static_cast<unsigned>(blocks), 256, smem, s>>>(
+            static_cast<const float *>(grad), momentum, sinkhorn_input, n, beta1, nesterov != 0, dev.status_word);
+    } else {
+        const int smem = sk_mom_smem(2);
+        if ((st = set_smem(reinterpret_cast<const void *>(sinkhorn_momentum_kernel<__nv_bfloat16>), smem)) !=
+            ENGRAM_OK)
+            return st;
+        sinkhorn_momentum_kernel<__nv_bfloat16><<<static_cast<unsigned>(blocks), 256, smem, s>>>(
+            static_cast<const __nv_bfloat16 *>(grad), momentum, sinkhorn_input, n, beta1, nesterov != 0,
+            dev.status_word);
+    }
     return check_launch(fn);
 }
 
