@@ -14,6 +14,7 @@ from .binding import (  # noqa: F401
     EngramError,
     HashSpec,
     abi_version,
+    check_wait_timeout,
     device_status,
     fuse_weight,
     gate_bwd,

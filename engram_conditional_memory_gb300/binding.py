@@ -72,6 +72,7 @@ def load_library():
             "engram_set_max_ctas": (_i32, [_i32]),
             "engram_read_error_word": (st, [_p, _p, _p]),
             "engram_device_status": (st, [_p, _i32]),
+            "engram_check_wait_timeout": (st, [_c.c_uint32, _p]),
             "engram_hash_gather": (st, [_p, _p, _p]),
             "engram_hash_gather_host": (st, [_p, _p, _p]),
             "engram_fuse_weight": (st, [_p, _p, _c.c_int, _p, _i32, _p]),
@@ -542,3 +543,9 @@ def device_status(clear: bool = False) -> int:
     if st not in (0, 6):
         _check(st, "engram_device_status")
     return out.value
+
+
+def check_wait_timeout(limit_us: int = 50000, stream=None):
+    """Launch the failure-detection self-check (a bounded wait that must give up); read the result
+    with device_status()."""
+    _check(load_library().engram_check_wait_timeout(int(limit_us), _stream(stream)), "engram_check_wait_timeout")

@@ -92,9 +92,38 @@ engram_status set_smem(const void *kernel, int bytes) {
 
 }  // namespace engram
 
+namespace engram {
+
+// The failure-detection self-check: one CTA waits, with the pipelines' own bounded wait, on an
+// mbarrier that nothing ever completes (no copy, no arrival is pending on it), gives up after
+// limit_ns and reports ENGRAM_DEVERR_TIMEOUT like a pipeline would.
+__global__ void wait_timeout_check_kernel(uint64_t limit_ns, uint32_t *status) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        mbar_init_fence();
+    }
+    __syncthreads();
+    const bool ok = mbar_wait(&bar, 0, limit_ns);
+    if (__syncthreads_or(!ok) && threadIdx.x == 0) report(status, nullptr, ENGRAM_DEVERR_TIMEOUT);
+}
+
+}  // namespace engram
+
 using namespace engram;
 
 extern "C" {
+
+engram_status engram_check_wait_timeout(uint32_t limit_us, engram_stream_t stream) {
+    if (limit_us < 1 || limit_us > 2000000)
+        return fail(ENGRAM_ERR_SHAPE, "engram_check_wait_timeout: limit_us = %u (1 .. 2000000)", limit_us);
+    DeviceInfo dev;
+    engram_status st = current_device(&dev);
+    if (st != ENGRAM_OK) return st;
+    wait_timeout_check_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        static_cast<uint64_t>(limit_us) * 1000u, dev.status_word);
+    return check_launch("engram_check_wait_timeout");
+}
 
 int32_t engram_abi_version(void) { return ENGRAM_ABI_VERSION; }
 

@@ -126,6 +126,14 @@ engram_status engram_read_error_word(const uint32_t *err_word, engram_stream_t s
  */
 engram_status engram_device_status(uint32_t *host_out, int32_t clear);
 
+/*
+ * Failure-detection self-check (no counterpart in the pages): launches one CTA that waits, with
+ * the same bounded wait the pipelines use, on an mbarrier nothing completes.  It gives up after
+ * limit_us microseconds (1 .. 2,000,000) and sets ENGRAM_DEVERR_TIMEOUT in the device status word,
+ * as a stalled pipeline would; the context stays usable.  Nothing faults, traps or hangs.
+ */
+engram_status engram_check_wait_timeout(uint32_t limit_us, engram_stream_t stream);
+
 /* ------------------------------------------------------------------------- */
 /* A0-A2: compression, multi-head N-gram hash and gather  (ch. 34 sec. 1.2 item 2, sec. 2.3) */
 /* ------------------------------------------------------------------------- */

@@ -172,3 +172,10 @@ def test_sinkhorn_partition_rule(lib):
         p = parts(rows)
         chunk = -(-rows // p)
         assert 1 <= p <= 1024 and (p - 1) * chunk < rows <= p * chunk
+
+
+def test_wait_timeout_check_rejects_bad_limits(lib):
+    lib.engram_check_wait_timeout.restype = ctypes.c_int
+    lib.engram_check_wait_timeout.argtypes = [ctypes.c_uint32, ctypes.c_void_p]
+    assert lib.engram_check_wait_timeout(0, None) == 2
+    assert lib.engram_check_wait_timeout(2000001, None) == 2
