@@ -29,6 +29,7 @@ from .binding import (  # noqa: F401
     load_library,
     read_error_word,
     set_max_ctas,
+    set_pdl,
     set_validation,
     short_conv_bwd,
     short_conv_dot_blocks,

@@ -70,6 +70,7 @@ def load_library():
             "engram_last_error_string": (_c.c_char_p, []),
             "engram_set_validation": (_i32, [_i32]),
             "engram_set_max_ctas": (_i32, [_i32]),
+            "engram_set_pdl": (_i32, [_i32]),
             "engram_read_error_word": (st, [_p, _p, _p]),
             "engram_device_status": (st, [_p, _i32]),
             "engram_check_wait_timeout": (st, [_c.c_uint32, _p]),
@@ -141,6 +142,11 @@ def set_validation(level: int) -> int:
 def set_max_ctas(max_ctas: int) -> int:
     """Cap the CTAs per launch (0 = none); returns the previous cap."""
     return load_library().engram_set_max_ctas(max_ctas)
+
+
+def set_pdl(on: bool) -> bool:
+    """Programmatic dependent launch for the step's kernels (on by default); returns the previous setting."""
+    return bool(load_library().engram_set_pdl(int(bool(on))))
 
 
 def abi_version() -> int:

@@ -18,6 +18,7 @@ namespace {
 thread_local char t_last_error[512] = "";
 std::atomic<int32_t> g_validation{1};
 std::atomic<int32_t> g_max_ctas{0};
+std::atomic<int32_t> g_pdl{1};
 
 constexpr int kMaxDevices = 64;
 std::mutex g_dev_mutex;
@@ -25,6 +26,8 @@ bool g_dev_ready[kMaxDevices];
 DeviceInfo g_dev_info[kMaxDevices];
 
 }  // namespace
+
+bool pdl_enabled() { return g_pdl.load(std::memory_order_relaxed) != 0; }
 
 engram_status fail(engram_status st, const char *fmt, ...) {
     va_list ap;
@@ -146,6 +149,8 @@ const char *engram_last_error_string(void) { return t_last_error; }
 int32_t engram_set_validation(int32_t level) { return g_validation.exchange(level != 0 ? 1 : 0); }
 
 int32_t engram_set_max_ctas(int32_t max_ctas) { return g_max_ctas.exchange(max_ctas > 0 ? max_ctas : 0); }
+
+int32_t engram_set_pdl(int32_t on) { return g_pdl.exchange(on != 0 ? 1 : 0); }
 
 engram_status engram_read_error_word(const uint32_t *err_word, engram_stream_t stream, uint32_t *host_out) {
     if (!err_word || !host_out) return fail(ENGRAM_ERR_NULL, "engram_read_error_word: NULL argument");

@@ -39,6 +39,7 @@ struct GateBwdParams {
 
 template <typename T, int NCW>
 __global__ void __launch_bounds__((NCW + 1) * 32) gate_bwd_kernel(const __grid_constant__ GateBwdParams p) {
+    pdl_wait();              // the previous kernel's writes are complete and visible
     using V = Vec<T>;
     constexpr int EV = V::N;
     constexpr int NC = NCW * 32;
@@ -227,6 +228,7 @@ __global__ void __launch_bounds__(kRG *kCV)
     grad_w_reduce_kernel(const float4 *__restrict__ part, int32_t P, int32_t d4, float4 *__restrict__ dweight,
                          const float4 *__restrict__ w_h, const float4 *__restrict__ w_k, float4 *__restrict__ g_h,
                          float4 *__restrict__ g_k) {
+    pdl_wait();
     __shared__ float4 sums[kRG][kCV];
     const int cv = threadIdx.x % kCV;
     const int r = threadIdx.x / kCV;
@@ -289,7 +291,9 @@ engram_status launch_bwd(const GateBwdParams &p, const DeviceInfo &dev, cudaStre
     q.stages = shape.stages;
     // One CTA per partial (the kernel's partial loop then runs once per CTA).
     const int64_t grid = cap_grid(p.P);
-    kern<<<static_cast<unsigned>(grid), (NCW + 1) * 32, shape.smem_bytes, stream>>>(q);
+    cudaError_t e = launch_kernel(kern, dim3(static_cast<unsigned>(grid)), dim3((NCW + 1) * 32), shape.smem_bytes,
+                                  stream, q);
+    if (e != cudaSuccess) return fail(ENGRAM_ERR_CUDA, "engram_gate_bwd launch: %s", cudaGetErrorString(e));
     return check_launch("engram_gate_bwd");
 }
 
@@ -394,10 +398,12 @@ extern "C" engram_status engram_grad_w_reduce(const float *dw_partial, int32_t P
         if ((st = check_device_ptr(ptrs[i], dev.device, names[i])) != ENGRAM_OK) return st;
     const int d4 = d / 4;
     const int blocks = (d4 + kCV - 1) / kCV;
-    grad_w_reduce_kernel<<<blocks, kRG * kCV, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+    cudaError_t e = launch_kernel(
+        grad_w_reduce_kernel, dim3(blocks), dim3(kRG * kCV), 0, reinterpret_cast<cudaStream_t>(stream),
         reinterpret_cast<const float4 *>(dw_partial), P, d4, reinterpret_cast<float4 *>(dweight_fused),
         reinterpret_cast<const float4 *>(w_h), reinterpret_cast<const float4 *>(w_k),
         reinterpret_cast<float4 *>(grad_w_h), reinterpret_cast<float4 *>(grad_w_k));
+    if (e != cudaSuccess) return fail(ENGRAM_ERR_CUDA, "engram_grad_w_reduce launch: %s", cudaGetErrorString(e));
     return check_launch("engram_grad_w_reduce");
 }
 

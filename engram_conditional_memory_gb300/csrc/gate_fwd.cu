@@ -28,6 +28,7 @@ struct GateFwdParams {
 
 template <typename T, int NCW>
 __global__ void __launch_bounds__((NCW + 1) * 32) gate_fwd_kernel(const __grid_constant__ GateFwdParams p) {
+    pdl_wait();              // the previous kernel's writes are complete and visible
     using V = Vec<T>;
     constexpr int EV = V::N;
     constexpr int NC = NCW * 32;
@@ -180,6 +181,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32) gate_fwd_kernel(const __grid_c
 template <typename T>
 __global__ void fuse_weight_kernel(const T *__restrict__ w_h, const T *__restrict__ w_k, float *__restrict__ w,
                                    int32_t d) {
+    pdl_wait();
     for (int32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < d; i += gridDim.x * blockDim.x)
         w[i] = static_cast<float>(w_h[i]) * static_cast<float>(w_k[i]);
 }
@@ -198,7 +200,9 @@ engram_status launch_fwd(const GateFwdParams &p, const DeviceInfo &dev, cudaStre
     int64_t grid = static_cast<int64_t>(dev.num_sms) * shape.blocks_per_sm;
     if (grid > p.T) grid = p.T;
     grid = cap_grid(grid);
-    kern<<<static_cast<unsigned>(grid), (NCW + 1) * 32, shape.smem_bytes, stream>>>(q);
+    cudaError_t e = launch_kernel(kern, dim3(static_cast<unsigned>(grid)), dim3((NCW + 1) * 32), shape.smem_bytes,
+                                  stream, q);
+    if (e != cudaSuccess) return fail(ENGRAM_ERR_CUDA, "engram_gate_fwd launch: %s", cudaGetErrorString(e));
     return check_launch("engram_gate_fwd");
 }
 
@@ -232,12 +236,14 @@ extern "C" engram_status engram_fuse_weight(const void *w_h, const void *w_k, en
     int blocks = (d + threads - 1) / threads;
     if (blocks > 4 * dev.num_sms) blocks = 4 * dev.num_sms;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e;
     if (dtype == ENGRAM_F32)
-        fuse_weight_kernel<float><<<blocks, threads, 0, s>>>(static_cast<const float *>(w_h),
-                                                             static_cast<const float *>(w_k), w_fused, d);
+        e = launch_kernel(fuse_weight_kernel<float>, dim3(blocks), dim3(threads), 0, s,
+                          static_cast<const float *>(w_h), static_cast<const float *>(w_k), w_fused, d);
     else
-        fuse_weight_kernel<__nv_bfloat16><<<blocks, threads, 0, s>>>(
-            static_cast<const __nv_bfloat16 *>(w_h), static_cast<const __nv_bfloat16 *>(w_k), w_fused, d);
+        e = launch_kernel(fuse_weight_kernel<__nv_bfloat16>, dim3(blocks), dim3(threads), 0, s,
+                          static_cast<const __nv_bfloat16 *>(w_h), static_cast<const __nv_bfloat16 *>(w_k), w_fused, d);
+    if (e != cudaSuccess) return fail(ENGRAM_ERR_CUDA, "engram_fuse_weight launch: %s", cudaGetErrorString(e));
     return check_launch("engram_fuse_weight");
 }
 

@@ -172,6 +172,7 @@ __device__ __forceinline__ void bulk_wait_read_all_but_one() {
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 __global__ void __launch_bounds__(kHashThreads) hash_gather_kernel(const __grid_constant__ HashGatherParams p) {
+    pdl_wait();              // the previous kernel's writes are complete and visible
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ TileIds st;
 
@@ -471,7 +472,9 @@ extern "C" engram_status engram_hash_gather(const engram_hash_spec *spec, const 
     int64_t grid = static_cast<int64_t>(dev.num_sms) * std::max(per_sm, 1);
     if (grid > ntiles) grid = ntiles;
     grid = cap_grid(grid);
-    hash_gather_kernel<<<static_cast<unsigned>(grid), kHashThreads, dyn, reinterpret_cast<cudaStream_t>(stream)>>>(p);
+    cudaError_t le = launch_kernel(hash_gather_kernel, dim3(static_cast<unsigned>(grid)), dim3(kHashThreads), dyn,
+                                   reinterpret_cast<cudaStream_t>(stream), p);
+    if (le != cudaSuccess) return fail(ENGRAM_ERR_CUDA, "engram_hash_gather launch: %s", cudaGetErrorString(le));
     return check_launch("engram_hash_gather");
 }
 

@@ -114,6 +114,15 @@ int32_t engram_set_validation(int32_t level);
 int32_t engram_set_max_ctas(int32_t max_ctas);
 
 /*
+ * Programmatic dependent launch for the step's kernels (hash gather, weight fold, gate forward,
+ * gate backward, weight-gradient reduction): with it on (the default), each is launched with the
+ * programmatic-stream-serialization attribute, so its launch overlaps the previous kernel's exit, and
+ * waits in-kernel for that kernel's completion before touching memory; results are identical either
+ * way.  Returns the previous setting.  Process-wide.
+ */
+int32_t engram_set_pdl(int32_t on);
+
+/*
  * Copies a device error word to *host_out.  SYNCHRONISES `stream` first.
  * Returns ENGRAM_ERR_INDEX when any bit is set, ENGRAM_OK otherwise.
  */
