@@ -6,9 +6,10 @@ tokens (65,536 tokens):
   1. hash + gather of every token's 16 table rows (orders {2, 3} x 8 heads,
      ~2.0M-row prime tables, 64 bf16 per row, 4.1 GB resident) -> e [65536, 1024];
   2. the weight fold w = w_h * w_k;
-  3. the context-aware gate, forward + backward + weight-gradient reduction,
-     on four micro-batches of T = 16384 tokens at d = 4096 (bf16), the
-     reduction accumulating into fp32 grad_w_h / grad_w_k.
+  3. the context-aware gate, forward + backward on four micro-batches of
+     T = 16384 tokens at d = 4096 (bf16), then one ordered reduction of the
+     four micro-batches' weight-gradient partials, accumulating into fp32
+     grad_w_h / grad_w_k (11 kernel launches).
 The reported value is tokens/s through the whole step (whole job, all ranks).
 Inputs are resident in HBM (the device-timed value) or copied from pinned host
 memory every step (the `e2e` value).  The per-step working set (4.1 GB table,
@@ -171,7 +172,7 @@ def algorithmic_bytes(P: int):
         "fuse_weight": 3 * 4 * D,
         "gate_fwd": MICRO_T * (8 * D + 16),                       # h, k, v read, out written, 4 fp32 stats
         "gate_bwd": MICRO_T * (14 * D + 16) + P * D * 4,         # dout, v, h, k, stats read; dh, dk, dv, partials
-        "grad_w_reduce": P * D * 4 + 7 * D * 4,                   # partials, w_h, w_k, grads (r+w), dweight
+        "grad_w_reduce": 4 * P * D * 4 + 7 * D * 4,               # 4 micro-batches' partials, w_h, w_k, grads, dweight
     }
 
 
@@ -209,7 +210,9 @@ def make_workload(device):
     wk["dv"] = [torch.empty_like(o) for o in wk["out"]]
     wk["stats"] = [tuple(torch.empty(MICRO_T, dtype=torch.float32, device=device) for _ in range(4))
                    for _ in range(4)]
-    wk["part"] = [torch.empty((P, D), dtype=torch.float32, device=device) for _ in range(4)]
+    # the four micro-batches' weight-gradient partials side by side: one ordered reduction per step
+    wk["part_all"] = torch.empty((4 * P, D), dtype=torch.float32, device=device)
+    wk["part"] = [wk["part_all"][i * P:(i + 1) * P] for i in range(4)]
     wk["dweight"] = torch.empty(D, dtype=torch.float32, device=device)
     wk["grad_w_h"] = torch.zeros(D, dtype=torch.float32, device=device)
     wk["grad_w_k"] = torch.zeros(D, dtype=torch.float32, device=device)
@@ -217,7 +220,7 @@ def make_workload(device):
 
 
 def run_step(wk, mark=None):
-    """Launch one step (14 kernels) on the current stream; `mark(name)` is called after each launch."""
+    """Launch one step (11 kernels) on the current stream; `mark(name)` is called after each launch."""
     import engram_conditional_memory_gb300 as ecm
 
     hw = wk["hw"]
@@ -233,16 +236,24 @@ def run_step(wk, mark=None):
         ecm.gate_bwd(m["dout"], m["h"], m["k"], m["v"], wk["w_fused"], *st, P=wk["P"], dh=wk["dh"][i],
                      dk=wk["dk"][i], dv=wk["dv"][i], dw_partial=wk["part"][i])
         mark and mark("gate_bwd")
-        ecm.grad_w_reduce(wk["part"][i], dweight_fused=wk["dweight"], w_h=wk["w_h"], w_k=wk["w_k"],
-                          grad_w_h=wk["grad_w_h"], grad_w_k=wk["grad_w_k"])
-        mark and mark("grad_w_reduce")
-    return 14
+    reduce_step(wk)
+    mark and mark("grad_w_reduce")
+    return 11
+
+
+def reduce_step(wk):
+    """The step's weight gradient: the four micro-batches' partials in one ordered reduction,
+    accumulated into grad_w_h and grad_w_k as gradient accumulation would."""
+    import engram_conditional_memory_gb300 as ecm
+
+    ecm.grad_w_reduce(wk["part_all"], dweight_fused=wk["dweight"], w_h=wk["w_h"], w_k=wk["w_k"],
+                      grad_w_h=wk["grad_w_h"], grad_w_k=wk["grad_w_k"])
 
 
 # ----------------------------------------------------------------------------- device timing
 
 def capture_step(wk, device):
-    """The step as one CUDA graph (14 kernel nodes).  The library's per-device set-up and each
+    """The step as one CUDA graph (11 kernel nodes).  The library's per-device set-up and each
     kernel's shared-memory attribute are done by an eager step first; device-pointer checks are
     off during capture (they were made by that eager step on the same buffers)."""
     import torch
@@ -285,7 +296,7 @@ def time_graph(graph, steps, warmup, device):
     torch.cuda.synchronize()
     wall1 = _dt.datetime.now()
     barrier(device)
-    return start.elapsed_time(end), 14 * steps, wall0, wall1
+    return start.elapsed_time(end), 11 * steps, wall0, wall1
 
 
 def time_device(wk, steps, warmup, device):
@@ -372,8 +383,7 @@ def time_e2e(wk, steps, warmup, device):
             ecm.gate_bwd(m["dout"], m["h"], m["k"], m["v"], wk["w_fused"], *st, P=wk["P"], dh=wk["dh"][i],
                          dk=wk["dk"][i], dv=wk["dv"][i], dw_partial=wk["part"][i])
             done[i].record(comp)
-            ecm.grad_w_reduce(wk["part"][i], dweight_fused=wk["dweight"], w_h=wk["w_h"], w_k=wk["w_k"],
-                              grad_w_h=wk["grad_w_h"], grad_w_k=wk["grad_w_k"])
+        reduce_step(wk)
         res_h[:D].copy_(wk["grad_w_h"], non_blocking=True)
         res_h[D:].copy_(wk["grad_w_k"], non_blocking=True)
 
@@ -667,8 +677,7 @@ def main_offload(args, device):
             ecm.gate_fwd(m["h"], m["k"], m["v"], wk["w_fused"], EPS, out=wk["out"][i], stats=st)
             ecm.gate_bwd(m["dout"], m["h"], m["k"], m["v"], wk["w_fused"], *st, P=wk["P"], dh=wk["dh"][i],
                          dk=wk["dk"][i], dv=wk["dv"][i], dw_partial=wk["part"][i])
-            ecm.grad_w_reduce(wk["part"][i], dweight_fused=wk["dweight"], w_h=wk["w_h"], w_k=wk["w_k"],
-                              grad_w_h=wk["grad_w_h"], grad_w_k=wk["grad_w_k"])
+        reduce_step(wk)
 
     def offload_step():
         side.wait_event(fetched)  # rows_next is free once the previous step's prefetch was consumed
@@ -807,7 +816,7 @@ def main_native(args, rank, local, world):
         avg = sum(times) / len(times)
         gbs = ab[name] / (avg / 1e3) / 1e9
         ops[name] = {"avg_ms": avg, "launches": len(times), "bytes": ab[name], "GBps": gbs, "frac": gbs / peak}
-    step_bytes = ab["hash_gather"] + ab["fuse_weight"] + 4 * (ab["gate_fwd"] + ab["gate_bwd"] + ab["grad_w_reduce"])
+    step_bytes = ab["hash_gather"] + ab["fuse_weight"] + 4 * (ab["gate_fwd"] + ab["gate_bwd"]) + ab["grad_w_reduce"]
     dom = "gate_bwd"
     roof = {"bound": "hbm", "kernel": dom, "achieved": ops[dom]["GBps"], "peak": peak, "unit": "GB/s",
             "frac": ops[dom]["GBps"] / peak, "peak_kind": f"{peak_kind} (copy bandwidth)",
@@ -834,7 +843,7 @@ def main_native(args, rank, local, world):
             "config": {"workload": WORKLOAD, "tokens_per_step": T_all, "global_batch": world * T_all,
                        "seq_len": SEQ_LEN, "parallelism": f"replicas x{world}",
                        "l2": "no flush: per-step working set 6.1 GB >> 129 MB L2",
-                       "timing": "value: CUDA-graph replays of the 14-launch step; ops/roofline: eager steps "
+                       "timing": "value: CUDA-graph replays of the 11-launch step; ops/roofline: eager steps "
                                  "with an event between launches; e2e: eager calls with host copies"},
             "hbm_gbs": step_bytes / (max_ms / args.steps / 1e3) / 1e9,
             "hash_gather_rows_per_s": 16 * T_all / (ops["hash_gather"]["avg_ms"] / 1e3),
