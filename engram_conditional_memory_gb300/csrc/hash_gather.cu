@@ -11,21 +11,21 @@
 //   h = XOR_{j<n} (uint64) id'(t - j) * M[table][j]  (mod 2^64),  idx = h mod p[table],
 //   id'(q) = pad id 0 for q before the start of t's sequence.
 //
-// Kernel layout: a persistent CTA walks tiles of consecutive tokens (as many as make a ~32 KB tile
-// of e_t rows, at most kTileMax), double-buffered, with the next tile's hashing overlapping the
-// current tile's copies:
-//   1. the compressed ids of the tile plus its (max_order - 1)-token look-back window and every
-//      token's sequence start (a binary search in the sequence offsets, staged in shared memory
-//      once per CTA when they fit) go to shared memory;
-//   2. the tile's tokens x tables hashes are computed, one per thread, into a shared table of row
-//      numbers (and the optional index output);
-//   3. every table row of the tile is fetched by one bulk asynchronous copy (TMA, 1-D) into the
-//      shared tile, in e_t order, completing on the tile's mbarrier; when all have landed, one
-//      thread stores the whole tile -- the tile's e_t rows are adjacent in the output -- with a
-//      single bulk copy back to global memory.
+// Kernel layout, two kernels for a table in device memory:
+//   hash_index_kernel: one thread per token computes its compressed window (the pad id 0 before its
+//      sequence's start, found by a binary search in the sequence offsets), every table's hash and
+//      index, and parks the absolute row numbers in the first 8 x tables bytes of the token's own
+//      e_t row (plus the optional index output);
+//   hash_gather_kernel: a persistent CTA walks double-buffered tiles of consecutive tokens (~32 KB
+//      of e_t rows, at most kTileMax tokens): it reads a tile's parked row numbers, fetches every
+//      table row by one bulk asynchronous copy (TMA, 1-D) into the shared tile in e_t order,
+//      completing on the tile's mbarrier, and when all have landed one thread stores the whole tile
+//      -- its e_t rows are adjacent in the output -- over the parked numbers with a single bulk copy.
+//      The next tile's row numbers are read while the current tile's copies are in flight.
 // Random 128-byte rows are where this beats 16-byte loads from every thread: the copy engine keeps
 // far more rows in flight per SM than the load units can (measured: 53 us against 70 us for the
-// 65,536-token, 16-table gather on GB300).
+// 65,536-token, 16-table gather on GB300).  With a table in host memory, hash_gather_host_kernel
+// keeps the tile hashing (tile_ids, tile_hash) and loads the rows over the host link.
 #include <algorithm>
 
 #include "engram_internal.cuh"
@@ -171,50 +171,97 @@ __device__ __forceinline__ void bulk_wait_read_all_but_one() {
 
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
-__global__ void __launch_bounds__(kHashThreads) hash_gather_kernel(const __grid_constant__ HashGatherParams p) {
-    pdl_wait();              // the previous kernel's writes are complete and visible
-    extern __shared__ __align__(128) uint8_t smem[];
-    __shared__ TileIds st;
+// Steps 1-2 for every token, one thread per token: its compressed window (the pad id 0 before its
+// sequence's start), every table's hash, the optional index output, and -- when rows are wanted --
+// the absolute row numbers (int64, row_off[table] + index) parked in the first 8 x tables bytes of
+// the token's own e_t row, which hash_gather_kernel reads back before it overwrites that row.
+// Block 0 also checks that 0 = o_0 <= o_1 <= ... <= o_S = T.
+__global__ void __launch_bounds__(256) hash_index_kernel(const __grid_constant__ HashGatherParams p) {
+    pdl_wait();  // the previous kernel's writes are complete and visible
+    if (blockIdx.x == 0) {
+        for (int s = threadIdx.x; s <= p.num_seqs; s += blockDim.x) {
+            const int64_t o = p.seq_offsets[s];
+            bool bad = (s == 0 && o != 0) || (s == p.num_seqs && o != p.T) || o < 0 || o > p.T;
+            if (s > 0 && p.seq_offsets[s - 1] > o) bad = true;
+            if (bad) report(p.status, p.err_word, ENGRAM_DEVERR_SEQ_OFFSETS);
+        }
+    }
+    const uint32_t et_bytes = static_cast<uint32_t>(p.tables) * p.row_bytes;
+    for (int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; t < p.T;
+         t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t s0 = sequence_start(p.seq_offsets, p.num_seqs, t);
+        uint64_t cid[ENGRAM_MAX_ORDER];
+#pragma unroll
+        for (int j = 0; j < ENGRAM_MAX_ORDER; ++j) {
+            cid[j] = 0;
+            const int64_t q = t - j;
+            if (j < p.max_order && q >= s0) {
+                const int32_t raw = __ldg(p.ids + q);
+                if (raw < 0 || raw >= p.vocab) {
+                    if (j == 0) report(p.status, p.err_word, ENGRAM_DEVERR_TOKEN_ID);
+                } else {
+                    const int32_t id = p.cmap ? __ldg(p.cmap + raw) : raw;
+                    if (id < 0 || id >= p.vocab_c) {
+                        if (j == 0) report(p.status, p.err_word, ENGRAM_DEVERR_COMPRESSED);
+                    } else {
+                        cid[j] = static_cast<uint64_t>(id);
+                    }
+                }
+            }
+        }
+        int64_t *park = p.out_rows ? reinterpret_cast<int64_t *>(p.out_rows + static_cast<size_t>(t) * et_bytes)
+                                   : nullptr;
+        for (int tb = 0; tb < p.tables; ++tb) {
+            const int n = p.order[tb];
+            uint64_t h = 0;
+#pragma unroll
+            for (int j = 0; j < ENGRAM_MAX_ORDER; ++j)
+                if (j < n) h ^= cid[j] * p.mult[tb][j];
+            const uint64_t idx = h % p.prime[tb];
+            if (park) park[tb] = p.row_off[tb] + static_cast<int64_t>(idx);
+            if (p.out_idx) p.out_idx[t * p.tables + tb] = static_cast<int32_t>(idx);
+        }
+    }
+}
 
+// Step 3 for a tile: the row numbers hash_index_kernel parked in the tile's own e_t rows.
+__device__ __forceinline__ void tile_rows(const HashGatherParams &p, int64_t *rows, int b, int64_t tile, int tid) {
+    const int64_t t0 = tile * p.tile_tokens;
+    const int ntok = static_cast<int>(p.T - t0 < p.tile_tokens ? p.T - t0 : p.tile_tokens);
+    const uint32_t et_bytes = static_cast<uint32_t>(p.tables) * p.row_bytes;
+    int64_t *r = rows + static_cast<size_t>(b) * p.tile_tokens * p.tables;
+    for (int e = tid; e < ntok * p.tables; e += kHashThreads) {
+        const int i = e / p.tables;
+        const int tb = e - i * p.tables;
+        r[e] = __ldcg(reinterpret_cast<const long long *>(p.out_rows + static_cast<size_t>(t0 + i) * et_bytes) + tb);
+    }
+}
+
+// Step 3: a persistent CTA walks tiles of consecutive tokens, double-buffered; every table row of
+// a tile is fetched by one bulk asynchronous copy (TMA, 1-D) into the shared tile, in e_t order,
+// completing on the tile's mbarrier, and one bulk store writes the tile's adjacent e_t rows back
+// -- over the row numbers that were parked there, which the CTA read before issuing the copies.
+// The next tile's row numbers are read while the current tile's copies are in flight.
+__global__ void __launch_bounds__(kHashThreads) hash_gather_kernel(const __grid_constant__ HashGatherParams p) {
+    pdl_wait();  // the row numbers of hash_index_kernel are complete and visible
+    extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x;
-    const int staged_entries = p.staged_seqs ? p.num_seqs + 1 : 0;
-    const HashSmemLayout L = hash_smem_layout(p.tile_tokens, p.tables, p.row_bytes, staged_entries);
+    const HashSmemLayout L = hash_smem_layout(p.tile_tokens, p.tables, p.row_bytes, 0);
     uint8_t *tiles = smem + L.tiles;
     int64_t *rows = reinterpret_cast<int64_t *>(smem + L.rows);
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + L.bars);
     const int64_t ntiles = (p.T + p.tile_tokens - 1) / p.tile_tokens;
     const uint32_t et_bytes = static_cast<uint32_t>(p.tables) * p.row_bytes;  // one token's e_t row
     const uint32_t tile_bytes = static_cast<uint32_t>(p.tile_tokens) * et_bytes;
-
-    // Sequence offsets: staged in shared memory when they fit; one CTA also checks that
-    // 0 = o_0 <= o_1 <= ... <= o_S = T.
-    const int64_t *offs = p.seq_offsets;
-    if (p.staged_seqs) {
-        int64_t *so = reinterpret_cast<int64_t *>(smem + L.offs);
-        for (int s = tid; s <= p.num_seqs; s += kHashThreads) so[s] = p.seq_offsets[s];
-        offs = so;
-    }
     if (tid == 0) {
         mbar_init(&bar[0], 1);
         mbar_init(&bar[1], 1);
         mbar_init_fence();
     }
     __syncthreads();
-    if (blockIdx.x == 0) {
-        for (int s = tid; s <= p.num_seqs; s += kHashThreads) {
-            const int64_t o = offs[s];
-            bool bad = (s == 0 && o != 0) || (s == p.num_seqs && o != p.T) || o < 0 || o > p.T;
-            if (s > 0 && offs[s - 1] > o) bad = true;
-            if (bad) report(p.status, p.err_word, ENGRAM_DEVERR_SEQ_OFFSETS);
-        }
-    }
 
     int64_t tile = blockIdx.x;
-    if (tile < ntiles) {
-        tile_ids(p, offs, st, 0, tile, tid);
-        __syncthreads();
-        tile_hash(p, st, rows, 0, tile, tid);
-    }
+    if (tile < ntiles) tile_rows(p, rows, 0, tile, tid);
     __syncthreads();
 
     bool failed = false;
@@ -224,10 +271,10 @@ __global__ void __launch_bounds__(kHashThreads) hash_gather_kernel(const __grid_
         const int ntok = static_cast<int>(p.T - t0 < p.tile_tokens ? p.T - t0 : p.tile_tokens);
         const int64_t next = tile + gridDim.x;
         uint8_t *tl = tiles + static_cast<size_t>(b) * tile_bytes;
-        const int ncopies = p.out_rows ? ntok * p.tables : 0;
+        const int ncopies = ntok * p.tables;
 
-        // 3a. tile buffer b was last stored two tiles ago: once that store has read it, refill it.
-        if (tid == 0 && ncopies) {
+        // tile buffer b was last stored two tiles ago: once that store has read it, refill it
+        if (tid == 0) {
             bulk_wait_read_all_but_one();
             mbar_arrive_expect_tx(&bar[b], static_cast<uint32_t>(ncopies) * p.row_bytes);
         }
@@ -237,13 +284,11 @@ __global__ void __launch_bounds__(kHashThreads) hash_gather_kernel(const __grid_
             bulk_load_plain(tl + static_cast<size_t>(e) * p.row_bytes,
                             p.table + static_cast<size_t>(r[e]) * p.row_bytes, p.row_bytes, &bar[b]);
 
-        // 1-2 of the next tile while those copies are in flight
-        if (next < ntiles) tile_ids(p, offs, st, b ^ 1, next, tid);
-        __syncthreads();
-        if (next < ntiles) tile_hash(p, st, rows, b ^ 1, next, tid);
+        // the next tile's row numbers while those copies are in flight
+        if (next < ntiles) tile_rows(p, rows, b ^ 1, next, tid);
 
-        // 3b. when the tile has landed, one bulk store of its e_t rows
-        if (tid == 0 && ncopies) {
+        // when the tile has landed, one bulk store of its e_t rows
+        if (tid == 0) {
             const uint32_t parity = static_cast<uint32_t>((it >> 1) & 1);
             if (!mbar_wait(&bar[b], parity)) {
                 report(p.status, p.err_word, ENGRAM_DEVERR_TIMEOUT);
@@ -455,15 +500,18 @@ extern "C" engram_status engram_hash_gather(const engram_hash_spec *spec, const 
     if (st != ENGRAM_OK) return st;
     const int tables = p.tables;
     const int64_t row_bytes = p.row_bytes;
-    // Tile of ~kTileBytes of e_t rows; persistent grid of as many CTAs as fit at once
-    // (>= 1: T = 0 still checks the offsets).
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // 1-2: one thread per token (>= 1 block: T = 0 still checks the offsets)
+    const int64_t iblocks = std::max<int64_t>(1, std::min<int64_t>((a->T + 255) / 256, 8LL * dev.num_sms));
+    cudaError_t le = launch_kernel(hash_index_kernel, dim3(static_cast<unsigned>(iblocks)), dim3(256), 0, s, p);
+    if (le != cudaSuccess) return fail(ENGRAM_ERR_CUDA, "engram_hash_gather launch: %s", cudaGetErrorString(le));
+    if ((st = check_launch("engram_hash_gather")) != ENGRAM_OK || !p.out_rows || a->T == 0) return st;
+    // 3: tiles of ~kTileBytes of e_t rows; persistent grid of as many CTAs as fit at once
     const int et_bytes = static_cast<int>(row_bytes) * tables;
     p.tile_tokens = std::min(kTileMax, std::max(1, kTileBytes / et_bytes));
-    p.staged_seqs = a->num_seqs + 1 <= kSmemSeqs ? 1 : 0;
-    const HashSmemLayout L = hash_smem_layout(p.tile_tokens, tables, p.row_bytes, p.staged_seqs ? a->num_seqs + 1 : 0);
+    const HashSmemLayout L = hash_smem_layout(p.tile_tokens, tables, p.row_bytes, 0);
     const int dyn = static_cast<int>(L.total);
-    if (dyn > dev.smem_optin - static_cast<int>(sizeof(TileIds)))
-        return fail(ENGRAM_ERR_SHAPE, "engram_hash_gather: %d bytes of shared memory needed", dyn);
+    if (dyn > dev.smem_optin) return fail(ENGRAM_ERR_SHAPE, "engram_hash_gather: %d bytes of shared memory needed", dyn);
     if ((st = set_smem(reinterpret_cast<const void *>(hash_gather_kernel), dyn)) != ENGRAM_OK) return st;
     int per_sm = 0;
     cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, hash_gather_kernel, kHashThreads, dyn);
@@ -472,8 +520,7 @@ extern "C" engram_status engram_hash_gather(const engram_hash_spec *spec, const 
     int64_t grid = static_cast<int64_t>(dev.num_sms) * std::max(per_sm, 1);
     if (grid > ntiles) grid = ntiles;
     grid = cap_grid(grid);
-    cudaError_t le = launch_kernel(hash_gather_kernel, dim3(static_cast<unsigned>(grid)), dim3(kHashThreads), dyn,
-                                   reinterpret_cast<cudaStream_t>(stream), p);
+    le = launch_kernel(hash_gather_kernel, dim3(static_cast<unsigned>(grid)), dim3(kHashThreads), dyn, s, p);
     if (le != cudaSuccess) return fail(ENGRAM_ERR_CUDA, "engram_hash_gather launch: %s", cudaGetErrorString(le));
     return check_launch("engram_hash_gather");
 }
