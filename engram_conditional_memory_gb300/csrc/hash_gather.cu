@@ -35,6 +35,7 @@ namespace engram {
 constexpr int kTileMax = 32;           // tokens per tile at most
 constexpr int kHashThreads = 256;      // threads per CTA
 constexpr int kTileBytes = 32 * 1024;  // target bytes of e_t rows per tile
+constexpr int kIndexThreads = 128;     // hash_index_kernel: one thread per token
 constexpr int kSmemSeqs = 4096;        // sequence offsets staged in shared memory up to this count
 constexpr int kMaxEtBytes = 64 * 1024; // largest e_t row (tables x row bytes) the kernel takes
 
@@ -58,6 +59,7 @@ struct HashGatherParams {
     int32_t staged_seqs;   // 1 when the offsets are staged in shared memory
     int8_t order[ENGRAM_MAX_TABLES];
     uint64_t prime[ENGRAM_MAX_TABLES];
+    uint64_t prime_inv[ENGRAM_MAX_TABLES];  // floor((2^64 - 1) / prime): Barrett reduction
     int64_t row_off[ENGRAM_MAX_TABLES];
     uint64_t mult[ENGRAM_MAX_TABLES][ENGRAM_MAX_ORDER];
 };
@@ -97,6 +99,16 @@ __device__ __forceinline__ int64_t sequence_start(const int64_t *offs, int32_t n
     if (s > t) s = t;
     if (s < 0) s = 0;
     return s;
+}
+
+// h mod p by Barrett reduction (P. Barrett, 1986) with inv = floor((2^64 - 1) / p): the quotient
+// estimate q = floor(h inv / 2^64) lies in [floor(h / p) - 2, floor(h / p)], so h - q p is below 3p
+// and at most two subtractions make it exact -- the same value as the % operator.
+__device__ __forceinline__ uint64_t mod_prime(uint64_t h, uint64_t p, uint64_t inv) {
+    uint64_t r = h - __umul64hi(h, inv) * p;
+    if (r >= p) r -= p;
+    if (r >= p) r -= p;
+    return r;
 }
 
 struct TileIds {
@@ -151,7 +163,7 @@ __device__ __forceinline__ void tile_hash(const HashGatherParams &p, const TileI
             const uint64_t id = (t - j >= st.start[b][i]) ? static_cast<uint64_t>(st.cid[b][i + back - j]) : 0ull;
             h ^= id * p.mult[tb][j];
         }
-        const uint64_t idx = h % p.prime[tb];
+        const uint64_t idx = mod_prime(h, p.prime[tb], p.prime_inv[tb]);
         r[e] = p.row_off[tb] + static_cast<int64_t>(idx);
         if (p.out_idx) p.out_idx[t * p.tables + tb] = static_cast<int32_t>(idx);
     }
@@ -176,20 +188,27 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 // the absolute row numbers (int64, row_off[table] + index) parked in the first 8 x tables bytes of
 // the token's own e_t row, which hash_gather_kernel reads back before it overwrites that row.
 // Block 0 also checks that 0 = o_0 <= o_1 <= ... <= o_S = T.
-__global__ void __launch_bounds__(256) hash_index_kernel(const __grid_constant__ HashGatherParams p) {
+__global__ void __launch_bounds__(kIndexThreads) hash_index_kernel(const __grid_constant__ HashGatherParams p) {
     pdl_wait();  // the previous kernel's writes are complete and visible
+    extern __shared__ __align__(16) int64_t so[];
+    const int64_t *offs = p.seq_offsets;
+    if (p.staged_seqs) {  // the sequence offsets in shared memory when they fit
+        for (int s = threadIdx.x; s <= p.num_seqs; s += blockDim.x) so[s] = p.seq_offsets[s];
+        offs = so;
+        __syncthreads();
+    }
     if (blockIdx.x == 0) {
         for (int s = threadIdx.x; s <= p.num_seqs; s += blockDim.x) {
-            const int64_t o = p.seq_offsets[s];
+            const int64_t o = offs[s];
             bool bad = (s == 0 && o != 0) || (s == p.num_seqs && o != p.T) || o < 0 || o > p.T;
-            if (s > 0 && p.seq_offsets[s - 1] > o) bad = true;
+            if (s > 0 && offs[s - 1] > o) bad = true;
             if (bad) report(p.status, p.err_word, ENGRAM_DEVERR_SEQ_OFFSETS);
         }
     }
     const uint32_t et_bytes = static_cast<uint32_t>(p.tables) * p.row_bytes;
     for (int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; t < p.T;
          t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t s0 = sequence_start(p.seq_offsets, p.num_seqs, t);
+        const int64_t s0 = sequence_start(offs, p.num_seqs, t);
         uint64_t cid[ENGRAM_MAX_ORDER];
 #pragma unroll
         for (int j = 0; j < ENGRAM_MAX_ORDER; ++j) {
@@ -217,7 +236,7 @@ __global__ void __launch_bounds__(256) hash_index_kernel(const __grid_constant__
 #pragma unroll
             for (int j = 0; j < ENGRAM_MAX_ORDER; ++j)
                 if (j < n) h ^= cid[j] * p.mult[tb][j];
-            const uint64_t idx = h % p.prime[tb];
+            const uint64_t idx = mod_prime(h, p.prime[tb], p.prime_inv[tb]);
             if (park) park[tb] = p.row_off[tb] + static_cast<int64_t>(idx);
             if (p.out_idx) p.out_idx[t * p.tables + tb] = static_cast<int32_t>(idx);
         }
@@ -433,6 +452,7 @@ engram_status prepare_hash_gather(const engram_hash_spec *spec, const engram_has
         if (pr == 0 || pr >= (1ull << 31)) return fail(ENGRAM_ERR_SHAPE, "engram_hash_gather: primes[%d] = %llu", tb,
                                                       (unsigned long long)pr);
         p.prime[tb] = pr;
+        p.prime_inv[tb] = ~0ull / pr;
         p.row_off[tb] = sum;
         sum += static_cast<int64_t>(pr);
         p.order[tb] = static_cast<int8_t>(spec->min_order + tb / spec->heads);
@@ -502,8 +522,12 @@ extern "C" engram_status engram_hash_gather(const engram_hash_spec *spec, const 
     const int64_t row_bytes = p.row_bytes;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     // 1-2: one thread per token (>= 1 block: T = 0 still checks the offsets)
-    const int64_t iblocks = std::max<int64_t>(1, std::min<int64_t>((a->T + 255) / 256, 8LL * dev.num_sms));
-    cudaError_t le = launch_kernel(hash_index_kernel, dim3(static_cast<unsigned>(iblocks)), dim3(256), 0, s, p);
+    const int64_t iblocks =
+        std::max<int64_t>(1, std::min<int64_t>((a->T + kIndexThreads - 1) / kIndexThreads, 16LL * dev.num_sms));
+    p.staged_seqs = a->num_seqs + 1 <= kSmemSeqs ? 1 : 0;
+    const int ismem = p.staged_seqs ? (a->num_seqs + 1) * 8 : 0;
+    if ((st = set_smem(reinterpret_cast<const void *>(hash_index_kernel), ismem)) != ENGRAM_OK) return st;
+    cudaError_t le = launch_kernel(hash_index_kernel, dim3(static_cast<unsigned>(iblocks)), dim3(kIndexThreads), ismem, s, p);
     if (le != cudaSuccess) return fail(ENGRAM_ERR_CUDA, "engram_hash_gather launch: %s", cudaGetErrorString(le));
     if ((st = check_launch("engram_hash_gather")) != ENGRAM_OK || !p.out_rows || a->T == 0) return st;
     // 3: tiles of ~kTileBytes of e_t rows; persistent grid of as many CTAs as fit at once
