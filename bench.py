@@ -536,7 +536,6 @@ def main_only(args, device):
         offs = torch.arange(0, T + 1, 4096, dtype=torch.int64, device=device)
         out, rstd = ecm.short_conv_fwd(v, nw, cwt, offs, cw.dilation, h=h, bias=bias)
         dv, part = ecm.short_conv_bwd(g, v, nw, cwt, rstd, offs, cw.dilation, bias=bias)
-        tdot = torch.empty((T, ecm.short_conv_dot_blocks(d)), dtype=torch.float32, device=device)
         red = ecm.short_conv_grad_reduce(part, cw.width, d)
         P = part.shape[0]
         if op == "short_conv_fwd":  # the op's own bytes: V~ and H read, out written, rstd written
@@ -548,8 +547,7 @@ def main_only(args, device):
             nbytes = 3 * T * d * 2 + 4 * T + P * (cw.width + 2) * d * 4
 
             def launch():
-                ecm.short_conv_bwd(g, v, nw, cwt, rstd, offs, cw.dilation, bias=bias, dv=dv, token_dot=tdot,
-                                   dw_partial=part)
+                ecm.short_conv_bwd(g, v, nw, cwt, rstd, offs, cw.dilation, bias=bias, dv=dv, dw_partial=part)
         else:
             nbytes = P * (cw.width + 2) * d * 4 + (cw.width + 2) * d * 4
 

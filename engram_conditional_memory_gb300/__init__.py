@@ -32,7 +32,6 @@ from .binding import (  # noqa: F401
     set_pdl,
     set_validation,
     short_conv_bwd,
-    short_conv_dot_blocks,
     short_conv_fwd,
     short_conv_grad_reduce,
     short_conv_num_partials,

@@ -91,9 +91,8 @@ def load_library():
             "engram_short_conv_fwd": (st, [_p, _p, _c.c_int, _p, _p, _p, _p, _i32, _i64, _i32, _i32, _i32,
                                            _c.c_float, _p, _p, _p]),
             "engram_short_conv_num_partials": (st, [_i64, _i32, _p]),
-            "engram_short_conv_dot_blocks": (st, [_i32, _p]),
             "engram_short_conv_bwd": (st, [_p, _p, _c.c_int, _p, _p, _p, _p, _p, _i32, _i64, _i32, _i32, _i32, _p,
-                                           _p, _p, _i32, _p]),
+                                           _p, _i32, _p]),
             "engram_short_conv_grad_reduce": (st, [_p, _i32, _i32, _i32, _p, _p, _p, _p]),
             "engram_sinkhorn_momentum_update": (st, [_p, _c.c_int, _p, _p, _i64, _c.c_float, _i32, _p]),
             "engram_sinkhorn_num_partials": (st, [_i64, _i32, _p]),
@@ -352,15 +351,8 @@ def short_conv_num_partials(T: int, dilation: int) -> int:
     return P.value
 
 
-def short_conv_dot_blocks(d: int) -> int:
-    lib = load_library()
-    nb = _c.c_int32(0)
-    _check(lib.engram_short_conv_dot_blocks(d, _c.byref(nb)), "engram_short_conv_dot_blocks")
-    return nb.value
-
-
-def short_conv_bwd(dout, v, norm_w, conv_w, rstd, seq_offsets, dilation: int, bias=None, dv=None, token_dot=None,
-                   dw_partial=None, stream=None):
+def short_conv_bwd(dout, v, norm_w, conv_w, rstd, seq_offsets, dilation: int, bias=None, dv=None, dw_partial=None,
+                   stream=None):
     """Returns (dv, dw_partial [P, width + 2, d]); dL/dh is dout itself."""
     lib = load_library()
     _need(dout, "dout", v.dtype)
@@ -369,13 +361,11 @@ def short_conv_bwd(dout, v, norm_w, conv_w, rstd, seq_offsets, dilation: int, bi
     width = conv_w.shape[1]
     P = short_conv_num_partials(T, dilation)
     dv = torch.empty_like(v) if dv is None else _need(dv, "dv", v.dtype)
-    if token_dot is None:
-        token_dot = torch.empty((T, short_conv_dot_blocks(d)), dtype=torch.float32, device=v.device)
     if dw_partial is None:
         dw_partial = torch.empty((P, width + 2, d), dtype=torch.float32, device=v.device)
     _check(lib.engram_short_conv_bwd(_ptr(dout), _ptr(v), _DTYPES[v.dtype], _ptr(norm_w), _ptr(conv_w), _ptr(bias),
                                      _ptr(rstd), _ptr(seq_offsets), seq_offsets.numel() - 1, T, d, width,
-                                     int(dilation), _ptr(dv), _ptr(token_dot), _ptr(dw_partial), P, _stream(stream)),
+                                     int(dilation), _ptr(dv), _ptr(dw_partial), P, _stream(stream)),
            "engram_short_conv_bwd")
     return dv, dw_partial
 

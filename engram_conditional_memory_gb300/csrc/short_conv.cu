@@ -11,57 +11,28 @@
 //     tokens plus the taps' halo into shared memory with 1-D bulk (TMA) copies, two or three tiles
 //     in flight, and compute every output from the tile: the taps are read back from shared memory
 //     instead of being carried along time, so there is no per-token bookkeeping;
-//   * conv_stencil_kernel (the backward): a warp owns 128 channels of one residue class
-//     t = r (mod dilation).  Every tap of a class token lies in the same class, so the warp sweeps
-//     its tokens in time order carrying the last three taps' inputs and the du still collecting
-//     contributions in registers.  Each warp streams its rows (V~ and dout) through its own ring of
-//     shared-memory stages filled by bulk copies that its lane 0 issues, and keeps a stage resident
-//     for the three tokens that read it back.  Per-token scalars (rstd, the row dots) come 64
-//     tokens at a time, two per lane, one window ahead, and reach a token by a shuffle.
-// The backward is two sweeps: the first gives each token's partial dot s = sum_j norm_w du V~ over
-// the warp's channels and the taps' and bias's gradient partials of its (time chunk, residue) work
-// item, the second the full dV~ = dout + rstd norm_w du - rstd^3 V~ s / d with s summed over the
-// channel blocks in a fixed order, and the norm weight's partials.  conv_grad_reduce_kernel sums
-// the partials in a fixed order.  The time chunks depend on T only, so the weight gradients are
-// bitwise reproducible on any GPU.
+//   * conv_bwd_kernel (the backward, one pass): a thread-block cluster of ceil(d / 1024) CTAs takes
+//     one residue class t = r (mod dilation) of one time chunk, each CTA 1024 channels.  Every tap of
+//     a class token lies in the same class, so the CTA sweeps its class tokens in time order, a
+//     producer warp streaming each token's V~ and dout row segments and rstd into a ring of
+//     shared-memory stages; each consumer thread carries its four channels' last three taps' inputs
+//     and the du still collecting contributions in registers.  The row dot s = sum_c norm_w du V~
+//     that dV~ needs couples all d channels of a token: each CTA sums its part for a few tokens at a
+//     time and exchanges it with the other CTAs of its cluster through distributed shared memory,
+//     then writes dV~ = dout + rstd norm_w du - rstd^3 V~ s / d and keeps the weight-gradient
+//     partials of its (time chunk, residue) work item;
+//   * conv_grad_reduce_kernel sums the partials in a fixed order.
+// The time chunks depend on T only, the clusters on d only, and every sum has a fixed order, so all
+// results are bitwise reproducible on any GPU.
 #include <algorithm>
+#include <atomic>
 
 #include "engram_internal.cuh"
 
 namespace engram {
 
-constexpr int kScWarps = 8;             // warps per CTA, each an independent work item
-constexpr int kScEV = 4;                // channels per lane
-constexpr int kScCols = 32 * kScEV;     // channels per warp
+constexpr int kScEV = 4;                // channels per thread
 constexpr int kScAges = 4;              // taps: width <= 4
-constexpr int kScRingBytes = 8192;      // per warp: stages x (V~ segment + second segment)
-constexpr int kScMaxBlocks = 64;        // channel blocks per row: d <= 64 * 128
-
-enum ScMode { kScBwdDot = 1, kScBwdFinal = 2 };  // the backward sweeps
-
-struct ScParams {
-    const uint8_t *v;          // V~ [T, d]
-    const uint8_t *x2;         // forward: H (nullable); backward: dout
-    const float *norm_w;       // [d]
-    const float *conv_w;       // [d, width]
-    const float *bias;         // [d] nullable
-    const float *rstd;         // [T]
-    const int64_t *offs;       // [num_seqs + 1]
-    const float *token_dot;    // final backward: [T, nb] partial dots
-    float *token_dot_out;      // first backward sweep: [T, nb]
-    uint8_t *out;              // forward: out; final backward: dv
-    float *partial;            // final backward: [nchunks * dil, width + 2, d]
-    uint32_t *status;
-    int64_t T;
-    int64_t chunk;             // tokens per time chunk
-    int64_t nchunks;
-    int32_t num_seqs;
-    int32_t d;
-    int32_t width;
-    int32_t dil;
-    int32_t nb;                // channel blocks of kScCols
-    int32_t stages;
-};
 
 // ---- four channels per lane: 8 bytes of bf16 or 16 bytes of fp32
 
@@ -337,319 +308,605 @@ __global__ void __launch_bounds__(256, 2) conv_fwd_kernel(const __grid_constant_
     }
 }
 
-// ------------------------------------------------------------------------------- the stencil sweep
+// ------------------------------------------------------------------------------- backward
 
-// Per-token scalars of the warp's sweep (indexed by the sweep position q), 64 at a time: lane l
-// holds positions w0 + l and w0 + 32 + l of the current window and the next window's two.
-struct ScWindow {
-    float lo, hi, nlo, nhi;
+constexpr int kBwCons = 256;                      // threads (8 warps), four channels each
+constexpr int kBwThreads = kBwCons;
+constexpr int kBwCW = kBwCons * kScEV;            // channels per CTA
+constexpr int kBwMaxCluster = 8;                  // CTAs per cluster: d <= 8 * 1024
+constexpr int kBwLag = kScAges - 1;               // taps behind a token and readers after it
+constexpr int kBwBatch = 4;                       // tokens whose row dots are exchanged together
+constexpr int kBwPrefetch = 5;                    // stages the copies may run ahead
+constexpr int kBwStages = 2 * kBwBatch + kBwLag + kBwPrefetch;  // two batches in flight
+enum ScKind { kScLead = 0, kScMain = 1, kScTail = 2 };
+
+struct ScBwdParams {
+    const uint8_t *v;          // V~ [T, d]
+    const uint8_t *dout;       // [T, d]
+    const float *norm_w;       // [d]
+    const float *conv_w;       // [d, width]
+    const float *bias;         // [d] nullable
+    const float *rstd;         // [T]
+    const int64_t *offs;       // [num_seqs + 1]
+    uint8_t *dv;               // [T, d]
+    float *partial;            // [nitems, width + 2, d]
+    uint32_t *status;
+    int64_t T;
+    int64_t chunk;             // tokens per time chunk
+    int64_t nitems;            // chunks x dilation
+    int32_t num_seqs;
+    int32_t d;
+    int32_t width;
+    int32_t dil;
 };
 
-template <typename E, int MODE>
-__global__ void __launch_bounds__(kScWarps * 32) conv_stencil_kernel(const __grid_constant__ ScParams p) {
+// Shared memory of one backward CTA: the stage ring; by batch parity the y rows [2][kBwBatch][kBwCons]
+// float4 and row-dot parts [2][kBwBatch][kBwCons]; by batch mod 4 the cluster's row dots
+// [4][kBwMaxCluster][kBwBatch]; the stages' position records (16 bytes each); by batch mod 4 the
+// batch tokens' stages [4][kBwBatch]; the mbarriers (full and empty per stage, 2 batch-done,
+// 4 exchange); then the copy producer's state.
+__host__ __device__ inline int sc_bwd_smem(int stages, int stage_bytes) {
+    return stages * stage_bytes + 2 * kBwBatch * kBwCons * 16 + 2 * kBwBatch * kBwCons * 4 +
+           4 * kBwMaxCluster * kBwBatch * 4 + stages * 16 + 4 * kBwBatch * 4 + (2 * stages + 6) * 8 + 128;
+}
+
+// A stage: the V~ segment of 1024 channels, then the dout segment.
+template <typename E>
+__host__ __device__ constexpr int sc_bwd_stage_bytes() {
+    return 2 * kBwCW * static_cast<int>(sizeof(E));
+}
+
+template <int N>
+struct ScIdx {
+    static constexpr int v = N;
+};
+
+__device__ __forceinline__ uint32_t sc_cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t sc_cluster_size() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t sc_cluster_id() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t sc_num_clusters() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+// Every thread of every CTA of the cluster; release / acquire order shared memory across it.
+__device__ __forceinline__ void sc_cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+// The shared::cluster address of this CTA's shared address `a` in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t sc_mapa(uint32_t a, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+    return r;
+}
+// A 4-byte store into another CTA's shared memory that completes 4 tx bytes on its mbarrier.
+__device__ __forceinline__ void sc_st_async(uint32_t raddr, float v, uint32_t rbar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(raddr),
+                 "r"(__float_as_uint(v)), "r"(rbar)
+                 : "memory");
+}
+// A 4-byte asynchronous global -> shared copy, and an arrival on `bar` once this thread's
+// earlier asynchronous copies have landed (the barrier's count includes it).
+__device__ __forceinline__ void sc_cp_async4(void *dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void sc_cp_async_arrive(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// One segment of a work item: the class tokens first, first + dil, ... (n_main of them) of one
+// sequence inside the item's chunk, with the n_lead class tokens before them whose V~ the first
+// taps read, and the n_tail class tokens after them whose dc completes the last du.
+struct ScSeg {
+    int64_t first;
+    int n_lead, n_main, n_tail;
+};
+
+// The next segment of class r in [x, t_hi); x and the sequence index s advance.  Offsets that are
+// not sorted still give progress and tokens inside [0, T).
+__device__ __forceinline__ bool sc_next_seg(const ScBwdParams &p, int r, int64_t t_hi, int64_t &x, int &s,
+                                            ScSeg &g) {
+    const int64_t dil = p.dil;
+    while (x < t_hi) {
+        while (s + 1 < p.num_seqs && __ldg(p.offs + s + 1) <= x) ++s;
+        int64_t s0 = __ldg(p.offs + s), s1 = __ldg(p.offs + s + 1);
+        if (s0 > x) s0 = x;
+        if (s0 < 0) s0 = 0;
+        if (s1 > p.T) s1 = p.T;
+        if (s1 <= x) s1 = x + 1;
+        const int64_t e = s1 < t_hi ? s1 : t_hi;
+        const int64_t first = x + ((r - x % dil) % dil + dil) % dil;
+        x = e;
+        if (first >= e) continue;
+        const int64_t last = first + (e - 1 - first) / dil * dil;
+        g.first = first;
+        g.n_main = static_cast<int>((last - first) / dil + 1);
+        const int64_t lead = (first - s0) / dil, tail = (s1 - 1 - last) / dil;
+        g.n_lead = static_cast<int>(lead < kBwLag ? lead : kBwLag);
+        g.n_tail = static_cast<int>(tail < kBwLag ? tail : kBwLag);
+        return true;
+    }
+    return false;
+}
+
+// What the producer tells the consumers about each sweep position, beside its stage: the token,
+// its rstd (copied asynchronously) and flags.
+struct ScMeta {
+    int64_t tok;
+    float rstd;
+    uint32_t flags;
+};
+constexpr uint32_t kFlKind = 3u;          // bits 0-1: kScLead, kScMain or kScTail
+constexpr int kFlSlotShift = 2;           // bits 2-3: slot (position in the segment mod 4)
+constexpr uint32_t kFlSegStart = 1u << 4;
+constexpr uint32_t kFlSegEnd = 1u << 5;
+constexpr uint32_t kFlGroup = 1u << 6;    // this and the next three positions form a steady group
+constexpr uint32_t kFlItemStart = 1u << 7;
+constexpr uint32_t kFlDone = 1u << 8;     // no position: the cluster's items are done
+constexpr int kFlItemShift = 12;          // bits 12-31: the work item, at an item start
+constexpr int64_t kBwMaxItems = int64_t(1) << 20;
+
+// The producer's place in the stream of sweep positions of its cluster's work items (thread 0
+// only, in shared memory).
+struct ScProd {
+    int64_t item;      // current work item
+    int64_t t_hi;      // its chunk's end
+    int64_t xs;        // where its next segment starts looking
+    int64_t t;         // token of the next position
+    uint32_t issued;   // positions issued so far (the sentinel included)
+    uint32_t round;    // times the ring has wrapped
+    int32_t st;        // stage of the next position
+    int32_t s;         // sequence index of xs
+    int32_t q, n, n_lead, n_main;  // next position of the segment, its positions, lead-in, chunk tokens
+    int32_t new_item;  // the next position starts a work item
+    int32_t state;     // 0 positions to issue, 1 only the sentinel, 2 finished
+};
+static_assert(sizeof(ScProd) <= 128, "the producer state fits its shared-memory slot");
+
+// The backward in one pass.  A cluster of ceil(d / 1024) CTAs takes work items (time chunk,
+// residue class t = r mod dilation); CTA `rank` holds channels [1024 rank, 1024 rank + 1024).
+// Thread 0 walks the items' segments and streams, per sweep position, the token's V~ and dout row
+// segments (1-D bulk copies) and its rstd (a 4-byte asynchronous copy) into a ring of stages, as
+// far ahead as the ring allows, with a record of the position (token, kind, segment and item
+// boundaries).  Every thread owns four channels and sweeps the positions in order:
+//   u  = V~ rstd norm_w (the last three kept by age in registers),
+//   dc = dout SiLU'(conv),  conv = bias + sum_a w_a u[t - a dil]   (w_a: tap width - 1 - a),
+//   the tap and bias gradients of the chunk's outputs, and the du = sum_a w_a dc[t + a dil] still
+//   collecting contributions (three of them, by age).
+// When a token's du is complete its stage is read back for V~ and dout:
+//   y = dout + rstd norm_w du  (kept in shared memory),  dnorm_w += du V~ rstd,
+//   and the thread's part of the row dot s = sum_c norm_w du V~.
+// Every four tokens a reducer warp sums the CTA's parts of each row dot (thread order, then
+// lanes) and sends the sums to the other CTAs of the cluster (distributed shared memory,
+// completing on their mbarrier); a batch later, when the cluster's sums have arrived, every thread
+// adds them in rank order and writes dv = y - rstd^3 V~ s / d.  All waits are bounded.
+// The chunks depend on T only and every sum has a fixed order, so results are bitwise reproducible.
+template <typename E>
+__global__ void __launch_bounds__(kBwThreads, 2) conv_bwd_kernel(const __grid_constant__ ScBwdParams p) {
     using EV = Ev4<E>;
     extern __shared__ __align__(128) uint8_t smem[];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int S = p.stages;
-    const int seg_max = kScCols * static_cast<int>(sizeof(E));
-    uint8_t *ring = smem + static_cast<size_t>(warp) * kScRingBytes;
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + static_cast<size_t>(kScWarps) * kScRingBytes) + warp * S;
+    constexpr int S = kBwStages;
+    constexpr int SB = sc_bwd_stage_bytes<E>();
+    constexpr int half = SB / 2;
+    uint8_t *ring = smem;
+    float4 *ybuf = reinterpret_cast<float4 *>(smem + static_cast<size_t>(S) * SB);
+    float *pbuf = reinterpret_cast<float *>(ybuf + 2 * kBwBatch * kBwCons);
+    float *box = pbuf + 2 * kBwBatch * kBwCons;
+    ScMeta *meta = reinterpret_cast<ScMeta *>(box + 4 * kBwMaxCluster * kBwBatch);
+    int *fin_stage = reinterpret_cast<int *>(meta + S);
+    uint64_t *full = reinterpret_cast<uint64_t *>(fin_stage + 4 * kBwBatch);
+    uint64_t *empty = full + S;
+    uint64_t *lbar = empty + S;
+    uint64_t *boxbar = lbar + 2;
+    ScProd *prod = reinterpret_cast<ScProd *>(boxbar + 4);
 
-    const int64_t item = static_cast<int64_t>(blockIdx.x) * kScWarps + warp;
-    const int cb = static_cast<int>(item % p.nb);
-    const int64_t kr = item / p.nb;
-    const int r = static_cast<int>(kr % p.dil);
-    const int64_t k = kr / p.dil;
-    if (k >= p.nchunks) return;  // whole warp: no shared state with the other warps
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const uint32_t rank = sc_cluster_rank();
+    const uint32_t C = sc_cluster_size();
+    const int c0 = static_cast<int>(rank) * kBwCW;
+    const int ncols = p.d - c0 < kBwCW ? p.d - c0 : kBwCW;
+    const int64_t dil = p.dil;
+    bool failed = false;
 
-    const int64_t t_lo = k * p.chunk;
-    const int64_t t_hi = t_lo + p.chunk < p.T ? t_lo + p.chunk : p.T;
-    const int c0 = cb * kScCols;
-    const int ncols = p.d - c0 < kScCols ? p.d - c0 : kScCols;
-    const uint32_t seg = static_cast<uint32_t>(ncols) * sizeof(E);
-    const bool active = lane * kScEV < ncols;
-    const size_t row_bytes = static_cast<size_t>(p.d) * sizeof(E);
-    const int dil = p.dil;
-    auto first_class = [&](int64_t x) { return x + ((r - x % dil) % dil + dil) % dil; };
+    // thread 0: the next segment of the producer's stream, moving on through the cluster's items
+    auto prod_next_seg = [&]() {
+        ScProd &P = *prod;
+        ScSeg g;
+        for (;;) {
+            int64_t xs = P.xs;
+            int s = P.s;
+            const bool found = sc_next_seg(p, static_cast<int>(P.item % dil), P.t_hi, xs, s, g);
+            P.xs = xs;
+            P.s = s;
+            if (found) {
+                P.q = 0;
+                P.n = g.n_lead + g.n_main + g.n_tail;
+                P.n_lead = g.n_lead;
+                P.n_main = g.n_main;
+                P.t = g.first - g.n_lead * dil;
+                return;
+            }
+            const int64_t next = P.item + sc_num_clusters();
+            if (next >= p.nitems) {
+                P.state = 1;
+                return;
+            }
+            P.item = next;
+            P.new_item = 1;
+            const int64_t t_lo = next / dil * p.chunk;
+            P.xs = t_lo;
+            P.t_hi = t_lo + p.chunk < p.T ? t_lo + p.chunk : p.T;
+            P.s = sc_seq_of(p.offs, p.num_seqs, t_lo);
+        }
+    };
+    // thread 0: issue every position whose stage is free; wait (bounded) until position `need` is
+    // issued, unless the stream ends first
+    auto produce = [&](uint32_t need) {
+        if (failed) return;
+        ScProd &P = *prod;
+        const uint32_t seg = static_cast<uint32_t>(ncols) * sizeof(E);
+        const size_t row_bytes = static_cast<size_t>(p.d) * sizeof(E);
+        const size_t col_off = static_cast<size_t>(c0) * sizeof(E);
+        while (P.state != 2) {
+            const int st = P.st;
+            if (P.round > 0) {
+                const uint32_t par = (P.round + 1) & 1u;
+                if (static_cast<int32_t>(P.issued - need) > 0) {
+                    if (!mbar_test_wait(&empty[st], par)) break;
+                } else if (!mbar_wait(&empty[st], par)) {
+                    report(p.status, nullptr, ENGRAM_DEVERR_TIMEOUT);
+                    failed = true;
+                    P.state = 2;
+                    break;
+                }
+            }
+            if (P.state == 1) {  // the sentinel: no copies, both arrivals
+                meta[st].tok = 0;
+                meta[st].flags = kFlDone;
+                mbar_arrive(&full[st]);
+                mbar_arrive(&full[st]);
+                P.state = 2;
+            } else {
+                const int q = P.q, n = P.n, nl = P.n_lead, nm = P.n_main;
+                const uint32_t kind = q < nl ? kScLead : (q < nl + nm ? kScMain : kScTail);
+                const bool group = (q & 3) == 0 && q >= nl + kBwLag && q + 4 <= nl + nm && q + 4 < n;
+                uint32_t fl = kind | (static_cast<uint32_t>(q & 3) << kFlSlotShift);
+                if (q == 0) fl |= kFlSegStart;
+                if (q == n - 1) fl |= kFlSegEnd;
+                if (group) fl |= kFlGroup;
+                if (P.new_item) fl |= kFlItemStart | (static_cast<uint32_t>(P.item) << kFlItemShift);
+                const int64_t t = P.t;
+                meta[st].tok = t;
+                meta[st].flags = fl;
+                uint8_t *dst = ring + static_cast<size_t>(st) * SB;
+                sc_cp_async4(&meta[st].rstd, p.rstd + t);
+                sc_cp_async_arrive(&full[st]);
+                mbar_arrive_expect_tx(&full[st], kind == kScLead ? seg : 2 * seg);
+                bulk_load_plain(dst, p.v + static_cast<size_t>(t) * row_bytes + col_off, seg, &full[st]);
+                if (kind != kScLead)
+                    bulk_load(dst + half, p.dout + static_cast<size_t>(t) * row_bytes + col_off, seg, &full[st],
+                              l2_evict_first_policy());
+                P.new_item = 0;
+                if (q + 1 == n) prod_next_seg();
+                else P.q = q + 1, P.t = t + dil;
+            }
+            ++P.issued;
+            if (st + 1 == S) P.st = 0, ++P.round;
+            else P.st = st + 1;
+        }
+    };
 
-    // per-lane constants: taps by age (age a multiplies the token a * dil back), norm weight, bias
-    float K[kScAges][kScEV], nw[kScEV], bias[kScEV];
+    if (tid == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(&full[i], 2);  // the producer's arrival and its rstd copy's
+            mbar_init(&empty[i], kBwCons / 32);
+        }
+        for (int i = 0; i < 2; ++i) mbar_init(&lbar[i], kBwCons / 32);
+        for (int i = 0; i < 4; ++i) mbar_init(&boxbar[i], 1);
+        mbar_init_fence();
+    }
+    sc_cluster_sync();  // every CTA's barriers exist before any remote arrival
+    pdl_wait();
+    if (tid == 0) {
+        ScProd &P = *prod;
+        P = ScProd{};
+        P.item = sc_cluster_id();
+        if (P.item >= p.nitems) {
+            P.state = 1;
+        } else {
+            const int64_t t_lo = P.item / dil * p.chunk;
+            P.xs = t_lo;
+            P.t_hi = t_lo + p.chunk < p.T ? t_lo + p.chunk : p.T;
+            P.s = sc_seq_of(p.offs, p.num_seqs, t_lo);
+            P.new_item = 1;
+            prod_next_seg();
+        }
+        produce(0);  // fill the ring
+    }
+    __syncthreads();
+
+    const bool active = tid * kScEV < ncols;
+    const int width = p.width, d = p.d;
+    float w[kScAges][kScEV], nw[kScEV], bias[kScEV];
 #pragma unroll
     for (int e = 0; e < kScEV; ++e) {
-        const int c = c0 + lane * kScEV + e;
-        const bool ok = active && c < p.d;
+        const int c = c0 + tid * kScEV + e;
+        const bool ok = active && c < d;
         nw[e] = ok ? __ldg(p.norm_w + c) : 0.f;
         bias[e] = ok && p.bias ? __ldg(p.bias + c) : 0.f;
 #pragma unroll
         for (int a = 0; a < kScAges; ++a)
-            K[a][e] = ok && a < p.width ? __ldg(p.conv_w + static_cast<size_t>(c) * p.width + (p.width - 1 - a)) : 0.f;
+            w[a][e] = ok && a < width ? __ldg(p.conv_w + static_cast<size_t>(c) * width + (width - 1 - a)) : 0.f;
     }
+    const float inv_d = 1.0f / static_cast<float>(d);
 
-    // the sweep: class tokens from up to three taps before the chunk (their inputs only) to the
-    // chunk's end, or three taps past it for the backward (their dc completes the chunk's du)
-    const int64_t t_first = first_class(t_lo);
-    int64_t n_sw = 0, t_a = t_first;
-    int s = 0;
-    if (t_first < t_hi) {
-        s = sc_seq_of(p.offs, p.num_seqs, t_first);
-        const int64_t hist = t_first - static_cast<int64_t>(kScAges - 1) * dil;
-        const int64_t s0 = __ldg(p.offs + s);
-        t_a = first_class(hist > s0 ? hist : s0);
-        int64_t t_b = t_hi + static_cast<int64_t>(kScAges - 1) * dil;
-        if (t_b > p.T) t_b = p.T;
-        n_sw = (t_b - t_a + dil - 1) / dil;
-    }
-
-    // lane 0 streams the sweep's rows: a lead-in token (before the chunk) needs V~ only.  A stage
-    // stays resident for three tokens after its own, which read it back as their taps' inputs.
-    const uint64_t pol = l2_evict_first_policy();
-    constexpr bool two = true;
-    const size_t col_off = static_cast<size_t>(c0) * sizeof(E);
-    const size_t step_bytes = static_cast<size_t>(dil) * row_bytes;
-    const uint8_t *src_v = p.v + static_cast<size_t>(t_a) * row_bytes + col_off;
-    const uint8_t *src_2 = two ? p.x2 + static_cast<size_t>(t_a) * row_bytes + col_off : nullptr;
-    int64_t issued = 0, t_issue = t_a;
-    int ist = 0;
-    auto issue = [&]() {
-        const bool second = two && t_issue >= t_lo;
-        uint8_t *dst = ring + static_cast<size_t>(ist) * 2 * seg_max;
-        mbar_arrive_expect_tx(&full[ist], second ? 2 * seg : seg);
-        bulk_load(dst, src_v, seg, &full[ist], pol);
-        if (second) bulk_load(dst + seg_max, src_2, seg, &full[ist], pol);
-        src_v += step_bytes;
-        if (two) src_2 += step_bytes;
-        t_issue += dil;
-        ++issued;
-        if (++ist == S) ist = 0;
-    };
-    if (lane == 0) {
-        for (int q = 0; q < S; ++q) mbar_init(&full[q], 1);
-        mbar_init_fence();
-        while (issued < S && issued < n_sw) issue();
-    }
-    __syncwarp();
-
-    // positions q of the sweep (token t_a + q dil): the chunk's tokens are [q_lo, q_hi)
-    const int64_t n_sw_l = n_sw;
-    const int nq = static_cast<int>(n_sw_l);
-    const int q_lo = static_cast<int>((t_first - t_a) / dil);
-    const int q_hi = static_cast<int>((t_hi - t_a + dil - 1) / dil);
-    const int nb = p.nb;
-    const float inv_d = 1.0f / static_cast<float>(p.d);
-    const int num_seqs = p.num_seqs;
-    const int64_t *offs = p.offs;
-    const float *rstd_p = p.rstd;
-    const float *tdot = p.token_dot;
-    float *tdot_out = p.token_dot_out;
-    auto pos_of = [&](int64_t tt) {  // first position whose token is >= tt
-        return tt <= t_a ? 0 : static_cast<int>((tt - t_a + dil - 1) / dil);
-    };
-
-    // scalar windows: rstd, and the backward's row-dot totals (column 0 of token_dot) in the final sweep
-    auto scalar_at = [&](int q, bool dot) -> float {
-        if (q >= nq) return 0.f;
-        const int64_t t = t_a + static_cast<int64_t>(q) * dil;
-        return dot ? __ldg(tdot + static_cast<size_t>(t) * nb) : __ldg(rstd_p + t);
-    };
-    ScWindow wr{0.f, 0.f, scalar_at(lane, false), scalar_at(32 + lane, false)};
-    ScWindow ws{0.f, 0.f, 0.f, 0.f};
-    if (MODE == kScBwdFinal) ws.nlo = scalar_at(lane, true), ws.nhi = scalar_at(32 + lane, true);
-    int w0 = -64;
-
-    // histories by age (1..3): the RMSNorm output u and the scalars of those tokens, and (backward)
-    // the du still collecting contributions and whether its token is the chunk's.  The raw rows of
-    // those tokens stay in their stages.
-    float u1[kScEV] = {}, u2[kScEV] = {}, u3[kScEV] = {};
-    float P1[kScEV] = {}, P2[kScEV] = {}, P3[kScEV] = {};
-    float r1 = 0.f, r2 = 0.f, r3 = 0.f, sd1 = 0.f, sd2 = 0.f, sd3 = 0.f;
+    float U[4][kScEV];                      // u by slot: position q's in slot q & 3
+    float P1[kScEV], P2[kScEV], P3[kScEV];  // du collecting contributions, by age 1..3
+    float A[kScAges][kScEV], db[kScEV], dnw[kScEV];
     bool pend1 = false, pend2 = false, pend3 = false;
-    int q_seq_end = nq > 0 ? pos_of(__ldg(offs + s + 1)) : 0;
-    float dK[kScAges][kScEV], db[kScEV], dnw[kScEV];
-#pragma unroll
-    for (int e = 0; e < kScEV; ++e) {
-        db[e] = dnw[e] = 0.f;
-#pragma unroll
-        for (int a = 0; a < kScAges; ++a) dK[a][e] = 0.f;
-    }
-    int st = 0;          // stage of position q
-    uint32_t ph = 0;     // its phase
-    auto stage_back = [&](int a) { return st - a < 0 ? st - a + S : st - a; };
-    // this lane's output row segment of position q, and the row-dot entry
-    uint8_t *out_q = p.out ? p.out + static_cast<size_t>(t_a) * row_bytes + col_off + lane * EV::kBytes : nullptr;
-    float *dot_q = tdot_out ? tdot_out + static_cast<size_t>(t_a) * nb + cb : nullptr;
-    const size_t dot_step = static_cast<size_t>(dil) * nb;
+    int st = 0;
+    uint32_t ph = 0, gpos = 0;
+    int nfin = 0, nb = 0, prev_n = 0;  // tokens of the open batch, batches posted, tokens of the pending one
 
-    // backward: a token's du is complete -> its row-dot partial, or its dv and dnorm_w share.  Its
-    // V~ and dout are read back from its stage, `age` positions behind the current one.
-    auto emit = [&](int age, const float (&du)[kScEV], float rt, float sd) {
-        float x[kScEV] = {}, g[kScEV] = {};
-        const uint8_t *stg = ring + static_cast<size_t>(stage_back(age)) * 2 * seg_max;
-        if (active) {
-            EV::load_smem(stg + lane * EV::kBytes, x);
-            if (MODE == kScBwdFinal) EV::load_smem(stg + seg_max + lane * EV::kBytes, g);
-        }
-        if (MODE == kScBwdDot) {
-            float acc = 0.f;
-#pragma unroll
-            for (int e = 0; e < kScEV; ++e) acc = fmaf(nw[e] * du[e], x[e], acc);
-            acc = warp_sum(acc);
-            if (lane == 0) dot_q[-static_cast<ptrdiff_t>(age * dot_step)] = acc;
-        } else if (MODE == kScBwdFinal) {
-            const float k3 = rt * rt * rt * sd * inv_d;
-            float o[kScEV];
-#pragma unroll
-            for (int e = 0; e < kScEV; ++e) {
-                o[e] = g[e] + rt * nw[e] * du[e] - k3 * x[e];
-                dnw[e] = fmaf(du[e] * x[e], rt, dnw[e]);
-            }
-            if (active) EV::store(out_q - static_cast<ptrdiff_t>(age * step_bytes), o);
-        }
-    };
-    // the pending du have no more contributions (a sequence ended, or the sweep did); called
-    // before position q is processed, so the pending tokens sit 1..3 positions back
-    auto flush = [&]() {
-        if (pend3) emit(3, P3, r3, sd3);
-        if (pend2) emit(2, P2, r2, sd2);
-        if (pend1) emit(1, P1, r1, sd1);
-        pend1 = pend2 = pend3 = false;
-#pragma unroll
-        for (int e = 0; e < kScEV; ++e) {
-            u1[e] = u2[e] = u3[e] = 0.f;
-            P1[e] = P2[e] = P3[e] = 0.f;
-        }
-    };
-
-    bool failed = false;
-    int q = 0;
-    for (; q < nq; ++q) {
-        // a new sequence: the taps reach back no further, and the pending du are complete
-        if (q >= q_seq_end) {
-            flush();
-            if (q >= q_hi) break;  // the backward's look-ahead stays in the chunk's last sequence
-            const int64_t t = t_a + static_cast<int64_t>(q) * dil;
-            while (s + 1 < num_seqs && t >= __ldg(offs + s + 1)) ++s;
-            q_seq_end = pos_of(__ldg(offs + s + 1));
-            if (q_seq_end <= q) q_seq_end = q + 1;  // malformed offsets: treat the token as its own sequence
-        }
-        // scalars of position q
-        if (q - w0 >= 64) {
-            w0 += 64;
-            wr.lo = wr.nlo, wr.hi = wr.nhi;
-            wr.nlo = scalar_at(w0 + 64 + lane, false), wr.nhi = scalar_at(w0 + 96 + lane, false);
-            if (MODE == kScBwdFinal) {
-                ws.lo = ws.nlo, ws.hi = ws.nhi;
-                ws.nlo = scalar_at(w0 + 64 + lane, true), ws.nhi = scalar_at(w0 + 96 + lane, true);
-            }
-        }
-        const int wq = q - w0;
-        const float rt = __shfl_sync(0xffffffffu, wq < 32 ? wr.lo : wr.hi, wq & 31);
-        const float sdt = MODE == kScBwdFinal ? __shfl_sync(0xffffffffu, wq < 32 ? ws.lo : ws.hi, wq & 31) : 0.f;
-
-        // the row segments of position q
-        const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[st], ph));
-        if (!ok) {
+    // a wait of the whole warp: every lane takes the same view of a failure
+    auto wait_warp = [&](uint64_t *bar, uint32_t parity) {
+        if (failed) return;
+        if (!__all_sync(0xffffffffu, mbar_wait(bar, parity))) {
             if (lane == 0) report(p.status, nullptr, ENGRAM_DEVERR_TIMEOUT);
             failed = true;
-            break;
         }
-        const uint8_t *stage = ring + static_cast<size_t>(st) * 2 * seg_max;
-        const bool in_chunk = q >= q_lo && q < q_hi;
-        const bool led = q < q_lo;  // lead-in: the taps' inputs only
-        float x0[kScEV] = {}, y0[kScEV] = {};
-        if (active) {
-            EV::load_smem(stage + lane * EV::kBytes, x0);
-            if (two && !led) EV::load_smem(stage + seg_max + lane * EV::kBytes, y0);
-        }
-
-        float u0[kScEV], c[kScEV];
-#pragma unroll
-        for (int e = 0; e < kScEV; ++e) {
-            u0[e] = x0[e] * rt * nw[e];
-            c[e] = fmaf(K[3][e], u3[e], fmaf(K[2][e], u2[e], fmaf(K[1][e], u1[e], fmaf(K[0][e], u0[e], bias[e]))));
-        }
-        {
-            // dc = dout SiLU'(c) for the chunk's tokens and the look-ahead; 0 for the lead-in
-            float dc[kScEV];
-#pragma unroll
-            for (int e = 0; e < kScEV; ++e) {
-                const float sg = sc_sigmoid_fast(c[e]);
-                dc[e] = led ? 0.f : y0[e] * sg * fmaf(c[e], 1.0f - sg, 1.0f);
-            }
-            if (MODE == kScBwdDot && in_chunk) {  // the taps' and the bias's gradients, in the first sweep
-#pragma unroll
-                for (int e = 0; e < kScEV; ++e) {
-                    db[e] += dc[e];
-                    dK[0][e] = fmaf(dc[e], u0[e], dK[0][e]);
-                    dK[1][e] = fmaf(dc[e], u1[e], dK[1][e]);
-                    dK[2][e] = fmaf(dc[e], u2[e], dK[2][e]);
-                    dK[3][e] = fmaf(dc[e], u3[e], dK[3][e]);
-                }
-            }
-            // the token three taps back has all its contributions
-            if (pend3) {
-                float du[kScEV];
-#pragma unroll
-                for (int e = 0; e < kScEV; ++e) du[e] = fmaf(K[3][e], dc[e], P3[e]);
-                emit(3, du, r3, sd3);
-            }
-#pragma unroll
-            for (int e = 0; e < kScEV; ++e) {
-                P3[e] = fmaf(K[2][e], dc[e], P2[e]);
-                P2[e] = fmaf(K[1][e], dc[e], P1[e]);
-                P1[e] = K[0][e] * dc[e];
-            }
-            pend3 = pend2, pend2 = pend1, pend1 = in_chunk;
-        }
-        // age the histories and move to the next position
-#pragma unroll
-        for (int e = 0; e < kScEV; ++e) u3[e] = u2[e], u2[e] = u1[e], u1[e] = u0[e];
-        r3 = r2, r2 = r1, r1 = rt;
-        sd3 = sd2, sd2 = sd1, sd1 = sdt;
-        if (++st == S) {
-            st = 0;
-            ph ^= 1u;
-        }
-        if (out_q) out_q += step_bytes;
-        if (dot_q) dot_q += dot_step;
-        // positions q - 2 .. q stay resident; the stage of q - 3 takes the next row
+    };
+    auto advance = [&]() {
+        if (++st == S) st = 0, ph ^= 1u;
+        ++gpos;
+    };
+    auto back = [&](int a) { return st - a < 0 ? st - a + S : st - a; };
+    // after a failure a warp arrives on no barrier and sends nothing: no phase can be overrun
+    auto release = [&](int stage) {
         __syncwarp();
-        if (lane == 0 && issued < n_sw_l && issued < q + S - 2) issue();
-    }
-    if (!failed) flush();
-
-    if (!failed && active) {
-        // this work item's weight-gradient partial row: the taps (by tap index) and the bias from the
-        // first sweep, the norm weight from the second
-        const int d = p.d, width = p.width;
-        float *prow = p.partial + static_cast<size_t>(k * dil + r) * (width + 2) * d;
+        if (lane == 0 && !failed) mbar_arrive(&empty[stage]);
+    };
+    // a token `a` positions back has its du: its y, row-dot part and norm-weight gradient
+    auto complete = [&](int a, const float (&du)[kScEV]) {
+        const int sa = back(a);
+        const uint8_t *stg = ring + static_cast<size_t>(sa) * SB + tid * EV::kBytes;
+        float x[kScEV], g[kScEV];
+        EV::load_smem(stg, x);
+        EV::load_smem(stg + half, g);
+        const float ra = meta[sa].rstd;
+        float part = 0.f, y[kScEV];
 #pragma unroll
         for (int e = 0; e < kScEV; ++e) {
-            const int c = c0 + lane * kScEV + e;
-            if (MODE == kScBwdDot) {
-                for (int i = 0; i < width; ++i) prow[static_cast<size_t>(i) * d + c] = dK[width - 1 - i][e];
-                prow[static_cast<size_t>(width) * d + c] = db[e];
-            } else {
-                prow[static_cast<size_t>(width + 1) * d + c] = dnw[e];
+            const float dn = nw[e] * du[e];
+            part = fmaf(dn, x[e], part);
+            dnw[e] = fmaf(du[e] * x[e], ra, dnw[e]);
+            y[e] = fmaf(ra, dn, g[e]);
+        }
+        const int slot = ((nb & 1) * kBwBatch + nfin) * kBwCons + tid;
+        pbuf[slot] = active ? part : 0.f;
+        ybuf[slot] = make_float4(y[0], y[1], y[2], y[3]);
+        if (tid == 0) fin_stage[(nb & 3) * kBwBatch + nfin] = sa;
+        ++nfin;
+    };
+    // batch bf's dv rows once the cluster's row dots have arrived; its stages go back to the producer
+    auto finalize = [&](int bf, int n) {
+        wait_warp(&boxbar[bf & 3], (bf >> 2) & 1);
+        const float *bx = box + (bf & 3) * kBwMaxCluster * kBwBatch;
+        const size_t row_bytes = static_cast<size_t>(d) * sizeof(E);
+        uint8_t *dv_col = p.dv + static_cast<size_t>(c0) * sizeof(E) + tid * EV::kBytes;
+        for (int j = 0; j < n; ++j) {
+            float s = 0.f;
+            for (int k = 0; k < static_cast<int>(C); ++k) s += bx[k * kBwBatch + j];
+            const int sj = fin_stage[(bf & 3) * kBwBatch + j];
+            const float r = meta[sj].rstd;
+            const float kk = r * r * r * s * inv_d;
+            float x[kScEV];
+            EV::load_smem(ring + static_cast<size_t>(sj) * SB + tid * EV::kBytes, x);
+            const float4 y = ybuf[((bf & 1) * kBwBatch + j) * kBwCons + tid];
+            float o[kScEV] = {fmaf(-kk, x[0], y.x), fmaf(-kk, x[1], y.y), fmaf(-kk, x[2], y.z),
+                              fmaf(-kk, x[3], y.w)};
+            if (active) EV::store(dv_col + static_cast<size_t>(meta[sj].tok) * row_bytes, o);
+        }
+        __syncwarp();
+        if (lane == 0 && !failed)
+            for (int j = 0; j < n; ++j) mbar_arrive(&empty[fin_stage[(bf & 3) * kBwBatch + j]]);
+    };
+    // the open batch is complete: this warp's part is announced; the batch's reducer warp sums the
+    // CTA's row dots (thread order, then lanes) and sends them to the cluster; then the previous
+    // batch, whose sums have had a batch's time to arrive, is finished
+    auto post = [&]() {
+        const int b = nb;
+        __syncwarp();
+        if (lane == 0 && !failed) mbar_arrive(&lbar[b & 1]);
+        if (warp == (b & 7) && !failed) {
+            wait_warp(&lbar[b & 1], (b >> 1) & 1);
+            const float *pb = pbuf + (b & 1) * kBwBatch * kBwCons;
+            const uint32_t box_lo = smem_addr(box), bar_lo = smem_addr(boxbar);
+            for (int j = 0; j < nfin; ++j) {
+                const float4 u0 = *reinterpret_cast<const float4 *>(pb + j * kBwCons + lane * 8);
+                const float4 u1 = *reinterpret_cast<const float4 *>(pb + j * kBwCons + lane * 8 + 4);
+                float v = ((((((u0.x + u0.y) + u0.z) + u0.w) + u1.x) + u1.y) + u1.z) + u1.w;
+                v = warp_sum(v);
+                const int slot = ((b & 3) * kBwMaxCluster + static_cast<int>(rank)) * kBwBatch + j;
+                if (lane == 0) box[slot] = v;
+                if (lane < static_cast<int>(C) && lane != static_cast<int>(rank) && !failed)
+                    sc_st_async(sc_mapa(box_lo + slot * 4, lane), v, sc_mapa(bar_lo + (b & 3) * 8, lane));
+            }
+            __syncwarp();
+            if (lane == 0 && !failed) mbar_arrive_expect_tx(&boxbar[b & 3], (C - 1) * nfin * 4);
+        }
+        if (prev_n > 0) finalize(b - 1, prev_n);
+        prev_n = nfin;
+        nfin = 0;
+        ++nb;
+    };
+    // one sweep position in slot J.  STEADY: a chunk token with three chunk tokens pending before it,
+    // so the one three back completes; otherwise `kind` and the pending flags decide.
+    auto step = [&](auto Jc, auto Sc, uint32_t kind) {
+        constexpr int J = decltype(Jc)::v;
+        constexpr bool STEADY = decltype(Sc)::v != 0;
+        wait_warp(&full[st], ph);
+        const uint8_t *stg = ring + static_cast<size_t>(st) * SB + tid * EV::kBytes;
+        const float rt = meta[st].rstd;
+        float x[kScEV];
+        EV::load_smem(stg, x);
+#pragma unroll
+        for (int e = 0; e < kScEV; ++e) U[J][e] = x[e] * rt * nw[e];
+        if (!STEADY && kind == kScLead) {
+            release(st);
+            advance();
+            return;
+        }
+        float g[kScEV], dc[kScEV];
+        EV::load_smem(stg + half, g);
+#pragma unroll
+        for (int e = 0; e < kScEV; ++e) {
+            const float c = fmaf(w[3][e], U[(J + 1) & 3][e],
+                                 fmaf(w[2][e], U[(J + 2) & 3][e],
+                                      fmaf(w[1][e], U[(J + 3) & 3][e], fmaf(w[0][e], U[J][e], bias[e]))));
+            const float sg = sc_sigmoid_fast(c);
+            // SiLU'(c) = sg (1 + c (1 - sg))
+            dc[e] = g[e] * fmaf(sg, fmaf(-c, sg, c), sg);
+        }
+        if (STEADY || kind == kScMain) {
+#pragma unroll
+            for (int e = 0; e < kScEV; ++e) {
+                db[e] += dc[e];
+                A[0][e] = fmaf(dc[e], U[J][e], A[0][e]);
+                A[1][e] = fmaf(dc[e], U[(J + 3) & 3][e], A[1][e]);
+                A[2][e] = fmaf(dc[e], U[(J + 2) & 3][e], A[2][e]);
+                A[3][e] = fmaf(dc[e], U[(J + 1) & 3][e], A[3][e]);
             }
         }
-    }
-    // copies issued but never consumed (the backward stops its look-ahead at a sequence end)
-    if (lane == 0)
-        for (int64_t qq = q; qq < issued; ++qq)
-            if (!mbar_wait(&full[qq % S], static_cast<uint32_t>((qq / S) & 1)))
-                report(p.status, nullptr, ENGRAM_DEVERR_TIMEOUT);
-}
+        if (STEADY || pend3) {
+            float du[kScEV];
+#pragma unroll
+            for (int e = 0; e < kScEV; ++e) du[e] = fmaf(w[3][e], dc[e], P3[e]);
+            complete(3, du);
+        }
+#pragma unroll
+        for (int e = 0; e < kScEV; ++e) {
+            P3[e] = fmaf(w[2][e], dc[e], P2[e]);
+            P2[e] = fmaf(w[1][e], dc[e], P1[e]);
+            P1[e] = w[0][e] * dc[e];
+        }
+        if (!STEADY) {
+            pend3 = pend2, pend2 = pend1, pend1 = kind == kScMain;
+            if (kind == kScTail) release(st);
+        }
+        advance();
+    };
 
-// The row-dot total of each token, its nb channel-block partials in ascending order, written to
-// the row's first entry (which the final sweep reads).
-__global__ void __launch_bounds__(256) conv_dot_total_kernel(float *__restrict__ token_dot, int64_t T, int32_t nb) {
-    for (int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; t < T;
-         t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        float *row = token_dot + static_cast<size_t>(t) * nb;
-        float s = 0.f;
-        for (int b = 0; b < nb; ++b) s += row[b];
-        row[0] = s;
+    // a work item's weight-gradient partial row: the taps (by tap index), the bias, the norm weight
+    const int64_t ncl = sc_num_clusters();
+    auto write_rows = [&](int64_t item, bool zero) {
+        if (!active) return;
+        float *prow = p.partial + static_cast<size_t>(item) * (width + 2) * d + c0 + tid * kScEV;
+#pragma unroll
+        for (int a = 0; a < kScAges; ++a)
+            if (a < width)
+                *reinterpret_cast<float4 *>(prow + static_cast<size_t>(width - 1 - a) * d) =
+                    zero ? make_float4(0.f, 0.f, 0.f, 0.f) : make_float4(A[a][0], A[a][1], A[a][2], A[a][3]);
+        *reinterpret_cast<float4 *>(prow + static_cast<size_t>(width) * d) =
+            zero ? make_float4(0.f, 0.f, 0.f, 0.f) : make_float4(db[0], db[1], db[2], db[3]);
+        *reinterpret_cast<float4 *>(prow + static_cast<size_t>(width + 1) * d) =
+            zero ? make_float4(0.f, 0.f, 0.f, 0.f) : make_float4(dnw[0], dnw[1], dnw[2], dnw[3]);
+    };
+    // rows of the item just finished (if any) and zeros for this cluster's items without tokens up to `next`
+    int64_t cur_item = -1;
+    auto finish_items = [&](int64_t next) {
+        int64_t it = sc_cluster_id();
+        if (cur_item >= 0) {
+            write_rows(cur_item, false);
+            it = cur_item + ncl;
+        }
+        for (; it < next; it += ncl) write_rows(it, true);
+#pragma unroll
+        for (int e = 0; e < kScEV; ++e) {
+            db[e] = dnw[e] = 0.f;
+#pragma unroll
+            for (int a = 0; a < kScAges; ++a) A[a][e] = 0.f;
+        }
+    };
+    finish_items(-1);  // clears the accumulators
+
+    for (;;) {
+        if (warp == 0) {  // the copies: every free stage, and at least the next four positions
+            if (lane == 0) produce(gpos + 3);
+            failed = __any_sync(0xffffffffu, failed);
+        }
+        wait_warp(&full[st], ph);
+        if (failed) break;
+        const uint32_t fl = meta[st].flags;
+        if (fl & kFlDone) break;
+        if (fl & kFlItemStart) {
+            const int64_t item = static_cast<int64_t>(fl >> kFlItemShift);
+            finish_items(item);
+            cur_item = item;
+        }
+        if (fl & kFlSegStart) {
+#pragma unroll
+            for (int e = 0; e < kScEV; ++e) {
+                U[0][e] = U[1][e] = U[2][e] = U[3][e] = 0.f;
+                P1[e] = P2[e] = P3[e] = 0.f;
+            }
+            pend1 = pend2 = pend3 = false;
+        }
+        if (fl & kFlGroup) {
+            if (nfin > 0) post();  // a steady group fills one batch of its own
+            step(ScIdx<0>{}, ScIdx<1>{}, kScMain);
+            step(ScIdx<1>{}, ScIdx<1>{}, kScMain);
+            step(ScIdx<2>{}, ScIdx<1>{}, kScMain);
+            step(ScIdx<3>{}, ScIdx<1>{}, kScMain);
+            pend1 = pend2 = pend3 = true;
+        } else {
+            const uint32_t kind = fl & kFlKind;
+            switch ((fl >> kFlSlotShift) & 3u) {
+                case 0: step(ScIdx<0>{}, ScIdx<0>{}, kind); break;
+                case 1: step(ScIdx<1>{}, ScIdx<0>{}, kind); break;
+                case 2: step(ScIdx<2>{}, ScIdx<0>{}, kind); break;
+                default: step(ScIdx<3>{}, ScIdx<0>{}, kind); break;
+            }
+        }
+        if (nfin == kBwBatch) post();
+        if (fl & kFlSegEnd) {
+            // the sequence (or the look-ahead) ends: the pending du have all their terms
+            if (pend3) {
+                complete(3, P3);
+                if (nfin == kBwBatch) post();
+            }
+            if (pend2) {
+                complete(2, P2);
+                if (nfin == kBwBatch) post();
+            }
+            if (pend1) complete(1, P1);
+            if (nfin > 0) post();
+            if (prev_n > 0) finalize(nb - 1, prev_n);
+            prev_n = 0;
+            pend1 = pend2 = pend3 = false;
+        }
     }
+    if (!failed) finish_items(p.nitems);
+    // after a failure, copies may still be landing: wait for them (bounded) before the CTA leaves
+    if (tid == 0 && failed) {
+        const uint32_t issued = prod->issued;
+        for (uint32_t q = issued > static_cast<uint32_t>(S) ? issued - S : 0; q < issued; ++q)
+            mbar_wait(&full[q % S], (q / S) & 1u, kWaitLimitNs / 16);
+    }
+    sc_cluster_sync();  // no CTA leaves while a peer may still write into its shared memory
 }
 
 // ------------------------------------------------------------------------------- weight-gradient reduction
@@ -702,7 +959,7 @@ engram_status sc_check(const char *fn, engram_dtype dtype, int64_t T, int32_t d,
     if (dil < 1) return fail(ENGRAM_ERR_SHAPE, "%s: dilation = %d", fn, dil);
     if ((static_cast<int64_t>(d) * dtype_size(dtype)) % 16 != 0)
         return fail(ENGRAM_ERR_ALIGN, "%s: a row of d = %d elements is not a multiple of 16 bytes", fn, d);
-    if (d > kScMaxBlocks * kScCols) return fail(ENGRAM_ERR_SHAPE, "%s: d = %d exceeds %d", fn, d, kScMaxBlocks * kScCols);
+    if (d > kBwMaxCluster * kBwCW) return fail(ENGRAM_ERR_SHAPE, "%s: d = %d exceeds %d", fn, d, kBwMaxCluster * kBwCW);
     return ENGRAM_OK;
 }
 
@@ -717,44 +974,54 @@ engram_status sc_ptrs(const char *fn, const void *const *ptrs, int n, int n_alig
     return ENGRAM_OK;
 }
 
-template <typename E, int MODE>
-engram_status sc_launch(const char *fn, ScParams prm, cudaStream_t s) {
-    prm.stages = kScRingBytes / (2 * kScCols * static_cast<int>(sizeof(E)));
-    const int smem = kScWarps * kScRingBytes + kScWarps * prm.stages * 8;
-    engram_status st = set_smem(reinterpret_cast<const void *>(conv_stencil_kernel<E, MODE>), smem);
+// Clusters of ceil(d / 1024) CTAs, as many as fit at once (at most one per work item), each
+// walking the work items cluster_id, cluster_id + clusters, ...
+constexpr int kScDevices = 64;
+
+template <typename E>
+engram_status sc_bwd_launch(const char *fn, ScBwdParams prm, const DeviceInfo &dev, cudaStream_t s) {
+    const int C = (prm.d + kBwCW - 1) / kBwCW;
+    const int smem = sc_bwd_smem(kBwStages, sc_bwd_stage_bytes<E>());
+    void (*kern)(ScBwdParams) = conv_bwd_kernel<E>;
+    engram_status st = set_smem(reinterpret_cast<const void *>(kern), smem);
     if (st != ENGRAM_OK) return st;
-    const int64_t items = prm.nchunks * prm.dil * prm.nb;
-    const int64_t grid = (items + kScWarps - 1) / kScWarps;
-    if (grid > 0x7fffffff) return fail(ENGRAM_ERR_SHAPE, "%s: too many work items", fn);
-    conv_stencil_kernel<E, MODE><<<static_cast<unsigned>(grid), kScWarps * 32, smem, s>>>(prm);
+    // two CTAs per SM: the largest shared-memory carveout
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared) !=
+        cudaSuccess)
+        return check_launch(fn);
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(C);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(C));
+    cfg.blockDim = dim3(kBwThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // clusters resident at once, per (device, element size, cluster size)
+    static std::atomic<int> cached[kScDevices][2][kBwMaxCluster + 1];
+    std::atomic<int> &slot = cached[dev.device % kScDevices][sizeof(E) == 4 ? 1 : 0][C];
+    int maxcl = slot.load(std::memory_order_relaxed);
+    if (maxcl <= 0) {
+        cudaError_t e = cudaOccupancyMaxActiveClusters(&maxcl, kern, &cfg);
+        if (e != cudaSuccess || maxcl < 1) {
+            cudaGetLastError();
+            return fail(ENGRAM_ERR_CUDA, "%s: no cluster of %d CTAs with %d bytes of shared memory fits (%s)", fn, C,
+                        smem, cudaGetErrorString(e));
+        }
+        slot.store(maxcl, std::memory_order_relaxed);
+    }
+    int64_t ncl = std::min<int64_t>(prm.nitems, maxcl);
+    ncl = std::max<int64_t>(1, cap_grid(ncl * C) / C);
+    cfg.gridDim = dim3(static_cast<unsigned>(ncl * C));
+    cfg.numAttrs = pdl_enabled() ? 2 : 1;
+    cudaLaunchKernelEx(&cfg, kern, prm);
     return check_launch(fn);
-}
-
-template <int MODE>
-engram_status sc_dispatch(const char *fn, engram_dtype dtype, const ScParams &prm, cudaStream_t s) {
-    return dtype == ENGRAM_F32 ? sc_launch<float, MODE>(fn, prm, s) : sc_launch<__nv_bfloat16, MODE>(fn, prm, s);
-}
-
-ScParams sc_params(const void *v, const float *norm_w, const float *conv_w, const float *bias, const float *rstd,
-                   const int64_t *offs, int32_t num_seqs, int64_t T, int32_t d, int32_t width, int32_t dil,
-                   const DeviceInfo &dev) {
-    ScParams prm{};
-    prm.v = static_cast<const uint8_t *>(v);
-    prm.norm_w = norm_w;
-    prm.conv_w = conv_w;
-    prm.bias = bias;
-    prm.rstd = rstd;
-    prm.offs = offs;
-    prm.status = dev.status_word;
-    prm.T = T;
-    prm.chunk = sc_chunk(T);
-    prm.nchunks = (T + prm.chunk - 1) / prm.chunk;
-    prm.num_seqs = num_seqs;
-    prm.d = d;
-    prm.width = width;
-    prm.dil = dil;
-    prm.nb = (d + kScCols - 1) / kScCols;
-    return prm;
 }
 
 }  // namespace
@@ -770,13 +1037,6 @@ extern "C" engram_status engram_short_conv_num_partials(int64_t T, int32_t dilat
     const int64_t p = ((T + chunk - 1) / chunk) * dilation;
     if (p > 0x7fffffff) return fail(ENGRAM_ERR_SHAPE, "engram_short_conv_num_partials: too many partials");
     *P = static_cast<int32_t>(p);
-    return ENGRAM_OK;
-}
-
-extern "C" engram_status engram_short_conv_dot_blocks(int32_t d, int32_t *nb) {
-    if (!nb) return fail(ENGRAM_ERR_NULL, "engram_short_conv_dot_blocks: NULL nb");
-    if (d <= 0) return fail(ENGRAM_ERR_SHAPE, "engram_short_conv_dot_blocks: d = %d", d);
-    *nb = (d + kScCols - 1) / kScCols;
     return ENGRAM_OK;
 }
 
@@ -846,8 +1106,7 @@ extern "C" engram_status engram_short_conv_bwd(const void *dout, const void *v, 
                                                const float *norm_w, const float *conv_w, const float *bias,
                                                const float *rstd, const int64_t *seq_offsets, int32_t num_seqs,
                                                int64_t T, int32_t d, int32_t width, int32_t dilation, void *dv,
-                                               float *token_dot, float *dw_partial, int32_t P,
-                                               engram_stream_t stream) {
+                                               float *dw_partial, int32_t P, engram_stream_t stream) {
     const char *fn = "engram_short_conv_bwd";
     engram_status st = sc_check(fn, dtype, T, d, width, dilation, num_seqs);
     if (st != ENGRAM_OK) return st;
@@ -856,25 +1115,32 @@ extern "C" engram_status engram_short_conv_bwd(const void *dout, const void *v, 
     if (P != want) return fail(ENGRAM_ERR_SHAPE, "%s: P = %d, engram_short_conv_num_partials gives %d", fn, P, want);
     if (!norm_w || !conv_w || !seq_offsets) return fail(ENGRAM_ERR_NULL, "%s: NULL pointer", fn);
     if (T == 0) return ENGRAM_OK;
-    if (!dout || !v || !rstd || !dv || !token_dot || !dw_partial) return fail(ENGRAM_ERR_NULL, "%s: NULL pointer", fn);
+    if (!dout || !v || !rstd || !dv || !dw_partial) return fail(ENGRAM_ERR_NULL, "%s: NULL pointer", fn);
     if (dv == v || dv == dout) return fail(ENGRAM_ERR_SHAPE, "%s: dv may not alias V~ or dout", fn);
-    const void *ptrs[] = {dout, v, dv, norm_w, conv_w, bias, rstd, seq_offsets, token_dot, dw_partial};
+    const void *ptrs[] = {dout, v, dv, dw_partial, norm_w, conv_w, bias, rstd, seq_offsets};
     DeviceInfo dev;
-    if ((st = sc_ptrs(fn, ptrs, 10, 3, &dev)) != ENGRAM_OK) return st;
+    if ((st = sc_ptrs(fn, ptrs, 9, 4, &dev)) != ENGRAM_OK) return st;
+    ScBwdParams prm{};
+    prm.v = static_cast<const uint8_t *>(v);
+    prm.dout = static_cast<const uint8_t *>(dout);
+    prm.norm_w = norm_w;
+    prm.conv_w = conv_w;
+    prm.bias = bias;
+    prm.rstd = rstd;
+    prm.offs = seq_offsets;
+    prm.dv = static_cast<uint8_t *>(dv);
+    prm.partial = dw_partial;
+    prm.status = dev.status_word;
+    prm.T = T;
+    prm.chunk = sc_chunk(T);
+    prm.nitems = static_cast<int64_t>(P);
+    if (prm.nitems > kBwMaxItems) return fail(ENGRAM_ERR_SHAPE, "%s: %d work items exceed %lld", fn, P, (long long)kBwMaxItems);
+    prm.num_seqs = num_seqs;
+    prm.d = d;
+    prm.width = width;
+    prm.dil = dilation;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    ScParams prm = sc_params(v, norm_w, conv_w, bias, rstd, seq_offsets, num_seqs, T, d, width, dilation, dev);
-    prm.x2 = static_cast<const uint8_t *>(dout);
-    prm.token_dot_out = token_dot;
-    prm.partial = dw_partial;
-    if ((st = sc_dispatch<kScBwdDot>(fn, dtype, prm, s)) != ENGRAM_OK) return st;
-    conv_dot_total_kernel<<<static_cast<unsigned>(std::min<int64_t>((T + 255) / 256, 4096)), 256, 0, s>>>(
-        token_dot, T, prm.nb);
-    if ((st = check_launch(fn)) != ENGRAM_OK) return st;
-    prm.token_dot = token_dot;
-    prm.token_dot_out = nullptr;
-    prm.out = static_cast<uint8_t *>(dv);
-    prm.partial = dw_partial;
-    return sc_dispatch<kScBwdFinal>(fn, dtype, prm, s);
+    return dtype == ENGRAM_F32 ? sc_bwd_launch<float>(fn, prm, dev, s) : sc_bwd_launch<__nv_bfloat16>(fn, prm, dev, s);
 }
 
 extern "C" engram_status engram_short_conv_grad_reduce(const float *dw_partial, int32_t P, int32_t width, int32_t d,

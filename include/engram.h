@@ -358,26 +358,26 @@ engram_status engram_short_conv_fwd(const void *v, const void *h, engram_dtype d
  */
 engram_status engram_short_conv_num_partials(int64_t T, int32_t dilation, int32_t *P);
 
-/* Channel blocks nb = ceil(d / 128): engram_short_conv_bwd's token_dot workspace is [T, nb] fp32. */
-engram_status engram_short_conv_dot_blocks(int32_t d, int32_t *nb);
-
 /*
  * Backward of engram_short_conv_fwd given dout = dL/dout [T, d] and its saved rstd; dL/dh = dout
  * (not written).  With dc = dout * SiLU'(conv) and, within each sequence,
  *     du[t, c] = sum_i conv_w[c, i] * dc[t + (width - 1 - i) * dilation, c],
- *     s[t]     = sum_c norm_w[c] du[t, c] V~[t, c]   (128-channel blocks in ascending order),
+ *     s[t]     = sum_c norm_w[c] du[t, c] V~[t, c],
  *     dv[t, c] = dout[t, c] + rstd norm_w[c] du[t, c] - rstd^3 V~[t, c] s[t] / d,
- * dv [T, d] in `dtype` (not aliasing v or dout), token_dot [T, nb] fp32 workspace, and
- * dw_partial [P, width + 2, d] fp32 with P = engram_short_conv_num_partials(T, dilation): row
- * (chunk, class) holds, over that work item's tokens, sum dc * u_tap for each tap i (rows
- * 0..width-1), sum dc (row width) and sum du * V~ * rstd (row width + 1), each token's terms in
- * ascending time order.  Reduce it with engram_short_conv_grad_reduce.
+ * dv [T, d] in `dtype` (not aliasing v or dout) and dw_partial [P, width + 2, d] fp32 with
+ * P = engram_short_conv_num_partials(T, dilation): row (chunk, class) holds, over that work item's
+ * tokens, sum dc * u_tap for each tap i (rows 0..width-1), sum dc (row width) and
+ * sum du * V~ * rstd (row width + 1), each token's terms in ascending time order.  Reduce it with
+ * engram_short_conv_grad_reduce.  s sums, in this order: four channels, eight such groups, a
+ * 32-lane butterfly (one 1024-channel block), then the ceil(d / 1024) blocks in ascending order.
+ * One pass over dout and V~ on thread-block clusters of ceil(d / 1024) CTAs; dout, v, dv and
+ * dw_partial 16-byte aligned.
  */
 engram_status engram_short_conv_bwd(const void *dout, const void *v, engram_dtype dtype, const float *norm_w,
                                     const float *conv_w, const float *bias, const float *rstd,
                                     const int64_t *seq_offsets, int32_t num_seqs, int64_t T, int32_t d,
-                                    int32_t width, int32_t dilation, void *dv, float *token_dot, float *dw_partial,
-                                    int32_t P, engram_stream_t stream);
+                                    int32_t width, int32_t dilation, void *dv, float *dw_partial, int32_t P,
+                                    engram_stream_t stream);
 
 /*
  * dconv_w [d, width], dbias [d] (nullable) and dnorm_w [d] = the sums of the P partial rows of
