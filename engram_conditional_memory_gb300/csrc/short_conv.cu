@@ -42,12 +42,10 @@ struct Ev4;
 template <>
 struct Ev4<float> {
     static constexpr int kBytes = 16;
+    // a plain shared-memory load (the waits before it order it; the compiler may schedule it freely)
     __device__ __forceinline__ static void load_smem(const uint8_t *p, float (&x)[4]) {
-        uint4 u;
-        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(u.x), "=r"(u.y), "=r"(u.z), "=r"(u.w)
-                     : "r"(smem_addr(p)));
-        x[0] = __uint_as_float(u.x), x[1] = __uint_as_float(u.y), x[2] = __uint_as_float(u.z),
-        x[3] = __uint_as_float(u.w);
+        const float4 u = *reinterpret_cast<const float4 *>(p);
+        x[0] = u.x, x[1] = u.y, x[2] = u.z, x[3] = u.w;
     }
     __device__ __forceinline__ static void store(uint8_t *p, const float (&x)[4]) {
         *reinterpret_cast<float4 *>(p) = make_float4(x[0], x[1], x[2], x[3]);
@@ -58,10 +56,9 @@ template <>
 struct Ev4<__nv_bfloat16> {
     static constexpr int kBytes = 8;
     __device__ __forceinline__ static void load_smem(const uint8_t *p, float (&x)[4]) {
-        uint32_t a, b;
-        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(a), "=r"(b) : "r"(smem_addr(p)));
-        x[0] = __uint_as_float(a << 16), x[1] = __uint_as_float(a & 0xffff0000u);
-        x[2] = __uint_as_float(b << 16), x[3] = __uint_as_float(b & 0xffff0000u);
+        const uint2 u = *reinterpret_cast<const uint2 *>(p);
+        x[0] = __uint_as_float(u.x << 16), x[1] = __uint_as_float(u.x & 0xffff0000u);
+        x[2] = __uint_as_float(u.y << 16), x[3] = __uint_as_float(u.y & 0xffff0000u);
     }
     __device__ __forceinline__ static void store(uint8_t *p, const float (&x)[4]) {
         *reinterpret_cast<uint2 *>(p) =
@@ -310,13 +307,14 @@ __global__ void __launch_bounds__(256, 2) conv_fwd_kernel(const __grid_constant_
 
 // ------------------------------------------------------------------------------- backward
 
-constexpr int kBwCons = 256;                      // threads (8 warps), four channels each
-constexpr int kBwThreads = kBwCons;
+constexpr int kBwWarps = 4;                       // consumer warps, four channels per thread
+constexpr int kBwCons = kBwWarps * 32;
+constexpr int kBwThreads = kBwCons + 32;          // + the copy producer's warp
 constexpr int kBwCW = kBwCons * kScEV;            // channels per CTA
-constexpr int kBwMaxCluster = 8;                  // CTAs per cluster: d <= 8 * 1024
+constexpr int kBwMaxCluster = 16;                 // CTAs per cluster: d <= 16 * 512
 constexpr int kBwLag = kScAges - 1;               // taps behind a token and readers after it
 constexpr int kBwBatch = 4;                       // tokens whose row dots are exchanged together
-constexpr int kBwPrefetch = 5;                    // stages the copies may run ahead
+constexpr int kBwPrefetch = 13;                   // stages the copies may run ahead
 constexpr int kBwStages = 2 * kBwBatch + kBwLag + kBwPrefetch;  // two batches in flight
 enum ScKind { kScLead = 0, kScMain = 1, kScTail = 2 };
 
@@ -494,7 +492,7 @@ static_assert(sizeof(ScProd) <= 128, "the producer state fits its shared-memory 
 // adds them in rank order and writes dv = y - rstd^3 V~ s / d.  All waits are bounded.
 // The chunks depend on T only and every sum has a fixed order, so results are bitwise reproducible.
 template <typename E>
-__global__ void __launch_bounds__(kBwThreads, 2) conv_bwd_kernel(const __grid_constant__ ScBwdParams p) {
+__global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_constant__ ScBwdParams p) {
     using EV = Ev4<E>;
     extern __shared__ __align__(128) uint8_t smem[];
     constexpr int S = kBwStages;
@@ -552,359 +550,406 @@ __global__ void __launch_bounds__(kBwThreads, 2) conv_bwd_kernel(const __grid_co
             P.s = sc_seq_of(p.offs, p.num_seqs, t_lo);
         }
     };
-    // thread 0: issue every position whose stage is free; wait (bounded) until position `need` is
-    // issued, unless the stream ends first
-    auto produce = [&](uint32_t need) {
-        if (failed) return;
+    // the producer warp: every position of the cluster's items in order, one position per lane as
+    // stages free up, then the sentinel.  The state is kept in registers (the copies' asm
+    // statements order shared memory, so shared fields would be reloaded around each of them).
+    auto produce_all = [&]() {
         ScProd &P = *prod;
         const uint32_t seg = static_cast<uint32_t>(ncols) * sizeof(E);
         const size_t row_bytes = static_cast<size_t>(p.d) * sizeof(E);
-        const size_t col_off = static_cast<size_t>(c0) * sizeof(E);
-        while (P.state != 2) {
-            const int st = P.st;
-            if (P.round > 0) {
-                const uint32_t par = (P.round + 1) & 1u;
-                if (static_cast<int32_t>(P.issued - need) > 0) {
-                    if (!mbar_test_wait(&empty[st], par)) break;
-                } else if (!mbar_wait(&empty[st], par)) {
-                    report(p.status, nullptr, ENGRAM_DEVERR_TIMEOUT);
+        const uint8_t *src_v = p.v + static_cast<size_t>(c0) * sizeof(E);
+        const uint8_t *src_g = p.dout + static_cast<size_t>(c0) * sizeof(E);
+        int st = P.st, state = P.state;
+        uint32_t round = P.round, issued = P.issued;
+        int q = P.q, n = P.n, nl = P.n_lead, nm = P.n_main, new_item = P.new_item;
+        uint32_t item_fl = static_cast<uint32_t>(P.item) << kFlItemShift;
+        int64_t t = P.t;
+        while (state != 2) {
+            // the free stages from st on: lane l tests the one of position issued + l
+            const int stl = st + lane < S ? st + lane : st + lane - S;
+            const uint32_t rl = round + (st + lane < S ? 0u : 1u);
+            const bool free_l = lane < S && (rl == 0 || mbar_test_wait(&empty[stl], (rl + 1) & 1u));
+            const uint32_t mask = __ballot_sync(0xffffffffu, free_l);
+            int cnt = __ffs(~mask) - 1;
+            if (cnt < 0) cnt = 32;
+            if (cnt == 0) {  // the ring is full: wait (bounded) for its oldest stage
+                bool ok = true;
+                if (lane == 0) ok = mbar_wait_sleep(&empty[st], (round + 1) & 1u);
+                if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                    if (lane == 0) report(p.status, nullptr, ENGRAM_DEVERR_TIMEOUT);
                     failed = true;
-                    P.state = 2;
                     break;
                 }
+                continue;
             }
-            if (P.state == 1) {  // the sentinel: no copies, both arrivals
-                meta[st].tok = 0;
-                meta[st].flags = kFlDone;
-                mbar_arrive(&full[st]);
-                mbar_arrive(&full[st]);
-                P.state = 2;
+            if (state == 1) {  // the sentinel: no copies, both arrivals
+                if (lane == 0) {
+                    meta[st].tok = 0;
+                    meta[st].flags = kFlDone;
+                    mbar_arrive(&full[st]);
+                    mbar_arrive(&full[st]);
+                }
+                state = 2;
+                cnt = 1;
             } else {
-                const int q = P.q, n = P.n, nl = P.n_lead, nm = P.n_main;
-                const uint32_t kind = q < nl ? kScLead : (q < nl + nm ? kScMain : kScTail);
-                const bool group = (q & 3) == 0 && q >= nl + kBwLag && q + 4 <= nl + nm && q + 4 < n;
-                uint32_t fl = kind | (static_cast<uint32_t>(q & 3) << kFlSlotShift);
-                if (q == 0) fl |= kFlSegStart;
-                if (q == n - 1) fl |= kFlSegEnd;
-                if (group) fl |= kFlGroup;
-                if (P.new_item) fl |= kFlItemStart | (static_cast<uint32_t>(P.item) << kFlItemShift);
-                const int64_t t = P.t;
-                meta[st].tok = t;
-                meta[st].flags = fl;
-                uint8_t *dst = ring + static_cast<size_t>(st) * SB;
-                sc_cp_async4(&meta[st].rstd, p.rstd + t);
-                sc_cp_async_arrive(&full[st]);
-                mbar_arrive_expect_tx(&full[st], kind == kScLead ? seg : 2 * seg);
-                bulk_load_plain(dst, p.v + static_cast<size_t>(t) * row_bytes + col_off, seg, &full[st]);
-                if (kind != kScLead)
-                    bulk_load(dst + half, p.dout + static_cast<size_t>(t) * row_bytes + col_off, seg, &full[st],
-                              l2_evict_first_policy());
-                P.new_item = 0;
-                if (q + 1 == n) prod_next_seg();
-                else P.q = q + 1, P.t = t + dil;
+                if (cnt > n - q) cnt = n - q;
+                if (lane < cnt) {
+                    const int ql = q + lane;
+                    const int64_t tl = t + lane * dil;
+                    const uint32_t kind = ql < nl ? kScLead : (ql < nl + nm ? kScMain : kScTail);
+                    const bool group = (ql & 3) == 0 && ql >= nl + kBwLag && ql + 4 <= nl + nm && ql + 4 < n;
+                    uint32_t fl = kind | (static_cast<uint32_t>(ql & 3) << kFlSlotShift);
+                    if (ql == 0) fl |= kFlSegStart;
+                    if (ql == n - 1) fl |= kFlSegEnd;
+                    if (group) fl |= kFlGroup;
+                    if (new_item && lane == 0) fl |= kFlItemStart | item_fl;
+                    meta[stl].tok = tl;
+                    meta[stl].flags = fl;
+                    uint8_t *dst = ring + static_cast<size_t>(stl) * SB;
+                    sc_cp_async4(&meta[stl].rstd, p.rstd + tl);
+                    sc_cp_async_arrive(&full[stl]);
+                    mbar_arrive_expect_tx(&full[stl], kind == kScLead ? seg : 2 * seg);
+                    bulk_load_plain(dst, src_v + static_cast<size_t>(tl) * row_bytes, seg, &full[stl]);
+                    if (kind != kScLead)
+                        bulk_load(dst + half, src_g + static_cast<size_t>(tl) * row_bytes, seg, &full[stl],
+                                  l2_evict_first_policy());
+                }
+                new_item = 0;
+                q += cnt;
+                t += cnt * dil;
+                if (q == n) {  // the segment ends: the next one (rare) through the shared state
+                    __syncwarp();
+                    if (lane == 0) {
+                        P.new_item = 0;
+                        prod_next_seg();
+                    }
+                    __syncwarp();
+                    state = P.state, q = P.q, n = P.n, nl = P.n_lead, nm = P.n_main, new_item = P.new_item;
+                    item_fl = static_cast<uint32_t>(P.item) << kFlItemShift;
+                    t = P.t;
+                }
             }
-            ++P.issued;
-            if (st + 1 == S) P.st = 0, ++P.round;
-            else P.st = st + 1;
+            issued += cnt;
+            st += cnt;
+            if (st >= S) st -= S, ++round;
         }
+        // after a failure, copies may still be landing: wait for them (bounded) before the CTA leaves
+        if (failed && lane == 0)
+            for (uint32_t q2 = issued > static_cast<uint32_t>(S) ? issued - S : 0; q2 < issued; ++q2)
+                mbar_wait_sleep(&full[q2 % S], (q2 / S) & 1u, kWaitLimitNs / 16);
+        __syncwarp();
     };
 
     if (tid == 0) {
         for (int i = 0; i < S; ++i) {
             mbar_init(&full[i], 2);  // the producer's arrival and its rstd copy's
-            mbar_init(&empty[i], kBwCons / 32);
+            mbar_init(&empty[i], kBwWarps);
         }
-        for (int i = 0; i < 2; ++i) mbar_init(&lbar[i], kBwCons / 32);
+        for (int i = 0; i < 2; ++i) mbar_init(&lbar[i], kBwWarps);
         for (int i = 0; i < 4; ++i) mbar_init(&boxbar[i], 1);
         mbar_init_fence();
     }
     sc_cluster_sync();  // every CTA's barriers exist before any remote arrival
     pdl_wait();
-    if (tid == 0) {
-        ScProd &P = *prod;
-        P = ScProd{};
-        P.item = sc_cluster_id();
-        if (P.item >= p.nitems) {
-            P.state = 1;
-        } else {
-            const int64_t t_lo = P.item / dil * p.chunk;
-            P.xs = t_lo;
-            P.t_hi = t_lo + p.chunk < p.T ? t_lo + p.chunk : p.T;
-            P.s = sc_seq_of(p.offs, p.num_seqs, t_lo);
-            P.new_item = 1;
-            prod_next_seg();
+    if (warp == kBwWarps) {
+        if (lane == 0) {
+            ScProd &P = *prod;
+            P = ScProd{};
+            P.item = sc_cluster_id();
+            if (P.item >= p.nitems) {
+                P.state = 1;
+            } else {
+                const int64_t t_lo = P.item / dil * p.chunk;
+                P.xs = t_lo;
+                P.t_hi = t_lo + p.chunk < p.T ? t_lo + p.chunk : p.T;
+                P.s = sc_seq_of(p.offs, p.num_seqs, t_lo);
+                P.new_item = 1;
+                prod_next_seg();
+            }
         }
-        produce(0);  // fill the ring
-    }
-    __syncthreads();
-
-    const bool active = tid * kScEV < ncols;
-    const int width = p.width, d = p.d;
-    float w[kScAges][kScEV], nw[kScEV], bias[kScEV];
-#pragma unroll
-    for (int e = 0; e < kScEV; ++e) {
-        const int c = c0 + tid * kScEV + e;
-        const bool ok = active && c < d;
-        nw[e] = ok ? __ldg(p.norm_w + c) : 0.f;
-        bias[e] = ok && p.bias ? __ldg(p.bias + c) : 0.f;
-#pragma unroll
-        for (int a = 0; a < kScAges; ++a)
-            w[a][e] = ok && a < width ? __ldg(p.conv_w + static_cast<size_t>(c) * width + (width - 1 - a)) : 0.f;
-    }
-    const float inv_d = 1.0f / static_cast<float>(d);
-
-    float U[4][kScEV];                      // u by slot: position q's in slot q & 3
-    float P1[kScEV], P2[kScEV], P3[kScEV];  // du collecting contributions, by age 1..3
-    float A[kScAges][kScEV], db[kScEV], dnw[kScEV];
-    bool pend1 = false, pend2 = false, pend3 = false;
-    int st = 0;
-    uint32_t ph = 0, gpos = 0;
-    int nfin = 0, nb = 0, prev_n = 0;  // tokens of the open batch, batches posted, tokens of the pending one
-
-    // a wait of the whole warp: every lane takes the same view of a failure
-    auto wait_warp = [&](uint64_t *bar, uint32_t parity) {
-        if (failed) return;
-        if (!__all_sync(0xffffffffu, mbar_wait(bar, parity))) {
-            if (lane == 0) report(p.status, nullptr, ENGRAM_DEVERR_TIMEOUT);
-            failed = true;
-        }
-    };
-    auto advance = [&]() {
-        if (++st == S) st = 0, ph ^= 1u;
-        ++gpos;
-    };
-    auto back = [&](int a) { return st - a < 0 ? st - a + S : st - a; };
-    // after a failure a warp arrives on no barrier and sends nothing: no phase can be overrun
-    auto release = [&](int stage) {
         __syncwarp();
-        if (lane == 0 && !failed) mbar_arrive(&empty[stage]);
-    };
-    // a token `a` positions back has its du: its y, row-dot part and norm-weight gradient
-    auto complete = [&](int a, const float (&du)[kScEV]) {
-        const int sa = back(a);
-        const uint8_t *stg = ring + static_cast<size_t>(sa) * SB + tid * EV::kBytes;
-        float x[kScEV], g[kScEV];
-        EV::load_smem(stg, x);
-        EV::load_smem(stg + half, g);
-        const float ra = meta[sa].rstd;
-        float part = 0.f, y[kScEV];
+        produce_all();
+    } else {
+
+        const bool active = tid * kScEV < ncols;
+        const int width = p.width, d = p.d;
+        float w[kScAges][kScEV], nw[kScEV], bias[kScEV];
 #pragma unroll
         for (int e = 0; e < kScEV; ++e) {
-            const float dn = nw[e] * du[e];
-            part = fmaf(dn, x[e], part);
-            dnw[e] = fmaf(du[e] * x[e], ra, dnw[e]);
-            y[e] = fmaf(ra, dn, g[e]);
+            const int c = c0 + tid * kScEV + e;
+            const bool ok = active && c < d;
+            nw[e] = ok ? __ldg(p.norm_w + c) : 0.f;
+            bias[e] = ok && p.bias ? __ldg(p.bias + c) : 0.f;
+#pragma unroll
+            for (int a = 0; a < kScAges; ++a)
+                w[a][e] = ok && a < width ? __ldg(p.conv_w + static_cast<size_t>(c) * width + (width - 1 - a)) : 0.f;
         }
-        const int slot = ((nb & 1) * kBwBatch + nfin) * kBwCons + tid;
-        pbuf[slot] = active ? part : 0.f;
-        ybuf[slot] = make_float4(y[0], y[1], y[2], y[3]);
-        if (tid == 0) fin_stage[(nb & 3) * kBwBatch + nfin] = sa;
-        ++nfin;
-    };
-    // batch bf's dv rows once the cluster's row dots have arrived; its stages go back to the producer
-    auto finalize = [&](int bf, int n) {
-        wait_warp(&boxbar[bf & 3], (bf >> 2) & 1);
-        const float *bx = box + (bf & 3) * kBwMaxCluster * kBwBatch;
-        const size_t row_bytes = static_cast<size_t>(d) * sizeof(E);
-        uint8_t *dv_col = p.dv + static_cast<size_t>(c0) * sizeof(E) + tid * EV::kBytes;
-        for (int j = 0; j < n; ++j) {
-            float s = 0.f;
-            for (int k = 0; k < static_cast<int>(C); ++k) s += bx[k * kBwBatch + j];
-            const int sj = fin_stage[(bf & 3) * kBwBatch + j];
-            const float r = meta[sj].rstd;
-            const float kk = r * r * r * s * inv_d;
-            float x[kScEV];
-            EV::load_smem(ring + static_cast<size_t>(sj) * SB + tid * EV::kBytes, x);
-            const float4 y = ybuf[((bf & 1) * kBwBatch + j) * kBwCons + tid];
-            float o[kScEV] = {fmaf(-kk, x[0], y.x), fmaf(-kk, x[1], y.y), fmaf(-kk, x[2], y.z),
-                              fmaf(-kk, x[3], y.w)};
-            if (active) EV::store(dv_col + static_cast<size_t>(meta[sj].tok) * row_bytes, o);
-        }
-        __syncwarp();
-        if (lane == 0 && !failed)
-            for (int j = 0; j < n; ++j) mbar_arrive(&empty[fin_stage[(bf & 3) * kBwBatch + j]]);
-    };
-    // the open batch is complete: this warp's part is announced; the batch's reducer warp sums the
-    // CTA's row dots (thread order, then lanes) and sends them to the cluster; then the previous
-    // batch, whose sums have had a batch's time to arrive, is finished
-    auto post = [&]() {
-        const int b = nb;
-        __syncwarp();
-        if (lane == 0 && !failed) mbar_arrive(&lbar[b & 1]);
-        if (warp == (b & 7) && !failed) {
-            wait_warp(&lbar[b & 1], (b >> 1) & 1);
-            const float *pb = pbuf + (b & 1) * kBwBatch * kBwCons;
-            const uint32_t box_lo = smem_addr(box), bar_lo = smem_addr(boxbar);
-            for (int j = 0; j < nfin; ++j) {
-                const float4 u0 = *reinterpret_cast<const float4 *>(pb + j * kBwCons + lane * 8);
-                const float4 u1 = *reinterpret_cast<const float4 *>(pb + j * kBwCons + lane * 8 + 4);
-                float v = ((((((u0.x + u0.y) + u0.z) + u0.w) + u1.x) + u1.y) + u1.z) + u1.w;
-                v = warp_sum(v);
-                const int slot = ((b & 3) * kBwMaxCluster + static_cast<int>(rank)) * kBwBatch + j;
-                if (lane == 0) box[slot] = v;
-                if (lane < static_cast<int>(C) && lane != static_cast<int>(rank) && !failed)
-                    sc_st_async(sc_mapa(box_lo + slot * 4, lane), v, sc_mapa(bar_lo + (b & 3) * 8, lane));
+        const float inv_d = 1.0f / static_cast<float>(d);
+
+        float U[4][kScEV];                      // u by slot: position q's in slot q & 3
+        float P1[kScEV], P2[kScEV], P3[kScEV];  // du collecting contributions, by age 1..3
+        float A[kScAges][kScEV], db[kScEV], dnw[kScEV];
+        bool pend1 = false, pend2 = false, pend3 = false;
+        int st = 0;
+        uint32_t ph = 0, gpos = 0;
+        int nfin = 0, nb = 0, prev_n = 0;  // tokens of the open batch, batches posted, tokens of the pending one
+
+        // a wait of the whole warp: every lane takes the same view of a failure
+        auto wait_warp = [&](uint64_t *bar, uint32_t parity) {
+            if (failed) return;
+            if (!__all_sync(0xffffffffu, mbar_wait_sleep(bar, parity))) {
+                if (lane == 0) report(p.status, nullptr, ENGRAM_DEVERR_TIMEOUT);
+                failed = true;
+            }
+        };
+        auto advance = [&]() {
+            if (++st == S) st = 0, ph ^= 1u;
+            ++gpos;
+        };
+        auto back = [&](int a) { return st - a < 0 ? st - a + S : st - a; };
+        // after a failure a warp arrives on no barrier and sends nothing: no phase can be overrun
+        auto release = [&](int stage) {
+            __syncwarp();
+            if (lane == 0 && !failed) mbar_arrive(&empty[stage]);
+        };
+        // a token `a` positions back has its du: its y, row-dot part and norm-weight gradient
+        auto complete = [&](int a, const float (&du)[kScEV]) {
+            const int sa = back(a);
+            const uint8_t *stg = ring + static_cast<size_t>(sa) * SB + tid * EV::kBytes;
+            float x[kScEV], g[kScEV];
+            EV::load_smem(stg, x);
+            EV::load_smem(stg + half, g);
+            const float ra = meta[sa].rstd;
+            float part = 0.f, y[kScEV];
+#pragma unroll
+            for (int e = 0; e < kScEV; ++e) {
+                const float dn = nw[e] * du[e];
+                part = fmaf(dn, x[e], part);
+                dnw[e] = fmaf(du[e] * x[e], ra, dnw[e]);
+                y[e] = fmaf(ra, dn, g[e]);
+            }
+            const int slot = ((nb & 1) * kBwBatch + nfin) * kBwCons + tid;
+            pbuf[slot] = active ? part : 0.f;
+            ybuf[slot] = make_float4(y[0], y[1], y[2], y[3]);
+            if (tid == 0) fin_stage[(nb & 3) * kBwBatch + nfin] = sa;
+            ++nfin;
+        };
+        // batch bf's dv rows once the cluster's row dots have arrived; its stages go back to the producer.
+        // Lane j works out token j's row dot (the ranks' sums in rank order) and scale; the tokens'
+        // rows are then independent of each other.
+        auto finalize = [&](int bf, int n) {
+            wait_warp(&boxbar[bf & 3], (bf >> 2) & 1);
+            const float *bx = box + (bf & 3) * kBwMaxCluster * kBwBatch;
+            const int *fs = fin_stage + (bf & 3) * kBwBatch;
+            float kk_l = 0.f;
+            int sj_l = 0;
+            long long tok_l = 0;
+            if (lane < n) {
+                sj_l = fs[lane];
+                float s = 0.f;
+                for (int k = 0; k < static_cast<int>(C); ++k) s += bx[k * kBwBatch + lane];
+                const float r = meta[sj_l].rstd;
+                kk_l = r * r * r * s * inv_d;
+                tok_l = meta[sj_l].tok;
+            }
+            const size_t row_bytes = static_cast<size_t>(d) * sizeof(E);
+            uint8_t *dv_col = p.dv + static_cast<size_t>(c0) * sizeof(E) + tid * EV::kBytes;
+#pragma unroll
+            for (int j = 0; j < kBwBatch; ++j) {
+                const float kk = __shfl_sync(0xffffffffu, kk_l, j);
+                const int sj = __shfl_sync(0xffffffffu, sj_l, j);
+                const long long tok = __shfl_sync(0xffffffffu, tok_l, j);
+                if (j < n) {
+                    float x[kScEV];
+                    EV::load_smem(ring + static_cast<size_t>(sj) * SB + tid * EV::kBytes, x);
+                    const float4 y = ybuf[((bf & 1) * kBwBatch + j) * kBwCons + tid];
+                    float o[kScEV] = {fmaf(-kk, x[0], y.x), fmaf(-kk, x[1], y.y), fmaf(-kk, x[2], y.z),
+                                      fmaf(-kk, x[3], y.w)};
+                    if (active) EV::store(dv_col + static_cast<size_t>(tok) * row_bytes, o);
+                }
             }
             __syncwarp();
-            if (lane == 0 && !failed) mbar_arrive_expect_tx(&boxbar[b & 3], (C - 1) * nfin * 4);
-        }
-        if (prev_n > 0) finalize(b - 1, prev_n);
-        prev_n = nfin;
-        nfin = 0;
-        ++nb;
-    };
-    // one sweep position in slot J.  STEADY: a chunk token with three chunk tokens pending before it,
-    // so the one three back completes; otherwise `kind` and the pending flags decide.
-    auto step = [&](auto Jc, auto Sc, uint32_t kind) {
-        constexpr int J = decltype(Jc)::v;
-        constexpr bool STEADY = decltype(Sc)::v != 0;
-        wait_warp(&full[st], ph);
-        const uint8_t *stg = ring + static_cast<size_t>(st) * SB + tid * EV::kBytes;
-        const float rt = meta[st].rstd;
-        float x[kScEV];
-        EV::load_smem(stg, x);
+            if (lane < n && !failed) mbar_arrive(&empty[sj_l]);
+        };
+        // the open batch is complete: this warp's part is announced; the batch's reducer warp sums the
+        // CTA's row dots (thread order, then lanes) and sends them to the cluster; then the previous
+        // batch, whose sums have had a batch's time to arrive, is finished
+        auto post = [&]() {
+            const int b = nb;
+            __syncwarp();
+            if (lane == 0 && !failed) mbar_arrive(&lbar[b & 1]);
+            if (warp == (b & (kBwWarps - 1)) && !failed) {
+                wait_warp(&lbar[b & 1], (b >> 1) & 1);
+                const float *pb = pbuf + (b & 1) * kBwBatch * kBwCons;
+                const uint32_t box_lo = smem_addr(box), bar_lo = smem_addr(boxbar);
+                for (int j = 0; j < nfin; ++j) {
+                    static_assert(kBwCons == 32 * 4, "a lane sums four threads' parts");
+                    const float4 u0 = *reinterpret_cast<const float4 *>(pb + j * kBwCons + lane * 4);
+                    float v = ((u0.x + u0.y) + u0.z) + u0.w;
+                    v = warp_sum(v);
+                    const int slot = ((b & 3) * kBwMaxCluster + static_cast<int>(rank)) * kBwBatch + j;
+                    if (lane == 0) box[slot] = v;
+                    if (lane < static_cast<int>(C) && lane != static_cast<int>(rank) && !failed)
+                        sc_st_async(sc_mapa(box_lo + slot * 4, lane), v, sc_mapa(bar_lo + (b & 3) * 8, lane));
+                }
+                __syncwarp();
+                if (lane == 0 && !failed) mbar_arrive_expect_tx(&boxbar[b & 3], (C - 1) * nfin * 4);
+            }
+            if (prev_n > 0) finalize(b - 1, prev_n);
+            prev_n = nfin;
+            nfin = 0;
+            ++nb;
+        };
+        // one sweep position in slot J, its stage already waited for.  STEADY: a chunk token with three
+        // chunk tokens pending before it, so the one three back completes; otherwise `kind` and the
+        // pending flags decide.
+        auto step = [&](auto Jc, auto Sc, uint32_t kind) {
+            constexpr int J = decltype(Jc)::v;
+            constexpr bool STEADY = decltype(Sc)::v != 0;
+            const uint8_t *stg = ring + static_cast<size_t>(st) * SB + tid * EV::kBytes;
+            const float rt = meta[st].rstd;
+            float x[kScEV];
+            EV::load_smem(stg, x);
 #pragma unroll
-        for (int e = 0; e < kScEV; ++e) U[J][e] = x[e] * rt * nw[e];
-        if (!STEADY && kind == kScLead) {
-            release(st);
+            for (int e = 0; e < kScEV; ++e) U[J][e] = x[e] * rt * nw[e];
+            if (!STEADY && kind == kScLead) {
+                release(st);
+                advance();
+                return;
+            }
+            float g[kScEV], dc[kScEV];
+            EV::load_smem(stg + half, g);
+#pragma unroll
+            for (int e = 0; e < kScEV; ++e) {
+                const float c = fmaf(w[3][e], U[(J + 1) & 3][e],
+                                     fmaf(w[2][e], U[(J + 2) & 3][e],
+                                          fmaf(w[1][e], U[(J + 3) & 3][e], fmaf(w[0][e], U[J][e], bias[e]))));
+                const float sg = sc_sigmoid_fast(c);
+                // SiLU'(c) = sg (1 + c (1 - sg))
+                dc[e] = g[e] * fmaf(sg, fmaf(-c, sg, c), sg);
+            }
+            if (STEADY || kind == kScMain) {
+#pragma unroll
+                for (int e = 0; e < kScEV; ++e) {
+                    db[e] += dc[e];
+                    A[0][e] = fmaf(dc[e], U[J][e], A[0][e]);
+                    A[1][e] = fmaf(dc[e], U[(J + 3) & 3][e], A[1][e]);
+                    A[2][e] = fmaf(dc[e], U[(J + 2) & 3][e], A[2][e]);
+                    A[3][e] = fmaf(dc[e], U[(J + 1) & 3][e], A[3][e]);
+                }
+            }
+            if (STEADY || pend3) {
+                float du[kScEV];
+#pragma unroll
+                for (int e = 0; e < kScEV; ++e) du[e] = fmaf(w[3][e], dc[e], P3[e]);
+                complete(3, du);
+            }
+#pragma unroll
+            for (int e = 0; e < kScEV; ++e) {
+                P3[e] = fmaf(w[2][e], dc[e], P2[e]);
+                P2[e] = fmaf(w[1][e], dc[e], P1[e]);
+                P1[e] = w[0][e] * dc[e];
+            }
+            if (!STEADY) {
+                pend3 = pend2, pend2 = pend1, pend1 = kind == kScMain;
+                if (kind == kScTail) release(st);
+            }
             advance();
-            return;
-        }
-        float g[kScEV], dc[kScEV];
-        EV::load_smem(stg + half, g);
+        };
+
+        // a work item's weight-gradient partial row: the taps (by tap index), the bias, the norm weight
+        const int64_t ncl = sc_num_clusters();
+        auto write_rows = [&](int64_t item, bool zero) {
+            if (!active) return;
+            float *prow = p.partial + static_cast<size_t>(item) * (width + 2) * d + c0 + tid * kScEV;
 #pragma unroll
-        for (int e = 0; e < kScEV; ++e) {
-            const float c = fmaf(w[3][e], U[(J + 1) & 3][e],
-                                 fmaf(w[2][e], U[(J + 2) & 3][e],
-                                      fmaf(w[1][e], U[(J + 3) & 3][e], fmaf(w[0][e], U[J][e], bias[e]))));
-            const float sg = sc_sigmoid_fast(c);
-            // SiLU'(c) = sg (1 + c (1 - sg))
-            dc[e] = g[e] * fmaf(sg, fmaf(-c, sg, c), sg);
-        }
-        if (STEADY || kind == kScMain) {
+            for (int a = 0; a < kScAges; ++a)
+                if (a < width)
+                    *reinterpret_cast<float4 *>(prow + static_cast<size_t>(width - 1 - a) * d) =
+                        zero ? make_float4(0.f, 0.f, 0.f, 0.f) : make_float4(A[a][0], A[a][1], A[a][2], A[a][3]);
+            *reinterpret_cast<float4 *>(prow + static_cast<size_t>(width) * d) =
+                zero ? make_float4(0.f, 0.f, 0.f, 0.f) : make_float4(db[0], db[1], db[2], db[3]);
+            *reinterpret_cast<float4 *>(prow + static_cast<size_t>(width + 1) * d) =
+                zero ? make_float4(0.f, 0.f, 0.f, 0.f) : make_float4(dnw[0], dnw[1], dnw[2], dnw[3]);
+        };
+        // rows of the item just finished (if any) and zeros for this cluster's items without tokens up to `next`
+        int64_t cur_item = -1;
+        auto finish_items = [&](int64_t next) {
+            int64_t it = sc_cluster_id();
+            if (cur_item >= 0) {
+                write_rows(cur_item, false);
+                it = cur_item + ncl;
+            }
+            for (; it < next; it += ncl) write_rows(it, true);
 #pragma unroll
             for (int e = 0; e < kScEV; ++e) {
-                db[e] += dc[e];
-                A[0][e] = fmaf(dc[e], U[J][e], A[0][e]);
-                A[1][e] = fmaf(dc[e], U[(J + 3) & 3][e], A[1][e]);
-                A[2][e] = fmaf(dc[e], U[(J + 2) & 3][e], A[2][e]);
-                A[3][e] = fmaf(dc[e], U[(J + 1) & 3][e], A[3][e]);
+                db[e] = dnw[e] = 0.f;
+#pragma unroll
+                for (int a = 0; a < kScAges; ++a) A[a][e] = 0.f;
             }
-        }
-        if (STEADY || pend3) {
-            float du[kScEV];
-#pragma unroll
-            for (int e = 0; e < kScEV; ++e) du[e] = fmaf(w[3][e], dc[e], P3[e]);
-            complete(3, du);
-        }
-#pragma unroll
-        for (int e = 0; e < kScEV; ++e) {
-            P3[e] = fmaf(w[2][e], dc[e], P2[e]);
-            P2[e] = fmaf(w[1][e], dc[e], P1[e]);
-            P1[e] = w[0][e] * dc[e];
-        }
-        if (!STEADY) {
-            pend3 = pend2, pend2 = pend1, pend1 = kind == kScMain;
-            if (kind == kScTail) release(st);
-        }
-        advance();
-    };
+        };
+        finish_items(-1);  // clears the accumulators
 
-    // a work item's weight-gradient partial row: the taps (by tap index), the bias, the norm weight
-    const int64_t ncl = sc_num_clusters();
-    auto write_rows = [&](int64_t item, bool zero) {
-        if (!active) return;
-        float *prow = p.partial + static_cast<size_t>(item) * (width + 2) * d + c0 + tid * kScEV;
-#pragma unroll
-        for (int a = 0; a < kScAges; ++a)
-            if (a < width)
-                *reinterpret_cast<float4 *>(prow + static_cast<size_t>(width - 1 - a) * d) =
-                    zero ? make_float4(0.f, 0.f, 0.f, 0.f) : make_float4(A[a][0], A[a][1], A[a][2], A[a][3]);
-        *reinterpret_cast<float4 *>(prow + static_cast<size_t>(width) * d) =
-            zero ? make_float4(0.f, 0.f, 0.f, 0.f) : make_float4(db[0], db[1], db[2], db[3]);
-        *reinterpret_cast<float4 *>(prow + static_cast<size_t>(width + 1) * d) =
-            zero ? make_float4(0.f, 0.f, 0.f, 0.f) : make_float4(dnw[0], dnw[1], dnw[2], dnw[3]);
-    };
-    // rows of the item just finished (if any) and zeros for this cluster's items without tokens up to `next`
-    int64_t cur_item = -1;
-    auto finish_items = [&](int64_t next) {
-        int64_t it = sc_cluster_id();
-        if (cur_item >= 0) {
-            write_rows(cur_item, false);
-            it = cur_item + ncl;
-        }
-        for (; it < next; it += ncl) write_rows(it, true);
-#pragma unroll
-        for (int e = 0; e < kScEV; ++e) {
-            db[e] = dnw[e] = 0.f;
-#pragma unroll
-            for (int a = 0; a < kScAges; ++a) A[a][e] = 0.f;
-        }
-    };
-    finish_items(-1);  // clears the accumulators
-
-    for (;;) {
-        if (warp == 0) {  // the copies: every free stage, and at least the next four positions
-            if (lane == 0) produce(gpos + 3);
-            failed = __any_sync(0xffffffffu, failed);
-        }
-        wait_warp(&full[st], ph);
-        if (failed) break;
-        const uint32_t fl = meta[st].flags;
-        if (fl & kFlDone) break;
-        if (fl & kFlItemStart) {
-            const int64_t item = static_cast<int64_t>(fl >> kFlItemShift);
-            finish_items(item);
-            cur_item = item;
-        }
-        if (fl & kFlSegStart) {
-#pragma unroll
-            for (int e = 0; e < kScEV; ++e) {
-                U[0][e] = U[1][e] = U[2][e] = U[3][e] = 0.f;
-                P1[e] = P2[e] = P3[e] = 0.f;
+        for (;;) {
+            wait_warp(&full[st], ph);
+            if (failed) break;
+            const uint32_t fl = meta[st].flags;
+            if (fl & kFlDone) break;
+            if (fl & kFlItemStart) {
+                const int64_t item = static_cast<int64_t>(fl >> kFlItemShift);
+                finish_items(item);
+                cur_item = item;
             }
-            pend1 = pend2 = pend3 = false;
-        }
-        if (fl & kFlGroup) {
-            if (nfin > 0) post();  // a steady group fills one batch of its own
-            step(ScIdx<0>{}, ScIdx<1>{}, kScMain);
-            step(ScIdx<1>{}, ScIdx<1>{}, kScMain);
-            step(ScIdx<2>{}, ScIdx<1>{}, kScMain);
-            step(ScIdx<3>{}, ScIdx<1>{}, kScMain);
-            pend1 = pend2 = pend3 = true;
-        } else {
-            const uint32_t kind = fl & kFlKind;
-            switch ((fl >> kFlSlotShift) & 3u) {
-                case 0: step(ScIdx<0>{}, ScIdx<0>{}, kind); break;
-                case 1: step(ScIdx<1>{}, ScIdx<0>{}, kind); break;
-                case 2: step(ScIdx<2>{}, ScIdx<0>{}, kind); break;
-                default: step(ScIdx<3>{}, ScIdx<0>{}, kind); break;
+            if (fl & kFlSegStart) {
+#pragma unroll
+                for (int e = 0; e < kScEV; ++e) {
+                    U[0][e] = U[1][e] = U[2][e] = U[3][e] = 0.f;
+                    P1[e] = P2[e] = P3[e] = 0.f;
+                }
+                pend1 = pend2 = pend3 = false;
+            }
+            if (fl & kFlGroup) {
+                if (nfin > 0) post();  // a steady group fills one batch of its own
+                // all four stages first, so that the four positions' loads and arithmetic may overlap
+#pragma unroll
+                for (int k = 1; k < 4; ++k) {
+                    const bool wrap = st + k >= S;
+                    wait_warp(&full[wrap ? st + k - S : st + k], wrap ? ph ^ 1u : ph);
+                }
+                if (failed) break;
+                step(ScIdx<0>{}, ScIdx<1>{}, kScMain);
+                step(ScIdx<1>{}, ScIdx<1>{}, kScMain);
+                step(ScIdx<2>{}, ScIdx<1>{}, kScMain);
+                step(ScIdx<3>{}, ScIdx<1>{}, kScMain);
+                pend1 = pend2 = pend3 = true;
+            } else {
+                const uint32_t kind = fl & kFlKind;
+                switch ((fl >> kFlSlotShift) & 3u) {
+                    case 0: step(ScIdx<0>{}, ScIdx<0>{}, kind); break;
+                    case 1: step(ScIdx<1>{}, ScIdx<0>{}, kind); break;
+                    case 2: step(ScIdx<2>{}, ScIdx<0>{}, kind); break;
+                    default: step(ScIdx<3>{}, ScIdx<0>{}, kind); break;
+                }
+            }
+            if (nfin == kBwBatch) post();
+            if (fl & kFlSegEnd) {
+                // the sequence (or the look-ahead) ends: the pending du have all their terms
+                if (pend3) {
+                    complete(3, P3);
+                    if (nfin == kBwBatch) post();
+                }
+                if (pend2) {
+                    complete(2, P2);
+                    if (nfin == kBwBatch) post();
+                }
+                if (pend1) complete(1, P1);
+                if (nfin > 0) post();
+                if (prev_n > 0) finalize(nb - 1, prev_n);
+                prev_n = 0;
+                pend1 = pend2 = pend3 = false;
             }
         }
-        if (nfin == kBwBatch) post();
-        if (fl & kFlSegEnd) {
-            // the sequence (or the look-ahead) ends: the pending du have all their terms
-            if (pend3) {
-                complete(3, P3);
-                if (nfin == kBwBatch) post();
-            }
-            if (pend2) {
-                complete(2, P2);
-                if (nfin == kBwBatch) post();
-            }
-            if (pend1) complete(1, P1);
-            if (nfin > 0) post();
-            if (prev_n > 0) finalize(nb - 1, prev_n);
-            prev_n = 0;
-            pend1 = pend2 = pend3 = false;
-        }
-    }
-    if (!failed) finish_items(p.nitems);
-    // after a failure, copies may still be landing: wait for them (bounded) before the CTA leaves
-    if (tid == 0 && failed) {
-        const uint32_t issued = prod->issued;
-        for (uint32_t q = issued > static_cast<uint32_t>(S) ? issued - S : 0; q < issued; ++q)
-            mbar_wait(&full[q % S], (q / S) & 1u, kWaitLimitNs / 16);
+        if (!failed) finish_items(p.nitems);
     }
     sc_cluster_sync();  // no CTA leaves while a peer may still write into its shared memory
 }
@@ -985,9 +1030,11 @@ engram_status sc_bwd_launch(const char *fn, ScBwdParams prm, const DeviceInfo &d
     void (*kern)(ScBwdParams) = conv_bwd_kernel<E>;
     engram_status st = set_smem(reinterpret_cast<const void *>(kern), smem);
     if (st != ENGRAM_OK) return st;
-    // two CTAs per SM: the largest shared-memory carveout
+    // three CTAs per SM: the largest shared-memory carveout; clusters above 8 CTAs (d > 4096) are
+    // a non-portable size
     if (cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared) !=
-        cudaSuccess)
+            cudaSuccess ||
+        (C > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess))
         return check_launch(fn);
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
