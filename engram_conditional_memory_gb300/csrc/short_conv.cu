@@ -47,6 +47,13 @@ struct Ev4<float> {
         const float4 u = *reinterpret_cast<const float4 *>(p);
         x[0] = u.x, x[1] = u.y, x[2] = u.z, x[3] = u.w;
     }
+    __device__ __forceinline__ static void load2(const uint8_t *p, float2 (&x)[2]) {
+        const float4 u = *reinterpret_cast<const float4 *>(p);
+        x[0] = make_float2(u.x, u.y), x[1] = make_float2(u.z, u.w);
+    }
+    __device__ __forceinline__ static void store2(uint8_t *p, const float2 (&x)[2]) {
+        *reinterpret_cast<float4 *>(p) = make_float4(x[0].x, x[0].y, x[1].x, x[1].y);
+    }
     __device__ __forceinline__ static void store(uint8_t *p, const float (&x)[4]) {
         *reinterpret_cast<float4 *>(p) = make_float4(x[0], x[1], x[2], x[3]);
     }
@@ -60,11 +67,27 @@ struct Ev4<__nv_bfloat16> {
         x[0] = __uint_as_float(u.x << 16), x[1] = __uint_as_float(u.x & 0xffff0000u);
         x[2] = __uint_as_float(u.y << 16), x[3] = __uint_as_float(u.y & 0xffff0000u);
     }
+    __device__ __forceinline__ static void load2(const uint8_t *p, float2 (&x)[2]) {
+        const uint2 u = *reinterpret_cast<const uint2 *>(p);
+        x[0] = make_float2(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u));
+        x[1] = make_float2(__uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+    }
+    __device__ __forceinline__ static void store2(uint8_t *p, const float2 (&x)[2]) {
+        *reinterpret_cast<uint2 *>(p) =
+            make_uint2(Vec<__nv_bfloat16>::pack2(x[0].x, x[0].y), Vec<__nv_bfloat16>::pack2(x[1].x, x[1].y));
+    }
     __device__ __forceinline__ static void store(uint8_t *p, const float (&x)[4]) {
         *reinterpret_cast<uint2 *>(p) =
             make_uint2(Vec<__nv_bfloat16>::pack2(x[0], x[1]), Vec<__nv_bfloat16>::pack2(x[2], x[3]));
     }
 };
+
+// Two channels at once: sm_100's paired fp32 instructions, each half rounded as the scalar
+// operation would be.
+__device__ __forceinline__ float2 p2fma(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 p2mul(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 p2add(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 p2(float v) { return make_float2(v, v); }
 
 // SiLU's sigmoid with the fast exponential and division (a few ulp; the outputs are rounded far
 // coarser, and the tolerances carry the bound).
@@ -506,8 +529,8 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
     int *fin_stage = reinterpret_cast<int *>(meta + S);
     uint64_t *full = reinterpret_cast<uint64_t *>(fin_stage + 4 * kBwBatch);
     uint64_t *empty = full + S;
-    uint64_t *lbar = empty + S;
-    uint64_t *boxbar = lbar + 2;
+    int *lcnt = reinterpret_cast<int *>(empty + S);  // [2] warps done with a batch, by batch parity
+    uint64_t *boxbar = empty + S + 2;
     ScProd *prod = reinterpret_cast<ScProd *>(boxbar + 4);
 
     const int tid = threadIdx.x;
@@ -645,7 +668,7 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
             mbar_init(&full[i], 2);  // the producer's arrival and its rstd copy's
             mbar_init(&empty[i], kBwWarps);
         }
-        for (int i = 0; i < 2; ++i) mbar_init(&lbar[i], kBwWarps);
+        lcnt[0] = lcnt[1] = 0;
         for (int i = 0; i < 4; ++i) mbar_init(&boxbar[i], 1);
         mbar_init_fence();
     }
@@ -673,22 +696,32 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
 
         const bool active = tid * kScEV < ncols;
         const int width = p.width, d = p.d;
-        float w[kScAges][kScEV], nw[kScEV], bias[kScEV];
+        // the thread's four channels as two pairs: [h] holds channels 2h and 2h + 1
+        float2 w[kScAges][2], nw[2], bias[2];
 #pragma unroll
-        for (int e = 0; e < kScEV; ++e) {
-            const int c = c0 + tid * kScEV + e;
-            const bool ok = active && c < d;
-            nw[e] = ok ? __ldg(p.norm_w + c) : 0.f;
-            bias[e] = ok && p.bias ? __ldg(p.bias + c) : 0.f;
+        for (int h = 0; h < 2; ++h) {
+            float v[2][2 + kScAges];
 #pragma unroll
-            for (int a = 0; a < kScAges; ++a)
-                w[a][e] = ok && a < width ? __ldg(p.conv_w + static_cast<size_t>(c) * width + (width - 1 - a)) : 0.f;
+            for (int k = 0; k < 2; ++k) {
+                const int c = c0 + tid * kScEV + 2 * h + k;
+                const bool ok = active && c < d;
+                v[k][0] = ok ? __ldg(p.norm_w + c) : 0.f;
+                v[k][1] = ok && p.bias ? __ldg(p.bias + c) : 0.f;
+#pragma unroll
+                for (int a = 0; a < kScAges; ++a)
+                    v[k][2 + a] =
+                        ok && a < width ? __ldg(p.conv_w + static_cast<size_t>(c) * width + (width - 1 - a)) : 0.f;
+            }
+            nw[h] = make_float2(v[0][0], v[1][0]);
+            bias[h] = make_float2(v[0][1], v[1][1]);
+#pragma unroll
+            for (int a = 0; a < kScAges; ++a) w[a][h] = make_float2(v[0][2 + a], v[1][2 + a]);
         }
         const float inv_d = 1.0f / static_cast<float>(d);
 
-        float U[4][kScEV];                      // u by slot: position q's in slot q & 3
-        float P1[kScEV], P2[kScEV], P3[kScEV];  // du collecting contributions, by age 1..3
-        float A[kScAges][kScEV], db[kScEV], dnw[kScEV];
+        float2 U[4][2];                 // u by slot: position q's in slot q & 3
+        float2 P1[2], P2[2], P3[2];     // du collecting contributions, by age 1..3
+        float2 A[kScAges][2], db[2], dnw[2];
         bool pend1 = false, pend2 = false, pend3 = false;
         int st = 0;
         uint32_t ph = 0, gpos = 0;
@@ -713,24 +746,25 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
             if (lane == 0 && !failed) mbar_arrive(&empty[stage]);
         };
         // a token `a` positions back has its du: its y, row-dot part and norm-weight gradient
-        auto complete = [&](int a, const float (&du)[kScEV]) {
+        auto complete = [&](int a, const float2 (&du)[2]) {
             const int sa = back(a);
             const uint8_t *stg = ring + static_cast<size_t>(sa) * SB + tid * EV::kBytes;
-            float x[kScEV], g[kScEV];
-            EV::load_smem(stg, x);
-            EV::load_smem(stg + half, g);
-            const float ra = meta[sa].rstd;
-            float part = 0.f, y[kScEV];
+            float2 x[2], g[2], dn[2], y[2];
+            EV::load2(stg, x);
+            EV::load2(stg + half, g);
+            const float2 ra = p2(meta[sa].rstd);
 #pragma unroll
-            for (int e = 0; e < kScEV; ++e) {
-                const float dn = nw[e] * du[e];
-                part = fmaf(dn, x[e], part);
-                dnw[e] = fmaf(du[e] * x[e], ra, dnw[e]);
-                y[e] = fmaf(ra, dn, g[e]);
+            for (int h = 0; h < 2; ++h) {
+                dn[h] = p2mul(nw[h], du[h]);
+                dnw[h] = p2fma(p2mul(du[h], x[h]), ra, dnw[h]);
+                y[h] = p2fma(ra, dn[h], g[h]);
             }
+            // the thread's part of the row dot: (c0 + c2) + (c1 + c3) of the products
+            const float2 pp = p2fma(dn[1], x[1], p2mul(dn[0], x[0]));
+            const float part = pp.x + pp.y;
             const int slot = ((nb & 1) * kBwBatch + nfin) * kBwCons + tid;
             pbuf[slot] = active ? part : 0.f;
-            ybuf[slot] = make_float4(y[0], y[1], y[2], y[3]);
+            ybuf[slot] = make_float4(y[0].x, y[0].y, y[1].x, y[1].y);
             if (tid == 0) fin_stage[(nb & 3) * kBwBatch + nfin] = sa;
             ++nfin;
         };
@@ -760,26 +794,35 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
                 const int sj = __shfl_sync(0xffffffffu, sj_l, j);
                 const long long tok = __shfl_sync(0xffffffffu, tok_l, j);
                 if (j < n) {
-                    float x[kScEV];
-                    EV::load_smem(ring + static_cast<size_t>(sj) * SB + tid * EV::kBytes, x);
+                    float2 x[2];
+                    EV::load2(ring + static_cast<size_t>(sj) * SB + tid * EV::kBytes, x);
                     const float4 y = ybuf[((bf & 1) * kBwBatch + j) * kBwCons + tid];
-                    float o[kScEV] = {fmaf(-kk, x[0], y.x), fmaf(-kk, x[1], y.y), fmaf(-kk, x[2], y.z),
-                                      fmaf(-kk, x[3], y.w)};
-                    if (active) EV::store(dv_col + static_cast<size_t>(tok) * row_bytes, o);
+                    const float2 o[2] = {p2fma(p2(-kk), x[0], make_float2(y.x, y.y)),
+                                         p2fma(p2(-kk), x[1], make_float2(y.z, y.w))};
+                    if (active) EV::store2(dv_col + static_cast<size_t>(tok) * row_bytes, o);
                 }
             }
             __syncwarp();
             if (lane < n && !failed) mbar_arrive(&empty[sj_l]);
         };
-        // the open batch is complete: this warp's part is announced; the batch's reducer warp sums the
-        // CTA's row dots (thread order, then lanes) and sends them to the cluster; then the previous
-        // batch, whose sums have had a batch's time to arrive, is finished
+        // the open batch is complete: this warp's parts are counted in, and the warp that completes the
+        // count sums the CTA's row dots (thread order, then lanes) and sends them to the cluster --
+        // nobody waits for the others; then the previous batch, whose sums have had a batch's time
+        // to arrive, is finished
         auto post = [&]() {
             const int b = nb;
             __syncwarp();
-            if (lane == 0 && !failed) mbar_arrive(&lbar[b & 1]);
-            if (warp == (b & (kBwWarps - 1)) && !failed) {
-                wait_warp(&lbar[b & 1], (b >> 1) & 1);
+            int last = 0;
+            if (lane == 0 && !failed) {
+                __threadfence_block();  // the warp's parts before its count
+                last = atomicAdd(&lcnt[b & 1], 1) == kBwWarps - 1;
+                if (last) {
+                    lcnt[b & 1] = 0;  // no warp counts batch b + 2 before this batch's sums were sent
+                    __threadfence_block();  // every warp's parts before the sums
+                }
+            }
+            if (__shfl_sync(0xffffffffu, last, 0)) {
+                __syncwarp();
                 const float *pb = pbuf + (b & 1) * kBwBatch * kBwCons;
                 const uint32_t box_lo = smem_addr(box), bar_lo = smem_addr(boxbar);
                 for (int j = 0; j < nfin; ++j) {
@@ -807,48 +850,48 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
             constexpr int J = decltype(Jc)::v;
             constexpr bool STEADY = decltype(Sc)::v != 0;
             const uint8_t *stg = ring + static_cast<size_t>(st) * SB + tid * EV::kBytes;
-            const float rt = meta[st].rstd;
-            float x[kScEV];
-            EV::load_smem(stg, x);
+            const float2 rt = p2(meta[st].rstd);
+            float2 x[2];
+            EV::load2(stg, x);
 #pragma unroll
-            for (int e = 0; e < kScEV; ++e) U[J][e] = x[e] * rt * nw[e];
+            for (int h = 0; h < 2; ++h) U[J][h] = p2mul(p2mul(x[h], rt), nw[h]);
             if (!STEADY && kind == kScLead) {
                 release(st);
                 advance();
                 return;
             }
-            float g[kScEV], dc[kScEV];
-            EV::load_smem(stg + half, g);
+            float2 g[2], dc[2];
+            EV::load2(stg + half, g);
 #pragma unroll
-            for (int e = 0; e < kScEV; ++e) {
-                const float c = fmaf(w[3][e], U[(J + 1) & 3][e],
-                                     fmaf(w[2][e], U[(J + 2) & 3][e],
-                                          fmaf(w[1][e], U[(J + 3) & 3][e], fmaf(w[0][e], U[J][e], bias[e]))));
-                const float sg = sc_sigmoid_fast(c);
+            for (int h = 0; h < 2; ++h) {
+                const float2 c = p2fma(w[3][h], U[(J + 1) & 3][h],
+                                       p2fma(w[2][h], U[(J + 2) & 3][h],
+                                             p2fma(w[1][h], U[(J + 3) & 3][h], p2fma(w[0][h], U[J][h], bias[h]))));
+                const float2 sg = make_float2(sc_sigmoid_fast(c.x), sc_sigmoid_fast(c.y));
                 // SiLU'(c) = sg (1 + c (1 - sg))
-                dc[e] = g[e] * fmaf(sg, fmaf(-c, sg, c), sg);
+                dc[h] = p2mul(g[h], p2fma(sg, p2fma(make_float2(-c.x, -c.y), sg, c), sg));
             }
             if (STEADY || kind == kScMain) {
 #pragma unroll
-                for (int e = 0; e < kScEV; ++e) {
-                    db[e] += dc[e];
-                    A[0][e] = fmaf(dc[e], U[J][e], A[0][e]);
-                    A[1][e] = fmaf(dc[e], U[(J + 3) & 3][e], A[1][e]);
-                    A[2][e] = fmaf(dc[e], U[(J + 2) & 3][e], A[2][e]);
-                    A[3][e] = fmaf(dc[e], U[(J + 1) & 3][e], A[3][e]);
+                for (int h = 0; h < 2; ++h) {
+                    db[h] = p2add(db[h], dc[h]);
+                    A[0][h] = p2fma(dc[h], U[J][h], A[0][h]);
+                    A[1][h] = p2fma(dc[h], U[(J + 3) & 3][h], A[1][h]);
+                    A[2][h] = p2fma(dc[h], U[(J + 2) & 3][h], A[2][h]);
+                    A[3][h] = p2fma(dc[h], U[(J + 1) & 3][h], A[3][h]);
                 }
             }
             if (STEADY || pend3) {
-                float du[kScEV];
+                float2 du[2];
 #pragma unroll
-                for (int e = 0; e < kScEV; ++e) du[e] = fmaf(w[3][e], dc[e], P3[e]);
+                for (int h = 0; h < 2; ++h) du[h] = p2fma(w[3][h], dc[h], P3[h]);
                 complete(3, du);
             }
 #pragma unroll
-            for (int e = 0; e < kScEV; ++e) {
-                P3[e] = fmaf(w[2][e], dc[e], P2[e]);
-                P2[e] = fmaf(w[1][e], dc[e], P1[e]);
-                P1[e] = w[0][e] * dc[e];
+            for (int h = 0; h < 2; ++h) {
+                P3[h] = p2fma(w[2][h], dc[h], P2[h]);
+                P2[h] = p2fma(w[1][h], dc[h], P1[h]);
+                P1[h] = p2mul(w[0][h], dc[h]);
             }
             if (!STEADY) {
                 pend3 = pend2, pend2 = pend1, pend1 = kind == kScMain;
@@ -866,11 +909,12 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
             for (int a = 0; a < kScAges; ++a)
                 if (a < width)
                     *reinterpret_cast<float4 *>(prow + static_cast<size_t>(width - 1 - a) * d) =
-                        zero ? make_float4(0.f, 0.f, 0.f, 0.f) : make_float4(A[a][0], A[a][1], A[a][2], A[a][3]);
+                        zero ? make_float4(0.f, 0.f, 0.f, 0.f)
+                             : make_float4(A[a][0].x, A[a][0].y, A[a][1].x, A[a][1].y);
             *reinterpret_cast<float4 *>(prow + static_cast<size_t>(width) * d) =
-                zero ? make_float4(0.f, 0.f, 0.f, 0.f) : make_float4(db[0], db[1], db[2], db[3]);
+                zero ? make_float4(0.f, 0.f, 0.f, 0.f) : make_float4(db[0].x, db[0].y, db[1].x, db[1].y);
             *reinterpret_cast<float4 *>(prow + static_cast<size_t>(width + 1) * d) =
-                zero ? make_float4(0.f, 0.f, 0.f, 0.f) : make_float4(dnw[0], dnw[1], dnw[2], dnw[3]);
+                zero ? make_float4(0.f, 0.f, 0.f, 0.f) : make_float4(dnw[0].x, dnw[0].y, dnw[1].x, dnw[1].y);
         };
         // rows of the item just finished (if any) and zeros for this cluster's items without tokens up to `next`
         int64_t cur_item = -1;
@@ -882,10 +926,10 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
             }
             for (; it < next; it += ncl) write_rows(it, true);
 #pragma unroll
-            for (int e = 0; e < kScEV; ++e) {
-                db[e] = dnw[e] = 0.f;
+            for (int h = 0; h < 2; ++h) {
+                db[h] = dnw[h] = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int a = 0; a < kScAges; ++a) A[a][e] = 0.f;
+                for (int a = 0; a < kScAges; ++a) A[a][h] = make_float2(0.f, 0.f);
             }
         };
         finish_items(-1);  // clears the accumulators
@@ -902,9 +946,9 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
             }
             if (fl & kFlSegStart) {
 #pragma unroll
-                for (int e = 0; e < kScEV; ++e) {
-                    U[0][e] = U[1][e] = U[2][e] = U[3][e] = 0.f;
-                    P1[e] = P2[e] = P3[e] = 0.f;
+                for (int h = 0; h < 2; ++h) {
+                    U[0][h] = U[1][h] = U[2][h] = U[3][h] = make_float2(0.f, 0.f);
+                    P1[h] = P2[h] = P3[h] = make_float2(0.f, 0.f);
                 }
                 pend1 = pend2 = pend3 = false;
             }

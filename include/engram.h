@@ -368,10 +368,10 @@ engram_status engram_short_conv_num_partials(int64_t T, int32_t dilation, int32_
  * P = engram_short_conv_num_partials(T, dilation): row (chunk, class) holds, over that work item's
  * tokens, sum dc * u_tap for each tap i (rows 0..width-1), sum dc (row width) and
  * sum du * V~ * rstd (row width + 1), each token's terms in ascending time order.  Reduce it with
- * engram_short_conv_grad_reduce.  s sums, in this order: four channels, eight such groups, a
- * 32-lane butterfly (one 1024-channel block), then the ceil(d / 1024) blocks in ascending order.
- * One pass over dout and V~ on thread-block clusters of ceil(d / 1024) CTAs; dout, v, dv and
- * dw_partial 16-byte aligned.
+ * engram_short_conv_grad_reduce.  s sums, in this order: a thread's four channels as
+ * (c0 + c2) + (c1 + c3), four threads in order, a 32-lane butterfly (one 512-channel block), then
+ * the ceil(d / 512) blocks in ascending order.  One pass over dout and V~ on thread-block
+ * clusters of ceil(d / 512) CTAs; dout, v, dv and dw_partial 16-byte aligned.
  */
 engram_status engram_short_conv_bwd(const void *dout, const void *v, engram_dtype dtype, const float *norm_w,
                                     const float *conv_w, const float *bias, const float *rstd,
