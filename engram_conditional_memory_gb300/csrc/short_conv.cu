@@ -7,10 +7,11 @@
 // GB300 design.  The convolution couples tokens only along time, one channel at a time, and the
 // RMSNorm couples channels only within a token, through one scalar.  So:
 //   * conv_rstd_kernel: a warp per token computes rstd = 1/sqrt(mean(V~^2) + eps);
-//   * conv_fwd_kernel: persistent CTAs, each on one 512-byte channel block, stream tiles of 64
-//     tokens plus the taps' halo into shared memory with 1-D bulk (TMA) copies, two or three tiles
-//     in flight, and compute every output from the tile: the taps are read back from shared memory
-//     instead of being carried along time, so there is no per-token bookkeeping;
+//   * conv_fwd_sweep_kernel: CTAs on one 512-channel block sweep residue classes t = r (mod
+//     dilation) of short time chunks.  A producer warp streams each token's V~ and H row segments
+//     and rstd into a ring of shared-memory stages with a record of the position; every thread
+//     carries its four channels' last three taps' inputs in registers, so each row is converted
+//     once;
 //   * conv_bwd_kernel (the backward, one pass): a thread-block cluster of ceil(d / 1024) CTAs takes
 //     one residue class t = r (mod dilation) of one time chunk, each CTA 1024 channels.  Every tap of
 //     a class token lies in the same class, so the CTA sweeps its class tokens in time order, a
@@ -89,9 +90,21 @@ __device__ __forceinline__ float2 p2mul(float2 a, float2 b) { return __fmul2_rn(
 __device__ __forceinline__ float2 p2add(float2 a, float2 b) { return __fadd2_rn(a, b); }
 __device__ __forceinline__ float2 p2(float v) { return make_float2(v, v); }
 
-// SiLU's sigmoid with the fast exponential and division (a few ulp; the outputs are rounded far
-// coarser, and the tolerances carry the bound).
-__device__ __forceinline__ float sc_sigmoid_fast(float c) { return __fdividef(1.0f, 1.0f + __expf(-c)); }
+// sigmoid(c) = 1 / (1 + e^-c) on a channel pair, with e^-c = 2^(-c log2 e) from the hardware's
+// approximate base-2 exponential and the sum's approximate reciprocal (a few ulp each; flushed
+// denormals give the limits 0 and 1).  The outputs are rounded far coarser, and the tolerances carry
+// the bound.
+__device__ __forceinline__ float2 p2sigmoid(float2 c) {
+    const float2 z = p2mul(c, p2(-1.44269504088896340736f));
+    float e0, e1, r0, r1;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e0) : "f"(z.x));
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e1) : "f"(z.y));
+    const float2 den = p2add(make_float2(e0, e1), p2(1.0f));
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r0) : "f"(den.x));
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r1) : "f"(den.y));
+    return make_float2(r0, r1);
+}
+
 
 // Index of the sequence holding token t: the largest s with offs[s] <= t (offsets assumed sorted).
 __device__ __forceinline__ int sc_seq_of(const int64_t *offs, int num_seqs, int64_t t) {
@@ -125,206 +138,6 @@ __global__ void __launch_bounds__(256) conv_rstd_kernel(const uint8_t *__restric
         }
         ss = warp_sum(ss);
         if (lane == 0) rstd[t] = rsqrtf(ss / static_cast<float>(d) + eps);
-    }
-}
-
-// ------------------------------------------------------------------------------- forward
-
-constexpr int kScTileTokens = 64;       // tokens per forward tile
-constexpr int kScMaxDil = 32;           // forward: the halo of (width - 1) * dilation rows stays small
-
-// Shared memory of one tile buffer: rows [rows_max][32] uint4, rstd [rows_max], sequence starts
-// [kScTileTokens] int64; two buffers, then two mbarriers.
-__host__ __device__ inline int sc_fwd_buf_bytes(int width, int dil) {
-    const int rows = kScTileTokens + (width - 1) * dil;
-    // rounded to 128 bytes: the second buffer's rows are bulk-copy destinations (16-byte aligned)
-    return (rows * 512 + ((rows + 1) & ~1) * 4 + kScTileTokens * 8 + 127) & ~127;
-}
-// three tile buffers where they fit two CTAs per SM, else two
-inline int sc_fwd_nbuf(int width, int dil) { return 3 * sc_fwd_buf_bytes(width, dil) + 24 <= 113 * 1024 ? 3 : 2; }
-inline int sc_fwd_smem(int width, int dil) { return sc_fwd_nbuf(width, dil) * (sc_fwd_buf_bytes(width, dil) + 8); }
-
-struct ScFwdParams {
-    const uint8_t *v, *h;
-    const float *norm_w, *conv_w, *bias, *rstd;
-    const int64_t *offs;
-    uint8_t *out;
-    uint32_t *status;
-    int64_t T;
-    int32_t num_seqs, d, width, dil, nblk, ntiles, nbuf;
-};
-
-// Persistent CTAs, each on one channel block of 512 bytes (its taps, folded with norm_w, loaded
-// once) and the tiles j, j + J, ... of kScTileTokens tokens (J CTAs per block).  A tile's V~ rows and
-// the halo of (width - 1) * dilation rows before it reach shared memory by 1-D bulk (TMA) copies,
-// one row segment per lane of warp 0, completing on the buffer's mbarrier; the next one or two
-// tiles' copies are in flight while this one is computed.  Lane l of warp w computes channel vector l of the
-// tile's tokens w, w + 8, ...:
-//   conv = bias + sum_a (conv_w[width-1-a] norm_w) rstd[t - a dil] V~[t - a dil],
-//   out  = H + SiLU(conv) + V~,
-// with taps before the token's sequence start left out.
-template <typename E>
-__global__ void __launch_bounds__(256, 2) conv_fwd_kernel(const __grid_constant__ ScFwdParams p) {
-    using V = Vec<E>;
-    constexpr int N = V::N;
-    extern __shared__ __align__(128) uint8_t smem[];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int width = p.width, dil = p.dil;
-    const int halo = (width - 1) * dil;
-    const int rows_max = kScTileTokens + halo;
-    const int buf_bytes = sc_fwd_buf_bytes(width, dil);
-    const int nbuf = p.nbuf;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + static_cast<size_t>(nbuf) * buf_bytes);
-    const int nvec = p.d / N;
-    const int cb = static_cast<int>(blockIdx.x % p.nblk);
-    const int J = static_cast<int>(gridDim.x / p.nblk);
-    const int j0 = static_cast<int>(blockIdx.x / p.nblk);
-    if (j0 >= J) return;  // whole CTA: a grid that is not a multiple of the block count
-    const int jv = cb * 32 + lane;
-    const bool active = jv < nvec;
-    const int jv_c = active ? jv : 0;
-    const int nv_blk = nvec - cb * 32 < 32 ? nvec - cb * 32 : 32;
-    const uint32_t seg = static_cast<uint32_t>(nv_blk) * 16u;
-    const size_t row_bytes = static_cast<size_t>(nvec) * 16;
-
-    auto tile_rows = [&](int b) { return reinterpret_cast<uint4(*)[32]>(smem + static_cast<size_t>(b) * buf_bytes); };
-    auto tile_rs = [&](int b) {
-        return reinterpret_cast<float *>(smem + static_cast<size_t>(b) * buf_bytes + static_cast<size_t>(rows_max) * 512);
-    };
-    auto tile_ss = [&](int b) {
-        return reinterpret_cast<int64_t *>(smem + static_cast<size_t>(b) * buf_bytes +
-                                           static_cast<size_t>(rows_max) * 512 + ((rows_max + 1) & ~1) * 4);
-    };
-    // tile j covers tokens [j K, min(T, (j + 1) K)) and buffers rows from max(0, j K - halo)
-    auto first_row = [&](int j) {
-        const int64_t t0 = static_cast<int64_t>(j) * kScTileTokens;
-        return t0 - halo > 0 ? t0 - halo : static_cast<int64_t>(0);
-    };
-    auto tile_end = [&](int j) {
-        const int64_t t1 = (static_cast<int64_t>(j) + 1) * kScTileTokens;
-        return t1 < p.T ? t1 : p.T;
-    };
-    // start tile j's copies into buffer b (warp 0), and its rstd and sequence starts (all threads)
-    auto stage_tile = [&](int j, int b) {
-        const int64_t r0 = first_row(j), t0 = static_cast<int64_t>(j) * kScTileTokens, t1 = tile_end(j);
-        const int nrows = static_cast<int>(t1 - r0);
-        if (warp == 0) {
-            if (lane == 0) mbar_arrive_expect_tx(&bars[b], seg * static_cast<uint32_t>(nrows));
-            __syncwarp();
-            uint4(*rows)[32] = tile_rows(b);
-            for (int i = lane; i < nrows; i += 32)
-                bulk_load_plain(&rows[i][0], p.v + static_cast<size_t>(r0 + i) * row_bytes + static_cast<size_t>(cb) * 512,
-                                seg, &bars[b]);
-        }
-        float *rs = tile_rs(b);
-        for (int i = threadIdx.x; i < nrows; i += blockDim.x) rs[i] = __ldg(p.rstd + r0 + i);
-        if (threadIdx.x < t1 - t0) tile_ss(b)[threadIdx.x] = __ldg(p.offs + sc_seq_of(p.offs, p.num_seqs, t0 + threadIdx.x));
-    };
-
-    // this lane's channels: the taps by age folded with norm_w, and the bias (16-byte loads)
-    float KW[kScAges][N], bv[N];
-    {
-        float nw[N], cw[N][kScAges];
-        const float4 *nw4 = reinterpret_cast<const float4 *>(p.norm_w + static_cast<size_t>(jv_c) * N);
-        const float4 *b4 = p.bias ? reinterpret_cast<const float4 *>(p.bias + static_cast<size_t>(jv_c) * N) : nullptr;
-#pragma unroll
-        for (int q = 0; q < N / 4; ++q) {
-            const float4 a = __ldg(nw4 + q);
-            nw[4 * q] = a.x, nw[4 * q + 1] = a.y, nw[4 * q + 2] = a.z, nw[4 * q + 3] = a.w;
-            const float4 bb = b4 ? __ldg(b4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
-            bv[4 * q] = bb.x, bv[4 * q + 1] = bb.y, bv[4 * q + 2] = bb.z, bv[4 * q + 3] = bb.w;
-        }
-#pragma unroll
-        for (int e = 0; e < N; ++e) {
-            const size_t c = static_cast<size_t>(jv_c) * N + e;
-            if (width == kScAges) {
-                const float4 w4 = __ldg(reinterpret_cast<const float4 *>(p.conv_w + c * kScAges));
-                cw[e][0] = w4.x, cw[e][1] = w4.y, cw[e][2] = w4.z, cw[e][3] = w4.w;
-            } else {
-#pragma unroll
-                for (int i = 0; i < kScAges; ++i) cw[e][i] = i < width ? __ldg(p.conv_w + c * width + i) : 0.f;
-            }
-#pragma unroll
-            for (int a = 0; a < kScAges; ++a) KW[a][e] = a < width ? cw[e][width - 1 - a] * nw[e] : 0.f;
-        }
-    }
-    const uint4 *h4 = p.h ? reinterpret_cast<const uint4 *>(p.h) + jv_c : nullptr;
-    uint4 *o4 = reinterpret_cast<uint4 *>(p.out) + jv_c;
-
-    if (threadIdx.x == 0) {
-        for (int q = 0; q < nbuf; ++q) mbar_init(&bars[q], 1);
-        mbar_init_fence();
-    }
-    __syncthreads();
-    for (int q = 0; q < nbuf - 1 && j0 + q * J < p.ntiles; ++q) stage_tile(j0 + q * J, q);
-    __syncthreads();  // the first tiles' rstd and sequence starts
-
-    constexpr int kPer = kScTileTokens / 8;  // tokens per warp and tile, their H rows in two halves
-    constexpr int kHalf = kPer / 2;
-    int it = 0;
-    for (int j = j0; j < p.ntiles; j += J, ++it) {
-        const int b = it % nbuf;
-        const uint32_t phase = static_cast<uint32_t>((it / nbuf) & 1);
-        const int jn = j + (nbuf - 1) * J;
-        const int bn = (it + nbuf - 1) % nbuf;
-        if (jn < p.ntiles) stage_tile(jn, bn);  // freed by the previous tile's closing barrier
-        const int64_t t0 = static_cast<int64_t>(j) * kScTileTokens, t1 = tile_end(j), r0 = first_row(j);
-        uint4 hv[kHalf];
-        auto load_h = [&](int k0) {
-#pragma unroll
-            for (int k = 0; k < kHalf; ++k) {
-                const int64_t t = t0 + warp + 8 * (k0 + k);
-                hv[k] = (h4 && t < t1) ? __ldcs(h4 + static_cast<size_t>(t) * nvec) : make_uint4(0u, 0u, 0u, 0u);
-            }
-        };
-        load_h(0);
-        const bool ok = mbar_wait(&bars[b], phase);
-        if (__syncthreads_or(!ok)) {
-            // a copy that never landed: report, and let thread 0 wait (bounded) for what is in flight
-            if (threadIdx.x == 0) {
-                report(p.status, nullptr, ENGRAM_DEVERR_TIMEOUT);
-                for (int q = 0; q < nbuf - 1 && j + q * J < p.ntiles; ++q)
-                    mbar_wait(&bars[(it + q) % nbuf], static_cast<uint32_t>(((it + q) / nbuf) & 1));
-            }
-            return;
-        }
-        uint4(*rows)[32] = tile_rows(b);
-        const float *rs = tile_rs(b);
-        const int64_t *ss = tile_ss(b);
-#pragma unroll
-        for (int k = 0; k < kPer; ++k) {
-            if (k == kHalf) load_h(kHalf);
-            const int lt = warp + 8 * k;
-            const int64_t t = t0 + lt;
-            if (t >= t1) break;
-            const int64_t s0 = ss[lt];
-            float c[N], x0[N];
-#pragma unroll
-            for (int e = 0; e < N; ++e) c[e] = bv[e];
-#pragma unroll
-            for (int a = 0; a < kScAges; ++a) {
-                const int64_t ta = t - static_cast<int64_t>(a) * dil;
-                if (a < width && ta >= s0) {
-                    const int ri = static_cast<int>(ta - r0);
-                    float x[N];
-                    V::unpack(rows[ri][lane], x);
-                    const float ra = rs[ri];
-#pragma unroll
-                    for (int e = 0; e < N; ++e) c[e] = fmaf(KW[a][e], x[e] * ra, c[e]);
-                    if (a == 0) {
-#pragma unroll
-                        for (int e = 0; e < N; ++e) x0[e] = x[e];
-                    }
-                }
-            }
-            float y[N];
-            V::unpack(hv[k % kHalf], y);
-            float o[N];
-#pragma unroll
-            for (int e = 0; e < N; ++e) o[e] = fmaf(c[e], sc_sigmoid_fast(c[e]), x0[e] + y[e]);
-            if (active) __stcs(o4 + static_cast<size_t>(t) * nvec, V::pack(o));
-        }
-        __syncthreads();  // buffer b is free; the next tile's rstd and sequence starts are visible
     }
 }
 
@@ -429,16 +242,17 @@ __device__ __forceinline__ void sc_cp_async_arrive(uint64_t *bar) {
 
 // One segment of a work item: the class tokens first, first + dil, ... (n_main of them) of one
 // sequence inside the item's chunk, with the n_lead class tokens before them whose V~ the first
-// taps read, and the n_tail class tokens after them whose dc completes the last du.
+// taps read, and (backward) the n_tail class tokens after them whose dc completes the last du.
 struct ScSeg {
     int64_t first;
     int n_lead, n_main, n_tail;
 };
 
-// The next segment of class r in [x, t_hi); x and the sequence index s advance.  Offsets that are
-// not sorted still give progress and tokens inside [0, T).
-__device__ __forceinline__ bool sc_next_seg(const ScBwdParams &p, int r, int64_t t_hi, int64_t &x, int &s,
-                                            ScSeg &g) {
+// The next segment of class r in [x, t_hi), with up to tail_max look-ahead tokens; x and the
+// sequence index s advance.  Offsets that are not sorted still give progress and tokens inside [0, T).
+template <typename Prm>
+__device__ __forceinline__ bool sc_next_seg(const Prm &p, int r, int64_t t_hi, int64_t &x, int &s, ScSeg &g,
+                                            int tail_max = kBwLag) {
     const int64_t dil = p.dil;
     while (x < t_hi) {
         while (s + 1 < p.num_seqs && __ldg(p.offs + s + 1) <= x) ++s;
@@ -456,7 +270,7 @@ __device__ __forceinline__ bool sc_next_seg(const ScBwdParams &p, int r, int64_t
         g.n_main = static_cast<int>((last - first) / dil + 1);
         const int64_t lead = (first - s0) / dil, tail = (s1 - 1 - last) / dil;
         g.n_lead = static_cast<int>(lead < kBwLag ? lead : kBwLag);
-        g.n_tail = static_cast<int>(tail < kBwLag ? tail : kBwLag);
+        g.n_tail = static_cast<int>(tail < tail_max ? tail : tail_max);
         return true;
     }
     return false;
@@ -867,7 +681,7 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
                 const float2 c = p2fma(w[3][h], U[(J + 1) & 3][h],
                                        p2fma(w[2][h], U[(J + 2) & 3][h],
                                              p2fma(w[1][h], U[(J + 3) & 3][h], p2fma(w[0][h], U[J][h], bias[h]))));
-                const float2 sg = make_float2(sc_sigmoid_fast(c.x), sc_sigmoid_fast(c.y));
+                const float2 sg = p2sigmoid(c);
                 // SiLU'(c) = sg (1 + c (1 - sg))
                 dc[h] = p2mul(g[h], p2fma(sg, p2fma(make_float2(-c.x, -c.y), sg, c), sg));
             }
@@ -998,6 +812,304 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
     sc_cluster_sync();  // no CTA leaves while a peer may still write into its shared memory
 }
 
+// ------------------------------------------------------------------------------- forward, swept
+
+constexpr int kFwWarps = 4;                       // consumer warps, four channels per thread
+constexpr int kFwCons = kFwWarps * 32;
+constexpr int kFwThreads = kFwCons + 32;          // + the copy producer's warp
+constexpr int kFwCW = kFwCons * kScEV;            // channels per CTA (one channel block)
+constexpr int kFwStages = 16;
+constexpr int kFwChunk = 128;                     // tokens per work item's time chunk
+
+struct ScFwdSweepParams {
+    const uint8_t *v, *h;                         // V~, H (nullable) [T, d]
+    const float *norm_w, *conv_w, *bias, *rstd;
+    const int64_t *offs;
+    uint8_t *out;
+    uint32_t *status;
+    int64_t T;
+    int64_t chunk;
+    int64_t items;                                // per channel block: chunks x dilation
+    int32_t num_seqs, d, width, dil, nblk, per_blk;  // per_blk: CTAs per channel block
+};
+
+template <typename E>
+__host__ __device__ constexpr int sc_fwd_stage_bytes() {
+    return 2 * kFwCW * static_cast<int>(sizeof(E));  // the V~ segment, then the H segment
+}
+// the ring, the stages' position records, full and empty mbarriers, the producer's state
+template <typename E>
+__host__ __device__ constexpr int sc_fwd_sweep_smem() {
+    return kFwStages * sc_fwd_stage_bytes<E>() + kFwStages * 16 + 2 * kFwStages * 8 + 128;
+}
+
+// The forward as a sweep.  CTA (block cb, j) owns channels [512 cb, 512 cb + 512) and the work items
+// j, j + per_blk, ... of that block, each one residue class t = r mod dilation of one time chunk.
+// Its producer warp walks the items' segments and streams, per sweep position, the token's V~ and
+// H row segments (1-D bulk copies) and rstd (a 4-byte asynchronous copy) into a ring of stages,
+// with a record of the position; a segment starts with up to three lead-in tokens whose V~ the
+// first taps read.  Every consumer thread owns four channels (two pairs) and carries the last three
+// taps' inputs u = V~ rstd in registers (slot q mod 4 for position q), so each row is converted
+// once:
+//   conv = bias + sum_a (conv_w[width-1-a] norm_w) u[t - a dil]   (a = 0, 1, 2, 3 in order),
+//   out  = H + SiLU(conv) + V~,
+// the taps before a sequence's start being zero.  All waits are bounded.
+template <typename E>
+__global__ void __launch_bounds__(kFwThreads, 6) conv_fwd_sweep_kernel(const __grid_constant__ ScFwdSweepParams p) {
+    using EV = Ev4<E>;
+    extern __shared__ __align__(128) uint8_t smem[];
+    constexpr int S = kFwStages;
+    constexpr int SB = sc_fwd_stage_bytes<E>();
+    constexpr int half = SB / 2;
+    uint8_t *ring = smem;
+    ScMeta *meta = reinterpret_cast<ScMeta *>(smem + static_cast<size_t>(S) * SB);
+    uint64_t *full = reinterpret_cast<uint64_t *>(meta + S);
+    uint64_t *empty = full + S;
+    ScProd *prod = reinterpret_cast<ScProd *>(empty + S);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int cb = static_cast<int>(blockIdx.x % p.nblk);
+    const int j0 = static_cast<int>(blockIdx.x / p.nblk);
+    const int c0 = cb * kFwCW;
+    const int ncols = p.d - c0 < kFwCW ? p.d - c0 : kFwCW;
+    const int64_t dil = p.dil;
+    bool failed = false;
+
+    if (tid == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(&full[i], 2);  // the producer's arrival and its rstd copy's
+            mbar_init(&empty[i], kFwWarps);
+        }
+        mbar_init_fence();
+    }
+    __syncthreads();
+    pdl_wait();
+
+    if (warp == kFwWarps) {
+        // ---- the producer warp: one position per lane as stages free up, then the sentinel
+        ScProd &P = *prod;
+        auto start_item = [&](int64_t item) {  // item: k * dil + r of this block
+            const int64_t t_lo = item / dil * p.chunk;
+            P.item = item;
+            P.xs = t_lo;
+            P.t_hi = t_lo + p.chunk < p.T ? t_lo + p.chunk : p.T;
+            P.s = sc_seq_of(p.offs, p.num_seqs, t_lo);
+        };
+        auto next_seg = [&]() {  // lane 0
+            ScSeg g;
+            for (;;) {
+                int64_t xs = P.xs;
+                int s = P.s;
+                const bool found = sc_next_seg(p, static_cast<int>(P.item % dil), P.t_hi, xs, s, g, 0);
+                P.xs = xs;
+                P.s = s;
+                if (found) {
+                    P.q = 0;
+                    P.n = g.n_lead + g.n_main;
+                    P.n_lead = g.n_lead;
+                    P.t = g.first - g.n_lead * dil;
+                    return;
+                }
+                const int64_t next = P.item + p.per_blk;
+                if (next >= p.items) {
+                    P.state = 1;
+                    return;
+                }
+                start_item(next);
+            }
+        };
+        if (lane == 0) {
+            P = ScProd{};
+            if (j0 >= p.items) {
+                P.state = 1;
+            } else {
+                start_item(j0);
+                next_seg();
+            }
+        }
+        __syncwarp();
+        const uint32_t seg = static_cast<uint32_t>(ncols) * sizeof(E);
+        const size_t row_bytes = static_cast<size_t>(p.d) * sizeof(E);
+        const uint8_t *src_v = p.v + static_cast<size_t>(c0) * sizeof(E);
+        const uint8_t *src_h = p.h ? p.h + static_cast<size_t>(c0) * sizeof(E) : nullptr;
+        int st = 0, state = P.state;
+        uint32_t round = 0, issued = 0;
+        int q = P.q, n = P.n, nl = P.n_lead;
+        int64_t t = P.t;
+        while (state != 2) {
+            const int stl = st + lane < S ? st + lane : st + lane - S;
+            const uint32_t rl = round + (st + lane < S ? 0u : 1u);
+            const bool free_l = lane < S && (rl == 0 || mbar_test_wait(&empty[stl], (rl + 1) & 1u));
+            const uint32_t mask = __ballot_sync(0xffffffffu, free_l);
+            int cnt = __ffs(~mask) - 1;
+            if (cnt < 0) cnt = 32;
+            if (cnt == 0) {  // the ring is full: wait (bounded) for its oldest stage
+                bool ok = true;
+                if (lane == 0) ok = mbar_wait_sleep(&empty[st], (round + 1) & 1u);
+                if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                    if (lane == 0) report(p.status, nullptr, ENGRAM_DEVERR_TIMEOUT);
+                    failed = true;
+                    break;
+                }
+                continue;
+            }
+            if (state == 1) {  // the sentinel: no copies, both arrivals
+                if (lane == 0) {
+                    meta[st].tok = 0;
+                    meta[st].flags = kFlDone;
+                    mbar_arrive(&full[st]);
+                    mbar_arrive(&full[st]);
+                }
+                state = 2;
+                cnt = 1;
+            } else {
+                if (cnt > n - q) cnt = n - q;
+                if (lane < cnt) {
+                    const int ql = q + lane;
+                    const int64_t tl = t + lane * dil;
+                    const bool lead = ql < nl;
+                    const bool group = (ql & 3) == 0 && ql >= nl && ql + 4 <= n;
+                    uint32_t fl = (lead ? kScLead : kScMain) | (static_cast<uint32_t>(ql & 3) << kFlSlotShift);
+                    if (ql == 0) fl |= kFlSegStart;
+                    if (group) fl |= kFlGroup;
+                    meta[stl].tok = tl;
+                    meta[stl].flags = fl;
+                    uint8_t *dst = ring + static_cast<size_t>(stl) * SB;
+                    const bool with_h = !lead && src_h;
+                    sc_cp_async4(&meta[stl].rstd, p.rstd + tl);
+                    sc_cp_async_arrive(&full[stl]);
+                    mbar_arrive_expect_tx(&full[stl], with_h ? 2 * seg : seg);
+                    bulk_load_plain(dst, src_v + static_cast<size_t>(tl) * row_bytes, seg, &full[stl]);
+                    if (with_h)
+                        bulk_load(dst + half, src_h + static_cast<size_t>(tl) * row_bytes, seg, &full[stl],
+                                  l2_evict_first_policy());
+                }
+                q += cnt;
+                t += cnt * dil;
+                if (q == n) {
+                    __syncwarp();
+                    if (lane == 0) next_seg();
+                    __syncwarp();
+                    state = P.state, q = P.q, n = P.n, nl = P.n_lead, t = P.t;
+                }
+            }
+            issued += cnt;
+            st += cnt;
+            if (st >= S) st -= S, ++round;
+        }
+        // after a failure, copies may still be landing: wait for them (bounded) before the CTA leaves
+        if (failed && lane == 0)
+            for (uint32_t q2 = issued > static_cast<uint32_t>(S) ? issued - S : 0; q2 < issued; ++q2)
+                mbar_wait(&full[q2 % S], (q2 / S) & 1u, kWaitLimitNs / 16);
+    } else {
+        // ---- consumers
+        const bool active = tid * kScEV < ncols;
+        const int width = p.width, d = p.d;
+        float2 K[kScAges][2], bias[2];  // taps by age folded with norm_w; [h]: channels 2h, 2h + 1
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            float v[2][1 + kScAges];
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const int c = c0 + tid * kScEV + 2 * h + k;
+                const bool ok = active && c < d;
+                const float nwc = ok ? __ldg(p.norm_w + c) : 0.f;
+                v[k][0] = ok && p.bias ? __ldg(p.bias + c) : 0.f;
+#pragma unroll
+                for (int a = 0; a < kScAges; ++a)
+                    v[k][1 + a] =
+                        ok && a < width ? __ldg(p.conv_w + static_cast<size_t>(c) * width + (width - 1 - a)) * nwc : 0.f;
+            }
+            bias[h] = make_float2(v[0][0], v[1][0]);
+#pragma unroll
+            for (int a = 0; a < kScAges; ++a) K[a][h] = make_float2(v[0][1 + a], v[1][1 + a]);
+        }
+        const size_t row_bytes = static_cast<size_t>(d) * sizeof(E);
+        uint8_t *out_col = p.out + static_cast<size_t>(c0) * sizeof(E) + tid * EV::kBytes;
+        const bool has_h = p.h != nullptr;
+        float2 U[4][2];  // u = V~ rstd by slot
+        int st = 0;
+        uint32_t ph = 0;
+
+        auto wait_warp = [&](uint64_t *bar, uint32_t parity) {
+            if (failed) return;
+            if (!__all_sync(0xffffffffu, mbar_wait_sleep(bar, parity))) {
+                if (lane == 0) report(p.status, nullptr, ENGRAM_DEVERR_TIMEOUT);
+                failed = true;
+            }
+        };
+        auto advance = [&]() {
+            if (++st == S) st = 0, ph ^= 1u;
+        };
+        // one position in slot J, its stage already waited for; GROUP: its stage is released with
+        // the group's
+        auto step = [&](auto Jc, auto Gc, bool lead) {
+            constexpr bool GROUP = decltype(Gc)::v != 0;
+            constexpr int J = decltype(Jc)::v;
+            const uint8_t *stg = ring + static_cast<size_t>(st) * SB + tid * EV::kBytes;
+            const float2 rt = p2(meta[st].rstd);
+            float2 x[2];
+            EV::load2(stg, x);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) U[J][h] = p2mul(x[h], rt);
+            if (!lead) {
+                float2 y[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                if (has_h) EV::load2(stg + half, y);
+                float2 o[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const float2 c = p2fma(K[3][h], U[(J + 1) & 3][h],
+                                           p2fma(K[2][h], U[(J + 2) & 3][h],
+                                                 p2fma(K[1][h], U[(J + 3) & 3][h], p2fma(K[0][h], U[J][h], bias[h]))));
+                    o[h] = p2fma(c, p2sigmoid(c), p2add(x[h], y[h]));
+                }
+                if (active) EV::store2(out_col + static_cast<size_t>(meta[st].tok) * row_bytes, o);
+            }
+            if (!GROUP) {
+                __syncwarp();
+                if (lane == 0 && !failed) mbar_arrive(&empty[st]);
+            }
+            advance();
+        };
+
+        for (;;) {
+            wait_warp(&full[st], ph);
+            if (failed) break;
+            const uint32_t fl = meta[st].flags;
+            if (fl & kFlDone) break;
+            if (fl & kFlSegStart) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) U[0][h] = U[1][h] = U[2][h] = U[3][h] = make_float2(0.f, 0.f);
+            }
+            if (fl & kFlGroup) {
+                // all four stages first, so that the four positions' loads and arithmetic may overlap
+#pragma unroll
+                for (int k = 1; k < 4; ++k) {
+                    const bool wrap = st + k >= S;
+                    wait_warp(&full[wrap ? st + k - S : st + k], wrap ? ph ^ 1u : ph);
+                }
+                if (failed) break;
+                const int st0 = st;
+                step(ScIdx<0>{}, ScIdx<1>{}, false);
+                step(ScIdx<1>{}, ScIdx<1>{}, false);
+                step(ScIdx<2>{}, ScIdx<1>{}, false);
+                step(ScIdx<3>{}, ScIdx<1>{}, false);
+                __syncwarp();  // the group's four stages at once, one lane each
+                if (lane < 4 && !failed) mbar_arrive(&empty[st0 + lane < S ? st0 + lane : st0 + lane - S]);
+            } else {
+                const bool lead = (fl & kFlKind) == kScLead;
+                switch ((fl >> kFlSlotShift) & 3u) {
+                    case 0: step(ScIdx<0>{}, ScIdx<0>{}, lead); break;
+                    case 1: step(ScIdx<1>{}, ScIdx<0>{}, lead); break;
+                    case 2: step(ScIdx<2>{}, ScIdx<0>{}, lead); break;
+                    default: step(ScIdx<3>{}, ScIdx<0>{}, lead); break;
+                }
+            }
+        }
+    }
+}
+
 // ------------------------------------------------------------------------------- weight-gradient reduction
 
 constexpr int kScRG = 64;
@@ -1115,6 +1227,39 @@ engram_status sc_bwd_launch(const char *fn, ScBwdParams prm, const DeviceInfo &d
     return check_launch(fn);
 }
 
+// The swept forward: nblk channel blocks x per_blk CTAs, as many as fit at once, with per_blk
+// chosen so that every CTA of a block takes the same number of work items.
+template <typename E>
+engram_status sc_fwd_launch(const char *fn, ScFwdSweepParams fp, const DeviceInfo &dev, cudaStream_t s) {
+    void (*kern)(ScFwdSweepParams) = conv_fwd_sweep_kernel<E>;
+    const int smem = sc_fwd_sweep_smem<E>();
+    engram_status st = set_smem(reinterpret_cast<const void *>(kern), smem);
+    if (st != ENGRAM_OK) return st;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared) !=
+        cudaSuccess)
+        return check_launch(fn);
+    static std::atomic<int> cached[kScDevices][2];
+    std::atomic<int> &slot = cached[dev.device % kScDevices][sizeof(E) == 4 ? 1 : 0];
+    int per_sm = slot.load(std::memory_order_relaxed);
+    if (per_sm <= 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kFwThreads, smem) != cudaSuccess ||
+            per_sm < 1) {
+            cudaGetLastError();
+            return fail(ENGRAM_ERR_CUDA, "%s: no CTA of %d bytes of shared memory fits", fn, smem);
+        }
+        slot.store(per_sm, std::memory_order_relaxed);
+    }
+    const int64_t cap = std::max<int64_t>(1, cap_grid(static_cast<int64_t>(per_sm) * dev.num_sms) / fp.nblk);
+    const int64_t rounds = (fp.items + cap - 1) / cap;
+    const int64_t per_blk = std::max<int64_t>(1, (fp.items + rounds - 1) / rounds);
+    fp.per_blk = static_cast<int32_t>(per_blk);
+    const int64_t grid = per_blk * fp.nblk;
+    if (grid > 0x7fffffff) return fail(ENGRAM_ERR_SHAPE, "%s: too many CTAs", fn);
+    cudaError_t e = launch_kernel(kern, dim3(static_cast<unsigned>(grid)), dim3(kFwThreads), smem, s, fp);
+    (void)e;
+    return check_launch(fn);
+}
+
 }  // namespace
 }  // namespace engram
 
@@ -1142,7 +1287,6 @@ extern "C" engram_status engram_short_conv_fwd(const void *v, const void *h, eng
     if (!norm_w || !conv_w || !seq_offsets) return fail(ENGRAM_ERR_NULL, "%s: NULL pointer", fn);
     if (T == 0) return ENGRAM_OK;
     if (!v || !out || !rstd) return fail(ENGRAM_ERR_NULL, "%s: NULL pointer", fn);
-    if (dilation > kScMaxDil) return fail(ENGRAM_ERR_SHAPE, "%s: dilation = %d exceeds %d", fn, dilation, kScMaxDil);
     if (out == v) return fail(ENGRAM_ERR_SHAPE, "%s: out may not alias V~ (later tokens read it as taps)", fn);
     const void *ptrs[] = {v, h, out, norm_w, conv_w, bias, seq_offsets, rstd};
     DeviceInfo dev;
@@ -1156,8 +1300,7 @@ extern "C" engram_status engram_short_conv_fwd(const void *v, const void *h, eng
         conv_rstd_kernel<__nv_bfloat16><<<static_cast<unsigned>(rgrid), 256, 0, s>>>(static_cast<const uint8_t *>(v),
                                                                                     T, d, eps, rstd);
     if ((st = check_launch(fn)) != ENGRAM_OK) return st;
-    const int nvec = static_cast<int>(static_cast<int64_t>(d) * dtype_size(dtype) / 16);
-    ScFwdParams fp{};
+    ScFwdSweepParams fp{};
     fp.v = static_cast<const uint8_t *>(v);
     fp.h = static_cast<const uint8_t *>(h);
     fp.norm_w = norm_w;
@@ -1168,29 +1311,14 @@ extern "C" engram_status engram_short_conv_fwd(const void *v, const void *h, eng
     fp.out = static_cast<uint8_t *>(out);
     fp.status = dev.status_word;
     fp.T = T;
+    fp.chunk = kFwChunk;
+    fp.items = (T + kFwChunk - 1) / kFwChunk * dilation;
     fp.num_seqs = num_seqs;
     fp.d = d;
     fp.width = width;
     fp.dil = dilation;
-    fp.nblk = (nvec + 31) / 32;
-    const int64_t ntiles = (T + kScTileTokens - 1) / kScTileTokens;
-    if (ntiles > 0x7fffffff) return fail(ENGRAM_ERR_SHAPE, "%s: too many tokens", fn);
-    fp.ntiles = static_cast<int32_t>(ntiles);
-    fp.nbuf = sc_fwd_nbuf(width, dilation);
-    // two CTAs per SM, each on one channel block; J CTAs share a block's tiles
-    const int64_t per_block = std::max<int64_t>(1, std::min<int64_t>(ntiles, (2 * dev.num_sms + fp.nblk - 1) / fp.nblk));
-    const int64_t grid = cap_grid(per_block * fp.nblk) / fp.nblk * fp.nblk;
-    if (grid < fp.nblk) return fail(ENGRAM_ERR_SHAPE, "%s: the CTA cap is below %d channel blocks", fn, fp.nblk);
-    const int smem = sc_fwd_smem(width, dilation);
-    if (dtype == ENGRAM_F32) {
-        if ((st = set_smem(reinterpret_cast<const void *>(conv_fwd_kernel<float>), smem)) != ENGRAM_OK) return st;
-        conv_fwd_kernel<float><<<static_cast<unsigned>(grid), 256, smem, s>>>(fp);
-    } else {
-        if ((st = set_smem(reinterpret_cast<const void *>(conv_fwd_kernel<__nv_bfloat16>), smem)) != ENGRAM_OK)
-            return st;
-        conv_fwd_kernel<__nv_bfloat16><<<static_cast<unsigned>(grid), 256, smem, s>>>(fp);
-    }
-    return check_launch(fn);
+    fp.nblk = (d + kFwCW - 1) / kFwCW;
+    return dtype == ENGRAM_F32 ? sc_fwd_launch<float>(fn, fp, dev, s) : sc_fwd_launch<__nv_bfloat16>(fn, fp, dev, s);
 }
 
 extern "C" engram_status engram_short_conv_bwd(const void *dout, const void *v, engram_dtype dtype,

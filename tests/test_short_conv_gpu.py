@@ -2,7 +2,7 @@
 against the CPU oracle, through the C ABI.
 
 Sizes: small packed batches (ragged and empty sequences, several time chunks, channel blocks with a
-ragged last block, widths 1 to 4, dilations 1 to 5, with and without H and bias, both dtypes, d up to
+ragged last block, widths 1 to 4, dilations 1 to 5 and 40, with and without H and bias, both dtypes, d up to
 the largest supported 8192); the 4 x 4096-token, d = 4096 bf16 workload element by element; edge
 cases (no token, in-place output) and bitwise reruns.
 
@@ -170,6 +170,7 @@ def _check(r, x, wl, f, b):
     ([5, 2], 8192, 4, 3, "bf16", True, True),
     ([300, 77], 512, 1, 3, "bf16", True, True),
     ([600], 1000, 4, 2, "bf16", True, False),
+    ([500, 1, 300], 64, 4, 40, "bf16", True, True),
 ])
 def test_small_cases(lengths, d, width, dil, dtype, bias, with_h):
     wl = W.ShortConvWorkload(name="t", lengths=lengths, d=d, width=width, dilation=dil, dtype=dtype,
