@@ -549,6 +549,27 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
                 failed = true;
             }
         };
+        // stages st + k0 .. st + k1 - 1 full: every lane tries them all back to back and the warp
+        // agrees; only when one is still filling, every lane waits for it (bounded)
+        auto wait_stages = [&](int k0, int k1) {
+            if (failed) return;
+            bool ok = true;
+#pragma unroll 4
+            for (int k = k0; k < k1; ++k) {
+                const bool wrap = st + k >= S;
+                ok &= mbar_try_wait(&full[wrap ? st + k - S : st + k], wrap ? ph ^ 1u : ph);
+            }
+            if (__all_sync(0xffffffffu, ok)) return;
+            ok = true;
+            for (int k = k0; k < k1; ++k) {
+                const bool wrap = st + k >= S;
+                ok = ok && mbar_wait_sleep(&full[wrap ? st + k - S : st + k], wrap ? ph ^ 1u : ph);
+            }
+            if (!__all_sync(0xffffffffu, ok)) {
+                if (lane == 0) report(p.status, nullptr, ENGRAM_DEVERR_TIMEOUT);
+                failed = true;
+            }
+        };
         auto advance = [&]() {
             if (++st == S) st = 0, ph ^= 1u;
             ++gpos;
@@ -557,7 +578,7 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
         // after a failure a warp arrives on no barrier and sends nothing: no phase can be overrun
         auto release = [&](int stage) {
             __syncwarp();
-            if (lane == 0 && !failed) mbar_arrive(&empty[stage]);
+            mbar_arrive_if(&empty[stage], lane == 0 && !failed);
         };
         // a token `a` positions back has its du: its y, row-dot part and norm-weight gradient
         auto complete = [&](int a, const float2 (&du)[2]) {
@@ -617,7 +638,7 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
                 }
             }
             __syncwarp();
-            if (lane < n && !failed) mbar_arrive(&empty[sj_l]);
+            mbar_arrive_if(&empty[sj_l], lane < n && !failed);
         };
         // the open batch is complete: this warp's parts are counted in, and the warp that completes the
         // count sums the CTA's row dots (thread order, then lanes) and sends them to the cluster --
@@ -749,7 +770,7 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
         finish_items(-1);  // clears the accumulators
 
         for (;;) {
-            wait_warp(&full[st], ph);
+            wait_stages(0, 1);
             if (failed) break;
             const uint32_t fl = meta[st].flags;
             if (fl & kFlDone) break;
@@ -769,11 +790,7 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
             if (fl & kFlGroup) {
                 if (nfin > 0) post();  // a steady group fills one batch of its own
                 // all four stages first, so that the four positions' loads and arithmetic may overlap
-#pragma unroll
-                for (int k = 1; k < 4; ++k) {
-                    const bool wrap = st + k >= S;
-                    wait_warp(&full[wrap ? st + k - S : st + k], wrap ? ph ^ 1u : ph);
-                }
+                wait_stages(1, 4);
                 if (failed) break;
                 step(ScIdx<0>{}, ScIdx<1>{}, kScMain);
                 step(ScIdx<1>{}, ScIdx<1>{}, kScMain);
@@ -854,7 +871,7 @@ __host__ __device__ constexpr int sc_fwd_sweep_smem() {
 //   conv = bias + sum_a (conv_w[width-1-a] norm_w) u[t - a dil]   (a = 0, 1, 2, 3 in order),
 //   out  = H + SiLU(conv) + V~,
 // the taps before a sequence's start being zero.  All waits are bounded.
-template <typename E>
+template <typename E, bool HAS_H>
 __global__ void __launch_bounds__(kFwThreads, 6) conv_fwd_sweep_kernel(const __grid_constant__ ScFwdSweepParams p) {
     using EV = Ev4<E>;
     extern __shared__ __align__(128) uint8_t smem[];
@@ -1027,14 +1044,27 @@ __global__ void __launch_bounds__(kFwThreads, 6) conv_fwd_sweep_kernel(const __g
         }
         const size_t row_bytes = static_cast<size_t>(d) * sizeof(E);
         uint8_t *out_col = p.out + static_cast<size_t>(c0) * sizeof(E) + tid * EV::kBytes;
-        const bool has_h = p.h != nullptr;
         float2 U[4][2];  // u = V~ rstd by slot
         int st = 0;
         uint32_t ph = 0;
 
-        auto wait_warp = [&](uint64_t *bar, uint32_t parity) {
+        // stages st + k0 .. st + k1 - 1 full: every lane tries them all back to back and the warp
+        // agrees; only when one is still filling, every lane waits for it (bounded)
+        auto wait_stages = [&](int k0, int k1) {
             if (failed) return;
-            if (!__all_sync(0xffffffffu, mbar_wait_sleep(bar, parity))) {
+            bool ok = true;
+#pragma unroll 4
+            for (int k = k0; k < k1; ++k) {
+                const bool wrap = st + k >= S;
+                ok &= mbar_try_wait(&full[wrap ? st + k - S : st + k], wrap ? ph ^ 1u : ph);
+            }
+            if (__all_sync(0xffffffffu, ok)) return;
+            ok = true;
+            for (int k = k0; k < k1; ++k) {
+                const bool wrap = st + k >= S;
+                ok = ok && mbar_wait_sleep(&full[wrap ? st + k - S : st + k], wrap ? ph ^ 1u : ph);
+            }
+            if (!__all_sync(0xffffffffu, ok)) {
                 if (lane == 0) report(p.status, nullptr, ENGRAM_DEVERR_TIMEOUT);
                 failed = true;
             }
@@ -1055,7 +1085,7 @@ __global__ void __launch_bounds__(kFwThreads, 6) conv_fwd_sweep_kernel(const __g
             for (int h = 0; h < 2; ++h) U[J][h] = p2mul(x[h], rt);
             if (!lead) {
                 float2 y[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-                if (has_h) EV::load2(stg + half, y);
+                if (HAS_H) EV::load2(stg + half, y);
                 float2 o[2];
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
@@ -1068,27 +1098,23 @@ __global__ void __launch_bounds__(kFwThreads, 6) conv_fwd_sweep_kernel(const __g
             }
             if (!GROUP) {
                 __syncwarp();
-                if (lane == 0 && !failed) mbar_arrive(&empty[st]);
+                mbar_arrive_if(&empty[st], lane == 0 && !failed);
             }
             advance();
         };
 
         for (;;) {
-            wait_warp(&full[st], ph);
+            wait_stages(0, 1);
             if (failed) break;
             const uint32_t fl = meta[st].flags;
-            if (fl & kFlDone) break;
-            if (fl & kFlSegStart) {
+            if (fl & (kFlDone | kFlSegStart)) {
+                if (fl & kFlDone) break;
 #pragma unroll
                 for (int h = 0; h < 2; ++h) U[0][h] = U[1][h] = U[2][h] = U[3][h] = make_float2(0.f, 0.f);
             }
             if (fl & kFlGroup) {
                 // all four stages first, so that the four positions' loads and arithmetic may overlap
-#pragma unroll
-                for (int k = 1; k < 4; ++k) {
-                    const bool wrap = st + k >= S;
-                    wait_warp(&full[wrap ? st + k - S : st + k], wrap ? ph ^ 1u : ph);
-                }
+                wait_stages(1, 4);
                 if (failed) break;
                 const int st0 = st;
                 step(ScIdx<0>{}, ScIdx<1>{}, false);
@@ -1096,7 +1122,8 @@ __global__ void __launch_bounds__(kFwThreads, 6) conv_fwd_sweep_kernel(const __g
                 step(ScIdx<2>{}, ScIdx<1>{}, false);
                 step(ScIdx<3>{}, ScIdx<1>{}, false);
                 __syncwarp();  // the group's four stages at once, one lane each
-                if (lane < 4 && !failed) mbar_arrive(&empty[st0 + lane < S ? st0 + lane : st0 + lane - S]);
+                mbar_arrive_if(&empty[st0 + (lane & 3) < S ? st0 + (lane & 3) : st0 + (lane & 3) - S],
+                               lane < 4 && !failed);
             } else {
                 const bool lead = (fl & kFlKind) == kScLead;
                 switch ((fl >> kFlSlotShift) & 3u) {
@@ -1231,15 +1258,15 @@ engram_status sc_bwd_launch(const char *fn, ScBwdParams prm, const DeviceInfo &d
 // chosen so that every CTA of a block takes the same number of work items.
 template <typename E>
 engram_status sc_fwd_launch(const char *fn, ScFwdSweepParams fp, const DeviceInfo &dev, cudaStream_t s) {
-    void (*kern)(ScFwdSweepParams) = conv_fwd_sweep_kernel<E>;
+    void (*kern)(ScFwdSweepParams) = fp.h ? conv_fwd_sweep_kernel<E, true> : conv_fwd_sweep_kernel<E, false>;
     const int smem = sc_fwd_sweep_smem<E>();
     engram_status st = set_smem(reinterpret_cast<const void *>(kern), smem);
     if (st != ENGRAM_OK) return st;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared) !=
         cudaSuccess)
         return check_launch(fn);
-    static std::atomic<int> cached[kScDevices][2];
-    std::atomic<int> &slot = cached[dev.device % kScDevices][sizeof(E) == 4 ? 1 : 0];
+    static std::atomic<int> cached[kScDevices][2][2];
+    std::atomic<int> &slot = cached[dev.device % kScDevices][sizeof(E) == 4 ? 1 : 0][fp.h ? 1 : 0];
     int per_sm = slot.load(std::memory_order_relaxed);
     if (per_sm <= 0) {
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kFwThreads, smem) != cudaSuccess ||
