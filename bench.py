@@ -599,11 +599,13 @@ def main_only(args, device):
 
             def launch():
                 ecm.gate_bwd(t["dout"], t["h"], t["k"], t["v"], wf, *st, P=P, dh=dh, dk=dk, dv=dv, dw_partial=part)
-        elif op == "grad_w_reduce":
-            nbytes = P * wl.d * 4 + wl.d * 4
+        elif op == "grad_w_reduce":  # the step's launch: four micro-batches' partials, both weight gradients
+            part4 = part.repeat(4, 1)
+            gh, gk = torch.zeros_like(t["w_h"]), torch.zeros_like(t["w_k"])
+            nbytes = 4 * P * wl.d * 4 + 7 * wl.d * 4
 
             def launch():
-                ecm.grad_w_reduce(part, dweight_fused=wf)
+                ecm.grad_w_reduce(part4, dweight_fused=wf, w_h=t["w_h"], w_k=t["w_k"], grad_w_h=gh, grad_w_k=gk)
         else:  # gate_fwd on T=16384 d=4096, or gate_fwd_2k on T=8192 d=2048
             nbytes = wl.T * (8 * wl.d + 16)
 
