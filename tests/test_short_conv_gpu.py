@@ -181,6 +181,17 @@ def test_small_cases(lengths, d, width, dil, dtype, bias, with_h):
     _check(r, x, wl, f, b)
 
 
+def test_long_sequences_larger_chunks():
+    """T above 65,536: the backward's chunks grow beyond 256 tokens (L = ceil(T / 256)), 256 of them."""
+    wl = W.ShortConvWorkload(name="long", lengths=[40000, 3, 30001], d=64, width=4, dilation=3, dtype="bf16",
+                             seed=97, bias=True, with_h=True)
+    x = W.short_conv_host_inputs(wl)
+    r = _run(x, wl)
+    assert r["part"].shape[0] == 256 * 3
+    f, b = _oracle(x, wl, threads=16)
+    _check(r, x, wl, f, b)
+
+
 def test_full_workload_every_element():
     wl = W.short_conv_4x4k()
     x = W.short_conv_host_inputs(wl)
