@@ -276,10 +276,10 @@ __device__ __forceinline__ bool sc_next_seg(const Prm &p, int r, int64_t t_hi, i
     return false;
 }
 
-// What the producer tells the consumers about each sweep position, beside its stage: the token,
-// its rstd (copied asynchronously) and flags.
+// What the producer tells the consumers about each sweep position, beside its stage: the byte
+// offset of the token's row in a [T, d] tensor, its rstd (copied asynchronously) and flags.
 struct ScMeta {
-    int64_t tok;
+    int64_t row;
     float rstd;
     uint32_t flags;
 };
@@ -421,7 +421,7 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
             }
             if (state == 1) {  // the sentinel: no copies, both arrivals
                 if (lane == 0) {
-                    meta[st].tok = 0;
+                    meta[st].row = 0;
                     meta[st].flags = kFlDone;
                     mbar_arrive(&full[st]);
                     mbar_arrive(&full[st]);
@@ -440,7 +440,7 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
                     if (ql == n - 1) fl |= kFlSegEnd;
                     if (group) fl |= kFlGroup;
                     if (new_item && lane == 0) fl |= kFlItemStart | item_fl;
-                    meta[stl].tok = tl;
+                    meta[stl].row = tl * static_cast<int64_t>(row_bytes);
                     meta[stl].flags = fl;
                     uint8_t *dst = ring + static_cast<size_t>(stl) * SB;
                     sc_cp_async4(&meta[stl].rstd, p.rstd + tl);
@@ -509,6 +509,7 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
     } else {
 
         const bool active = tid * kScEV < ncols;
+        const uint8_t *my_ring = ring + tid * EV::kBytes;  // this thread's channels in stage 0
         const int width = p.width, d = p.d;
         // the thread's four channels as two pairs: [h] holds channels 2h and 2h + 1
         float2 w[kScAges][2], nw[2], bias[2];
@@ -583,7 +584,7 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
         // a token `a` positions back has its du: its y, row-dot part and norm-weight gradient
         auto complete = [&](int a, const float2 (&du)[2]) {
             const int sa = back(a);
-            const uint8_t *stg = ring + static_cast<size_t>(sa) * SB + tid * EV::kBytes;
+            const uint8_t *stg = my_ring + sa * SB;
             float2 x[2], g[2], dn[2], y[2];
             EV::load2(stg, x);
             EV::load2(stg + half, g);
@@ -619,9 +620,8 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
                 for (int k = 0; k < static_cast<int>(C); ++k) s += bx[k * kBwBatch + lane];
                 const float r = meta[sj_l].rstd;
                 kk_l = r * r * r * s * inv_d;
-                tok_l = meta[sj_l].tok;
+                tok_l = meta[sj_l].row;
             }
-            const size_t row_bytes = static_cast<size_t>(d) * sizeof(E);
             uint8_t *dv_col = p.dv + static_cast<size_t>(c0) * sizeof(E) + tid * EV::kBytes;
 #pragma unroll
             for (int j = 0; j < kBwBatch; ++j) {
@@ -630,11 +630,11 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
                 const long long tok = __shfl_sync(0xffffffffu, tok_l, j);
                 if (j < n) {
                     float2 x[2];
-                    EV::load2(ring + static_cast<size_t>(sj) * SB + tid * EV::kBytes, x);
+                    EV::load2(my_ring + sj * SB, x);
                     const float4 y = ybuf[((bf & 1) * kBwBatch + j) * kBwCons + tid];
                     const float2 o[2] = {p2fma(p2(-kk), x[0], make_float2(y.x, y.y)),
                                          p2fma(p2(-kk), x[1], make_float2(y.z, y.w))};
-                    if (active) EV::store2(dv_col + static_cast<size_t>(tok) * row_bytes, o);
+                    if (active) EV::store2(dv_col + tok, o);
                 }
             }
             __syncwarp();
@@ -684,7 +684,7 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
         auto step = [&](auto Jc, auto Sc, uint32_t kind) {
             constexpr int J = decltype(Jc)::v;
             constexpr bool STEADY = decltype(Sc)::v != 0;
-            const uint8_t *stg = ring + static_cast<size_t>(st) * SB + tid * EV::kBytes;
+            const uint8_t *stg = my_ring + st * SB;
             const float2 rt = p2(meta[st].rstd);
             float2 x[2];
             EV::load2(stg, x);
@@ -973,7 +973,7 @@ __global__ void __launch_bounds__(kFwThreads, 6) conv_fwd_sweep_kernel(const __g
             }
             if (state == 1) {  // the sentinel: no copies, both arrivals
                 if (lane == 0) {
-                    meta[st].tok = 0;
+                    meta[st].row = 0;
                     meta[st].flags = kFlDone;
                     mbar_arrive(&full[st]);
                     mbar_arrive(&full[st]);
@@ -990,7 +990,7 @@ __global__ void __launch_bounds__(kFwThreads, 6) conv_fwd_sweep_kernel(const __g
                     uint32_t fl = (lead ? kScLead : kScMain) | (static_cast<uint32_t>(ql & 3) << kFlSlotShift);
                     if (ql == 0) fl |= kFlSegStart;
                     if (group) fl |= kFlGroup;
-                    meta[stl].tok = tl;
+                    meta[stl].row = tl * static_cast<int64_t>(row_bytes);
                     meta[stl].flags = fl;
                     uint8_t *dst = ring + static_cast<size_t>(stl) * SB;
                     const bool with_h = !lead && src_h;
@@ -1022,6 +1022,7 @@ __global__ void __launch_bounds__(kFwThreads, 6) conv_fwd_sweep_kernel(const __g
     } else {
         // ---- consumers
         const bool active = tid * kScEV < ncols;
+        const uint8_t *my_ring = ring + tid * EV::kBytes;  // this thread's channels in stage 0
         const int width = p.width, d = p.d;
         float2 K[kScAges][2], bias[2];  // taps by age folded with norm_w; [h]: channels 2h, 2h + 1
 #pragma unroll
@@ -1042,7 +1043,6 @@ __global__ void __launch_bounds__(kFwThreads, 6) conv_fwd_sweep_kernel(const __g
 #pragma unroll
             for (int a = 0; a < kScAges; ++a) K[a][h] = make_float2(v[0][1 + a], v[1][1 + a]);
         }
-        const size_t row_bytes = static_cast<size_t>(d) * sizeof(E);
         uint8_t *out_col = p.out + static_cast<size_t>(c0) * sizeof(E) + tid * EV::kBytes;
         float2 U[4][2];  // u = V~ rstd by slot
         int st = 0;
@@ -1077,7 +1077,7 @@ __global__ void __launch_bounds__(kFwThreads, 6) conv_fwd_sweep_kernel(const __g
         auto step = [&](auto Jc, auto Gc, bool lead) {
             constexpr bool GROUP = decltype(Gc)::v != 0;
             constexpr int J = decltype(Jc)::v;
-            const uint8_t *stg = ring + static_cast<size_t>(st) * SB + tid * EV::kBytes;
+            const uint8_t *stg = my_ring + st * SB;
             const float2 rt = p2(meta[st].rstd);
             float2 x[2];
             EV::load2(stg, x);
@@ -1094,7 +1094,7 @@ __global__ void __launch_bounds__(kFwThreads, 6) conv_fwd_sweep_kernel(const __g
                                                  p2fma(K[1][h], U[(J + 3) & 3][h], p2fma(K[0][h], U[J][h], bias[h]))));
                     o[h] = p2fma(c, p2sigmoid(c), p2add(x[h], y[h]));
                 }
-                if (active) EV::store2(out_col + static_cast<size_t>(meta[st].tok) * row_bytes, o);
+                if (active) EV::store2(out_col + meta[st].row, o);
             }
             if (!GROUP) {
                 __syncwarp();
