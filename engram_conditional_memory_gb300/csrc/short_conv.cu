@@ -1045,38 +1045,34 @@ __global__ void __launch_bounds__(kFwThreads, 6) conv_fwd_sweep_kernel(const __g
         }
         uint8_t *out_col = p.out + static_cast<size_t>(c0) * sizeof(E) + tid * EV::kBytes;
         float2 U[4][2];  // u = V~ rstd by slot
-        int st = 0;
-        uint32_t ph = 0;
+        static_assert((S & (S - 1)) == 0, "stage and phase from the position count by mask and shift");
+        constexpr int kLogS = S == 16 ? 4 : (S == 32 ? 5 : 3);
+        static_assert((1 << kLogS) == S, "the ring's size is 8, 16 or 32");
+        uint32_t gq = 0;  // positions consumed: position gq + k sits in stage (gq + k) mod S
+        auto stage_of = [&](uint32_t k) { return static_cast<int>((gq + k) & (S - 1)); };
+        auto parity_of = [&](uint32_t k) { return ((gq + k) >> kLogS) & 1u; };
 
-        // stages st + k0 .. st + k1 - 1 full: every lane tries them all back to back and the warp
-        // agrees; only when one is still filling, every lane waits for it (bounded)
+        // stages of positions gq + k0 .. gq + k1 - 1 full: every lane tries them all back to back and
+        // the warp agrees; only when one is still filling, every lane waits for it (bounded)
         auto wait_stages = [&](int k0, int k1) {
             if (failed) return;
             bool ok = true;
 #pragma unroll 4
-            for (int k = k0; k < k1; ++k) {
-                const bool wrap = st + k >= S;
-                ok &= mbar_try_wait(&full[wrap ? st + k - S : st + k], wrap ? ph ^ 1u : ph);
-            }
+            for (int k = k0; k < k1; ++k) ok &= mbar_try_wait(&full[stage_of(k)], parity_of(k));
             if (__all_sync(0xffffffffu, ok)) return;
             ok = true;
-            for (int k = k0; k < k1; ++k) {
-                const bool wrap = st + k >= S;
-                ok = ok && mbar_wait_sleep(&full[wrap ? st + k - S : st + k], wrap ? ph ^ 1u : ph);
-            }
+            for (int k = k0; k < k1; ++k) ok = ok && mbar_wait_sleep(&full[stage_of(k)], parity_of(k));
             if (!__all_sync(0xffffffffu, ok)) {
                 if (lane == 0) report(p.status, nullptr, ENGRAM_DEVERR_TIMEOUT);
                 failed = true;
             }
         };
-        auto advance = [&]() {
-            if (++st == S) st = 0, ph ^= 1u;
-        };
-        // one position in slot J, its stage already waited for; GROUP: its stage is released with
+        // position gq + K in slot J, its stage already waited for; GROUP: its stage is released with
         // the group's
-        auto step = [&](auto Jc, auto Gc, bool lead) {
+        auto step = [&](auto Jc, auto Kc, auto Gc, bool lead) {
             constexpr bool GROUP = decltype(Gc)::v != 0;
             constexpr int J = decltype(Jc)::v;
+            const int st = stage_of(decltype(Kc)::v);
             const uint8_t *stg = my_ring + st * SB;
             const float2 rt = p2(meta[st].rstd);
             float2 x[2];
@@ -1100,13 +1096,12 @@ __global__ void __launch_bounds__(kFwThreads, 6) conv_fwd_sweep_kernel(const __g
                 __syncwarp();
                 mbar_arrive_if(&empty[st], lane == 0 && !failed);
             }
-            advance();
         };
 
         for (;;) {
             wait_stages(0, 1);
             if (failed) break;
-            const uint32_t fl = meta[st].flags;
+            const uint32_t fl = meta[stage_of(0)].flags;
             if (fl & (kFlDone | kFlSegStart)) {
                 if (fl & kFlDone) break;
 #pragma unroll
@@ -1116,22 +1111,22 @@ __global__ void __launch_bounds__(kFwThreads, 6) conv_fwd_sweep_kernel(const __g
                 // all four stages first, so that the four positions' loads and arithmetic may overlap
                 wait_stages(1, 4);
                 if (failed) break;
-                const int st0 = st;
-                step(ScIdx<0>{}, ScIdx<1>{}, false);
-                step(ScIdx<1>{}, ScIdx<1>{}, false);
-                step(ScIdx<2>{}, ScIdx<1>{}, false);
-                step(ScIdx<3>{}, ScIdx<1>{}, false);
+                step(ScIdx<0>{}, ScIdx<0>{}, ScIdx<1>{}, false);
+                step(ScIdx<1>{}, ScIdx<1>{}, ScIdx<1>{}, false);
+                step(ScIdx<2>{}, ScIdx<2>{}, ScIdx<1>{}, false);
+                step(ScIdx<3>{}, ScIdx<3>{}, ScIdx<1>{}, false);
                 __syncwarp();  // the group's four stages at once, one lane each
-                mbar_arrive_if(&empty[st0 + (lane & 3) < S ? st0 + (lane & 3) : st0 + (lane & 3) - S],
-                               lane < 4 && !failed);
+                mbar_arrive_if(&empty[stage_of(lane & 3)], lane < 4 && !failed);
+                gq += 4;
             } else {
                 const bool lead = (fl & kFlKind) == kScLead;
                 switch ((fl >> kFlSlotShift) & 3u) {
-                    case 0: step(ScIdx<0>{}, ScIdx<0>{}, lead); break;
-                    case 1: step(ScIdx<1>{}, ScIdx<0>{}, lead); break;
-                    case 2: step(ScIdx<2>{}, ScIdx<0>{}, lead); break;
-                    default: step(ScIdx<3>{}, ScIdx<0>{}, lead); break;
+                    case 0: step(ScIdx<0>{}, ScIdx<0>{}, ScIdx<0>{}, lead); break;
+                    case 1: step(ScIdx<1>{}, ScIdx<0>{}, ScIdx<0>{}, lead); break;
+                    case 2: step(ScIdx<2>{}, ScIdx<0>{}, ScIdx<0>{}, lead); break;
+                    default: step(ScIdx<3>{}, ScIdx<0>{}, ScIdx<0>{}, lead); break;
                 }
+                gq += 1;
             }
         }
     }
