@@ -15,7 +15,8 @@
 //   hash_index_kernel: one thread per token computes its compressed window (the pad id 0 before its
 //      sequence's start, found by a binary search in the sequence offsets), every table's hash and
 //      index, and parks the absolute row numbers in the first 8 x tables bytes of the token's own
-//      e_t row (plus the optional index output);
+//      e_t row (plus the optional index output).  A warp stages its 32 tokens' numbers in shared
+//      memory and writes them out as whole lines;
 //   hash_gather_kernel: a persistent CTA walks double-buffered tiles of consecutive tokens (~32 KB
 //      of e_t rows, at most kTileMax tokens): it reads a tile's parked row numbers, fetches every
 //      table row by one bulk asynchronous copy (TMA, 1-D) into the shared tile in e_t order,
@@ -183,14 +184,42 @@ __device__ __forceinline__ void bulk_wait_read_all_but_one() {
 
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// Index of a token in table tb: the multiply-XOR hash of its compressed window, reduced mod the prime.
+// The multipliers of a table beyond its order are zero (set so on the host), so every table runs
+// the kernel-wide max_order terms and the extra ones add nothing; compressed ids are below 2^31, so
+// each product is a 32 x 64-bit multiply.
+__device__ __forceinline__ uint64_t table_index(const HashGatherParams &p, const uint32_t (&cid)[ENGRAM_MAX_ORDER],
+                                                int tb) {
+    uint64_t h = 0;
+#pragma unroll
+    for (int j = 0; j < ENGRAM_MAX_ORDER; ++j) {
+        if (j >= p.max_order) break;
+        h ^= static_cast<uint64_t>(cid[j]) * p.mult[tb][j];
+    }
+    return mod_prime(h, p.prime[tb], p.prime_inv[tb]);
+}
+
+// Dynamic shared memory of hash_index_kernel: per warp [32][tables + 1] int64 row numbers (the odd
+// row pitch in 8-byte words keeps the per-token writes free of bank conflicts), then the staged
+// sequence offsets.
+__host__ __device__ inline int index_smem_bytes(int tables, int staged_entries) {
+    return (kIndexThreads * (tables + 1) + staged_entries) * 8;
+}
+
 // Steps 1-2 for every token, one thread per token: its compressed window (the pad id 0 before its
-// sequence's start), every table's hash, the optional index output, and -- when rows are wanted --
-// the absolute row numbers (int64, row_off[table] + index) parked in the first 8 x tables bytes of
-// the token's own e_t row, which hash_gather_kernel reads back before it overwrites that row.
-// Block 0 also checks that 0 = o_0 <= o_1 <= ... <= o_S = T.
+// sequence's start), every table's hash (the tables in the same order on every lane, so that their
+// constants are read once per warp), the optional index output, and -- when rows are wanted -- the
+// absolute row numbers (int64, row_off[table] + index) parked in the first 8 x tables bytes of the
+// token's own e_t row, which hash_gather_kernel reads back before it overwrites that row.  The row
+// numbers go through shared memory, so that the warp's stores cover whole lines instead of 32 lines
+// 8 bytes at a time.  Block 0 also checks that 0 = o_0 <= o_1 <= ... <= o_S = T.
 __global__ void __launch_bounds__(kIndexThreads) hash_index_kernel(const __grid_constant__ HashGatherParams p) {
     pdl_wait();  // the previous kernel's writes are complete and visible
-    extern __shared__ __align__(16) int64_t so[];
+    extern __shared__ __align__(16) int64_t dyn[];
+    const int warp = static_cast<int>(threadIdx.x) >> 5, lane = static_cast<int>(threadIdx.x) & 31;
+    const int pitch = p.tables + 1;
+    int64_t *rows_s = dyn + static_cast<size_t>(warp) * 32 * pitch;  // this warp's tokens' row numbers
+    int64_t *so = dyn + static_cast<size_t>(kIndexThreads) * pitch;
     const int64_t *offs = p.seq_offsets;
     if (p.staged_seqs) {  // the sequence offsets in shared memory when they fit
         for (int s = threadIdx.x; s <= p.num_seqs; s += blockDim.x) so[s] = p.seq_offsets[s];
@@ -206,39 +235,54 @@ __global__ void __launch_bounds__(kIndexThreads) hash_index_kernel(const __grid_
         }
     }
     const uint32_t et_bytes = static_cast<uint32_t>(p.tables) * p.row_bytes;
-    for (int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; t < p.T;
-         t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t s0 = sequence_start(offs, p.num_seqs, t);
-        uint64_t cid[ENGRAM_MAX_ORDER];
+    // the copy-out walks units u = lane, lane + 32, ... of (token, table) pairs: token u / tables,
+    // table u mod tables, advanced by 32 = q32 tables + r32 each step
+    const int q32 = 32 / p.tables, r32 = 32 - q32 * p.tables;
+    const int tok_first = lane / p.tables, tb_first = lane - tok_first * p.tables;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kIndexThreads;
+    for (int64_t t0 = static_cast<int64_t>(blockIdx.x) * kIndexThreads + warp * 32; t0 < p.T; t0 += stride) {
+        const int ntok = p.T - t0 < 32 ? static_cast<int>(p.T - t0) : 32;
+        const int64_t t = t0 + lane;
+        if (lane < ntok) {
+            const int64_t s0 = sequence_start(offs, p.num_seqs, t);
+            uint32_t cid[ENGRAM_MAX_ORDER];
 #pragma unroll
-        for (int j = 0; j < ENGRAM_MAX_ORDER; ++j) {
-            cid[j] = 0;
-            const int64_t q = t - j;
-            if (j < p.max_order && q >= s0) {
-                const int32_t raw = __ldg(p.ids + q);
-                if (raw < 0 || raw >= p.vocab) {
-                    if (j == 0) report(p.status, p.err_word, ENGRAM_DEVERR_TOKEN_ID);
-                } else {
-                    const int32_t id = p.cmap ? __ldg(p.cmap + raw) : raw;
-                    if (id < 0 || id >= p.vocab_c) {
-                        if (j == 0) report(p.status, p.err_word, ENGRAM_DEVERR_COMPRESSED);
+            for (int j = 0; j < ENGRAM_MAX_ORDER; ++j) {
+                cid[j] = 0;
+                const int64_t q = t - j;
+                if (j < p.max_order && q >= s0) {
+                    const int32_t raw = __ldg(p.ids + q);
+                    if (raw < 0 || raw >= p.vocab) {
+                        if (j == 0) report(p.status, p.err_word, ENGRAM_DEVERR_TOKEN_ID);
                     } else {
-                        cid[j] = static_cast<uint64_t>(id);
+                        const int32_t id = p.cmap ? __ldg(p.cmap + raw) : raw;
+                        if (id < 0 || id >= p.vocab_c) {
+                            if (j == 0) report(p.status, p.err_word, ENGRAM_DEVERR_COMPRESSED);
+                        } else {
+                            cid[j] = static_cast<uint32_t>(id);
+                        }
                     }
                 }
             }
+            int64_t *mine = rows_s + lane * pitch;
+#pragma unroll 4
+            for (int tb = 0; tb < p.tables; ++tb) {
+                const uint64_t idx = table_index(p, cid, tb);
+                mine[tb] = p.row_off[tb] + static_cast<int64_t>(idx);
+                if (p.out_idx) p.out_idx[t * p.tables + tb] = static_cast<int32_t>(idx);
+            }
         }
-        int64_t *park = p.out_rows ? reinterpret_cast<int64_t *>(p.out_rows + static_cast<size_t>(t) * et_bytes)
-                                   : nullptr;
-        for (int tb = 0; tb < p.tables; ++tb) {
-            const int n = p.order[tb];
-            uint64_t h = 0;
-#pragma unroll
-            for (int j = 0; j < ENGRAM_MAX_ORDER; ++j)
-                if (j < n) h ^= cid[j] * p.mult[tb][j];
-            const uint64_t idx = mod_prime(h, p.prime[tb], p.prime_inv[tb]);
-            if (park) park[tb] = p.row_off[tb] + static_cast<int64_t>(idx);
-            if (p.out_idx) p.out_idx[t * p.tables + tb] = static_cast<int32_t>(idx);
+        if (p.out_rows) {
+            __syncwarp();
+            int tok = tok_first, tb = tb_first;
+            for (int u = lane; u < ntok * p.tables; u += 32) {
+                int64_t *park = reinterpret_cast<int64_t *>(p.out_rows + static_cast<size_t>(t0 + tok) * et_bytes);
+                park[tb] = rows_s[tok * pitch + tb];
+                tok += q32;
+                tb += r32;
+                if (tb >= p.tables) tb -= p.tables, ++tok;
+            }
+            __syncwarp();  // the staged numbers are read before the next tokens overwrite them
         }
     }
 }
@@ -525,7 +569,7 @@ extern "C" engram_status engram_hash_gather(const engram_hash_spec *spec, const 
     const int64_t iblocks =
         std::max<int64_t>(1, std::min<int64_t>((a->T + kIndexThreads - 1) / kIndexThreads, 16LL * dev.num_sms));
     p.staged_seqs = a->num_seqs + 1 <= kSmemSeqs ? 1 : 0;
-    const int ismem = p.staged_seqs ? (a->num_seqs + 1) * 8 : 0;
+    const int ismem = index_smem_bytes(tables, p.staged_seqs ? a->num_seqs + 1 : 0);
     if ((st = set_smem(reinterpret_cast<const void *>(hash_index_kernel), ismem)) != ENGRAM_OK) return st;
     cudaError_t le = launch_kernel(hash_index_kernel, dim3(static_cast<unsigned>(iblocks)), dim3(kIndexThreads), ismem, s, p);
     if (le != cudaSuccess) return fail(ENGRAM_ERR_CUDA, "engram_hash_gather launch: %s", cudaGetErrorString(le));

@@ -12,8 +12,8 @@
 //     and rstd into a ring of shared-memory stages with a record of the position; every thread
 //     carries its four channels' last three taps' inputs in registers, so each row is converted
 //     once;
-//   * conv_bwd_kernel (the backward, one pass): a thread-block cluster of ceil(d / 1024) CTAs takes
-//     one residue class t = r (mod dilation) of one time chunk, each CTA 1024 channels.  Every tap of
+//   * conv_bwd_kernel (the backward, one pass): a thread-block cluster of ceil(d / 512) CTAs takes
+//     one residue class t = r (mod dilation) of one time chunk, each CTA 512 channels.  Every tap of
 //     a class token lies in the same class, so the CTA sweeps its class tokens in time order, a
 //     producer warp streaming each token's V~ and dout row segments and rstd into a ring of
 //     shared-memory stages; each consumer thread carries its four channels' last three taps' inputs
@@ -184,7 +184,7 @@ __host__ __device__ inline int sc_bwd_smem(int stages, int stage_bytes) {
            4 * kBwMaxCluster * kBwBatch * 4 + stages * 16 + 4 * kBwBatch * 4 + (2 * stages + 6) * 8 + 128;
 }
 
-// A stage: the V~ segment of 1024 channels, then the dout segment.
+// A stage: the V~ segment of 512 channels, then the dout segment.
 template <typename E>
 __host__ __device__ constexpr int sc_bwd_stage_bytes() {
     return 2 * kBwCW * static_cast<int>(sizeof(E));
@@ -293,8 +293,8 @@ constexpr uint32_t kFlDone = 1u << 8;     // no position: the cluster's items ar
 constexpr int kFlItemShift = 12;          // bits 12-31: the work item, at an item start
 constexpr int64_t kBwMaxItems = int64_t(1) << 20;
 
-// The producer's place in the stream of sweep positions of its cluster's work items (thread 0
-// only, in shared memory).
+// The producer's place in the stream of sweep positions of its cluster's work items (in shared
+// memory; lane 0 of the producer warp moves it on from one segment to the next).
 struct ScProd {
     int64_t item;      // current work item
     int64_t t_hi;      // its chunk's end
@@ -310,12 +310,13 @@ struct ScProd {
 };
 static_assert(sizeof(ScProd) <= 128, "the producer state fits its shared-memory slot");
 
-// The backward in one pass.  A cluster of ceil(d / 1024) CTAs takes work items (time chunk,
-// residue class t = r mod dilation); CTA `rank` holds channels [1024 rank, 1024 rank + 1024).
-// Thread 0 walks the items' segments and streams, per sweep position, the token's V~ and dout row
-// segments (1-D bulk copies) and its rstd (a 4-byte asynchronous copy) into a ring of stages, as
-// far ahead as the ring allows, with a record of the position (token, kind, segment and item
-// boundaries).  Every thread owns four channels and sweeps the positions in order:
+// The backward in one pass.  A cluster of ceil(d / 512) CTAs takes work items (time chunk,
+// residue class t = r mod dilation); CTA `rank` holds channels [512 rank, 512 rank + 512).
+// A producer warp walks the items' segments and streams, per sweep position (one per lane), the
+// token's V~ and dout row segments (1-D bulk copies) and its rstd (a 4-byte asynchronous copy)
+// into a ring of stages, as far ahead as the ring allows, with a record of the position (row
+// offset, kind, slot, segment and item boundaries).  Each of the 128 consumer threads owns four
+// channels and sweeps the positions in order:
 //   u  = V~ rstd norm_w (the last three kept by age in registers),
 //   dc = dout SiLU'(conv),  conv = bias + sum_a w_a u[t - a dil]   (w_a: tap width - 1 - a),
 //   the tap and bias gradients of the chunk's outputs, and the du = sum_a w_a dc[t + a dil] still
@@ -356,7 +357,7 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
     const int64_t dil = p.dil;
     bool failed = false;
 
-    // thread 0: the next segment of the producer's stream, moving on through the cluster's items
+    // producer lane 0: the next segment of the producer's stream, moving on through the cluster's items
     auto prod_next_seg = [&]() {
         ScProd &P = *prod;
         ScSeg g;
@@ -1197,7 +1198,7 @@ engram_status sc_ptrs(const char *fn, const void *const *ptrs, int n, int n_alig
     return ENGRAM_OK;
 }
 
-// Clusters of ceil(d / 1024) CTAs, as many as fit at once (at most one per work item), each
+// Clusters of ceil(d / 512) CTAs, as many as fit at once (at most one per work item), each
 // walking the work items cluster_id, cluster_id + clusters, ...
 constexpr int kScDevices = 64;
 
