@@ -9,7 +9,7 @@ tokens (65,536 tokens):
   3. the context-aware gate, forward + backward on four micro-batches of
      T = 16384 tokens at d = 4096 (bf16), then one ordered reduction of the
      four micro-batches' weight-gradient partials, accumulating into fp32
-     grad_w_h / grad_w_k (12 kernel launches: the hash + gather is two).
+     grad_w_h / grad_w_k (11 kernel launches: the hash + gather is one).
 The reported value is tokens/s through the whole step (whole job, all ranks).
 Inputs are resident in HBM (the device-timed value) or copied from pinned host
 memory every step (the `e2e` value).  The per-step working set (4.1 GB table,
@@ -220,7 +220,7 @@ def make_workload(device):
 
 
 def run_step(wk, mark=None):
-    """Launch one step (12 kernels) on the current stream; `mark(name)` is called after each call."""
+    """Launch one step (11 kernels) on the current stream; `mark(name)` is called after each call."""
     import engram_conditional_memory_gb300 as ecm
 
     hw = wk["hw"]
@@ -238,7 +238,7 @@ def run_step(wk, mark=None):
         mark and mark("gate_bwd")
     reduce_step(wk)
     mark and mark("grad_w_reduce")
-    return 12
+    return 11
 
 
 def reduce_step(wk):
@@ -253,7 +253,7 @@ def reduce_step(wk):
 # ----------------------------------------------------------------------------- device timing
 
 def capture_step(wk, device):
-    """The step as one CUDA graph (12 kernel nodes).  The library's per-device set-up and each
+    """The step as one CUDA graph (11 kernel nodes).  The library's per-device set-up and each
     kernel's shared-memory attribute are done by an eager step first; device-pointer checks are
     off during capture (they were made by that eager step on the same buffers)."""
     import torch
@@ -296,7 +296,7 @@ def time_graph(graph, steps, warmup, device):
     torch.cuda.synchronize()
     wall1 = _dt.datetime.now()
     barrier(device)
-    return start.elapsed_time(end), 12 * steps, wall0, wall1
+    return start.elapsed_time(end), 11 * steps, wall0, wall1
 
 
 def time_device(wk, steps, warmup, device):
@@ -843,7 +843,7 @@ def main_native(args, rank, local, world):
             "config": {"workload": WORKLOAD, "tokens_per_step": T_all, "global_batch": world * T_all,
                        "seq_len": SEQ_LEN, "parallelism": f"replicas x{world}",
                        "l2": "no flush: per-step working set 6.1 GB >> 129 MB L2",
-                       "timing": "value: CUDA-graph replays of the 12-launch step; ops/roofline: eager steps "
+                       "timing": "value: CUDA-graph replays of the 11-launch step; ops/roofline: eager steps "
                                  "with an event between launches; e2e: eager calls with host copies"},
             "hbm_gbs": step_bytes / (max_ms / args.steps / 1e3) / 1e9,
             "hash_gather_rows_per_s": 16 * T_all / (ops["hash_gather"]["avg_ms"] / 1e3),

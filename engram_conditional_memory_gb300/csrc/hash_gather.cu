@@ -11,18 +11,17 @@
 //   h = XOR_{j<n} (uint64) id'(t - j) * M[table][j]  (mod 2^64),  idx = h mod p[table],
 //   id'(q) = pad id 0 for q before the start of t's sequence.
 //
-// Kernel layout, two kernels for a table in device memory:
-//   hash_index_kernel: one thread per token computes its compressed window (the pad id 0 before its
-//      sequence's start, found by a binary search in the sequence offsets), every table's hash and
-//      index, and parks the absolute row numbers in the first 8 x tables bytes of the token's own
-//      e_t row (plus the optional index output).  A warp stages its 32 tokens' numbers in shared
-//      memory and writes them out as whole lines;
-//   hash_gather_kernel: a persistent CTA walks double-buffered tiles of consecutive tokens (~32 KB
-//      of e_t rows, at most kTileMax tokens): it reads a tile's parked row numbers, fetches every
-//      table row by one bulk asynchronous copy (TMA, 1-D) into the shared tile in e_t order,
-//      completing on the tile's mbarrier, and when all have landed one thread stores the whole tile
-//      -- its e_t rows are adjacent in the output -- over the parked numbers with a single bulk copy.
-//      The next tile's row numbers are read while the current tile's copies are in flight.
+// Kernel layout for a table in device memory:
+//   hash_gather_kernel (rows wanted): a persistent CTA walks tiles of consecutive tokens (~32 KB of
+//      e_t rows, at most kTileMax tokens).  Its hash warp computes each tile's row numbers (lane =
+//      token: the compressed window, the pad id 0 before the sequence's start found by a binary
+//      search in the sequence offsets, every table's hash) into a ring of shared-memory slots, up to
+//      kRowRing tiles ahead; its copy threads fetch every table row of a tile by one bulk
+//      asynchronous copy (TMA, 1-D) into a double-buffered shared tile in e_t order, completing on
+//      the tile's mbarrier, and when all have landed one thread stores the whole tile -- its e_t rows
+//      are adjacent in the output -- with a single bulk copy.  The hashing of later tiles overlaps
+//      the copies of the current one;
+//   hash_index_kernel (the index output alone): one thread per token.
 // Random 128-byte rows are where this beats 16-byte loads from every thread: the copy engine keeps
 // far more rows in flight per SM than the load units can (measured: 53 us against 70 us for the
 // 65,536-token, 16-table gather on GB300).  With a table in host memory, hash_gather_host_kernel
@@ -34,7 +33,7 @@
 namespace engram {
 
 constexpr int kTileMax = 32;           // tokens per tile at most
-constexpr int kHashThreads = 256;      // threads per CTA
+constexpr int kHashThreads = 256;      // copy threads of a gather CTA (all of a host-table CTA)
 constexpr int kTileBytes = 32 * 1024;  // target bytes of e_t rows per tile
 constexpr int kIndexThreads = 128;     // hash_index_kernel: one thread per token
 constexpr int kSmemSeqs = 4096;        // sequence offsets staged in shared memory up to this count
@@ -182,6 +181,9 @@ __device__ __forceinline__ void bulk_wait_read_all_but_one() {
     asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 
+// Waits until no committed bulk store still reads shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Index of a token in table tb: the multiply-XOR hash of its compressed window, reduced mod the prime.
@@ -199,172 +201,248 @@ __device__ __forceinline__ uint64_t table_index(const HashGatherParams &p, const
     return mod_prime(h, p.prime[tb], p.prime_inv[tb]);
 }
 
-// Dynamic shared memory of hash_index_kernel: per warp [32][tables + 1] int64 row numbers (the odd
-// row pitch in 8-byte words keeps the per-token writes free of bank conflicts), then the staged
-// sequence offsets.
-__host__ __device__ inline int index_smem_bytes(int tables, int staged_entries) {
-    return (kIndexThreads * (tables + 1) + staged_entries) * 8;
+// Steps 1-2 for token t: its compressed window (the pad id 0 before its sequence's start) and the
+// index of tables tb_first, tb_first + tb_step, ..., the tables in one order on every lane so that a
+// warp reads each table's constants once; the absolute row numbers row_off[table] + index go to
+// dst[table] when dst is given, the indices to the optional index output.  An invalid id is
+// reported by the token that holds it.
+__device__ __forceinline__ void token_rows(const HashGatherParams &p, const int64_t *offs, int64_t t, int64_t *dst,
+                                           int tb_first = 0, int tb_step = 1) {
+    const int64_t s0 = sequence_start(offs, p.num_seqs, t);
+    uint32_t cid[ENGRAM_MAX_ORDER];
+#pragma unroll
+    for (int j = 0; j < ENGRAM_MAX_ORDER; ++j) {
+        cid[j] = 0;
+        const int64_t q = t - j;
+        if (j < p.max_order && q >= s0) {
+            const int32_t raw = __ldg(p.ids + q);
+            if (raw < 0 || raw >= p.vocab) {
+                if (j == 0) report(p.status, p.err_word, ENGRAM_DEVERR_TOKEN_ID);
+            } else {
+                const int32_t id = p.cmap ? __ldg(p.cmap + raw) : raw;
+                if (id < 0 || id >= p.vocab_c) {
+                    if (j == 0) report(p.status, p.err_word, ENGRAM_DEVERR_COMPRESSED);
+                } else {
+                    cid[j] = static_cast<uint32_t>(id);
+                }
+            }
+        }
+    }
+#pragma unroll 4
+    for (int tb = tb_first; tb < p.tables; tb += tb_step) {
+        const uint64_t idx = table_index(p, cid, tb);
+        if (dst) dst[tb] = p.row_off[tb] + static_cast<int64_t>(idx);
+        if (p.out_idx) p.out_idx[t * p.tables + tb] = static_cast<int32_t>(idx);
+    }
 }
 
-// Steps 1-2 for every token, one thread per token: its compressed window (the pad id 0 before its
-// sequence's start), every table's hash (the tables in the same order on every lane, so that their
-// constants are read once per warp), the optional index output, and -- when rows are wanted -- the
-// absolute row numbers (int64, row_off[table] + index) parked in the first 8 x tables bytes of the
-// token's own e_t row, which hash_gather_kernel reads back before it overwrites that row.  The row
-// numbers go through shared memory, so that the warp's stores cover whole lines instead of 32 lines
-// 8 bytes at a time.  Block 0 also checks that 0 = o_0 <= o_1 <= ... <= o_S = T.
+// Checks, in block 0, that 0 = o_0 <= o_1 <= ... <= o_S = T.
+__device__ __forceinline__ void check_offsets(const HashGatherParams &p, const int64_t *offs) {
+    if (blockIdx.x != 0) return;
+    for (int s = threadIdx.x; s <= p.num_seqs; s += blockDim.x) {
+        const int64_t o = offs[s];
+        bool bad = (s == 0 && o != 0) || (s == p.num_seqs && o != p.T) || o < 0 || o > p.T;
+        if (s > 0 && offs[s - 1] > o) bad = true;
+        if (bad) report(p.status, p.err_word, ENGRAM_DEVERR_SEQ_OFFSETS);
+    }
+}
+
+// Steps 1-2 alone, for the index output without rows: one thread per token.
 __global__ void __launch_bounds__(kIndexThreads) hash_index_kernel(const __grid_constant__ HashGatherParams p) {
     pdl_wait();  // the previous kernel's writes are complete and visible
-    extern __shared__ __align__(16) int64_t dyn[];
-    const int warp = static_cast<int>(threadIdx.x) >> 5, lane = static_cast<int>(threadIdx.x) & 31;
-    const int pitch = p.tables + 1;
-    int64_t *rows_s = dyn + static_cast<size_t>(warp) * 32 * pitch;  // this warp's tokens' row numbers
-    int64_t *so = dyn + static_cast<size_t>(kIndexThreads) * pitch;
+    extern __shared__ __align__(16) int64_t so[];
     const int64_t *offs = p.seq_offsets;
     if (p.staged_seqs) {  // the sequence offsets in shared memory when they fit
         for (int s = threadIdx.x; s <= p.num_seqs; s += blockDim.x) so[s] = p.seq_offsets[s];
         offs = so;
         __syncthreads();
     }
-    if (blockIdx.x == 0) {
-        for (int s = threadIdx.x; s <= p.num_seqs; s += blockDim.x) {
-            const int64_t o = offs[s];
-            bool bad = (s == 0 && o != 0) || (s == p.num_seqs && o != p.T) || o < 0 || o > p.T;
-            if (s > 0 && offs[s - 1] > o) bad = true;
-            if (bad) report(p.status, p.err_word, ENGRAM_DEVERR_SEQ_OFFSETS);
-        }
-    }
-    const uint32_t et_bytes = static_cast<uint32_t>(p.tables) * p.row_bytes;
-    // the copy-out walks units u = lane, lane + 32, ... of (token, table) pairs: token u / tables,
-    // table u mod tables, advanced by 32 = q32 tables + r32 each step
-    const int q32 = 32 / p.tables, r32 = 32 - q32 * p.tables;
-    const int tok_first = lane / p.tables, tb_first = lane - tok_first * p.tables;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * kIndexThreads;
-    for (int64_t t0 = static_cast<int64_t>(blockIdx.x) * kIndexThreads + warp * 32; t0 < p.T; t0 += stride) {
-        const int ntok = p.T - t0 < 32 ? static_cast<int>(p.T - t0) : 32;
-        const int64_t t = t0 + lane;
-        if (lane < ntok) {
-            const int64_t s0 = sequence_start(offs, p.num_seqs, t);
-            uint32_t cid[ENGRAM_MAX_ORDER];
-#pragma unroll
-            for (int j = 0; j < ENGRAM_MAX_ORDER; ++j) {
-                cid[j] = 0;
-                const int64_t q = t - j;
-                if (j < p.max_order && q >= s0) {
-                    const int32_t raw = __ldg(p.ids + q);
-                    if (raw < 0 || raw >= p.vocab) {
-                        if (j == 0) report(p.status, p.err_word, ENGRAM_DEVERR_TOKEN_ID);
-                    } else {
-                        const int32_t id = p.cmap ? __ldg(p.cmap + raw) : raw;
-                        if (id < 0 || id >= p.vocab_c) {
-                            if (j == 0) report(p.status, p.err_word, ENGRAM_DEVERR_COMPRESSED);
-                        } else {
-                            cid[j] = static_cast<uint32_t>(id);
-                        }
-                    }
-                }
-            }
-            int64_t *mine = rows_s + lane * pitch;
-#pragma unroll 4
-            for (int tb = 0; tb < p.tables; ++tb) {
-                const uint64_t idx = table_index(p, cid, tb);
-                mine[tb] = p.row_off[tb] + static_cast<int64_t>(idx);
-                if (p.out_idx) p.out_idx[t * p.tables + tb] = static_cast<int32_t>(idx);
-            }
-        }
-        if (p.out_rows) {
-            __syncwarp();
-            int tok = tok_first, tb = tb_first;
-            for (int u = lane; u < ntok * p.tables; u += 32) {
-                int64_t *park = reinterpret_cast<int64_t *>(p.out_rows + static_cast<size_t>(t0 + tok) * et_bytes);
-                park[tb] = rows_s[tok * pitch + tb];
-                tok += q32;
-                tb += r32;
-                if (tb >= p.tables) tb -= p.tables, ++tok;
-            }
-            __syncwarp();  // the staged numbers are read before the next tokens overwrite them
-        }
-    }
+    check_offsets(p, offs);
+    for (int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; t < p.T;
+         t += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        token_rows(p, offs, t, nullptr);
 }
 
-// Step 3 for a tile: the row numbers hash_index_kernel parked in the tile's own e_t rows.
-__device__ __forceinline__ void tile_rows(const HashGatherParams &p, int64_t *rows, int b, int64_t tile, int tid) {
-    const int64_t t0 = tile * p.tile_tokens;
-    const int ntok = static_cast<int>(p.T - t0 < p.tile_tokens ? p.T - t0 : p.tile_tokens);
-    const uint32_t et_bytes = static_cast<uint32_t>(p.tables) * p.row_bytes;
-    int64_t *r = rows + static_cast<size_t>(b) * p.tile_tokens * p.tables;
-    for (int e = tid; e < ntok * p.tables; e += kHashThreads) {
-        const int i = e / p.tables;
-        const int tb = e - i * p.tables;
-        r[e] = __ldcg(reinterpret_cast<const long long *>(p.out_rows + static_cast<size_t>(t0 + i) * et_bytes) + tb);
-    }
+// ---- steps 1-3 in one persistent kernel: a hash warp and the copy threads
+
+constexpr int kRowRing = 4;                        // tiles of row numbers the hash warp may run ahead
+constexpr int kGatherThreads = kHashThreads + 32;  // the copy threads, then the hash warp
+constexpr int kGatherSeqs = 512;                   // sequence offsets staged in shared memory up to this count
+
+// Dynamic shared memory of hash_gather_kernel, laid out by the host and the kernel alike.
+struct GatherSmemLayout {
+    uint32_t tiles;    // 2 tiles of e_t rows (tile_tokens x tables x row_bytes each)
+    uint32_t rows;     // int64 [kRowRing][tile_tokens][tables] row numbers
+    uint32_t offs;     // int64 [num_seqs + 1] staged offsets (or empty)
+    uint32_t bars;     // mbarriers: 2 tiles landed, kRowRing row numbers ready, kRowRing row numbers read
+    uint32_t total;
+};
+
+__host__ __device__ inline GatherSmemLayout gather_smem_layout(int tile_tokens, int tables, uint32_t row_bytes,
+                                                              int staged_entries) {
+    GatherSmemLayout L;
+    const uint32_t tile = static_cast<uint32_t>(tile_tokens) * tables * row_bytes;
+    L.tiles = 0;
+    L.rows = 2 * tile;
+    L.offs = L.rows + static_cast<uint32_t>(kRowRing) * tile_tokens * tables * 8u;
+    L.bars = L.offs + static_cast<uint32_t>(staged_entries) * 8u;
+    L.total = L.bars + (2u + 2u * kRowRing) * 8u;
+    return L;
 }
 
-// Step 3: a persistent CTA walks tiles of consecutive tokens, double-buffered; every table row of
-// a tile is fetched by one bulk asynchronous copy (TMA, 1-D) into the shared tile, in e_t order,
-// completing on the tile's mbarrier, and one bulk store writes the tile's adjacent e_t rows back
-// -- over the row numbers that were parked there, which the CTA read before issuing the copies.
-// The next tile's row numbers are read while the current tile's copies are in flight.
-__global__ void __launch_bounds__(kHashThreads) hash_gather_kernel(const __grid_constant__ HashGatherParams p) {
-    pdl_wait();  // the row numbers of hash_index_kernel are complete and visible
+// Named barrier 1 over the copy threads alone (the hash warp never takes part): true on every
+// copy thread when `v` holds on any.
+__device__ __forceinline__ bool copy_threads_any(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, 1, %2, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(v)), "n"(kHashThreads)
+        : "memory");
+    return r != 0;
+}
+
+// Steps 1-3.  A persistent CTA walks tiles of consecutive tokens (tile, tile + gridDim.x, ...).
+//   The hash warp (lane = token of the tile, token_rows) writes each tile's absolute row numbers
+//   into a ring of kRowRing slots, up to kRowRing tiles ahead, and marks the slot ready.
+//   The copy threads take a tile's row numbers, fetch every table row with one bulk asynchronous
+//   copy (TMA, 1-D) into a double-buffered shared tile in e_t order, completing on the tile's
+//   mbarrier, release the slot, and one thread stores the landed tile's adjacent e_t rows with a
+//   single bulk copy.
+// So the hashing runs beside the copies instead of before them.  All waits are bounded.
+__global__ void __launch_bounds__(kGatherThreads) hash_gather_kernel(const __grid_constant__ HashGatherParams p) {
+    pdl_wait();  // the previous kernel's writes are complete and visible
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x;
-    const HashSmemLayout L = hash_smem_layout(p.tile_tokens, p.tables, p.row_bytes, 0);
+    const int staged = p.staged_seqs ? p.num_seqs + 1 : 0;
+    const GatherSmemLayout L = gather_smem_layout(p.tile_tokens, p.tables, p.row_bytes, staged);
     uint8_t *tiles = smem + L.tiles;
     int64_t *rows = reinterpret_cast<int64_t *>(smem + L.rows);
-    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + L.bars);
+    int64_t *so = reinterpret_cast<int64_t *>(smem + L.offs);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + L.bars);  // [2] a tile's rows have landed
+    uint64_t *rows_full = bar + 2;                                  // [kRowRing] a slot's row numbers are ready
+    uint64_t *rows_empty = rows_full + kRowRing;                    // [kRowRing] a slot's row numbers were read
     const int64_t ntiles = (p.T + p.tile_tokens - 1) / p.tile_tokens;
     const uint32_t et_bytes = static_cast<uint32_t>(p.tables) * p.row_bytes;  // one token's e_t row
     const uint32_t tile_bytes = static_cast<uint32_t>(p.tile_tokens) * et_bytes;
+    const int slot_words = p.tile_tokens * p.tables;
     if (tid == 0) {
         mbar_init(&bar[0], 1);
         mbar_init(&bar[1], 1);
+        for (int i = 0; i < kRowRing; ++i) {
+            mbar_init(&rows_full[i], 1);
+            mbar_init(&rows_empty[i], kHashThreads);
+        }
         mbar_init_fence();
     }
+    const int64_t *offs = p.seq_offsets;
+    if (p.staged_seqs) {
+        for (int s = tid; s <= p.num_seqs; s += blockDim.x) so[s] = p.seq_offsets[s];
+        offs = so;
+    }
     __syncthreads();
+    check_offsets(p, offs);
 
-    int64_t tile = blockIdx.x;
-    if (tile < ntiles) tile_rows(p, rows, 0, tile, tid);
-    __syncthreads();
+    if (tid >= kHashThreads) {
+        // ---- the hash warp, from the CTA's second tile on
+        const int lane = tid - kHashThreads;
+        int k = 1;
+        for (int64_t tile = blockIdx.x + gridDim.x; tile < ntiles; tile += gridDim.x, ++k) {
+            const int slot = k & (kRowRing - 1);
+            if (k >= kRowRing) {  // the slot's previous tile was read by every copy thread
+                bool ok = true;
+                if (lane == 0) ok = mbar_wait_sleep(&rows_empty[slot], static_cast<uint32_t>((k / kRowRing - 1) & 1));
+                if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                    if (lane == 0) report(p.status, p.err_word, ENGRAM_DEVERR_TIMEOUT);
+                    break;
+                }
+            }
+            const int64_t t0 = tile * p.tile_tokens;
+            const int ntok = static_cast<int>(p.T - t0 < p.tile_tokens ? p.T - t0 : p.tile_tokens);
+            if (lane < ntok) token_rows(p, offs, t0 + lane, rows + static_cast<size_t>(slot) * slot_words + lane * p.tables);
+            __syncwarp();  // every lane's row numbers before the release
+            if (lane == 0) mbar_arrive(&rows_full[slot]);
+        }
+        return;
+    }
 
+    // ---- the copy threads: tile k's copies are issued before tile k - 1 is waited for and stored, so
+    // two tiles are in flight
     bool failed = false;
-    for (int it = 0; tile < ntiles; tile += gridDim.x, ++it) {
-        const int b = it & 1;
+    int k = 0;
+    int pend_k = -1;         // (thread 0) the tile issued last and not yet stored: its iteration,
+    int64_t pend_t0 = 0;     // first token
+    int pend_ntok = 0;       // and tokens
+    // (thread 0) waits until tile kk has landed in buffer kk & 1 and stores it; false on a timeout
+    auto land_and_store = [&](int kk, int64_t t0, int ntok) {
+        const int bb = kk & 1;
+        const uint32_t parity = static_cast<uint32_t>((kk >> 1) & 1);
+        if (!mbar_wait(&bar[bb], parity)) {
+            report(p.status, p.err_word, ENGRAM_DEVERR_TIMEOUT);
+            // the copies into this CTA's shared memory may still be in flight: wait once more
+            if (!mbar_wait(&bar[bb], parity)) report(p.status, p.err_word, ENGRAM_DEVERR_TIMEOUT);
+            return false;
+        }
+        bulk_store_commit(p.out_rows + static_cast<size_t>(t0) * et_bytes, tiles + static_cast<size_t>(bb) * tile_bytes,
+                          static_cast<uint32_t>(ntok) * et_bytes);
+        return true;
+    };
+    if (blockIdx.x < ntiles) {
+        // the CTA's first tile is hashed by the copy warps themselves, so that its copies start
+        // after two tables' hashes instead of all of them: warp w takes tables w, w + 8, ...
+        const int warp = tid >> 5, lane = tid & 31;
+        const int64_t t0 = static_cast<int64_t>(blockIdx.x) * p.tile_tokens;
+        const int ntok = static_cast<int>(p.T - t0 < p.tile_tokens ? p.T - t0 : p.tile_tokens);
+        if (lane < ntok) token_rows(p, offs, t0 + lane, rows + lane * p.tables, warp, kHashThreads / 32);
+        copy_threads_any(false);  // every copy warp's row numbers are in slot 0
+        if (tid == 0) mbar_arrive(&rows_full[0]);
+    }
+    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++k) {
+        const int b = k & 1, slot = k & (kRowRing - 1);
         const int64_t t0 = tile * p.tile_tokens;
         const int ntok = static_cast<int>(p.T - t0 < p.tile_tokens ? p.T - t0 : p.tile_tokens);
-        const int64_t next = tile + gridDim.x;
         uint8_t *tl = tiles + static_cast<size_t>(b) * tile_bytes;
         const int ncopies = ntok * p.tables;
 
-        // tile buffer b was last stored two tiles ago: once that store has read it, refill it
+        const bool got = mbar_wait_sleep(&rows_full[slot], static_cast<uint32_t>((k / kRowRing) & 1));
+        // buffer b held tile k - 2, whose store was issued in the previous iteration: once that store
+        // has read it, refill it
         if (tid == 0) {
-            bulk_wait_read_all_but_one();
-            mbar_arrive_expect_tx(&bar[b], static_cast<uint32_t>(ncopies) * p.row_bytes);
+            bulk_wait_read_all();
+            if (got) mbar_arrive_expect_tx(&bar[b], static_cast<uint32_t>(ncopies) * p.row_bytes);
         }
-        __syncthreads();
-        const int64_t *r = rows + static_cast<size_t>(b) * p.tile_tokens * p.tables;
+        if (copy_threads_any(!got)) {
+            if (tid == 0) report(p.status, p.err_word, ENGRAM_DEVERR_TIMEOUT);
+            failed = true;
+            break;
+        }
+        const int64_t *r = rows + static_cast<size_t>(slot) * slot_words;
         for (int e = tid; e < ncopies; e += kHashThreads)
             bulk_load_plain(tl + static_cast<size_t>(e) * p.row_bytes,
                             p.table + static_cast<size_t>(r[e]) * p.row_bytes, p.row_bytes, &bar[b]);
+        mbar_arrive(&rows_empty[slot]);  // this thread has read its row numbers from the slot
 
-        // the next tile's row numbers while those copies are in flight
-        if (next < ntiles) tile_rows(p, rows, b ^ 1, next, tid);
-
-        // when the tile has landed, one bulk store of its e_t rows
         if (tid == 0) {
-            const uint32_t parity = static_cast<uint32_t>((it >> 1) & 1);
-            if (!mbar_wait(&bar[b], parity)) {
-                report(p.status, p.err_word, ENGRAM_DEVERR_TIMEOUT);
-                // the copies into this CTA's shared memory may still be in flight: wait once more
-                if (!mbar_wait(&bar[b], parity)) report(p.status, p.err_word, ENGRAM_DEVERR_TIMEOUT);
-                failed = true;
-            }
-            if (!failed) bulk_store_commit(p.out_rows + static_cast<size_t>(t0) * et_bytes, tl,
-                                           static_cast<uint32_t>(ntok) * et_bytes);
+            if (pend_k >= 0 && !land_and_store(pend_k, pend_t0, pend_ntok)) failed = true;
+            pend_k = k, pend_t0 = t0, pend_ntok = ntok;
         }
-        if (__syncthreads_or(failed)) break;
+        if (copy_threads_any(failed)) break;
     }
-    if (tid == 0) bulk_wait_all();  // every store has completed before the CTA's shared memory goes away
+    if (tid == 0) {
+        // the last tile (after a failure: only wait for its copies)
+        if (pend_k >= 0) {
+            if (failed) {
+                const uint32_t parity = static_cast<uint32_t>((pend_k >> 1) & 1);
+                if (!mbar_wait(&bar[pend_k & 1], parity)) report(p.status, p.err_word, ENGRAM_DEVERR_TIMEOUT);
+            } else {
+                land_and_store(pend_k, pend_t0, pend_ntok);
+            }
+        }
+        bulk_wait_all();  // every store has completed before the CTA's shared memory goes away
+    }
 }
 
 // The same hash + gather with the table in page-locked host memory (NEXT-3: the paper's offload
@@ -565,30 +643,35 @@ extern "C" engram_status engram_hash_gather(const engram_hash_spec *spec, const 
     const int tables = p.tables;
     const int64_t row_bytes = p.row_bytes;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    // 1-2: one thread per token (>= 1 block: T = 0 still checks the offsets)
-    const int64_t iblocks =
-        std::max<int64_t>(1, std::min<int64_t>((a->T + kIndexThreads - 1) / kIndexThreads, 16LL * dev.num_sms));
-    p.staged_seqs = a->num_seqs + 1 <= kSmemSeqs ? 1 : 0;
-    const int ismem = index_smem_bytes(tables, p.staged_seqs ? a->num_seqs + 1 : 0);
-    if ((st = set_smem(reinterpret_cast<const void *>(hash_index_kernel), ismem)) != ENGRAM_OK) return st;
-    cudaError_t le = launch_kernel(hash_index_kernel, dim3(static_cast<unsigned>(iblocks)), dim3(kIndexThreads), ismem, s, p);
-    if (le != cudaSuccess) return fail(ENGRAM_ERR_CUDA, "engram_hash_gather launch: %s", cudaGetErrorString(le));
-    if ((st = check_launch("engram_hash_gather")) != ENGRAM_OK || !p.out_rows || a->T == 0) return st;
-    // 3: tiles of ~kTileBytes of e_t rows; persistent grid of as many CTAs as fit at once
+    if (!p.out_rows) {
+        // the index output alone: one thread per token (>= 1 block: T = 0 still checks the offsets)
+        const int64_t iblocks =
+            std::max<int64_t>(1, std::min<int64_t>((a->T + kIndexThreads - 1) / kIndexThreads, 16LL * dev.num_sms));
+        p.staged_seqs = a->num_seqs + 1 <= kSmemSeqs ? 1 : 0;
+        const int ismem = p.staged_seqs ? (a->num_seqs + 1) * 8 : 0;
+        if ((st = set_smem(reinterpret_cast<const void *>(hash_index_kernel), ismem)) != ENGRAM_OK) return st;
+        cudaError_t le =
+            launch_kernel(hash_index_kernel, dim3(static_cast<unsigned>(iblocks)), dim3(kIndexThreads), ismem, s, p);
+        if (le != cudaSuccess) return fail(ENGRAM_ERR_CUDA, "engram_hash_gather launch: %s", cudaGetErrorString(le));
+        return check_launch("engram_hash_gather");
+    }
+    // tiles of ~kTileBytes of e_t rows; persistent grid of as many CTAs as fit at once (>= 1 block:
+    // T = 0 still checks the offsets)
     const int et_bytes = static_cast<int>(row_bytes) * tables;
     p.tile_tokens = std::min(kTileMax, std::max(1, kTileBytes / et_bytes));
-    const HashSmemLayout L = hash_smem_layout(p.tile_tokens, tables, p.row_bytes, 0);
+    p.staged_seqs = a->num_seqs + 1 <= kGatherSeqs ? 1 : 0;
+    const GatherSmemLayout L = gather_smem_layout(p.tile_tokens, tables, p.row_bytes, p.staged_seqs ? a->num_seqs + 1 : 0);
     const int dyn = static_cast<int>(L.total);
     if (dyn > dev.smem_optin) return fail(ENGRAM_ERR_SHAPE, "engram_hash_gather: %d bytes of shared memory needed", dyn);
     if ((st = set_smem(reinterpret_cast<const void *>(hash_gather_kernel), dyn)) != ENGRAM_OK) return st;
     int per_sm = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, hash_gather_kernel, kHashThreads, dyn);
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, hash_gather_kernel, kGatherThreads, dyn);
     if (e != cudaSuccess) return fail(ENGRAM_ERR_CUDA, "engram_hash_gather occupancy: %s", cudaGetErrorString(e));
     const int64_t ntiles = (a->T + p.tile_tokens - 1) / p.tile_tokens;
     int64_t grid = static_cast<int64_t>(dev.num_sms) * std::max(per_sm, 1);
     if (grid > ntiles) grid = ntiles;
-    grid = cap_grid(grid);
-    le = launch_kernel(hash_gather_kernel, dim3(static_cast<unsigned>(grid)), dim3(kHashThreads), dyn, s, p);
+    grid = cap_grid(std::max<int64_t>(grid, 1));
+    cudaError_t le = launch_kernel(hash_gather_kernel, dim3(static_cast<unsigned>(grid)), dim3(kGatherThreads), dyn, s, p);
     if (le != cudaSuccess) return fail(ENGRAM_ERR_CUDA, "engram_hash_gather launch: %s", cudaGetErrorString(le));
     return check_launch("engram_hash_gather");
 }

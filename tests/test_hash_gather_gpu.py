@@ -185,6 +185,27 @@ def test_indices_are_reproducible_across_grids():
         ecm.set_max_ctas(0)
 
 
+def test_rows_reproducible_across_grids():
+    """One or three CTAs walk every tile, so the hash warp's ring of row-number slots wraps dozens of
+    times ahead of the copies; rows and indices match the default grid bit for bit and the oracle."""
+    lengths = [1500, 700, 1]
+    T = sum(lengths)
+    ids = G.uniform_int(91, T, 0, 3000)
+    w = _custom(ids, lengths, 2, 2, 8, 64, "bf16", vocab=3000, seed=8, anchor=5003)  # 16 tables, 2 KB e_t rows
+    table = SD.hash_table(w, DEV)
+    base_rows, base_idx = _run(w, table)
+    _check(w, table, base_rows, base_idx)
+    try:
+        for cap in (1, 3):
+            ecm.set_max_ctas(cap)
+            rows, idx = _run(w, table)
+            assert torch.equal(idx, base_idx)
+            assert torch.equal(rows.view(torch.int16), base_rows.view(torch.int16))
+    finally:
+        ecm.set_max_ctas(0)
+    assert ecm.device_status(clear=True) == 0
+
+
 # ----------------------------------------------------------------------------- tables in host memory
 
 @pytest.mark.parametrize("lengths,row_dim,dtype", [([64], 16, "f32"), ([31, 1, 0, 100], 64, "bf16"),
