@@ -7,10 +7,10 @@
 // GB300 design.  The convolution couples tokens only along time, one channel at a time, and the
 // RMSNorm couples channels only within a token, through one scalar.  So:
 //   * conv_rstd_kernel: a warp per token computes rstd = 1/sqrt(mean(V~^2) + eps);
-//   * conv_fwd_sweep_kernel: CTAs on one 512-channel block sweep residue classes t = r (mod
+//   * conv_fwd_sweep_kernel: CTAs on one 1024-channel block sweep residue classes t = r (mod
 //     dilation) of short time chunks.  A producer warp streams each token's V~ and H row segments
 //     and rstd into a ring of shared-memory stages with a record of the position; every thread
-//     carries its four channels' last three taps' inputs in registers, so each row is converted
+//     carries its eight channels' last three taps' inputs in registers, so each row is converted
 //     once;
 //   * conv_bwd_kernel (the backward, one pass): a thread-block cluster of ceil(d / 512) CTAs takes
 //     one residue class t = r (mod dilation) of one time chunk, each CTA 512 channels.  Every tap of
@@ -80,6 +80,43 @@ struct Ev4<__nv_bfloat16> {
     __device__ __forceinline__ static void store(uint8_t *p, const float (&x)[4]) {
         *reinterpret_cast<uint2 *>(p) =
             make_uint2(Vec<__nv_bfloat16>::pack2(x[0], x[1]), Vec<__nv_bfloat16>::pack2(x[2], x[3]));
+    }
+};
+
+// ---- eight channels per lane (the forward): 16 bytes of bf16 or 32 bytes of fp32, as four pairs
+
+template <typename E>
+struct Ev8;
+
+template <>
+struct Ev8<float> {
+    static constexpr int kBytes = 32;
+    __device__ __forceinline__ static void load4(const uint8_t *p, float2 (&x)[4]) {
+        const float4 u = *reinterpret_cast<const float4 *>(p);
+        const float4 v = *reinterpret_cast<const float4 *>(p + 16);
+        x[0] = make_float2(u.x, u.y), x[1] = make_float2(u.z, u.w);
+        x[2] = make_float2(v.x, v.y), x[3] = make_float2(v.z, v.w);
+    }
+    __device__ __forceinline__ static void store4(uint8_t *p, const float2 (&x)[4]) {
+        *reinterpret_cast<float4 *>(p) = make_float4(x[0].x, x[0].y, x[1].x, x[1].y);
+        *reinterpret_cast<float4 *>(p + 16) = make_float4(x[2].x, x[2].y, x[3].x, x[3].y);
+    }
+};
+
+template <>
+struct Ev8<__nv_bfloat16> {
+    static constexpr int kBytes = 16;
+    __device__ __forceinline__ static float2 unpack(uint32_t w) {
+        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+    }
+    __device__ __forceinline__ static void load4(const uint8_t *p, float2 (&x)[4]) {
+        const uint4 u = *reinterpret_cast<const uint4 *>(p);
+        x[0] = unpack(u.x), x[1] = unpack(u.y), x[2] = unpack(u.z), x[3] = unpack(u.w);
+    }
+    __device__ __forceinline__ static void store4(uint8_t *p, const float2 (&x)[4]) {
+        *reinterpret_cast<uint4 *>(p) =
+            make_uint4(Vec<__nv_bfloat16>::pack2(x[0].x, x[0].y), Vec<__nv_bfloat16>::pack2(x[1].x, x[1].y),
+                       Vec<__nv_bfloat16>::pack2(x[2].x, x[2].y), Vec<__nv_bfloat16>::pack2(x[3].x, x[3].y));
     }
 };
 
@@ -832,11 +869,15 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
 
 // ------------------------------------------------------------------------------- forward, swept
 
-constexpr int kFwWarps = 4;                       // consumer warps, four channels per thread
+constexpr int kFwWarps = 4;                       // consumer warps
+constexpr int kFwEV = 8;                          // channels per consumer thread (four pairs)
+constexpr int kFwPairs = kFwEV / 2;
 constexpr int kFwCons = kFwWarps * 32;
 constexpr int kFwThreads = kFwCons + 32;          // + the copy producer's warp
-constexpr int kFwCW = kFwCons * kScEV;            // channels per CTA (one channel block)
-constexpr int kFwStages = 16;
+constexpr int kFwCW = kFwCons * kFwEV;            // channels per CTA (one channel block)
+// ring stages: 16 of 4 KB (bf16), 8 of 8 KB (fp32)
+template <typename E>
+__host__ __device__ constexpr int sc_fwd_stages() { return sizeof(E) == 2 ? 16 : 8; }
 constexpr int kFwChunk = 128;                     // tokens per work item's time chunk
 
 struct ScFwdSweepParams {
@@ -858,25 +899,25 @@ __host__ __device__ constexpr int sc_fwd_stage_bytes() {
 // the ring, the stages' position records, full and empty mbarriers, the producer's state
 template <typename E>
 __host__ __device__ constexpr int sc_fwd_sweep_smem() {
-    return kFwStages * sc_fwd_stage_bytes<E>() + kFwStages * 16 + 2 * kFwStages * 8 + 128;
+    return sc_fwd_stages<E>() * (sc_fwd_stage_bytes<E>() + 16 + 2 * 8) + 128;
 }
 
-// The forward as a sweep.  CTA (block cb, j) owns channels [512 cb, 512 cb + 512) and the work items
+// The forward as a sweep.  CTA (block cb, j) owns channels [1024 cb, 1024 cb + 1024) and the work items
 // j, j + per_blk, ... of that block, each one residue class t = r mod dilation of one time chunk.
 // Its producer warp walks the items' segments and streams, per sweep position, the token's V~ and
 // H row segments (1-D bulk copies) and rstd (a 4-byte asynchronous copy) into a ring of stages,
 // with a record of the position; a segment starts with up to three lead-in tokens whose V~ the
-// first taps read.  Every consumer thread owns four channels (two pairs) and carries the last three
+// first taps read.  Every consumer thread owns eight channels (four pairs) and carries the last three
 // taps' inputs u = V~ rstd in registers (slot q mod 4 for position q), so each row is converted
 // once:
 //   conv = bias + sum_a (conv_w[width-1-a] norm_w) u[t - a dil]   (a = 0, 1, 2, 3 in order),
 //   out  = H + SiLU(conv) + V~,
 // the taps before a sequence's start being zero.  All waits are bounded.
 template <typename E, bool HAS_H>
-__global__ void __launch_bounds__(kFwThreads, 6) conv_fwd_sweep_kernel(const __grid_constant__ ScFwdSweepParams p) {
-    using EV = Ev4<E>;
+__global__ void __launch_bounds__(kFwThreads, 3) conv_fwd_sweep_kernel(const __grid_constant__ ScFwdSweepParams p) {
+    using EV = Ev8<E>;
     extern __shared__ __align__(128) uint8_t smem[];
-    constexpr int S = kFwStages;
+    constexpr int S = sc_fwd_stages<E>();
     constexpr int SB = sc_fwd_stage_bytes<E>();
     constexpr int half = SB / 2;
     uint8_t *ring = smem;
@@ -1022,16 +1063,16 @@ __global__ void __launch_bounds__(kFwThreads, 6) conv_fwd_sweep_kernel(const __g
                 mbar_wait(&full[q2 % S], (q2 / S) & 1u, kWaitLimitNs / 16);
     } else {
         // ---- consumers
-        const bool active = tid * kScEV < ncols;
+        const bool active = tid * kFwEV < ncols;
         const uint8_t *my_ring = ring + tid * EV::kBytes;  // this thread's channels in stage 0
         const int width = p.width, d = p.d;
-        float2 K[kScAges][2], bias[2];  // taps by age folded with norm_w; [h]: channels 2h, 2h + 1
+        float2 K[kScAges][kFwPairs], bias[kFwPairs];  // taps by age folded with norm_w; [h]: channels 2h, 2h + 1
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < kFwPairs; ++h) {
             float v[2][1 + kScAges];
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
-                const int c = c0 + tid * kScEV + 2 * h + k;
+                const int c = c0 + tid * kFwEV + 2 * h + k;
                 const bool ok = active && c < d;
                 const float nwc = ok ? __ldg(p.norm_w + c) : 0.f;
                 v[k][0] = ok && p.bias ? __ldg(p.bias + c) : 0.f;
@@ -1045,7 +1086,7 @@ __global__ void __launch_bounds__(kFwThreads, 6) conv_fwd_sweep_kernel(const __g
             for (int a = 0; a < kScAges; ++a) K[a][h] = make_float2(v[0][1 + a], v[1][1 + a]);
         }
         uint8_t *out_col = p.out + static_cast<size_t>(c0) * sizeof(E) + tid * EV::kBytes;
-        float2 U[4][2];  // u = V~ rstd by slot
+        float2 U[4][kFwPairs];  // u = V~ rstd by slot
         static_assert((S & (S - 1)) == 0, "stage and phase from the position count by mask and shift");
         constexpr int kLogS = S == 16 ? 4 : (S == 32 ? 5 : 3);
         static_assert((1 << kLogS) == S, "the ring's size is 8, 16 or 32");
@@ -1076,22 +1117,24 @@ __global__ void __launch_bounds__(kFwThreads, 6) conv_fwd_sweep_kernel(const __g
             const int st = stage_of(decltype(Kc)::v);
             const uint8_t *stg = my_ring + st * SB;
             const float2 rt = p2(meta[st].rstd);
-            float2 x[2];
-            EV::load2(stg, x);
+            float2 x[kFwPairs];
+            EV::load4(stg, x);
 #pragma unroll
-            for (int h = 0; h < 2; ++h) U[J][h] = p2mul(x[h], rt);
+            for (int h = 0; h < kFwPairs; ++h) U[J][h] = p2mul(x[h], rt);
             if (!lead) {
-                float2 y[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-                if (HAS_H) EV::load2(stg + half, y);
-                float2 o[2];
+                float2 y[kFwPairs];
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
+                for (int h = 0; h < kFwPairs; ++h) y[h] = make_float2(0.f, 0.f);
+                if (HAS_H) EV::load4(stg + half, y);
+                float2 o[kFwPairs];
+#pragma unroll
+                for (int h = 0; h < kFwPairs; ++h) {
                     const float2 c = p2fma(K[3][h], U[(J + 1) & 3][h],
                                            p2fma(K[2][h], U[(J + 2) & 3][h],
                                                  p2fma(K[1][h], U[(J + 3) & 3][h], p2fma(K[0][h], U[J][h], bias[h]))));
                     o[h] = p2fma(c, p2sigmoid(c), p2add(x[h], y[h]));
                 }
-                if (active) EV::store2(out_col + meta[st].row, o);
+                if (active) EV::store4(out_col + meta[st].row, o);
             }
             if (!GROUP) {
                 __syncwarp();
@@ -1106,7 +1149,7 @@ __global__ void __launch_bounds__(kFwThreads, 6) conv_fwd_sweep_kernel(const __g
             if (fl & (kFlDone | kFlSegStart)) {
                 if (fl & kFlDone) break;
 #pragma unroll
-                for (int h = 0; h < 2; ++h) U[0][h] = U[1][h] = U[2][h] = U[3][h] = make_float2(0.f, 0.f);
+                for (int h = 0; h < kFwPairs; ++h) U[0][h] = U[1][h] = U[2][h] = U[3][h] = make_float2(0.f, 0.f);
             }
             if (fl & kFlGroup) {
                 // all four stages first, so that the four positions' loads and arithmetic may overlap
