@@ -18,6 +18,7 @@
 #include <algorithm>
 #include <mutex>
 
+#include "colsum.cuh"
 #include "gate_pipeline.cuh"
 
 namespace engram {
@@ -213,99 +214,24 @@ __global__ void __launch_bounds__((NCW + 1) * 32) gate_bwd_kernel(const __grid_c
     }
 }
 
-// S = sum_p partial[p], one column at a time in a fixed order that depends on P only:
-//   kRG row groups, group g summing the contiguous partials [g R, min(P, (g + 1) R)),
-//   R = ceil(P / kRG), in ascending order;
-//   kRG / kRun runs of kRun consecutive group sums, each in ascending order;
-//   the run sums in ascending order.
-// A CTA of kRedThreads threads per SM owns a contiguous share of the float4 columns (the shares
-// differ by one column at most), chunks of kRedCols columns at a time: thread i of a chunk takes
-// column i mod ncols of group i / ncols and keeps kReduceBatch 16-byte loads in flight, so about
-// 128 KB of partials are in flight on every SM.  Which CTA owns a column does not change its sums.
-constexpr int kRG = 128;
-constexpr int kRun = 16;
-constexpr int kRedThreads = 1024;
-constexpr int kRedCols = kRedThreads / kRG;  // float4 columns per chunk
-constexpr int kReduceBatch = 8;
-static_assert(kRG % kRun == 0 && kRG / kRun <= 32, "run sums");
-
-__global__ void __launch_bounds__(kRedThreads, 1)
+// S = sum_p partial[p] (column_sums: an order that depends on P only), then the accumulate.
+__global__ void __launch_bounds__(kColThreads, 1)
     grad_w_reduce_kernel(const float4 *__restrict__ part, int32_t P, int32_t d4, float4 *__restrict__ dweight,
                          const float4 *__restrict__ w_h, const float4 *__restrict__ w_k, float4 *__restrict__ g_h,
                          float4 *__restrict__ g_k) {
     pdl_wait();
-    __shared__ float4 gsum[kRG * kRedCols];                // [group][column of the chunk]
-    __shared__ float4 rsum[(kRG / kRun) * kRedCols];       // [run][column of the chunk]
-    const int tid = threadIdx.x;
-    const int c_begin = static_cast<int>(static_cast<int64_t>(blockIdx.x) * d4 / gridDim.x);
-    const int c_end = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * d4 / gridDim.x);
-    const int rows = (P + kRG - 1) / kRG;
-    for (int cc = c_begin; cc < c_end; cc += kRedCols) {
-        const int ncols = c_end - cc < kRedCols ? c_end - cc : kRedCols;
-        // group sums: thread i -> column i mod ncols of group i / ncols
-        if (tid < ncols * kRG) {
-            const int g = tid / ncols;
-            const int j = tid - g * ncols;
-            const int p0 = g * rows;
-            const int p1 = p0 + rows < P ? p0 + rows : P;
-            const float4 *src = part + cc + j;
-            float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int q0 = p0; q0 < p1; q0 += kReduceBatch) {
-                float4 x[kReduceBatch];
-#pragma unroll
-                for (int b = 0; b < kReduceBatch; ++b)
-                    if (q0 + b < p1) x[b] = __ldg(src + static_cast<size_t>(q0 + b) * d4);
-#pragma unroll
-                for (int b = 0; b < kReduceBatch; ++b)
-                    if (q0 + b < p1) {
-                        s.x += x[b].x;
-                        s.y += x[b].y;
-                        s.z += x[b].z;
-                        s.w += x[b].w;
-                    }
-            }
-            gsum[g * kRedCols + j] = s;
+    __shared__ ColSumSmem sm;
+    column_sums(part, P, d4, sm, [&](int col, const float4 &t) {
+        if (dweight) dweight[col] = t;
+        if (g_h) {
+            const float4 a = w_k[col], b = w_h[col];
+            float4 gh = g_h[col], gk = g_k[col];
+            gh.x += t.x * a.x; gh.y += t.y * a.y; gh.z += t.z * a.z; gh.w += t.w * a.w;
+            gk.x += t.x * b.x; gk.y += t.y * b.y; gk.z += t.z * b.z; gk.w += t.w * b.w;
+            g_h[col] = gh;
+            g_k[col] = gk;
         }
-        __syncthreads();
-        // run sums: thread i -> column i mod ncols of run i / ncols
-        if (tid < ncols * (kRG / kRun)) {
-            const int u = tid / ncols;
-            const int j = tid - u * ncols;
-            float4 t = gsum[(u * kRun) * kRedCols + j];
-#pragma unroll
-            for (int q = 1; q < kRun; ++q) {
-                const float4 x = gsum[(u * kRun + q) * kRedCols + j];
-                t.x += x.x;
-                t.y += x.y;
-                t.z += x.z;
-                t.w += x.w;
-            }
-            rsum[u * kRedCols + j] = t;
-        }
-        __syncthreads();
-        if (tid < ncols) {
-            const int col = cc + tid;
-            float4 t = rsum[tid];
-#pragma unroll
-            for (int u = 1; u < kRG / kRun; ++u) {
-                const float4 x = rsum[u * kRedCols + tid];
-                t.x += x.x;
-                t.y += x.y;
-                t.z += x.z;
-                t.w += x.w;
-            }
-            if (dweight) dweight[col] = t;
-            if (g_h) {
-                const float4 a = w_k[col], b = w_h[col];
-                float4 gh = g_h[col], gk = g_k[col];
-                gh.x += t.x * a.x; gh.y += t.y * a.y; gh.z += t.z * a.z; gh.w += t.w * a.w;
-                gk.x += t.x * b.x; gk.y += t.y * b.y; gk.z += t.z * b.z; gk.w += t.w * b.w;
-                g_h[col] = gh;
-                g_k[col] = gk;
-            }
-        }
-        __syncthreads();  // the chunk's sums are read before the next chunk's overwrite them
-    }
+    });
 }
 
 namespace {
@@ -430,9 +356,9 @@ extern "C" engram_status engram_grad_w_reduce(const float *dw_partial, int32_t P
         if ((st = check_device_ptr(ptrs[i], dev.device, names[i])) != ENGRAM_OK) return st;
     const int d4 = d / 4;
     // one CTA per SM, no more than there are columns
-    const int blocks = static_cast<int>(cap_grid(std::max(1, std::min(d4, dev.num_sms))));
     cudaError_t e = launch_kernel(
-        grad_w_reduce_kernel, dim3(blocks), dim3(kRedThreads), 0, reinterpret_cast<cudaStream_t>(stream),
+        grad_w_reduce_kernel, dim3(column_sum_grid(d4, dev.num_sms)), dim3(kColThreads), 0,
+        reinterpret_cast<cudaStream_t>(stream),
         reinterpret_cast<const float4 *>(dw_partial), P, d4, reinterpret_cast<float4 *>(dweight_fused),
         reinterpret_cast<const float4 *>(w_h), reinterpret_cast<const float4 *>(w_k),
         reinterpret_cast<float4 *>(grad_w_h), reinterpret_cast<float4 *>(grad_w_k));
@@ -549,8 +475,7 @@ extern "C" engram_status engram_gate_bwd_reduce_noalloc(
 
     // Ordered reduction of the partials, on the same stream.
     const int d4 = d / 4;
-    const int blocks = static_cast<int>(cap_grid(std::max(1, std::min(d4, dev.num_sms))));
-    grad_w_reduce_kernel<<<blocks, kRedThreads, 0, s>>>(
+    grad_w_reduce_kernel<<<column_sum_grid(d4, dev.num_sms), kColThreads, 0, s>>>(
         reinterpret_cast<const float4 *>(scratch), P, d4, reinterpret_cast<float4 *>(dweight_fused),
         reinterpret_cast<const float4 *>(w_h), reinterpret_cast<const float4 *>(w_k),
         reinterpret_cast<float4 *>(grad_w_h), reinterpret_cast<float4 *>(grad_w_k));

@@ -28,7 +28,7 @@
 #include <algorithm>
 #include <atomic>
 
-#include "engram_internal.cuh"
+#include "colsum.cuh"
 
 namespace engram {
 
@@ -1178,37 +1178,25 @@ __global__ void __launch_bounds__(kFwThreads, 3) conv_fwd_sweep_kernel(const __g
 
 // ------------------------------------------------------------------------------- weight-gradient reduction
 
-constexpr int kScRG = 64;
-constexpr int kScCV = 4;
-
-// S[j] = sum_p partial[p, j] over the (width + 2) * d columns: 64 groups of consecutive partials,
-// each summed in ascending order, then the groups in ascending order.  Then
-// dconv_w[c, i] = S[i * d + c], dbias[c] = S[width * d + c], dnorm_w[c] = S[(width + 1) * d + c].
-__global__ void __launch_bounds__(kScRG *kScCV)
-    conv_grad_reduce_kernel(const float *__restrict__ part, int32_t P, int32_t width, int32_t d,
+// S = sum_p partial[p] over the (width + 2) * d columns (column_sums: an order that depends on P
+// only), then dconv_w[c, i] = S[i * d + c], dbias[c] = S[width * d + c], dnorm_w[c] = S[(width + 1) * d + c]
+// (d is a multiple of 4, so the four columns of a float4 lie in one row of S).
+__global__ void __launch_bounds__(kColThreads, 1)
+    conv_grad_reduce_kernel(const float4 *__restrict__ part, int32_t P, int32_t width, int32_t d,
                             float *__restrict__ dconv_w, float *__restrict__ dbias, float *__restrict__ dnorm_w) {
-    __shared__ float sums[kScRG][kScCV];
-    const int64_t ncol = static_cast<int64_t>(width + 2) * d;
-    const int cv = threadIdx.x % kScCV;
-    const int g = threadIdx.x / kScCV;
-    const int64_t col = static_cast<int64_t>(blockIdx.x) * kScCV + cv;
-    const int per = (P + kScRG - 1) / kScRG;
-    const int p0 = g * per;
-    const int p1 = p0 + per < P ? p0 + per : P;
-    float s = 0.f;
-    if (col < ncol)
-        for (int q = p0; q < p1; ++q) s += __ldcs(part + static_cast<size_t>(q) * ncol + col);
-    sums[g][cv] = s;
-    __syncthreads();
-    if (g == 0 && col < ncol) {
-        float t = sums[0][cv];
-        for (int q = 1; q < kScRG; ++q) t += sums[q][cv];
-        const int row = static_cast<int>(col / d), c = static_cast<int>(col % d);
-        if (row < width) dconv_w[static_cast<size_t>(c) * width + row] = t;
-        else if (row == width) {
-            if (dbias) dbias[c] = t;
-        } else dnorm_w[c] = t;
-    }
+    __shared__ ColSumSmem sm;
+    const int d4 = (width + 2) * (d / 4);
+    column_sums(part, P, d4, sm, [&](int col, const float4 &t) {
+        const int row = (4 * col) / d, c = 4 * col - row * d;
+        const float v[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (row < width) dconv_w[static_cast<size_t>(c + i) * width + row] = v[i];
+            else if (row == width) {
+                if (dbias) dbias[c + i] = v[i];
+            } else dnorm_w[c + i] = v[i];
+        }
+    });
 }
 
 // ------------------------------------------------------------------------------- host side
@@ -1435,13 +1423,14 @@ extern "C" engram_status engram_short_conv_grad_reduce(const float *dw_partial, 
     if (P < 0 || d <= 0 || width < 1 || width > kScAges)
         return fail(ENGRAM_ERR_SHAPE, "%s: P = %d, d = %d, width = %d", fn, P, d, width);
     if ((!dw_partial && P > 0) || !dconv_w || !dnorm_w) return fail(ENGRAM_ERR_NULL, "%s: NULL pointer", fn);
+    if (d % 4 != 0) return fail(ENGRAM_ERR_ALIGN, "%s: d = %d is not a multiple of 4", fn, d);
+    if ((static_cast<int64_t>(width) + 2) * (d / 4) > 0x7fffffff) return fail(ENGRAM_ERR_SHAPE, "%s: d = %d", fn, d);
     const void *ptrs[] = {dw_partial, dconv_w, dbias, dnorm_w};
     DeviceInfo dev;
-    engram_status st = sc_ptrs(fn, ptrs, 4, 0, &dev);
+    engram_status st = sc_ptrs(fn, ptrs, 4, 1, &dev);  // the partials are read as float4
     if (st != ENGRAM_OK) return st;
-    const int64_t ncol = static_cast<int64_t>(width + 2) * d;
-    conv_grad_reduce_kernel<<<static_cast<unsigned>((ncol + kScCV - 1) / kScCV), kScRG * kScCV, 0,
-                              reinterpret_cast<cudaStream_t>(stream)>>>(dw_partial, P, width, d, dconv_w, dbias,
-                                                                         dnorm_w);
+    const int d4 = (width + 2) * (d / 4);
+    conv_grad_reduce_kernel<<<column_sum_grid(d4, dev.num_sms), kColThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        reinterpret_cast<const float4 *>(dw_partial), P, width, d, dconv_w, dbias, dnorm_w);
     return check_launch(fn);
 }

@@ -28,6 +28,7 @@
 // partials and the reduced columns are bitwise reproducible for any grid.
 #include <algorithm>
 
+#include "colsum.cuh"
 #include "gate_pipeline.cuh"
 
 namespace engram {
@@ -365,43 +366,13 @@ __global__ void __launch_bounds__(kSkThreads, 1) sinkhorn_finalize_kernel(const 
 
 // ------------------------------------------------------------------------------- ordered reduction
 
-constexpr int kSkRG = 64;  // row groups of the partials
-constexpr int kSkCV = 4;   // float4 columns per CTA
-
-// Column c of S = sum_p partial[p, c]: thread group r sums partials [r * R, (r + 1) * R) in
-// ascending order, then the 64 group sums are added in ascending order.  The order depends on P
-// only.  With col_scale given, col_scale[c] /= sqrt(S) + eps in place.
-__global__ void __launch_bounds__(kSkRG *kSkCV)
+// S = sum_p partial[p] (column_sums: an order that depends on P only).  With col_scale given,
+// col_scale[c] /= sqrt(S[c]) + eps in place.
+__global__ void __launch_bounds__(kColThreads, 1)
     sinkhorn_reduce_kernel(const float4 *__restrict__ part, int32_t P, int32_t d4, float4 *__restrict__ col_sumsq,
                            float4 *__restrict__ col_scale, float eps) {
-    __shared__ float4 sums[kSkRG][kSkCV];
-    const int cv = threadIdx.x % kSkCV;
-    const int r = threadIdx.x / kSkCV;
-    const int col = blockIdx.x * kSkCV + cv;
-    const int per = (P + kSkRG - 1) / kSkRG;
-    const int p0 = r * per;
-    const int p1 = p0 + per < P ? p0 + per : P;
-    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (col < d4) {
-        for (int q = p0; q < p1; ++q) {
-            const float4 x = __ldcs(part + static_cast<size_t>(q) * d4 + col);
-            s.x += x.x;
-            s.y += x.y;
-            s.z += x.z;
-            s.w += x.w;
-        }
-    }
-    sums[r][cv] = s;
-    __syncthreads();
-    if (r == 0 && col < d4) {
-        float4 t = sums[0][cv];
-        for (int q = 1; q < kSkRG; ++q) {
-            const float4 x = sums[q][cv];
-            t.x += x.x;
-            t.y += x.y;
-            t.z += x.z;
-            t.w += x.w;
-        }
+    __shared__ ColSumSmem sm;
+    column_sums(part, P, d4, sm, [&](int col, const float4 &t) {
         if (col_sumsq) col_sumsq[col] = t;
         if (col_scale) {
             float4 c = col_scale[col];
@@ -411,7 +382,7 @@ __global__ void __launch_bounds__(kSkRG *kSkCV)
             c.w /= sqrtf(t.w) + eps;
             col_scale[col] = c;
         }
-    }
+    });
 }
 
 // ------------------------------------------------------------------------------- momentum
@@ -690,7 +661,7 @@ extern "C" engram_status engram_sinkhorn_step_reduce(const float *col_sumsq_part
     DeviceInfo dev;
     if ((st = sk_check_ptrs(fn, ptrs, 3, 3, &dev)) != ENGRAM_OK) return st;
     const int d4 = head_dim / 4;
-    sinkhorn_reduce_kernel<<<(d4 + kSkCV - 1) / kSkCV, kSkRG * kSkCV, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+    sinkhorn_reduce_kernel<<<column_sum_grid(d4, dev.num_sms), kColThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
         reinterpret_cast<const float4 *>(col_sumsq_partial), P, d4, reinterpret_cast<float4 *>(col_sumsq),
         reinterpret_cast<float4 *>(col_scale), eps);
     return check_launch(fn);

@@ -381,8 +381,9 @@ engram_status engram_short_conv_bwd(const void *dout, const void *v, engram_dtyp
 
 /*
  * dconv_w [d, width], dbias [d] (nullable) and dnorm_w [d] = the sums of the P partial rows of
- * engram_short_conv_bwd, in a fixed order that depends on P only (64 groups of consecutive
- * partials, each in ascending order, then the groups in ascending order).  P = 0 writes zeros.
+ * engram_short_conv_bwd, in a fixed order that depends on P only (128 groups of ceil(P / 128) consecutive partials, each summed in ascending order; runs of 16
+ * consecutive group sums, each in ascending order; then the 8 run sums in ascending order).
+ * P = 0 writes zeros.  dw_partial 16-byte aligned; d a multiple of 4.
  */
 engram_status engram_short_conv_grad_reduce(const float *dw_partial, int32_t P, int32_t width, int32_t d,
                                             float *dconv_w, float *dbias, float *dnorm_w, engram_stream_t stream);
@@ -430,8 +431,8 @@ engram_status engram_sinkhorn_step(const float *matrix, float *row_scale, const 
 
 /*
  * col_sumsq[c] = sum over p < P of col_sumsq_partial[p, c] in a fixed order that depends on P
- * only (groups of ceil(P / 64) consecutive partials, each summed in ascending order, then the
- * groups in ascending order).  col_sumsq [head_dim] is nullable; when col_scale [head_dim] is
+ * only (128 groups of ceil(P / 128) consecutive partials, each summed in ascending order; runs of 16
+ * consecutive group sums, each in ascending order; then the 8 run sums in ascending order).  col_sumsq [head_dim] is nullable; when col_scale [head_dim] is
  * given, the column step of the alternating iteration is applied in place:
  *     col_scale[c] = col_scale[c] / (sqrt(col_sumsq[c]) + eps).
  * At least one of the two outputs must be given.  16-byte aligned device pointers.
