@@ -185,6 +185,22 @@ def test_indices_are_reproducible_across_grids():
         ecm.set_max_ctas(0)
 
 
+def test_many_sequences_offsets_in_global_memory():
+    """More sequences than either kernel stages in shared memory (the gather above 511, the
+    index-only kernel above 4095): the sequence-start search then reads the offsets from global
+    memory.  5000 sequences of 0 to 7 tokens, rows and indices against the oracle."""
+    lengths = [int(x) for x in G.uniform_int(4242, 5000, 0, 8)]
+    T = sum(lengths)
+    ids = G.uniform_int(4243, T, 0, 3000)
+    w = _custom(ids, lengths, 2, 2, 8, 64, "bf16", vocab=3000, seed=13, anchor=5003)
+    table = SD.hash_table(w, DEV)
+    rows, idx = _run(w, table)
+    _check(w, table, rows, idx)
+    _, idx_only = _run(w, table, want_rows=False)
+    assert torch.equal(idx_only, idx)
+    assert ecm.device_status(clear=True) == 0
+
+
 def test_rows_reproducible_across_grids():
     """One or three CTAs walk every tile, so the hash warp's ring of row-number slots wraps dozens of
     times ahead of the copies; rows and indices match the default grid bit for bit and the oracle."""
