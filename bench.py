@@ -543,6 +543,11 @@ def main_only(args, device):
 
             def launch():
                 ecm.short_conv_fwd(v, nw, cwt, offs, cw.dilation, h=h, bias=bias, out=out, rstd=rstd)
+        elif op == "short_conv_fwd_given":  # the same with rstd given (made by the gate): rstd read
+            nbytes = 3 * T * d * 2 + 4 * T
+
+            def launch():
+                ecm.short_conv_fwd(v, nw, cwt, offs, cw.dilation, h=h, bias=bias, out=out, given_rstd=rstd)
         elif op == "short_conv_bwd":  # dout, V~, rstd read; dv and the partials written
             nbytes = 3 * T * d * 2 + 4 * T + P * (cw.width + 2) * d * 4
 
@@ -587,6 +592,31 @@ def main_only(args, device):
                     fns[k][1]()
         else:
             nbytes, launch = fns[op]
+    elif op.startswith("gate_conv"):
+        # the gate's forward and the short conv after it, T = 16384, d = 4096 bf16: with the conv's own
+        # statistic pass (gate_conv_fwd) or with the statistic made by the gate (gate_conv_fwd_fused)
+        wl, cw = W.gate_train_4k(), W.short_conv_4x4k()
+        t = SD.gate_device_inputs(wl, device)
+        T, d = wl.T, wl.d
+        wf = ecm.fuse_weight(t["w_h"], t["w_k"])
+        h = SD.normal_tensor((T, d), cw.seed + 2, 0.0, 1.0, "bf16", device)
+        nw = SD.normal_tensor((1, d), cw.seed + 4, 1.0, 0.1, "f32", device).reshape(-1)
+        cwt = SD.normal_tensor((d, cw.width), cw.seed + 5, 0.0, 0.5, "f32", device)
+        bias = SD.normal_tensor((1, d), cw.seed + 6, 0.0, 0.1, "f32", device).reshape(-1)
+        offs = torch.arange(0, T + 1, 4096, dtype=torch.int64, device=device)
+        vt, *st = ecm.gate_fwd(t["h"], t["k"], t["v"], wf, EPS)
+        _, *_, vstat = ecm.gate_fwd_rms(t["h"], t["k"], t["v"], wf, EPS, out_eps=cw.eps, stats=st)
+        out, rstd = ecm.short_conv_fwd(vt, nw, cwt, offs, cw.dilation, h=h, bias=bias, eps=cw.eps)
+        nbytes = T * (8 * d + 16) + 3 * T * d * 2 + 4 * T  # the two ops' own bytes
+
+        if op == "gate_conv_fwd_fused":
+            def launch():
+                ecm.gate_fwd_rms(t["h"], t["k"], t["v"], wf, EPS, out_eps=cw.eps, out=vt, stats=st, out_rstd=vstat)
+                ecm.short_conv_fwd(vt, nw, cwt, offs, cw.dilation, h=h, bias=bias, out=out, given_rstd=vstat)
+        else:
+            def launch():
+                ecm.gate_fwd(t["h"], t["k"], t["v"], wf, EPS, out=vt, stats=st)
+                ecm.short_conv_fwd(vt, nw, cwt, offs, cw.dilation, h=h, bias=bias, eps=cw.eps, out=out, rstd=rstd)
     else:
         wl = {"gate_fwd_2k": W.gate_fwd_2k()}.get(op, W.gate_train_4k())
         t = SD.gate_device_inputs(wl, device)
@@ -735,7 +765,8 @@ def main():
     ap.add_argument("--only", choices=["hash_gather", "hash_gather_small", "hash_gather_host", "gate_fwd",
                                        "gate_fwd_2k", "gate_bwd", "grad_w_reduce", "gate_hc_fwd", "gate_hc_bwd",
                                        "sinkhorn", "sinkhorn_momentum", "sinkhorn_step", "sinkhorn_reduce",
-                                       "sinkhorn_finalize", "short_conv_fwd", "short_conv_bwd", "short_conv_reduce"],
+                                       "sinkhorn_finalize", "short_conv_fwd", "short_conv_fwd_given", "short_conv_bwd",
+                                       "short_conv_reduce", "gate_conv_fwd", "gate_conv_fwd_fused"],
                     help="time one kernel alone on its workload (consecutive launches, L2 not flushed)")
     args = ap.parse_args()
     if args.warmup < 3:

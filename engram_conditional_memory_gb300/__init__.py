@@ -21,6 +21,7 @@ from .binding import (  # noqa: F401
     gate_bwd_reduce_noalloc,
     gate_bwd_num_partials,
     gate_fwd,
+    gate_fwd_rms,
     gate_hc_bwd,
     gate_hc_fwd,
     grad_w_reduce,

@@ -78,6 +78,8 @@ def load_library():
             "engram_hash_gather_host": (st, [_p, _p, _p]),
             "engram_fuse_weight": (st, [_p, _p, _c.c_int, _p, _i32, _p]),
             "engram_gate_fwd": (st, [_p, _p, _p, _c.c_int, _p, _i64, _i32, _c.c_float, _p, _p, _p, _p, _p, _p]),
+            "engram_gate_fwd_rms": (st, [_p, _p, _p, _c.c_int, _p, _i64, _i32, _c.c_float, _p, _p, _p, _p, _p, _p,
+                                         _c.c_float, _p]),
             "engram_gate_bwd_num_partials": (st, [_i64, _i32, _p]),
             "engram_gate_bwd": (st, [_p, _p, _p, _p, _c.c_int, _p, _p, _p, _p, _p, _i64, _i32, _p, _p, _p, _p,
                                      _i32, _p]),
@@ -90,6 +92,8 @@ def load_library():
                                                     _p, _p, _p, _p, _p, _p, _p]),
             "engram_short_conv_fwd": (st, [_p, _p, _c.c_int, _p, _p, _p, _p, _i32, _i64, _i32, _i32, _i32,
                                            _c.c_float, _p, _p, _p]),
+            "engram_short_conv_fwd_given_rstd": (st, [_p, _p, _c.c_int, _p, _p, _p, _p, _i32, _i64, _i32, _i32,
+                                                      _i32, _p, _p, _p]),
             "engram_short_conv_num_partials": (st, [_i64, _i32, _p]),
             "engram_short_conv_bwd": (st, [_p, _p, _c.c_int, _p, _p, _p, _p, _p, _i32, _i64, _i32, _i32, _i32, _p,
                                            _p, _i32, _p]),
@@ -190,6 +194,33 @@ def gate_fwd(h, k, v, w_fused, eps: float = 1e-6, out=None, save_for_backward: b
                                _ptr(out), _ptr(alpha), _ptr(rh), _ptr(rk), _ptr(dot), _stream(stream)),
            "engram_gate_fwd")
     return out, alpha, rh, rk, dot
+
+
+def gate_fwd_rms(h, k, v, w_fused, eps: float = 1e-6, out_eps: float = 1e-6, out=None, save_for_backward: bool = True,
+                 stats=None, out_rstd=None, stream=None):
+    """gate_fwd plus out_rstd [T] = 1/sqrt(mean(out_t^2) + out_eps) of each stored output row, the statistic the
+    short convolution's RMSNorm needs (short_conv_fwd(..., given_rstd=out_rstd)).
+    Returns (out, alpha, rstd_h, rstd_k, dot, out_rstd)."""
+    lib = load_library()
+    _need(h, "h")
+    _need(k, "k", h.dtype)
+    _need(v, "v", h.dtype)
+    _need(w_fused, "w_fused", torch.float32)
+    T, d = h.shape
+    out = torch.empty_like(v) if out is None else _need(out, "out", h.dtype)
+    if save_for_backward:
+        if stats is None:
+            stats = tuple(torch.empty(T, dtype=torch.float32, device=h.device) for _ in range(4))
+        alpha, rh, rk, dot = (_need(x, "stat", torch.float32) for x in stats)
+    else:
+        alpha = rh = rk = dot = None
+    out_rstd = (torch.empty(T, dtype=torch.float32, device=h.device) if out_rstd is None
+                else _need(out_rstd, "out_rstd", torch.float32))
+    _check(lib.engram_gate_fwd_rms(_ptr(h), _ptr(k), _ptr(v), _DTYPES[h.dtype], _ptr(w_fused), T, d, float(eps),
+                                   _ptr(out), _ptr(alpha), _ptr(rh), _ptr(rk), _ptr(dot), _ptr(out_rstd),
+                                   float(out_eps), _stream(stream)),
+           "engram_gate_fwd_rms")
+    return out, alpha, rh, rk, dot, out_rstd
 
 
 # ----------------------------------------------------------------------------- B2 / B3
@@ -322,8 +353,11 @@ def gate_hc_bwd(dout, x, kv, w_fused, gate, rstd_x, rstd_k, dot, clamp: float = 
 
 
 def short_conv_fwd(v, norm_w, conv_w, seq_offsets, dilation: int, h=None, bias=None, eps: float = 1e-6, out=None,
-                   rstd=None, stream=None):
-    """out = h + SiLU(causal depthwise conv of RMSNorm(v)) + v, per sequence.  Returns (out, rstd)."""
+                   rstd=None, given_rstd=None, stream=None):
+    """out = h + SiLU(causal depthwise conv of RMSNorm(v)) + v, per sequence.  Returns (out, rstd).
+
+    given_rstd: the RMSNorm statistic of v already made (gate_fwd_rms), read instead of computed; it is
+    then the returned rstd."""
     lib = load_library()
     _need(v, "v")
     _need(norm_w, "norm_w", torch.float32)
@@ -336,6 +370,14 @@ def short_conv_fwd(v, norm_w, conv_w, seq_offsets, dilation: int, h=None, bias=N
     T, d = v.shape
     width = conv_w.shape[1]
     out = torch.empty_like(v) if out is None else _need(out, "out", v.dtype)
+    if given_rstd is not None:
+        _need(given_rstd, "given_rstd", torch.float32)
+        _check(lib.engram_short_conv_fwd_given_rstd(_ptr(v), _ptr(h), _DTYPES[v.dtype], _ptr(norm_w), _ptr(conv_w),
+                                                    _ptr(bias), _ptr(seq_offsets), seq_offsets.numel() - 1, T, d,
+                                                    width, int(dilation), _ptr(given_rstd), _ptr(out),
+                                                    _stream(stream)),
+               "engram_short_conv_fwd_given_rstd")
+        return out, given_rstd
     rstd = torch.empty(T, dtype=torch.float32, device=v.device) if rstd is None else _need(rstd, "rstd", torch.float32)
     _check(lib.engram_short_conv_fwd(_ptr(v), _ptr(h), _DTYPES[v.dtype], _ptr(norm_w), _ptr(conv_w), _ptr(bias),
                                      _ptr(seq_offsets), seq_offsets.numel() - 1, T, d, width, int(dilation), float(eps),

@@ -17,16 +17,22 @@ struct GateFwdParams {
     const float *w;
     uint8_t *out;
     float *alpha, *rstd_h, *rstd_k, *dot;
+    float *out_rstd;  // with RMS: 1/sqrt(mean(out_t^2) + out_eps) of each stored output row
     uint32_t *status;
     int64_t T;
     int32_t d;
     uint32_t row_bytes;
     int32_t stages;
     float eps;
+    float out_eps;
     float scale;  // 1/sqrt(d)
 };
 
-template <typename T, int NCW>
+// RMS: also the RMS statistic of each output row as stored (rounded to `T`), the input of an RMSNorm
+// that reads this output next: every warp adds its part of sum(out^2) to its slot of the token's
+// reduction buffer in the output pass, and thread 0 sums the warps' parts in warp order once the
+// next token's reduction barrier (or, for the last token, one more barrier) shows them complete.
+template <typename T, int NCW, bool RMS>
 __global__ void __launch_bounds__((NCW + 1) * 32) gate_fwd_kernel(const __grid_constant__ GateFwdParams p) {
     pdl_wait();              // the previous kernel's writes are complete and visible
     using V = Vec<T>;
@@ -103,6 +109,15 @@ __global__ void __launch_bounds__((NCW + 1) * 32) gate_fwd_kernel(const __grid_c
         }
     }
     const float inv_d = 1.0f / static_cast<float>(p.d);
+    // (thread 0) the statistic of token `it`, from the warps' parts in its buffer's fourth slots
+    auto out_stat = [&](int64_t it) {
+        const float *buf = red + (it & 1) * NCW * 4;
+        float so = 0.f;
+#pragma unroll
+        for (int q = 0; q < NCW; ++q) so += buf[q * 4 + 3];
+        p.out_rstd[first + it * stride] = 1.0f / sqrtf(so * inv_d + p.out_eps);
+    };
+    bool completed = true;
 
     for (int64_t it = 0; it < n_my; ++it) {
         const int s = static_cast<int>(it % S);
@@ -139,8 +154,11 @@ __global__ void __launch_bounds__((NCW + 1) * 32) gate_fwd_kernel(const __grid_c
         }
         if (named_sync_or(1, NC, !ok)) {
             if (c == 0) report(p.status, nullptr, ENGRAM_DEVERR_TIMEOUT);
+            completed = false;
             break;
         }
+        // every warp has finished the previous token's output pass
+        if (RMS && c == 0 && it > 0) out_stat(it - 1);
         float SH = 0.f, SK = 0.f, SD = 0.f;
 #pragma unroll
         for (int q = 0; q < NCW; ++q) {
@@ -156,6 +174,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32) gate_fwd_kernel(const __grid_c
         // pass 2: out = alpha * v
         const int64_t tok = first + it * stride;
         uint8_t *orow = p.out + static_cast<size_t>(tok) * rb;
+        float so = 0.f;
 #pragma unroll
         for (int m = 0; m < kVPT; ++m) {
             const int j = c + m * NC;
@@ -164,8 +183,19 @@ __global__ void __launch_bounds__((NCW + 1) * 32) gate_fwd_kernel(const __grid_c
                 V::unpack(*reinterpret_cast<const uint4 *>(st + 2 * rb + j * 16), vx);
 #pragma unroll
                 for (int e = 0; e < EV; ++e) vx[e] *= a;
-                st_global_v4(orow + j * 16, V::pack(vx));
+                const uint4 packed = V::pack(vx);
+                st_global_v4(orow + j * 16, packed);
+                if (RMS) {  // the squares of the values as stored
+                    float ox[EV];
+                    V::unpack(packed, ox);
+#pragma unroll
+                    for (int e = 0; e < EV; ++e) so = fmaf(ox[e], ox[e], so);
+                }
             }
+        }
+        if (RMS) {
+            so = warp_sum(so);
+            if (lane == 0) rb_buf[warp * 4 + 3] = so;
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
@@ -175,6 +205,10 @@ __global__ void __launch_bounds__((NCW + 1) * 32) gate_fwd_kernel(const __grid_c
             if (p.rstd_k) p.rstd_k[tok] = rk;
             if (p.dot) p.dot[tok] = SD;
         }
+    }
+    if (RMS && completed && n_my > 0) {
+        named_sync_or(1, NC, false);  // every warp has finished the last token's output pass
+        if (c == 0) out_stat(n_my - 1);
     }
 }
 
@@ -190,7 +224,7 @@ namespace {
 
 template <typename T, int NCW>
 engram_status launch_fwd(const GateFwdParams &p, const DeviceInfo &dev, cudaStream_t stream) {
-    const auto kern = gate_fwd_kernel<T, NCW>;
+    const auto kern = p.out_rstd ? gate_fwd_kernel<T, NCW, true> : gate_fwd_kernel<T, NCW, false>;
     const PipelineShape shape = pick_fwd_pipeline(3 * static_cast<int>(p.row_bytes), NCW, dev.smem_optin);
     if (shape.stages == 0) return fail(ENGRAM_ERR_SHAPE, "engram_gate_fwd: row of %u bytes does not fit", p.row_bytes);
     engram_status st = set_smem(reinterpret_cast<const void *>(kern), shape.smem_bytes);
@@ -247,10 +281,11 @@ extern "C" engram_status engram_fuse_weight(const void *w_h, const void *w_k, en
     return check_launch("engram_fuse_weight");
 }
 
-extern "C" engram_status engram_gate_fwd(const void *h, const void *k, const void *v, engram_dtype dtype,
-                                         const float *w_fused, int64_t T, int32_t d, float eps, void *out,
-                                         float *alpha, float *rstd_h, float *rstd_k, float *dot,
-                                         engram_stream_t stream) {
+namespace {
+
+engram_status gate_fwd_impl(const void *h, const void *k, const void *v, engram_dtype dtype, const float *w_fused,
+                            int64_t T, int32_t d, float eps, void *out, float *alpha, float *rstd_h, float *rstd_k,
+                            float *dot, float *out_rstd, float out_eps, engram_stream_t stream) {
     // Per-token tensors may be NULL only when there is no token (an empty tensor has no storage).
     if (!w_fused || (T > 0 && (!h || !k || !v || !out))) return fail(ENGRAM_ERR_NULL, "engram_gate_fwd: NULL pointer");
     const int es = dtype_size(dtype);
@@ -270,7 +305,8 @@ extern "C" engram_status engram_gate_fwd(const void *h, const void *k, const voi
         (st = check_device_ptr(v, dev.device, "v")) || (st = check_device_ptr(w_fused, dev.device, "w_fused")) ||
         (st = check_device_ptr(out, dev.device, "out")) || (st = check_device_ptr(alpha, dev.device, "alpha")) ||
         (st = check_device_ptr(rstd_h, dev.device, "rstd_h")) ||
-        (st = check_device_ptr(rstd_k, dev.device, "rstd_k")) || (st = check_device_ptr(dot, dev.device, "dot")))
+        (st = check_device_ptr(rstd_k, dev.device, "rstd_k")) || (st = check_device_ptr(dot, dev.device, "dot")) ||
+        (st = check_device_ptr(out_rstd, dev.device, "out_rstd")))
         return st;
     if (T == 0) return ENGRAM_OK;
 
@@ -284,6 +320,8 @@ extern "C" engram_status engram_gate_fwd(const void *h, const void *k, const voi
     p.rstd_h = rstd_h;
     p.rstd_k = rstd_k;
     p.dot = dot;
+    p.out_rstd = out_rstd;
+    p.out_eps = out_eps;
     p.status = dev.status_word;
     p.T = T;
     p.d = d;
@@ -292,4 +330,22 @@ extern "C" engram_status engram_gate_fwd(const void *h, const void *k, const voi
     p.scale = 1.0f / sqrtf(static_cast<float>(d));
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     return dtype == ENGRAM_F32 ? dispatch_fwd<float>(p, dev, s) : dispatch_fwd<__nv_bfloat16>(p, dev, s);
+}
+
+}  // namespace
+
+extern "C" engram_status engram_gate_fwd(const void *h, const void *k, const void *v, engram_dtype dtype,
+                                         const float *w_fused, int64_t T, int32_t d, float eps, void *out,
+                                         float *alpha, float *rstd_h, float *rstd_k, float *dot,
+                                         engram_stream_t stream) {
+    return gate_fwd_impl(h, k, v, dtype, w_fused, T, d, eps, out, alpha, rstd_h, rstd_k, dot, nullptr, 0.f, stream);
+}
+
+extern "C" engram_status engram_gate_fwd_rms(const void *h, const void *k, const void *v, engram_dtype dtype,
+                                             const float *w_fused, int64_t T, int32_t d, float eps, void *out,
+                                             float *alpha, float *rstd_h, float *rstd_k, float *dot, float *out_rstd,
+                                             float out_eps, engram_stream_t stream) {
+    if (!out_rstd && T > 0) return fail(ENGRAM_ERR_NULL, "engram_gate_fwd_rms: NULL out_rstd");
+    return gate_fwd_impl(h, k, v, dtype, w_fused, T, d, eps, out, alpha, rstd_h, rstd_k, dot, out_rstd, out_eps,
+                         stream);
 }

@@ -1330,12 +1330,13 @@ extern "C" engram_status engram_short_conv_num_partials(int64_t T, int32_t dilat
     return ENGRAM_OK;
 }
 
-extern "C" engram_status engram_short_conv_fwd(const void *v, const void *h, engram_dtype dtype, const float *norm_w,
-                                               const float *conv_w, const float *bias, const int64_t *seq_offsets,
-                                               int32_t num_seqs, int64_t T, int32_t d, int32_t width,
-                                               int32_t dilation, float eps, void *out, float *rstd,
-                                               engram_stream_t stream) {
-    const char *fn = "engram_short_conv_fwd";
+namespace {
+
+// The forward; with `own_rstd` the statistic pass first writes rstd, else rstd is the caller's.
+engram_status sc_fwd(const char *fn, const void *v, const void *h, engram_dtype dtype, const float *norm_w,
+                     const float *conv_w, const float *bias, const int64_t *seq_offsets, int32_t num_seqs, int64_t T,
+                     int32_t d, int32_t width, int32_t dilation, float eps, void *out, float *rstd, bool own_rstd,
+                     engram_stream_t stream) {
     engram_status st = sc_check(fn, dtype, T, d, width, dilation, num_seqs);
     if (st != ENGRAM_OK) return st;
     if (!norm_w || !conv_w || !seq_offsets) return fail(ENGRAM_ERR_NULL, "%s: NULL pointer", fn);
@@ -1346,14 +1347,16 @@ extern "C" engram_status engram_short_conv_fwd(const void *v, const void *h, eng
     DeviceInfo dev;
     if ((st = sc_ptrs(fn, ptrs, 8, 6, &dev)) != ENGRAM_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const int64_t rgrid = cap_grid(std::min<int64_t>((T + 7) / 8, static_cast<int64_t>(dev.num_sms) * 8));
-    if (dtype == ENGRAM_F32)
-        conv_rstd_kernel<float><<<static_cast<unsigned>(rgrid), 256, 0, s>>>(static_cast<const uint8_t *>(v), T, d,
-                                                                            eps, rstd);
-    else
-        conv_rstd_kernel<__nv_bfloat16><<<static_cast<unsigned>(rgrid), 256, 0, s>>>(static_cast<const uint8_t *>(v),
-                                                                                    T, d, eps, rstd);
-    if ((st = check_launch(fn)) != ENGRAM_OK) return st;
+    if (own_rstd) {
+        const int64_t rgrid = cap_grid(std::min<int64_t>((T + 7) / 8, static_cast<int64_t>(dev.num_sms) * 8));
+        if (dtype == ENGRAM_F32)
+            conv_rstd_kernel<float><<<static_cast<unsigned>(rgrid), 256, 0, s>>>(static_cast<const uint8_t *>(v), T,
+                                                                                d, eps, rstd);
+        else
+            conv_rstd_kernel<__nv_bfloat16><<<static_cast<unsigned>(rgrid), 256, 0, s>>>(
+                static_cast<const uint8_t *>(v), T, d, eps, rstd);
+        if ((st = check_launch(fn)) != ENGRAM_OK) return st;
+    }
     ScFwdSweepParams fp{};
     fp.v = static_cast<const uint8_t *>(v);
     fp.h = static_cast<const uint8_t *>(h);
@@ -1373,6 +1376,26 @@ extern "C" engram_status engram_short_conv_fwd(const void *v, const void *h, eng
     fp.dil = dilation;
     fp.nblk = (d + kFwCW - 1) / kFwCW;
     return dtype == ENGRAM_F32 ? sc_fwd_launch<float>(fn, fp, dev, s) : sc_fwd_launch<__nv_bfloat16>(fn, fp, dev, s);
+}
+
+}  // namespace
+
+extern "C" engram_status engram_short_conv_fwd(const void *v, const void *h, engram_dtype dtype, const float *norm_w,
+                                               const float *conv_w, const float *bias, const int64_t *seq_offsets,
+                                               int32_t num_seqs, int64_t T, int32_t d, int32_t width,
+                                               int32_t dilation, float eps, void *out, float *rstd,
+                                               engram_stream_t stream) {
+    return sc_fwd("engram_short_conv_fwd", v, h, dtype, norm_w, conv_w, bias, seq_offsets, num_seqs, T, d, width,
+                  dilation, eps, out, rstd, true, stream);
+}
+
+extern "C" engram_status engram_short_conv_fwd_given_rstd(const void *v, const void *h, engram_dtype dtype,
+                                                          const float *norm_w, const float *conv_w, const float *bias,
+                                                          const int64_t *seq_offsets, int32_t num_seqs, int64_t T,
+                                                          int32_t d, int32_t width, int32_t dilation,
+                                                          const float *rstd, void *out, engram_stream_t stream) {
+    return sc_fwd("engram_short_conv_fwd_given_rstd", v, h, dtype, norm_w, conv_w, bias, seq_offsets, num_seqs, T, d,
+                  width, dilation, 0.f, out, const_cast<float *>(rstd), false, stream);
 }
 
 extern "C" engram_status engram_short_conv_bwd(const void *dout, const void *v, engram_dtype dtype,

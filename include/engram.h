@@ -242,6 +242,20 @@ engram_status engram_gate_fwd(const void *h, const void *k, const void *v, engra
                               void *out, float *alpha, float *rstd_h, float *rstd_k, float *dot,
                               engram_stream_t stream);
 
+/*
+ * engram_gate_fwd, plus the RMS statistic of every output row as stored (after its rounding to
+ * `dtype`), for the RMSNorm that reads the gate's output next (the short convolution, ch. 34
+ * sec. 1.2 item 4):
+ *     out_rstd[t] = 1/sqrt(sum_i out_t,i^2 / d + out_eps)      (out_rstd [T] fp32, not NULL)
+ * The sum adds each thread's squares in element order, a 32-lane butterfly per warp, then the
+ * warps in order: it depends on d only.  The other outputs are bitwise those of engram_gate_fwd.
+ * engram_short_conv_fwd_given_rstd takes out_rstd in place of its own statistic pass.
+ */
+engram_status engram_gate_fwd_rms(const void *h, const void *k, const void *v, engram_dtype dtype,
+                                  const float *w_fused, int64_t T, int32_t d, float eps,
+                                  void *out, float *alpha, float *rstd_h, float *rstd_k, float *dot,
+                                  float *out_rstd, float out_eps, engram_stream_t stream);
+
 /* ------------------------------------------------------------------------- */
 /* B2: gate backward  (ch. 34 sec. 4.1-4.2)                                   */
 /* ------------------------------------------------------------------------- */
@@ -350,6 +364,17 @@ engram_status engram_short_conv_fwd(const void *v, const void *h, engram_dtype d
                                     const float *conv_w, const float *bias, const int64_t *seq_offsets,
                                     int32_t num_seqs, int64_t T, int32_t d, int32_t width, int32_t dilation,
                                     float eps, void *out, float *rstd, engram_stream_t stream);
+
+/*
+ * engram_short_conv_fwd with rstd [T] given (read, not written): the statistic of V~ that
+ * engram_gate_fwd_rms produced with V~, so that V~ is read once here instead of twice.  The same
+ * conditions on the other arguments; the eps of the RMSNorm is the one rstd was made with.
+ */
+engram_status engram_short_conv_fwd_given_rstd(const void *v, const void *h, engram_dtype dtype,
+                                               const float *norm_w, const float *conv_w, const float *bias,
+                                               const int64_t *seq_offsets, int32_t num_seqs, int64_t T,
+                                               int32_t d, int32_t width, int32_t dilation, const float *rstd,
+                                               void *out, engram_stream_t stream);
 
 /*
  * Weight-gradient partials of engram_short_conv_bwd: P = ceil(T / L) * dilation with

@@ -32,6 +32,7 @@ import torch
 
 import engram_conditional_memory_gb300 as ecm
 import oracle
+from synth import generators as G
 from synth import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -111,8 +112,9 @@ def _shift(a, back, seq_start, seq_end):
     return out
 
 
-def _check(r, x, wl, f, b):
-    d, T = wl.d, wl.T
+def _check_fwd(r, x, wl, f):
+    """rstd and out against the oracle's forward; returns the conv's error bound for the backward."""
+    d = wl.d
     rr = _r_rel(d)
     bf16 = wl.dtype == "bf16"
     np.testing.assert_allclose(_f64(r["rstd"]), f["rstd"], rtol=2 * rr)
@@ -134,6 +136,15 @@ def _check(r, x, wl, f, b):
     tol = round_out + 1.1 * err_c + 4 * U * np.abs(silu) + 2 * U * mag
     bad = np.abs(_f64(r["out"]) - f["out"]) > 2 * tol + 1e-30
     assert not bad.any(), f"out: {bad.sum()} of {bad.size}; first {np.argwhere(bad)[0].tolist()}"
+    return err_c, u, seq_start, seq_end, cw
+
+
+def _check(r, x, wl, f, b):
+    d, T = wl.d, wl.T
+    rr = _r_rel(d)
+    bf16 = wl.dtype == "bf16"
+    err_c, u, seq_start, seq_end, cw = _check_fwd(r, x, wl, f)
+    v, g = _h64(x["v"]), _h64(x["dout"])
     # backward.  Besides the relative error of its own arithmetic, each dc = dout SiLU'(c) carries
     # the conv's absolute error through SiLU'' (|SiLU''| <= 1/2): dc_err = |dout| (err_c / 2 + 4.4 u);
     # du gathers it through the taps, dv through rstd norm_w and the row dot s.
@@ -219,6 +230,42 @@ def test_in_place_output_and_bitwise_reruns():
             assert torch.equal(dcw, a["dconv_w"]) and torch.equal(dbias, a["dbias"]) and torch.equal(dnw, a["dnorm_w"])
     finally:
         ecm.set_max_ctas(0)
+
+
+@pytest.mark.parametrize("lengths,d,dtype", [([700, 0, 300, 1], 4096, "bf16"), ([500], 136, "f32"),
+                                             ([64, 64], 8192, "bf16")])
+def test_gate_statistic_feeds_the_conv(lengths, d, dtype):
+    """The gate writes V~ with its RMS statistic (gate_fwd_rms), and the conv takes that statistic
+    instead of its own pass: the gate's other outputs are those of gate_fwd bit for bit, the
+    statistic matches the oracle's rstd of the stored V~, and the conv's output the oracle's conv of
+    that V~, within the forward's bounds."""
+    wl = W.ShortConvWorkload(name="g", lengths=lengths, d=d, width=4, dilation=3, dtype=dtype, seed=900 + d)
+    x = W.short_conv_host_inputs(wl)
+    T = wl.T
+    cv = (lambda a: a.astype(np.float32)) if dtype == "f32" else G.to_bf16_bits
+    hg, kg, vg = (_t(cv(G.normal(930 + i, T * d).reshape(T, d))) for i in range(3))
+    wf = ecm.fuse_weight(_t(G.normal(934, d, 1.0, 0.1).astype(np.float32)),
+                         _t(G.normal(935, d, 1.0, 0.1).astype(np.float32)))
+    ref = ecm.gate_fwd(hg, kg, vg, wf, 1e-6)
+    got = ecm.gate_fwd_rms(hg, kg, vg, wf, 1e-6, out_eps=wl.eps)
+    for a, b in zip(ref, got[:5]):
+        assert torch.equal(a, b)
+    vt, out_rstd = got[0], got[5]
+    # the conv over V~ = the gate's output as stored, with the statistic given
+    x["v"] = vt.cpu().view(torch.int16).numpy().view(np.uint16) if dtype == "bf16" else vt.cpu().numpy()
+    t = {k: _t(v) for k, v in x.items()}
+    o, r_std = ecm.short_conv_fwd(vt, t["norm_w"], t["conv_w"], t["seq_offsets"], wl.dilation, h=t["h"],
+                                  bias=t["bias"], given_rstd=out_rstd)
+    assert r_std.data_ptr() == out_rstd.data_ptr()
+    f = oracle.short_conv_fwd(x["v"], x["h"], x["norm_w"], x["conv_w"], x["bias"], x["seq_offsets"], wl.dilation,
+                              wl.eps, 0, T)
+    _check_fwd({"out": o, "rstd": out_rstd}, x, wl, f)
+    # with the conv's own statistic given back, its output is the ordinary forward's bit for bit
+    o2, r2 = ecm.short_conv_fwd(vt, t["norm_w"], t["conv_w"], t["seq_offsets"], wl.dilation, h=t["h"],
+                                bias=t["bias"])
+    o3, _ = ecm.short_conv_fwd(vt, t["norm_w"], t["conv_w"], t["seq_offsets"], wl.dilation, h=t["h"],
+                               bias=t["bias"], given_rstd=r2)
+    assert torch.equal(o2, o3)
 
 
 def test_no_token():
