@@ -501,8 +501,11 @@ def main_only(args, device):
         def launch():
             ecm.hash_gather(spec, ids, offs, table, cmap, hw.vocab, hw.vocab_c, out_rows=rows)
     elif op.startswith("gate_hc"):
-        # the multi-branch gate at its production shape: T = 8192, hc = 4, d = 4096, bf16
+        # the multi-branch gate at its production shape: T = 8192, hc = 4, d = 4096, bf16; the _d7168
+        # ops take rows too large for a whole token (T = 4096, hc = 4, d = 7168), run branch by branch
         wl = W.gate_hc_4x4k()
+        if op.endswith("_d7168"):
+            wl = W.GateHcWorkload(name="gate_hc4_T4096_d7168", T=4096, hc=4, d=7168, dtype="bf16", seed=wl.seed)
         T, hc, d = wl.T, wl.hc, wl.d
         x = SD.normal_tensor((T * hc, d), wl.seed + 1, 0.0, 1.0, "bf16", device).reshape(T, hc, d)
         kv = SD.normal_tensor((T * (hc + 1), d), wl.seed + 2, 0.0, 1.0, "bf16", device).reshape(T, hc + 1, d)
@@ -513,7 +516,7 @@ def main_only(args, device):
         out, *st = ecm.gate_hc_fwd(x, kv, wf, wl.eps, wl.clamp)
         P = ecm.gate_bwd_num_partials(T, hc * d)
         dx, dkv, part = ecm.gate_hc_bwd(g, x, kv, wf, *st, clamp=wl.clamp, P=P)
-        if op == "gate_hc_bwd":
+        if op.startswith("gate_hc_bwd"):
             nbytes = T * ((5 * hc + 2) * 2 * d + 16 * hc) + P * hc * d * 4
 
             def launch():
@@ -766,7 +769,8 @@ def main():
                                        "gate_fwd_2k", "gate_bwd", "grad_w_reduce", "gate_hc_fwd", "gate_hc_bwd",
                                        "sinkhorn", "sinkhorn_momentum", "sinkhorn_step", "sinkhorn_reduce",
                                        "sinkhorn_finalize", "short_conv_fwd", "short_conv_fwd_given", "short_conv_bwd",
-                                       "short_conv_reduce", "gate_conv_fwd", "gate_conv_fwd_fused"],
+                                       "short_conv_reduce", "gate_conv_fwd", "gate_conv_fwd_fused", "gate_hc_fwd_d7168",
+                                       "gate_hc_bwd_d7168"],
                     help="time one kernel alone on its workload (consecutive launches, L2 not flushed)")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -71,6 +71,7 @@ def load_library():
             "engram_set_validation": (_i32, [_i32]),
             "engram_set_max_ctas": (_i32, [_i32]),
             "engram_set_pdl": (_i32, [_i32]),
+            "engram_set_hc_split": (_i32, [_i32]),
             "engram_read_error_word": (st, [_p, _p, _p]),
             "engram_device_status": (st, [_p, _i32]),
             "engram_check_wait_timeout": (st, [_c.c_uint32, _p]),
@@ -145,6 +146,12 @@ def set_validation(level: int) -> int:
 def set_max_ctas(max_ctas: int) -> int:
     """Cap the CTAs per launch (0 = none); returns the previous cap."""
     return load_library().engram_set_max_ctas(max_ctas)
+
+
+def set_hc_split(on: bool) -> bool:
+    """Force the multi-branch gate's branch-by-branch form at every size (a test knob); returns the
+    previous setting."""
+    return bool(load_library().engram_set_hc_split(1 if on else 0))
 
 
 def set_pdl(on: bool) -> bool:

@@ -18,6 +18,7 @@
 // vectors jj = c, c + 32*NCW, ... of every branch row.  The weight-gradient partials are laid out
 // [P, hc * d], so the plain weight fold and the ordered reduction serve this variant unchanged.
 #include <algorithm>
+#include <atomic>
 
 #include "gate_pipeline.cuh"
 
@@ -30,6 +31,11 @@ struct HcShape {
     static constexpr int kVpb = 4 / HC;
 };
 
+// Token layouts: token t's HC rows of x (and out) start at t * x_stride bytes; its kv block at
+// t * kv_stride, with its HC key rows at k_off and its value row at v_off within it; its statistics
+// at t * st_stride.  The natural [T, HC, d] / [T, HC + 1, d] / [T, HC] layouts are x_stride =
+// HC rows, kv_stride = HC + 1 rows, k_off = 0, v_off = HC rows, st_stride = HC; one branch of a
+// wider tensor is a view with the same strides and offset bases.
 struct GateHcFwdParams {
     const uint8_t *x, *kv;
     const float *w;  // [hc, d]
@@ -37,12 +43,18 @@ struct GateHcFwdParams {
     float *gate, *rstd_x, *rstd_k, *dot;  // [T, hc]
     uint32_t *status;
     int64_t T;
+    int64_t x_stride, kv_stride;
+    uint32_t k_off, v_off;
+    int32_t st_stride;
     int32_t d;
     uint32_t row_bytes;
     int32_t stages;
     float eps, clamp, scale;
 };
 
+// The same layouts as the forward (dout and dx like x, dkv like kv); the weight-gradient partial
+// rows are part_stride floats apart.  write_dv = 0 leaves the value row's gradient to
+// hc_dv_kernel (a branch view sees one term of its sum).
 struct GateHcBwdParams {
     const uint8_t *g, *x, *kv;
     const float *w, *gate, *rstd_x, *rstd_k, *dot;
@@ -50,6 +62,10 @@ struct GateHcBwdParams {
     float *dw_partial;  // [P, hc * d]
     uint32_t *status;
     int64_t T;
+    int64_t x_stride, kv_stride, part_stride;
+    uint32_t k_off, v_off;
+    int32_t st_stride;
+    int32_t write_dv;
     int64_t chunk;
     int32_t P;
     int32_t d;
@@ -75,11 +91,25 @@ __device__ __forceinline__ float hc_activation(float z, float clamp) {
 // Issue the copies of one token into a stage and arm its barrier (thread 0 only).
 __device__ __forceinline__ void hc_issue(uint8_t *dst, uint64_t *bar, uint32_t bytes, uint64_t pol,
                                          const uint8_t *a, uint32_t na, const uint8_t *b, uint32_t nb,
-                                         const uint8_t *c, uint32_t nc) {
+                                         const uint8_t *c, uint32_t nc, const uint8_t *e = nullptr,
+                                         uint32_t ne = 0) {
     mbar_arrive_expect_tx(bar, bytes);
     bulk_load(dst, a, na, bar, pol);
     bulk_load(dst + na, b, nb, bar, pol);
     if (c) bulk_load(dst + na + nb, c, nc, bar, pol);
+    if (e) bulk_load(dst + na + nb + nc, e, ne, bar, pol);
+}
+
+// A token's key rows and value row into the stage at dst (after `before` bytes already issued):
+// one copy when they are adjacent, else two.
+struct HcKv {
+    const uint8_t *k, *v;
+    bool adjacent;
+};
+__device__ __forceinline__ HcKv hc_kv(const uint8_t *kv, int64_t t, int64_t kv_stride, uint32_t k_off,
+                                      uint32_t v_off, uint32_t hc_rows) {
+    const uint8_t *blk = kv + t * kv_stride;
+    return {blk + k_off, blk + v_off, v_off == k_off + hc_rows};
 }
 
 // Forward: G groups of NCW warps share one CTA and a ring of S token stages; group g works on
@@ -87,7 +117,7 @@ __device__ __forceinline__ void hc_issue(uint8_t *dst, uint64_t *bar, uint32_t b
 // landing and being read, so the CTA's one-token-at-a-time latency is hidden inside the SM.
 // Thread index gc within a group owns vectors jj = gc, gc + 32*NCW, ... (VPB of them) of every
 // branch row.  Groups synchronise on their own named barriers (ids 1..G).
-template <typename T, int HC, int NCW, int G, int VPB>
+template <typename T, int HC, int NCW, int G, int VPB, bool STRIDED>
 __global__ void __launch_bounds__(G * NCW * 32, 1) gate_hc_fwd_kernel(const __grid_constant__ GateHcFwdParams p) {
     using V = Vec<T>;
     constexpr int EV = V::N;
@@ -95,6 +125,11 @@ __global__ void __launch_bounds__(G * NCW * 32, 1) gate_hc_fwd_kernel(const __gr
     extern __shared__ __align__(128) uint8_t smem[];
 
     const uint32_t rb = p.row_bytes;
+    // the token layout: the natural one at compile time, or the view's strides (STRIDED)
+    const int64_t x_stride = STRIDED ? p.x_stride : static_cast<int64_t>(HC) * rb;
+    const int64_t kv_stride = STRIDED ? p.kv_stride : static_cast<int64_t>(HC + 1) * rb;
+    const uint32_t k_off = STRIDED ? p.k_off : 0u, v_off = STRIDED ? p.v_off : HC * rb;
+    const int st_stride = STRIDED ? p.st_stride : HC;
     const uint32_t stage = (2 * HC + 1) * rb;  // x [HC rows] then kv [HC + 1 rows]
     const int S = p.stages;
     const int nvec = static_cast<int>(rb / 16);
@@ -113,9 +148,13 @@ __global__ void __launch_bounds__(G * NCW * 32, 1) gate_hc_fwd_kernel(const __gr
         const int64_t tok = first + it * stride;
         const int st = static_cast<int>(it % S);
         issued_cnt[st] += 1;
-        hc_issue(smem + static_cast<size_t>(st) * stage, &full[st], stage, pol,
-                 p.x + static_cast<size_t>(tok) * HC * rb, HC * rb, p.kv + static_cast<size_t>(tok) * (HC + 1) * rb,
-                 (HC + 1) * rb, nullptr, 0);
+        const HcKv kv = hc_kv(p.kv, tok, kv_stride, k_off, v_off, HC * rb);
+        if (!STRIDED || kv.adjacent)
+            hc_issue(smem + static_cast<size_t>(st) * stage, &full[st], stage, pol, p.x + tok * x_stride, HC * rb,
+                     kv.k, (HC + 1) * rb, nullptr, 0);
+        else
+            hc_issue(smem + static_cast<size_t>(st) * stage, &full[st], stage, pol, p.x + tok * x_stride, HC * rb,
+                     kv.k, HC * rb, kv.v, rb);
     };
     if (threadIdx.x == 0) {
         for (int q = 0; q < S; ++q) {
@@ -211,7 +250,7 @@ __global__ void __launch_bounds__(G * NCW * 32, 1) gate_hc_fwd_kernel(const __gr
 
         // out = x + gate * v (the value row is kv row HC)
         const int64_t tok = first + it * stride;
-        uint8_t *orow = p.out + static_cast<size_t>(tok) * HC * rb;
+        uint8_t *orow = p.out + tok * x_stride;
 #pragma unroll
         for (int m = 0; m < VPB; ++m) {
             const int jj = gc + m * NC;
@@ -229,7 +268,7 @@ __global__ void __launch_bounds__(G * NCW * 32, 1) gate_hc_fwd_kernel(const __gr
             }
         }
         if (gc < HC) {
-            const size_t o = static_cast<size_t>(tok) * HC + gc;
+            const size_t o = static_cast<size_t>(tok) * st_stride + gc;
             if (p.gate) p.gate[o] = gate[gc];
             if (p.rstd_x) p.rstd_x[o] = rx[gc];
             if (p.rstd_k) p.rstd_k[o] = rk[gc];
@@ -247,7 +286,7 @@ __global__ void __launch_bounds__(G * NCW * 32, 1) gate_hc_fwd_kernel(const __gr
                 report(p.status, nullptr, ENGRAM_DEVERR_TIMEOUT);
 }
 
-template <typename T, int HC, int NCW>
+template <typename T, int HC, int NCW, bool STRIDED>
 __global__ void __launch_bounds__(NCW * 32, 1) gate_hc_bwd_kernel(const __grid_constant__ GateHcBwdParams p) {
     using V = Vec<T>;
     constexpr int EV = V::N;
@@ -256,6 +295,13 @@ __global__ void __launch_bounds__(NCW * 32, 1) gate_hc_bwd_kernel(const __grid_c
     extern __shared__ __align__(128) uint8_t smem[];
 
     const uint32_t rb = p.row_bytes;
+    // the token layout: the natural one at compile time, or the view's strides (STRIDED)
+    const int64_t x_stride = STRIDED ? p.x_stride : static_cast<int64_t>(HC) * rb;
+    const int64_t kv_stride = STRIDED ? p.kv_stride : static_cast<int64_t>(HC + 1) * rb;
+    const int64_t part_stride = STRIDED ? p.part_stride : static_cast<int64_t>(HC) * p.d;
+    const uint32_t k_off = STRIDED ? p.k_off : 0u, v_off = STRIDED ? p.v_off : HC * rb;
+    const int st_stride = STRIDED ? p.st_stride : HC;
+    const bool write_dv = !STRIDED || p.write_dv;
     const uint32_t stage = (3 * HC + 1) * rb;  // dout [HC], x [HC], kv [HC + 1]
     const int S = p.stages;
     const int nvec = static_cast<int>(rb / 16);
@@ -277,9 +323,13 @@ __global__ void __launch_bounds__(NCW * 32, 1) gate_hc_bwd_kernel(const __grid_c
     auto token_of = [&](int64_t j) { return (blockIdx.x + (j / C) * G) * C + j % C; };
     auto issue = [&](int64_t j) {
         const int64_t t = token_of(j);
-        hc_issue(smem + static_cast<size_t>(j % S) * stage, &full[j % S], stage, pol,
-                 p.g + static_cast<size_t>(t) * HC * rb, HC * rb, p.x + static_cast<size_t>(t) * HC * rb, HC * rb,
-                 p.kv + static_cast<size_t>(t) * (HC + 1) * rb, (HC + 1) * rb);
+        const HcKv kv = hc_kv(p.kv, t, kv_stride, k_off, v_off, HC * rb);
+        if (!STRIDED || kv.adjacent)
+            hc_issue(smem + static_cast<size_t>(j % S) * stage, &full[j % S], stage, pol, p.g + t * x_stride,
+                     HC * rb, p.x + t * x_stride, HC * rb, kv.k, (HC + 1) * rb);
+        else
+            hc_issue(smem + static_cast<size_t>(j % S) * stage, &full[j % S], stage, pol, p.g + t * x_stride,
+                     HC * rb, p.x + t * x_stride, HC * rb, kv.k, HC * rb, kv.v, rb);
     };
     int64_t issued = 0;
     if (c == 0) {
@@ -328,7 +378,7 @@ __global__ void __launch_bounds__(NCW * 32, 1) gate_hc_bwd_kernel(const __grid_c
             float gt[HC], rx[HC], rk[HC], dt[HC];
 #pragma unroll
             for (int h = 0; h < HC; ++h) {
-                const size_t o = static_cast<size_t>(t) * HC + h;
+                const size_t o = static_cast<size_t>(t) * st_stride + h;
                 gt[h] = __ldg(p.gate + o);
                 rx[h] = __ldg(p.rstd_x + o);
                 rk[h] = __ldg(p.rstd_k + o);
@@ -362,7 +412,7 @@ __global__ void __launch_bounds__(NCW * 32, 1) gate_hc_bwd_kernel(const __grid_c
                                 dv[e] = fmaf(gt[h], gv[e], dv[e]);
                             }
                         }
-                        st_global_v4(p.dkv + (static_cast<size_t>(t) * (HC + 1) + HC) * rb + jj * 16, V::pack(dv));
+                        if (write_dv) st_global_v4(p.dkv + t * kv_stride + v_off + jj * 16, V::pack(dv));
                     }
                 }
             }
@@ -415,8 +465,8 @@ __global__ void __launch_bounds__(NCW * 32, 1) gate_hc_bwd_kernel(const __grid_c
                             okk[e] = fmaf(cw, xv[e], -ck[h] * kx[e]);
                             acc[h][m][e] = fmaf(cc[h] * xv[e], kx[e], acc[h][m][e]);
                         }
-                        st_global_v4(p.dx + (static_cast<size_t>(t) * HC + h) * rb + jj * 16, V::pack(ox));
-                        st_global_v4(p.dkv + (static_cast<size_t>(t) * (HC + 1) + h) * rb + jj * 16, V::pack(okk));
+                        st_global_v4(p.dx + t * x_stride + h * rb + jj * 16, V::pack(ox));
+                        st_global_v4(p.dkv + t * kv_stride + k_off + h * rb + jj * 16, V::pack(okk));
                     }
                 }
             __syncthreads();  // every thread is done with stage s: refill it
@@ -424,7 +474,7 @@ __global__ void __launch_bounds__(NCW * 32, 1) gate_hc_bwd_kernel(const __grid_c
         }
         if (failed) break;
 
-        float *prow = p.dw_partial + static_cast<size_t>(pp) * HC * p.d;
+        float *prow = p.dw_partial + pp * part_stride;
 #pragma unroll
         for (int h = 0; h < HC; ++h)
 #pragma unroll
@@ -444,6 +494,32 @@ __global__ void __launch_bounds__(NCW * 32, 1) gate_hc_bwd_kernel(const __grid_c
                 report(p.status, nullptr, ENGRAM_DEVERR_TIMEOUT);
 }
 
+// dv_t = sum_h gate[t, h] dout_t,h for the per-branch form of the backward: the same fused
+// multiply-add chain over the branches in order that gate_hc_bwd_kernel runs, rounded once.
+template <typename E>
+__global__ void __launch_bounds__(256) hc_dv_kernel(const uint8_t *__restrict__ g, const float *__restrict__ gate,
+                                                    uint8_t *__restrict__ dkv, int64_t T, int32_t hc, uint32_t rb) {
+    using V = Vec<E>;
+    constexpr int EV = V::N;
+    const int64_t nvec = rb / 16;
+    const int64_t total = T * nvec;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t t = i / nvec, jj = i - t * nvec;
+        float dv[EV];
+#pragma unroll
+        for (int e = 0; e < EV; ++e) dv[e] = 0.f;
+        for (int h = 0; h < hc; ++h) {
+            const float a = __ldg(gate + t * hc + h);
+            float gv[EV];
+            V::unpack(__ldg(reinterpret_cast<const uint4 *>(g + (t * hc + h) * rb) + jj), gv);
+#pragma unroll
+            for (int e = 0; e < EV; ++e) dv[e] = fmaf(a, gv[e], dv[e]);
+        }
+        st_global_v4(dkv + (t * (hc + 1) + hc) * rb + jj * 16, V::pack(dv));
+    }
+}
+
 namespace {
 
 // Smallest NCW in {2, 4, 8, 16} whose threads cover a branch row with at most HcShape<HC>::kVpb
@@ -457,11 +533,11 @@ int hc_consumer_warps(int nvec) {
 
 // Forward launch: two groups of NCW warps, VPB = 2 * HcShape<HC>::kVpb vectors per branch row
 // (the forward keeps no gradient accumulators, so it can afford twice the weights per thread).
-template <typename T, int HC, int NCW>
+template <typename T, int HC, int NCW, bool STRIDED>
 engram_status launch_hc_fwd(const GateHcFwdParams &p, const DeviceInfo &dev, cudaStream_t stream) {
     constexpr int G = 2;
     constexpr int NCWG = NCW / 2 > 0 ? NCW / 2 : 1;
-    const auto kern = gate_hc_fwd_kernel<T, HC, NCWG, G, 2 * HcShape<HC>::kVpb>;
+    const auto kern = gate_hc_fwd_kernel<T, HC, NCWG, G, 2 * HcShape<HC>::kVpb, STRIDED>;
     // As many stages as fit (2..4): one stage is a whole token, and with a single CTA per SM the
     // refill of a stage is issued only once the CTA is done with it, so depth must come from stages.
     const int stage = (2 * HC + 1) * static_cast<int>(p.row_bytes);
@@ -484,9 +560,9 @@ engram_status launch_hc_fwd(const GateHcFwdParams &p, const DeviceInfo &dev, cud
     return check_launch("engram_gate_hc_fwd");
 }
 
-template <typename T, int HC, int NCW>
+template <typename T, int HC, int NCW, bool STRIDED>
 engram_status launch_hc_bwd(const GateHcBwdParams &p, const DeviceInfo &dev, cudaStream_t stream) {
-    const auto kern = gate_hc_bwd_kernel<T, HC, NCW>;
+    const auto kern = gate_hc_bwd_kernel<T, HC, NCW, STRIDED>;
     const int stage = (3 * HC + 1) * static_cast<int>(p.row_bytes);
     int S = 3;
     while (S >= 2 && hc_smem_bytes(S, stage, NCW, HC) > dev.smem_optin) --S;
@@ -503,44 +579,107 @@ engram_status launch_hc_bwd(const GateHcBwdParams &p, const DeviceInfo &dev, cud
     return check_launch("engram_gate_hc_bwd");
 }
 
-template <typename T, int HC>
+template <typename T, int HC, bool STRIDED = false>
 engram_status dispatch_hc_fwd(const GateHcFwdParams &p, const DeviceInfo &dev, cudaStream_t s) {
     switch (hc_consumer_warps<HC>(static_cast<int>(p.row_bytes / 16))) {
-        case 2: return launch_hc_fwd<T, HC, 2>(p, dev, s);
-        case 4: return launch_hc_fwd<T, HC, 4>(p, dev, s);
-        case 8: return launch_hc_fwd<T, HC, 8>(p, dev, s);
-        case 16: return launch_hc_fwd<T, HC, 16>(p, dev, s);
+        case 2: return launch_hc_fwd<T, HC, 2, STRIDED>(p, dev, s);
+        case 4: return launch_hc_fwd<T, HC, 4, STRIDED>(p, dev, s);
+        case 8: return launch_hc_fwd<T, HC, 8, STRIDED>(p, dev, s);
+        case 16: return launch_hc_fwd<T, HC, 16, STRIDED>(p, dev, s);
         default: return fail(ENGRAM_ERR_SHAPE, "engram_gate_hc_fwd: d = %d too large for %d branches", p.d, HC);
     }
 }
 
-template <typename T, int HC>
+template <typename T, int HC, bool STRIDED = false>
 engram_status dispatch_hc_bwd(const GateHcBwdParams &p, const DeviceInfo &dev, cudaStream_t s) {
     switch (hc_consumer_warps<HC>(static_cast<int>(p.row_bytes / 16))) {
-        case 2: return launch_hc_bwd<T, HC, 2>(p, dev, s);
-        case 4: return launch_hc_bwd<T, HC, 4>(p, dev, s);
-        case 8: return launch_hc_bwd<T, HC, 8>(p, dev, s);
-        case 16: return launch_hc_bwd<T, HC, 16>(p, dev, s);
+        case 2: return launch_hc_bwd<T, HC, 2, STRIDED>(p, dev, s);
+        case 4: return launch_hc_bwd<T, HC, 4, STRIDED>(p, dev, s);
+        case 8: return launch_hc_bwd<T, HC, 8, STRIDED>(p, dev, s);
+        case 16: return launch_hc_bwd<T, HC, 16, STRIDED>(p, dev, s);
         default: return fail(ENGRAM_ERR_SHAPE, "engram_gate_hc_bwd: d = %d too large for %d branches", p.d, HC);
     }
 }
 
+// Whether a whole token of HC branches fits the fused kernels: the consumer threads cover a row and
+// two token stages fit in shared memory.
+template <int HC>
+bool hc_fwd_fits(int rb, int smem_optin) {
+    const int ncw = hc_consumer_warps<HC>(rb / 16);
+    return ncw > 0 && hc_smem_bytes(2, (2 * HC + 1) * rb, ncw, HC) <= smem_optin;
+}
+template <int HC>
+bool hc_bwd_fits(int rb, int smem_optin) {
+    const int ncw = hc_consumer_warps<HC>(rb / 16);
+    return ncw > 0 && hc_smem_bytes(2, (3 * HC + 1) * rb, ncw, HC) <= smem_optin;
+}
+bool hc_fits(int hc, bool fwd, int rb, int smem_optin) {
+    switch (hc) {
+        case 1: return fwd ? hc_fwd_fits<1>(rb, smem_optin) : hc_bwd_fits<1>(rb, smem_optin);
+        case 2: return fwd ? hc_fwd_fits<2>(rb, smem_optin) : hc_bwd_fits<2>(rb, smem_optin);
+        default: return fwd ? hc_fwd_fits<4>(rb, smem_optin) : hc_bwd_fits<4>(rb, smem_optin);
+    }
+}
+
+std::atomic<int> g_hc_split{0};
+
+// Per-branch form, for rows too large for a whole token of hc branches (or when forced): branch h
+// is a one-branch problem on strided views of x, kv, out and the statistics, with its row of the
+// fused weight; in the backward the value row's gradient sum_h gate_h dout_h is one more kernel.
 template <typename T>
 engram_status dispatch_hc_fwd_t(int hc, const GateHcFwdParams &p, const DeviceInfo &dev, cudaStream_t s) {
-    switch (hc) {
-        case 1: return dispatch_hc_fwd<T, 1>(p, dev, s);
-        case 2: return dispatch_hc_fwd<T, 2>(p, dev, s);
-        default: return dispatch_hc_fwd<T, 4>(p, dev, s);
+    if (g_hc_split.load(std::memory_order_relaxed) == 0 && hc_fits(hc, true, p.row_bytes, dev.smem_optin)) {
+        switch (hc) {
+            case 1: return dispatch_hc_fwd<T, 1>(p, dev, s);
+            case 2: return dispatch_hc_fwd<T, 2>(p, dev, s);
+            default: return dispatch_hc_fwd<T, 4>(p, dev, s);
+        }
     }
+    for (int h = 0; h < hc; ++h) {
+        GateHcFwdParams q = p;
+        q.x += static_cast<size_t>(h) * p.row_bytes;
+        q.out += static_cast<size_t>(h) * p.row_bytes;
+        q.k_off = p.k_off + h * p.row_bytes;
+        q.w += static_cast<size_t>(h) * p.d;
+        if (q.gate) q.gate += h;
+        if (q.rstd_x) q.rstd_x += h;
+        if (q.rstd_k) q.rstd_k += h;
+        if (q.dot) q.dot += h;
+        engram_status st = dispatch_hc_fwd<T, 1, true>(q, dev, s);
+        if (st != ENGRAM_OK) return st;
+    }
+    return ENGRAM_OK;
 }
 
 template <typename T>
 engram_status dispatch_hc_bwd_t(int hc, const GateHcBwdParams &p, const DeviceInfo &dev, cudaStream_t s) {
-    switch (hc) {
-        case 1: return dispatch_hc_bwd<T, 1>(p, dev, s);
-        case 2: return dispatch_hc_bwd<T, 2>(p, dev, s);
-        default: return dispatch_hc_bwd<T, 4>(p, dev, s);
+    if (g_hc_split.load(std::memory_order_relaxed) == 0 && hc_fits(hc, false, p.row_bytes, dev.smem_optin)) {
+        switch (hc) {
+            case 1: return dispatch_hc_bwd<T, 1>(p, dev, s);
+            case 2: return dispatch_hc_bwd<T, 2>(p, dev, s);
+            default: return dispatch_hc_bwd<T, 4>(p, dev, s);
+        }
     }
+    for (int h = 0; h < hc; ++h) {
+        GateHcBwdParams q = p;
+        q.g += static_cast<size_t>(h) * p.row_bytes;
+        q.x += static_cast<size_t>(h) * p.row_bytes;
+        q.dx += static_cast<size_t>(h) * p.row_bytes;
+        q.k_off = p.k_off + h * p.row_bytes;
+        q.w += static_cast<size_t>(h) * p.d;
+        q.gate += h;
+        q.rstd_x += h;
+        q.rstd_k += h;
+        q.dot += h;
+        q.dw_partial += static_cast<size_t>(h) * p.d;
+        q.write_dv = 0;
+        engram_status st = dispatch_hc_bwd<T, 1, true>(q, dev, s);
+        if (st != ENGRAM_OK) return st;
+    }
+    const int64_t work = p.T * (p.row_bytes / 16);
+    const int64_t grid = cap_grid(std::max<int64_t>(1, std::min<int64_t>((work + 255) / 256, 8LL * dev.num_sms)));
+    hc_dv_kernel<T><<<static_cast<unsigned>(grid), 256, 0, s>>>(p.g, p.gate, p.dkv, p.T, hc, p.row_bytes);
+    return check_launch("engram_gate_hc_bwd");
 }
 
 engram_status hc_common_checks(const char *fn, engram_dtype dtype, int64_t T, int32_t hc, int32_t d, int *es,
@@ -595,6 +734,11 @@ extern "C" engram_status engram_gate_hc_fwd(const void *x, const void *kv, engra
     p.dot = dot;
     p.status = dev.status_word;
     p.T = T;
+    p.x_stride = hc * row_bytes;
+    p.kv_stride = (hc + 1) * row_bytes;
+    p.k_off = 0;
+    p.v_off = static_cast<uint32_t>(hc * row_bytes);
+    p.st_stride = hc;
     p.d = d;
     p.row_bytes = static_cast<uint32_t>(row_bytes);
     p.eps = eps;
@@ -641,6 +785,13 @@ extern "C" engram_status engram_gate_hc_bwd(const void *dout, const void *x, con
     p.dw_partial = dw_partial;
     p.status = dev.status_word;
     p.T = T;
+    p.x_stride = hc * row_bytes;
+    p.kv_stride = (hc + 1) * row_bytes;
+    p.part_stride = static_cast<int64_t>(hc) * d;
+    p.k_off = 0;
+    p.v_off = static_cast<uint32_t>(hc * row_bytes);
+    p.st_stride = hc;
+    p.write_dv = 1;
     p.P = P;
     p.chunk = (T + P - 1) / P;
     p.d = d;
@@ -650,3 +801,5 @@ extern "C" engram_status engram_gate_hc_bwd(const void *dout, const void *x, con
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     return dtype == ENGRAM_F32 ? dispatch_hc_bwd_t<float>(hc, p, dev, s) : dispatch_hc_bwd_t<__nv_bfloat16>(hc, p, dev, s);
 }
+
+extern "C" int32_t engram_set_hc_split(int32_t on) { return g_hc_split.exchange(on ? 1 : 0); }

@@ -123,6 +123,16 @@ int32_t engram_set_max_ctas(int32_t max_ctas);
 int32_t engram_set_pdl(int32_t on);
 
 /*
+ * The multi-branch gate (engram_gate_hc_fwd / _bwd) runs a whole token of hc branches in one
+ * kernel when its rows fit twice in shared memory, and branch by branch on strided views (plus one
+ * kernel for the shared value's gradient) when they do not.  on = 1 forces the branch-by-branch
+ * form at every size, for testing; results agree with the oracle either way, though not bit for
+ * bit with each other (the sums' thread layouts differ).  Returns the previous setting.
+ * Process-wide.
+ */
+int32_t engram_set_hc_split(int32_t on);
+
+/*
  * Copies a device error word to *host_out.  SYNCHRONISES `stream` first.
  * Returns ENGRAM_ERR_INDEX when any bit is set, ENGRAM_OK otherwise.
  */
@@ -317,9 +327,10 @@ engram_status engram_grad_w_reduce(const float *dw_partial, int32_t P, int32_t d
  *     out    = x + gate * v.
  * gate, rstd_x, rstd_k, dot are [T, hc] fp32, each nullable.  out may equal x (in-place
  * writing) only when no statistic is saved: a backward needs the original x, so that
- * combination is refused (ENGRAM_ERR_SHAPE).  One token's rows must fit twice in shared
- * memory ((2 hc + 1) * d * element size per copy) and d must be at most 4096 bf16 / 2048
- * fp32 elements for hc = 4 (twice / four times that for hc = 2 / 1).
+ * combination is refused (ENGRAM_ERR_SHAPE).  Rows up to ENGRAM_MAX_ROW_BYTES: a token whose
+ * (2 hc + 1) rows fit twice in shared memory, with d at most 4096 bf16 / 2048 fp32 elements for
+ * hc = 4 (twice / four times that for hc = 2 / 1), runs as one kernel; a larger one runs branch by
+ * branch (engram_set_hc_split).
  */
 engram_status engram_gate_hc_fwd(const void *x, const void *kv, engram_dtype dtype, const float *w_fused,
                                  int64_t T, int32_t hc, int32_t d, float eps, float clamp_value, void *out,

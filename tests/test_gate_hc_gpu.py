@@ -103,6 +103,38 @@ def test_small_cases(dtype, hc, d, T):
     _check(r, x, wl)
 
 
+@pytest.mark.parametrize("dtype,hc,d,T", [("bf16", 4, 7168, 41), ("bf16", 4, 8192, 9), ("f32", 4, 3072, 17),
+                                          ("f32", 2, 4096, 13)])
+def test_rows_too_large_for_a_whole_token(dtype, hc, d, T):
+    """Rows whose token does not fit twice in shared memory (d = 7168 at hc = 4, the largest rows,
+    fp32 past its whole-token limit) run branch by branch on strided views, plus the value row's
+    gradient in one more kernel: every output against the oracle."""
+    wl = W.GateHcWorkload(name="t", T=T, hc=hc, d=d, dtype=dtype, seed=760 + hc * d + T)
+    x = W.gate_hc_host_inputs(wl)
+    r = _run(_dev(x), wl)
+    torch.cuda.synchronize()
+    _check(r, x, wl)
+
+
+@pytest.mark.parametrize("dtype,hc,d,T", [("bf16", 4, 1024, 300), ("f32", 2, 96, 77), ("bf16", 4, 4096, 40)])
+def test_branch_by_branch_form_at_whole_token_sizes(dtype, hc, d, T):
+    """The branch-by-branch form forced where the whole-token kernels also run: both against the
+    oracle, and in-place writing (out = x) kept."""
+    wl = W.GateHcWorkload(name="t", T=T, hc=hc, d=d, dtype=dtype, seed=780 + hc * d + T)
+    x = W.gate_hc_host_inputs(wl)
+    prev = ecm.set_hc_split(True)
+    try:
+        t = _dev(x)
+        r = _run(t, wl)
+        torch.cuda.synchronize()
+        _check(r, x, wl)
+        xi = t["x"].clone()
+        ecm.gate_hc_fwd(xi, t["kv"], r["wf"], wl.eps, wl.clamp, inplace=True, save_for_backward=False)
+        assert torch.equal(xi, r["out"])
+    finally:
+        ecm.set_hc_split(prev)
+
+
 def test_production_shape_every_element():
     wl = W.gate_hc_4x4k()
     x = W.gate_hc_host_inputs(wl)
