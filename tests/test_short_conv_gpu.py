@@ -233,7 +233,7 @@ def test_in_place_output_and_bitwise_reruns():
 
 
 @pytest.mark.parametrize("lengths,d,dtype", [([700, 0, 300, 1], 4096, "bf16"), ([500], 136, "f32"),
-                                             ([64, 64], 8192, "bf16")])
+                                             ([64, 64], 8192, "bf16"), ([1], 8, "bf16")])
 def test_gate_statistic_feeds_the_conv(lengths, d, dtype):
     """The gate writes V~ with its RMS statistic (gate_fwd_rms), and the conv takes that statistic
     instead of its own pass: the gate's other outputs are those of gate_fwd bit for bit, the
@@ -266,6 +266,17 @@ def test_gate_statistic_feeds_the_conv(lengths, d, dtype):
     o3, _ = ecm.short_conv_fwd(vt, t["norm_w"], t["conv_w"], t["seq_offsets"], wl.dilation, h=t["h"],
                                bias=t["bias"], given_rstd=r2)
     assert torch.equal(o2, o3)
+
+
+def test_gate_statistic_empty_batch():
+    h = torch.empty((0, 64), dtype=torch.bfloat16, device=DEV)
+    wf = torch.ones(64, dtype=torch.float32, device=DEV)
+    out, *_, ostd = ecm.gate_fwd_rms(h, h, h, wf)
+    assert out.shape == (0, 64) and ostd.shape == (0,)
+    v = torch.empty((0, 64), dtype=torch.bfloat16, device=DEV)
+    offs = torch.zeros(2, dtype=torch.int64, device=DEV)
+    o, _ = ecm.short_conv_fwd(v, wf, torch.ones((64, 4), dtype=torch.float32, device=DEV), offs, 3, given_rstd=ostd)
+    assert o.shape == (0, 64)
 
 
 def test_no_token():
