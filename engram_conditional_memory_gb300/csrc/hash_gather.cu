@@ -64,7 +64,8 @@ struct HashGatherParams {
     uint64_t mult[ENGRAM_MAX_TABLES][ENGRAM_MAX_ORDER];
 };
 
-// Dynamic shared memory of one CTA, laid out by the host and the kernel alike.
+// Dynamic shared memory of a host-table CTA (hash_gather_host_kernel, which passes row_bytes 0: its
+// rows go through registers, not tiles), laid out by the host and the kernel alike.
 struct HashSmemLayout {
     uint32_t tiles;    // 2 tiles of e_t rows (tile_tokens x tables x row_bytes each), 128-byte aligned
     uint32_t rows;     // int64 [2][tile_tokens][tables] row numbers
@@ -174,11 +175,6 @@ __device__ __forceinline__ void bulk_store_commit(void *dst_gmem, const void *sr
                  "r"(smem_addr(src_smem)), "r"(bytes)
                  : "memory");
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-
-// Waits until at most one committed bulk store still reads shared memory.
-__device__ __forceinline__ void bulk_wait_read_all_but_one() {
-    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 
 // Waits until no committed bulk store still reads shared memory.
