@@ -66,6 +66,33 @@ def test_host_side_rejections(lib):
     assert lib.engram_grad_w_reduce(fake, -1, 64, fake, None, None, None, None, None) == 2
 
 
+def test_newer_entry_points_reject_on_the_host(lib):
+    """The gate with its output statistic, the conv taking it, the conv's reduction and the
+    multi-branch gate's knob: argument errors come back before any CUDA call."""
+    st, vp, i32, i64, f32 = ctypes.c_int, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+    fake = vp(0x10000)
+    g = lib.engram_gate_fwd_rms
+    g.restype = st
+    g.argtypes = [vp, vp, vp, ctypes.c_int, vp, i64, i32, f32, vp, vp, vp, vp, vp, vp, f32, vp]
+    assert g(fake, fake, fake, 1, fake, 8, 64, 1e-6, fake, None, None, None, None, None, 1e-6, None) == 1  # no out_rstd
+    assert g(None, fake, fake, 1, fake, 8, 64, 1e-6, fake, None, None, None, None, fake, 1e-6, None) == 1
+    assert g(fake, fake, fake, 7, fake, 8, 64, 1e-6, fake, None, None, None, None, fake, 1e-6, None) == 3
+    c = lib.engram_short_conv_fwd_given_rstd
+    c.restype = st
+    c.argtypes = [vp, vp, ctypes.c_int, vp, vp, vp, vp, i32, i64, i32, i32, i32, vp, vp, vp]
+    assert c(fake, None, 1, fake, fake, None, fake, 1, 8, 64, 4, 3, None, fake, None) == 1  # no rstd
+    assert c(fake, None, 1, fake, fake, None, fake, 1, 8, 64, 5, 3, fake, fake, None) == 2  # width 5
+    assert c(fake, None, 1, fake, fake, None, fake, 1, 8, 64, 4, 0, fake, fake, None) == 2  # dilation 0
+    r = lib.engram_short_conv_grad_reduce
+    r.restype = st
+    r.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp]
+    assert r(fake, 4, 4, 6, fake, None, fake, None) == 4  # d not a multiple of 4
+    assert r(None, 4, 4, 64, fake, None, fake, None) == 1
+    k = lib.engram_set_hc_split
+    k.restype, k.argtypes = i32, [i32]
+    assert k(1) == 0 and k(0) == 1 and k(0) == 0
+
+
 def test_partition_rule(lib):
     lib.engram_gate_bwd_num_partials.restype = ctypes.c_int
     lib.engram_gate_bwd_num_partials.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.POINTER(ctypes.c_int32)]
