@@ -16,8 +16,8 @@ memory every step (the `e2e` value).  The per-step working set (4.1 GB table,
 2 GB of gate inputs) is far larger than L2, so no flush is needed.
 
 `--impl reference` times the CPU oracle (the correctness reference, plain C,
-fp64) on the host cores instead, each step a bounded sample of the same
-workload scaled to the whole step.
+fp64) on the host cores instead: every timed step is one whole step of the same
+workload, nothing sampled or scaled.
 """
 from __future__ import annotations
 
@@ -409,12 +409,22 @@ def _oracle_threads():
     return max(1, os.cpu_count() or 1)
 
 
-def oracle_step_seconds(hw, table_host, gate_host, gate_tokens: int, hash_tokens: int):
-    """Wall time of the oracle on a sample: hash + gather of `hash_tokens` tokens and gate fwd + bwd of
-    `gate_tokens` tokens, split over all host threads; returns (t_hash, t_gate, threads)."""
+def _ranges(n: int, parts: int):
+    parts = max(1, min(parts, n)) if n else 1
+    return [(n * i // parts, n * (i + 1) // parts) for i in range(parts)]
+
+
+ORACLE_GATE_CHUNK = 256  # tokens per oracle call in the gate legs (bounds each call's fp64 outputs)
+
+
+def oracle_step(pool, threads, hw, table_host, mbs_host, w_h, w_k):
+    """Seconds of ONE WHOLE step computed by the oracle over the full workload, nothing sampled
+    or scaled: hash + gather of all 65,536 tokens from the full 4.1 GB table, the fold, gate
+    forward + backward of all four micro-batches (4 x 16384 tokens), then the ordered reduction of
+    the per-range weight-gradient sums into both weight gradients.  Token ranges run on `threads`
+    host threads (ctypes releases the GIL inside each oracle call)."""
     import oracle
 
-    n = _oracle_threads()
     s = hw.spec
 
     def hash_part(b):
@@ -422,53 +432,192 @@ def oracle_step_seconds(hw, table_host, gate_host, gate_tokens: int, hash_tokens
                                   s.num_orders, s.heads, s.multipliers, s.primes, b[0], b[1])
         oracle.gather_rows(table_host, s.primes, idx)
 
-    def gate_part(b):
-        sl = slice(b[0], b[1])
-        g = gate_host
-        oracle.gate_fwd(g["h"][sl], g["k"][sl], g["v"][sl], g["w_h"], g["w_k"], EPS)
-        oracle.gate_bwd(g["dout"][sl], g["h"][sl], g["k"][sl], g["v"][sl], g["w_h"], g["w_k"], EPS)
+    def gate_part(args):
+        m, (t0, t1) = args
+        oracle.gate_fwd(m["h"], m["k"], m["v"], w_h, w_k, EPS, t0, t1)
+        return oracle.gate_bwd(m["dout"], m["h"], m["k"], m["v"], w_h, w_k, EPS, t0, t1)["dweight"]
 
-    with ThreadPoolExecutor(n) as ex:
-        hb = [(hash_tokens * i // n, hash_tokens * (i + 1) // n) for i in range(n)]
-        t0 = time.perf_counter()
-        list(ex.map(hash_part, hb))
-        t1 = time.perf_counter()
-        gb = [(gate_tokens * i // n, gate_tokens * (i + 1) // n) for i in range(n)]
-        list(ex.map(gate_part, gb))
-        t2 = time.perf_counter()
-    return t1 - t0, t2 - t1, n
+    t0 = time.perf_counter()
+    list(pool.map(hash_part, _ranges(hw.T, 4 * threads)))
+    oracle.fuse_weight(w_h, w_k)
+    work = [(m, b) for m in mbs_host for b in _ranges(MICRO_T, MICRO_T // ORACLE_GATE_CHUNK)]
+    partials = np.stack(list(pool.map(gate_part, work)))
+    oracle.grad_w_reduce(partials, w_h, w_k)
+    return time.perf_counter() - t0
 
 
-def gate_host_sample(wk, n_tokens):
-    """Host copies (bf16 bits) of the first n_tokens rows of micro-batch 0."""
-    out = {}
-    m = wk["mb"][0]
-    for name in ("h", "k", "v", "dout"):
-        t = m[name][:n_tokens].contiguous().cpu()
-        out[name] = t.view(__import__("torch").int16).numpy().view(np.uint16)
-    out["w_h"] = m["w_h"].cpu().numpy()
-    out["w_k"] = m["w_k"].cpu().numpy()
-    return out
+def _bf16_bits(t):
+    """Host numpy view (raw uint16 bits) of a CPU bf16 tensor, no copy."""
+    import torch
+
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
-def gate_host_sample_synth(n_tokens):
-    """The same micro-batch drawn on the host (the reference arm runs without a GPU)."""
+def oracle_inputs_from_device(wk):
+    """Host copies of the step's device inputs: the full table and all four micro-batches."""
+    table_host = _bf16_bits(wk["table"].cpu())
+    mbs = [{n: _bf16_bits(m[n].cpu()) for n in ("h", "k", "v", "dout")} for m in wk["mb"]]
+    return table_host, mbs, wk["w_h"].cpu().numpy(), wk["w_k"].cpu().numpy()
+
+
+def oracle_inputs_on_host(hw):
+    """The same workload drawn on the host with torch's CPU generator from the same seeds and recipe
+    (values differ from the device draws; sizes and distributions are the same).  Every page of the
+    4.1 GB table and of the 2.1 GB of gate inputs is written, so the oracle reads real memory."""
+    from synth import device as SD
     from synth import workloads as W
 
-    g = W.GateWorkload(name="mb0", T=n_tokens, d=D, dtype="bf16", seed=3 * 101 + 7)
-    return W.gate_host_inputs(g)
+    table_host = _bf16_bits(SD.hash_table(hw, "cpu"))
+    mbs = []
+    for i in range(4):
+        g = W.GateWorkload(name=f"mb{i}", T=MICRO_T, d=D, dtype="bf16", seed=3 * 101 + 7 + 1000003 * i)
+        t = SD.gate_device_inputs(g, "cpu")
+        mbs.append({n: _bf16_bits(t[n]) for n in ("h", "k", "v", "dout")})
+        if i == 0:
+            w_h, w_k = t["w_h"].numpy(), t["w_k"].numpy()
+    return table_host, mbs, w_h, w_k
 
 
-def cpu_baseline(hw, gate_host, gate_tokens, reps=1):
-    table_host = np.zeros((hw.spec.total_rows, hw.row_dim), dtype=np.uint16)
-    T_all = hw.T
-    oracle_step_seconds(hw, table_host, gate_host, min(gate_tokens, 256), T_all)  # first touch of table pages
-    best = None
-    for _ in range(reps):
-        t_hash, t_gate, n = oracle_step_seconds(hw, table_host, gate_host, gate_tokens, T_all)
-        step_s = t_hash + t_gate * (4 * MICRO_T / gate_tokens)
-        best = step_s if best is None else min(best, step_s)
-    return T_all / best, n, best
+def time_oracle_steps(hw, table_host, mbs, w_h, w_k, steps: int, warmup: int):
+    """Wall seconds of each of `steps` whole oracle steps after `warmup` untimed ones."""
+    threads = _oracle_threads()
+    times = []
+    with ThreadPoolExecutor(threads) as pool:
+        for i in range(warmup + steps):
+            t = oracle_step(pool, threads, hw, table_host, mbs, w_h, w_k)
+            if i >= warmup:
+                times.append(t)
+    return times, threads
+
+
+def oracle_sample_text(steps: int, threads: int) -> str:
+    return (f"{steps} whole steps timed one by one (none sampled or scaled): hash+gather of all {SEQS * SEQ_LEN} "
+            f"tokens from the full 4.1 GB table, fold, gate fwd+bwd of all 4 x {MICRO_T} tokens, ordered "
+            f"weight-gradient reduction; {threads} host threads")
+
+
+# ----------------------------------------------------------------------------- the gate at every workload size
+
+L2_BYTES = 129 * 2 ** 20
+
+
+def _gate_config_entry(wl, device, steps: int, warmup: int, peak: float, fwd_only: bool):
+    """Gate kernels of one workload, each timed on its own over rotating input sets (so a launch
+    never finds its inputs in L2 from the previous use), plus the fwd -> bwd -> grad_w_reduce
+    sequence for training workloads.  Every timing is a CUDA-graph replay with events between
+    replays on the replaying stream; per launch = median replay time / launches per replay."""
+    import torch
+
+    import engram_conditional_memory_gb300 as ecm
+    from synth import device as SD
+
+    T, d = wl.T, wl.d
+    fwd_b = T * (8 * d + 16)
+    sets = max(2, min(8, math.ceil(6 * L2_BYTES / fwd_b)))
+    P = ecm.gate_bwd_num_partials(T, d)
+    bwd_b = T * (14 * d + 16) + 4 * d * P
+    red_b = 4 * d * P + 28 * d
+    S = []
+    for j in range(sets):
+        w = wl if j == 0 else type(wl)(**{**wl.__dict__, "seed": wl.seed + 7919 * j})
+        t = SD.gate_device_inputs(w, device, with_dout=not fwd_only)
+        s = {"in": t, "wf": ecm.fuse_weight(t["w_h"], t["w_k"]), "out": torch.empty_like(t["v"]),
+             "st": tuple(torch.empty(T, dtype=torch.float32, device=device) for _ in range(4))}
+        if not fwd_only:
+            s.update(dh=torch.empty_like(t["h"]), dk=torch.empty_like(t["k"]), dv=torch.empty_like(t["v"]),
+                     part=torch.empty((P, d), dtype=torch.float32, device=device),
+                     dw=torch.empty(d, dtype=torch.float32, device=device),
+                     gh=torch.zeros(d, dtype=torch.float32, device=device),
+                     gk=torch.zeros(d, dtype=torch.float32, device=device))
+        S.append(s)
+
+    def fwd(s):
+        t = s["in"]
+        ecm.gate_fwd(t["h"], t["k"], t["v"], s["wf"], wl.eps, out=s["out"], stats=s["st"])
+
+    def bwd(s):
+        t = s["in"]
+        ecm.gate_bwd(t["dout"], t["h"], t["k"], t["v"], s["wf"], *s["st"], P=P, dh=s["dh"], dk=s["dk"],
+                     dv=s["dv"], dw_partial=s["part"])
+
+    def red(s):
+        t = s["in"]
+        ecm.grad_w_reduce(s["part"], dweight_fused=s["dw"], w_h=t["w_h"], w_k=t["w_k"], grad_w_h=s["gh"],
+                          grad_w_k=s["gk"])
+
+    def seq(s):
+        fwd(s)
+        bwd(s)
+        red(s)
+
+    stream = torch.cuda.current_stream()
+
+    def graph_time(fn, per_replay: int):
+        for s in S:  # eager first: per-device set-up and pointer checks outside the capture
+            fn(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        prev = ecm.set_validation(0)
+        try:
+            with torch.cuda.graph(g):
+                for s in S:
+                    fn(s)
+        finally:
+            ecm.set_validation(prev)
+        for _ in range(warmup):
+            g.replay()
+        reps = max(3, math.ceil(steps / sets))
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+        torch.cuda.synchronize()
+        ev[0].record(stream)
+        for i in range(reps):
+            g.replay()
+            ev[i + 1].record(stream)
+        torch.cuda.synchronize()
+        ms = statistics.median(ev[i].elapsed_time(ev[i + 1]) for i in range(reps))
+        return ms / (sets * per_replay), reps * sets * per_replay
+
+    def entry(ms, nbytes, launches):
+        gbs = nbytes / (ms / 1e3) / 1e9
+        return {"avg_us": ms * 1e3, "bytes": nbytes, "GBps": gbs, "frac": gbs / peak, "launches_timed": launches}
+
+    res = {"T": T, "d": d, "dtype": wl.dtype, "sets": sets,
+           "l2": f"{sets} rotating input sets: {sets - 1} other launches' inputs between reuses of one set"}
+    if wl.seq_lengths is not None:
+        res["ragged"] = {"sequences": int(len(wl.seq_lengths)), "min_len": int(wl.seq_lengths.min()),
+                         "max_len": int(wl.seq_lengths.max()), "packed_as_one_T": T}
+    ms, n = graph_time(fwd, 1)
+    res["gate_fwd"] = entry(ms, fwd_b, n)
+    res["gate_fwd"]["tokens_per_s"] = T / (ms / 1e3)
+    if not fwd_only:
+        res["P"] = P
+        ms, n = graph_time(bwd, 1)
+        res["gate_bwd"] = entry(ms, bwd_b, n)
+        ms, n = graph_time(red, 1)
+        res["grad_w_reduce"] = entry(ms, red_b, n)
+        res["grad_w_reduce"]["note"] = "alone, partials read from HBM"
+        ms, n = graph_time(seq, 3)
+        step = entry(3 * ms, fwd_b + bwd_b + red_b, n)
+        step["tokens_per_s"] = T / (3 * ms / 1e3)
+        step["launches_per_step"] = 3
+        res["fwd_bwd_reduce"] = step
+    del S
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
+
+
+def time_gate_configs(device, steps: int, warmup: int, peak: float):
+    """The gate-only workloads: forward at T = 8192, d = 2048, and fwd + bwd + grad_w_reduce at
+    d = 7168 for T in {4096, 32768, 131072} and a ragged pack of 64 sequences (the gate sees one T)."""
+    from synth import workloads as W
+
+    out = {}
+    wl = W.gate_fwd_2k()
+    out[wl.name] = _gate_config_entry(wl, device, steps, warmup, peak, fwd_only=True)
+    for wl in (W.gate_sweep_7k(4096), W.gate_sweep_7k(32768), W.gate_sweep_7k(131072), W.gate_ragged_7k()):
+        out[wl.name] = _gate_config_entry(wl, device, steps, warmup, peak, fwd_only=False)
+    return out
 
 
 # ----------------------------------------------------------------------------- single-op runs (profiling)
@@ -762,6 +911,8 @@ def main():
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end timing (profiling runs)")
+    ap.add_argument("--cpu-steps", type=int, default=3, help="whole oracle steps timed for cpu_baseline")
+    ap.add_argument("--no-configs", action="store_true", help="skip the gate-only workloads (profiling runs)")
     ap.add_argument("--offload", action="store_true",
                     help="the step with the tables in host memory, prefetched on a side stream (vs in HBM)")
     ap.add_argument("--offload-ctas", type=int, default=32, help="CTAs of the host-table gather in --offload")
@@ -782,32 +933,27 @@ def main():
 
 
 def main_reference(args, rank, world):
-    """The CPU oracle on the host cores; rank 0 alone works and prints under torchrun."""
+    """The CPU oracle on the host cores, one whole step of the workload per timed step; rank 0 alone
+    works and prints under torchrun."""
     if rank != 0:
         return 0
     from synth import workloads as W
 
     hw = W.hash_gather_64k(num_seqs=SEQS, seq_len=SEQ_LEN)
-    gate_tokens = 1024
-    gate_host = gate_host_sample_synth(gate_tokens)
-    table_host = np.zeros((hw.spec.total_rows, hw.row_dim), dtype=np.uint16)
+    table_host, mbs, w_h, w_k = oracle_inputs_on_host(hw)
+    times, threads = time_oracle_steps(hw, table_host, mbs, w_h, w_k, args.steps, args.warmup)
     T_all = hw.T
-    step_s = []
-    n = 1
-    for i in range(args.warmup + args.steps):
-        t_hash, t_gate, n = oracle_step_seconds(hw, table_host, gate_host, gate_tokens, T_all)
-        if i >= args.warmup:
-            step_s.append(t_hash + t_gate * (4 * MICRO_T / gate_tokens))
-    mean_s = sum(step_s) / len(step_s)
+    mean_s = sum(times) / len(times)
     value = T_all / mean_s
-    sample = (f"per step: hash+gather of all {T_all} tokens, gate fwd+bwd of {gate_tokens} of the "
-              f"{4 * MICRO_T} gate tokens (scaled x{4 * MICRO_T // gate_tokens})")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_s * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "tokens_per_step": T_all, "parallelism": "replicas"},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": n, "kind": "oracle", "sample": sample},
+        "config": {"workload": WORKLOAD, "tokens_per_step": T_all, "parallelism": "replicas",
+                   "inputs": "drawn on the host (torch CPU generator, same seeds and recipe as the device draws)"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": oracle_sample_text(args.steps, threads),
+                         "step_ms_min": min(times) * 1e3, "step_ms_max": max(times) * 1e3},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -862,13 +1008,16 @@ def main_native(args, rank, local, world):
         e_max = aggregate_max(e_ms, device)
         e2e = {"value": world * T_all * args.steps / (e_max / 1e3), "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    configs = None if args.no_configs else time_gate_configs(device, args.steps, args.warmup, peak)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        gate_tokens = 16384
-        v, n, step_s = cpu_baseline(wk["hw"], gate_host_sample(wk, gate_tokens), gate_tokens)
-        cpu = {"value": v, "unit": "tokens/s", "cores": n, "kind": "oracle",
-               "sample": f"hash+gather of all {T_all} tokens and gate fwd+bwd of {gate_tokens} of the "
-                         f"{4 * MICRO_T} gate tokens (micro-batch 0, scaled x4); est. {step_s:.2f} s/step"}
+        table_host, mbs, w_h, w_k = oracle_inputs_from_device(wk)
+        times, threads = time_oracle_steps(wk["hw"], table_host, mbs, w_h, w_k, args.cpu_steps, 1)
+        del table_host, mbs
+        mean_s = sum(times) / len(times)
+        cpu = {"value": T_all / mean_s, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "sample": oracle_sample_text(args.cpu_steps, threads) + "; inputs copied from the device",
+               "step_ms_mean": mean_s * 1e3, "step_ms_min": min(times) * 1e3}
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -882,7 +1031,7 @@ def main_native(args, rank, local, world):
                                  "with an event between launches; e2e: eager calls with host copies"},
             "hbm_gbs": step_bytes / (max_ms / args.steps / 1e3) / 1e9,
             "hash_gather_rows_per_s": 16 * T_all / (ops["hash_gather"]["avg_ms"] / 1e3),
-            "roofline": roof, "ops": ops, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+            "roofline": roof, "ops": ops, "configs": configs, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)

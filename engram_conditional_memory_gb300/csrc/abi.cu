@@ -152,13 +152,22 @@ int32_t engram_set_max_ctas(int32_t max_ctas) { return g_max_ctas.exchange(max_c
 
 int32_t engram_set_pdl(int32_t on) { return g_pdl.exchange(on != 0 ? 1 : 0); }
 
-engram_status engram_read_error_word(const uint32_t *err_word, engram_stream_t stream, uint32_t *host_out) {
-    if (!err_word || !host_out) return fail(ENGRAM_ERR_NULL, "engram_read_error_word: NULL argument");
+static engram_status read_error_word(const char *fn, const uint32_t *err_word, engram_stream_t stream,
+                                     uint32_t *host_out) {
+    if (!err_word || !host_out) return fail(ENGRAM_ERR_NULL, "%s: NULL argument", fn);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = cudaMemcpyAsync(host_out, err_word, sizeof(uint32_t), cudaMemcpyDeviceToHost, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-    if (e != cudaSuccess) return fail(ENGRAM_ERR_CUDA, "engram_read_error_word: %s", cudaGetErrorString(e));
+    if (e != cudaSuccess) return fail(ENGRAM_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
     return *host_out ? ENGRAM_ERR_INDEX : ENGRAM_OK;
+}
+
+engram_status engram_read_error_word(const uint32_t *err_word, engram_stream_t stream, uint32_t *host_out) {
+    return read_error_word("engram_read_error_word", err_word, stream, host_out);
+}
+
+engram_status engram_get_error(const uint32_t *err_word, engram_stream_t stream, uint32_t *host_out) {
+    return read_error_word("engram_get_error", err_word, stream, host_out);
 }
 
 engram_status engram_device_status(uint32_t *host_out, int32_t clear) {

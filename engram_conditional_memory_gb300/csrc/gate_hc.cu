@@ -660,6 +660,17 @@ engram_status dispatch_hc_bwd_t(int hc, const GateHcBwdParams &p, const DeviceIn
             default: return dispatch_hc_bwd<T, 4>(p, dev, s);
         }
     }
+    // The value row's gradient reads dout; the branch kernels read the value row of kv.  So with
+    // dx written over dout it runs first, and otherwise last (which keeps dkv written over kv
+    // correct); the host refuses the two together in this form.
+    const int64_t work = p.T * (p.row_bytes / 16);
+    const int64_t grid = cap_grid(std::max<int64_t>(1, std::min<int64_t>((work + 255) / 256, 8LL * dev.num_sms)));
+    const bool dx_on_dout = p.dx == p.g;
+    if (dx_on_dout) {
+        hc_dv_kernel<T><<<static_cast<unsigned>(grid), 256, 0, s>>>(p.g, p.gate, p.dkv, p.T, hc, p.row_bytes);
+        engram_status st = check_launch("engram_gate_hc_bwd");
+        if (st != ENGRAM_OK) return st;
+    }
     for (int h = 0; h < hc; ++h) {
         GateHcBwdParams q = p;
         q.g += static_cast<size_t>(h) * p.row_bytes;
@@ -676,10 +687,15 @@ engram_status dispatch_hc_bwd_t(int hc, const GateHcBwdParams &p, const DeviceIn
         engram_status st = dispatch_hc_bwd<T, 1, true>(q, dev, s);
         if (st != ENGRAM_OK) return st;
     }
-    const int64_t work = p.T * (p.row_bytes / 16);
-    const int64_t grid = cap_grid(std::max<int64_t>(1, std::min<int64_t>((work + 255) / 256, 8LL * dev.num_sms)));
+    if (dx_on_dout) return ENGRAM_OK;
     hc_dv_kernel<T><<<static_cast<unsigned>(grid), 256, 0, s>>>(p.g, p.gate, p.dkv, p.T, hc, p.row_bytes);
     return check_launch("engram_gate_hc_bwd");
+}
+
+// Whether the byte ranges [a, a + na) and [b, b + nb) share a byte.
+bool overlaps(const void *a, int64_t na, const void *b, int64_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return na > 0 && nb > 0 && x < y + static_cast<uintptr_t>(nb) && y < x + static_cast<uintptr_t>(na);
 }
 
 engram_status hc_common_checks(const char *fn, engram_dtype dtype, int64_t T, int32_t hc, int32_t d, int *es,
@@ -766,8 +782,19 @@ extern "C" engram_status engram_gate_hc_bwd(const void *dout, const void *x, con
     const void *al[] = {dout, x, kv, w_fused, dx, dkv, dw_partial};
     for (const void *q : al)
         if (!aligned16(q)) return fail(ENGRAM_ERR_ALIGN, "%s: tensor not 16-byte aligned", fn);
+    // Outputs may be written over the input of the same layout (dx over dout or x, dkv over kv):
+    // every kernel reads a token's rows before writing that token's.  Any other overlap is refused.
+    const int64_t xb = T * hc * row_bytes, kvb = T * (hc + 1) * row_bytes;
+    if ((dx != dout && overlaps(dx, xb, dout, xb)) || (dx != x && overlaps(dx, xb, x, xb)) ||
+        overlaps(dx, xb, kv, kvb) || (dkv != kv && overlaps(dkv, kvb, kv, kvb)) || overlaps(dkv, kvb, dout, xb) ||
+        overlaps(dkv, kvb, x, xb) || overlaps(dx, xb, dkv, kvb))
+        return fail(ENGRAM_ERR_SHAPE, "%s: dx or dkv overlaps an input other than in place", fn);
     DeviceInfo dev;
     if ((st = current_device(&dev)) != ENGRAM_OK) return st;
+    if (T > 0 && dx == dout && dkv == kv &&
+        (g_hc_split.load(std::memory_order_relaxed) != 0 || !hc_fits(hc, false, row_bytes, dev.smem_optin)))
+        return fail(ENGRAM_ERR_SHAPE, "%s: dx over dout together with dkv over kv needs the whole-token form; "
+                    "rows of %lld bytes at hc = %d run branch by branch", fn, (long long)row_bytes, hc);
     const void *dp[] = {dout, x, kv, w_fused, gate, rstd_x, rstd_k, dot, dx, dkv, dw_partial};
     for (const void *q : dp)
         if ((st = check_device_ptr(q, dev.device, fn)) != ENGRAM_OK) return st;

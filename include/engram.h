@@ -32,8 +32,8 @@
  *     [T, d] tensors are d elements long (so d * element size must be a
  *     multiple of 16 bytes).
  *   - Every call is asynchronous on `stream` (NULL = the legacy default
- *     stream) and never synchronises, except engram_read_error_word and
- *     engram_device_status, which say so.
+ *     stream) and never synchronises, except engram_read_error_word (also
+ *     exported as engram_get_error) and engram_device_status, which say so.
  *   - Host-side argument checks run before anything is launched; a call that
  *     returns an error other than ENGRAM_ERR_CUDA has launched nothing.
  *   - Thread safety: calls from several host threads are safe; the text behind
@@ -41,6 +41,11 @@
  *   - The kernels contain no unbounded wait: a pipeline wait that exceeds about
  *     two seconds gives up, sets ENGRAM_DEVERR_TIMEOUT in the library's device
  *     status word and returns.
+ *   - Per-device state is looked up on a device's first call and cached for the
+ *     life of the process: the address of the library's status word and of the
+ *     allocation-free entry point's array, and kernel attributes.  A
+ *     cudaDeviceReset of a device the library has run on leaves those addresses
+ *     stale, so the library must not be called on that device after such a reset.
  */
 #ifndef ENGRAM_GB300_H
 #define ENGRAM_GB300_H
@@ -137,6 +142,9 @@ int32_t engram_set_hc_split(int32_t on);
  * Returns ENGRAM_ERR_INDEX when any bit is set, ENGRAM_OK otherwise.
  */
 engram_status engram_read_error_word(const uint32_t *err_word, engram_stream_t stream, uint32_t *host_out);
+
+/* The same call under a second name (identical arguments, behaviour and return codes). */
+engram_status engram_get_error(const uint32_t *err_word, engram_stream_t stream, uint32_t *host_out);
 
 /*
  * The library's own device status word of the current device (ENGRAM_DEVERR_* bits
@@ -347,6 +355,11 @@ engram_status engram_gate_hc_fwd(const void *x, const void *kv, engram_dtype dty
  * dx is [T, hc, d]; dkv is [T, hc+1, d] (row hc = dv).  dw_partial is [P, hc, d] fp32 with
  * partial p the sum of c_h x_h k_h over tokens [p*C, min(T, (p+1)*C)), C = ceil(T / P) --
  * reduce it with engram_grad_w_reduce over hc*d columns.
+ * In-place writing: dx may be dout or x, and dkv may be kv (the same pointer, the same layout);
+ * any other overlap between dx, dkv and the inputs is refused (ENGRAM_ERR_SHAPE).  Rows that run
+ * branch by branch (see engram_gate_hc_fwd) take dx over dout or dkv over kv, but not both in one
+ * call: the value row's gradient reads dout and the branch kernels read the value row, so that
+ * pair is refused there (ENGRAM_ERR_SHAPE) and served only by the whole-token form.
  */
 engram_status engram_gate_hc_bwd(const void *dout, const void *x, const void *kv, engram_dtype dtype,
                                  const float *w_fused, const float *gate, const float *rstd_x,
@@ -515,7 +528,9 @@ engram_status engram_sinkhorn_finalize(const float *matrix, const float *row_sca
  *     ENGRAM_ERR_SHAPE and a message; use engram_gate_bwd with a buffer then.
  *   - The first call on a device looks up the array's device address on that
  *     device (cudaGetSymbolAddress) and caches it: make that first call, with the
- *     device current, before any stream capture on it.
+ *     device current, before any stream capture on it.  The cached address does
+ *     not survive a cudaDeviceReset of that device: do not call this entry point
+ *     (or any other of the library) on a device after resetting it.
  *   - All calls share the one array, which keeps whatever the last call left
  *     there.  Each call overwrites every partial row it reads, so nothing has to
  *     be cleared between calls, but calls that overlap on the GPU (other

@@ -92,3 +92,62 @@ def oracle_gate_bwd(g, h, k, v, w_h, w_k, eps):
     out["dweight"] = np.sum([p["dweight"] for p in parts], axis=0)
     out["dweight_abs"] = np.sum([p["dweight_abs"] for p in parts], axis=0)
     return out
+
+
+def _bf16_bad(g: np.ndarray, ref: np.ndarray) -> np.ndarray:
+    """Elements of a bf16 result (raw bits) outside the bf16 output tolerance of an fp64 reference."""
+    return np.abs(_f64(g) - ref) > BF16_ATOL + BF16_RTOL * np.abs(ref)
+
+
+def check_gate_train_by_partials(t: dict, r: dict, eps: float, what: str, group_tokens: int = 16384):
+    """Every element of the gate's forward and backward outputs and every weight-gradient partial of a
+    bf16 training step (`r`, on the device, made from the inputs `t`) against the oracle.
+
+    The oracle runs once per partial, over exactly that partial's token range, so each partial is
+    compared with the oracle's sum over the same tokens; out, the statistics, dh, dk and dv of those
+    tokens are compared element by element.  Host copies are taken a group of partials at a time to
+    bound host memory, and the partials of a group run on all host threads.  Finally the reduced
+    dweight is compared with the oracle's sum over all partials in order."""
+    T, d = t["h"].shape
+    P = r["part"].shape[0]
+    C = -(-T // P) if T else 1
+    w_h, w_k = host_bits(t["w_h"]), host_bits(t["w_k"])
+    w = (w_h * w_k).astype(np.float64)
+    parts = as_f64(r["part"])
+    total, total_abs = np.zeros(d), np.zeros(d)
+    per_group = max(1, group_tokens // C)
+    n = _threads()
+    for g0 in range(0, P, per_group):
+        p1 = min(P, g0 + per_group)
+        t0, t1 = g0 * C, min(T, p1 * C)
+        if t0 >= T:
+            assert (parts[g0:] == 0).all(), f"{what}: partials past the last token are not zero"
+            break
+        x = {k: host_bits(t[k][t0:t1]) for k in ("h", "k", "v", "dout")}
+        y = {k: host_bits(r[k][t0:t1]) for k in ("out", "dh", "dk", "dv")}
+        s = {k: as_f64(r[k][t0:t1]) for k in ("alpha", "rstd_h", "rstd_k", "dot")}
+
+        def task(p):
+            a, b = p * C - t0, min(T, (p + 1) * C) - t0
+            if a >= b:
+                return p, np.zeros(d), np.zeros(d)
+            f = oracle.gate_fwd(x["h"], x["k"], x["v"], w_h, w_k, eps, a, b)
+            bw = oracle.gate_bwd(x["dout"], x["h"], x["k"], x["v"], w_h, w_k, eps, a, b)
+            assert np.abs(s["alpha"][a:b] - f["alpha"]).max() <= ALPHA_ATOL, f"{what} alpha, partial {p}"
+            for key in ("rstd_h", "rstd_k"):
+                assert (np.abs(s[key][a:b] - f[key]) <= RSTD_RTOL * np.abs(f[key])).all(), f"{what} {key}, p {p}"
+            scale = np.abs(_f64(x["h"][a:b]) * w[None, :] * _f64(x["k"][a:b])).sum(-1)
+            assert (np.abs(s["dot"][a:b] - f["dot"]) <= 2e-5 * scale + 1e-6).all(), f"{what} dot, partial {p}"
+            for key, ref in (("out", f["out"]), ("dh", bw["dh"]), ("dk", bw["dk"]), ("dv", bw["dv"])):
+                bad = _bf16_bad(y[key][a:b], ref)
+                assert not bad.any(), f"{what} {key}: {bad.sum()} of {bad.size} outside tolerance in partial {p}"
+            got = parts[p]
+            assert (np.abs(got - bw["dweight"]) <= 1e-4 * bw["dweight_abs"] + 1e-7).all(), f"{what} partial {p}"
+            return p, bw["dweight"], bw["dweight_abs"]
+
+        with ThreadPoolExecutor(n) as ex:
+            for _, dw_p, abs_p in ex.map(task, range(g0, p1)):  # in partial order
+                total += dw_p
+                total_abs += abs_p
+    dw = as_f64(r["dw"])
+    assert (np.abs(dw - total) <= 1e-4 * total_abs + 1e-7).all(), f"{what}: reduced dweight"

@@ -26,8 +26,9 @@ def _declared():
 
 def test_header_declares_the_boundary():
     names = _declared()
+    # the hot path's entry points and the error reader, under the names the scope table gives them
     for required in ("engram_hash_gather", "engram_fuse_weight", "engram_gate_fwd", "engram_gate_bwd",
-                     "engram_gate_bwd_num_partials", "engram_grad_w_reduce"):
+                     "engram_gate_bwd_num_partials", "engram_grad_w_reduce", "engram_get_error"):
         assert required in names
 
 

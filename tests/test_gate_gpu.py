@@ -3,7 +3,8 @@
 Every comparison goes through the C ABI (via the thin binding).  Sizes: the tiny
 fp32 workload; the T = 8192, d = 2048 and T = 16384, d = 4096 bf16 workloads in
 full; the d = 7168 sweep (T = 4096, 32768, 131072 and a ragged 64-sequence pack)
-on sampled tokens and sampled partials, plus properties that hold at any size.
+element by element, each weight-gradient partial against the oracle over its own
+token range, plus properties that hold at any size.
 """
 import numpy as np
 import pytest
@@ -82,41 +83,16 @@ def test_full_size_bf16_workloads(wl):
     assert (np.abs(dw - b["dweight"]) <= 1e-4 * b["dweight_abs"] + 1e-7).all()
 
 
-def _sample_tokens(T, n, seed):
-    pick = set(G.uniform_int(seed, n, 0, T).tolist()) | {0, T - 1, T // 2}
-    return np.array(sorted(pick), dtype=np.int64)
-
-
 SWEEP = [W.gate_sweep_7k(4096), W.gate_sweep_7k(32768), W.gate_sweep_7k(131072), W.gate_ragged_7k()]
 
 
 @pytest.mark.parametrize("wl", SWEEP, ids=lambda w: w.name)
-def test_large_hidden_sweep_sampled(wl):
+def test_large_hidden_sweep_every_element(wl):
     t = SD.gate_device_inputs(wl, DEV)
     r = _train_step(t, wl.eps)
     torch.cuda.synchronize()
-    idx = _sample_tokens(wl.T, 96, wl.seed)
-    it = torch.from_numpy(idx).to(DEV)
-    x = {n: H.host_bits(t[n].index_select(0, it)) for n in ("h", "k", "v", "dout")}
-    w_h, w_k = H.host_bits(t["w_h"]), H.host_bits(t["w_k"])
-    f = H.oracle_gate_fwd(x["h"], x["k"], x["v"], w_h, w_k, wl.eps)
-    b = H.oracle_gate_bwd(x["dout"], x["h"], x["k"], x["v"], w_h, w_k, wl.eps)
-    sel = {n: r[n].index_select(0, it) for n in ("out", "dh", "dk", "dv", "alpha", "rstd_h", "rstd_k", "dot")}
-    H.check_stats(sel["alpha"], sel["rstd_h"], sel["rstd_k"], sel["dot"], f, x["h"], x["k"], w_h * w_k, wl.name)
-    H.assert_close_bf16(sel["out"], f["out"], "out")
-    for name in ("dh", "dk", "dv"):
-        H.assert_close_bf16(sel[name], b[name], name)
-
-    # sampled partials against the oracle over exactly their token ranges
-    P = r["part"].shape[0]
-    chunk = -(-wl.T // P)
-    for p in sorted({0, P - 1, P // 3}):
-        t0, t1 = p * chunk, min(wl.T, (p + 1) * chunk)
-        sl = slice(t0, t1)
-        ob = oracle.gate_bwd(*(H.host_bits(t[n][sl]) for n in ("dout", "h", "k", "v")), w_h, w_k, wl.eps)
-        got = H.as_f64(r["part"][p])
-        assert (np.abs(got - ob["dweight"]) <= 1e-4 * ob["dweight_abs"] + 1e-7).all(), f"partial {p}"
-    # the reduction is the sum of the partials (property at full size)
+    H.check_gate_train_by_partials(t, r, wl.eps, wl.name)
+    # the reduction is the sum of the partials (a property that holds at any size)
     S = r["part"].double().sum(0).cpu().numpy()
     A = r["part"].double().abs().sum(0).cpu().numpy()
     assert (np.abs(H.as_f64(r["dw"]) - S) <= 1e-5 * A + 1e-7).all()

@@ -1,8 +1,8 @@
 """GPU parity of the multi-branch gate (x [T, hc, d], kv [T, hc+1, d]) against the CPU oracle.
 
 Sizes: small fp32/bf16 cases for hc = 1, 2, 4; the production shape T = 8192, hc = 4, d = 4096
-(bf16) element by element; edge cases: the clamp branch (k = 0), in-place writing, an empty
-batch, and bitwise reruns.  The fused weight is [hc, d] (engram_fuse_weight over hc*d) and the
+(bf16) element by element; edge cases: the clamp branch (k = 0), in-place writing (forward and
+backward, in both forms), an empty batch, and bitwise reruns.  The fused weight is [hc, d] (engram_fuse_weight over hc*d) and the
 partials reduce with engram_grad_w_reduce over hc*d columns.
 """
 import math
@@ -202,3 +202,47 @@ def test_empty_batch_and_bitwise_reruns():
     a, b = _run(t, wl), _run(t, wl)
     for k in ("out", "gate", "dx", "dkv", "part", "dw"):
         assert torch.equal(a[k], b[k]), k
+
+
+@pytest.mark.parametrize("split", [False, True], ids=["whole_token", "branch_by_branch"])
+def test_in_place_backward(split):
+    """dx written over dout, and dkv over kv, give bitwise the out-of-place results in both forms.
+    The pair together is served by the whole-token form and refused, before anything is written,
+    in the branch-by-branch form (the value row's gradient reads dout, the branch kernels read the
+    value row).  Other overlaps of an output with an input are refused."""
+    wl = W.GateHcWorkload(name="ipb", T=300, hc=4, d=1024, dtype="bf16", seed=43)
+    t = _dev(W.gate_hc_host_inputs(wl))
+    prev = ecm.set_hc_split(split)
+    try:
+        r = _run(t, wl)
+        st = (r["gate"], r["rstd_x"], r["rstd_k"], r["dot"])
+        P = r["part"].shape[0]
+
+        def bwd(dout, kv, **kw):
+            return ecm.gate_hc_bwd(dout, t["x"], kv, r["wf"], *st, wl.clamp, P=P, **kw)
+
+        g = t["dout"].clone()
+        dx, dkv, part = bwd(g, t["kv"], dx=g)
+        assert dx.data_ptr() == g.data_ptr()
+        assert torch.equal(g, r["dx"]) and torch.equal(dkv, r["dkv"]) and torch.equal(part, r["part"])
+        kv = t["kv"].clone()
+        dx, _, part = bwd(t["dout"], kv, dkv=kv)
+        assert torch.equal(dx, r["dx"]) and torch.equal(kv, r["dkv"]) and torch.equal(part, r["part"])
+        g, kv = t["dout"].clone(), t["kv"].clone()
+        if split:
+            with pytest.raises(ecm.EngramError) as e:
+                bwd(g, kv, dx=g, dkv=kv)
+            assert e.value.status == 2
+            torch.cuda.synchronize()
+            assert torch.equal(g, t["dout"]) and torch.equal(kv, t["kv"])
+        else:
+            bwd(g, kv, dx=g, dkv=kv)
+            assert torch.equal(g, r["dx"]) and torch.equal(kv, r["dkv"])
+        # an output shifted by one token against its input, and dx over the keys: refused
+        big = torch.cat([t["dout"], t["dout"][:1]]).contiguous()
+        with pytest.raises(ecm.EngramError):
+            bwd(big[1:], t["kv"], dx=big[:-1])
+        with pytest.raises(ecm.EngramError):
+            bwd(t["dout"], t["kv"], dx=t["kv"].view(-1)[: 300 * 4 * 1024].view(300, 4, 1024))
+    finally:
+        ecm.set_hc_split(prev)
