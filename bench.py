@@ -7,9 +7,10 @@ tokens (65,536 tokens):
      ~2.0M-row prime tables, 64 bf16 per row, 4.1 GB resident) -> e [65536, 1024];
   2. the weight fold w = w_h * w_k;
   3. the context-aware gate, forward + backward on four micro-batches of
-     T = 16384 tokens at d = 4096 (bf16), then one ordered reduction of the
-     four micro-batches' weight-gradient partials, accumulating into fp32
-     grad_w_h / grad_w_k (11 kernel launches: the hash + gather is one).
+     T = 16384 tokens at d = 4096 (bf16), the backwards adding into one array
+     of weight-gradient partials (the first writes it), then one ordered
+     reduction of those partials, accumulating into fp32 grad_w_h / grad_w_k
+     (11 kernel launches: the hash + gather is one).
 The reported value is tokens/s through the whole step (whole job, all ranks).
 Inputs are resident in HBM (the device-timed value) or copied from pinned host
 memory every step (the `e2e` value).  The per-step working set (4.1 GB table,
@@ -172,7 +173,8 @@ def algorithmic_bytes(P: int):
         "fuse_weight": 3 * 4 * D,
         "gate_fwd": MICRO_T * (8 * D + 16),                       # h, k, v read, out written, 4 fp32 stats
         "gate_bwd": MICRO_T * (14 * D + 16) + P * D * 4,         # dout, v, h, k, stats read; dh, dk, dv, partials
-        "grad_w_reduce": 4 * P * D * 4 + 7 * D * 4,               # 4 micro-batches' partials, w_h, w_k, grads, dweight
+        "gate_bwd_accumulate": MICRO_T * (14 * D + 16) + 2 * P * D * 4,  # the same + the partials read back
+        "grad_w_reduce": P * D * 4 + 7 * D * 4,                   # the accumulated partials, w_h, w_k, grads, dweight
     }
 
 
@@ -210,9 +212,8 @@ def make_workload(device):
     wk["dv"] = [torch.empty_like(o) for o in wk["out"]]
     wk["stats"] = [tuple(torch.empty(MICRO_T, dtype=torch.float32, device=device) for _ in range(4))
                    for _ in range(4)]
-    # the four micro-batches' weight-gradient partials side by side: one ordered reduction per step
-    wk["part_all"] = torch.empty((4 * P, D), dtype=torch.float32, device=device)
-    wk["part"] = [wk["part_all"][i * P:(i + 1) * P] for i in range(4)]
+    # one array of weight-gradient partials: micro-batch 0 writes it, 1-3 add to it, one reduction
+    wk["part"] = torch.empty((P, D), dtype=torch.float32, device=device)
     wk["dweight"] = torch.empty(D, dtype=torch.float32, device=device)
     wk["grad_w_h"] = torch.zeros(D, dtype=torch.float32, device=device)
     wk["grad_w_k"] = torch.zeros(D, dtype=torch.float32, device=device)
@@ -234,19 +235,19 @@ def run_step(wk, mark=None):
         ecm.gate_fwd(m["h"], m["k"], m["v"], wk["w_fused"], EPS, out=wk["out"][i], stats=st)
         mark and mark("gate_fwd")
         ecm.gate_bwd(m["dout"], m["h"], m["k"], m["v"], wk["w_fused"], *st, P=wk["P"], dh=wk["dh"][i],
-                     dk=wk["dk"][i], dv=wk["dv"][i], dw_partial=wk["part"][i])
-        mark and mark("gate_bwd")
+                     dk=wk["dk"][i], dv=wk["dv"][i], dw_partial=wk["part"], accumulate=i > 0)
+        mark and mark("gate_bwd_accumulate" if i else "gate_bwd")
     reduce_step(wk)
     mark and mark("grad_w_reduce")
     return 11
 
 
 def reduce_step(wk):
-    """The step's weight gradient: the four micro-batches' partials in one ordered reduction,
-    accumulated into grad_w_h and grad_w_k as gradient accumulation would."""
+    """The step's weight gradient: one ordered reduction of the partials the four micro-batches
+    added into, accumulated into grad_w_h and grad_w_k as gradient accumulation would."""
     import engram_conditional_memory_gb300 as ecm
 
-    ecm.grad_w_reduce(wk["part_all"], dweight_fused=wk["dweight"], w_h=wk["w_h"], w_k=wk["w_k"],
+    ecm.grad_w_reduce(wk["part"], dweight_fused=wk["dweight"], w_h=wk["w_h"], w_k=wk["w_k"],
                       grad_w_h=wk["grad_w_h"], grad_w_k=wk["grad_w_k"])
 
 
@@ -381,7 +382,7 @@ def time_e2e(wk, steps, warmup, device):
             st = wk["stats"][i]
             ecm.gate_fwd(m["h"], m["k"], m["v"], wk["w_fused"], EPS, out=wk["out"][i], stats=st)
             ecm.gate_bwd(m["dout"], m["h"], m["k"], m["v"], wk["w_fused"], *st, P=wk["P"], dh=wk["dh"][i],
-                         dk=wk["dk"][i], dv=wk["dv"][i], dw_partial=wk["part"][i])
+                         dk=wk["dk"][i], dv=wk["dv"][i], dw_partial=wk["part"], accumulate=i > 0)
             done[i].record(comp)
         reduce_step(wk)
         res_h[:D].copy_(wk["grad_w_h"], non_blocking=True)
@@ -781,13 +782,18 @@ def main_only(args, device):
 
             def launch():
                 ecm.gate_bwd(t["dout"], t["h"], t["k"], t["v"], wf, *st, P=P, dh=dh, dk=dk, dv=dv, dw_partial=part)
-        elif op == "grad_w_reduce":  # the step's launch: four micro-batches' partials, both weight gradients
-            part4 = part.repeat(4, 1)
-            gh, gk = torch.zeros_like(t["w_h"]), torch.zeros_like(t["w_k"])
-            nbytes = 4 * P * wl.d * 4 + 7 * wl.d * 4
+        elif op == "gate_bwd_accumulate":  # the step's later backwards: partials read back and added to
+            nbytes = wl.T * (14 * wl.d + 16) + 2 * P * wl.d * 4
 
             def launch():
-                ecm.grad_w_reduce(part4, dweight_fused=wf, w_h=t["w_h"], w_k=t["w_k"], grad_w_h=gh, grad_w_k=gk)
+                ecm.gate_bwd(t["dout"], t["h"], t["k"], t["v"], wf, *st, P=P, dh=dh, dk=dk, dv=dv, dw_partial=part,
+                             accumulate=True)
+        elif op == "grad_w_reduce":  # the step's launch: the accumulated partials, both weight gradients
+            gh, gk = torch.zeros_like(t["w_h"]), torch.zeros_like(t["w_k"])
+            nbytes = P * wl.d * 4 + 7 * wl.d * 4
+
+            def launch():
+                ecm.grad_w_reduce(part, dweight_fused=wf, w_h=t["w_h"], w_k=t["w_k"], grad_w_h=gh, grad_w_k=gk)
         else:  # gate_fwd on T=16384 d=4096, or gate_fwd_2k on T=8192 d=2048
             nbytes = wl.T * (8 * wl.d + 16)
 
@@ -858,7 +864,7 @@ def main_offload(args, device):
             st = wk["stats"][i]
             ecm.gate_fwd(m["h"], m["k"], m["v"], wk["w_fused"], EPS, out=wk["out"][i], stats=st)
             ecm.gate_bwd(m["dout"], m["h"], m["k"], m["v"], wk["w_fused"], *st, P=wk["P"], dh=wk["dh"][i],
-                         dk=wk["dk"][i], dv=wk["dv"][i], dw_partial=wk["part"][i])
+                         dk=wk["dk"][i], dv=wk["dv"][i], dw_partial=wk["part"], accumulate=i > 0)
         reduce_step(wk)
 
     def offload_step():
@@ -917,7 +923,8 @@ def main():
                     help="the step with the tables in host memory, prefetched on a side stream (vs in HBM)")
     ap.add_argument("--offload-ctas", type=int, default=32, help="CTAs of the host-table gather in --offload")
     ap.add_argument("--only", choices=["hash_gather", "hash_gather_small", "hash_gather_host", "gate_fwd",
-                                       "gate_fwd_2k", "gate_bwd", "grad_w_reduce", "gate_hc_fwd", "gate_hc_bwd",
+                                       "gate_fwd_2k", "gate_bwd", "gate_bwd_accumulate", "grad_w_reduce",
+                                       "gate_hc_fwd", "gate_hc_bwd",
                                        "sinkhorn", "sinkhorn_momentum", "sinkhorn_step", "sinkhorn_reduce",
                                        "sinkhorn_finalize", "short_conv_fwd", "short_conv_fwd_given", "short_conv_bwd",
                                        "short_conv_reduce", "gate_conv_fwd", "gate_conv_fwd_fused", "gate_hc_fwd_d7168",
@@ -997,8 +1004,9 @@ def main_native(args, rank, local, world):
         avg = sum(times) / len(times)
         gbs = ab[name] / (avg / 1e3) / 1e9
         ops[name] = {"avg_ms": avg, "launches": len(times), "bytes": ab[name], "GBps": gbs, "frac": gbs / peak}
-    step_bytes = ab["hash_gather"] + ab["fuse_weight"] + 4 * (ab["gate_fwd"] + ab["gate_bwd"]) + ab["grad_w_reduce"]
-    dom = "gate_bwd"
+    step_bytes = (ab["hash_gather"] + ab["fuse_weight"] + 4 * ab["gate_fwd"] + ab["gate_bwd"]
+                  + 3 * ab["gate_bwd_accumulate"] + ab["grad_w_reduce"])
+    dom = "gate_bwd_accumulate"  # three of the four backward launches
     roof = {"bound": "hbm", "kernel": dom, "achieved": ops[dom]["GBps"], "peak": peak, "unit": "GB/s",
             "frac": ops[dom]["GBps"] / peak, "peak_kind": f"{peak_kind} (copy bandwidth)",
             "traffic": load_traffic(dom), "algorithmic_bytes_per_launch": ab[dom]}

@@ -84,6 +84,8 @@ def load_library():
             "engram_gate_bwd_num_partials": (st, [_i64, _i32, _p]),
             "engram_gate_bwd": (st, [_p, _p, _p, _p, _c.c_int, _p, _p, _p, _p, _p, _i64, _i32, _p, _p, _p, _p,
                                      _i32, _p]),
+            "engram_gate_bwd_accumulate": (st, [_p, _p, _p, _p, _c.c_int, _p, _p, _p, _p, _p, _i64, _i32, _p, _p,
+                                                _p, _p, _i32, _p]),
             "engram_grad_w_reduce": (st, [_p, _i32, _i32, _p, _p, _p, _p, _p, _p]),
             "engram_gate_hc_fwd": (st, [_p, _p, _c.c_int, _p, _i64, _i32, _i32, _c.c_float, _c.c_float, _p, _p, _p,
                                         _p, _p, _p]),
@@ -241,8 +243,9 @@ def gate_bwd_num_partials(T: int, d: int) -> int:
 
 
 def gate_bwd(dout, h, k, v, w_fused, alpha, rstd_h, rstd_k, dot, P: int | None = None, dh=None, dk=None, dv=None,
-             dw_partial=None, stream=None):
-    """Returns (dh, dk, dv, dw_partial [P, d] fp32)."""
+             dw_partial=None, accumulate: bool = False, stream=None):
+    """Returns (dh, dk, dv, dw_partial [P, d] fp32).  accumulate=True adds each partial's terms onto the
+    given dw_partial's rows (engram_gate_bwd_accumulate) instead of overwriting them."""
     lib = load_library()
     for name, t in (("dout", dout), ("h", h), ("k", k), ("v", v)):
         _need(t, name, h.dtype)
@@ -255,13 +258,15 @@ def gate_bwd(dout, h, k, v, w_fused, alpha, rstd_h, rstd_k, dot, P: int | None =
     dk = torch.empty_like(k) if dk is None else _need(dk, "dk", h.dtype)
     dv = torch.empty_like(v) if dv is None else _need(dv, "dv", h.dtype)
     if dw_partial is None:
+        if accumulate:
+            raise ValueError("accumulate=True needs the dw_partial to add to")
         dw_partial = torch.empty((P, d), dtype=torch.float32, device=h.device)
     else:
         _need(dw_partial, "dw_partial", torch.float32)
-    _check(lib.engram_gate_bwd(_ptr(dout), _ptr(h), _ptr(k), _ptr(v), _DTYPES[h.dtype], _ptr(w_fused), _ptr(alpha),
-                               _ptr(rstd_h), _ptr(rstd_k), _ptr(dot), T, d, _ptr(dh), _ptr(dk), _ptr(dv),
-                               _ptr(dw_partial), P, _stream(stream)),
-           "engram_gate_bwd")
+    fn = lib.engram_gate_bwd_accumulate if accumulate else lib.engram_gate_bwd
+    _check(fn(_ptr(dout), _ptr(h), _ptr(k), _ptr(v), _DTYPES[h.dtype], _ptr(w_fused), _ptr(alpha), _ptr(rstd_h),
+              _ptr(rstd_k), _ptr(dot), T, d, _ptr(dh), _ptr(dk), _ptr(dv), _ptr(dw_partial), P, _stream(stream)),
+           "engram_gate_bwd_accumulate" if accumulate else "engram_gate_bwd")
     return dh, dk, dv, dw_partial
 
 

@@ -8,9 +8,12 @@
 //   kColGroups / kColRun runs of kColRun consecutive group sums, each in ascending order;
 //   the run sums in ascending order.
 // A CTA of kColThreads threads, one per SM, owns a contiguous share of the columns (the shares differ
-// by one column at most) and takes them kColCols at a time: thread i of a chunk sums column
-// i mod ncols of group i / ncols with kColBatch 16-byte loads in flight, so that every SM keeps about
-// 128 KB of partials in flight.  Which CTA owns a column does not change its sum.
+// by one column at most) and takes them up to kColCols at a time.  The (group, column) sums of a chunk
+// are spread over the threads, item i being column i mod ncols of group i / ncols, and a thread walks
+// its items' rows as one sequence in batches of kColBatch 16-byte loads that cross item boundaries:
+// with few rows per group (small P) every load of a chunk is still in flight at once, and with many
+// every SM keeps about 128 KB of partials in flight.  Which CTA owns a column, and which thread sums a
+// group, does not change its sum.
 #pragma once
 
 #include "engram_internal.cuh"
@@ -20,7 +23,7 @@ namespace engram {
 constexpr int kColGroups = 128;
 constexpr int kColRun = 16;
 constexpr int kColThreads = 1024;
-constexpr int kColCols = kColThreads / kColGroups;  // float4 columns per chunk
+constexpr int kColCols = 20;  // float4 columns per chunk (the chunk's group sums fill 40 KB of shared memory)
 constexpr int kColBatch = 8;
 static_assert(kColGroups % kColRun == 0, "runs of whole groups");
 
@@ -51,25 +54,48 @@ __device__ __forceinline__ void column_sums(const float4 *__restrict__ part, int
     int c_begin, c_end;
     column_share(d4, c_begin, c_end);
     const int rows = (P + kColGroups - 1) / kColGroups;
+    const int geff = rows > 0 ? (P + rows - 1) / rows : 0;  // groups with at least one row
     for (int cc = c_begin; cc < c_end; cc += kColCols) {
         const int ncols = c_end - cc < kColCols ? c_end - cc : kColCols;
-        if (tid < ncols * kColGroups) {
-            const int g = tid / ncols;
-            const int j = tid - g * ncols;
-            const int p0 = g * rows;
-            const int p1 = p0 + rows < P ? p0 + rows : P;
-            const float4 *src = part + cc + j;
-            float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int q0 = p0; q0 < p1; q0 += kColBatch) {
-                float4 x[kColBatch];
+        for (int i = geff * ncols + tid; i < kColGroups * ncols; i += kColThreads)  // groups without rows
+            sm.group[(i / ncols) * kColCols + i % ncols] = make_float4(0.f, 0.f, 0.f, 0.f);
+        const int nitems = geff * ncols;
+        // issue cursor: item `it` = (group g, column j), next row p of [g rows, pend)
+        int it = tid, g = it / ncols, j = it - g * ncols, p = g * rows;
+        int pend = min(P, p + rows);
+        // consume cursor: the same sequence, behind by the loads of one batch
+        int cit = it, cg = g, cj = j, cp = p, cpend = pend;
+        float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+        while (it < nitems) {
+            float4 x[kColBatch];
 #pragma unroll
-                for (int b = 0; b < kColBatch; ++b)
-                    if (q0 + b < p1) x[b] = __ldcs(src + static_cast<size_t>(q0 + b) * d4);
-#pragma unroll
-                for (int b = 0; b < kColBatch; ++b)
-                    if (q0 + b < p1) add4(s, x[b]);
+            for (int b = 0; b < kColBatch; ++b) {
+                if (it < nitems) {
+                    x[b] = __ldcs(part + static_cast<size_t>(p) * d4 + cc + j);
+                    if (++p == pend) {
+                        it += kColThreads;
+                        g = it / ncols;
+                        j = it - g * ncols;
+                        p = g * rows;
+                        pend = min(P, p + rows);
+                    }
+                }
             }
-            sm.group[g * kColCols + j] = s;
+#pragma unroll
+            for (int b = 0; b < kColBatch; ++b) {
+                if (cit < nitems) {
+                    add4(s, x[b]);
+                    if (++cp == cpend) {
+                        sm.group[cg * kColCols + cj] = s;
+                        s = make_float4(0.f, 0.f, 0.f, 0.f);
+                        cit += kColThreads;
+                        cg = cit / ncols;
+                        cj = cit - cg * ncols;
+                        cp = cg * rows;
+                        cpend = min(P, cp + rows);
+                    }
+                }
+            }
         }
         __syncthreads();
         if (tid < ncols * (kColGroups / kColRun)) {

@@ -35,6 +35,7 @@ struct GateBwdParams {
     int32_t d;
     uint32_t row_bytes;
     int32_t stages;
+    int32_t accumulate;  // 1: each partial row adds its tokens' terms onto the row's current contents
     float scale;  // 1/sqrt(d)
 };
 
@@ -122,11 +123,23 @@ __global__ void __launch_bounds__((NCW + 1) * 32) gate_bwd_kernel(const __grid_c
     for (int64_t pp = blockIdx.x; pp < p.P && !failed; pp += gridDim.x) {
         const int64_t t0 = pp * p.chunk;
         const int64_t t1 = t0 + p.chunk < p.T ? t0 + p.chunk : p.T;
+        // the partial row's accumulators: zero, or (accumulate) the row as a previous call left it, its
+        // load overlapping the first stage's wait
+        float *prow = p.dw_partial + static_cast<size_t>(pp) * p.d;
         float acc[kVPT][EV];
 #pragma unroll
-        for (int m = 0; m < kVPT; ++m)
+        for (int m = 0; m < kVPT; ++m) {
+            const int j = c + m * NC;
 #pragma unroll
-            for (int e = 0; e < EV; ++e) acc[m][e] = 0.f;
+            for (int e = 0; e < EV; e += 4) {
+                float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (p.accumulate && j < nvec) q = *reinterpret_cast<const float4 *>(prow + j * EV + e);
+                acc[m][e] = q.x;
+                acc[m][e + 1] = q.y;
+                acc[m][e + 2] = q.z;
+                acc[m][e + 3] = q.w;
+            }
+        }
 
         for (int64_t t = t0; t < t1; ++t, ++it) {
             const int s = static_cast<int>(it % S);
@@ -199,8 +212,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32) gate_bwd_kernel(const __grid_c
         }
         if (failed) break;
 
-        // this partial's row of dw_partial (zeros for a partial with no token)
-        float *prow = p.dw_partial + static_cast<size_t>(pp) * p.d;
+        // this partial's row of dw_partial (zeros, or the row unchanged, for a partial with no token)
 #pragma unroll
         for (int m = 0; m < kVPT; ++m) {
             const int j = c + m * NC;
@@ -280,27 +292,28 @@ extern "C" engram_status engram_gate_bwd_num_partials(int64_t T, int32_t d, int3
     return ENGRAM_OK;
 }
 
-extern "C" engram_status engram_gate_bwd(const void *dout, const void *h, const void *k, const void *v,
-                                         engram_dtype dtype, const float *w_fused, const float *alpha,
-                                         const float *rstd_h, const float *rstd_k, const float *dot, int64_t T,
-                                         int32_t d, void *dh, void *dk, void *dv, float *dw_partial, int32_t P,
-                                         engram_stream_t stream) {
+namespace {
+
+engram_status gate_bwd_call(const char *fn, int accumulate, const void *dout, const void *h, const void *k,
+                            const void *v, engram_dtype dtype, const float *w_fused, const float *alpha,
+                            const float *rstd_h, const float *rstd_k, const float *dot, int64_t T, int32_t d,
+                            void *dh, void *dk, void *dv, float *dw_partial, int32_t P, engram_stream_t stream) {
     // Per-token tensors may be NULL only when there is no token; dw_partial is always written.
     if (!w_fused || !dw_partial ||
         (T > 0 && (!dout || !h || !k || !v || !alpha || !rstd_h || !rstd_k || !dot || !dh || !dk || !dv)))
-        return fail(ENGRAM_ERR_NULL, "engram_gate_bwd: NULL pointer");
+        return fail(ENGRAM_ERR_NULL, "%s: NULL pointer", fn);
     const int es = dtype_size(dtype);
-    if (es == 0) return fail(ENGRAM_ERR_DTYPE, "engram_gate_bwd: dtype %d", (int)dtype);
+    if (es == 0) return fail(ENGRAM_ERR_DTYPE, "%s: dtype %d", fn, (int)dtype);
     if (T < 0 || d <= 0 || P < 1)
-        return fail(ENGRAM_ERR_SHAPE, "engram_gate_bwd: T = %lld, d = %d, P = %d", (long long)T, d, P);
+        return fail(ENGRAM_ERR_SHAPE, "%s: T = %lld, d = %d, P = %d", fn, (long long)T, d, P);
     const int64_t row_bytes = static_cast<int64_t>(d) * es;
-    if (row_bytes % 16 != 0) return fail(ENGRAM_ERR_ALIGN, "engram_gate_bwd: row of %lld bytes", (long long)row_bytes);
+    if (row_bytes % 16 != 0) return fail(ENGRAM_ERR_ALIGN, "%s: row of %lld bytes", fn, (long long)row_bytes);
     if (row_bytes > ENGRAM_MAX_ROW_BYTES)
-        return fail(ENGRAM_ERR_SHAPE, "engram_gate_bwd: row of %lld bytes exceeds %d", (long long)row_bytes,
+        return fail(ENGRAM_ERR_SHAPE, "%s: row of %lld bytes exceeds %d", fn, (long long)row_bytes,
                     ENGRAM_MAX_ROW_BYTES);
     if (!aligned16(dout) || !aligned16(h) || !aligned16(k) || !aligned16(v) || !aligned16(w_fused) ||
         !aligned16(dh) || !aligned16(dk) || !aligned16(dv) || !aligned16(dw_partial))
-        return fail(ENGRAM_ERR_ALIGN, "engram_gate_bwd: tensor not 16-byte aligned");
+        return fail(ENGRAM_ERR_ALIGN, "%s: tensor not 16-byte aligned", fn);
     DeviceInfo dev;
     engram_status st = current_device(&dev);
     if (st != ENGRAM_OK) return st;
@@ -330,9 +343,30 @@ extern "C" engram_status engram_gate_bwd(const void *dout, const void *h, const 
     p.chunk = ceil_div(T, P);
     p.d = d;
     p.row_bytes = static_cast<uint32_t>(row_bytes);
+    p.accumulate = accumulate;
     p.scale = 1.0f / sqrtf(static_cast<float>(d));
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     return dtype == ENGRAM_F32 ? dispatch_bwd<float>(p, dev, s) : dispatch_bwd<__nv_bfloat16>(p, dev, s);
+}
+
+}  // namespace
+
+extern "C" engram_status engram_gate_bwd(const void *dout, const void *h, const void *k, const void *v,
+                                         engram_dtype dtype, const float *w_fused, const float *alpha,
+                                         const float *rstd_h, const float *rstd_k, const float *dot, int64_t T,
+                                         int32_t d, void *dh, void *dk, void *dv, float *dw_partial, int32_t P,
+                                         engram_stream_t stream) {
+    return gate_bwd_call("engram_gate_bwd", 0, dout, h, k, v, dtype, w_fused, alpha, rstd_h, rstd_k, dot, T, d, dh,
+                         dk, dv, dw_partial, P, stream);
+}
+
+extern "C" engram_status engram_gate_bwd_accumulate(const void *dout, const void *h, const void *k, const void *v,
+                                                    engram_dtype dtype, const float *w_fused, const float *alpha,
+                                                    const float *rstd_h, const float *rstd_k, const float *dot,
+                                                    int64_t T, int32_t d, void *dh, void *dk, void *dv,
+                                                    float *dw_partial, int32_t P, engram_stream_t stream) {
+    return gate_bwd_call("engram_gate_bwd_accumulate", 1, dout, h, k, v, dtype, w_fused, alpha, rstd_h, rstd_k, dot,
+                         T, d, dh, dk, dv, dw_partial, P, stream);
 }
 
 extern "C" engram_status engram_grad_w_reduce(const float *dw_partial, int32_t P, int32_t d, float *dweight_fused,

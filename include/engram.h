@@ -305,6 +305,23 @@ engram_status engram_gate_bwd(const void *dout, const void *h, const void *k, co
                               void *dh, void *dk, void *dv, float *dw_partial, int32_t P,
                               engram_stream_t stream);
 
+/*
+ * engram_gate_bwd for gradient accumulation over micro-batches (ch. 34 sec. 4.3-4.4: the
+ * partials feed one reduction, whose result accumulates like a main_grad buffer).  Arguments,
+ * layouts and checks are those of engram_gate_bwd; dh, dk, dv are written the same way, but each
+ * partial row is added to instead of overwritten:
+ *     dw_partial[p, i] = dw_partial[p, i] + c_t h_t,i k_t,i + ... over t in [p*C, min(T, (p+1)*C))
+ * in ascending token order, starting from the row's current value (a partial with no token keeps
+ * its row).  Calls in stream order on one [P, d] array, the first of them engram_gate_bwd, so
+ * give bitwise reproducible partials; one engram_grad_w_reduce over those P rows then reduces
+ * every micro-batch at once.  P must be the same in every call on the array.
+ */
+engram_status engram_gate_bwd_accumulate(const void *dout, const void *h, const void *k, const void *v,
+                                         engram_dtype dtype, const float *w_fused, const float *alpha,
+                                         const float *rstd_h, const float *rstd_k, const float *dot, int64_t T,
+                                         int32_t d, void *dh, void *dk, void *dv, float *dw_partial, int32_t P,
+                                         engram_stream_t stream);
+
 /* ------------------------------------------------------------------------- */
 /* B3: weight-gradient reduction  (ch. 34 sec. 4.3-4.4; determinism: the DSL article's
  *     "partitioned writes plus one ordered reduction instead of atomics")      */

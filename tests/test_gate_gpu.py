@@ -194,3 +194,59 @@ def test_grad_w_reduce_and_accumulate(P, d):
     # bitwise reproducible
     S2 = ecm.grad_w_reduce(part)
     assert torch.equal(S, S2)
+
+
+@pytest.mark.parametrize("P", [333, 6000])
+def test_backward_accumulates_partials_over_micro_batches(P):
+    """engram_gate_bwd then engram_gate_bwd_accumulate on one partial array: dh, dk, dv bitwise those of
+    the plain call; each partial equals the oracle's sum over its token range in both micro-batches;
+    partials with no token keep their rows; accumulating onto zeros is bitwise the plain call; and
+    the result does not depend on the grid."""
+    wa = W.GateWorkload(name="acc_a", T=5000, d=256, dtype="bf16", seed=21)
+    wb = W.GateWorkload(name="acc_b", T=5000, d=256, dtype="bf16", seed=22)
+    xa, xb = W.gate_host_inputs(wa), W.gate_host_inputs(wb)
+    xb["w_h"], xb["w_k"] = xa["w_h"], xa["w_k"]  # one set of weights across the micro-batches
+    ta, tb = (SD.gate_inputs_to_device(x, "bf16", DEV) for x in (xa, xb))
+    wf = ecm.fuse_weight(ta["w_h"], ta["w_k"])
+
+    def run(cap=0):
+        ecm.set_max_ctas(cap)
+        try:
+            part = torch.empty((P, 256), dtype=torch.float32, device=DEV)
+            outs = []
+            for i, t in enumerate((ta, tb)):
+                _, *st = ecm.gate_fwd(t["h"], t["k"], t["v"], wf, wa.eps)
+                outs.append(ecm.gate_bwd(t["dout"], t["h"], t["k"], t["v"], wf, *st, P=P, dw_partial=part,
+                                         accumulate=i > 0)[:3])
+            return part, outs
+        finally:
+            ecm.set_max_ctas(0)
+
+    part, outs = run()
+    # the accumulating call writes dh, dk, dv exactly as the plain call does
+    _, *st = ecm.gate_fwd(tb["h"], tb["k"], tb["v"], wf, wa.eps)
+    plain = ecm.gate_bwd(tb["dout"], tb["h"], tb["k"], tb["v"], wf, *st, P=P)
+    for got, ref in zip(outs[1], plain[:3]):
+        assert torch.equal(got, ref)
+    # onto zeros, the accumulating call is bitwise the plain call
+    z = torch.zeros((P, 256), dtype=torch.float32, device=DEV)
+    ecm.gate_bwd(tb["dout"], tb["h"], tb["k"], tb["v"], wf, *st, P=P, dw_partial=z, accumulate=True)
+    assert torch.equal(z, plain[3])
+    # each partial against the oracle over its token range in both micro-batches
+    chunk = -(-5000 // P)
+    got = H.as_f64(part)
+    for p in sorted({0, 1, P // 2, P - 1}):
+        t0, t1 = p * chunk, min(5000, (p + 1) * chunk)
+        if t0 >= 5000:
+            assert (part[p] == 0).all()  # written as zeros by the first call, kept by the second
+            continue
+        ref, mag = np.zeros(256), np.zeros(256)
+        for x in (xa, xb):
+            ob = oracle.gate_bwd(*(x[n][t0:t1] for n in ("dout", "h", "k", "v")), xa["w_h"], xa["w_k"], wa.eps)
+            ref += ob["dweight"]
+            mag += ob["dweight_abs"]
+        assert (np.abs(got[p] - ref) <= 1e-4 * mag + 1e-7).all(), f"partial {p}"
+    # grid independence, bitwise
+    for cap in (1, 7, 151):
+        part2, _ = run(cap)
+        assert torch.equal(part2, part), cap
