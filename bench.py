@@ -5,12 +5,12 @@ One step = one pass of the whole hot path over one batch of 16 sequences x 4096
 tokens (65,536 tokens):
   1. hash + gather of every token's 16 table rows (orders {2, 3} x 8 heads,
      ~2.0M-row prime tables, 64 bf16 per row, 4.1 GB resident) -> e [65536, 1024];
-  2. the weight fold w = w_h * w_k;
-  3. the context-aware gate, forward + backward on four micro-batches of
-     T = 16384 tokens at d = 4096 (bf16), the backwards adding into one array
-     of weight-gradient partials (the first writes it), then one ordered
-     reduction of those partials, accumulating into fp32 grad_w_h / grad_w_k
-     (11 kernel launches: the hash + gather is one).
+  2. the context-aware gate, forward + backward on four micro-batches of
+     T = 16384 tokens at d = 4096 (bf16), the first forward also forming the
+     weight fold w = w_h * w_k that the others use, the backwards adding into
+     one array of weight-gradient partials (the first writes it), then one
+     ordered reduction of those partials, accumulating into fp32 grad_w_h /
+     grad_w_k (10 kernel launches: the hash + gather is one).
 The reported value is tokens/s through the whole step (whole job, all ranks).
 Inputs are resident in HBM (the device-timed value) or copied from pinned host
 memory every step (the `e2e` value).  The per-step working set (4.1 GB table,
@@ -43,6 +43,7 @@ METRIC = "gate fwd+bwd tokens/s and HBM GB/s (% of roofline); hash-gather rows/s
 SEQS, SEQ_LEN = 16, 4096
 MICRO_T, D = 16384, 4096
 EPS = 1e-6
+STEP_LAUNCHES = 10
 WORKLOAD = (f"engram step: hash+gather {SEQS}x{SEQ_LEN} tokens (Zipf(1.1) ids over V=128000 -> V'=98560, "
             f"16 tables of ~2.0M x 64 bf16 = 4.1 GB) + weight fold + gate fwd/bwd/grad_w_reduce on "
             f"4 micro-batches T={MICRO_T} d={D} bf16")
@@ -170,7 +171,7 @@ def algorithmic_bytes(P: int):
     tables, row_bytes = 16, 128
     return {
         "hash_gather": T_all * (4 + 4 + 2 * tables * row_bytes),  # id, compressed id, 16 rows read + e_t written
-        "fuse_weight": 3 * 4 * D,
+        "gate_fwd_fold": MICRO_T * (8 * D + 16) + 3 * 4 * D,      # the forward + w_h, w_k read, w_fused written
         "gate_fwd": MICRO_T * (8 * D + 16),                       # h, k, v read, out written, 4 fp32 stats
         "gate_bwd": MICRO_T * (14 * D + 16) + P * D * 4,         # dout, v, h, k, stats read; dh, dk, dv, partials
         "gate_bwd_accumulate": MICRO_T * (14 * D + 16) + 2 * P * D * 4,  # the same + the partials read back
@@ -220,26 +221,36 @@ def make_workload(device):
     return wk
 
 
+def gate_forward(wk, i):
+    """Micro-batch i's forward; the first one also forms the weight fold the later calls use."""
+    import engram_conditional_memory_gb300 as ecm
+
+    m, st = wk["mb"][i], wk["stats"][i]
+    if i == 0:
+        ecm.gate_fwd_fold(m["h"], m["k"], m["v"], wk["w_h"], wk["w_k"], EPS, out=wk["out"][i], stats=st,
+                          w_fused_out=wk["w_fused"])
+    else:
+        ecm.gate_fwd(m["h"], m["k"], m["v"], wk["w_fused"], EPS, out=wk["out"][i], stats=st)
+
+
 def run_step(wk, mark=None):
-    """Launch one step (11 kernels) on the current stream; `mark(name)` is called after each call."""
+    """Launch one step (10 kernels) on the current stream; `mark(name)` is called after each call."""
     import engram_conditional_memory_gb300 as ecm
 
     hw = wk["hw"]
     ecm.hash_gather(wk["spec"], wk["ids"], wk["offs"], wk["table"], wk["cmap"], hw.vocab, hw.vocab_c,
                     out_rows=wk["rows"])
     mark and mark("hash_gather")
-    ecm.fuse_weight(wk["w_h"], wk["w_k"], out=wk["w_fused"])
-    mark and mark("fuse_weight")
     for i, m in enumerate(wk["mb"]):
         st = wk["stats"][i]
-        ecm.gate_fwd(m["h"], m["k"], m["v"], wk["w_fused"], EPS, out=wk["out"][i], stats=st)
-        mark and mark("gate_fwd")
+        gate_forward(wk, i)
+        mark and mark("gate_fwd_fold" if i == 0 else "gate_fwd")
         ecm.gate_bwd(m["dout"], m["h"], m["k"], m["v"], wk["w_fused"], *st, P=wk["P"], dh=wk["dh"][i],
                      dk=wk["dk"][i], dv=wk["dv"][i], dw_partial=wk["part"], accumulate=i > 0)
         mark and mark("gate_bwd_accumulate" if i else "gate_bwd")
     reduce_step(wk)
     mark and mark("grad_w_reduce")
-    return 11
+    return STEP_LAUNCHES
 
 
 def reduce_step(wk):
@@ -254,7 +265,7 @@ def reduce_step(wk):
 # ----------------------------------------------------------------------------- device timing
 
 def capture_step(wk, device):
-    """The step as one CUDA graph (11 kernel nodes).  The library's per-device set-up and each
+    """The step as one CUDA graph (10 kernel nodes).  The library's per-device set-up and each
     kernel's shared-memory attribute are done by an eager step first; device-pointer checks are
     off during capture (they were made by that eager step on the same buffers)."""
     import torch
@@ -297,7 +308,7 @@ def time_graph(graph, steps, warmup, device):
     torch.cuda.synchronize()
     wall1 = _dt.datetime.now()
     barrier(device)
-    return start.elapsed_time(end), 11 * steps, wall0, wall1
+    return start.elapsed_time(end), STEP_LAUNCHES * steps, wall0, wall1
 
 
 def time_device(wk, steps, warmup, device):
@@ -376,11 +387,10 @@ def time_e2e(wk, steps, warmup, device):
         ecm.hash_gather(wk["spec"], wk["ids"], wk["offs"], wk["table"], wk["cmap"], hw.vocab, hw.vocab_c,
                         out_rows=wk["rows"])
         hash_done.record(comp)
-        ecm.fuse_weight(wk["w_h"], wk["w_k"], out=wk["w_fused"])
         for i, m in enumerate(wk["mb"]):
             comp.wait_event(ready[i])
             st = wk["stats"][i]
-            ecm.gate_fwd(m["h"], m["k"], m["v"], wk["w_fused"], EPS, out=wk["out"][i], stats=st)
+            gate_forward(wk, i)
             ecm.gate_bwd(m["dout"], m["h"], m["k"], m["v"], wk["w_fused"], *st, P=wk["P"], dh=wk["dh"][i],
                          dk=wk["dk"][i], dv=wk["dv"][i], dw_partial=wk["part"], accumulate=i > 0)
             done[i].record(comp)
@@ -859,10 +869,9 @@ def main_offload(args, device):
     fetched = torch.cuda.Event()
 
     def gate_part():
-        ecm.fuse_weight(wk["w_h"], wk["w_k"], out=wk["w_fused"])
         for i, m in enumerate(wk["mb"]):
             st = wk["stats"][i]
-            ecm.gate_fwd(m["h"], m["k"], m["v"], wk["w_fused"], EPS, out=wk["out"][i], stats=st)
+            gate_forward(wk, i)
             ecm.gate_bwd(m["dout"], m["h"], m["k"], m["v"], wk["w_fused"], *st, P=wk["P"], dh=wk["dh"][i],
                          dk=wk["dk"][i], dv=wk["dv"][i], dw_partial=wk["part"], accumulate=i > 0)
         reduce_step(wk)
@@ -1004,7 +1013,7 @@ def main_native(args, rank, local, world):
         avg = sum(times) / len(times)
         gbs = ab[name] / (avg / 1e3) / 1e9
         ops[name] = {"avg_ms": avg, "launches": len(times), "bytes": ab[name], "GBps": gbs, "frac": gbs / peak}
-    step_bytes = (ab["hash_gather"] + ab["fuse_weight"] + 4 * ab["gate_fwd"] + ab["gate_bwd"]
+    step_bytes = (ab["hash_gather"] + ab["gate_fwd_fold"] + 3 * ab["gate_fwd"] + ab["gate_bwd"]
                   + 3 * ab["gate_bwd_accumulate"] + ab["grad_w_reduce"])
     dom = "gate_bwd_accumulate"  # three of the four backward launches
     roof = {"bound": "hbm", "kernel": dom, "achieved": ops[dom]["GBps"], "peak": peak, "unit": "GB/s",
@@ -1035,7 +1044,7 @@ def main_native(args, rank, local, world):
             "config": {"workload": WORKLOAD, "tokens_per_step": T_all, "global_batch": world * T_all,
                        "seq_len": SEQ_LEN, "parallelism": f"replicas x{world}",
                        "l2": "no flush: per-step working set 6.1 GB >> 129 MB L2",
-                       "timing": "value: CUDA-graph replays of the 11-launch step; ops/roofline: eager steps "
+                       "timing": "value: CUDA-graph replays of the 10-launch step; ops/roofline: eager steps "
                                  "with an event between launches; e2e: eager calls with host copies"},
             "hbm_gbs": step_bytes / (max_ms / args.steps / 1e3) / 1e9,
             "hash_gather_rows_per_s": 16 * T_all / (ops["hash_gather"]["avg_ms"] / 1e3),

@@ -79,6 +79,8 @@ def load_library():
             "engram_hash_gather_host": (st, [_p, _p, _p]),
             "engram_fuse_weight": (st, [_p, _p, _c.c_int, _p, _i32, _p]),
             "engram_gate_fwd": (st, [_p, _p, _p, _c.c_int, _p, _i64, _i32, _c.c_float, _p, _p, _p, _p, _p, _p]),
+            "engram_gate_fwd_fold": (st, [_p, _p, _p, _c.c_int, _p, _p, _c.c_int, _i64, _i32, _c.c_float, _p, _p, _p,
+                                          _p, _p, _p, _p]),
             "engram_gate_fwd_rms": (st, [_p, _p, _p, _c.c_int, _p, _i64, _i32, _c.c_float, _p, _p, _p, _p, _p, _p,
                                          _c.c_float, _p]),
             "engram_gate_bwd_num_partials": (st, [_i64, _i32, _p]),
@@ -203,6 +205,34 @@ def gate_fwd(h, k, v, w_fused, eps: float = 1e-6, out=None, save_for_backward: b
                                _ptr(out), _ptr(alpha), _ptr(rh), _ptr(rk), _ptr(dot), _stream(stream)),
            "engram_gate_fwd")
     return out, alpha, rh, rk, dot
+
+
+def gate_fwd_fold(h, k, v, w_h, w_k, eps: float = 1e-6, out=None, save_for_backward: bool = True, stats=None,
+                  w_fused_out=None, stream=None):
+    """gate_fwd with the weight fold w_h * w_k done inside the forward (one launch instead of fuse_weight +
+    gate_fwd); the fold is written to w_fused_out for the backward.
+    Returns (out, alpha, rstd_h, rstd_k, dot, w_fused)."""
+    lib = load_library()
+    _need(h, "h")
+    _need(k, "k", h.dtype)
+    _need(v, "v", h.dtype)
+    _need(w_h, "w_h")
+    _need(w_k, "w_k", w_h.dtype)
+    T, d = h.shape
+    out = torch.empty_like(v) if out is None else _need(out, "out", h.dtype)
+    if save_for_backward:
+        if stats is None:
+            stats = tuple(torch.empty(T, dtype=torch.float32, device=h.device) for _ in range(4))
+        alpha, rh, rk, dot = (_need(x, "stat", torch.float32) for x in stats)
+    else:
+        alpha = rh = rk = dot = None
+    w_fused_out = (torch.empty(d, dtype=torch.float32, device=h.device) if w_fused_out is None
+                   else _need(w_fused_out, "w_fused_out", torch.float32))
+    _check(lib.engram_gate_fwd_fold(_ptr(h), _ptr(k), _ptr(v), _DTYPES[h.dtype], _ptr(w_h), _ptr(w_k),
+                                    _DTYPES[w_h.dtype], T, d, float(eps), _ptr(out), _ptr(alpha), _ptr(rh), _ptr(rk),
+                                    _ptr(dot), _ptr(w_fused_out), _stream(stream)),
+           "engram_gate_fwd_fold")
+    return out, alpha, rh, rk, dot, w_fused_out
 
 
 def gate_fwd_rms(h, k, v, w_fused, eps: float = 1e-6, out_eps: float = 1e-6, out=None, save_for_backward: bool = True,

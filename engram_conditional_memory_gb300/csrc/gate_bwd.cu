@@ -39,7 +39,8 @@ struct GateBwdParams {
     float scale;  // 1/sqrt(d)
 };
 
-template <typename T, int NCW>
+// ACC: each partial row adds its tokens' terms onto the row's current contents (p.accumulate).
+template <typename T, int NCW, bool ACC>
 __global__ void __launch_bounds__((NCW + 1) * 32) gate_bwd_kernel(const __grid_constant__ GateBwdParams p) {
     pdl_wait();              // the previous kernel's writes are complete and visible
     using V = Vec<T>;
@@ -133,7 +134,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32) gate_bwd_kernel(const __grid_c
 #pragma unroll
             for (int e = 0; e < EV; e += 4) {
                 float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (p.accumulate && j < nvec) q = *reinterpret_cast<const float4 *>(prow + j * EV + e);
+                if (ACC && j < nvec) q = *reinterpret_cast<const float4 *>(prow + j * EV + e);
                 acc[m][e] = q.x;
                 acc[m][e + 1] = q.y;
                 acc[m][e + 2] = q.z;
@@ -252,7 +253,7 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 template <typename T, int NCW>
 engram_status launch_bwd(const GateBwdParams &p, const DeviceInfo &dev, cudaStream_t stream) {
-    const auto kern = gate_bwd_kernel<T, NCW>;
+    const auto kern = p.accumulate ? gate_bwd_kernel<T, NCW, true> : gate_bwd_kernel<T, NCW, false>;
     const PipelineShape shape = pick_bwd_pipeline(4 * static_cast<int>(p.row_bytes), NCW, dev.smem_optin);
     if (shape.stages == 0) return fail(ENGRAM_ERR_SHAPE, "engram_gate_bwd: row of %u bytes does not fit", p.row_bytes);
     engram_status st = set_smem(reinterpret_cast<const void *>(kern), shape.smem_bytes);

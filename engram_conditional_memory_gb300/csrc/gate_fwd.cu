@@ -15,6 +15,11 @@ namespace engram {
 struct GateFwdParams {
     const uint8_t *h, *k, *v;
     const float *w;
+    // fold: with w_h and w_k given (w unused), each thread forms its slice of w_h (*) w_k itself, as
+    // engram_fuse_weight rounds it, and CTA 0 writes the whole fold to w_out (nullable)
+    const void *w_h, *w_k;
+    float *w_out;
+    int32_t w_bf16;
     uint8_t *out;
     float *alpha, *rstd_h, *rstd_k, *dot;
     float *out_rstd;  // with RMS: 1/sqrt(mean(out_t^2) + out_eps) of each stored output row
@@ -100,7 +105,29 @@ __global__ void __launch_bounds__((NCW + 1) * 32) gate_fwd_kernel(const __grid_c
         if (j < nvec) {
 #pragma unroll
             for (int e = 0; e < EV; e += 4) {
-                const float4 q = __ldg(reinterpret_cast<const float4 *>(p.w + j * EV + e));
+                const int i = j * EV + e;
+                float4 q;
+                if (p.w_h == nullptr) {
+                    q = __ldg(reinterpret_cast<const float4 *>(p.w + i));
+                } else {
+                    float a[4], b[4];
+                    if (p.w_bf16) {
+                        const uint2 ua = __ldg(reinterpret_cast<const uint2 *>(static_cast<const __nv_bfloat16 *>(p.w_h) + i));
+                        const uint2 ub = __ldg(reinterpret_cast<const uint2 *>(static_cast<const __nv_bfloat16 *>(p.w_k) + i));
+                        a[0] = __uint_as_float(ua.x << 16), a[1] = __uint_as_float(ua.x & 0xffff0000u);
+                        a[2] = __uint_as_float(ua.y << 16), a[3] = __uint_as_float(ua.y & 0xffff0000u);
+                        b[0] = __uint_as_float(ub.x << 16), b[1] = __uint_as_float(ub.x & 0xffff0000u);
+                        b[2] = __uint_as_float(ub.y << 16), b[3] = __uint_as_float(ub.y & 0xffff0000u);
+                    } else {
+                        const float4 fa = __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(p.w_h) + i));
+                        const float4 fb = __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(p.w_k) + i));
+                        a[0] = fa.x, a[1] = fa.y, a[2] = fa.z, a[3] = fa.w;
+                        b[0] = fb.x, b[1] = fb.y, b[2] = fb.z, b[3] = fb.w;
+                    }
+                    q = make_float4(__fmul_rn(a[0], b[0]), __fmul_rn(a[1], b[1]), __fmul_rn(a[2], b[2]),
+                                    __fmul_rn(a[3], b[3]));
+                    if (p.w_out && blockIdx.x == 0) *reinterpret_cast<float4 *>(p.w_out + i) = q;
+                }
                 w[m][e] = q.x;
                 w[m][e + 1] = q.y;
                 w[m][e + 2] = q.z;
@@ -283,11 +310,21 @@ extern "C" engram_status engram_fuse_weight(const void *w_h, const void *w_k, en
 
 namespace {
 
+// The forward; with fold != nullptr (w_fused unused) the weights are fold->w_h and fold->w_k, multiplied in
+// the kernel, and the fold is written to fold->w_out.
+struct FoldArgs {
+    const void *w_h, *w_k;
+    engram_dtype w_dtype;
+    float *w_out;
+};
+
 engram_status gate_fwd_impl(const void *h, const void *k, const void *v, engram_dtype dtype, const float *w_fused,
                             int64_t T, int32_t d, float eps, void *out, float *alpha, float *rstd_h, float *rstd_k,
-                            float *dot, float *out_rstd, float out_eps, engram_stream_t stream) {
+                            float *dot, float *out_rstd, float out_eps, engram_stream_t stream,
+                            const FoldArgs *fold = nullptr) {
     // Per-token tensors may be NULL only when there is no token (an empty tensor has no storage).
-    if (!w_fused || (T > 0 && (!h || !k || !v || !out))) return fail(ENGRAM_ERR_NULL, "engram_gate_fwd: NULL pointer");
+    if ((!fold && !w_fused) || (T > 0 && (!h || !k || !v || !out)))
+        return fail(ENGRAM_ERR_NULL, "engram_gate_fwd: NULL pointer");
     const int es = dtype_size(dtype);
     if (es == 0) return fail(ENGRAM_ERR_DTYPE, "engram_gate_fwd: dtype %d", (int)dtype);
     if (T < 0 || d <= 0) return fail(ENGRAM_ERR_SHAPE, "engram_gate_fwd: T = %lld, d = %d", (long long)T, d);
@@ -301,6 +338,17 @@ engram_status gate_fwd_impl(const void *h, const void *k, const void *v, engram_
     DeviceInfo dev;
     engram_status st = current_device(&dev);
     if (st != ENGRAM_OK) return st;
+    if (fold) {
+        if (!aligned16(fold->w_h) || !aligned16(fold->w_k) || !aligned16(fold->w_out))
+            return fail(ENGRAM_ERR_ALIGN, "engram_gate_fwd_fold: weight not 16-byte aligned");
+        if ((st = check_device_ptr(fold->w_h, dev.device, "w_h")) ||
+            (st = check_device_ptr(fold->w_k, dev.device, "w_k")) ||
+            (st = check_device_ptr(fold->w_out, dev.device, "w_fused_out")))
+            return st;
+        if (T == 0)  // no token, so no forward to fold it in: the fold alone, for the backward
+            return fold->w_out ? engram_fuse_weight(fold->w_h, fold->w_k, fold->w_dtype, fold->w_out, d, stream)
+                               : ENGRAM_OK;
+    }
     if ((st = check_device_ptr(h, dev.device, "h")) || (st = check_device_ptr(k, dev.device, "k")) ||
         (st = check_device_ptr(v, dev.device, "v")) || (st = check_device_ptr(w_fused, dev.device, "w_fused")) ||
         (st = check_device_ptr(out, dev.device, "out")) || (st = check_device_ptr(alpha, dev.device, "alpha")) ||
@@ -328,6 +376,13 @@ engram_status gate_fwd_impl(const void *h, const void *k, const void *v, engram_
     p.row_bytes = static_cast<uint32_t>(row_bytes);
     p.eps = eps;
     p.scale = 1.0f / sqrtf(static_cast<float>(d));
+    if (fold) {
+        p.w = nullptr;
+        p.w_h = fold->w_h;
+        p.w_k = fold->w_k;
+        p.w_bf16 = fold->w_dtype == ENGRAM_BF16;
+        p.w_out = fold->w_out;
+    }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     return dtype == ENGRAM_F32 ? dispatch_fwd<float>(p, dev, s) : dispatch_fwd<__nv_bfloat16>(p, dev, s);
 }
@@ -348,4 +403,15 @@ extern "C" engram_status engram_gate_fwd_rms(const void *h, const void *k, const
     if (!out_rstd && T > 0) return fail(ENGRAM_ERR_NULL, "engram_gate_fwd_rms: NULL out_rstd");
     return gate_fwd_impl(h, k, v, dtype, w_fused, T, d, eps, out, alpha, rstd_h, rstd_k, dot, out_rstd, out_eps,
                          stream);
+}
+
+extern "C" engram_status engram_gate_fwd_fold(const void *h, const void *k, const void *v, engram_dtype dtype,
+                                              const void *w_h, const void *w_k, engram_dtype w_dtype, int64_t T,
+                                              int32_t d, float eps, void *out, float *alpha, float *rstd_h,
+                                              float *rstd_k, float *dot, float *w_fused_out, engram_stream_t stream) {
+    if (!w_h || !w_k) return fail(ENGRAM_ERR_NULL, "engram_gate_fwd_fold: NULL weight");
+    if (dtype_size(w_dtype) == 0) return fail(ENGRAM_ERR_DTYPE, "engram_gate_fwd_fold: weight dtype %d", (int)w_dtype);
+    const FoldArgs fold{w_h, w_k, w_dtype, w_fused_out};
+    return gate_fwd_impl(h, k, v, dtype, nullptr, T, d, eps, out, alpha, rstd_h, rstd_k, dot, nullptr, 0.f, stream,
+                         &fold);
 }

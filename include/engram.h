@@ -261,6 +261,19 @@ engram_status engram_gate_fwd(const void *h, const void *k, const void *v, engra
                               engram_stream_t stream);
 
 /*
+ * engram_gate_fwd with the fold of engram_fuse_weight done in the forward's weight preload (ch. 34
+ * sec. 3.1): w_h and w_k [d] in w_dtype (fp32 or bf16) replace w_fused, every CTA forms its slice
+ * of w_h (*) w_k in fp32 exactly as engram_fuse_weight rounds it, and w_fused_out [d] fp32
+ * (nullable) receives that fold for the backward.  Outputs are bitwise those of engram_fuse_weight
+ * followed by engram_gate_fwd; one launch instead of two, for the first forward after a weight
+ * update.  T = 0 writes only w_fused_out.  w_h, w_k, w_fused_out 16-byte aligned device memory.
+ */
+engram_status engram_gate_fwd_fold(const void *h, const void *k, const void *v, engram_dtype dtype,
+                                   const void *w_h, const void *w_k, engram_dtype w_dtype, int64_t T, int32_t d,
+                                   float eps, void *out, float *alpha, float *rstd_h, float *rstd_k, float *dot,
+                                   float *w_fused_out, engram_stream_t stream);
+
+/*
  * engram_gate_fwd, plus the RMS statistic of every output row as stored (after its rounding to
  * `dtype`), for the RMSNorm that reads the gate's output next (the short convolution, ch. 34
  * sec. 1.2 item 4):

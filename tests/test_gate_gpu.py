@@ -250,3 +250,20 @@ def test_backward_accumulates_partials_over_micro_batches(P):
     for cap in (1, 7, 151):
         part2, _ = run(cap)
         assert torch.equal(part2, part), cap
+
+
+@pytest.mark.parametrize("dtype,wdtype,d,T", [("bf16", "f32", 4096, 3001), ("bf16", "bf16", 2048, 700),
+                                              ("f32", "f32", 100, 257), ("bf16", "f32", 8192, 40),
+                                              ("bf16", "f32", 512, 0)])
+def test_forward_with_the_fold_inside_matches_fold_then_forward(dtype, wdtype, d, T):
+    """engram_gate_fwd_fold: every output, and the fold it writes for the backward, bitwise those of
+    engram_fuse_weight followed by engram_gate_fwd (an empty batch writes only the fold)."""
+    wl = W.GateWorkload(name="fold", T=T, d=d, dtype=dtype, seed=77 + d + T)
+    t = SD.gate_device_inputs(wl, DEV, with_dout=False)
+    w_h, w_k = (t[n] if wdtype == "f32" else t[n].bfloat16() for n in ("w_h", "w_k"))
+    wf = ecm.fuse_weight(w_h, w_k)
+    ref = ecm.gate_fwd(t["h"], t["k"], t["v"], wf, wl.eps)
+    got = ecm.gate_fwd_fold(t["h"], t["k"], t["v"], w_h, w_k, wl.eps)
+    assert torch.equal(got[5], wf)
+    for name, g_, r_ in zip(("out", "alpha", "rstd_h", "rstd_k", "dot"), got[:5], ref):
+        assert torch.equal(g_, r_), name
