@@ -152,10 +152,14 @@ def set_max_ctas(max_ctas: int) -> int:
     return load_library().engram_set_max_ctas(max_ctas)
 
 
-def set_hc_split(on: bool) -> bool:
-    """Force the multi-branch gate's branch-by-branch form at every size (a test knob); returns the
-    previous setting."""
-    return bool(load_library().engram_set_hc_split(1 if on else 0))
+HC_AUTO, HC_BRANCHES, HC_ROW_SPLIT, HC_ROW_SPLIT4 = 0, 1, 2, 4
+
+
+def set_hc_split(mode) -> int:
+    """The multi-branch gate's form (a test knob): HC_AUTO (0, each call picks), HC_BRANCHES (1 or True,
+    branch by branch at every size), HC_ROW_SPLIT / HC_ROW_SPLIT4 (2 / 4, each token shared by a cluster
+    of two / four CTAs where their parts fit); returns the previous mode."""
+    return int(load_library().engram_set_hc_split(int(mode)))
 
 
 def set_pdl(on: bool) -> bool:

@@ -117,31 +117,47 @@ __device__ __forceinline__ HcKv hc_kv(const uint8_t *kv, int64_t t, int64_t kv_s
 // landing and being read, so the CTA's one-token-at-a-time latency is hidden inside the SM.
 // Thread index gc within a group owns vectors jj = gc, gc + 32*NCW, ... (VPB of them) of every
 // branch row.  Groups synchronise on their own named barriers (ids 1..G).
-template <typename T, int HC, int NCW, int G, int VPB, bool STRIDED>
-__global__ void __launch_bounds__(G * NCW * 32, 1) gate_hc_fwd_kernel(const __grid_constant__ GateHcFwdParams p) {
+//
+// SPLIT = 2 or 4 (rows too large for a whole token in one CTA's shared memory): a cluster of SPLIT
+// CTAs shares each token, CTA `rank` holding bytes [rank * rb / SPLIT, (rank + 1) * rb / SPLIT) of
+// every row.  Each group sums its part of the token's 3 HC sums, sends the totals to the same group
+// of every other CTA (4-byte stores into their shared memory that complete on their mbarriers, one
+// slot per sender and token parity), and adds all parts in rank order; every CTA of the cluster then
+// holds the same statistics.  With SPLIT = 4 two CTAs share an SM (MINB), so one's wait for the
+// others' parts overlaps the other's work.
+template <typename T, int HC, int NCW, int G, int VPB, bool STRIDED, int SPLIT, int MINB = (SPLIT >= 4 ? 2 : 1)>
+__global__ void __launch_bounds__(G * NCW * 32, MINB) gate_hc_fwd_kernel(const __grid_constant__ GateHcFwdParams p) {
+    static_assert(SPLIT == 1 || ((SPLIT == 2 || SPLIT == 4) && !STRIDED), "the row split takes the natural layouts");
     using V = Vec<T>;
     constexpr int EV = V::N;
     constexpr int NC = NCW * 32;
     extern __shared__ __align__(128) uint8_t smem[];
 
     const uint32_t rb = p.row_bytes;
+    const uint32_t hb = rb / SPLIT;  // bytes of each row this CTA holds
+    const uint32_t rank = SPLIT > 1 ? cluster_ctarank() : 0u;
+    const uint32_t coff = rank * hb;
+    const int wcol = static_cast<int>(rank) * (p.d / SPLIT);
     // the token layout: the natural one at compile time, or the view's strides (STRIDED)
     const int64_t x_stride = STRIDED ? p.x_stride : static_cast<int64_t>(HC) * rb;
     const int64_t kv_stride = STRIDED ? p.kv_stride : static_cast<int64_t>(HC + 1) * rb;
     const uint32_t k_off = STRIDED ? p.k_off : 0u, v_off = STRIDED ? p.v_off : HC * rb;
     const int st_stride = STRIDED ? p.st_stride : HC;
-    const uint32_t stage = (2 * HC + 1) * rb;  // x [HC rows] then kv [HC + 1 rows]
+    const uint32_t stage = (2 * HC + 1) * hb;  // x [HC rows] then kv [HC + 1 rows]
     const int S = p.stages;
-    const int nvec = static_cast<int>(rb / 16);
+    const int nvec = static_cast<int>(hb / 16);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + static_cast<size_t>(S) * stage);
     uint32_t *issued_cnt = reinterpret_cast<uint32_t *>(full + S);  // per stage, for the final drain
     float *red = reinterpret_cast<float *>(full + 2 * S);           // [G][2][NCW][4 * HC]
+    float *xbuf = red + G * 2 * NCW * 4 * HC;             // [G][2][SPLIT][4 * HC] the other parts' totals
+    uint64_t *xbar = reinterpret_cast<uint64_t *>(xbuf + G * 2 * SPLIT * 4 * HC);  // [G][2]
 
     const int group = threadIdx.x / NC;
     const int gc = threadIdx.x - group * NC;
     const int gwarp = gc >> 5;
     const int lane = gc & 31;
-    const int64_t first = blockIdx.x, stride = gridDim.x;
+    const int64_t first = SPLIT > 1 ? cluster_index() : blockIdx.x;
+    const int64_t stride = SPLIT > 1 ? cluster_count() : gridDim.x;
     const int64_t n_my = first < p.T ? (p.T - 1 - first) / stride + 1 : 0;
     const uint64_t pol = l2_evict_first_policy();
     auto issue = [&](int64_t it) {
@@ -149,18 +165,29 @@ __global__ void __launch_bounds__(G * NCW * 32, 1) gate_hc_fwd_kernel(const __gr
         const int st = static_cast<int>(it % S);
         issued_cnt[st] += 1;
         const HcKv kv = hc_kv(p.kv, tok, kv_stride, k_off, v_off, HC * rb);
-        if (!STRIDED || kv.adjacent)
+        if (SPLIT > 1) {  // this CTA's half of each of the token's 2 HC + 1 rows
+            uint8_t *dst = smem + static_cast<size_t>(st) * stage;
+            mbar_arrive_expect_tx(&full[st], stage);
+            for (int r = 0; r < HC; ++r)
+                bulk_load(dst + r * hb, p.x + tok * x_stride + r * rb + coff, hb, &full[st], pol);
+            for (int r = 0; r < HC; ++r)
+                bulk_load(dst + (HC + r) * hb, kv.k + r * rb + coff, hb, &full[st], pol);
+            bulk_load(dst + 2 * HC * hb, kv.v + coff, hb, &full[st], pol);
+        } else if (!STRIDED || kv.adjacent) {
             hc_issue(smem + static_cast<size_t>(st) * stage, &full[st], stage, pol, p.x + tok * x_stride, HC * rb,
                      kv.k, (HC + 1) * rb, nullptr, 0);
-        else
+        } else {
             hc_issue(smem + static_cast<size_t>(st) * stage, &full[st], stage, pol, p.x + tok * x_stride, HC * rb,
                      kv.k, HC * rb, kv.v, rb);
+        }
     };
     if (threadIdx.x == 0) {
         for (int q = 0; q < S; ++q) {
             mbar_init(&full[q], 1);
             issued_cnt[q] = 0;
         }
+        if (SPLIT > 1)
+            for (int q = 0; q < 2 * G; ++q) mbar_init(&xbar[q], 1);
         mbar_init_fence();
         for (int64_t q = 0; q < S && q < n_my; ++q) issue(q);
     }
@@ -176,7 +203,8 @@ __global__ void __launch_bounds__(G * NCW * 32, 1) gate_hc_fwd_kernel(const __gr
             if (jj < nvec) {
 #pragma unroll
                 for (int e = 0; e < EV; e += 4) {
-                    const float4 q = __ldg(reinterpret_cast<const float4 *>(p.w + static_cast<size_t>(h) * p.d + jj * EV + e));
+                    const float4 q = __ldg(reinterpret_cast<const float4 *>(p.w + static_cast<size_t>(h) * p.d + wcol +
+                                                                         jj * EV + e));
                     w[h][m][e] = q.x;
                     w[h][m][e + 1] = q.y;
                     w[h][m][e + 2] = q.z;
@@ -185,7 +213,10 @@ __global__ void __launch_bounds__(G * NCW * 32, 1) gate_hc_fwd_kernel(const __gr
             }
         }
     const float inv_d = 1.0f / static_cast<float>(p.d);
-    __syncthreads();  // barriers initialised
+    if (SPLIT > 1)
+        cluster_barrier();  // both CTAs' barriers initialised before any store into the other's memory
+    else
+        __syncthreads();  // barriers initialised
 
     float *gred = red + static_cast<size_t>(group) * 2 * NCW * 4 * HC;
     int64_t li = 0;  // this group's iteration count
@@ -193,7 +224,7 @@ __global__ void __launch_bounds__(G * NCW * 32, 1) gate_hc_fwd_kernel(const __gr
         const int s = static_cast<int>(it % S);
         const bool ok = mbar_wait(&full[s], static_cast<uint32_t>((it / S) & 1));
         const uint8_t *st = smem + static_cast<size_t>(s) * stage;
-        const uint8_t *kst = st + HC * rb;
+        const uint8_t *kst = st + HC * hb;  // stage rows are hb apart
 
         float acc[HC][3];
 #pragma unroll
@@ -206,8 +237,8 @@ __global__ void __launch_bounds__(G * NCW * 32, 1) gate_hc_fwd_kernel(const __gr
                     const int jj = gc + m * NC;
                     if (jj < nvec) {
                         float xv[EV], kx[EV];
-                        V::unpack(*reinterpret_cast<const uint4 *>(st + h * rb + jj * 16), xv);
-                        V::unpack(*reinterpret_cast<const uint4 *>(kst + h * rb + jj * 16), kx);
+                        V::unpack(*reinterpret_cast<const uint4 *>(st + h * hb + jj * 16), xv);
+                        V::unpack(*reinterpret_cast<const uint4 *>(kst + h * hb + jj * 16), kx);
 #pragma unroll
                         for (int e = 0; e < EV; ++e) {
                             acc[h][0] = fmaf(xv[e], xv[e], acc[h][0]);
@@ -236,6 +267,25 @@ __global__ void __launch_bounds__(G * NCW * 32, 1) gate_hc_fwd_kernel(const __gr
 #pragma unroll
             for (int q = 0; q < NCW; ++q) tot += rbuf[q * HC * 4 + lane];
         }
+        bool xfail = false;
+        if (SPLIT > 1) {  // this part's totals to the other CTAs, then the parts' sum in rank order
+            float *xs = xbuf + (group * 2 + (li & 1)) * SPLIT * 4 * HC;
+            uint64_t *xb = xbar + group * 2 + (li & 1);
+            if (gc == 0) mbar_arrive_expect_tx(xb, (SPLIT - 1) * 4 * HC * 4);
+            if (gwarp == 0 && lane < 4 * HC)
+                for (uint32_t q = 1; q < SPLIT; ++q) {
+                    const uint32_t peer = (rank + q) % SPLIT;
+                    cluster_store_tx(cluster_map(smem_addr(xs + rank * 4 * HC + lane), peer), tot,
+                                     cluster_map(smem_addr(xb), peer));
+                }
+            xfail = !mbar_wait(xb, static_cast<uint32_t>((li >> 1) & 1));
+            if (lane < 4 * HC) {
+                float sum = 0.f;
+#pragma unroll
+                for (int r = 0; r < SPLIT; ++r) sum += r == static_cast<int>(rank) ? tot : xs[r * 4 * HC + lane];
+                tot = sum;
+            }
+        }
         float gate[HC], rx[HC], rk[HC], dt[HC];
 #pragma unroll
         for (int h = 0; h < HC; ++h) {
@@ -250,31 +300,39 @@ __global__ void __launch_bounds__(G * NCW * 32, 1) gate_hc_fwd_kernel(const __gr
 
         // out = x + gate * v (the value row is kv row HC)
         const int64_t tok = first + it * stride;
-        uint8_t *orow = p.out + tok * x_stride;
+        uint8_t *orow = p.out + tok * x_stride + coff;
 #pragma unroll
         for (int m = 0; m < VPB; ++m) {
             const int jj = gc + m * NC;
             if (jj < nvec) {
                 float vv[EV];
-                V::unpack(*reinterpret_cast<const uint4 *>(kst + HC * rb + jj * 16), vv);
+                V::unpack(*reinterpret_cast<const uint4 *>(kst + HC * hb + jj * 16), vv);
 #pragma unroll
                 for (int h = 0; h < HC; ++h) {
                     float xv[EV];
-                    V::unpack(*reinterpret_cast<const uint4 *>(st + h * rb + jj * 16), xv);
+                    V::unpack(*reinterpret_cast<const uint4 *>(st + h * hb + jj * 16), xv);
 #pragma unroll
                     for (int e = 0; e < EV; ++e) xv[e] = fmaf(gate[h], vv[e], xv[e]);
                     st_global_v4(orow + h * rb + jj * 16, V::pack(xv));
                 }
             }
         }
-        if (gc < HC) {
+        if (gc < HC && rank == 0) {
             const size_t o = static_cast<size_t>(tok) * st_stride + gc;
             if (p.gate) p.gate[o] = gate[gc];
             if (p.rstd_x) p.rstd_x[o] = rx[gc];
             if (p.rstd_k) p.rstd_k[o] = rk[gc];
             if (p.dot) p.dot[o] = dt[gc];
         }
-        named_sync(1 + group, NC);  // the whole group is done with stage s: refill it
+        // the whole group is done with stage s (refill it) and, split, agrees on whether the other half came
+        if (SPLIT > 1) {
+            if (named_sync_or(1 + group, NC, xfail)) {
+                if (gc == 0) report(p.status, nullptr, ENGRAM_DEVERR_TIMEOUT);
+                break;
+            }
+        } else {
+            named_sync(1 + group, NC);
+        }
         if (gc == 0 && it + S < n_my) issue(it + S);
     }
     // Never leave while a copy into this CTA's shared memory may be in flight: wait for the last
@@ -284,10 +342,15 @@ __global__ void __launch_bounds__(G * NCW * 32, 1) gate_hc_fwd_kernel(const __gr
         for (int q = 0; q < S; ++q)
             if (issued_cnt[q] > 0 && !mbar_wait(&full[q], (issued_cnt[q] - 1) & 1u))
                 report(p.status, nullptr, ENGRAM_DEVERR_TIMEOUT);
+    if (SPLIT > 1) cluster_barrier();  // no CTA leaves while the other may still store into it
 }
 
-template <typename T, int HC, int NCW, bool STRIDED>
-__global__ void __launch_bounds__(NCW * 32, 1) gate_hc_bwd_kernel(const __grid_constant__ GateHcBwdParams p) {
+// SPLIT = 2 or 4: a cluster of SPLIT CTAs shares each token as in the forward; the parts' dgate sums
+// are exchanged the same way.  dv, dx, dk and the weight-gradient partials are per column, so each
+// CTA writes its own part of them.
+template <typename T, int HC, int NCW, bool STRIDED, int SPLIT, int MINB = (SPLIT >= 4 ? 2 : 1)>
+__global__ void __launch_bounds__(NCW * 32, MINB) gate_hc_bwd_kernel(const __grid_constant__ GateHcBwdParams p) {
+    static_assert(SPLIT == 1 || ((SPLIT == 2 || SPLIT == 4) && !STRIDED), "the row split takes the natural layouts");
     using V = Vec<T>;
     constexpr int EV = V::N;
     constexpr int NC = NCW * 32;
@@ -295,6 +358,10 @@ __global__ void __launch_bounds__(NCW * 32, 1) gate_hc_bwd_kernel(const __grid_c
     extern __shared__ __align__(128) uint8_t smem[];
 
     const uint32_t rb = p.row_bytes;
+    const uint32_t hb = rb / SPLIT;  // bytes of each row this CTA holds
+    const uint32_t rank = SPLIT > 1 ? cluster_ctarank() : 0u;
+    const uint32_t coff = rank * hb;
+    const int wcol = static_cast<int>(rank) * (p.d / SPLIT);
     // the token layout: the natural one at compile time, or the view's strides (STRIDED)
     const int64_t x_stride = STRIDED ? p.x_stride : static_cast<int64_t>(HC) * rb;
     const int64_t kv_stride = STRIDED ? p.kv_stride : static_cast<int64_t>(HC + 1) * rb;
@@ -302,29 +369,41 @@ __global__ void __launch_bounds__(NCW * 32, 1) gate_hc_bwd_kernel(const __grid_c
     const uint32_t k_off = STRIDED ? p.k_off : 0u, v_off = STRIDED ? p.v_off : HC * rb;
     const int st_stride = STRIDED ? p.st_stride : HC;
     const bool write_dv = !STRIDED || p.write_dv;
-    const uint32_t stage = (3 * HC + 1) * rb;  // dout [HC], x [HC], kv [HC + 1]
+    const uint32_t stage = (3 * HC + 1) * hb;  // dout [HC], x [HC], kv [HC + 1]
     const int S = p.stages;
-    const int nvec = static_cast<int>(rb / 16);
+    const int nvec = static_cast<int>(hb / 16);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + static_cast<size_t>(S) * stage);
     float *red = reinterpret_cast<float *>(full + 2 * S);  // [2][NCW][4 * HC]
+    float *xbuf = red + 2 * NCW * 4 * HC;                    // [2][SPLIT][4 * HC] the other parts' dgate sums
+    uint64_t *xbar = reinterpret_cast<uint64_t *>(xbuf + 2 * SPLIT * 4 * HC);  // [2]
 
     const int c = threadIdx.x;
     const int warp = c >> 5;
     const int lane = c & 31;
-    // The CTA's tokens, in order: its partials b, b + G, ... each a chunk of C tokens (only the
-    // last partial of the whole pass can be shorter, and it is the last of its CTA).
-    const int64_t G = gridDim.x, C = p.chunk;
+    // The CTA's (cluster's) tokens, in order: its partials b, b + G, ... each a chunk of C tokens (only
+    // the last partial of the whole pass can be shorter, and it is the last of its CTA).
+    const int64_t G = SPLIT > 1 ? cluster_count() : gridDim.x, C = p.chunk;
+    const int64_t b0 = SPLIT > 1 ? cluster_index() : blockIdx.x;
     int64_t n_my = 0;
-    for (int64_t pp = blockIdx.x; pp < p.P; pp += G) {
+    for (int64_t pp = b0; pp < p.P; pp += G) {
         const int64_t t0 = pp * C;
         n_my += t0 >= p.T ? 0 : (t0 + C < p.T ? C : p.T - t0);
     }
     const uint64_t pol = l2_evict_first_policy();
-    auto token_of = [&](int64_t j) { return (blockIdx.x + (j / C) * G) * C + j % C; };
+    auto token_of = [&](int64_t j) { return (b0 + (j / C) * G) * C + j % C; };
     auto issue = [&](int64_t j) {
         const int64_t t = token_of(j);
         const HcKv kv = hc_kv(p.kv, t, kv_stride, k_off, v_off, HC * rb);
-        if (!STRIDED || kv.adjacent)
+        if (SPLIT > 1) {  // this CTA's half of each of the token's 3 HC + 1 rows
+            uint8_t *dst = smem + static_cast<size_t>(j % S) * stage;
+            uint64_t *bar = &full[j % S];
+            mbar_arrive_expect_tx(bar, stage);
+            for (int r = 0; r < HC; ++r) bulk_load(dst + r * hb, p.g + t * x_stride + r * rb + coff, hb, bar, pol);
+            for (int r = 0; r < HC; ++r)
+                bulk_load(dst + (HC + r) * hb, p.x + t * x_stride + r * rb + coff, hb, bar, pol);
+            for (int r = 0; r < HC; ++r) bulk_load(dst + (2 * HC + r) * hb, kv.k + r * rb + coff, hb, bar, pol);
+            bulk_load(dst + 3 * HC * hb, kv.v + coff, hb, bar, pol);
+        } else if (!STRIDED || kv.adjacent)
             hc_issue(smem + static_cast<size_t>(j % S) * stage, &full[j % S], stage, pol, p.g + t * x_stride,
                      HC * rb, p.x + t * x_stride, HC * rb, kv.k, (HC + 1) * rb);
         else
@@ -334,6 +413,7 @@ __global__ void __launch_bounds__(NCW * 32, 1) gate_hc_bwd_kernel(const __grid_c
     int64_t issued = 0;
     if (c == 0) {
         for (int q = 0; q < S; ++q) mbar_init(&full[q], 1);
+        if (SPLIT > 1) mbar_init(&xbar[0], 1), mbar_init(&xbar[1], 1);
         mbar_init_fence();
         for (; issued < S && issued < n_my; ++issued) issue(issued);
     }
@@ -349,7 +429,8 @@ __global__ void __launch_bounds__(NCW * 32, 1) gate_hc_bwd_kernel(const __grid_c
             if (jj < nvec) {
 #pragma unroll
                 for (int e = 0; e < EV; e += 4) {
-                    const float4 q = __ldg(reinterpret_cast<const float4 *>(p.w + static_cast<size_t>(h) * p.d + jj * EV + e));
+                    const float4 q = __ldg(reinterpret_cast<const float4 *>(p.w + static_cast<size_t>(h) * p.d + wcol +
+                                                                         jj * EV + e));
                     w[h][m][e] = q.x;
                     w[h][m][e + 1] = q.y;
                     w[h][m][e + 2] = q.z;
@@ -358,11 +439,14 @@ __global__ void __launch_bounds__(NCW * 32, 1) gate_hc_bwd_kernel(const __grid_c
             }
         }
     const float inv_d = 1.0f / static_cast<float>(p.d);
-    __syncthreads();  // barriers initialised
+    if (SPLIT > 1)
+        cluster_barrier();  // both CTAs' barriers initialised before any store into the other's memory
+    else
+        __syncthreads();  // barriers initialised
 
     int64_t it = 0;
     bool failed = false;
-    for (int64_t pp = blockIdx.x; pp < p.P && !failed; pp += G) {
+    for (int64_t pp = b0; pp < p.P && !failed; pp += G) {
         const int64_t t0 = pp * C;
         const int64_t t1 = t0 + C < p.T ? t0 + C : p.T;
         float acc[HC][VPB][EV];
@@ -386,8 +470,8 @@ __global__ void __launch_bounds__(NCW * 32, 1) gate_hc_bwd_kernel(const __grid_c
             }
             const bool ok = mbar_wait(&full[s], static_cast<uint32_t>((it / S) & 1));
             const uint8_t *gst = smem + static_cast<size_t>(s) * stage;
-            const uint8_t *xst = gst + HC * rb;
-            const uint8_t *kst = gst + 2 * HC * rb;
+            const uint8_t *xst = gst + HC * hb;  // stage rows are hb apart
+            const uint8_t *kst = gst + 2 * HC * hb;
 
             // pass 1: dgate_h partials, and dv = sum_h gate_h dout_h
             float dg[HC];
@@ -399,20 +483,20 @@ __global__ void __launch_bounds__(NCW * 32, 1) gate_hc_bwd_kernel(const __grid_c
                     const int jj = c + m * NC;
                     if (jj < nvec) {
                         float vv[EV], dv[EV];
-                        V::unpack(*reinterpret_cast<const uint4 *>(kst + HC * rb + jj * 16), vv);
+                        V::unpack(*reinterpret_cast<const uint4 *>(kst + HC * hb + jj * 16), vv);
 #pragma unroll
                         for (int e = 0; e < EV; ++e) dv[e] = 0.f;
 #pragma unroll
                         for (int h = 0; h < HC; ++h) {
                             float gv[EV];
-                            V::unpack(*reinterpret_cast<const uint4 *>(gst + h * rb + jj * 16), gv);
+                            V::unpack(*reinterpret_cast<const uint4 *>(gst + h * hb + jj * 16), gv);
 #pragma unroll
                             for (int e = 0; e < EV; ++e) {
                                 dg[h] = fmaf(gv[e], vv[e], dg[h]);
                                 dv[e] = fmaf(gt[h], gv[e], dv[e]);
                             }
                         }
-                        if (write_dv) st_global_v4(p.dkv + t * kv_stride + v_off + jj * 16, V::pack(dv));
+                        if (write_dv) st_global_v4(p.dkv + t * kv_stride + v_off + coff + jj * 16, V::pack(dv));
                     }
                 }
             }
@@ -432,6 +516,25 @@ __global__ void __launch_bounds__(NCW * 32, 1) gate_hc_bwd_kernel(const __grid_c
             if (lane < HC) {
 #pragma unroll
                 for (int q = 0; q < NCW; ++q) tot += rbuf[(q * HC + lane) * 4];
+            }
+            bool xfail = false;
+            if (SPLIT > 1) {  // this part's sums to the other CTAs, then the parts' sum in rank order
+                float *xs = xbuf + (it & 1) * SPLIT * 4 * HC;
+                uint64_t *xb = xbar + (it & 1);
+                if (c == 0) mbar_arrive_expect_tx(xb, (SPLIT - 1) * HC * 4);
+                if (warp == 0 && lane < HC)
+                    for (uint32_t q = 1; q < SPLIT; ++q) {
+                        const uint32_t peer = (rank + q) % SPLIT;
+                        cluster_store_tx(cluster_map(smem_addr(xs + rank * 4 * HC + lane), peer), tot,
+                                         cluster_map(smem_addr(xb), peer));
+                    }
+                xfail = !mbar_wait(xb, static_cast<uint32_t>((it >> 1) & 1));
+                if (lane < HC) {
+                    float sum = 0.f;
+#pragma unroll
+                    for (int r = 0; r < SPLIT; ++r) sum += r == static_cast<int>(rank) ? tot : xs[r * 4 * HC + lane];
+                    tot = sum;
+                }
             }
             float cc[HC], cx[HC], ck[HC];
 #pragma unroll
@@ -455,9 +558,9 @@ __global__ void __launch_bounds__(NCW * 32, 1) gate_hc_bwd_kernel(const __grid_c
                     const int jj = c + m * NC;
                     if (jj < nvec) {
                         float xv[EV], kx[EV], gv[EV], ox[EV], okk[EV];
-                        V::unpack(*reinterpret_cast<const uint4 *>(xst + h * rb + jj * 16), xv);
-                        V::unpack(*reinterpret_cast<const uint4 *>(kst + h * rb + jj * 16), kx);
-                        V::unpack(*reinterpret_cast<const uint4 *>(gst + h * rb + jj * 16), gv);
+                        V::unpack(*reinterpret_cast<const uint4 *>(xst + h * hb + jj * 16), xv);
+                        V::unpack(*reinterpret_cast<const uint4 *>(kst + h * hb + jj * 16), kx);
+                        V::unpack(*reinterpret_cast<const uint4 *>(gst + h * hb + jj * 16), gv);
 #pragma unroll
                         for (int e = 0; e < EV; ++e) {
                             const float cw = cc[h] * w[h][m][e];
@@ -465,16 +568,26 @@ __global__ void __launch_bounds__(NCW * 32, 1) gate_hc_bwd_kernel(const __grid_c
                             okk[e] = fmaf(cw, xv[e], -ck[h] * kx[e]);
                             acc[h][m][e] = fmaf(cc[h] * xv[e], kx[e], acc[h][m][e]);
                         }
-                        st_global_v4(p.dx + t * x_stride + h * rb + jj * 16, V::pack(ox));
-                        st_global_v4(p.dkv + t * kv_stride + k_off + h * rb + jj * 16, V::pack(okk));
+                        st_global_v4(p.dx + t * x_stride + h * rb + coff + jj * 16, V::pack(ox));
+                        st_global_v4(p.dkv + t * kv_stride + k_off + h * rb + coff + jj * 16, V::pack(okk));
                     }
                 }
-            __syncthreads();  // every thread is done with stage s: refill it
+            // every thread is done with stage s (refill it) and, split, agrees on whether the other half came
+            if (SPLIT > 1) {
+                if (__syncthreads_or(xfail)) {
+                    if (c == 0) report(p.status, nullptr, ENGRAM_DEVERR_TIMEOUT);
+                    failed = true;
+                    ++it;
+                    break;
+                }
+            } else {
+                __syncthreads();
+            }
             if (c == 0 && issued < n_my) issue(issued++);
         }
         if (failed) break;
 
-        float *prow = p.dw_partial + pp * part_stride;
+        float *prow = p.dw_partial + pp * part_stride + wcol;
 #pragma unroll
         for (int h = 0; h < HC; ++h)
 #pragma unroll
@@ -492,6 +605,7 @@ __global__ void __launch_bounds__(NCW * 32, 1) gate_hc_bwd_kernel(const __grid_c
         for (int64_t q = it; q < issued; ++q)
             if (!mbar_wait(&full[q % S], static_cast<uint32_t>((q / S) & 1)))
                 report(p.status, nullptr, ENGRAM_DEVERR_TIMEOUT);
+    if (SPLIT > 1) cluster_barrier();  // no CTA leaves while the other may still store into it
 }
 
 // dv_t = sum_h gate[t, h] dout_t,h for the per-branch form of the backward: the same fused
@@ -531,108 +645,213 @@ int hc_consumer_warps(int nvec) {
     return 0;
 }
 
+constexpr int kHcDevices = 64;
+
+// Shared memory of a CTA of either kernel: the ring, its mbarriers and cross-warp buffers, and with
+// the row split the other parts' totals ([groups][2][split][4 HC] floats) and their mbarriers
+// ([groups][2]).
+inline int hc_kernel_smem(int stages, int stage_bytes, int ncw, int hc, int groups, int split) {
+    return hc_smem_bytes(stages, stage_bytes, ncw, hc) + (split > 1 ? groups * 2 * (split * 4 * hc * 4 + 8) : 0);
+}
+
+// A kernel of the row split: launched in clusters of `split` CTAs (no dependent-launch attribute, like
+// the other multi-branch launches).
+template <typename Kern, typename Prm>
+cudaError_t hc_cluster_launch(Kern kern, int split, int64_t grid, int threads, int smem, cudaStream_t stream,
+                              const Prm &q) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(split);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, q);
+}
+
 // Forward launch: two groups of NCW warps, VPB = 2 * HcShape<HC>::kVpb vectors per branch row
 // (the forward keeps no gradient accumulators, so it can afford twice the weights per thread).
-template <typename T, int HC, int NCW, bool STRIDED>
+// With the row split the persistent grid is as many clusters as are resident at once.
+template <typename T, int HC, int NCW, bool STRIDED, int SPLIT>
 engram_status launch_hc_fwd(const GateHcFwdParams &p, const DeviceInfo &dev, cudaStream_t stream) {
     constexpr int G = 2;
     constexpr int NCWG = NCW / 2 > 0 ? NCW / 2 : 1;
-    const auto kern = gate_hc_fwd_kernel<T, HC, NCWG, G, 2 * HcShape<HC>::kVpb, STRIDED>;
-    // As many stages as fit (2..4): one stage is a whole token, and with a single CTA per SM the
-    // refill of a stage is issued only once the CTA is done with it, so depth must come from stages.
-    const int stage = (2 * HC + 1) * static_cast<int>(p.row_bytes);
+    const auto kern = gate_hc_fwd_kernel<T, HC, NCWG, G, 2 * HcShape<HC>::kVpb, STRIDED, SPLIT>;
+    // As many stages as fit (2..4): one stage is a whole token (or its part of every row), and with a
+    // single CTA per SM the refill of a stage is issued only once the CTA is done with it, so depth
+    // must come from stages.  With SPLIT = 4 two CTAs share an SM.
+    const int stage = (2 * HC + 1) * static_cast<int>(p.row_bytes / SPLIT);
+    const int per_cta = SPLIT >= 4 ? 113 * 1024 : 220 * 1024;
     int S = 4;
-    while (S > 2 && hc_smem_bytes(S, stage, NCW, HC) > 220 * 1024) --S;
-    const int smem = hc_smem_bytes(S, stage, NCW, HC);
+    while (S > 2 && hc_kernel_smem(S, stage, NCW, HC, G, SPLIT) > per_cta) --S;
+    const int smem = hc_kernel_smem(S, stage, NCW, HC, G, SPLIT);
     if (smem > dev.smem_optin)
         return fail(ENGRAM_ERR_SHAPE, "engram_gate_hc_fwd: a token of %d bytes does not fit twice in shared memory",
                     stage);
     engram_status st = set_smem(reinterpret_cast<const void *>(kern), smem);
     if (st != ENGRAM_OK) return st;
-    int b = 227 * 1024 / smem;
-    b = b < 1 ? 1 : (b > 4 ? 4 : b);
     GateHcFwdParams q = p;
     q.stages = S;
-    int64_t grid = static_cast<int64_t>(dev.num_sms) * b;
-    if (grid > p.T) grid = p.T;
-    grid = cap_grid(grid);
-    kern<<<static_cast<unsigned>(grid), G * NCWG * 32, smem, stream>>>(q);
+    if (SPLIT == 1) {
+        int b = 227 * 1024 / smem;
+        b = b < 1 ? 1 : (b > 4 ? 4 : b);
+        int64_t grid = static_cast<int64_t>(dev.num_sms) * b;
+        if (grid > p.T) grid = p.T;
+        grid = cap_grid(grid);
+        kern<<<static_cast<unsigned>(grid), G * NCWG * 32, smem, stream>>>(q);
+        return check_launch("engram_gate_hc_fwd");
+    }
+    static std::atomic<int> resident[kHcDevices];  // clusters resident at once, per device
+    std::atomic<int> &slot = resident[dev.device % kHcDevices];
+    int maxcl = slot.load(std::memory_order_relaxed);
+    if (maxcl <= 0) {
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = SPLIT;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(SPLIT);
+        cfg.blockDim = dim3(G * NCWG * 32);
+        cfg.dynamicSmemBytes = smem;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        const cudaError_t e = cudaOccupancyMaxActiveClusters(&maxcl, kern, &cfg);
+        if (e != cudaSuccess || maxcl < 1) {
+            cudaGetLastError();
+            return fail(ENGRAM_ERR_CUDA, "engram_gate_hc_fwd: no cluster of %d CTAs with %d bytes fits (%s)", SPLIT,
+                        smem, cudaGetErrorString(e));
+        }
+        slot.store(maxcl, std::memory_order_relaxed);
+    }
+    int64_t ncl = std::min<int64_t>(maxcl, p.T);
+    ncl = std::max<int64_t>(1, cap_grid(SPLIT * ncl) / SPLIT);
+    const cudaError_t e = hc_cluster_launch(kern, SPLIT, SPLIT * ncl, G * NCWG * 32, smem, stream, q);
+    if (e != cudaSuccess) return fail(ENGRAM_ERR_CUDA, "engram_gate_hc_fwd launch: %s", cudaGetErrorString(e));
     return check_launch("engram_gate_hc_fwd");
 }
 
-template <typename T, int HC, int NCW, bool STRIDED>
+// Backward launch: one CTA (one cluster, split) per partial, as in the single-branch backward.
+template <typename T, int HC, int NCW, bool STRIDED, int SPLIT>
 engram_status launch_hc_bwd(const GateHcBwdParams &p, const DeviceInfo &dev, cudaStream_t stream) {
-    const auto kern = gate_hc_bwd_kernel<T, HC, NCW, STRIDED>;
-    const int stage = (3 * HC + 1) * static_cast<int>(p.row_bytes);
+    const auto kern = gate_hc_bwd_kernel<T, HC, NCW, STRIDED, SPLIT>;
+    const int stage = (3 * HC + 1) * static_cast<int>(p.row_bytes / SPLIT);
+    const int per_cta = SPLIT >= 4 ? 113 * 1024 : dev.smem_optin;  // two CTAs per SM with SPLIT = 4
     int S = 3;
-    while (S >= 2 && hc_smem_bytes(S, stage, NCW, HC) > dev.smem_optin) --S;
+    while (S >= 2 && hc_kernel_smem(S, stage, NCW, HC, 1, SPLIT) > per_cta) --S;
     if (S < 2)
         return fail(ENGRAM_ERR_SHAPE, "engram_gate_hc_bwd: a token of %d bytes does not fit twice in shared memory",
                     stage);
-    const int smem = hc_smem_bytes(S, stage, NCW, HC);
+    const int smem = hc_kernel_smem(S, stage, NCW, HC, 1, SPLIT);
     engram_status st = set_smem(reinterpret_cast<const void *>(kern), smem);
     if (st != ENGRAM_OK) return st;
     GateHcBwdParams q = p;
     q.stages = S;
-    const int64_t grid = cap_grid(p.P);  // one CTA per partial, as in the single-branch backward
-    kern<<<static_cast<unsigned>(grid), NCW * 32, smem, stream>>>(q);
+    if (SPLIT == 1) {
+        const int64_t grid = cap_grid(p.P);
+        kern<<<static_cast<unsigned>(grid), NCW * 32, smem, stream>>>(q);
+        return check_launch("engram_gate_hc_bwd");
+    }
+    const int64_t ncl = std::max<int64_t>(1, cap_grid(SPLIT * static_cast<int64_t>(p.P)) / SPLIT);
+    const cudaError_t e = hc_cluster_launch(kern, SPLIT, SPLIT * ncl, NCW * 32, smem, stream, q);
+    if (e != cudaSuccess) return fail(ENGRAM_ERR_CUDA, "engram_gate_hc_bwd launch: %s", cudaGetErrorString(e));
     return check_launch("engram_gate_hc_bwd");
 }
 
-template <typename T, int HC, bool STRIDED = false>
+template <typename T, int HC, bool STRIDED = false, int SPLIT = 1>
 engram_status dispatch_hc_fwd(const GateHcFwdParams &p, const DeviceInfo &dev, cudaStream_t s) {
-    switch (hc_consumer_warps<HC>(static_cast<int>(p.row_bytes / 16))) {
-        case 2: return launch_hc_fwd<T, HC, 2, STRIDED>(p, dev, s);
-        case 4: return launch_hc_fwd<T, HC, 4, STRIDED>(p, dev, s);
-        case 8: return launch_hc_fwd<T, HC, 8, STRIDED>(p, dev, s);
-        case 16: return launch_hc_fwd<T, HC, 16, STRIDED>(p, dev, s);
+    switch (hc_consumer_warps<HC>(static_cast<int>(p.row_bytes / SPLIT / 16))) {
+        case 2: return launch_hc_fwd<T, HC, 2, STRIDED, SPLIT>(p, dev, s);
+        case 4: return launch_hc_fwd<T, HC, 4, STRIDED, SPLIT>(p, dev, s);
+        case 8: return launch_hc_fwd<T, HC, 8, STRIDED, SPLIT>(p, dev, s);
+        case 16: return launch_hc_fwd<T, HC, 16, STRIDED, SPLIT>(p, dev, s);
         default: return fail(ENGRAM_ERR_SHAPE, "engram_gate_hc_fwd: d = %d too large for %d branches", p.d, HC);
     }
 }
 
-template <typename T, int HC, bool STRIDED = false>
+template <typename T, int HC, bool STRIDED = false, int SPLIT = 1>
 engram_status dispatch_hc_bwd(const GateHcBwdParams &p, const DeviceInfo &dev, cudaStream_t s) {
-    switch (hc_consumer_warps<HC>(static_cast<int>(p.row_bytes / 16))) {
-        case 2: return launch_hc_bwd<T, HC, 2, STRIDED>(p, dev, s);
-        case 4: return launch_hc_bwd<T, HC, 4, STRIDED>(p, dev, s);
-        case 8: return launch_hc_bwd<T, HC, 8, STRIDED>(p, dev, s);
-        case 16: return launch_hc_bwd<T, HC, 16, STRIDED>(p, dev, s);
+    switch (hc_consumer_warps<HC>(static_cast<int>(p.row_bytes / SPLIT / 16))) {
+        case 2: return launch_hc_bwd<T, HC, 2, STRIDED, SPLIT>(p, dev, s);
+        case 4: return launch_hc_bwd<T, HC, 4, STRIDED, SPLIT>(p, dev, s);
+        case 8: return launch_hc_bwd<T, HC, 8, STRIDED, SPLIT>(p, dev, s);
+        case 16: return launch_hc_bwd<T, HC, 16, STRIDED, SPLIT>(p, dev, s);
         default: return fail(ENGRAM_ERR_SHAPE, "engram_gate_hc_bwd: d = %d too large for %d branches", p.d, HC);
     }
 }
 
-// Whether a whole token of HC branches fits the fused kernels: the consumer threads cover a row and
-// two token stages fit in shared memory.
+// Whether a token of HC branches (split = 1) or each CTA's part of every row (split = 2, 4) fits the
+// fused kernels: the consumer threads cover the row part and two stages fit in shared memory (in half
+// of it with split = 4, two CTAs per SM).
 template <int HC>
-bool hc_fwd_fits(int rb, int smem_optin) {
-    const int ncw = hc_consumer_warps<HC>(rb / 16);
-    return ncw > 0 && hc_smem_bytes(2, (2 * HC + 1) * rb, ncw, HC) <= smem_optin;
+bool hc_fwd_fits(int rb, int smem_optin, int split) {
+    if (rb % (16 * split) != 0) return false;
+    const int ncw = hc_consumer_warps<HC>(rb / split / 16);
+    const int cap = split >= 4 ? 113 * 1024 : smem_optin;
+    return ncw > 0 && hc_kernel_smem(2, (2 * HC + 1) * rb / split, ncw, HC, 2, split) <= cap;
 }
 template <int HC>
-bool hc_bwd_fits(int rb, int smem_optin) {
-    const int ncw = hc_consumer_warps<HC>(rb / 16);
-    return ncw > 0 && hc_smem_bytes(2, (3 * HC + 1) * rb, ncw, HC) <= smem_optin;
+bool hc_bwd_fits(int rb, int smem_optin, int split) {
+    if (rb % (16 * split) != 0) return false;
+    const int ncw = hc_consumer_warps<HC>(rb / split / 16);
+    const int cap = split >= 4 ? 113 * 1024 : smem_optin;
+    return ncw > 0 && hc_kernel_smem(2, (3 * HC + 1) * rb / split, ncw, HC, 1, split) <= cap;
 }
-bool hc_fits(int hc, bool fwd, int rb, int smem_optin) {
+bool hc_fits(int hc, bool fwd, int rb, int smem_optin, int split) {
     switch (hc) {
-        case 1: return fwd ? hc_fwd_fits<1>(rb, smem_optin) : hc_bwd_fits<1>(rb, smem_optin);
-        case 2: return fwd ? hc_fwd_fits<2>(rb, smem_optin) : hc_bwd_fits<2>(rb, smem_optin);
-        default: return fwd ? hc_fwd_fits<4>(rb, smem_optin) : hc_bwd_fits<4>(rb, smem_optin);
+        case 1: return fwd ? hc_fwd_fits<1>(rb, smem_optin, split) : hc_bwd_fits<1>(rb, smem_optin, split);
+        case 2: return fwd ? hc_fwd_fits<2>(rb, smem_optin, split) : hc_bwd_fits<2>(rb, smem_optin, split);
+        default: return fwd ? hc_fwd_fits<4>(rb, smem_optin, split) : hc_bwd_fits<4>(rb, smem_optin, split);
     }
 }
 
+// 0: each call picks its form; 1: branch by branch; 2 or 4: the row split over clusters of 2 or 4 CTAs
+// (where it fits).
 std::atomic<int> g_hc_split{0};
+
+enum HcForm { kHcWhole = 0, kHcBranches = 1, kHcSplit2 = 2, kHcSplit4 = 4 };
+
+// The form a call runs in: a whole token per CTA when it fits, else each token shared by a cluster of
+// CTAs when the parts fit (the value row and dout then still cross HBM once per token), else branch
+// by branch; engram_set_hc_split forces one of them.  Measured at T = 4096, hc = 4, d = 7168 bf16:
+// the forward 137 us on clusters of two against 139-141 on four; the backward, which has one group
+// of warps per CTA and so waits for the other parts with nothing else to do, 248 us on four (two
+// CTAs per SM) against 256 on two.
+HcForm hc_form(int hc, bool fwd, int rb, int smem_optin) {
+    const int force = g_hc_split.load(std::memory_order_relaxed);
+    if (force == 1) return kHcBranches;
+    if (force == 2 || force == 4)
+        return hc_fits(hc, fwd, rb, smem_optin, force) ? static_cast<HcForm>(force) : kHcBranches;
+    if (hc_fits(hc, fwd, rb, smem_optin, 1)) return kHcWhole;
+    const int first = fwd ? 2 : 4, second = fwd ? 4 : 2;
+    if (hc_fits(hc, fwd, rb, smem_optin, first)) return static_cast<HcForm>(first);
+    return hc_fits(hc, fwd, rb, smem_optin, second) ? static_cast<HcForm>(second) : kHcBranches;
+}
 
 // Per-branch form, for rows too large for a whole token of hc branches (or when forced): branch h
 // is a one-branch problem on strided views of x, kv, out and the statistics, with its row of the
 // fused weight; in the backward the value row's gradient sum_h gate_h dout_h is one more kernel.
 template <typename T>
 engram_status dispatch_hc_fwd_t(int hc, const GateHcFwdParams &p, const DeviceInfo &dev, cudaStream_t s) {
-    if (g_hc_split.load(std::memory_order_relaxed) == 0 && hc_fits(hc, true, p.row_bytes, dev.smem_optin)) {
+    const HcForm form = hc_form(hc, true, p.row_bytes, dev.smem_optin);
+    if (form == kHcWhole) {
         switch (hc) {
             case 1: return dispatch_hc_fwd<T, 1>(p, dev, s);
             case 2: return dispatch_hc_fwd<T, 2>(p, dev, s);
             default: return dispatch_hc_fwd<T, 4>(p, dev, s);
+        }
+    }
+    if (form == kHcSplit2 || form == kHcSplit4) {
+        const bool four = form == kHcSplit4;
+        switch (hc) {
+            case 1: return four ? dispatch_hc_fwd<T, 1, false, 4>(p, dev, s) : dispatch_hc_fwd<T, 1, false, 2>(p, dev, s);
+            case 2: return four ? dispatch_hc_fwd<T, 2, false, 4>(p, dev, s) : dispatch_hc_fwd<T, 2, false, 2>(p, dev, s);
+            default: return four ? dispatch_hc_fwd<T, 4, false, 4>(p, dev, s) : dispatch_hc_fwd<T, 4, false, 2>(p, dev, s);
         }
     }
     for (int h = 0; h < hc; ++h) {
@@ -653,11 +872,20 @@ engram_status dispatch_hc_fwd_t(int hc, const GateHcFwdParams &p, const DeviceIn
 
 template <typename T>
 engram_status dispatch_hc_bwd_t(int hc, const GateHcBwdParams &p, const DeviceInfo &dev, cudaStream_t s) {
-    if (g_hc_split.load(std::memory_order_relaxed) == 0 && hc_fits(hc, false, p.row_bytes, dev.smem_optin)) {
+    const HcForm form = hc_form(hc, false, p.row_bytes, dev.smem_optin);
+    if (form == kHcWhole) {
         switch (hc) {
             case 1: return dispatch_hc_bwd<T, 1>(p, dev, s);
             case 2: return dispatch_hc_bwd<T, 2>(p, dev, s);
             default: return dispatch_hc_bwd<T, 4>(p, dev, s);
+        }
+    }
+    if (form == kHcSplit2 || form == kHcSplit4) {
+        const bool four = form == kHcSplit4;
+        switch (hc) {
+            case 1: return four ? dispatch_hc_bwd<T, 1, false, 4>(p, dev, s) : dispatch_hc_bwd<T, 1, false, 2>(p, dev, s);
+            case 2: return four ? dispatch_hc_bwd<T, 2, false, 4>(p, dev, s) : dispatch_hc_bwd<T, 2, false, 2>(p, dev, s);
+            default: return four ? dispatch_hc_bwd<T, 4, false, 4>(p, dev, s) : dispatch_hc_bwd<T, 4, false, 2>(p, dev, s);
         }
     }
     // The value row's gradient reads dout; the branch kernels read the value row of kv.  So with
@@ -792,9 +1020,9 @@ extern "C" engram_status engram_gate_hc_bwd(const void *dout, const void *x, con
     DeviceInfo dev;
     if ((st = current_device(&dev)) != ENGRAM_OK) return st;
     if (T > 0 && dx == dout && dkv == kv &&
-        (g_hc_split.load(std::memory_order_relaxed) != 0 || !hc_fits(hc, false, row_bytes, dev.smem_optin)))
-        return fail(ENGRAM_ERR_SHAPE, "%s: dx over dout together with dkv over kv needs the whole-token form; "
-                    "rows of %lld bytes at hc = %d run branch by branch", fn, (long long)row_bytes, hc);
+        hc_form(hc, false, static_cast<int>(row_bytes), dev.smem_optin) == kHcBranches)
+        return fail(ENGRAM_ERR_SHAPE, "%s: dx over dout together with dkv over kv: rows of %lld bytes at hc = %d run "
+                    "branch by branch here, which serves only one of the two", fn, (long long)row_bytes, hc);
     const void *dp[] = {dout, x, kv, w_fused, gate, rstd_x, rstd_k, dot, dx, dkv, dw_partial};
     for (const void *q : dp)
         if ((st = check_device_ptr(q, dev.device, fn)) != ENGRAM_OK) return st;
@@ -829,4 +1057,6 @@ extern "C" engram_status engram_gate_hc_bwd(const void *dout, const void *x, con
     return dtype == ENGRAM_F32 ? dispatch_hc_bwd_t<float>(hc, p, dev, s) : dispatch_hc_bwd_t<__nv_bfloat16>(hc, p, dev, s);
 }
 
-extern "C" int32_t engram_set_hc_split(int32_t on) { return g_hc_split.exchange(on ? 1 : 0); }
+extern "C" int32_t engram_set_hc_split(int32_t on) {
+    return g_hc_split.exchange(on == 1 || on == 2 || on == 4 ? on : 0);
+}

@@ -129,11 +129,14 @@ int32_t engram_set_pdl(int32_t on);
 
 /*
  * The multi-branch gate (engram_gate_hc_fwd / _bwd) runs a whole token of hc branches in one
- * kernel when its rows fit twice in shared memory, and branch by branch on strided views (plus one
- * kernel for the shared value's gradient) when they do not.  on = 1 forces the branch-by-branch
- * form at every size, for testing; results agree with the oracle either way, though not bit for
- * bit with each other (the sums' thread layouts differ).  Returns the previous setting.
- * Process-wide.
+ * kernel when its rows fit twice in shared memory.  When they do not, a cluster of two CTAs (or
+ * four, two per SM) shares each token, each holding its part of every row and the CTAs exchanging
+ * their parts' sums through distributed shared memory (rows a multiple of 32 / 64 bytes).  Only
+ * when that does not fit either does it run branch by branch on strided views (plus one kernel for
+ * the shared value's gradient).  on = 1 forces the branch-by-branch form at every size, on = 2 / 4
+ * the cluster form over 2 / 4 CTAs wherever its parts fit, on = 0 (or any other value) restores the
+ * choice above; for testing: results agree with the oracle in every form, though not bit for bit
+ * with each other (the sums' thread layouts differ).  Returns the previous setting.  Process-wide.
  */
 int32_t engram_set_hc_split(int32_t on);
 
@@ -367,8 +370,9 @@ engram_status engram_grad_w_reduce(const float *dw_partial, int32_t P, int32_t d
  * writing) only when no statistic is saved: a backward needs the original x, so that
  * combination is refused (ENGRAM_ERR_SHAPE).  Rows up to ENGRAM_MAX_ROW_BYTES: a token whose
  * (2 hc + 1) rows fit twice in shared memory, with d at most 4096 bf16 / 2048 fp32 elements for
- * hc = 4 (twice / four times that for hc = 2 / 1), runs as one kernel; a larger one runs branch by
- * branch (engram_set_hc_split).
+ * hc = 4 (twice / four times that for hc = 2 / 1), runs in one CTA; a larger one (d = 7168 bf16
+ * at hc = 4, the release's width, among them) in a cluster of two CTAs that each hold half of
+ * every row (engram_set_hc_split).
  */
 engram_status engram_gate_hc_fwd(const void *x, const void *kv, engram_dtype dtype, const float *w_fused,
                                  int64_t T, int32_t hc, int32_t d, float eps, float clamp_value, void *out,
@@ -386,10 +390,10 @@ engram_status engram_gate_hc_fwd(const void *x, const void *kv, engram_dtype dty
  * partial p the sum of c_h x_h k_h over tokens [p*C, min(T, (p+1)*C)), C = ceil(T / P) --
  * reduce it with engram_grad_w_reduce over hc*d columns.
  * In-place writing: dx may be dout or x, and dkv may be kv (the same pointer, the same layout);
- * any other overlap between dx, dkv and the inputs is refused (ENGRAM_ERR_SHAPE).  Rows that run
- * branch by branch (see engram_gate_hc_fwd) take dx over dout or dkv over kv, but not both in one
+ * any other overlap between dx, dkv and the inputs is refused (ENGRAM_ERR_SHAPE).  The branch-by-
+ * branch form (see engram_set_hc_split) takes dx over dout or dkv over kv, but not both in one
  * call: the value row's gradient reads dout and the branch kernels read the value row, so that
- * pair is refused there (ENGRAM_ERR_SHAPE) and served only by the whole-token form.
+ * pair is refused there (ENGRAM_ERR_SHAPE) and served by the other two forms.
  */
 engram_status engram_gate_hc_bwd(const void *dout, const void *x, const void *kv, engram_dtype dtype,
                                  const float *w_fused, const float *gate, const float *rstd_x,

@@ -92,6 +92,7 @@ def test_newer_entry_points_reject_on_the_host(lib):
     k = lib.engram_set_hc_split
     k.restype, k.argtypes = i32, [i32]
     assert k(1) == 0 and k(0) == 1 and k(0) == 0
+    assert k(2) == 0 and k(4) == 2 and k(7) == 4 and k(0) == 0  # modes 0, 1, 2, 4; any other value is 0
 
 
 def test_partition_rule(lib):

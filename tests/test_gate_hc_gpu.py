@@ -106,9 +106,9 @@ def test_small_cases(dtype, hc, d, T):
 @pytest.mark.parametrize("dtype,hc,d,T", [("bf16", 4, 7168, 41), ("bf16", 4, 8192, 9), ("f32", 4, 3072, 17),
                                           ("f32", 2, 4096, 13)])
 def test_rows_too_large_for_a_whole_token(dtype, hc, d, T):
-    """Rows whose token does not fit twice in shared memory (d = 7168 at hc = 4, the largest rows,
-    fp32 past its whole-token limit) run branch by branch on strided views, plus the value row's
-    gradient in one more kernel: every output against the oracle."""
+    """Rows whose token does not fit twice in one CTA's shared memory (d = 7168 at hc = 4, the largest
+    rows, fp32 past its whole-token limit) run on clusters of two CTAs that each hold half of every
+    row and exchange their halves' sums: every output against the oracle."""
     wl = W.GateHcWorkload(name="t", T=T, hc=hc, d=d, dtype=dtype, seed=760 + hc * d + T)
     x = W.gate_hc_host_inputs(wl)
     r = _run(_dev(x), wl)
@@ -116,13 +116,30 @@ def test_rows_too_large_for_a_whole_token(dtype, hc, d, T):
     _check(r, x, wl)
 
 
+@pytest.mark.parametrize("dtype,hc,d,T", [("bf16", 4, 7168, 41), ("bf16", 4, 8192, 9)])
+def test_large_rows_in_clusters_of_four(dtype, hc, d, T):
+    """The row split over clusters of four CTAs (two per SM) forced at the large rows: every output
+    against the oracle."""
+    wl = W.GateHcWorkload(name="t4", T=T, hc=hc, d=d, dtype=dtype, seed=770 + hc * d + T)
+    x = W.gate_hc_host_inputs(wl)
+    prev = ecm.set_hc_split(ecm.HC_ROW_SPLIT4)
+    try:
+        r = _run(_dev(x), wl)
+        torch.cuda.synchronize()
+    finally:
+        ecm.set_hc_split(prev)
+    _check(r, x, wl)
+
+
 @pytest.mark.parametrize("dtype,hc,d,T", [("bf16", 4, 1024, 300), ("f32", 2, 96, 77), ("bf16", 4, 4096, 40)])
-def test_branch_by_branch_form_at_whole_token_sizes(dtype, hc, d, T):
-    """The branch-by-branch form forced where the whole-token kernels also run: both against the
-    oracle, and in-place writing (out = x) kept."""
+@pytest.mark.parametrize("mode", [ecm.HC_BRANCHES, ecm.HC_ROW_SPLIT, ecm.HC_ROW_SPLIT4],
+                         ids=["branch_by_branch", "row_split", "row_split4"])
+def test_other_forms_at_whole_token_sizes(dtype, hc, d, T, mode):
+    """The branch-by-branch form and the two-CTA row split forced where the whole-token kernels also
+    run: each against the oracle, and in-place writing (out = x) kept."""
     wl = W.GateHcWorkload(name="t", T=T, hc=hc, d=d, dtype=dtype, seed=780 + hc * d + T)
     x = W.gate_hc_host_inputs(wl)
-    prev = ecm.set_hc_split(True)
+    prev = ecm.set_hc_split(mode)
     try:
         t = _dev(x)
         r = _run(t, wl)
@@ -204,15 +221,17 @@ def test_empty_batch_and_bitwise_reruns():
         assert torch.equal(a[k], b[k]), k
 
 
-@pytest.mark.parametrize("split", [False, True], ids=["whole_token", "branch_by_branch"])
-def test_in_place_backward(split):
-    """dx written over dout, and dkv over kv, give bitwise the out-of-place results in both forms.
-    The pair together is served by the whole-token form and refused, before anything is written,
-    in the branch-by-branch form (the value row's gradient reads dout, the branch kernels read the
-    value row).  Other overlaps of an output with an input are refused."""
+@pytest.mark.parametrize("mode", [ecm.HC_AUTO, ecm.HC_BRANCHES, ecm.HC_ROW_SPLIT, ecm.HC_ROW_SPLIT4],
+                         ids=["whole_token", "branch_by_branch", "row_split", "row_split4"])
+def test_in_place_backward(mode):
+    """dx written over dout, and dkv over kv, give bitwise the out-of-place results in every form.
+    The pair together is served by the whole-token and row-split forms and refused, before anything
+    is written, in the branch-by-branch form (the value row's gradient reads dout, the branch
+    kernels read the value row).  Other overlaps of an output with an input are refused."""
     wl = W.GateHcWorkload(name="ipb", T=300, hc=4, d=1024, dtype="bf16", seed=43)
     t = _dev(W.gate_hc_host_inputs(wl))
-    prev = ecm.set_hc_split(split)
+    split = mode == ecm.HC_BRANCHES
+    prev = ecm.set_hc_split(mode)
     try:
         r = _run(t, wl)
         st = (r["gate"], r["rstd_x"], r["rstd_k"], r["dot"])
