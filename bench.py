@@ -12,6 +12,9 @@ tokens (65,536 tokens):
      ordered reduction of those partials, accumulating into fp32 grad_w_h /
      grad_w_k (10 kernel launches: the hash + gather is one).
 The reported value is tokens/s through the whole step (whole job, all ranks).
+The same line also carries the gate on its own workloads (`configs`: forward
+alone at T = 8192, d = 2048; fwd + bwd + reduce at d = 7168 for three token
+counts and a ragged pack) and the NEXT rows' kernels on theirs (`next_rows`).
 Inputs are resident in HBM (the device-timed value) or copied from pinned host
 memory every step (the `e2e` value).  The per-step working set (4.1 GB table,
 2 GB of gate inputs) is far larger than L2, so no flush is needed.
@@ -633,15 +636,19 @@ def time_gate_configs(device, steps: int, warmup: int, peak: float):
 
 # ----------------------------------------------------------------------------- single-op runs (profiling)
 
-def main_only(args, device):
-    """Time one kernel alone on its workload: the small cases the ncu captures are taken on."""
+def time_only(op: str, steps: int, warmup: int, device) -> dict:
+    """Time one kernel (or one fixed sequence of kernels) alone on its workload, as CUDA-graph replays
+    with an event between replays (eager where capture is refused): the NEXT rows' workloads and the
+    small cases the ncu captures are taken on."""
+    import types
+
     import torch
 
     import engram_conditional_memory_gb300 as ecm
     from synth import device as SD
     from synth import workloads as W
 
-    op = args.only
+    args = types.SimpleNamespace(only=op, steps=steps, warmup=warmup)
     stream = torch.cuda.current_stream()
     if op.startswith("hash_gather"):
         if op == "hash_gather_small":  # 4 x 4096 tokens, 16 tables of ~200k rows (0.41 GB, > L2)
@@ -844,10 +851,55 @@ def main_only(args, device):
     peak, kind = load_peaks()
     med = statistics.median(times)
     gbs = nbytes / (med / 1e3) / 1e9
-    print(json.dumps({"only": op, "median_ms": med, "min_ms": min(times), "eager_median_ms": statistics.median(eager),
-                      "timing": "graph" if graph_times else "eager", "bytes": nbytes, "GBps": gbs,
-                      "frac": gbs / peak, "peak": peak, "peak_kind": kind, "launches": args.steps}), flush=True)
+    return {"only": op, "median_ms": med, "min_ms": min(times), "eager_median_ms": statistics.median(eager),
+            "timing": "graph" if graph_times else "eager", "bytes": nbytes, "GBps": gbs, "frac": gbs / peak,
+            "peak": peak, "peak_kind": kind, "launches": args.steps}
+
+
+def main_only(args, device):
+    print(json.dumps(time_only(args.only, args.steps, args.warmup, device)), flush=True)
     return 0
+
+
+# The NEXT rows' own workloads, timed in the default run: the multi-branch gate (whole token at d = 4096,
+# clusters at d = 7168), the short convolution after the gate, the Engram Sinkhorn and the gather from a
+# host-resident table.  Whether consecutive launches find their inputs in L2: the reductions' (19-21 MB)
+# do, every other workload here is far larger than the 129 MB L2.
+NEXT_OPS = [
+    ("gate_hc_fwd", "hc=4 T=8192 d=4096 bf16, whole token per CTA", False),
+    ("gate_hc_bwd", "hc=4 T=8192 d=4096 bf16, whole token per CTA", False),
+    ("gate_hc_fwd_d7168", "hc=4 T=4096 d=7168 bf16, clusters of 2 CTAs", False),
+    ("gate_hc_bwd_d7168", "hc=4 T=4096 d=7168 bf16, clusters of 4 CTAs", False),
+    ("short_conv_fwd", "4x4096 tokens d=4096 bf16 width 4 dilation 3, rstd pass + sweep", False),
+    ("short_conv_fwd_given", "the same with rstd made by the gate (the sweep alone)", False),
+    ("gate_conv_fwd_fused", "gate_fwd_rms then short_conv_fwd_given, T=16384 d=4096", False),
+    ("short_conv_bwd", "4x4096 tokens d=4096 bf16, one pass on clusters of 8", False),
+    ("short_conv_reduce", "P=192 partials of (width+2) x 4096", True),
+    ("sinkhorn", "16384 x 5120 fp32: momentum + row step + reduce + finalize", False),
+    ("sinkhorn_momentum", "16384 x 5120, bf16 gradient, Nesterov", False),
+    ("sinkhorn_step", "16384 x 5120, P=1024", False),
+    ("sinkhorn_reduce", "P=1024 x 5120 + column step", True),
+    ("sinkhorn_finalize", "16384 x 5120", False),
+    ("hash_gather_host", "the 65,536-token gather from the 4.1 GB table in pinned host memory", False),
+]
+
+
+def time_next_rows(device, steps: int, warmup: int) -> dict:
+    import torch
+
+    out = {}
+    for op, what, l2_resident in NEXT_OPS:
+        r = time_only(op, steps, warmup, device)
+        out[op] = {"workload": what, "median_us": r["median_ms"] * 1e3, "bytes": r["bytes"], "GBps": r["GBps"],
+                   "frac": r["frac"], "timing": r["timing"], "launches": r["launches"],
+                   "inputs_in_l2_between_launches": l2_resident}
+        if op == "hash_gather_host":  # bound by the host link, not HBM: the rows cross it once
+            link = SEQS * SEQ_LEN * 16 * 128
+            out[op].update(bound="host link", link_bytes=link, link_GBps=link / (r["median_ms"] / 1e3) / 1e9,
+                           frac_note="frac is against the HBM peak; the rows cross the host link at link_GBps")
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return out
 
 
 # ----------------------------------------------------------------------------- table offload
@@ -928,6 +980,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end timing (profiling runs)")
     ap.add_argument("--cpu-steps", type=int, default=3, help="whole oracle steps timed for cpu_baseline")
     ap.add_argument("--no-configs", action="store_true", help="skip the gate-only workloads (profiling runs)")
+    ap.add_argument("--no-next", action="store_true", help="skip the NEXT rows' workloads (profiling runs)")
     ap.add_argument("--offload", action="store_true",
                     help="the step with the tables in host memory, prefetched on a side stream (vs in HBM)")
     ap.add_argument("--offload-ctas", type=int, default=32, help="CTAs of the host-table gather in --offload")
@@ -1026,6 +1079,7 @@ def main_native(args, rank, local, world):
         e2e = {"value": world * T_all * args.steps / (e_max / 1e3), "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
     configs = None if args.no_configs else time_gate_configs(device, args.steps, args.warmup, peak)
+    next_rows = None if args.no_next else time_next_rows(device, args.steps, args.warmup)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         table_host, mbs, w_h, w_k = oracle_inputs_from_device(wk)
@@ -1048,7 +1102,8 @@ def main_native(args, rank, local, world):
                                  "with an event between launches; e2e: eager calls with host copies"},
             "hbm_gbs": step_bytes / (max_ms / args.steps / 1e3) / 1e9,
             "hash_gather_rows_per_s": 16 * T_all / (ops["hash_gather"]["avg_ms"] / 1e3),
-            "roofline": roof, "ops": ops, "configs": configs, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+            "roofline": roof, "ops": ops, "configs": configs, "next_rows": next_rows, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": launches,
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
