@@ -454,7 +454,8 @@ def oracle_step(pool, threads, hw, table_host, mbs_host, w_h, w_k):
     t0 = time.perf_counter()
     list(pool.map(hash_part, _ranges(hw.T, 4 * threads)))
     oracle.fuse_weight(w_h, w_k)
-    work = [(m, b) for m in mbs_host for b in _ranges(MICRO_T, MICRO_T // ORACLE_GATE_CHUNK)]
+    work = [(m, b) for m in mbs_host
+            for b in _ranges(m["h"].shape[0], max(1, m["h"].shape[0] // ORACLE_GATE_CHUNK))]
     partials = np.stack(list(pool.map(gate_part, work)))
     oracle.grad_w_reduce(partials, w_h, w_k)
     return time.perf_counter() - t0

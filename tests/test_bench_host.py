@@ -64,3 +64,27 @@ def test_algorithmic_bytes_per_unit():
     assert ab["hash_gather"] == T_all * 4104          # 4 + 4 + 16 rows x 128 B read + written
     assert ab["gate_fwd"] == bench.MICRO_T * 32784    # 8d + 16 at d = 4096
     assert ab["gate_bwd"] == bench.MICRO_T * 57360 + 1024 * d * 4  # 14d + 16, plus the partial rows
+    assert ab["gate_bwd_accumulate"] == ab["gate_bwd"] + 1024 * d * 4  # the partial rows read back too
+    assert ab["gate_fwd_fold"] == ab["gate_fwd"] + 3 * 4 * d          # w_h, w_k read, the fold written
+    assert ab["grad_w_reduce"] == 1024 * d * 4 + 7 * d * 4           # one array of accumulated partials
+
+
+def test_oracle_step_runs_a_whole_step_on_a_small_workload():
+    """The oracle step both oracle timings run (the reference arm and cpu_baseline): hash + gather of
+    every token, the fold, gate fwd + bwd of every micro-batch, the ordered reduction -- here on the
+    tiny workloads, with more than one call per micro-batch and per hash range."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import numpy as np
+
+    from synth import workloads as W
+
+    hw = W.tiny_hash()
+    g = [W.gate_host_inputs(W.GateWorkload(name=f"mb{i}", T=600, d=64, dtype="bf16", seed=40 + i)) for i in range(2)]
+    mbs = [{n: x[n] for n in ("h", "k", "v", "dout")} for x in g]
+    table = hw.table_host.view(np.uint32).astype(np.uint16)  # any 16-bit table of the right shape
+    with ThreadPoolExecutor(3) as pool:
+        t = bench.oracle_step(pool, 3, hw, np.ascontiguousarray(table), mbs, g[0]["w_h"], g[0]["w_k"])
+    assert t > 0
+    times, threads = bench.time_oracle_steps(hw, np.ascontiguousarray(table), mbs, g[0]["w_h"], g[0]["w_k"], 2, 1)
+    assert len(times) == 2 and all(x > 0 for x in times) and threads >= 1

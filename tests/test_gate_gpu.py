@@ -123,8 +123,12 @@ def test_empty_batch_writes_nothing_and_zero_partials():
     out, a, rh, rk, dot = ecm.gate_fwd(h, h, h, wf)
     assert out.shape == (0, d)
     part = torch.full((3, d), 7.0, dtype=torch.float32, device=DEV)
+    ecm.gate_bwd(h, h, h, h, wf, a, rh, rk, dot, dw_partial=part, accumulate=True)
+    assert (part == 7.0).all()  # accumulating no token keeps every row
     ecm.gate_bwd(h, h, h, h, wf, a, rh, rk, dot, dw_partial=part)
     assert (part == 0).all()
+    with pytest.raises(ValueError):  # nothing to add to
+        ecm.gate_bwd(h, h, h, h, wf, a, rh, rk, dot, P=3, accumulate=True)
 
 
 def test_zero_key_gives_half_and_stats_are_optional():
