@@ -265,3 +265,17 @@ def test_in_place_backward(mode):
             bwd(t["dout"], t["kv"], dx=t["kv"].view(-1)[: 300 * 4 * 1024].view(300, 4, 1024))
     finally:
         ecm.set_hc_split(prev)
+
+
+@pytest.mark.parametrize("dtype,hc,d,T", [("bf16", 4, 4160, 37), ("bf16", 4, 6144, 3), ("f32", 4, 2080, 11),
+                                          ("bf16", 4, 4104, 5), ("bf16", 4, 7168, 1), ("bf16", 4, 4112, 19)])
+def test_forms_chosen_at_unusual_widths(dtype, hc, d, T):
+    """Widths between the forms' limits, each run in the form the library picks: d = 4160 and 6144 bf16
+    and 2080 fp32 on clusters of 2 (forward) and 4 (backward); d = 4112, whose quarter rows are not a
+    multiple of 16 bytes, on pairs in both directions; d = 4104, whose half rows are not either,
+    branch by branch; and a single token.  Every output against the oracle."""
+    wl = W.GateHcWorkload(name="u", T=T, hc=hc, d=d, dtype=dtype, seed=990 + d + T)
+    x = W.gate_hc_host_inputs(wl)
+    r = _run(_dev(x), wl)
+    torch.cuda.synchronize()
+    _check(r, x, wl)
