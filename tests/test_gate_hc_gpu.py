@@ -152,8 +152,12 @@ def test_other_forms_at_whole_token_sizes(dtype, hc, d, T, mode):
         ecm.set_hc_split(prev)
 
 
-def test_production_shape_every_element():
-    wl = W.gate_hc_4x4k()
+@pytest.mark.parametrize("wl", [W.gate_hc_4x4k(),
+                                W.GateHcWorkload(name="gate_hc4_T2048_d7168", T=2048, hc=4, d=7168, dtype="bf16",
+                                                 seed=6 * 101 + 31)], ids=lambda w: w.name)
+def test_production_shape_every_element(wl):
+    """The release's shape, hc = 4 at d = 4096 (whole token per CTA) and at its width d = 7168 (a token
+    shared by clusters of two CTAs forward and four backward): every element against the oracle."""
     x = W.gate_hc_host_inputs(wl)
     r = _run(_dev(x), wl)
     torch.cuda.synchronize()
