@@ -283,3 +283,24 @@ def test_forms_chosen_at_unusual_widths(dtype, hc, d, T):
     r = _run(_dev(x), wl)
     torch.cuda.synchronize()
     _check(r, x, wl)
+
+
+@pytest.mark.parametrize("mode", [ecm.HC_ROW_SPLIT, ecm.HC_ROW_SPLIT4], ids=["row_split", "row_split4"])
+def test_cluster_forms_bitwise_across_grids(mode):
+    """The cluster forms give bitwise the same outputs, statistics and partials whatever the grid:
+    capped at 1 CTA (one cluster walks every token and partial), at 7 and 151 CTAs, and uncapped."""
+    wl = W.GateHcWorkload(name="g", T=700, hc=4, d=2048, dtype="bf16", seed=55)
+    t = _dev(W.gate_hc_host_inputs(wl))
+    prev = ecm.set_hc_split(mode)
+    try:
+        base = _run(t, wl)
+        for cap in (1, 7, 151, 0):
+            ecm.set_max_ctas(cap)
+            try:
+                r = _run(t, wl)
+            finally:
+                ecm.set_max_ctas(0)
+            for k in ("out", "gate", "rstd_x", "rstd_k", "dot", "dx", "dkv", "part", "dw"):
+                assert torch.equal(r[k], base[k]), (cap, k)
+    finally:
+        ecm.set_hc_split(prev)
