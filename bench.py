@@ -1079,8 +1079,10 @@ def main_native(args, rank, local, world):
         e_max = aggregate_max(e_ms, device)
         e2e = {"value": world * T_all * args.steps / (e_max / 1e3), "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
-    configs = None if args.no_configs else time_gate_configs(device, args.steps, args.warmup, peak)
-    next_rows = None if args.no_next else time_next_rows(device, args.steps, args.warmup)
+    # per-GPU measurements of the gate's and the NEXT rows' own workloads: at N = 1 only (each replica
+    # would repeat them), after the timed step
+    configs = None if args.no_configs or world > 1 else time_gate_configs(device, args.steps, args.warmup, peak)
+    next_rows = None if args.no_next or world > 1 else time_next_rows(device, args.steps, args.warmup)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         table_host, mbs, w_h, w_k = oracle_inputs_from_device(wk)
