@@ -789,13 +789,15 @@ def time_only(op: str, steps: int, warmup: int, device) -> dict:
                 ecm.gate_fwd(t["h"], t["k"], t["v"], wf, EPS, out=vt, stats=st)
                 ecm.short_conv_fwd(vt, nw, cwt, offs, cw.dilation, h=h, bias=bias, eps=cw.eps, out=out, rstd=rstd)
     else:
-        wl = {"gate_fwd_2k": W.gate_fwd_2k()}.get(op, W.gate_train_4k())
+        # gate_fwd_2k: T=8192 d=2048; gate_fwd_7k / gate_bwd_7k: T=131072 d=7168; otherwise T=16384 d=4096
+        wl = {"gate_fwd_2k": W.gate_fwd_2k(), "gate_fwd_7k": W.gate_sweep_7k(131072),
+              "gate_bwd_7k": W.gate_sweep_7k(131072)}.get(op, W.gate_train_4k())
         t = SD.gate_device_inputs(wl, device)
         wf = ecm.fuse_weight(t["w_h"], t["w_k"])
         out, *st = ecm.gate_fwd(t["h"], t["k"], t["v"], wf, EPS)
         P = ecm.gate_bwd_num_partials(wl.T, wl.d)
         dh, dk, dv, part = ecm.gate_bwd(t["dout"], t["h"], t["k"], t["v"], wf, *st, P=P)
-        if op == "gate_bwd":
+        if op in ("gate_bwd", "gate_bwd_7k"):
             nbytes = wl.T * (14 * wl.d + 16) + P * wl.d * 4
 
             def launch():
@@ -812,7 +814,7 @@ def time_only(op: str, steps: int, warmup: int, device) -> dict:
 
             def launch():
                 ecm.grad_w_reduce(part, dweight_fused=wf, w_h=t["w_h"], w_k=t["w_k"], grad_w_h=gh, grad_w_k=gk)
-        else:  # gate_fwd on T=16384 d=4096, or gate_fwd_2k on T=8192 d=2048
+        else:  # gate_fwd on T=16384 d=4096, gate_fwd_2k on T=8192 d=2048, gate_fwd_7k on T=131072 d=7168
             nbytes = wl.T * (8 * wl.d + 16)
 
             def launch():
@@ -986,7 +988,8 @@ def main():
                     help="the step with the tables in host memory, prefetched on a side stream (vs in HBM)")
     ap.add_argument("--offload-ctas", type=int, default=32, help="CTAs of the host-table gather in --offload")
     ap.add_argument("--only", choices=["hash_gather", "hash_gather_small", "hash_gather_host", "gate_fwd",
-                                       "gate_fwd_2k", "gate_bwd", "gate_bwd_accumulate", "grad_w_reduce",
+                                       "gate_fwd_2k", "gate_fwd_7k", "gate_bwd", "gate_bwd_7k",
+                                       "gate_bwd_accumulate", "grad_w_reduce",
                                        "gate_hc_fwd", "gate_hc_bwd",
                                        "sinkhorn", "sinkhorn_momentum", "sinkhorn_step", "sinkhorn_reduce",
                                        "sinkhorn_finalize", "short_conv_fwd", "short_conv_fwd_given", "short_conv_bwd",
