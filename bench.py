@@ -1066,10 +1066,14 @@ def main_native(args, rank, local, world):
     peak, peak_kind = load_peaks()
     ab = algorithmic_bytes(wk["P"])
     ops = {}
+    tokens_per_launch = {"hash_gather": T_all, "gate_fwd_fold": MICRO_T, "gate_fwd": MICRO_T, "gate_bwd": MICRO_T,
+                         "gate_bwd_accumulate": MICRO_T}
     for name, times in per.items():
         avg = sum(times) / len(times)
         gbs = ab[name] / (avg / 1e3) / 1e9
         ops[name] = {"avg_ms": avg, "launches": len(times), "bytes": ab[name], "GBps": gbs, "frac": gbs / peak}
+        if name in tokens_per_launch:
+            ops[name]["tokens_per_s"] = tokens_per_launch[name] / (avg / 1e3)
     step_bytes = (ab["hash_gather"] + ab["gate_fwd_fold"] + 3 * ab["gate_fwd"] + ab["gate_bwd"]
                   + 3 * ab["gate_bwd_accumulate"] + ab["grad_w_reduce"])
     dom = "gate_bwd_accumulate"  # three of the four backward launches
