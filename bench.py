@@ -221,6 +221,7 @@ def make_workload(device):
     wk["dweight"] = torch.empty(D, dtype=torch.float32, device=device)
     wk["grad_w_h"] = torch.zeros(D, dtype=torch.float32, device=device)
     wk["grad_w_k"] = torch.zeros(D, dtype=torch.float32, device=device)
+    wk["num_sms"] = torch.cuda.get_device_properties(device).multi_processor_count
     return wk
 
 
@@ -236,14 +237,34 @@ def gate_forward(wk, i):
         ecm.gate_fwd(m["h"], m["k"], m["v"], wk["w_fused"], EPS, out=wk["out"][i], stats=st)
 
 
-def run_step(wk, mark=None):
-    """Launch one step (10 kernels) on the current stream; `mark(name)` is called after each call."""
+def run_step(wk, mark=None, gather_stream=None):
+    """Launch one step (10 kernels) on the current stream; `mark(name)` is called after each call.
+
+    With `gather_stream`, the hash + gather runs there, beside the gate work, with one CTA per SM (so
+    that each SM also holds the gate's CTAs), and the current stream waits for it at the end.  The
+    rows a token needs follow from its ids alone, so a pipelined step gathers while the gate work runs:
+    across steps that is the same throughput as gathering the next batch during this one's gate work.
+    The gather's latency-bound DRAM traffic (random 128-byte rows) then shares HBM with the gate's
+    streaming instead of running alone."""
+    import torch
+
     import engram_conditional_memory_gb300 as ecm
 
     hw = wk["hw"]
-    ecm.hash_gather(wk["spec"], wk["ids"], wk["offs"], wk["table"], wk["cmap"], hw.vocab, hw.vocab_c,
-                    out_rows=wk["rows"])
-    mark and mark("hash_gather")
+    main = torch.cuda.current_stream()
+    if gather_stream is not None:
+        gather_stream.wait_stream(main)
+        with torch.cuda.stream(gather_stream):
+            prev = ecm.set_max_ctas(wk["num_sms"])
+            try:
+                ecm.hash_gather(wk["spec"], wk["ids"], wk["offs"], wk["table"], wk["cmap"], hw.vocab, hw.vocab_c,
+                                out_rows=wk["rows"])
+            finally:
+                ecm.set_max_ctas(prev)
+    else:
+        ecm.hash_gather(wk["spec"], wk["ids"], wk["offs"], wk["table"], wk["cmap"], hw.vocab, hw.vocab_c,
+                        out_rows=wk["rows"])
+        mark and mark("hash_gather")
     for i, m in enumerate(wk["mb"]):
         st = wk["stats"][i]
         gate_forward(wk, i)
@@ -253,6 +274,8 @@ def run_step(wk, mark=None):
         mark and mark("gate_bwd_accumulate" if i else "gate_bwd")
     reduce_step(wk)
     mark and mark("grad_w_reduce")
+    if gather_stream is not None:
+        main.wait_stream(gather_stream)
     return STEP_LAUNCHES
 
 
@@ -268,24 +291,26 @@ def reduce_step(wk):
 # ----------------------------------------------------------------------------- device timing
 
 def capture_step(wk, device):
-    """The step as one CUDA graph (10 kernel nodes).  The library's per-device set-up and each
-    kernel's shared-memory attribute are done by an eager step first; device-pointer checks are
-    off during capture (they were made by that eager step on the same buffers)."""
+    """The step as one CUDA graph (10 kernel nodes, the hash + gather on a branch of its own beside
+    the gate work).  The library's per-device set-up and each kernel's shared-memory attribute are
+    done by an eager step first; device-pointer checks are off during capture (they were made by
+    that eager step on the same buffers)."""
     import torch
 
     import engram_conditional_memory_gb300 as ecm
 
     side = torch.cuda.Stream(device)
+    gather = torch.cuda.Stream(device)
     side.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(side):
-        run_step(wk)
+        run_step(wk, gather_stream=gather)
     torch.cuda.current_stream().wait_stream(side)
     torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()
     prev = ecm.set_validation(0)
     try:
         with torch.cuda.graph(graph):
-            run_step(wk)
+            run_step(wk, gather_stream=gather)
     finally:
         ecm.set_validation(prev)
     return graph
@@ -1108,7 +1133,8 @@ def main_native(args, rank, local, world):
             "config": {"workload": WORKLOAD, "tokens_per_step": T_all, "global_batch": world * T_all,
                        "seq_len": SEQ_LEN, "parallelism": f"replicas x{world}",
                        "l2": "no flush: per-step working set 6.1 GB >> 129 MB L2",
-                       "timing": "value: CUDA-graph replays of the 10-launch step; ops/roofline: eager steps "
+                       "timing": "value: CUDA-graph replays of the 10-launch step, the hash + gather on a branch "
+                                 "beside the gate work; ops/roofline: eager serial steps "
                                  "with an event between launches; e2e: eager calls with host copies"},
             "hbm_gbs": step_bytes / (max_ms / args.steps / 1e3) / 1e9,
             "hash_gather_rows_per_s": 16 * T_all / (ops["hash_gather"]["avg_ms"] / 1e3),
