@@ -353,18 +353,22 @@ static_assert(sizeof(ScProd) <= 128, "the producer state fits its shared-memory 
 // token's V~ and dout row segments (1-D bulk copies) and its rstd (a 4-byte asynchronous copy)
 // into a ring of stages, as far ahead as the ring allows, with a record of the position (row
 // offset, kind, slot, segment and item boundaries).  Each of the 128 consumer threads owns four
-// channels and sweeps the positions in order:
-//   u  = V~ rstd norm_w (the last three kept by age in registers),
-//   dc = dout SiLU'(conv),  conv = bias + sum_a w_a u[t - a dil]   (w_a: tap width - 1 - a),
-//   the tap and bias gradients of the chunk's outputs, and the du = sum_a w_a dc[t + a dil] still
-//   collecting contributions (three of them, by age).
-// When a token's du is complete its stage is read back for V~ and dout:
-//   y = dout + rstd norm_w du  (kept in shared memory),  dnorm_w += du V~ rstd,
-//   and the thread's part of the row dot s = sum_c norm_w du V~.
+// channels and sweeps the positions in order.  With the norm weight folded into the taps
+// (w'_a = w_a norm_w, w_a: tap width - 1 - a) and u' = V~ rstd (the last three kept by age in
+// registers):
+//   conv = bias + sum_a w'_a u'[t - a dil],  dc = dout SiLU'(conv),
+//   A_a += dc u'[t - a dil] and db += dc over the chunk's outputs, and the
+//   dn = norm_w du = sum_a w'_a dc[t + a dil] still collecting contributions (three, by age).
+// When a token's dn is complete its stage is read back for V~ and dout:
+//   y = dout + rstd dn  (kept in shared memory),  and the thread's part of the row dot
+//   s = sum_c norm_w du V~ = sum_c dn V~.
 // Every four tokens a reducer warp sums the CTA's parts of each row dot (thread order, then
 // lanes) and sends the sums to the other CTAs of the cluster (distributed shared memory,
-// completing on their mbarrier); a batch later, when the cluster's sums have arrived, every thread
-// adds them in rank order and writes dv = y - rstd^3 V~ s / d.  All waits are bounded.
+// completing on their mbarrier); a batch later, when the cluster's sums have arrived, every warp
+// adds them in a fixed pairwise order and writes dv = y - rstd^3 V~ s / d.  At a work item's end its partial
+// rows are norm_w A_a (tap width - 1 - a), db, and, for the norm weight, sum_i conv_w[i] A_(width-1-i):
+// over a sequence dL/dnorm_w = sum_t du u' = sum_a w_a sum_t dc[t] u'[t - a dil], so no per-token
+// accumulator and no norm weight are needed in the sweep.  All waits are bounded.
 // The chunks depend on T only and every sum has a fixed order, so results are bitwise reproducible.
 template <typename E>
 __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_constant__ ScBwdParams p) {
@@ -549,32 +553,35 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
         const bool active = tid * kScEV < ncols;
         const uint8_t *my_ring = ring + tid * EV::kBytes;  // this thread's channels in stage 0
         const int width = p.width, d = p.d;
-        // the thread's four channels as two pairs: [h] holds channels 2h and 2h + 1
-        float2 w[kScAges][2], nw[2], bias[2];
+        const int cth = c0 + tid * kScEV;                  // the thread's first channel
+        // the thread's four channels as two pairs: [h] holds channels 2h and 2h + 1; the taps carry
+        // the norm weight (w'_a = w_a norm_w, rounded once)
+        float2 w[kScAges][2], bias[2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            float v[2][2 + kScAges];
+            float v[2][1 + kScAges];
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
-                const int c = c0 + tid * kScEV + 2 * h + k;
+                const int c = cth + 2 * h + k;
                 const bool ok = active && c < d;
-                v[k][0] = ok ? __ldg(p.norm_w + c) : 0.f;
-                v[k][1] = ok && p.bias ? __ldg(p.bias + c) : 0.f;
+                const float nwc = ok ? __ldg(p.norm_w + c) : 0.f;
+                v[k][0] = ok && p.bias ? __ldg(p.bias + c) : 0.f;
 #pragma unroll
                 for (int a = 0; a < kScAges; ++a)
-                    v[k][2 + a] =
-                        ok && a < width ? __ldg(p.conv_w + static_cast<size_t>(c) * width + (width - 1 - a)) : 0.f;
+                    v[k][1 + a] = ok && a < width ? __fmul_rn(__ldg(p.conv_w + static_cast<size_t>(c) * width +
+                                                                    (width - 1 - a)),
+                                                              nwc)
+                                                  : 0.f;
             }
-            nw[h] = make_float2(v[0][0], v[1][0]);
-            bias[h] = make_float2(v[0][1], v[1][1]);
+            bias[h] = make_float2(v[0][0], v[1][0]);
 #pragma unroll
-            for (int a = 0; a < kScAges; ++a) w[a][h] = make_float2(v[0][2 + a], v[1][2 + a]);
+            for (int a = 0; a < kScAges; ++a) w[a][h] = make_float2(v[0][1 + a], v[1][1 + a]);
         }
         const float inv_d = 1.0f / static_cast<float>(d);
 
-        float2 U[4][2];                 // u by slot: position q's in slot q & 3
-        float2 P1[2], P2[2], P3[2];     // du collecting contributions, by age 1..3
-        float2 A[kScAges][2], db[2], dnw[2];
+        float2 U[4][2];                 // u' by slot: position q's in slot q & 3
+        float2 P1[2], P2[2], P3[2];     // dn collecting contributions, by age 1..3
+        float2 A[kScAges][2], db[2];
         bool pend1 = false, pend2 = false, pend3 = false;
         int st = 0;
         uint32_t ph = 0, gpos = 0;
@@ -619,20 +626,16 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
             __syncwarp();
             mbar_arrive_if(&empty[stage], lane == 0 && !failed);
         };
-        // a token `a` positions back has its du: its y, row-dot part and norm-weight gradient
-        auto complete = [&](int a, const float2 (&du)[2]) {
+        // a token `a` positions back has its dn: its y and row-dot part
+        auto complete = [&](int a, const float2 (&dn)[2]) {
             const int sa = back(a);
             const uint8_t *stg = my_ring + sa * SB;
-            float2 x[2], g[2], dn[2], y[2];
+            float2 x[2], g[2], y[2];
             EV::load2(stg, x);
             EV::load2(stg + half, g);
             const float2 ra = p2(meta[sa].rstd);
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                dn[h] = p2mul(nw[h], du[h]);
-                dnw[h] = p2fma(p2mul(du[h], x[h]), ra, dnw[h]);
-                y[h] = p2fma(ra, dn[h], g[h]);
-            }
+            for (int h = 0; h < 2; ++h) y[h] = p2fma(ra, dn[h], g[h]);
             // the thread's part of the row dot: (c0 + c2) + (c1 + c3) of the products
             const float2 pp = p2fma(dn[1], x[1], p2mul(dn[0], x[0]));
             const float part = pp.x + pp.y;
@@ -643,19 +646,26 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
             ++nfin;
         };
         // batch bf's dv rows once the cluster's row dots have arrived; its stages go back to the producer.
-        // Lane j works out token j's row dot (the ranks' sums in rank order) and scale; the tokens'
-        // rows are then independent of each other.
+        // Token j's row dot is the sum of the ranks' sums b_0 .. b_(C-1): lane 4k + j takes b_k (plus
+        // b_(k+8) for clusters above 8) and a butterfly over k adds them pairwise, so lane j holds
+        // ((b_0 + b_1) + (b_2 + b_3)) + ((b_4 + b_5) + (b_6 + b_7)); lane j then forms token j's scale.
+        // The tokens' rows are then independent of each other.
         auto finalize = [&](int bf, int n) {
             wait_warp(&boxbar[bf & 3], (bf >> 2) & 1);
             const float *bx = box + (bf & 3) * kBwMaxCluster * kBwBatch;
             const int *fs = fin_stage + (bf & 3) * kBwBatch;
+            static_assert(kBwBatch == 4 && kBwMaxCluster == 16, "32 lanes take 8 ranks x 4 tokens, twice");
+            const int kr = lane >> 2;
+            float s = kr < static_cast<int>(C) ? bx[lane] : 0.f;
+            if (kr + 8 < static_cast<int>(C)) s += bx[lane + 8 * kBwBatch];
+            s += __shfl_xor_sync(0xffffffffu, s, 4);
+            s += __shfl_xor_sync(0xffffffffu, s, 8);
+            s += __shfl_xor_sync(0xffffffffu, s, 16);
             float kk_l = 0.f;
             int sj_l = 0;
             long long tok_l = 0;
             if (lane < n) {
                 sj_l = fs[lane];
-                float s = 0.f;
-                for (int k = 0; k < static_cast<int>(C); ++k) s += bx[k * kBwBatch + lane];
                 const float r = meta[sj_l].rstd;
                 kk_l = r * r * r * s * inv_d;
                 tok_l = meta[sj_l].row;
@@ -727,7 +737,7 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
             float2 x[2];
             EV::load2(stg, x);
 #pragma unroll
-            for (int h = 0; h < 2; ++h) U[J][h] = p2mul(p2mul(x[h], rt), nw[h]);
+            for (int h = 0; h < 2; ++h) U[J][h] = p2mul(x[h], rt);
             if (!STEADY && kind == kScLead) {
                 release(st);
                 advance();
@@ -755,10 +765,10 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
                 }
             }
             if (STEADY || pend3) {
-                float2 du[2];
+                float2 dn[2];
 #pragma unroll
-                for (int h = 0; h < 2; ++h) du[h] = p2fma(w[3][h], dc[h], P3[h]);
-                complete(3, du);
+                for (int h = 0; h < 2; ++h) dn[h] = p2fma(w[3][h], dc[h], P3[h]);
+                complete(3, dn);
             }
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
@@ -773,21 +783,38 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
             advance();
         };
 
-        // a work item's weight-gradient partial row: the taps (by tap index), the bias, the norm weight
+        // a work item's weight-gradient partial rows: the taps (by tap index) norm_w A_a, the bias, and
+        // the norm weight sum_i conv_w[i] A_(width-1-i) (ascending i); the unfolded weights are read
+        // again here, once per item
         const int64_t ncl = sc_num_clusters();
         auto write_rows = [&](int64_t item, bool zero) {
             if (!active) return;
-            float *prow = p.partial + static_cast<size_t>(item) * (width + 2) * d + c0 + tid * kScEV;
+            float *prow = p.partial + static_cast<size_t>(item) * (width + 2) * d + cth;
+            float tap[kScAges][kScEV], dnw[kScEV];
+#pragma unroll
+            for (int k = 0; k < kScEV; ++k) {
+                const int c = cth + k;
+                const float nwc = __ldg(p.norm_w + c);
+                dnw[k] = 0.f;
+#pragma unroll
+                for (int a = kScAges - 1; a >= 0; --a) {
+                    const float Aa = (k & 1) ? A[a][k >> 1].y : A[a][k >> 1].x;
+                    tap[a][k] = __fmul_rn(nwc, Aa);
+                    if (a < width)
+                        dnw[k] = __fmaf_rn(__ldg(p.conv_w + static_cast<size_t>(c) * width + (width - 1 - a)), Aa,
+                                           dnw[k]);
+                }
+            }
+            const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int a = 0; a < kScAges; ++a)
                 if (a < width)
                     *reinterpret_cast<float4 *>(prow + static_cast<size_t>(width - 1 - a) * d) =
-                        zero ? make_float4(0.f, 0.f, 0.f, 0.f)
-                             : make_float4(A[a][0].x, A[a][0].y, A[a][1].x, A[a][1].y);
+                        zero ? z : make_float4(tap[a][0], tap[a][1], tap[a][2], tap[a][3]);
             *reinterpret_cast<float4 *>(prow + static_cast<size_t>(width) * d) =
-                zero ? make_float4(0.f, 0.f, 0.f, 0.f) : make_float4(db[0].x, db[0].y, db[1].x, db[1].y);
+                zero ? z : make_float4(db[0].x, db[0].y, db[1].x, db[1].y);
             *reinterpret_cast<float4 *>(prow + static_cast<size_t>(width + 1) * d) =
-                zero ? make_float4(0.f, 0.f, 0.f, 0.f) : make_float4(dnw[0].x, dnw[0].y, dnw[1].x, dnw[1].y);
+                zero ? z : make_float4(dnw[0], dnw[1], dnw[2], dnw[3]);
         };
         // rows of the item just finished (if any) and zeros for this cluster's items without tokens up to `next`
         int64_t cur_item = -1;
@@ -800,7 +827,7 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
             for (; it < next; it += ncl) write_rows(it, true);
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                db[h] = dnw[h] = make_float2(0.f, 0.f);
+                db[h] = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int a = 0; a < kScAges; ++a) A[a][h] = make_float2(0.f, 0.f);
             }

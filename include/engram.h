@@ -448,12 +448,16 @@ engram_status engram_short_conv_num_partials(int64_t T, int32_t dilation, int32_
  *     s[t]     = sum_c norm_w[c] du[t, c] V~[t, c],
  *     dv[t, c] = dout[t, c] + rstd norm_w[c] du[t, c] - rstd^3 V~[t, c] s[t] / d,
  * dv [T, d] in `dtype` (not aliasing v or dout) and dw_partial [P, width + 2, d] fp32 with
- * P = engram_short_conv_num_partials(T, dilation): row (chunk, class) holds, over that work item's
- * tokens, sum dc * u_tap for each tap i (rows 0..width-1), sum dc (row width) and
- * sum du * V~ * rstd (row width + 1), each token's terms in ascending time order.  Reduce it with
- * engram_short_conv_grad_reduce.  s sums, in this order: a thread's four channels as
+ * P = engram_short_conv_num_partials(T, dilation).  With u' = V~ rstd and A_i = the sum, over the
+ * outputs t of work item (chunk, class) in ascending time order, of dc[t] u'[t - (width-1-i) dilation]:
+ * row i (0..width-1) holds norm_w * A_i, row width the sum of dc, and row width + 1
+ * sum_i conv_w[c, i] A_i (ascending i; summed over a sequence that is sum_t du V~ rstd, the chain
+ * rule grouped the other way).  The convolution is recomputed with the norm weight folded into the
+ * taps (conv_w[c, i] * norm_w[c], rounded once) and du carried as norm_w du.  Reduce the partials
+ * with engram_short_conv_grad_reduce.  s sums, in this order: a thread's four channels as
  * (c0 + c2) + (c1 + c3), four threads in order, a 32-lane butterfly (one 512-channel block), then
- * the ceil(d / 512) blocks in ascending order.  One pass over dout and V~ on thread-block
+ * the C = ceil(d / 512) block sums b_k pairwise: b_k + b_(k+8) first when C > 8, then
+ * ((b_0 + b_1) + (b_2 + b_3)) + ((b_4 + b_5) + (b_6 + b_7)), absent blocks adding zero.  One pass over dout and V~ on thread-block
  * clusters of ceil(d / 512) CTAs; dout, v, dv and dw_partial 16-byte aligned.
  */
 engram_status engram_short_conv_bwd(const void *dout, const void *v, engram_dtype dtype, const float *norm_w,
