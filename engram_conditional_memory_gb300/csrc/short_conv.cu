@@ -189,6 +189,7 @@ constexpr int kBwLag = kScAges - 1;               // taps behind a token and rea
 constexpr int kBwBatch = 4;                       // tokens whose row dots are exchanged together
 constexpr int kBwPrefetch = 13;                   // stages the copies may run ahead
 constexpr int kBwStages = 2 * kBwBatch + kBwLag + kBwPrefetch;  // two batches in flight
+static_assert(kBwStages % 4 == 0, "a steady group's four stages are consecutive in the ring");
 enum ScKind { kScLead = 0, kScMain = 1, kScTail = 2 };
 
 struct ScBwdParams {
@@ -321,10 +322,11 @@ struct ScMeta {
     uint32_t flags;
 };
 constexpr uint32_t kFlKind = 3u;          // bits 0-1: kScLead, kScMain or kScTail
-constexpr int kFlSlotShift = 2;           // bits 2-3: slot (position in the segment mod 4)
+constexpr int kFlSlotShift = 2;           // bits 2-3: slot (the position's place in the stream mod 4)
 constexpr uint32_t kFlSegStart = 1u << 4;
 constexpr uint32_t kFlSegEnd = 1u << 5;
 constexpr uint32_t kFlGroup = 1u << 6;    // this and the next three positions form a steady group
+                                          // (backward: it starts at a stream position divisible by 4)
 constexpr uint32_t kFlItemStart = 1u << 7;
 constexpr uint32_t kFlDone = 1u << 8;     // no position: the cluster's items are done
 constexpr int kFlItemShift = 12;          // bits 12-31: the work item, at an item start
@@ -476,8 +478,11 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
                     const int ql = q + lane;
                     const int64_t tl = t + lane * dil;
                     const uint32_t kind = ql < nl ? kScLead : (ql < nl + nm ? kScMain : kScTail);
-                    const bool group = (ql & 3) == 0 && ql >= nl + kBwLag && ql + 4 <= nl + nm && ql + 4 < n;
-                    uint32_t fl = kind | (static_cast<uint32_t>(ql & 3) << kFlSlotShift);
+                    // slots and steady groups by the position's place in the stream: the ring has a
+                    // multiple of 4 stages, so a group's four stages are consecutive in it
+                    const uint32_t gp = issued + static_cast<uint32_t>(lane);
+                    const bool group = (gp & 3u) == 0 && ql >= nl + kBwLag && ql + 4 <= nl + nm && ql + 4 < n;
+                    uint32_t fl = kind | ((gp & 3u) << kFlSlotShift);
                     if (ql == 0) fl |= kFlSegStart;
                     if (ql == n - 1) fl |= kFlSegEnd;
                     if (group) fl |= kFlGroup;
@@ -584,7 +589,7 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
         float2 A[kScAges][2], db[2];
         bool pend1 = false, pend2 = false, pend3 = false;
         int st = 0;
-        uint32_t ph = 0, gpos = 0;
+        uint32_t ph = 0;
         int nfin = 0, nb = 0, prev_n = 0;  // tokens of the open batch, batches posted, tokens of the pending one
 
         // a wait of the whole warp: every lane takes the same view of a failure
@@ -618,7 +623,6 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
         };
         auto advance = [&]() {
             if (++st == S) st = 0, ph ^= 1u;
-            ++gpos;
         };
         auto back = [&](int a) { return st - a < 0 ? st - a + S : st - a; };
         // after a failure a warp arrives on no barrier and sends nothing: no phase can be overrun
@@ -626,9 +630,8 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
             __syncwarp();
             mbar_arrive_if(&empty[stage], lane == 0 && !failed);
         };
-        // a token `a` positions back has its dn: its y and row-dot part
-        auto complete = [&](int a, const float2 (&dn)[2]) {
-            const int sa = back(a);
+        // the token at stage sa has its dn: its y and row-dot part, token k of the open batch
+        auto complete_at = [&](int sa, int k, const float2 (&dn)[2]) {
             const uint8_t *stg = my_ring + sa * SB;
             float2 x[2], g[2], y[2];
             EV::load2(stg, x);
@@ -639,10 +642,14 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
             // the thread's part of the row dot: (c0 + c2) + (c1 + c3) of the products
             const float2 pp = p2fma(dn[1], x[1], p2mul(dn[0], x[0]));
             const float part = pp.x + pp.y;
-            const int slot = ((nb & 1) * kBwBatch + nfin) * kBwCons + tid;
+            const int slot = ((nb & 1) * kBwBatch + k) * kBwCons + tid;
             pbuf[slot] = active ? part : 0.f;
             ybuf[slot] = make_float4(y[0].x, y[0].y, y[1].x, y[1].y);
-            if (tid == 0) fin_stage[(nb & 3) * kBwBatch + nfin] = sa;
+            if (tid == 0) fin_stage[(nb & 3) * kBwBatch + k] = sa;
+        };
+        // a token `a` positions back has its dn
+        auto complete = [&](int a, const float2 (&dn)[2]) {
+            complete_at(back(a), nfin, dn);
             ++nfin;
         };
         // batch bf's dv rows once the cluster's row dots have arrived; its stages go back to the producer.
@@ -726,20 +733,21 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
             nfin = 0;
             ++nb;
         };
-        // one sweep position in slot J, its stage already waited for.  STEADY: a chunk token with three
-        // chunk tokens pending before it, so the one three back completes; otherwise `kind` and the
-        // pending flags decide.
-        auto step = [&](auto Jc, auto Sc, uint32_t kind) {
+        // one sweep position in slot J at stage sp, already waited for.  STEADY: position J of a steady
+        // group (stages st0 + J of a group starting at st0 = st), a chunk token with three chunk tokens
+        // pending before it, so the one three back (stage sa3) completes as token J of its batch; the
+        // group moves st on.  Otherwise `kind` and the pending flags decide, and the step moves st on.
+        auto step = [&](auto Jc, auto Sc, uint32_t kind, int sp, int sa3) {
             constexpr int J = decltype(Jc)::v;
             constexpr bool STEADY = decltype(Sc)::v != 0;
-            const uint8_t *stg = my_ring + st * SB;
-            const float2 rt = p2(meta[st].rstd);
+            const uint8_t *stg = my_ring + sp * SB;
+            const float2 rt = p2(meta[sp].rstd);
             float2 x[2];
             EV::load2(stg, x);
 #pragma unroll
             for (int h = 0; h < 2; ++h) U[J][h] = p2mul(x[h], rt);
             if (!STEADY && kind == kScLead) {
-                release(st);
+                release(sp);
                 advance();
                 return;
             }
@@ -768,7 +776,8 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
                 float2 dn[2];
 #pragma unroll
                 for (int h = 0; h < 2; ++h) dn[h] = p2fma(w[3][h], dc[h], P3[h]);
-                complete(3, dn);
+                if (STEADY) complete_at(sa3, J, dn);
+                else complete(3, dn);
             }
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
@@ -778,9 +787,9 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
             }
             if (!STEADY) {
                 pend3 = pend2, pend2 = pend1, pend1 = kind == kScMain;
-                if (kind == kScTail) release(st);
+                if (kind == kScTail) release(sp);
+                advance();
             }
-            advance();
         };
 
         // a work item's weight-gradient partial rows: the taps (by tap index) norm_w A_a, the bias, and
@@ -854,21 +863,28 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
             }
             if (fl & kFlGroup) {
                 if (nfin > 0) post();  // a steady group fills one batch of its own
-                // all four stages first, so that the four positions' loads and arithmetic may overlap
+                // all four stages first, so that the four positions' loads and arithmetic may overlap.
+                // The group starts at a stage divisible by 4, so its stages st0 .. st0 + 3 do not wrap;
+                // the tokens three back are at st0 - 3 .. st0 - 1 (wrapping when st0 = 0), then st0.
                 wait_stages(1, 4);
                 if (failed) break;
-                step(ScIdx<0>{}, ScIdx<1>{}, kScMain);
-                step(ScIdx<1>{}, ScIdx<1>{}, kScMain);
-                step(ScIdx<2>{}, ScIdx<1>{}, kScMain);
-                step(ScIdx<3>{}, ScIdx<1>{}, kScMain);
+                const int st0 = st;
+                const int bk = (st0 == 0 ? S : st0) - kBwLag;
+                step(ScIdx<0>{}, ScIdx<1>{}, kScMain, st0, bk);
+                step(ScIdx<1>{}, ScIdx<1>{}, kScMain, st0 + 1, bk + 1);
+                step(ScIdx<2>{}, ScIdx<1>{}, kScMain, st0 + 2, bk + 2);
+                step(ScIdx<3>{}, ScIdx<1>{}, kScMain, st0 + 3, st0);
+                nfin = kBwBatch;
+                st = st0 + 4;
+                if (st == S) st = 0, ph ^= 1u;
                 pend1 = pend2 = pend3 = true;
             } else {
                 const uint32_t kind = fl & kFlKind;
                 switch ((fl >> kFlSlotShift) & 3u) {
-                    case 0: step(ScIdx<0>{}, ScIdx<0>{}, kind); break;
-                    case 1: step(ScIdx<1>{}, ScIdx<0>{}, kind); break;
-                    case 2: step(ScIdx<2>{}, ScIdx<0>{}, kind); break;
-                    default: step(ScIdx<3>{}, ScIdx<0>{}, kind); break;
+                    case 0: step(ScIdx<0>{}, ScIdx<0>{}, kind, st, 0); break;
+                    case 1: step(ScIdx<1>{}, ScIdx<0>{}, kind, st, 0); break;
+                    case 2: step(ScIdx<2>{}, ScIdx<0>{}, kind, st, 0); break;
+                    default: step(ScIdx<3>{}, ScIdx<0>{}, kind, st, 0); break;
                 }
             }
             if (nfin == kBwBatch) post();
