@@ -715,16 +715,36 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
                 __syncwarp();
                 const float *pb = pbuf + (b & 1) * kBwBatch * kBwCons;
                 const uint32_t box_lo = smem_addr(box), bar_lo = smem_addr(boxbar);
-                for (int j = 0; j < nfin; ++j) {
-                    static_assert(kBwCons == 32 * 4, "a lane sums four threads' parts");
+                static_assert(kBwCons == 32 * 4 && kBwBatch == 4, "a lane sums four threads' parts of four tokens");
+                // each lane's four threads' parts of each token, in thread order (the slots of tokens
+                // past nfin hold older parts and are not used)
+                float v[kBwBatch];
+#pragma unroll
+                for (int j = 0; j < kBwBatch; ++j) {
                     const float4 u0 = *reinterpret_cast<const float4 *>(pb + j * kBwCons + lane * 4);
-                    float v = ((u0.x + u0.y) + u0.z) + u0.w;
-                    v = warp_sum(v);
-                    const int slot = ((b & 3) * kBwMaxCluster + static_cast<int>(rank)) * kBwBatch + j;
-                    if (lane == 0) box[slot] = v;
-                    if (lane < static_cast<int>(C) && lane != static_cast<int>(rank) && !failed)
-                        sc_st_async(sc_mapa(box_lo + slot * 4, lane), v, sc_mapa(bar_lo + (b & 3) * 8, lane));
+                    v[j] = ((u0.x + u0.y) + u0.z) + u0.w;
                 }
+                // the four tokens' butterflies at once, pairing lanes 16, 8, 4, 2, 1 apart as a
+                // single token's would: each lane passes on the tokens it does not keep, and after
+                // the first two steps lanes 8t .. 8t + 7 carry token t
+                const bool hi = (lane & 16) != 0, b3 = (lane & 8) != 0;
+                float s0 = hi ? v[2] : v[0], s1 = hi ? v[3] : v[1];
+                s0 += __shfl_xor_sync(0xffffffffu, hi ? v[0] : v[2], 16);
+                s1 += __shfl_xor_sync(0xffffffffu, hi ? v[1] : v[3], 16);
+                float sum = b3 ? s1 : s0;
+                sum += __shfl_xor_sync(0xffffffffu, b3 ? s0 : s1, 8);
+                sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+                sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+                sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+                // lane 8t + q gives token t's sum to ranks q and q + 8: its own slot, or a peer's
+                const int tk = lane >> 3;
+                const int slot = ((b & 3) * kBwMaxCluster + static_cast<int>(rank)) * kBwBatch + tk;
+                if (tk < nfin)
+                    for (int r = lane & 7; r < static_cast<int>(C); r += 8) {
+                        if (r == static_cast<int>(rank)) box[slot] = sum;
+                        else if (!failed)
+                            sc_st_async(sc_mapa(box_lo + slot * 4, r), sum, sc_mapa(bar_lo + (b & 3) * 8, r));
+                    }
                 __syncwarp();
                 if (lane == 0 && !failed) mbar_arrive_expect_tx(&boxbar[b & 3], (C - 1) * nfin * 4);
             }
