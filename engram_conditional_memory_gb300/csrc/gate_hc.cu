@@ -446,6 +446,7 @@ __global__ void __launch_bounds__(NCW * 32, MINB) gate_hc_bwd_kernel(const __gri
 
     int64_t it = 0;
     bool failed = false;
+    bool xfail = false;  // the last token's exchange gave up (agreed at the next barrier)
     for (int64_t pp = b0; pp < p.P && !failed; pp += G) {
         const int64_t t0 = pp * C;
         const int64_t t1 = t0 + C < p.T ? t0 + C : p.T;
@@ -506,18 +507,22 @@ __global__ void __launch_bounds__(NCW * 32, MINB) gate_hc_bwd_kernel(const __gri
                 const float v = warp_sum(dg[h]);
                 if (lane == 0) rbuf[(warp * HC + h) * 4] = v;
             }
-            if (__syncthreads_or(!ok)) {
+            // Split rows: one barrier per token.  The warps' dgate sums are in, every thread is done
+            // with the previous token (so its stage is refilled here), and all agree on a failed
+            // wait, this token's stage or the previous token's exchange.  Whole rows keep a second
+            // barrier at the token's end and refill there, which measured faster for them.
+            if (__syncthreads_or(!ok || xfail)) {
                 if (c == 0) report(p.status, nullptr, ENGRAM_DEVERR_TIMEOUT);
                 failed = true;
                 break;
             }
+            if (SPLIT > 1 && c == 0 && it > 0 && issued < n_my) issue(issued++);
             // cross-warp totals of dgate: lane h sums branch h over the warps, then a broadcast
             float tot = 0.f;
             if (lane < HC) {
 #pragma unroll
                 for (int q = 0; q < NCW; ++q) tot += rbuf[(q * HC + lane) * 4];
             }
-            bool xfail = false;
             if (SPLIT > 1) {  // this part's sums to the other CTAs, then the parts' sum in rank order
                 float *xs = xbuf + (it & 1) * SPLIT * 4 * HC;
                 uint64_t *xb = xbar + (it & 1);
@@ -572,18 +577,10 @@ __global__ void __launch_bounds__(NCW * 32, MINB) gate_hc_bwd_kernel(const __gri
                         st_global_v4(p.dkv + t * kv_stride + k_off + h * rb + coff + jj * 16, V::pack(okk));
                     }
                 }
-            // every thread is done with stage s (refill it) and, split, agrees on whether the other half came
-            if (SPLIT > 1) {
-                if (__syncthreads_or(xfail)) {
-                    if (c == 0) report(p.status, nullptr, ENGRAM_DEVERR_TIMEOUT);
-                    failed = true;
-                    ++it;
-                    break;
-                }
-            } else {
+            if (SPLIT == 1) {  // every thread is done with stage s: refill it
                 __syncthreads();
+                if (c == 0 && issued < n_my) issue(issued++);
             }
-            if (c == 0 && issued < n_my) issue(issued++);
         }
         if (failed) break;
 
@@ -601,6 +598,8 @@ __global__ void __launch_bounds__(NCW * 32, MINB) gate_hc_bwd_kernel(const __gri
                 }
             }
     }
+    // the last token's exchange, agreed here (a failed run has agreed already)
+    if (__syncthreads_or(xfail) && !failed && c == 0) report(p.status, nullptr, ENGRAM_DEVERR_TIMEOUT);
     if (c == 0)
         for (int64_t q = it; q < issued; ++q)
             if (!mbar_wait(&full[q % S], static_cast<uint32_t>((q / S) & 1)))
