@@ -205,6 +205,7 @@ struct ScBwdParams {
     uint32_t *status;
     int64_t T;
     int64_t chunk;             // tokens per time chunk
+    int64_t nchunks;           // time chunks
     int64_t nitems;            // chunks x dilation
     int32_t num_seqs;
     int32_t d;
@@ -214,12 +215,11 @@ struct ScBwdParams {
 
 // Shared memory of one backward CTA: the stage ring; by batch parity the y rows [2][kBwBatch][kBwCons]
 // float4 and row-dot parts [2][kBwBatch][kBwCons]; by batch mod 4 the cluster's row dots
-// [4][kBwMaxCluster][kBwBatch]; the stages' position records (16 bytes each); by batch mod 4 the
-// batch tokens' stages [4][kBwBatch]; the mbarriers (full and empty per stage, 2 batch-done,
-// 4 exchange); then the copy producer's state.
+// [4][kBwMaxCluster][kBwBatch]; the stages' position records (16 bytes each); the mbarriers (full
+// and empty per stage, 2 batch-done, 4 exchange); then the copy producer's state.
 __host__ __device__ inline int sc_bwd_smem(int stages, int stage_bytes) {
     return stages * stage_bytes + 2 * kBwBatch * kBwCons * 16 + 2 * kBwBatch * kBwCons * 4 +
-           4 * kBwMaxCluster * kBwBatch * 4 + stages * 16 + 4 * kBwBatch * 4 + (2 * stages + 6) * 8 + 128;
+           4 * kBwMaxCluster * kBwBatch * 4 + stages * 16 + (2 * stages + 6) * 8 + 128;
 }
 
 // A stage: the V~ segment of 512 channels, then the dout segment.
@@ -329,25 +329,49 @@ constexpr uint32_t kFlGroup = 1u << 6;    // this and the next three positions f
                                           // (backward: it starts at a stream position divisible by 4)
 constexpr uint32_t kFlItemStart = 1u << 7;
 constexpr uint32_t kFlDone = 1u << 8;     // no position: the cluster's items are done
-constexpr int kFlItemShift = 12;          // bits 12-31: the work item, at an item start
+constexpr int kFlItemShift = 12;          // bits 12-31: the work item's stream index, at an item start
 constexpr int64_t kBwMaxItems = int64_t(1) << 20;
 
-// The producer's place in the stream of sweep positions of its cluster's work items (in shared
+// The backward's work items in stream order: index k = r * nchunks + c is time chunk c of residue
+// class r, so that consecutive indices of one class continue one sweep; its partial row is
+// item c * dilation + r.  A cluster takes a contiguous range of indices.
+__host__ __device__ inline int64_t sc_bwd_item(int64_t k, int64_t nchunks, int64_t dil) {
+    return (k % nchunks) * dil + k / nchunks;
+}
+__host__ __device__ inline int64_t sc_bwd_range_lo(int64_t cluster, int64_t ncl, int64_t nitems) {
+    return cluster * nitems / ncl;
+}
+
+// The producer's place in the stream of sweep positions of its cluster's range of work items (in
+// shared memory; lane 0 of the producer warp moves it on from one segment to the next).
+struct ScBwdProd {
+    int64_t kend;      // end of the current class's share of the range (stream index)
+    int64_t khi;       // end of the cluster's range
+    int64_t t_hi;      // end of the current class's tokens in the range
+    int64_t xs;        // where the class's next segment starts looking
+    int64_t t;         // token of the next position
+    int64_t last_k;    // stream index of the last chunk token issued
+    uint32_t issued;   // positions issued so far (the sentinel included)
+    uint32_t round;    // times the ring has wrapped
+    int32_t st;        // stage of the next position
+    int32_t s;         // sequence index of xs
+    int32_t r;         // the current class
+    int32_t q, n, n_lead, n_main;  // next position of the segment, its positions, lead-in, chunk tokens
+    int32_t state;     // 0 positions to issue, 1 only the sentinel, 2 finished
+};
+// The forward producer's place in the stream of sweep positions of its CTA's work items (in shared
 // memory; lane 0 of the producer warp moves it on from one segment to the next).
 struct ScProd {
     int64_t item;      // current work item
     int64_t t_hi;      // its chunk's end
     int64_t xs;        // where its next segment starts looking
     int64_t t;         // token of the next position
-    uint32_t issued;   // positions issued so far (the sentinel included)
-    uint32_t round;    // times the ring has wrapped
-    int32_t st;        // stage of the next position
     int32_t s;         // sequence index of xs
-    int32_t q, n, n_lead, n_main;  // next position of the segment, its positions, lead-in, chunk tokens
-    int32_t new_item;  // the next position starts a work item
+    int32_t q, n, n_lead;  // next position of the segment, its positions, lead-in
     int32_t state;     // 0 positions to issue, 1 only the sentinel, 2 finished
 };
 static_assert(sizeof(ScProd) <= 128, "the producer state fits its shared-memory slot");
+static_assert(sizeof(ScBwdProd) <= 128, "the producer state fits its shared-memory slot");
 
 // The backward in one pass.  A cluster of ceil(d / 512) CTAs takes work items (time chunk,
 // residue class t = r mod dilation); CTA `rank` holds channels [512 rank, 512 rank + 512).
@@ -384,12 +408,11 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
     float *pbuf = reinterpret_cast<float *>(ybuf + 2 * kBwBatch * kBwCons);
     float *box = pbuf + 2 * kBwBatch * kBwCons;
     ScMeta *meta = reinterpret_cast<ScMeta *>(box + 4 * kBwMaxCluster * kBwBatch);
-    int *fin_stage = reinterpret_cast<int *>(meta + S);
-    uint64_t *full = reinterpret_cast<uint64_t *>(fin_stage + 4 * kBwBatch);
+    uint64_t *full = reinterpret_cast<uint64_t *>(meta + S);
     uint64_t *empty = full + S;
     int *lcnt = reinterpret_cast<int *>(empty + S);  // [2] warps done with a batch, by batch parity
     uint64_t *boxbar = empty + S + 2;
-    ScProd *prod = reinterpret_cast<ScProd *>(boxbar + 4);
+    ScBwdProd *prod = reinterpret_cast<ScBwdProd *>(boxbar + 4);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -400,14 +423,26 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
     const int64_t dil = p.dil;
     bool failed = false;
 
-    // producer lane 0: the next segment of the producer's stream, moving on through the cluster's items
+    // producer lane 0: the tokens of class k / nchunks in the range's chunks from stream index k on
+    auto prod_start_class = [&](int64_t k) {
+        ScBwdProd &P = *prod;
+        const int64_t r = k / p.nchunks;
+        P.r = static_cast<int32_t>(r);
+        P.kend = P.khi < (r + 1) * p.nchunks ? P.khi : (r + 1) * p.nchunks;
+        P.xs = (k - r * p.nchunks) * p.chunk;
+        const int64_t e = (P.kend - r * p.nchunks) * p.chunk;
+        P.t_hi = e < p.T ? e : p.T;
+        P.s = sc_seq_of(p.offs, p.num_seqs, P.xs);
+    };
+    // producer lane 0: the next segment of the producer's stream (one sequence's class tokens in the
+    // current class's chunks, which may span several work items), moving on through the classes
     auto prod_next_seg = [&]() {
-        ScProd &P = *prod;
+        ScBwdProd &P = *prod;
         ScSeg g;
         for (;;) {
             int64_t xs = P.xs;
             int s = P.s;
-            const bool found = sc_next_seg(p, static_cast<int>(P.item % dil), P.t_hi, xs, s, g);
+            const bool found = sc_next_seg(p, P.r, P.t_hi, xs, s, g);
             P.xs = xs;
             P.s = s;
             if (found) {
@@ -418,32 +453,28 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
                 P.t = g.first - g.n_lead * dil;
                 return;
             }
-            const int64_t next = P.item + sc_num_clusters();
-            if (next >= p.nitems) {
+            if (P.kend >= P.khi) {
                 P.state = 1;
                 return;
             }
-            P.item = next;
-            P.new_item = 1;
-            const int64_t t_lo = next / dil * p.chunk;
-            P.xs = t_lo;
-            P.t_hi = t_lo + p.chunk < p.T ? t_lo + p.chunk : p.T;
-            P.s = sc_seq_of(p.offs, p.num_seqs, t_lo);
+            prod_start_class(P.kend);
         }
     };
     // the producer warp: every position of the cluster's items in order, one position per lane as
     // stages free up, then the sentinel.  The state is kept in registers (the copies' asm
     // statements order shared memory, so shared fields would be reloaded around each of them).
     auto produce_all = [&]() {
-        ScProd &P = *prod;
+        ScBwdProd &P = *prod;
         const uint32_t seg = static_cast<uint32_t>(ncols) * sizeof(E);
         const size_t row_bytes = static_cast<size_t>(p.d) * sizeof(E);
         const uint8_t *src_v = p.v + static_cast<size_t>(c0) * sizeof(E);
         const uint8_t *src_g = p.dout + static_cast<size_t>(c0) * sizeof(E);
+        const int64_t L = p.chunk;
         int st = P.st, state = P.state;
         uint32_t round = P.round, issued = P.issued;
-        int q = P.q, n = P.n, nl = P.n_lead, nm = P.n_main, new_item = P.new_item;
-        uint32_t item_fl = static_cast<uint32_t>(P.item) << kFlItemShift;
+        int q = P.q, n = P.n, nl = P.n_lead, nm = P.n_main;
+        int64_t kcls = static_cast<int64_t>(P.r) * p.nchunks;  // stream index of the class's chunk 0
+        int64_t last_k = P.last_k;
         int64_t t = P.t;
         while (state != 2) {
             // the free stages from st on: lane l tests the one of position issued + l
@@ -478,15 +509,22 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
                     const int ql = q + lane;
                     const int64_t tl = t + lane * dil;
                     const uint32_t kind = ql < nl ? kScLead : (ql < nl + nm ? kScMain : kScTail);
+                    // the chunk token's work item: it starts one where the previous chunk token of the
+                    // stream lies in another chunk (or, for a segment's first, another item)
+                    const int64_t c = tl / L;
+                    const int64_t kl = kcls + c;
+                    const bool istart = kind == kScMain && (ql > nl ? tl - c * L < dil : kl != last_k);
                     // slots and steady groups by the position's place in the stream: the ring has a
-                    // multiple of 4 stages, so a group's four stages are consecutive in it
+                    // multiple of 4 stages, so a group's four stages are consecutive in it; a group's
+                    // four chunk tokens lie in one item
                     const uint32_t gp = issued + static_cast<uint32_t>(lane);
-                    const bool group = (gp & 3u) == 0 && ql >= nl + kBwLag && ql + 4 <= nl + nm && ql + 4 < n;
+                    const bool group = (gp & 3u) == 0 && ql >= nl + kBwLag && ql + 4 <= nl + nm && ql + 4 < n &&
+                                       tl - c * L + 3 * dil < L;
                     uint32_t fl = kind | ((gp & 3u) << kFlSlotShift);
                     if (ql == 0) fl |= kFlSegStart;
                     if (ql == n - 1) fl |= kFlSegEnd;
                     if (group) fl |= kFlGroup;
-                    if (new_item && lane == 0) fl |= kFlItemStart | item_fl;
+                    if (istart) fl |= kFlItemStart | (static_cast<uint32_t>(kl) << kFlItemShift);
                     meta[stl].row = tl * static_cast<int64_t>(row_bytes);
                     meta[stl].flags = fl;
                     uint8_t *dst = ring + static_cast<size_t>(stl) * SB;
@@ -498,18 +536,17 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
                         bulk_load(dst + half, src_g + static_cast<size_t>(tl) * row_bytes, seg, &full[stl],
                                   l2_evict_first_policy());
                 }
-                new_item = 0;
+                // the last chunk token issued, for the next segment's first
+                const int lm = (q + cnt < nl + nm ? q + cnt : nl + nm) - 1;
+                if (lm >= q && lm >= nl) last_k = kcls + (t + (lm - q) * dil) / L;
                 q += cnt;
                 t += cnt * dil;
                 if (q == n) {  // the segment ends: the next one (rare) through the shared state
                     __syncwarp();
-                    if (lane == 0) {
-                        P.new_item = 0;
-                        prod_next_seg();
-                    }
+                    if (lane == 0) prod_next_seg();
                     __syncwarp();
-                    state = P.state, q = P.q, n = P.n, nl = P.n_lead, nm = P.n_main, new_item = P.new_item;
-                    item_fl = static_cast<uint32_t>(P.item) << kFlItemShift;
+                    state = P.state, q = P.q, n = P.n, nl = P.n_lead, nm = P.n_main;
+                    kcls = static_cast<int64_t>(P.r) * p.nchunks;
                     t = P.t;
                 }
             }
@@ -535,19 +572,19 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
     }
     sc_cluster_sync();  // every CTA's barriers exist before any remote arrival
     pdl_wait();
+    const int64_t ncl = sc_num_clusters();
+    const int64_t klo = sc_bwd_range_lo(sc_cluster_id(), ncl, p.nitems);
+    const int64_t khi = sc_bwd_range_lo(sc_cluster_id() + 1, ncl, p.nitems);
     if (warp == kBwWarps) {
         if (lane == 0) {
-            ScProd &P = *prod;
-            P = ScProd{};
-            P.item = sc_cluster_id();
-            if (P.item >= p.nitems) {
+            ScBwdProd &P = *prod;
+            P = ScBwdProd{};
+            P.khi = khi;
+            P.last_k = -1;
+            if (klo >= khi) {
                 P.state = 1;
             } else {
-                const int64_t t_lo = P.item / dil * p.chunk;
-                P.xs = t_lo;
-                P.t_hi = t_lo + p.chunk < p.T ? t_lo + p.chunk : p.T;
-                P.s = sc_seq_of(p.offs, p.num_seqs, t_lo);
-                P.new_item = 1;
+                prod_start_class(klo);
                 prod_next_seg();
             }
         }
@@ -591,6 +628,7 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
         int st = 0;
         uint32_t ph = 0;
         int nfin = 0, nb = 0, prev_n = 0;  // tokens of the open batch, batches posted, tokens of the pending one
+        uint32_t bst = 0, pst = 0;         // the stages of the open and the pending batch's tokens, a byte each
 
         // a wait of the whole warp: every lane takes the same view of a failure
         auto wait_warp = [&](uint64_t *bar, uint32_t parity) {
@@ -645,22 +683,22 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
             const int slot = ((nb & 1) * kBwBatch + k) * kBwCons + tid;
             pbuf[slot] = active ? part : 0.f;
             ybuf[slot] = make_float4(y[0].x, y[0].y, y[1].x, y[1].y);
-            if (tid == 0) fin_stage[(nb & 3) * kBwBatch + k] = sa;
+            bst |= static_cast<uint32_t>(sa) << (8 * k);
         };
         // a token `a` positions back has its dn
         auto complete = [&](int a, const float2 (&dn)[2]) {
             complete_at(back(a), nfin, dn);
             ++nfin;
         };
-        // batch bf's dv rows once the cluster's row dots have arrived; its stages go back to the producer.
-        // Token j's row dot is the sum of the ranks' sums b_0 .. b_(C-1): lane 4k + j takes b_k (plus
-        // b_(k+8) for clusters above 8) and a butterfly over k adds them pairwise, so lane j holds
-        // ((b_0 + b_1) + (b_2 + b_3)) + ((b_4 + b_5) + (b_6 + b_7)); lane j then forms token j's scale.
-        // The tokens' rows are then independent of each other.
-        auto finalize = [&](int bf, int n) {
+        // batch bf's dv rows once the cluster's row dots have arrived; its stages (a byte each in `stg`)
+        // go back to the producer.  Token j's row dot is the sum of the ranks' sums b_0 .. b_(C-1): lane
+        // 4k + j takes b_k (plus b_(k+8) for clusters above 8) and a butterfly over k adds them pairwise,
+        // so lane j holds ((b_0 + b_1) + (b_2 + b_3)) + ((b_4 + b_5) + (b_6 + b_7)); lane j then forms
+        // token j's scale.  The tokens' rows are then independent of each other.  FULL: four tokens.
+        auto finalize = [&](auto Fc, int bf, int n, uint32_t stg) {
+            constexpr bool FULL = decltype(Fc)::v != 0;
             wait_warp(&boxbar[bf & 3], (bf >> 2) & 1);
             const float *bx = box + (bf & 3) * kBwMaxCluster * kBwBatch;
-            const int *fs = fin_stage + (bf & 3) * kBwBatch;
             static_assert(kBwBatch == 4 && kBwMaxCluster == 16, "32 lanes take 8 ranks x 4 tokens, twice");
             const int kr = lane >> 2;
             float s = kr < static_cast<int>(C) ? bx[lane] : 0.f;
@@ -668,28 +706,21 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
             s += __shfl_xor_sync(0xffffffffu, s, 4);
             s += __shfl_xor_sync(0xffffffffu, s, 8);
             s += __shfl_xor_sync(0xffffffffu, s, 16);
-            float kk_l = 0.f;
-            int sj_l = 0;
-            long long tok_l = 0;
-            if (lane < n) {
-                sj_l = fs[lane];
-                const float r = meta[sj_l].rstd;
-                kk_l = r * r * r * s * inv_d;
-                tok_l = meta[sj_l].row;
-            }
+            const int sj_l = static_cast<int>((stg >> (8 * (lane & 3))) & 0xffu);
+            const float r = meta[sj_l].rstd;
+            const float kk_l = r * r * r * s * inv_d;
             uint8_t *dv_col = p.dv + static_cast<size_t>(c0) * sizeof(E) + tid * EV::kBytes;
 #pragma unroll
             for (int j = 0; j < kBwBatch; ++j) {
                 const float kk = __shfl_sync(0xffffffffu, kk_l, j);
-                const int sj = __shfl_sync(0xffffffffu, sj_l, j);
-                const long long tok = __shfl_sync(0xffffffffu, tok_l, j);
-                if (j < n) {
+                const int sj = static_cast<int>((stg >> (8 * j)) & 0xffu);
+                if (FULL || j < n) {
                     float2 x[2];
                     EV::load2(my_ring + sj * SB, x);
                     const float4 y = ybuf[((bf & 1) * kBwBatch + j) * kBwCons + tid];
                     const float2 o[2] = {p2fma(p2(-kk), x[0], make_float2(y.x, y.y)),
                                          p2fma(p2(-kk), x[1], make_float2(y.z, y.w))};
-                    if (active) EV::store2(dv_col + tok, o);
+                    if (active) EV::store2(dv_col + meta[sj].row, o);
                 }
             }
             __syncwarp();
@@ -748,8 +779,11 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
                 __syncwarp();
                 if (lane == 0 && !failed) mbar_arrive_expect_tx(&boxbar[b & 3], (C - 1) * nfin * 4);
             }
-            if (prev_n > 0) finalize(b - 1, prev_n);
+            if (prev_n == kBwBatch) finalize(ScIdx<1>{}, b - 1, kBwBatch, pst);
+            else if (prev_n > 0) finalize(ScIdx<0>{}, b - 1, prev_n, pst);
             prev_n = nfin;
+            pst = bst;
+            bst = 0;
             nfin = 0;
             ++nb;
         };
@@ -815,7 +849,6 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
         // a work item's weight-gradient partial rows: the taps (by tap index) norm_w A_a, the bias, and
         // the norm weight sum_i conv_w[i] A_(width-1-i) (ascending i); the unfolded weights are read
         // again here, once per item
-        const int64_t ncl = sc_num_clusters();
         auto write_rows = [&](int64_t item, bool zero) {
             if (!active) return;
             float *prow = p.partial + static_cast<size_t>(item) * (width + 2) * d + cth;
@@ -845,15 +878,16 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
             *reinterpret_cast<float4 *>(prow + static_cast<size_t>(width + 1) * d) =
                 zero ? z : make_float4(dnw[0], dnw[1], dnw[2], dnw[3]);
         };
-        // rows of the item just finished (if any) and zeros for this cluster's items without tokens up to `next`
-        int64_t cur_item = -1;
+        // rows of the item just finished (if any) and zeros for the range's items without tokens before
+        // stream index `next`
+        int64_t cur_k = -1;
         auto finish_items = [&](int64_t next) {
-            int64_t it = sc_cluster_id();
-            if (cur_item >= 0) {
-                write_rows(cur_item, false);
-                it = cur_item + ncl;
+            int64_t k = klo;
+            if (cur_k >= 0) {
+                write_rows(sc_bwd_item(cur_k, p.nchunks, dil), false);
+                k = cur_k + 1;
             }
-            for (; it < next; it += ncl) write_rows(it, true);
+            for (; k < next; ++k) write_rows(sc_bwd_item(k, p.nchunks, dil), true);
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 db[h] = make_float2(0.f, 0.f);
@@ -869,9 +903,9 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
             const uint32_t fl = meta[st].flags;
             if (fl & kFlDone) break;
             if (fl & kFlItemStart) {
-                const int64_t item = static_cast<int64_t>(fl >> kFlItemShift);
-                finish_items(item);
-                cur_item = item;
+                const int64_t k = static_cast<int64_t>(fl >> kFlItemShift);
+                finish_items(k);
+                cur_k = k;
             }
             if (fl & kFlSegStart) {
 #pragma unroll
@@ -920,12 +954,14 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
                 }
                 if (pend1) complete(1, P1);
                 if (nfin > 0) post();
-                if (prev_n > 0) finalize(nb - 1, prev_n);
+                if (prev_n == kBwBatch) finalize(ScIdx<1>{}, nb - 1, kBwBatch, pst);
+                else if (prev_n > 0) finalize(ScIdx<0>{}, nb - 1, prev_n, pst);
                 prev_n = 0;
+                pst = 0;
                 pend1 = pend2 = pend3 = false;
             }
         }
-        if (!failed) finish_items(p.nitems);
+        if (!failed) finish_items(khi);
     }
     sc_cluster_sync();  // no CTA leaves while a peer may still write into its shared memory
 }
@@ -1492,6 +1528,7 @@ extern "C" engram_status engram_short_conv_bwd(const void *dout, const void *v, 
     prm.status = dev.status_word;
     prm.T = T;
     prm.chunk = sc_chunk(T);
+    prm.nchunks = (T + prm.chunk - 1) / prm.chunk;
     prm.nitems = static_cast<int64_t>(P);
     if (prm.nitems > kBwMaxItems) return fail(ENGRAM_ERR_SHAPE, "%s: %d work items exceed %lld", fn, P, (long long)kBwMaxItems);
     prm.num_seqs = num_seqs;
