@@ -214,12 +214,13 @@ struct ScBwdParams {
 };
 
 // Shared memory of one backward CTA: the stage ring; by batch parity the y rows [2][kBwBatch][kBwCons]
-// float4 and row-dot parts [2][kBwBatch][kBwCons]; by batch mod 4 the cluster's row dots
-// [4][kBwMaxCluster][kBwBatch]; the stages' position records (16 bytes each); the mbarriers (full
-// and empty per stage, 2 batch-done, 4 exchange); then the copy producer's state.
+// float4 and each thread's row-dot parts [2][kBwCons][kBwBatch]; by batch mod 4 the cluster's warp
+// sums of the row dots [4][kBwMaxCluster rank][kBwBatch token][kBwWarps warp]; the stages' position
+// records (16 bytes each); the mbarriers (full and empty per stage, 2 unused, 4 exchange); then the
+// copy producer's state.
 __host__ __device__ inline int sc_bwd_smem(int stages, int stage_bytes) {
     return stages * stage_bytes + 2 * kBwBatch * kBwCons * 16 + 2 * kBwBatch * kBwCons * 4 +
-           4 * kBwMaxCluster * kBwBatch * 4 + stages * 16 + (2 * stages + 6) * 8 + 128;
+           4 * kBwMaxCluster * kBwBatch * kBwWarps * 4 + stages * 16 + (2 * stages + 6) * 8 + 128;
 }
 
 // A stage: the V~ segment of 512 channels, then the dout segment.
@@ -268,6 +269,26 @@ __device__ __forceinline__ void sc_st_async(uint32_t raddr, float v, uint32_t rb
     asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(raddr),
                  "r"(__float_as_uint(v)), "r"(rbar)
                  : "memory");
+}
+// Whether the current phases of four consecutive mbarriers, bar0 .. bar0 + 3, with the same parity
+// have completed: the four tests are issued back to back, so their latencies overlap.  Like
+// mbar_try_wait, each may suspend the thread for a while before it answers.
+__device__ __forceinline__ bool sc_try_wait4(uint64_t *bar0, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p0, p1, p2, p3;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p0, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p1, [%1+8], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p2, [%1+16], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p3, [%1+24], %2;\n\t"
+        "and.pred p0, p0, p1;\n\t"
+        "and.pred p2, p2, p3;\n\t"
+        "and.pred p0, p0, p2;\n\t"
+        "selp.u32 %0, 1, 0, p0;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar0)), "r"(parity)
+        : "memory");
+    return done != 0;
 }
 // A 4-byte asynchronous global -> shared copy, and an arrival on `bar` once this thread's
 // earlier asynchronous copies have landed (the barrier's count includes it).
@@ -373,27 +394,28 @@ struct ScProd {
 static_assert(sizeof(ScProd) <= 128, "the producer state fits its shared-memory slot");
 static_assert(sizeof(ScBwdProd) <= 128, "the producer state fits its shared-memory slot");
 
-// The backward in one pass.  A cluster of ceil(d / 512) CTAs takes work items (time chunk,
-// residue class t = r mod dilation); CTA `rank` holds channels [512 rank, 512 rank + 512).
-// A producer warp walks the items' segments and streams, per sweep position (one per lane), the
-// token's V~ and dout row segments (1-D bulk copies) and its rstd (a 4-byte asynchronous copy)
-// into a ring of stages, as far ahead as the ring allows, with a record of the position (row
-// offset, kind, slot, segment and item boundaries).  Each of the 128 consumer threads owns four
-// channels and sweeps the positions in order.  With the norm weight folded into the taps
-// (w'_a = w_a norm_w, w_a: tap width - 1 - a) and u' = V~ rstd (the last three kept by age in
-// registers):
+// The backward in one pass.  A cluster of ceil(d / 512) CTAs takes a contiguous range of work
+// items (time chunk, residue class t = r mod dilation) in class order, so that one class's
+// consecutive chunks form one sweep; CTA `rank` holds channels [512 rank, 512 rank + 512).
+// A producer warp walks the range's segments (a sequence's class tokens in the range) and streams,
+// per sweep position (one per lane), the token's V~ and dout row segments (1-D bulk copies) and its
+// rstd (a 4-byte asynchronous copy) into a ring of stages, as far ahead as the ring allows, with a
+// record of the position (row offset, kind, slot, segment and item boundaries).  Each of the 128
+// consumer threads owns four channels and sweeps the positions in order.  With the norm weight
+// folded into the taps (w'_a = w_a norm_w, w_a: tap width - 1 - a) and u' = V~ rstd (the last
+// three kept by age in registers):
 //   conv = bias + sum_a w'_a u'[t - a dil],  dc = dout SiLU'(conv),
-//   A_a += dc u'[t - a dil] and db += dc over the chunk's outputs, and the
+//   A_a += dc u'[t - a dil] and db += dc over the item's outputs, and the
 //   dn = norm_w du = sum_a w'_a dc[t + a dil] still collecting contributions (three, by age).
 // When a token's dn is complete its stage is read back for V~ and dout:
 //   y = dout + rstd dn  (kept in shared memory),  and the thread's part of the row dot
 //   s = sum_c norm_w du V~ = sum_c dn V~.
-// Every four tokens a reducer warp sums the CTA's parts of each row dot (thread order, then
-// lanes) and sends the sums to the other CTAs of the cluster (distributed shared memory,
-// completing on their mbarrier); a batch later, when the cluster's sums have arrived, every warp
-// adds them in a fixed pairwise order and writes dv = y - rstd^3 V~ s / d.  At a work item's end its partial
-// rows are norm_w A_a (tap width - 1 - a), db, and, for the norm weight, sum_i conv_w[i] A_(width-1-i):
-// over a sequence dL/dnorm_w = sum_t du u' = sum_a w_a sum_t dc[t] u'[t - a dil], so no per-token
+// Every four tokens each warp sums its threads' parts of each row dot (one butterfly) and sends the
+// sums to every CTA of the cluster (distributed shared memory, completing on their mbarrier); a
+// batch later, when all the cluster's warp sums have arrived, every warp adds them in a fixed order
+// and writes dv = y - rstd^3 V~ s / d.  At a work item's end its partial rows are norm_w A_a
+// (tap width - 1 - a), db, and, for the norm weight, sum_i conv_w[i] A_(width-1-i): over a
+// sequence dL/dnorm_w = sum_t du u' = sum_a w_a sum_t dc[t] u'[t - a dil], so no per-token
 // accumulator and no norm weight are needed in the sweep.  All waits are bounded.
 // The chunks depend on T only and every sum has a fixed order, so results are bitwise reproducible.
 template <typename E>
@@ -407,10 +429,9 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
     float4 *ybuf = reinterpret_cast<float4 *>(smem + static_cast<size_t>(S) * SB);
     float *pbuf = reinterpret_cast<float *>(ybuf + 2 * kBwBatch * kBwCons);
     float *box = pbuf + 2 * kBwBatch * kBwCons;
-    ScMeta *meta = reinterpret_cast<ScMeta *>(box + 4 * kBwMaxCluster * kBwBatch);
+    ScMeta *meta = reinterpret_cast<ScMeta *>(box + 4 * kBwMaxCluster * kBwBatch * kBwWarps);
     uint64_t *full = reinterpret_cast<uint64_t *>(meta + S);
     uint64_t *empty = full + S;
-    int *lcnt = reinterpret_cast<int *>(empty + S);  // [2] warps done with a batch, by batch parity
     uint64_t *boxbar = empty + S + 2;
     ScBwdProd *prod = reinterpret_cast<ScBwdProd *>(boxbar + 4);
 
@@ -470,6 +491,10 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
         const uint8_t *src_v = p.v + static_cast<size_t>(c0) * sizeof(E);
         const uint8_t *src_g = p.dout + static_cast<size_t>(c0) * sizeof(E);
         const int64_t L = p.chunk;
+        const bool small = p.T <= 0x7fffffff;  // chunk of a token by 32-bit division
+        auto chunk_of = [&](int64_t tk) {
+            return small ? static_cast<int64_t>(static_cast<uint32_t>(tk) / static_cast<uint32_t>(L)) : tk / L;
+        };
         int st = P.st, state = P.state;
         uint32_t round = P.round, issued = P.issued;
         int q = P.q, n = P.n, nl = P.n_lead, nm = P.n_main;
@@ -511,7 +536,7 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
                     const uint32_t kind = ql < nl ? kScLead : (ql < nl + nm ? kScMain : kScTail);
                     // the chunk token's work item: it starts one where the previous chunk token of the
                     // stream lies in another chunk (or, for a segment's first, another item)
-                    const int64_t c = tl / L;
+                    const int64_t c = chunk_of(tl);
                     const int64_t kl = kcls + c;
                     const bool istart = kind == kScMain && (ql > nl ? tl - c * L < dil : kl != last_k);
                     // slots and steady groups by the position's place in the stream: the ring has a
@@ -538,7 +563,7 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
                 }
                 // the last chunk token issued, for the next segment's first
                 const int lm = (q + cnt < nl + nm ? q + cnt : nl + nm) - 1;
-                if (lm >= q && lm >= nl) last_k = kcls + (t + (lm - q) * dil) / L;
+                if (lm >= q && lm >= nl) last_k = kcls + chunk_of(t + (lm - q) * dil);
                 q += cnt;
                 t += cnt * dil;
                 if (q == n) {  // the segment ends: the next one (rare) through the shared state
@@ -566,7 +591,6 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
             mbar_init(&full[i], 2);  // the producer's arrival and its rstd copy's
             mbar_init(&empty[i], kBwWarps);
         }
-        lcnt[0] = lcnt[1] = 0;
         for (int i = 0; i < 4; ++i) mbar_init(&boxbar[i], 1);
         mbar_init_fence();
     }
@@ -680,9 +704,8 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
             // the thread's part of the row dot: (c0 + c2) + (c1 + c3) of the products
             const float2 pp = p2fma(dn[1], x[1], p2mul(dn[0], x[0]));
             const float part = pp.x + pp.y;
-            const int slot = ((nb & 1) * kBwBatch + k) * kBwCons + tid;
-            pbuf[slot] = active ? part : 0.f;
-            ybuf[slot] = make_float4(y[0].x, y[0].y, y[1].x, y[1].y);
+            pbuf[((nb & 1) * kBwCons + tid) * kBwBatch + k] = active ? part : 0.f;
+            ybuf[((nb & 1) * kBwBatch + k) * kBwCons + tid] = make_float4(y[0].x, y[0].y, y[1].x, y[1].y);
             bst |= static_cast<uint32_t>(sa) << (8 * k);
         };
         // a token `a` positions back has its dn
@@ -691,18 +714,33 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
             ++nfin;
         };
         // batch bf's dv rows once the cluster's row dots have arrived; its stages (a byte each in `stg`)
-        // go back to the producer.  Token j's row dot is the sum of the ranks' sums b_0 .. b_(C-1): lane
-        // 4k + j takes b_k (plus b_(k+8) for clusters above 8) and a butterfly over k adds them pairwise,
-        // so lane j holds ((b_0 + b_1) + (b_2 + b_3)) + ((b_4 + b_5) + (b_6 + b_7)); lane j then forms
-        // token j's scale.  The tokens' rows are then independent of each other.  FULL: four tokens.
+        // go back to the producer.  Rank k's sum of token j is b_k = (w_0 + w_1) + (w_2 + w_3) over its
+        // warps' sums; token j's row dot is the sum of b_0 .. b_(C-1): lane 4k + j takes b_k (plus
+        // b_(k+8) for clusters above 8) and a butterfly over k adds them pairwise, so lane j holds
+        // ((b_0 + b_1) + (b_2 + b_3)) + ((b_4 + b_5) + (b_6 + b_7)); lane j then forms token j's scale.
+        // The tokens' rows are then independent of each other.  FULL: four tokens.
+        // batch bf's dv rows once the cluster's row dots have arrived; its stages (a byte each in `stg`)
+        // go back to the producer.  Rank k's sum of token j is b_k = (w_0 + w_1) + (w_2 + w_3) over its
+        // warps' sums; token j's row dot is the sum of b_0 .. b_(C-1): lane 4k + j takes b_k (plus
+        // b_(k+8) for clusters above 8) and a butterfly over k adds them pairwise, so lane j holds
+        // ((b_0 + b_1) + (b_2 + b_3)) + ((b_4 + b_5) + (b_6 + b_7)); lane j then forms token j's scale.
+        // The tokens' rows are then independent of each other.  FULL: four tokens.
         auto finalize = [&](auto Fc, int bf, int n, uint32_t stg) {
             constexpr bool FULL = decltype(Fc)::v != 0;
             wait_warp(&boxbar[bf & 3], (bf >> 2) & 1);
-            const float *bx = box + (bf & 3) * kBwMaxCluster * kBwBatch;
-            static_assert(kBwBatch == 4 && kBwMaxCluster == 16, "32 lanes take 8 ranks x 4 tokens, twice");
+            const float4 *bx = reinterpret_cast<const float4 *>(box) + (bf & 3) * kBwMaxCluster * kBwBatch;
+            static_assert(kBwBatch == 4 && kBwMaxCluster == 16 && kBwWarps == 4,
+                          "32 lanes take 8 ranks x 4 tokens, twice; a rank's four warp sums are one float4");
             const int kr = lane >> 2;
-            float s = kr < static_cast<int>(C) ? bx[lane] : 0.f;
-            if (kr + 8 < static_cast<int>(C)) s += bx[lane + 8 * kBwBatch];
+            float s = 0.f;
+            if (kr < static_cast<int>(C)) {
+                const float4 u = bx[lane];
+                s = (u.x + u.y) + (u.z + u.w);
+            }
+            if (kr + 8 < static_cast<int>(C)) {
+                const float4 u = bx[lane + 8 * kBwBatch];
+                s += (u.x + u.y) + (u.z + u.w);
+            }
             s += __shfl_xor_sync(0xffffffffu, s, 4);
             s += __shfl_xor_sync(0xffffffffu, s, 8);
             s += __shfl_xor_sync(0xffffffffu, s, 16);
@@ -726,61 +764,41 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
             __syncwarp();
             mbar_arrive_if(&empty[sj_l], lane < n && !failed);
         };
-        // the open batch is complete: this warp's parts are counted in, and the warp that completes the
-        // count sums the CTA's row dots (thread order, then lanes) and sends them to the cluster --
-        // nobody waits for the others; then the previous batch, whose sums have had a batch's time
-        // to arrive, is finished
+        auto finalize_any = [&](int bf, int n, uint32_t stg) {
+            if (n == kBwBatch) finalize(ScIdx<1>{}, bf, n, stg);
+            else finalize(ScIdx<0>{}, bf, n, stg);
+        };
+        // the open batch is complete: the warp sums its threads' parts of each token in one transposed
+        // butterfly (pairing lanes 16, 8, 4, 2, 1 apart; each lane passes on the tokens it does not
+        // keep, so that after two steps lanes 8t .. 8t + 7 carry token t) and sends the sums to every
+        // CTA of the cluster, itself included, with stores that complete on their exchange barrier,
+        // which warp 0 arms; then the previous batch, whose sums have had a batch's time to arrive, is
+        // finished.  Nobody waits for the others here.
+        const uint32_t box_lo = smem_addr(box), bar_lo = smem_addr(boxbar);
         auto post = [&]() {
             const int b = nb;
-            __syncwarp();
-            int last = 0;
-            if (lane == 0 && !failed) {
-                __threadfence_block();  // the warp's parts before its count
-                last = atomicAdd(&lcnt[b & 1], 1) == kBwWarps - 1;
-                if (last) {
-                    lcnt[b & 1] = 0;  // no warp counts batch b + 2 before this batch's sums were sent
-                    __threadfence_block();  // every warp's parts before the sums
-                }
+            static_assert(kBwBatch == 4, "a thread's four parts are one float4");
+            const float4 pp = *reinterpret_cast<const float4 *>(pbuf + ((b & 1) * kBwCons + tid) * kBwBatch);
+            const bool hi = (lane & 16) != 0, b3 = (lane & 8) != 0;
+            float s0 = hi ? pp.z : pp.x, s1 = hi ? pp.w : pp.y;
+            s0 += __shfl_xor_sync(0xffffffffu, hi ? pp.x : pp.z, 16);
+            s1 += __shfl_xor_sync(0xffffffffu, hi ? pp.y : pp.w, 16);
+            float sum = b3 ? s1 : s0;
+            sum += __shfl_xor_sync(0xffffffffu, b3 ? s0 : s1, 8);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+            // lane 8t + q sends token t's sum to ranks q and q + 8, into slot [rank][t][warp]
+            const int tk = lane >> 3;
+            if (!failed && tk < nfin) {
+                const uint32_t slot =
+                    ((static_cast<uint32_t>(b & 3) * kBwMaxCluster + rank) * kBwBatch + tk) * kBwWarps + warp;
+                for (int r = lane & 7; r < static_cast<int>(C); r += 8)
+                    sc_st_async(sc_mapa(box_lo + slot * 4, r), sum, sc_mapa(bar_lo + (b & 3) * 8, r));
             }
-            if (__shfl_sync(0xffffffffu, last, 0)) {
-                __syncwarp();
-                const float *pb = pbuf + (b & 1) * kBwBatch * kBwCons;
-                const uint32_t box_lo = smem_addr(box), bar_lo = smem_addr(boxbar);
-                static_assert(kBwCons == 32 * 4 && kBwBatch == 4, "a lane sums four threads' parts of four tokens");
-                // each lane's four threads' parts of each token, in thread order (the slots of tokens
-                // past nfin hold older parts and are not used)
-                float v[kBwBatch];
-#pragma unroll
-                for (int j = 0; j < kBwBatch; ++j) {
-                    const float4 u0 = *reinterpret_cast<const float4 *>(pb + j * kBwCons + lane * 4);
-                    v[j] = ((u0.x + u0.y) + u0.z) + u0.w;
-                }
-                // the four tokens' butterflies at once, pairing lanes 16, 8, 4, 2, 1 apart as a
-                // single token's would: each lane passes on the tokens it does not keep, and after
-                // the first two steps lanes 8t .. 8t + 7 carry token t
-                const bool hi = (lane & 16) != 0, b3 = (lane & 8) != 0;
-                float s0 = hi ? v[2] : v[0], s1 = hi ? v[3] : v[1];
-                s0 += __shfl_xor_sync(0xffffffffu, hi ? v[0] : v[2], 16);
-                s1 += __shfl_xor_sync(0xffffffffu, hi ? v[1] : v[3], 16);
-                float sum = b3 ? s1 : s0;
-                sum += __shfl_xor_sync(0xffffffffu, b3 ? s0 : s1, 8);
-                sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-                sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-                sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-                // lane 8t + q gives token t's sum to ranks q and q + 8: its own slot, or a peer's
-                const int tk = lane >> 3;
-                const int slot = ((b & 3) * kBwMaxCluster + static_cast<int>(rank)) * kBwBatch + tk;
-                if (tk < nfin)
-                    for (int r = lane & 7; r < static_cast<int>(C); r += 8) {
-                        if (r == static_cast<int>(rank)) box[slot] = sum;
-                        else if (!failed)
-                            sc_st_async(sc_mapa(box_lo + slot * 4, r), sum, sc_mapa(bar_lo + (b & 3) * 8, r));
-                    }
-                __syncwarp();
-                if (lane == 0 && !failed) mbar_arrive_expect_tx(&boxbar[b & 3], (C - 1) * nfin * 4);
-            }
-            if (prev_n == kBwBatch) finalize(ScIdx<1>{}, b - 1, kBwBatch, pst);
-            else if (prev_n > 0) finalize(ScIdx<0>{}, b - 1, prev_n, pst);
+            if (warp == 0 && lane == 0 && !failed)
+                mbar_arrive_expect_tx(&boxbar[b & 3], C * kBwWarps * static_cast<uint32_t>(nfin) * 4);
+            if (prev_n > 0) finalize_any(b - 1, prev_n, pst);
             prev_n = nfin;
             pst = bst;
             bst = 0;
@@ -898,7 +916,11 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
         finish_items(-1);  // clears the accumulators
 
         for (;;) {
-            wait_stages(0, 1);
+            // a steady group starts only at a stage divisible by 4: there, its four stages are tried at
+            // once (they do not wrap); otherwise, or while one is still filling, the first alone
+            bool four = false;
+            if (!failed && (st & 3) == 0) four = __all_sync(0xffffffffu, sc_try_wait4(&full[st], ph));
+            if (!four) wait_stages(0, 1);
             if (failed) break;
             const uint32_t fl = meta[st].flags;
             if (fl & kFlDone) break;
@@ -920,7 +942,7 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
                 // all four stages first, so that the four positions' loads and arithmetic may overlap.
                 // The group starts at a stage divisible by 4, so its stages st0 .. st0 + 3 do not wrap;
                 // the tokens three back are at st0 - 3 .. st0 - 1 (wrapping when st0 = 0), then st0.
-                wait_stages(1, 4);
+                if (!four) wait_stages(1, 4);
                 if (failed) break;
                 const int st0 = st;
                 const int bk = (st0 == 0 ? S : st0) - kBwLag;
@@ -954,8 +976,7 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
                 }
                 if (pend1) complete(1, P1);
                 if (nfin > 0) post();
-                if (prev_n == kBwBatch) finalize(ScIdx<1>{}, nb - 1, kBwBatch, pst);
-                else if (prev_n > 0) finalize(ScIdx<0>{}, nb - 1, prev_n, pst);
+                if (prev_n > 0) finalize_any(nb - 1, prev_n, pst);
                 prev_n = 0;
                 pst = 0;
                 pend1 = pend2 = pend3 = false;

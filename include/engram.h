@@ -455,10 +455,12 @@ engram_status engram_short_conv_num_partials(int64_t T, int32_t dilation, int32_
  * rule grouped the other way).  The convolution is recomputed with the norm weight folded into the
  * taps (conv_w[c, i] * norm_w[c], rounded once) and du carried as norm_w du.  Reduce the partials
  * with engram_short_conv_grad_reduce.  s sums, in this order: a thread's four channels as
- * (c0 + c2) + (c1 + c3), four threads in order, a 32-lane butterfly (one 512-channel block), then
- * the C = ceil(d / 512) block sums b_k pairwise: b_k + b_(k+8) first when C > 8, then
- * ((b_0 + b_1) + (b_2 + b_3)) + ((b_4 + b_5) + (b_6 + b_7)), absent blocks adding zero.  One pass over dout and V~ on thread-block
- * clusters of ceil(d / 512) CTAs; dout, v, dv and dw_partial 16-byte aligned.
+ * (c0 + c2) + (c1 + c3); a warp's 32 threads (128 channels) as a butterfly pairing lanes 16, 8, 4,
+ * 2, 1 apart; a 512-channel block's four warp sums as (w_0 + w_1) + (w_2 + w_3); then the
+ * C = ceil(d / 512) block sums b_k pairwise: b_k + b_(k+8) first when C > 8, then
+ * ((b_0 + b_1) + (b_2 + b_3)) + ((b_4 + b_5) + (b_6 + b_7)), absent blocks adding zero.  One pass
+ * over dout and V~ on thread-block clusters of ceil(d / 512) CTAs; dout, v, dv and dw_partial
+ * 16-byte aligned.
  */
 engram_status engram_short_conv_bwd(const void *dout, const void *v, engram_dtype dtype, const float *norm_w,
                                     const float *conv_w, const float *bias, const float *rstd,
