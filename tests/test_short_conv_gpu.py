@@ -14,8 +14,10 @@ Tolerances come from the fp32 arithmetic (u = 2^-24):
     and |SiLU'| <= 1.1 times the conv error; the two residual adds 2u of the magnitudes; the output
     rounding half an ulp of |out| (an ulp for bf16, whose rounding the fp32 error can tip);
   * backward: dv = dout + rstd norm_w du - rstd^3 V~ s/d, with du from 4 products of the taps and
-    dc, s a sum over d of 4 per thread (two pairs), 4 per lane, 5 shuffle levels and up to 16
-    cluster blocks in order: rel_b = 3 r_rel + 16u + 29u, times the oracle's magnitude sum
+    dc, s a sum over d of 4 per thread (two pairs), a warp's 32 lanes in 5 shuffle levels, a
+    CTA's 4 warps in 2 levels and up to 16 cluster blocks in order (26 levels; 29u is kept, the
+    bound of the earlier order, a thread's 4 lanes in order before the shuffles):
+    rel_b = 3 r_rel + 16u + 29u, times the oracle's magnitude sum
     |dout| + |rstd norm_w du| +
     |rstd^3 V~| sum|norm_w du V~|/d; and the conv's absolute error, carried into dc through SiLU''
     (at most 1/2 in size) and from there through the taps into du, dv and the weight gradients;
