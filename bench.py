@@ -536,12 +536,70 @@ def oracle_sample_text(steps: int, threads: int) -> str:
             f"weight-gradient reduction; {threads} host threads")
 
 
+ORACLE_CONFIG_SAMPLE = 4096  # tokens the per-config oracle rates are measured on (whole T where smaller)
+
+
+def _rates(run_part, reduce, ranges, n_tokens: int, what: str) -> dict:
+    """tokens/s of the oracle over `ranges` (then `reduce` of the parts), first on one core (one call
+    after another), then on every core (the same calls on a thread pool)."""
+    t0 = time.perf_counter()
+    reduce([run_part(b) for b in ranges])
+    t1 = time.perf_counter() - t0
+    threads = _oracle_threads()
+    with ThreadPoolExecutor(threads) as pool:
+        t0 = time.perf_counter()
+        reduce(list(pool.map(run_part, ranges)))
+        t2 = time.perf_counter() - t0
+    return {"single_core": {"tokens_per_s": n_tokens / t1, "cores": 1, "seconds": t1},
+            "all_cores": {"tokens_per_s": n_tokens / t2, "cores": threads, "seconds": t2},
+            "sample": what}
+
+
+def oracle_gate_rates(x: dict, fwd_only: bool, T_config: int) -> dict:
+    """The oracle's gate on host copies of a config's first tokens: the forward, or forward +
+    backward of every token then the ordered reduction of the per-call weight-gradient sums."""
+    import oracle
+
+    n = x["h"].shape[0]
+    ranges = _ranges(n, max(1, n // ORACLE_GATE_CHUNK))
+
+    def part(b):
+        oracle.gate_fwd(x["h"], x["k"], x["v"], x["w_h"], x["w_k"], EPS, b[0], b[1])
+        if not fwd_only:
+            return oracle.gate_bwd(x["dout"], x["h"], x["k"], x["v"], x["w_h"], x["w_k"], EPS, b[0], b[1])["dweight"]
+
+    def reduce(parts):
+        if not fwd_only:
+            oracle.grad_w_reduce(np.stack(parts), x["w_h"], x["w_k"])
+
+    ops = "gate fwd" if fwd_only else "gate fwd + bwd + ordered reduction"
+    what = (f"{ops} of all {n} tokens" if n == T_config else
+            f"{ops} of the first {n} of the {T_config} tokens (the oracle's cost per token does not depend on T)")
+    return _rates(part, reduce, ranges, n, what + f", in {len(ranges)} calls")
+
+
+def oracle_hash_rates(hw, table_host) -> dict:
+    """The oracle's hash + gather of every token of the step's batch from the full host table."""
+    import oracle
+
+    s = hw.spec
+
+    def part(b):
+        idx = oracle.hash_indices(hw.token_ids, hw.seq_offsets, hw.compress_map, hw.vocab, s.min_order,
+                                  s.num_orders, s.heads, s.multipliers, s.primes, b[0], b[1])
+        oracle.gather_rows(table_host, s.primes, idx)
+
+    ranges = _ranges(hw.T, 4 * _oracle_threads())
+    return _rates(part, lambda parts: None, ranges, hw.T,
+                  f"hash + gather of all {hw.T} tokens from the full 4.1 GB table, in {len(ranges)} calls")
+
+
 # ----------------------------------------------------------------------------- the gate at every workload size
 
 L2_BYTES = 129 * 2 ** 20
 
 
-def _gate_config_entry(wl, device, steps: int, warmup: int, peak: float, fwd_only: bool):
+def _gate_config_entry(wl, device, steps: int, warmup: int, peak: float, fwd_only: bool, with_oracle: bool = False):
     """Gate kernels of one workload, each timed on its own over rotating input sets (so a launch
     never finds its inputs in L2 from the previous use), plus the fwd -> bwd -> grad_w_reduce
     sequence for training workloads.  Every timing is a CUDA-graph replay with events between
@@ -641,22 +699,29 @@ def _gate_config_entry(wl, device, steps: int, warmup: int, peak: float, fwd_onl
         step["tokens_per_s"] = T / (3 * ms / 1e3)
         step["launches_per_step"] = 3
         res["fwd_bwd_reduce"] = step
+    if with_oracle:  # the oracle on host copies of set 0's first tokens, on one core and on all
+        n = min(T, ORACLE_CONFIG_SAMPLE) if T > 2 * ORACLE_CONFIG_SAMPLE else T
+        t = S[0]["in"]
+        x = {nm: _bf16_bits(t[nm][:n].cpu()) for nm in (("h", "k", "v") if fwd_only else ("h", "k", "v", "dout"))}
+        x["w_h"], x["w_k"] = t["w_h"].cpu().numpy(), t["w_k"].cpu().numpy()
+        res["oracle"] = oracle_gate_rates(x, fwd_only, T)
     del S
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
     return res
 
 
-def time_gate_configs(device, steps: int, warmup: int, peak: float):
+def time_gate_configs(device, steps: int, warmup: int, peak: float, with_oracle: bool = False):
     """The gate-only workloads: forward at T = 8192, d = 2048, and fwd + bwd + grad_w_reduce at
-    d = 7168 for T in {4096, 32768, 131072} and a ragged pack of 64 sequences (the gate sees one T)."""
+    d = 7168 for T in {4096, 32768, 131072} and a ragged pack of 64 sequences (the gate sees one T);
+    with_oracle: also the oracle's rate on each, on one core and on all host cores."""
     from synth import workloads as W
 
     out = {}
     wl = W.gate_fwd_2k()
-    out[wl.name] = _gate_config_entry(wl, device, steps, warmup, peak, fwd_only=True)
+    out[wl.name] = _gate_config_entry(wl, device, steps, warmup, peak, fwd_only=True, with_oracle=with_oracle)
     for wl in (W.gate_sweep_7k(4096), W.gate_sweep_7k(32768), W.gate_sweep_7k(131072), W.gate_ragged_7k()):
-        out[wl.name] = _gate_config_entry(wl, device, steps, warmup, peak, fwd_only=False)
+        out[wl.name] = _gate_config_entry(wl, device, steps, warmup, peak, fwd_only=False, with_oracle=with_oracle)
     return out
 
 
@@ -1113,17 +1178,20 @@ def main_native(args, rank, local, world):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
     # per-GPU measurements of the gate's and the NEXT rows' own workloads: at N = 1 only (each replica
     # would repeat them), after the timed step
-    configs = None if args.no_configs or world > 1 else time_gate_configs(device, args.steps, args.warmup, peak)
+    configs = None if args.no_configs or world > 1 else time_gate_configs(
+        device, args.steps, args.warmup, peak, with_oracle=rank == 0 and not args.no_cpu_baseline)
     next_rows = None if args.no_next or world > 1 else time_next_rows(device, args.steps, args.warmup)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         table_host, mbs, w_h, w_k = oracle_inputs_from_device(wk)
         times, threads = time_oracle_steps(wk["hw"], table_host, mbs, w_h, w_k, args.cpu_steps, 1)
+        hash_rates = oracle_hash_rates(wk["hw"], table_host)
         del table_host, mbs
         mean_s = sum(times) / len(times)
         cpu = {"value": T_all / mean_s, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                "sample": oracle_sample_text(args.cpu_steps, threads) + "; inputs copied from the device",
-               "step_ms_mean": mean_s * 1e3, "step_ms_min": min(times) * 1e3}
+               "step_ms_mean": mean_s * 1e3, "step_ms_min": min(times) * 1e3,
+               "hash_gather_64k": hash_rates}
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,

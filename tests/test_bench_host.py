@@ -88,3 +88,23 @@ def test_oracle_step_runs_a_whole_step_on_a_small_workload():
     assert t > 0
     times, threads = bench.time_oracle_steps(hw, np.ascontiguousarray(table), mbs, g[0]["w_h"], g[0]["w_k"], 2, 1)
     assert len(times) == 2 and all(x > 0 for x in times) and threads >= 1
+
+
+def test_oracle_rates_per_config_on_one_core_and_on_all():
+    """The per-config oracle rates (one core, then every core) on the tiny workloads: the gate forward
+    alone, the forward + backward + reduction, and the hash + gather."""
+    import numpy as np
+
+    from synth import workloads as W
+
+    x = W.gate_host_inputs(W.GateWorkload(name="r", T=700, d=64, dtype="bf16", seed=61))
+    for fwd_only in (True, False):
+        r = bench.oracle_gate_rates(x, fwd_only, T_config=700 if fwd_only else 70000)
+        assert r["single_core"]["cores"] == 1 and r["single_core"]["tokens_per_s"] > 0
+        assert r["all_cores"]["cores"] >= 1 and r["all_cores"]["tokens_per_s"] > 0
+        assert ("all 700 tokens" in r["sample"]) == fwd_only and ("first 700 of the 70000" in r["sample"]) != fwd_only
+    hw = W.tiny_hash()
+    table = np.ascontiguousarray(hw.table_host.view(np.uint32).astype(np.uint16))
+    r = bench.oracle_hash_rates(hw, table)
+    assert r["single_core"]["tokens_per_s"] > 0 and r["all_cores"]["tokens_per_s"] > 0
+    assert f"all {hw.T} tokens" in r["sample"]
