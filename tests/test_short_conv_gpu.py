@@ -234,6 +234,29 @@ def test_in_place_output_and_bitwise_reruns():
         ecm.set_max_ctas(0)
 
 
+def test_backward_bitwise_across_grids():
+    """The backward's clusters take contiguous ranges of work items in class order, so the grid decides
+    where one cluster's sweep stops and the next one's starts; outputs and partials must not depend on
+    it.  63 work items (21 time chunks x 3 classes, ragged sequences) on 1, 2, 3 and 7 clusters of 2
+    CTAs, against the uncapped grid, bit for bit; a single cluster sweeps every class in turn."""
+    wl = W.ShortConvWorkload(name="grids", lengths=[3000, 1, 1500, 700], d=1024, width=4, dilation=3,
+                             dtype="bf16", seed=83, bias=True, with_h=False)
+    x = W.short_conv_host_inputs(wl)
+    t = {k: _t(v) for k, v in x.items() if v is not None}
+    a = _run(x, wl)
+    try:
+        for ncl in (1, 2, 3, 7):
+            ecm.set_max_ctas(2 * ncl)
+            dv, part = ecm.short_conv_bwd(t["dout"], t["v"], t["norm_w"], t["conv_w"], a["rstd"], t["seq_offsets"],
+                                          wl.dilation, bias=t.get("bias"))
+            torch.cuda.synchronize()
+            assert torch.equal(dv, a["dv"]), f"dv on {ncl} clusters"
+            assert torch.equal(part, a["part"]), f"partials on {ncl} clusters"
+    finally:
+        ecm.set_max_ctas(0)
+    assert ecm.device_status() == 0
+
+
 @pytest.mark.parametrize("lengths,d,dtype", [([700, 0, 300, 1], 4096, "bf16"), ([500], 136, "f32"),
                                              ([64, 64], 8192, "bf16"), ([1], 8, "bf16")])
 def test_gate_statistic_feeds_the_conv(lengths, d, dtype):
