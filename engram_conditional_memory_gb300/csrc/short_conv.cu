@@ -216,11 +216,11 @@ struct ScBwdParams {
 // Shared memory of one backward CTA: the stage ring; by batch parity the y rows [2][kBwBatch][kBwCons]
 // float4 and each thread's row-dot parts [2][kBwCons][kBwBatch]; by batch mod 4 the cluster's warp
 // sums of the row dots [4][kBwMaxCluster rank][kBwBatch token][kBwWarps warp]; the stages' position
-// records (16 bytes each); the mbarriers (full and empty per stage, 2 unused, 4 exchange); then the
-// copy producer's state.
+// records (16 bytes each); the mbarriers (full and empty per stage, 4 exchange); then the copy
+// producer's state.
 __host__ __device__ inline int sc_bwd_smem(int stages, int stage_bytes) {
     return stages * stage_bytes + 2 * kBwBatch * kBwCons * 16 + 2 * kBwBatch * kBwCons * 4 +
-           4 * kBwMaxCluster * kBwBatch * kBwWarps * 4 + stages * 16 + (2 * stages + 6) * 8 + 128;
+           4 * kBwMaxCluster * kBwBatch * kBwWarps * 4 + stages * 16 + (2 * stages + 4) * 8 + 128;
 }
 
 // A stage: the V~ segment of 512 channels, then the dout segment.
@@ -432,7 +432,7 @@ __global__ void __launch_bounds__(kBwThreads, 3) conv_bwd_kernel(const __grid_co
     ScMeta *meta = reinterpret_cast<ScMeta *>(box + 4 * kBwMaxCluster * kBwBatch * kBwWarps);
     uint64_t *full = reinterpret_cast<uint64_t *>(meta + S);
     uint64_t *empty = full + S;
-    uint64_t *boxbar = empty + S + 2;
+    uint64_t *boxbar = empty + S;
     ScBwdProd *prod = reinterpret_cast<ScBwdProd *>(boxbar + 4);
 
     const int tid = threadIdx.x;
