@@ -13,15 +13,16 @@
 //     carries its eight channels' last three taps' inputs in registers, so each row is converted
 //     once;
 //   * conv_bwd_kernel (the backward, one pass): a thread-block cluster of ceil(d / 512) CTAs takes
-//     one residue class t = r (mod dilation) of one time chunk, each CTA 512 channels.  Every tap of
-//     a class token lies in the same class, so the CTA sweeps its class tokens in time order, a
-//     producer warp streaming each token's V~ and dout row segments and rstd into a ring of
-//     shared-memory stages; each consumer thread carries its four channels' last three taps' inputs
-//     and the du still collecting contributions in registers.  The row dot s = sum_c norm_w du V~
-//     that dV~ needs couples all d channels of a token: each CTA sums its part for a few tokens at a
-//     time and exchanges it with the other CTAs of its cluster through distributed shared memory,
-//     then writes dV~ = dout + rstd norm_w du - rstd^3 V~ s / d and keeps the weight-gradient
-//     partials of its (time chunk, residue) work item;
+//     a contiguous range of work items (time chunk, residue class t = r (mod dilation)) in class
+//     order, each CTA 512 channels.  Every tap of a class token lies in the same class, so the CTA
+//     sweeps its class tokens in time order, across the chunks of its range, a producer warp
+//     streaming each token's V~ and dout row segments and rstd into a ring of shared-memory stages;
+//     each consumer thread carries its four channels' last three taps' inputs and the du still
+//     collecting contributions in registers.  The row dot s = sum_c norm_w du V~ that dV~ needs
+//     couples all d channels of a token: each warp sums its part for a few tokens at a time and
+//     sends it to every CTA of its cluster through distributed shared memory, then it writes
+//     dV~ = dout + rstd norm_w du - rstd^3 V~ s / d and keeps the weight-gradient partials of each
+//     (time chunk, residue) work item;
 //   * conv_grad_reduce_kernel sums the partials in a fixed order.
 // The time chunks depend on T only, the clusters on d only, and every sum has a fixed order, so all
 // results are bitwise reproducible on any GPU.
