@@ -234,21 +234,28 @@ def test_in_place_output_and_bitwise_reruns():
         ecm.set_max_ctas(0)
 
 
-def test_backward_bitwise_across_grids():
+@pytest.mark.parametrize("lengths,dil", [([3000, 1, 1500, 700], 3), ([513], 3), ([300, 213], 40)],
+                         ids=["ragged", "empty_items", "empty_items_dil40"])
+def test_backward_bitwise_across_grids(lengths, dil):
     """The backward's clusters take contiguous ranges of work items in class order, so the grid decides
     where one cluster's sweep stops and the next one's starts; outputs and partials must not depend on
-    it.  63 work items (21 time chunks x 3 classes, ragged sequences) on 1, 2, 3 and 7 clusters of 2
-    CTAs, against the uncapped grid, bit for bit; a single cluster sweeps every class in turn."""
-    wl = W.ShortConvWorkload(name="grids", lengths=[3000, 1, 1500, 700], d=1024, width=4, dilation=3,
-                             dtype="bf16", seed=83, bias=True, with_h=False)
+    it.  On 1, 2, 3 and 7 clusters of 2 CTAs against the uncapped grid, bit for bit: 63 work items of
+    ragged sequences; and last time chunks shorter than the dilation (513 tokens: chunk 2 holds token
+    512 alone, so 2 of 3 classes, or at dilation 40 with a sequence boundary at 300, 39 of 40, have
+    no token there), whose empty items then sit inside one cluster's range and still get zero rows.
+    The partials are filled with NaN before each capped run, so a row left unwritten would show."""
+    wl = W.ShortConvWorkload(name="grids", lengths=lengths, d=1024, width=4, dilation=dil, dtype="bf16",
+                             seed=83 + dil, bias=True, with_h=False)
     x = W.short_conv_host_inputs(wl)
     t = {k: _t(v) for k, v in x.items() if v is not None}
     a = _run(x, wl)
+    assert not torch.isnan(a["part"]).any()
     try:
         for ncl in (1, 2, 3, 7):
             ecm.set_max_ctas(2 * ncl)
+            part = torch.full_like(a["part"], float("nan"))
             dv, part = ecm.short_conv_bwd(t["dout"], t["v"], t["norm_w"], t["conv_w"], a["rstd"], t["seq_offsets"],
-                                          wl.dilation, bias=t.get("bias"))
+                                          wl.dilation, bias=t.get("bias"), dw_partial=part)
             torch.cuda.synchronize()
             assert torch.equal(dv, a["dv"]), f"dv on {ncl} clusters"
             assert torch.equal(part, a["part"]), f"partials on {ncl} clusters"
