@@ -702,7 +702,8 @@ def _gate_config_entry(wl, device, steps: int, warmup: int, peak: float, fwd_onl
     if with_oracle:  # the oracle on host copies of set 0's first tokens, on one core and on all
         n = min(T, ORACLE_CONFIG_SAMPLE) if T > 2 * ORACLE_CONFIG_SAMPLE else T
         t = S[0]["in"]
-        x = {nm: _bf16_bits(t[nm][:n].cpu()) for nm in (("h", "k", "v") if fwd_only else ("h", "k", "v", "dout"))}
+        host = (lambda a: _bf16_bits(a)) if t["h"].dtype == torch.bfloat16 else (lambda a: a.contiguous().numpy())
+        x = {nm: host(t[nm][:n].cpu()) for nm in (("h", "k", "v") if fwd_only else ("h", "k", "v", "dout"))}
         x["w_h"], x["w_k"] = t["w_h"].cpu().numpy(), t["w_k"].cpu().numpy()
         res["oracle"] = oracle_gate_rates(x, fwd_only, T)
     del S
