@@ -208,3 +208,37 @@ def test_wait_timeout_check_rejects_bad_limits(lib):
     lib.engram_check_wait_timeout.argtypes = [ctypes.c_uint32, ctypes.c_void_p]
     assert lib.engram_check_wait_timeout(0, None) == 2
     assert lib.engram_check_wait_timeout(2000001, None) == 2
+
+
+def test_short_conv_backward_rejects_on_the_host(lib):
+    """engram_short_conv_bwd and its partial count: a wrong P, missing pointers, dv over an input, and
+    bad width or dilation come back before any CUDA call; P is (time chunks) x dilation with chunks
+    of max(256, ceil(T / 256)) tokens."""
+    st, vp, i32, i64 = ctypes.c_int, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    n = lib.engram_short_conv_num_partials
+    n.restype, n.argtypes = st, [i64, i32, ctypes.POINTER(i32)]
+    P = i32()
+
+    def parts(T, dil):
+        assert n(T, dil, ctypes.byref(P)) == 0
+        return P.value
+
+    assert parts(16384, 3) == 64 * 3 and parts(513, 3) == 3 * 3 and parts(513, 40) == 3 * 40
+    assert parts(70004, 3) == 256 * 3 and parts(1, 1) == 1
+    assert n(-1, 3, ctypes.byref(P)) == 2 and n(16, 0, ctypes.byref(P)) == 2 and n(16, 3, None) == 1
+    b = lib.engram_short_conv_bwd
+    b.restype = st
+    b.argtypes = [vp, vp, ctypes.c_int, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32, vp, vp, i32, vp]
+    f = [vp(0x10000 + 0x1000 * i) for i in range(8)]  # dout, v, norm_w, conv_w, rstd, offsets, dv, partials
+    ok = parts(513, 3)
+
+    def call(dout=f[0], v=f[1], dt=1, nw=f[2], cw=f[3], rstd=f[4], offs=f[5], T=513, d=64, width=4, dil=3, dv=f[6],
+             part=f[7], P_=ok):
+        return b(dout, v, dt, nw, cw, None, rstd, offs, 1, T, d, width, dil, dv, part, P_, None)
+
+    assert call(P_=ok + 1) == 2                      # P not the partial count
+    assert call(dil=40) == 2                         # P of dilation 3 for dilation 40
+    assert call(width=5) == 2 and call(dil=0) == 2   # width above 4, no dilation
+    assert call(dt=7) == 3                           # no such dtype
+    assert call(rstd=None) == 1 and call(dv=None) == 1 and call(part=None) == 1 and call(nw=None) == 1
+    assert call(dv=f[1]) == 2 and call(dv=f[0]) == 2  # dv over V~ or over dout
