@@ -242,3 +242,37 @@ def test_short_conv_backward_rejects_on_the_host(lib):
     assert call(dt=7) == 3                           # no such dtype
     assert call(rstd=None) == 1 and call(dv=None) == 1 and call(part=None) == 1 and call(nw=None) == 1
     assert call(dv=f[1]) == 2 and call(dv=f[0]) == 2  # dv over V~ or over dout
+
+
+def test_multi_branch_gate_rejects_on_the_host(lib):
+    """engram_gate_hc_fwd / _bwd: missing pointers, a branch count other than 1, 2 or 4, rows not a
+    multiple of 16 bytes, a negative clamp, no partials, in place with saved statistics, and outputs
+    that overlap an input other than in place, all before any CUDA call."""
+    st, vp, i32, i64, f32 = ctypes.c_int, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+    T, hc, d = 8, 4, 64
+    xb, kvb = T * hc * d * 2, T * (hc + 1) * d * 2  # bytes of x-like and kv-like tensors (bf16)
+    base = 0x100000
+    dout, x, kv, w, stat, dx, dkv, part = (vp(base + i * 0x10000) for i in range(8))
+    fw = lib.engram_gate_hc_fwd
+    fw.restype = st
+    fw.argtypes = [vp, vp, ctypes.c_int, vp, i64, i32, i32, f32, f32, vp, vp, vp, vp, vp, vp]
+
+    def fwd(x_=x, kv_=kv, dt=1, hc_=hc, d_=d, clamp=1e-6, out=dx, gate=stat, w_=w):
+        return fw(x_, kv_, dt, w_, T, hc_, d_, 1e-6, clamp, out, gate, None, None, None, None)
+
+    assert fwd(x_=None) == 1 and fwd(w_=None) == 1
+    assert fwd(hc_=3) == 2 and fwd(dt=9) == 3 and fwd(d_=60) == 4 and fwd(clamp=-1.0) == 2
+    assert fwd(out=x) == 2  # in place with a saved statistic
+    bw = lib.engram_gate_hc_bwd
+    bw.restype = st
+    bw.argtypes = [vp, vp, vp, ctypes.c_int, vp, vp, vp, vp, vp, i64, i32, i32, f32, vp, vp, vp, i32, vp]
+
+    def bwd(dx_=dx, dkv_=dkv, part_=part, P=1, hc_=hc, clamp=1e-6):
+        return bw(dout, x, kv, 1, w, stat, stat, stat, stat, T, hc_, d, clamp, dx_, dkv_, part_, P, None)
+
+    assert bwd(part_=None) == 1 and bwd(dx_=None) == 1
+    assert bwd(P=0) == 2 and bwd(hc_=8) == 2 and bwd(clamp=-0.5) == 2
+    assert bwd(dx_=kv) == 2                                   # dx over the keys
+    assert bwd(dx_=vp(dout.value + 16)) == 2                  # dx shifted against dout
+    assert bwd(dkv_=x) == 2 and bwd(dx_=dkv) == 2             # dkv over x; dx over dkv
+    assert xb < 0x10000 and kvb < 0x10000                     # the fake tensors do not overlap one another
